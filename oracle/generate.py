@@ -16,8 +16,8 @@ Decoding 101", Floors 4-5 and the Boss Level replay):
   first rejection is discarded (the cache is simply rebuilt from seq here).
 * The target's K+1 logit rows of this step are the "previous-step logits"
   of the next.  Before the first step they are the target logits at prompt
-  positions L-2-K .. L-2 (the last K+1 positions a prefill of prompt[0..L-2]
-  scores).
+  positions L-1-K .. L-1: the last K+1 positions scored by a prefill of
+  everything before the pending token.
 * ``generate(n)`` steps until at least n tokens are emitted and truncates to n.
 
 Random draws follow the layout in ``philox`` (step s counts speculative steps
@@ -75,12 +75,12 @@ def verify(p_logits, q_logits, drafts, temperature, seed, step, row=0, tie_eps=a
 
 
 def prefill_prev_logits(target: Model, prompt, k):
-    """Target logits at prompt positions L-2-K .. L-2 ([K+1, V])."""
+    """Target logits at prompt positions L-1-K .. L-1 ([K+1, V])."""
     seq = [int(t) for t in prompt]
     L = len(seq) - 1
-    if L - 2 - k < 0:
+    if L - 1 - k < 0:
         raise ValueError("prompt too short for the previous-logit rows")
-    return target.logits(seq[:L - 1], last=k + 1)
+    return target.logits(seq[:L], last=k + 1)
 
 
 def spec_step(target: Model, draft: Model, seq, k, temperature, seed, step,

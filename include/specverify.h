@@ -1,0 +1,229 @@
+/*
+ * specverify.h -- C ABI of the GB300 speculative-decoding verification step.
+ *
+ * One draft model proposes K tokens; one forward of the target model scores
+ * the pending token plus the K drafts (K+1 positions, weights read once);
+ * a fused kernel applies the acceptance rule and commits the result.
+ *
+ * Sources for the operations declared here (restated, not copied):
+ *  [INT]  "Speculative decoding internals" (tarrragon LLM notes):
+ *         section "演算法核心：sampling 階段的接受邏輯", Steps 1-4;
+ *         section "為什麼能加速：memory bandwidth bound 的縫隙";
+ *         section "怎麼挑 drafter" (draft and target share one vocabulary).
+ *  [101]  "Speculative Decoding 101" (gu-log, English): Floor 3 (one pass
+ *         scores every position), Floor 4 (greedy rule, 1..K+1 tokens per
+ *         round), Floor 5 (acceptance rule, residual draw, bonus token).
+ *
+ * Conventions shared by every entry point:
+ *  - Return value: SPEC_OK (0) or a negative SPEC_E_* code.  After an error
+ *    spec_last_error() returns a message; a failed call leaves a context's
+ *    committed state unchanged.
+ *  - Weights are caller-owned DEVICE memory and must outlive the context.
+ *    Matrices are row-major [out_features][in_features] (the nn.Linear
+ *    convention), in the model's dtype; RMSNorm gains are fp32.
+ *  - KV caches, activations, scratch and RNG state are library-owned device
+ *    memory allocated by spec_init and released by spec_free.
+ *  - Token buffers of the context API are caller-owned HOST memory; every
+ *    context call returns only after its outputs are written.
+ *  - Only batch 1 is supported by the context API in this version.
+ *  - All work runs on one GPU, on the stream given in spec_opts (or a
+ *    stream the library creates).  There is no CPU fallback: without a
+ *    usable GPU every call fails with SPEC_E_CUDA.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define SPEC_OK             0
+#define SPEC_E_ARG         -1   /* bad pointer, size or option */
+#define SPEC_E_VOCAB       -2   /* draft and target vocabularies differ [INT 怎麼挑 drafter] */
+#define SPEC_E_SHAPE       -3   /* unsupported model shape */
+#define SPEC_E_CAPACITY    -4   /* context would exceed max_ctx */
+#define SPEC_E_CUDA        -5   /* CUDA runtime error (no GPU, launch failure ...) */
+#define SPEC_E_OOM         -6   /* device allocation failed */
+#define SPEC_E_TIMEOUT     -7   /* a bounded device-side wait gave up */
+#define SPEC_E_STATE       -8   /* call out of order (e.g. step before prefill) */
+
+/* ---- model dtypes ---- */
+#define SPEC_DTYPE_F32      0
+#define SPEC_DTYPE_BF16     1
+
+/* ---- per-step flags (spec_step out_flags) ---- */
+#define SPEC_FLAG_RESID_ZERO   0x1u  /* rejection with zero residual mass; drew from p */
+#define SPEC_FLAG_ALL_ACCEPTED 0x2u  /* all K drafts accepted; last token is the bonus */
+
+/* ---- option flags (spec_opts.flags) ---- */
+#define SPEC_OPT_NO_GRAPH      0x1   /* launch the step kernel by kernel (no CUDA graph) */
+#define SPEC_OPT_TIMING        0x2   /* record CUDA events around every weight-streaming
+                                        GEMM of the verify pass (implies NO_GRAPH) */
+
+typedef struct spec_ctx spec_ctx;
+
+/* Weights of one decoder layer (device pointers). */
+typedef struct spec_layer_weights {
+    const void* attn_norm;   /* [d_model] fp32 */
+    const void* wq;          /* [n_heads*head_dim][d_model] */
+    const void* wk;          /* [n_kv_heads*head_dim][d_model] */
+    const void* wv;          /* [n_kv_heads*head_dim][d_model] */
+    const void* wo;          /* [d_model][n_heads*head_dim] */
+    const void* ffn_norm;    /* [d_model] fp32 */
+    const void* w_gate;      /* [ffn_dim][d_model] */
+    const void* w_up;        /* [ffn_dim][d_model] */
+    const void* w_down;      /* [d_model][ffn_dim] */
+} spec_layer_weights;
+
+/* A Llama-style decoder: pre-norm RMSNorm blocks, rotate-half RoPE,
+ * grouped-query causal attention (query head h reads KV head
+ * h*n_kv_heads/n_heads), SwiGLU MLP, untied LM head. */
+typedef struct spec_model_desc {
+    int   n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+    float rope_theta, rms_eps;
+    int   dtype;                        /* SPEC_DTYPE_F32 or SPEC_DTYPE_BF16 */
+    const void* embed;                  /* [vocab][d_model] */
+    const void* final_norm;             /* [d_model] fp32 */
+    const void* lm_head;                /* [vocab][d_model] */
+    const spec_layer_weights* layers;   /* host array [n_layers]; copied by spec_init */
+} spec_model_desc;
+
+typedef struct spec_opts {
+    int      batch;             /* must be 1 */
+    int      max_ctx;           /* KV capacity in positions (prompt + generated + K + 1) */
+    float    temperature;       /* 0 = greedy; >0 scales target and draft logits */
+    uint64_t seed;              /* Philox key of every random draw */
+    float    draft_mix_lambda;  /* 0 = off; else q-logits = (1-l)*draft + l*target's
+                                   previous-step logits (same row index) */
+    void*    cuda_stream;       /* cudaStream_t to run on; NULL = library-created stream */
+    int      flags;             /* SPEC_OPT_* */
+} spec_opts;
+
+typedef struct spec_stats {
+    int64_t steps;              /* speculative steps run since prefill */
+    int64_t ar_steps;           /* plain autoregressive steps run since prefill */
+    int64_t tokens_emitted;     /* by speculative steps */
+    int64_t drafts_accepted;    /* sum of n (accepted drafts) over steps */
+    int64_t accept_hist[17];    /* steps with n = 0..K accepted drafts (K <= 16) */
+    int32_t context_len;        /* committed tokens including the pending one */
+    int32_t kernels_per_step;   /* kernel launches of one spec_step */
+    int32_t kernels_per_ar_step;
+    int32_t gemm_launches_per_verify;
+    double  verify_weight_bytes;  /* matrix bytes one target pass streams */
+    double  draft_weight_bytes;   /* matrix bytes one draft pass streams */
+    double  kv_bytes_per_token_target;
+    double  kv_bytes_per_token_draft;
+    double  timed_gemm_ms;      /* SPEC_OPT_TIMING: summed event time of verify GEMMs */
+    double  timed_gemm_bytes;   /* SPEC_OPT_TIMING: weight bytes of those GEMMs */
+    int64_t timed_gemm_launches;
+} spec_stats;
+
+/* Create a context for one target/draft pair and K drafts per step.
+ * Checks shapes (head_dim in {32, 64, 128}; n_heads a multiple of
+ * n_kv_heads; d_model, ffn_dim and n_heads*head_dim multiples of 64 for
+ * bf16 models, of 4 for fp32 models), equal vocabularies
+ * (SPEC_E_VOCAB, [INT 怎麼挑 drafter]) and 1 <= K <= 16; allocates the KV
+ * caches for max_ctx positions, activations and scratch.  *out receives the
+ * context (NULL on error; spec_last_error(NULL) then has the message). */
+SPEC_API int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K,
+              const spec_opts* opts, spec_ctx** out);
+
+/* Release everything spec_init allocated.  NULL is a no-op. */
+SPEC_API void spec_free(spec_ctx* ctx);
+
+/* Message of the last error on ctx (or of the last failed spec_init /
+ * stateless call on this thread when ctx is NULL).  Never NULL. */
+SPEC_API const char* spec_last_error(const spec_ctx* ctx);
+
+/* Prefill: tokens[0..L-1] (host, int32, 0 <= id < vocab).  Both models
+ * score positions 0..L-2 into their KV caches; tokens[L-1] becomes the
+ * pending token of the first step (it is the x of [INT 演算法核心] Step 2's
+ * T(.|x)).  Resets the step counters.  Requires 2 <= L and
+ * L + K + 1 <= max_ctx; with draft_mix_lambda != 0 also L >= K + 2. */
+SPEC_API int spec_prefill(spec_ctx* ctx, const int32_t* tokens, int L);
+
+/* One speculative step [INT 演算法核心 Steps 1-4; 101 Floors 4-5]:
+ *  1. draft loop: K draft forwards, d_i ~ softmax(q_i / T) (argmax at T=0);
+ *  2. one target forward over [pending, d_1..d_K] -> K+1 distributions;
+ *  3. left to right, accept d_i iff r_i < min(1, p_i(d_i)/q_i(d_i)); on the
+ *     first reject draw from normalize((p_i - q_i)+) and stop; if all K are
+ *     accepted draw the bonus from p_{K+1} (greedy: match / first mismatch
+ *     emits the target's argmax / bonus argmax);
+ *  4. commit: the emitted tokens extend the context, the last one becomes
+ *     the pending token; KV entries past the accepted prefix are dropped by
+ *     length truncation (no copies).
+ * out_tokens (host, capacity K+1) receives the n+1 emitted tokens,
+ * *out_count = n+1 (1 <= n+1 <= K+1, [101 Floor 4]); out_flags may be NULL.
+ * Fails with SPEC_E_STATE before prefill, SPEC_E_CAPACITY when the context
+ * plus K+1 would exceed max_ctx. */
+SPEC_API int spec_step(spec_ctx* ctx, int32_t* out_tokens, int32_t* out_count, uint32_t* out_flags);
+
+/* Speculative generation of n_new tokens: spec_step until at least n_new
+ * tokens are emitted; out (host, capacity n_new) receives the first n_new,
+ * *out_n = n_new.  Extra emitted tokens of the last step stay committed. */
+SPEC_API int spec_generate(spec_ctx* ctx, int n_new, int32_t* out, int32_t* out_n);
+
+/* Plain autoregressive decoding on the same kernels [101 Floor 1]: one
+ * target forward over the pending token, one draw from softmax(p / T)
+ * (argmax at T=0), committed like a step.  *out_token receives it. */
+SPEC_API int spec_ar_step(spec_ctx* ctx, int32_t* out_token);
+
+/* Counters and byte accounting of the context. */
+SPEC_API int spec_get_stats(const spec_ctx* ctx, spec_stats* out);
+
+/* Copy the internals of the last spec_step to host buffers (any may be
+ * NULL): target logits [K+1][vocab] fp32, draft q logits after mixing
+ * [K][vocab] fp32, draft tokens [K], committed context tokens
+ * [context_len] (capacity max_ctx).  For verification against a reference. */
+SPEC_API int spec_last_step_debug(spec_ctx* ctx, float* p_logits, float* q_logits,
+                         int32_t* drafts, int32_t* context, int32_t* context_len);
+
+/* Run one model's forward over n tokens (host ids) at positions pos0 ..
+ * pos0+n-1 of its own KV cache (pos0 <= its current valid length; the valid
+ * length becomes pos0+n) and write fp32 logits of all n positions to
+ * logits_dev ([n][vocab], device).  which: 0 = target, 1 = draft.  This is
+ * the forward the step uses [101 Floor 3]; it does not touch the step state
+ * (call spec_prefill again before stepping). */
+SPEC_API int spec_model_forward(spec_ctx* ctx, int which, const int32_t* tokens, int n, int pos0,
+                       float* logits_dev);
+
+/* Stateless fused acceptance over `rows` independent verify rows
+ * [INT 演算法核心 Step 3-4]: row r has target logits p[r] ([K+1][V] fp32,
+ * device, row stride p_row_stride floats between verify rows), draft logits
+ * q[r] ([K][V], stride q_row_stride) and drafts d[r] ([K] int32, device).
+ * Random draws use Philox key `seed` and step counter step_base + r.
+ * Writes tokens[r][0..K] (int32, device, K+1 per row), counts[r] and
+ * flags[r] (may be NULL).  temperature 0 = greedy rule.  Scratch comes from
+ * the stream-ordered allocator of the current device.  Asynchronous on
+ * `stream` (cudaStream_t; NULL = default stream). */
+SPEC_API int spec_accept_rows(const float* p_logits, int64_t p_row_stride,
+                     const float* q_logits, int64_t q_row_stride,
+                     const int32_t* drafts, int rows, int K, int V, float temperature,
+                     uint64_t seed, uint64_t step_base, int32_t* tokens, int32_t* counts,
+                     uint32_t* flags, void* stream);
+
+/* Stateless draft sampler: one token per row from softmax(logits[r] / T)
+ * by inverse CDF (argmax at T=0), with the Philox draw (seed; step_base+r,
+ * position, stream 0, row 0).  logits: [rows] rows of V fp32 (device,
+ * stride row_stride floats).  tokens: [rows] int32 device.  Asynchronous. */
+SPEC_API int spec_sample_rows(const float* logits, int64_t row_stride, int rows, int V,
+                     float temperature, uint64_t seed, uint64_t step_base, int position,
+                     int32_t* tokens, void* stream);
+
+/* Library version string. */
+SPEC_API const char* spec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

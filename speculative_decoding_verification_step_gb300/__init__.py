@@ -1,0 +1,255 @@
+"""GB300 speculative-decoding verification step -- Python binding.
+
+A thin ctypes layer over the C ABI in ``include/specverify.h``: it marshals
+arguments and raises on error codes.  Every step of the path runs in the
+CUDA library (``_lib/libspecverify.so``, built by ``build()``); there is no
+CPU fallback, and using the binding without the built library raises.
+Device memory (weights, logits) is passed as torch CUDA tensors, read by
+pointer.
+"""
+import ctypes
+import os
+
+from ._build import LIB, build
+
+__all__ = ["build", "lib", "SpecError", "SpecDecoder", "accept_rows", "sample_rows",
+           "SPEC_DTYPE_F32", "SPEC_DTYPE_BF16", "SPEC_OPT_NO_GRAPH", "SPEC_OPT_TIMING",
+           "SPEC_FLAG_RESID_ZERO", "SPEC_FLAG_ALL_ACCEPTED"]
+
+SPEC_OK = 0
+ERRORS = {-1: "SPEC_E_ARG", -2: "SPEC_E_VOCAB", -3: "SPEC_E_SHAPE", -4: "SPEC_E_CAPACITY",
+          -5: "SPEC_E_CUDA", -6: "SPEC_E_OOM", -7: "SPEC_E_TIMEOUT", -8: "SPEC_E_STATE"}
+SPEC_DTYPE_F32 = 0
+SPEC_DTYPE_BF16 = 1
+SPEC_FLAG_RESID_ZERO = 0x1
+SPEC_FLAG_ALL_ACCEPTED = 0x2
+SPEC_OPT_NO_GRAPH = 0x1
+SPEC_OPT_TIMING = 0x2
+
+_LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _LAYER_FIELDS]
+
+
+class ModelDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("d_model", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("dtype", ctypes.c_int), ("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("lm_head", ctypes.c_void_p), ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("max_ctx", ctypes.c_int), ("temperature", ctypes.c_float),
+                ("seed", ctypes.c_uint64), ("draft_mix_lambda", ctypes.c_float),
+                ("cuda_stream", ctypes.c_void_p), ("flags", ctypes.c_int)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("ar_steps", ctypes.c_int64),
+                ("tokens_emitted", ctypes.c_int64), ("drafts_accepted", ctypes.c_int64),
+                ("accept_hist", ctypes.c_int64 * 17), ("context_len", ctypes.c_int32),
+                ("kernels_per_step", ctypes.c_int32), ("kernels_per_ar_step", ctypes.c_int32),
+                ("gemm_launches_per_verify", ctypes.c_int32),
+                ("verify_weight_bytes", ctypes.c_double), ("draft_weight_bytes", ctypes.c_double),
+                ("kv_bytes_per_token_target", ctypes.c_double),
+                ("kv_bytes_per_token_draft", ctypes.c_double),
+                ("timed_gemm_ms", ctypes.c_double), ("timed_gemm_bytes", ctypes.c_double),
+                ("timed_gemm_launches", ctypes.c_int64)]
+
+    def as_dict(self):
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["accept_hist"] = list(self.accept_hist)
+        return d
+
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_U32P = ctypes.POINTER(ctypes.c_uint32)
+_F32P = ctypes.POINTER(ctypes.c_float)
+_VP = ctypes.c_void_p
+
+# name -> (restype, argtypes); every function declared in include/specverify.h
+SIGNATURES = {
+    "spec_init": (ctypes.c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(ModelDesc), ctypes.c_int,
+                                 ctypes.POINTER(Opts), ctypes.POINTER(_VP)]),
+    "spec_free": (None, [_VP]),
+    "spec_last_error": (ctypes.c_char_p, [_VP]),
+    "spec_prefill": (ctypes.c_int, [_VP, _I32P, ctypes.c_int]),
+    "spec_step": (ctypes.c_int, [_VP, _I32P, _I32P, _U32P]),
+    "spec_generate": (ctypes.c_int, [_VP, ctypes.c_int, _I32P, _I32P]),
+    "spec_ar_step": (ctypes.c_int, [_VP, _I32P]),
+    "spec_get_stats": (ctypes.c_int, [_VP, ctypes.POINTER(Stats)]),
+    "spec_last_step_debug": (ctypes.c_int, [_VP, _F32P, _F32P, _I32P, _I32P, _I32P]),
+    "spec_model_forward": (ctypes.c_int, [_VP, ctypes.c_int, _I32P, ctypes.c_int, ctypes.c_int, _VP]),
+    "spec_accept_rows": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, ctypes.c_int64, _VP, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_uint64,
+                                        ctypes.c_uint64, _VP, _VP, _VP, _VP]),
+    "spec_sample_rows": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64,
+                                        ctypes.c_int, _VP, _VP]),
+    "spec_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: run build() first; this package has no CPU fallback")
+        handle = ctypes.CDLL(LIB)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _check(rc, ctx=None):
+    if rc != SPEC_OK:
+        msg = lib().spec_last_error(ctx).decode(errors="replace")
+        raise SpecError(rc, msg)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def model_desc(shape, weights):
+    """ModelDesc for a shape (attributes n_layers, d_model, n_heads, n_kv_heads,
+    head_dim, ffn_dim, vocab, rope_theta, rms_eps, dtype 'f32'|'bf16') and a
+    weights dict {'embed', 'final_norm', 'lm_head', 'layers': [dict]} of CUDA
+    tensors.  Returns (desc, keepalive)."""
+    layers = (LayerWeights * shape.n_layers)()
+    for i, lw in enumerate(weights["layers"]):
+        for n in _LAYER_FIELDS:
+            setattr(layers[i], n, lw[n].data_ptr())
+    d = ModelDesc(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                  shape.ffn_dim, shape.vocab, shape.rope_theta, shape.rms_eps,
+                  SPEC_DTYPE_F32 if shape.dtype == "f32" else SPEC_DTYPE_BF16,
+                  weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
+                  weights["lm_head"].data_ptr(), layers)
+    return d, (layers, weights)
+
+
+class SpecDecoder:
+    """One target/draft pair with K drafts per step (batch 1)."""
+
+    def __init__(self, target_shape, target_w, draft_shape, draft_w, k, max_ctx,
+                 temperature=0.0, seed=0, mix_lambda=0.0, stream=None, flags=0):
+        self.k = k
+        self.vocab = target_shape.vocab
+        self._td, self._tk = model_desc(target_shape, target_w)
+        self._dd, self._dk = model_desc(draft_shape, draft_w)
+        opts = Opts(1, max_ctx, temperature, seed, mix_lambda,
+                    ctypes.c_void_p(stream) if stream else ctypes.c_void_p(0), flags)
+        h = ctypes.c_void_p()
+        rc = lib().spec_init(ctypes.byref(self._td), ctypes.byref(self._dd), k, ctypes.byref(opts),
+                             ctypes.byref(h))
+        _check(rc)
+        self.ctx = h
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            lib().spec_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, tokens):
+        arr = (ctypes.c_int32 * len(tokens))(*[int(t) for t in tokens])
+        _check(lib().spec_prefill(self.ctx, arr, len(tokens)), self.ctx)
+
+    def step(self):
+        out = (ctypes.c_int32 * (self.k + 1))()
+        cnt = ctypes.c_int32()
+        flags = ctypes.c_uint32()
+        _check(lib().spec_step(self.ctx, out, ctypes.byref(cnt), ctypes.byref(flags)), self.ctx)
+        return list(out[:cnt.value]), flags.value
+
+    def generate(self, n_new):
+        out = (ctypes.c_int32 * max(1, n_new))()
+        got = ctypes.c_int32()
+        _check(lib().spec_generate(self.ctx, n_new, out, ctypes.byref(got)), self.ctx)
+        return list(out[:got.value])
+
+    def ar_step(self):
+        tok = ctypes.c_int32()
+        _check(lib().spec_ar_step(self.ctx, ctypes.byref(tok)), self.ctx)
+        return tok.value
+
+    def stats(self):
+        s = Stats()
+        _check(lib().spec_get_stats(self.ctx, ctypes.byref(s)), self.ctx)
+        return s.as_dict()
+
+    def last_step_debug(self, max_ctx):
+        """(p_logits [K+1, V], q_logits [K, V], drafts [K], context tokens) as numpy."""
+        import numpy as np
+        k, v = self.k, self.vocab
+        p = np.zeros((k + 1, v), dtype=np.float32)
+        q = np.zeros((k, v), dtype=np.float32)
+        d = np.zeros(k, dtype=np.int32)
+        ctx = np.zeros(max_ctx, dtype=np.int32)
+        n = ctypes.c_int32()
+        _check(lib().spec_last_step_debug(self.ctx, p.ctypes.data_as(_F32P), q.ctypes.data_as(_F32P),
+                                          d.ctypes.data_as(_I32P), ctx.ctypes.data_as(_I32P),
+                                          ctypes.byref(n)), self.ctx)
+        return p, q, d, ctx[:n.value].copy()
+
+    def model_forward(self, which, tokens, pos0, logits):
+        """Forward of the target (0) or draft (1) over host token ids at
+        positions pos0.. into logits (CUDA fp32 tensor [n, V])."""
+        arr = (ctypes.c_int32 * len(tokens))(*[int(t) for t in tokens])
+        _check(lib().spec_model_forward(self.ctx, which, arr, len(tokens), pos0, _ptr(logits)), self.ctx)
+
+
+def accept_rows(p_logits, q_logits, drafts, temperature, seed, step_base=0, stream=None,
+                p_row_stride=None, q_row_stride=None, rows=None):
+    """Fused acceptance over independent verify rows (CUDA tensors):
+    p_logits [R, K+1, V] fp32, q_logits [R, K, V] fp32, drafts [R, K] int32.
+    Returns (tokens [R, K+1] int32, counts [R] int32, flags [R] int32)."""
+    import torch
+    K = q_logits.shape[-2]
+    V = p_logits.shape[-1]
+    R = rows if rows is not None else p_logits.shape[0]
+    dev = p_logits.device
+    tokens = torch.empty((R, K + 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(R, dtype=torch.int32, device=dev)
+    flags = torch.empty(R, dtype=torch.int32, device=dev)
+    ps = p_row_stride if p_row_stride is not None else (K + 1) * V
+    qs = q_row_stride if q_row_stride is not None else K * V
+    st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _check(lib().spec_accept_rows(_ptr(p_logits), ps, _ptr(q_logits), qs, _ptr(drafts), R, K, V,
+                                  float(temperature), int(seed), int(step_base), _ptr(tokens),
+                                  _ptr(counts), _ptr(flags), ctypes.c_void_p(st)))
+    return tokens, counts, flags
+
+
+def sample_rows(logits, temperature, seed, step_base=0, position=1, stream=None, row_stride=None,
+                rows=None):
+    """Inverse-CDF draw per row of logits [R, V] (CUDA fp32); returns int32 [R]."""
+    import torch
+    V = logits.shape[-1]
+    R = rows if rows is not None else logits.shape[0]
+    out = torch.empty(R, dtype=torch.int32, device=logits.device)
+    st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    rs = row_stride if row_stride is not None else V
+    _check(lib().spec_sample_rows(_ptr(logits), rs, R, V, float(temperature), int(seed),
+                                  int(step_base), int(position), _ptr(out), ctypes.c_void_p(st)))
+    return out

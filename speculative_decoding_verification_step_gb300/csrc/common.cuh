@@ -1,0 +1,92 @@
+// Shared device helpers of the GB300 speculative-verification library.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#define SV_DEV __device__ __forceinline__
+
+namespace sv {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kWarp = 32;
+SV_DEV float neg_inf() { return __int_as_float(0xff800000u); }
+
+// ---------------------------------------------------------------------------
+// Philox-4x32-10, restated from its published definition (Salmon, Moraes,
+// Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11): ten
+// rounds; each multiplies counter words 0 and 2 by two odd constants, XORs
+// the high halves with words 1 and 3 and the round key, keeps the low halves,
+// and bumps the key by two Weyl increments.
+//
+// Draw layout of the speculative step: key = (seed lo, seed hi), counter =
+// (step, position, stream, row), uniform = (word0 >> 8) * 2^-24 in [0, 1).
+// ---------------------------------------------------------------------------
+enum Stream : uint32_t { kStreamDraft = 0, kStreamAccept = 1, kStreamResidual = 2,
+                         kStreamBonus = 3, kStreamAR = 4 };
+
+SV_DEV uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
+  }
+  return c;
+}
+
+SV_DEV float philox_uniform(uint64_t seed, uint32_t step, uint32_t position, uint32_t stream,
+                            uint32_t row) {
+  const uint4 o = philox4x32_10(make_uint4(step, position, stream, row),
+                                make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+  return (float)(o.x >> 8) * (1.0f / 16777216.0f);
+}
+
+// ---------------------------------------------------------------------------
+// Element helpers
+// ---------------------------------------------------------------------------
+SV_DEV float to_f32(float x) { return x; }
+SV_DEV float to_f32(bf16 x) { return __bfloat162float(x); }
+template <typename T> SV_DEV T from_f32(float x);
+template <> SV_DEV float from_f32<float>(float x) { return x; }
+template <> SV_DEV bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// Two bf16 packed in one 32-bit word (low half first) -> floats.
+SV_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+SV_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Streaming 128-bit load of weights: read once per launch, do not keep in L1.
+SV_DEV uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// Warp-level tensor-core MMA m16n8k16, bf16 inputs, fp32 accumulate.
+SV_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                           uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+SV_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+SV_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+SV_DEV float silu(float x) { return x / (1.0f + expf(-x)); }
+
+}  // namespace sv

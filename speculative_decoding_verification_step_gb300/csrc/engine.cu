@@ -1,0 +1,736 @@
+// Context, forward orchestration and the C ABI (include/specverify.h).
+//
+// One speculative step ("Speculative decoding internals", 演算法核心 Steps
+// 1-4; "Speculative Decoding 101", Floors 3-5 and the Boss Level replay):
+//
+//   state on the device: seq[0..L] committed tokens (seq[L] = pending token,
+//   not yet scored), L, the step counters.
+//   draft pass 1 : tokens seq[L-1], seq[L] at positions L-1, L (the first
+//                  row rewrites an identical KV entry unless the previous step
+//                  accepted all K drafts, in which case the draft has not yet
+//                  seen d_K); its last row gives q_1, d_1 -> seq[L+1]
+//   draft pass i : token seq[L+i-1] at position L+i-1 -> q_i, d_i -> seq[L+i]
+//   verify       : target over seq[L..L+K] at positions L..L+K -> p_1..p_{K+1}
+//   accept       : fused kernel; writes the emitted tokens over seq[L+1..],
+//                  L += n+1, step += 1 (KV rollback = the new L; no copies)
+//   readback     : one small device-to-host copy of (tokens, count, flags).
+// Every position and index is read from device memory, so the whole step is
+// captured once as a CUDA graph and replayed.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "specverify.h"
+
+using namespace sv;
+
+namespace {
+
+thread_local std::string g_err = "no error";
+
+struct ModelState {
+  spec_model_desc d{};
+  std::vector<spec_layer_weights> layers;
+  void* kc = nullptr;   // [n_layers][hkv][cap][hd]
+  void* vc = nullptr;
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+  int esize = 4;
+  int qkv_rows() const { return (d.n_heads + 2 * d.n_kv_heads) * d.head_dim; }
+  size_t layer_kv_elems(int cap) const { return (size_t)d.n_kv_heads * cap * d.head_dim; }
+  double matrix_bytes_layer() const {
+    const double hd = d.head_dim, dm = d.d_model;
+    return ((2.0 * d.n_heads + 2.0 * d.n_kv_heads) * hd * dm + 3.0 * dm * d.ffn_dim) * esize;
+  }
+  double head_bytes() const { return (double)d.vocab * d.d_model * esize; }
+  double weight_bytes() const { return d.n_layers * matrix_bytes_layer() + head_bytes(); }
+  double kv_bytes_per_token() const { return 2.0 * d.n_layers * d.n_kv_heads * d.head_dim * esize; }
+};
+
+}  // namespace
+
+struct spec_ctx {
+  ModelState tgt, drf;
+  int K = 0;
+  spec_opts opts{};
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  int num_sms = 0;
+  int cap = 0;
+  int max_chunks = 0;
+  // device state
+  int32_t* st = nullptr;    // [0] L, [1] spec step, [2] ar step, [3] eager position scratch
+  int32_t* seq = nullptr;   // [cap + K + 2]
+  int32_t* fwd_tok = nullptr;  // [kGemmMaxTok] host-supplied tokens of spec_model_forward
+  // activations
+  float* x = nullptr;
+  void* xn = nullptr;
+  void* hbuf = nullptr;
+  float* qkv = nullptr;
+  float* q = nullptr;
+  void* attn = nullptr;
+  float* attn_part = nullptr;
+  float* logits_p = nullptr;  // [K+1][V]
+  float* logits_q = nullptr;  // [K][V]
+  GemmScratch gs{};
+  float* samp_part = nullptr;
+  int* samp_tick = nullptr;
+  float* acc_part = nullptr;
+  int* acc_tick = nullptr;
+  int32_t* result = nullptr;    // device [K+1 tokens][count][flags][drafts K]
+  int32_t* h_result = nullptr;  // pinned host mirror
+  int32_t* h_pos = nullptr;     // pinned host scratch for eager positions
+  std::vector<void*> allocs;
+  // graphs
+  cudaGraphExec_t step_exec = nullptr;
+  cudaGraphExec_t ar_exec = nullptr;
+  // host mirror of the state
+  bool prefilled = false;
+  bool draft_stale = false;
+  int host_L = 0;
+  int kernels_step = 0, kernels_ar = 0, gemms_verify = 0;
+  int64_t steps = 0, ar_steps = 0, emitted = 0, accepted = 0;
+  int64_t hist[17] = {0};
+  // timing (SPEC_OPT_TIMING)
+  std::vector<cudaEvent_t> ev;
+  std::vector<double> ev_bytes;
+  int ev_used = 0;
+  bool timing_verify = false;
+  double timed_ms = 0.0, timed_bytes = 0.0;
+  int64_t timed_launches = 0;
+  int launch_count = 0;
+  std::string err = "no error";
+};
+
+namespace {
+
+int fail(spec_ctx* c, int code, const std::string& msg) {
+  if (c) c->err = msg;
+  g_err = msg;
+  return code;
+}
+
+#define CUDA_TRY(c, expr)                                                                   \
+  do {                                                                                      \
+    cudaError_t e__ = (expr);                                                               \
+    if (e__ != cudaSuccess)                                                                 \
+      return fail((c), SPEC_E_CUDA, std::string(#expr) + ": " + cudaGetErrorString(e__));   \
+  } while (0)
+
+template <typename T>
+cudaError_t dalloc(spec_ctx* c, T** p, size_t bytes) {
+  void* v = nullptr;
+  cudaError_t e = cudaMalloc(&v, bytes < 16 ? 16 : bytes);
+  if (e != cudaSuccess) return e;
+  c->allocs.push_back(v);
+  *p = (T*)v;
+  return cudaSuccess;
+}
+
+bool valid_hd(int hd) { return hd == 32 || hd == 64 || hd == 128; }
+
+int check_model(const spec_model_desc* m, const char* which, std::string* why) {
+  char buf[256];
+  if (!m) { *why = std::string(which) + ": null model"; return SPEC_E_ARG; }
+  if (m->n_layers < 1 || m->d_model < 1 || m->n_heads < 1 || m->n_kv_heads < 1 ||
+      m->ffn_dim < 1 || m->vocab < 2 || !(m->rms_eps > 0.f) || !(m->rope_theta > 0.f)) {
+    *why = std::string(which) + ": non-positive dimension or parameter";
+    return SPEC_E_SHAPE;
+  }
+  if (m->dtype != SPEC_DTYPE_F32 && m->dtype != SPEC_DTYPE_BF16) {
+    *why = std::string(which) + ": unknown dtype";
+    return SPEC_E_SHAPE;
+  }
+  if (!valid_hd(m->head_dim) || m->n_heads % m->n_kv_heads != 0) {
+    snprintf(buf, sizeof buf, "%s: head_dim %d must be 32/64/128 and n_heads %% n_kv_heads == 0",
+             which, m->head_dim);
+    *why = buf;
+    return SPEC_E_SHAPE;
+  }
+  const int kmul = m->dtype == SPEC_DTYPE_BF16 ? 64 : 4;
+  if (m->d_model % kmul || m->ffn_dim % kmul || (m->n_heads * m->head_dim) % kmul ||
+      m->ffn_dim % 8) {
+    snprintf(buf, sizeof buf, "%s: d_model, ffn_dim and n_heads*head_dim must be multiples of %d",
+             which, kmul);
+    *why = buf;
+    return SPEC_E_SHAPE;
+  }
+  if (!m->embed || !m->final_norm || !m->lm_head || !m->layers) {
+    *why = std::string(which) + ": null weight pointer";
+    return SPEC_E_ARG;
+  }
+  for (int l = 0; l < m->n_layers; ++l) {
+    const spec_layer_weights& w = m->layers[l];
+    if (!w.attn_norm || !w.wq || !w.wk || !w.wv || !w.wo || !w.ffn_norm || !w.w_gate ||
+        !w.w_up || !w.w_down) {
+      snprintf(buf, sizeof buf, "%s: null weight pointer in layer %d", which, l);
+      *why = buf;
+      return SPEC_E_ARG;
+    }
+  }
+  return SPEC_OK;
+}
+
+// ---------------------------------------------------------------- launches
+struct Launch {
+  spec_ctx* c;
+  cudaError_t e = cudaSuccess;
+  void note(cudaError_t r) {
+    if (e == cudaSuccess && r != cudaSuccess) e = r;
+    c->launch_count++;
+  }
+};
+
+void gemm(Launch& L, const GemmDesc& g, int dtype) {
+  spec_ctx* c = L.c;
+  const bool timed = c->timing_verify && c->ev_used + 2 <= (int)c->ev.size();
+  if (timed) cudaEventRecord(c->ev[c->ev_used], c->stream);
+  L.note(launch_gemm(g, dtype, c->gs, c->num_sms, c->stream, false));
+  if (timed) {
+    cudaEventRecord(c->ev[c->ev_used + 1], c->stream);
+    const double es = dtype == SPEC_DTYPE_BF16 ? 2.0 : 4.0;
+    const double rows = g.epi == kEpiSwiglu ? 2.0 * g.n : (double)g.n;
+    c->ev_bytes[c->ev_used / 2] = rows * g.k * es;
+    c->ev_used += 2;
+  }
+}
+
+// Forward of one model over ntok tokens.  tokens = tok_base + *tok_idx +
+// tok_off; positions = *pos_idx + pos_off + t.  LM-head logits of rows
+// [lrow0, lrow0 + lrows) go to logits ([lrows][V]).
+void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const int32_t* tok_idx,
+             int tok_off, const int32_t* pos_idx, int pos_off, int lrow0, int lrows,
+             float* logits) {
+  spec_ctx* c = L.c;
+  const spec_model_desc& d = m.d;
+  const int dm = d.d_model, hq = d.n_heads, hkv = d.n_kv_heads, hd = d.head_dim;
+  const int qkvr = m.qkv_rows();
+  const int dt = d.dtype;
+  cudaStream_t s = c->stream;
+  L.note(launch_embed(tok_base, tok_idx, tok_off, d.embed, dt, c->x, ntok, dm, s));
+  for (int l = 0; l < d.n_layers; ++l) {
+    const spec_layer_weights& w = m.layers[l];
+    L.note(launch_rmsnorm(c->x, (const float*)w.attn_norm, d.rms_eps, c->xn, dt, ntok, dm, s));
+    GemmDesc g{};
+    g.w[0] = w.wq; g.w[1] = w.wk; g.w[2] = w.wv;
+    g.seg_rows[0] = hq * hd; g.seg_rows[1] = hkv * hd; g.seg_rows[2] = hkv * hd;
+    g.n = qkvr; g.k = dm; g.x = c->xn; g.ldx = dm; g.ntok = ntok;
+    g.epi = kEpiStore; g.out = c->qkv; g.ldo = qkvr;
+    gemm(L, g, dt);
+    const size_t kvoff = (size_t)l * m.layer_kv_elems(c->cap) * m.esize;
+    RopeDesc r{};
+    r.qkv = c->qkv; r.pos_base = pos_idx; r.pos_off = pos_off;
+    r.rope_cos = m.rope_cos; r.rope_sin = m.rope_sin; r.q_out = c->q;
+    r.kc = (char*)m.kc + kvoff; r.vc = (char*)m.vc + kvoff;
+    r.ntok = ntok; r.hq = hq; r.hkv = hkv; r.hd = hd; r.cap = c->cap; r.dtype = dt;
+    L.note(launch_rope_append(r, s));
+    AttnDesc a{};
+    a.q = c->q; a.kc = r.kc; a.vc = r.vc; a.pos_base = pos_idx; a.pos_off = pos_off;
+    a.partials = c->attn_part; a.out = c->attn;
+    a.ntok = ntok; a.hq = hq; a.hkv = hkv; a.hd = hd; a.cap = c->cap;
+    a.max_chunks = c->max_chunks; a.dtype = dt;
+    a.scale = 1.0f / sqrtf((float)hd);
+    L.note(launch_attention(a, s));
+    c->launch_count++;  // combine kernel
+    GemmDesc o{};
+    o.w[0] = w.wo; o.seg_rows[0] = dm; o.n = dm; o.k = hq * hd; o.x = c->attn; o.ldx = hq * hd;
+    o.ntok = ntok; o.epi = kEpiAdd; o.out = c->x; o.ldo = dm;
+    gemm(L, o, dt);
+    L.note(launch_rmsnorm(c->x, (const float*)w.ffn_norm, d.rms_eps, c->xn, dt, ntok, dm, s));
+    GemmDesc gu{};
+    gu.w[0] = w.w_gate; gu.w[1] = w.w_up; gu.n = d.ffn_dim; gu.k = dm; gu.x = c->xn; gu.ldx = dm;
+    gu.ntok = ntok; gu.epi = kEpiSwiglu; gu.out = c->hbuf; gu.ldo = d.ffn_dim;
+    gemm(L, gu, dt);
+    GemmDesc dn{};
+    dn.w[0] = w.w_down; dn.seg_rows[0] = dm; dn.n = dm; dn.k = d.ffn_dim; dn.x = c->hbuf;
+    dn.ldx = d.ffn_dim; dn.ntok = ntok; dn.epi = kEpiAdd; dn.out = c->x; dn.ldo = dm;
+    gemm(L, dn, dt);
+  }
+  if (lrows > 0) {
+    L.note(launch_rmsnorm(c->x + (size_t)lrow0 * dm, (const float*)d.final_norm, d.rms_eps, c->xn,
+                          dt, lrows, dm, s));
+    GemmDesc h{};
+    h.w[0] = d.lm_head; h.seg_rows[0] = d.vocab; h.n = d.vocab; h.k = dm; h.x = c->xn; h.ldx = dm;
+    h.ntok = lrows; h.epi = kEpiStore; h.out = logits; h.ldo = d.vocab;
+    gemm(L, h, dt);
+  }
+}
+
+void enqueue_step(Launch& L) {
+  spec_ctx* c = L.c;
+  const int K = c->K, V = c->tgt.d.vocab;
+  const int32_t* Lp = c->st;  // committed length index (position of the pending token)
+  const bool mix = c->opts.draft_mix_lambda != 0.f;
+  for (int i = 1; i <= K; ++i) {
+    float* qrow = c->logits_q + (size_t)(i - 1) * V;
+    if (i == 1)
+      forward(L, c->drf, 2, c->seq, Lp, -1, Lp, -1, 1, 1, qrow);
+    else
+      forward(L, c->drf, 1, c->seq, Lp, i - 1, Lp, i - 1, 0, 1, qrow);
+    SampleDesc sd{};
+    sd.logits = qrow; sd.ld = V;
+    if (mix) {
+      sd.mix_src = c->logits_p + (size_t)(i - 1) * V; sd.mix_ld = V;
+      sd.lambda = c->opts.draft_mix_lambda; sd.mixed_out = qrow; sd.mixed_ld = V;
+    }
+    sd.rows = 1; sd.V = V; sd.temperature = c->opts.temperature; sd.seed = c->opts.seed;
+    sd.step_dev = c->st + 1; sd.step_base = 0; sd.position = (uint32_t)i; sd.stream = kStreamDraft;
+    sd.out_token = c->seq; sd.out_idx = Lp; sd.out_off = i;
+    sd.partials = c->samp_part; sd.tickets = c->samp_tick;
+    L.note(launch_sample(sd, c->stream));
+  }
+  const bool was = c->timing_verify;
+  c->timing_verify = (c->opts.flags & SPEC_OPT_TIMING) != 0;
+  forward(L, c->tgt, K + 1, c->seq, Lp, 0, Lp, 0, 0, K + 1, c->logits_p);
+  c->timing_verify = was;
+  AcceptDesc ad{};
+  ad.p = c->logits_p; ad.p_ld = 0; ad.q = c->logits_q; ad.q_ld = 0;
+  ad.drafts = c->seq; ad.drafts_idx = Lp; ad.drafts_off = 1;
+  ad.drafts_copy = c->result + (K + 3);
+  ad.rows = 1; ad.K = K; ad.V = V; ad.temperature = c->opts.temperature; ad.seed = c->opts.seed;
+  ad.step_dev = c->st + 1; ad.step_base = 0;
+  ad.out_tokens = c->result; ad.out_count = c->result + (K + 1);
+  ad.out_flags = (uint32_t*)(c->result + (K + 2));
+  ad.commit_seq = c->seq; ad.commit_len = c->st; ad.commit_step = c->st + 1;
+  ad.partials = c->acc_part; ad.tickets = c->acc_tick;
+  L.note(launch_accept(ad, c->stream));
+  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 3),
+                         cudaMemcpyDeviceToHost, c->stream));
+  c->launch_count--;  // the copy is not a kernel
+}
+
+void enqueue_ar(Launch& L) {
+  spec_ctx* c = L.c;
+  const int V = c->tgt.d.vocab;
+  const int32_t* Lp = c->st;
+  forward(L, c->tgt, 1, c->seq, Lp, 0, Lp, 0, 0, 1, c->logits_p);
+  SampleDesc sd{};
+  sd.logits = c->logits_p; sd.ld = V; sd.rows = 1; sd.V = V;
+  sd.temperature = c->opts.temperature; sd.seed = c->opts.seed;
+  sd.step_dev = c->st + 2; sd.position = 0; sd.stream = kStreamAR;
+  sd.out_token = c->result; sd.out_idx = nullptr; sd.out_off = 0;
+  sd.commit_seq = c->seq; sd.commit_len = c->st; sd.commit_step = c->st + 2;
+  sd.partials = c->samp_part; sd.tickets = c->samp_tick;
+  L.note(launch_sample(sd, c->stream));
+  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                         c->stream));
+  c->launch_count--;
+}
+
+bool use_graph(const spec_ctx* c) {
+  return !(c->opts.flags & (SPEC_OPT_NO_GRAPH | SPEC_OPT_TIMING));
+}
+
+int run_captured(spec_ctx* c, cudaGraphExec_t* exec, void (*enq)(Launch&), int* nkern) {
+  if (!use_graph(c)) {
+    Launch L{c};
+    c->launch_count = 0;
+    enq(L);
+    *nkern = c->launch_count;
+    CUDA_TRY(c, L.e);
+    return SPEC_OK;
+  }
+  if (!*exec) {
+    CUDA_TRY(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeRelaxed));
+    Launch L{c};
+    c->launch_count = 0;
+    enq(L);
+    cudaGraph_t g = nullptr;
+    cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+    CUDA_TRY(c, L.e);
+    CUDA_TRY(c, e2);
+    *nkern = c->launch_count;
+    cudaError_t e3 = cudaGraphInstantiate(exec, g, 0);
+    cudaGraphDestroy(g);
+    CUDA_TRY(c, e3);
+  }
+  CUDA_TRY(c, cudaGraphLaunch(*exec, c->stream));
+  return SPEC_OK;
+}
+
+void free_ctx(spec_ctx* c) {
+  if (!c) return;
+  if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
+  if (c->ar_exec) cudaGraphExecDestroy(c->ar_exec);
+  for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
+  for (void* p : c->allocs) cudaFree(p);
+  if (c->h_result) cudaFreeHost(c->h_result);
+  if (c->h_pos) cudaFreeHost(c->h_pos);
+  if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+  delete c;
+}
+
+int set_eager_pos(spec_ctx* c, int pos) {
+  *c->h_pos = pos;
+  CUDA_TRY(c, cudaMemcpyAsync(c->st + 3, c->h_pos, sizeof(int32_t), cudaMemcpyHostToDevice,
+                              c->stream));
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_version(void) { return "specverify-gb300 0.1 (sm_103a)"; }
+
+const char* spec_last_error(const spec_ctx* ctx) {
+  return ctx ? ctx->err.c_str() : g_err.c_str();
+}
+
+void spec_free(spec_ctx* ctx) { free_ctx(ctx); }
+
+int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K,
+              const spec_opts* opts, spec_ctx** out) {
+  if (!out) return fail(nullptr, SPEC_E_ARG, "spec_init: null output pointer");
+  *out = nullptr;
+  std::string why;
+  int rc;
+  if ((rc = check_model(target, "target", &why)) != SPEC_OK) return fail(nullptr, rc, why);
+  if ((rc = check_model(draft, "draft", &why)) != SPEC_OK) return fail(nullptr, rc, why);
+  if (!opts) return fail(nullptr, SPEC_E_ARG, "spec_init: null opts");
+  if (target->vocab != draft->vocab)
+    return fail(nullptr, SPEC_E_VOCAB, "draft and target vocabularies differ (" +
+                                           std::to_string(draft->vocab) + " vs " +
+                                           std::to_string(target->vocab) + ")");
+  if (K < 1 || K > 16) return fail(nullptr, SPEC_E_ARG, "K must be in 1..16");
+  if (opts->batch != 1) return fail(nullptr, SPEC_E_ARG, "only batch 1 is supported");
+  if (opts->max_ctx < K + 3) return fail(nullptr, SPEC_E_ARG, "max_ctx must be at least K + 3");
+  if (!(opts->temperature >= 0.f)) return fail(nullptr, SPEC_E_ARG, "temperature must be >= 0");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(nullptr, SPEC_E_CUDA, std::string("no CUDA device: ") + cudaGetErrorString(e));
+
+  spec_ctx* c = new spec_ctx();
+  c->K = K;
+  c->opts = *opts;
+  c->cap = opts->max_ctx;
+  c->max_chunks = (c->cap + kAttnChunk - 1) / kAttnChunk;
+  auto setup_model = [&](ModelState& m, const spec_model_desc* d) {
+    m.d = *d;
+    m.layers.assign(d->layers, d->layers + d->n_layers);
+    m.d.layers = m.layers.data();
+    m.esize = d->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  };
+  setup_model(c->tgt, target);
+  setup_model(c->drf, draft);
+#define INIT_TRY(expr)                                                                      \
+  do {                                                                                      \
+    cudaError_t e__ = (expr);                                                               \
+    if (e__ != cudaSuccess) {                                                               \
+      const int code__ = (e__ == cudaErrorMemoryAllocation) ? SPEC_E_OOM : SPEC_E_CUDA;     \
+      std::string m__ = std::string(#expr) + ": " + cudaGetErrorString(e__);                \
+      free_ctx(c);                                                                          \
+      return fail(nullptr, code__, m__);                                                    \
+    }                                                                                       \
+  } while (0)
+  INIT_TRY(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev));
+  INIT_TRY(configure_kernels());
+  if (opts->cuda_stream) {
+    c->stream = (cudaStream_t)opts->cuda_stream;
+  } else {
+    INIT_TRY(cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking));
+    c->own_stream = true;
+  }
+  const int V = target->vocab;
+  const int maxN = kGemmMaxTok;
+  auto mx = [&](auto f) { return std::max(f(c->tgt.d), f(c->drf.d)); };
+  const size_t dmax = mx([](const spec_model_desc& d) { return (size_t)d.d_model; });
+  const size_t fmax = mx([](const spec_model_desc& d) { return (size_t)d.ffn_dim; });
+  const size_t qkvmax = mx([](const spec_model_desc& d) {
+    return (size_t)(d.n_heads + 2 * d.n_kv_heads) * d.head_dim; });
+  const size_t hqd = mx([](const spec_model_desc& d) { return (size_t)d.n_heads * d.head_dim; });
+  const size_t hqmax = mx([](const spec_model_desc& d) { return (size_t)d.n_heads; });
+  const size_t hdmax = mx([](const spec_model_desc& d) { return (size_t)d.head_dim; });
+  INIT_TRY(dalloc(c, &c->st, 16 * sizeof(int32_t)));
+  INIT_TRY(cudaMemset(c->st, 0, 16 * sizeof(int32_t)));
+  INIT_TRY(dalloc(c, &c->seq, sizeof(int32_t) * (c->cap + K + 2)));
+  INIT_TRY(cudaMemset(c->seq, 0, sizeof(int32_t) * (c->cap + K + 2)));
+  INIT_TRY(dalloc(c, &c->fwd_tok, sizeof(int32_t) * maxN));
+  INIT_TRY(dalloc(c, &c->x, sizeof(float) * maxN * dmax));
+  INIT_TRY(dalloc(c, &c->xn, 4 * maxN * dmax));
+  INIT_TRY(dalloc(c, &c->hbuf, 4 * maxN * fmax));
+  INIT_TRY(dalloc(c, &c->qkv, sizeof(float) * maxN * qkvmax));
+  INIT_TRY(dalloc(c, &c->q, sizeof(float) * maxN * hqd));
+  INIT_TRY(dalloc(c, &c->attn, 4 * maxN * hqd));
+  INIT_TRY(dalloc(c, &c->attn_part,
+                  sizeof(float) * attn_partial_floats(maxN, (int)hqmax, (int)hdmax, c->max_chunks)));
+  INIT_TRY(dalloc(c, &c->logits_p, sizeof(float) * (size_t)(K + 1) * V));
+  INIT_TRY(dalloc(c, &c->logits_q, sizeof(float) * (size_t)K * V));
+  c->gs.partial_floats = gemm_partial_floats(c->num_sms);
+  c->gs.max_tiles = (int)std::max<size_t>(
+      (V + 15) / 16, std::max(fmax / 8, (std::max(qkvmax, dmax) + 15) / 16));
+  INIT_TRY(dalloc(c, &c->gs.partials, sizeof(float) * c->gs.partial_floats));
+  INIT_TRY(dalloc(c, &c->gs.tickets, sizeof(int) * c->gs.max_tiles));
+  INIT_TRY(cudaMemset(c->gs.tickets, 0, sizeof(int) * c->gs.max_tiles));
+  INIT_TRY(dalloc(c, &c->samp_part, sizeof(float) * sample_partial_floats(1, V)));
+  INIT_TRY(dalloc(c, &c->samp_tick, sizeof(int) * 4));
+  INIT_TRY(cudaMemset(c->samp_tick, 0, sizeof(int) * 4));
+  INIT_TRY(dalloc(c, &c->acc_part, sizeof(float) * accept_partial_floats(1, K, V)));
+  INIT_TRY(dalloc(c, &c->acc_tick, sizeof(int) * 4));
+  INIT_TRY(cudaMemset(c->acc_tick, 0, sizeof(int) * 4));
+  INIT_TRY(dalloc(c, &c->result, sizeof(int32_t) * (2 * K + 8)));
+  INIT_TRY(cudaMallocHost(&c->h_result, sizeof(int32_t) * (2 * K + 8)));
+  INIT_TRY(cudaMallocHost(&c->h_pos, sizeof(int32_t) * 4));
+  for (ModelState* m : {&c->tgt, &c->drf}) {
+    const size_t kvb = (size_t)m->d.n_layers * m->layer_kv_elems(c->cap) * m->esize;
+    INIT_TRY(dalloc(c, &m->kc, kvb));
+    INIT_TRY(dalloc(c, &m->vc, kvb));
+    INIT_TRY(cudaMemset(m->kc, 0, kvb));
+    INIT_TRY(cudaMemset(m->vc, 0, kvb));
+    const size_t tb = sizeof(float) * (size_t)c->cap * (m->d.head_dim / 2);
+    INIT_TRY(dalloc(c, &m->rope_cos, tb));
+    INIT_TRY(dalloc(c, &m->rope_sin, tb));
+    INIT_TRY(launch_rope_table(m->rope_cos, m->rope_sin, c->cap, m->d.head_dim,
+                               (double)m->d.rope_theta, c->stream));
+  }
+  if (opts->flags & SPEC_OPT_TIMING) {
+    const int n = 2 * (4 * target->n_layers + 1);
+    c->ev.resize(n);
+    c->ev_bytes.assign(n / 2, 0.0);
+    for (auto& ev : c->ev) INIT_TRY(cudaEventCreate(&ev));
+  }
+  INIT_TRY(cudaStreamSynchronize(c->stream));
+#undef INIT_TRY
+  *out = c;
+  return SPEC_OK;
+}
+
+int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  if (!tokens || L < 2) return fail(c, SPEC_E_ARG, "prefill needs at least 2 tokens");
+  if (L + c->K + 1 > c->cap) return fail(c, SPEC_E_CAPACITY, "prompt + K + 1 exceeds max_ctx");
+  const bool mix = c->opts.draft_mix_lambda != 0.f;
+  if (mix && L < c->K + 2) return fail(c, SPEC_E_ARG, "mixed draft needs a prompt of at least K + 2 tokens");
+  const int V = c->tgt.d.vocab;
+  for (int i = 0; i < L; ++i)
+    if (tokens[i] < 0 || tokens[i] >= V) return fail(c, SPEC_E_ARG, "token id out of range");
+  c->prefilled = false;
+  CUDA_TRY(c, cudaMemcpyAsync(c->seq, tokens, sizeof(int32_t) * L, cudaMemcpyHostToDevice, c->stream));
+  // st[0] = L - 1 (position of the pending token), step counters = 0
+  int32_t init[3] = {L - 1, 0, 0};
+  memcpy(c->h_result, init, sizeof init);
+  CUDA_TRY(c, cudaMemcpyAsync(c->st, c->h_result, sizeof init, cudaMemcpyHostToDevice, c->stream));
+  const int n = L - 1;   // positions 0..L-2 are scored; token L-1 is pending
+  const int K = c->K;
+  const int lo = n - (K + 1);  // rows of the previous-step logits before step 0
+  Launch Lc{c};
+  for (int p0 = 0; p0 < n; p0 += kGemmMaxTok) {
+    const int nt = std::min(kGemmMaxTok, n - p0);
+    int rc = set_eager_pos(c, p0);
+    if (rc) return rc;
+    forward(Lc, c->drf, nt, c->seq, nullptr, p0, c->st + 3, 0, 0, 0, nullptr);
+    int r0 = 0, rn = 0;
+    if (mix) {
+      r0 = std::max(lo, p0) - p0;
+      rn = std::min(n, p0 + nt) - p0 - r0;
+      if (rn < 0) rn = 0;
+    }
+    float* dst = c->logits_p + (size_t)std::max(0, p0 + r0 - lo) * V;
+    forward(Lc, c->tgt, nt, c->seq, nullptr, p0, c->st + 3, 0, r0, rn, dst);
+    CUDA_TRY(c, Lc.e);
+    // the pinned position slot is reused by the next chunk
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  }
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  c->host_L = L - 1;
+  c->prefilled = true;
+  c->draft_stale = false;
+  c->steps = c->ar_steps = c->emitted = c->accepted = 0;
+  std::fill(std::begin(c->hist), std::end(c->hist), 0);
+  return SPEC_OK;
+}
+
+int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* out_flags) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  if (!out_tokens || !out_count) return fail(c, SPEC_E_ARG, "null output buffer");
+  if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_step before spec_prefill");
+  if (c->draft_stale) return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
+  if (c->host_L + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
+  const int K = c->K;
+  c->ev_used = 0;
+  int rc = run_captured(c, &c->step_exec, enqueue_step, &c->kernels_step);
+  if (rc) return rc;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  const int32_t* h = c->h_result;
+  const int cnt = h[K + 1];
+  if (cnt < 1 || cnt > K + 1) return fail(c, SPEC_E_CUDA, "acceptance kernel returned an invalid count");
+  for (int i = 0; i < cnt; ++i) out_tokens[i] = h[i];
+  *out_count = cnt;
+  if (out_flags) *out_flags = (uint32_t)h[K + 2];
+  c->host_L += cnt;
+  c->steps++;
+  c->emitted += cnt;
+  c->accepted += cnt - 1;
+  c->hist[cnt - 1]++;
+  if (c->opts.flags & SPEC_OPT_TIMING) {
+    for (int i = 0; i + 1 < c->ev_used; i += 2) {
+      float ms = 0.f;
+      CUDA_TRY(c, cudaEventElapsedTime(&ms, c->ev[i], c->ev[i + 1]));
+      c->timed_ms += ms;
+      c->timed_bytes += c->ev_bytes[i / 2];
+      c->timed_launches++;
+    }
+  }
+  return SPEC_OK;
+}
+
+int spec_generate(spec_ctx* c, int n_new, int32_t* out, int32_t* out_n) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  if (n_new < 0 || (!out && n_new > 0) || !out_n) return fail(c, SPEC_E_ARG, "bad output buffer");
+  std::vector<int32_t> buf(c->K + 1);
+  int got = 0;
+  while (got < n_new) {
+    int32_t cnt = 0;
+    int rc = spec_step(c, buf.data(), &cnt, nullptr);
+    if (rc) return rc;
+    for (int i = 0; i < cnt && got < n_new; ++i) out[got++] = buf[i];
+  }
+  *out_n = got;
+  return SPEC_OK;
+}
+
+int spec_ar_step(spec_ctx* c, int32_t* out_token) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  if (!out_token) return fail(c, SPEC_E_ARG, "null output buffer");
+  if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_ar_step before spec_prefill");
+  if (c->host_L + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
+  int rc = run_captured(c, &c->ar_exec, enqueue_ar, &c->kernels_ar);
+  if (rc) return rc;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  *out_token = c->h_result[0];
+  c->host_L += 1;
+  c->ar_steps++;
+  c->draft_stale = true;
+  return SPEC_OK;
+}
+
+int spec_get_stats(const spec_ctx* c, spec_stats* o) {
+  if (!c || !o) return fail(const_cast<spec_ctx*>(c), SPEC_E_ARG, "null argument");
+  memset(o, 0, sizeof *o);
+  o->steps = c->steps;
+  o->ar_steps = c->ar_steps;
+  o->tokens_emitted = c->emitted;
+  o->drafts_accepted = c->accepted;
+  for (int i = 0; i < 17; ++i) o->accept_hist[i] = c->hist[i];
+  o->context_len = c->host_L + 1;
+  o->kernels_per_step = c->kernels_step;
+  o->kernels_per_ar_step = c->kernels_ar;
+  o->gemm_launches_per_verify = 4 * c->tgt.d.n_layers + 1;
+  o->verify_weight_bytes = c->tgt.weight_bytes();
+  o->draft_weight_bytes = c->drf.weight_bytes();
+  o->kv_bytes_per_token_target = c->tgt.kv_bytes_per_token();
+  o->kv_bytes_per_token_draft = c->drf.kv_bytes_per_token();
+  o->timed_gemm_ms = c->timed_ms;
+  o->timed_gemm_bytes = c->timed_bytes;
+  o->timed_gemm_launches = c->timed_launches;
+  return SPEC_OK;
+}
+
+int spec_last_step_debug(spec_ctx* c, float* p_logits, float* q_logits, int32_t* drafts,
+                         int32_t* context, int32_t* context_len) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  const int K = c->K, V = c->tgt.d.vocab;
+  if (p_logits)
+    CUDA_TRY(c, cudaMemcpyAsync(p_logits, c->logits_p, sizeof(float) * (size_t)(K + 1) * V,
+                                cudaMemcpyDeviceToHost, c->stream));
+  if (q_logits)
+    CUDA_TRY(c, cudaMemcpyAsync(q_logits, c->logits_q, sizeof(float) * (size_t)K * V,
+                                cudaMemcpyDeviceToHost, c->stream));
+  if (drafts)
+    CUDA_TRY(c, cudaMemcpyAsync(drafts, c->result + (K + 3), sizeof(int32_t) * K,
+                                cudaMemcpyDeviceToHost, c->stream));
+  if (context)
+    CUDA_TRY(c, cudaMemcpyAsync(context, c->seq, sizeof(int32_t) * (c->host_L + 1),
+                                cudaMemcpyDeviceToHost, c->stream));
+  if (context_len) *context_len = c->host_L + 1;
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  return SPEC_OK;
+}
+
+int spec_model_forward(spec_ctx* c, int which, const int32_t* tokens, int n, int pos0,
+                       float* logits_dev) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  if (which != 0 && which != 1) return fail(c, SPEC_E_ARG, "which must be 0 (target) or 1 (draft)");
+  if (!tokens || n < 1 || pos0 < 0) return fail(c, SPEC_E_ARG, "bad tokens");
+  if (pos0 + n > c->cap) return fail(c, SPEC_E_CAPACITY, "positions exceed max_ctx");
+  ModelState& m = which == 0 ? c->tgt : c->drf;
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= m.d.vocab) return fail(c, SPEC_E_ARG, "token id out of range");
+  c->prefilled = false;
+  Launch L{c};
+  for (int p = 0; p < n; p += kGemmMaxTok) {
+    const int nt = std::min(kGemmMaxTok, n - p);
+    CUDA_TRY(c, cudaMemcpyAsync(c->fwd_tok, tokens + p, sizeof(int32_t) * nt,
+                                cudaMemcpyHostToDevice, c->stream));
+    int rc = set_eager_pos(c, pos0 + p);
+    if (rc) return rc;
+    forward(L, m, nt, c->fwd_tok, nullptr, 0, c->st + 3, 0, 0, logits_dev ? nt : 0,
+            logits_dev ? logits_dev + (size_t)p * m.d.vocab : nullptr);
+    CUDA_TRY(c, L.e);
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  }
+  return SPEC_OK;
+}
+
+int spec_accept_rows(const float* p_logits, int64_t p_row_stride, const float* q_logits,
+                     int64_t q_row_stride, const int32_t* drafts, int rows, int K, int V,
+                     float temperature, uint64_t seed, uint64_t step_base, int32_t* tokens,
+                     int32_t* counts, uint32_t* flags, void* stream) {
+  if (!p_logits || !q_logits || !drafts || !tokens || !counts)
+    return fail(nullptr, SPEC_E_ARG, "spec_accept_rows: null pointer");
+  if (rows < 1 || K < 1 || K > 16 || V < 2 || !(temperature >= 0.f))
+    return fail(nullptr, SPEC_E_ARG, "spec_accept_rows: bad size or temperature");
+  if (rows > 65535) return fail(nullptr, SPEC_E_ARG, "spec_accept_rows: at most 65535 rows per call");
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t pf = accept_partial_floats(rows, K, V);
+  void* scratch = nullptr;
+  const size_t bytes = pf * sizeof(float) + (size_t)rows * sizeof(int);
+  cudaError_t e = cudaMallocAsync(&scratch, bytes, st);
+  if (e != cudaSuccess) return fail(nullptr, SPEC_E_OOM, std::string("spec_accept_rows: ") + cudaGetErrorString(e));
+  int* tick = (int*)((float*)scratch + pf);
+  e = cudaMemsetAsync(tick, 0, (size_t)rows * sizeof(int), st);
+  AcceptDesc a{};
+  a.p = p_logits; a.p_ld = p_row_stride; a.q = q_logits; a.q_ld = q_row_stride;
+  a.drafts = drafts; a.rows = rows; a.K = K; a.V = V; a.temperature = temperature;
+  a.seed = seed; a.step_base = step_base; a.out_tokens = tokens; a.out_count = counts;
+  a.out_flags = flags; a.partials = (float*)scratch; a.tickets = tick;
+  if (e == cudaSuccess) e = launch_accept(a, st);
+  cudaError_t e2 = cudaFreeAsync(scratch, st);
+  if (e != cudaSuccess) return fail(nullptr, SPEC_E_CUDA, std::string("spec_accept_rows: ") + cudaGetErrorString(e));
+  if (e2 != cudaSuccess) return fail(nullptr, SPEC_E_CUDA, std::string("spec_accept_rows: ") + cudaGetErrorString(e2));
+  return SPEC_OK;
+}
+
+int spec_sample_rows(const float* logits, int64_t row_stride, int rows, int V, float temperature,
+                     uint64_t seed, uint64_t step_base, int position, int32_t* tokens,
+                     void* stream) {
+  if (!logits || !tokens) return fail(nullptr, SPEC_E_ARG, "spec_sample_rows: null pointer");
+  if (rows < 1 || rows > 65535 || V < 2 || !(temperature >= 0.f) || position < 0)
+    return fail(nullptr, SPEC_E_ARG, "spec_sample_rows: bad size or temperature");
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t pf = sample_partial_floats(rows, V);
+  void* scratch = nullptr;
+  const size_t bytes = pf * sizeof(float) + (size_t)rows * sizeof(int);
+  cudaError_t e = cudaMallocAsync(&scratch, bytes, st);
+  if (e != cudaSuccess) return fail(nullptr, SPEC_E_OOM, std::string("spec_sample_rows: ") + cudaGetErrorString(e));
+  int* tick = (int*)((float*)scratch + pf);
+  e = cudaMemsetAsync(tick, 0, (size_t)rows * sizeof(int), st);
+  SampleDesc s{};
+  s.logits = logits; s.ld = row_stride; s.rows = rows; s.V = V; s.temperature = temperature;
+  s.seed = seed; s.step_base = step_base; s.position = (uint32_t)position;
+  s.stream = kStreamDraft; s.out_token = tokens; s.partials = (float*)scratch; s.tickets = tick;
+  if (e == cudaSuccess) e = launch_sample(s, st);
+  cudaError_t e2 = cudaFreeAsync(scratch, st);
+  if (e != cudaSuccess) return fail(nullptr, SPEC_E_CUDA, std::string("spec_sample_rows: ") + cudaGetErrorString(e));
+  if (e2 != cudaSuccess) return fail(nullptr, SPEC_E_CUDA, std::string("spec_sample_rows: ") + cudaGetErrorString(e2));
+  return SPEC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads,
+exports every function include/specverify.h declares, and rejects bad
+arguments with the documented codes before touching the device.  Without a
+GPU, a valid spec_init fails with SPEC_E_CUDA: there is no CPU fallback."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import speculative_decoding_verification_step_gb300 as sv
+from speculative_decoding_verification_step_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return sv.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"^SPEC_API\s+[\w\s\*]+?\b(spec_\w+)\s*\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in sv.SIGNATURES, n
+    assert set(sv.SIGNATURES) == set(names)
+
+
+def test_version(L):
+    assert b"sm_103a" in L.spec_version()
+
+
+def _desc(vocab=256, head_dim=32, dtype=sv.SPEC_DTYPE_F32, layers=None):
+    fake = 0x1000
+    lay = (sv.LayerWeights * 1)()
+    for n in sv._LAYER_FIELDS:
+        setattr(lay[0], n, fake)
+    d = sv.ModelDesc(1, 128, 4, 4, head_dim, 512, vocab, 10000.0, 1e-5, dtype, fake, fake, fake,
+                     lay if layers is None else layers)
+    return d, lay
+
+
+def _init(L, t, d, k=4, max_ctx=128):
+    opts = sv.Opts(1, max_ctx, 1.0, 0, 0.0, None, 0)
+    h = ctypes.c_void_p()
+    rc = L.spec_init(ctypes.byref(t) if t is not None else None,
+                     ctypes.byref(d) if d is not None else None, k, ctypes.byref(opts), ctypes.byref(h))
+    return rc, h
+
+
+def test_init_argument_errors(L):
+    t, _a = _desc()
+    d, _b = _desc()
+    assert _init(L, None, d)[0] == -1                       # SPEC_E_ARG
+    bad, _c = _desc(vocab=300)
+    rc, h = _init(L, t, bad)
+    assert rc == -2 and not h.value                         # SPEC_E_VOCAB
+    assert b"vocabular" in L.spec_last_error(None)
+    hd, _d = _desc(head_dim=48)
+    assert _init(L, t, hd)[0] == -3                         # SPEC_E_SHAPE
+    assert _init(L, t, d, k=0)[0] == -1
+    assert _init(L, t, d, k=17)[0] == -1
+    bf, _e = _desc(dtype=sv.SPEC_DTYPE_BF16)                # d_model 128 ok, ffn 512 ok
+    bf.d_model = 96                                         # not a multiple of 64
+    assert _init(L, bf, d)[0] == -3
+    nulls = (sv.LayerWeights * 1)()
+    nl, _f = _desc(layers=nulls)
+    assert _init(L, nl, d)[0] == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_no_cpu_fallback(L):
+    t, _a = _desc()
+    d, _b = _desc()
+    rc, h = _init(L, t, d)
+    assert rc == -5 and not h.value                         # SPEC_E_CUDA
+    assert L.spec_last_error(None)
+
+
+def test_stateless_argument_errors(L):
+    rc = L.spec_accept_rows(None, 0, None, 0, None, 1, 4, 10, 1.0, 0, 0, None, None, None, None)
+    assert rc == -1
+    p = ctypes.c_void_p(0x1000)
+    assert L.spec_accept_rows(p, 0, p, 0, p, 1, 17, 10, 1.0, 0, 0, p, p, None, None) == -1
+    assert L.spec_accept_rows(p, 0, p, 0, p, 0, 4, 10, 1.0, 0, 0, p, p, None, None) == -1
+    assert L.spec_sample_rows(None, 0, 1, 10, 1.0, 0, 0, 1, None, None) == -1
+    assert L.spec_sample_rows(p, 0, 1, 10, -1.0, 0, 0, 1, p, None) == -1
+
+
+def test_null_context_calls(L):
+    L.spec_free(None)
+    assert L.spec_prefill(None, None, 0) == -1
+    assert L.spec_step(None, None, None, None) == -1
+    assert L.spec_ar_step(None, None) == -1
+    assert L.spec_get_stats(None, None) == -1
+    assert L.spec_last_error(None)
+
+
+def test_binding_refuses_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(sv, "_lib", None)
+    monkeypatch.setattr(sv, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        sv.lib()

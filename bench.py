@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Speculative-decoding verification step on GB300: accepted tokens/s at batch
+1, K = 5, with an 8B-shaped bf16 target and a 1B-shaped bf16 draft (random
+N(0, 0.02^2) weights, 512-token uniform-random prompts, 128 new tokens per
+generation), plus verify-step HBM GB/s.
+
+One "step" is one speculative step: K draft passes + samplers, one target
+pass over the K+1 positions, the fused acceptance kernel and the commit.
+The timed region runs whole generations (prompt -> 128 tokens) back to back;
+each generation's prefill happens outside the timed region, with inputs
+already resident.  Every step streams ~17.5 GB of weights, far larger than
+the 129 MB L2, so no L2 flush is needed between steps.
+
+--gpus N (torchrun) runs N independent replicas, one per GPU (the step does
+not shard at batch 1): value = tokens of all ranks / max time over ranks.
+--impl reference times the fp64 CPU oracle on this host instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("accepted tokens/s at batch 1, K=5 (8B-shaped bf16); verify-step HBM GB/s")
+HBM_ROOFLINE_GBS = 8000.0          # the figure the step's roofline target is stated against
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=240)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--k", type=int, default=5)
+    ap.add_argument("--temperature", type=float, default=1.0)
+    ap.add_argument("--mix", type=float, default=0.5, help="draft/target-previous-logit mix lambda")
+    ap.add_argument("--prompt", type=int, default=512)
+    ap.add_argument("--new-tokens", type=int, default=128)
+    ap.add_argument("--workload", choices=["8b", "1b"], default="8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--ar-tokens", type=int, default=128)
+    return ap.parse_args()
+
+
+def workload_shapes(name):
+    import workloads
+    if name == "8b":
+        return workloads.EIGHT_B, workloads.ONE_B, "8B-shaped target + 1B-shaped draft"
+    return workloads.ONE_B, None, "1B-shaped target + its first 2 layers as draft"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.idx)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.f.seek(0)
+        rows = [r.split(", ") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                mhz.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def gemm_traffic_record():
+    """DRAM traffic of the GEMM kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemm_bf16_streamk_traffic.json")
+    src = os.path.join(ROOT, "speculative_decoding_verification_step_gb300", "csrc", "gemm.cu")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return rec if rec.get("gemm_cu_sha256_16") == h else None
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- oracle
+def oracle_step_sample(tshape, tw, dshape, dw, k, temperature, mix, prompt_len=16, seed=0):
+    """One full-depth oracle speculative step on a short prompt; returns
+    (tokens emitted, seconds, threads)."""
+    import torch
+    import workloads
+    from oracle import generate as gen
+    T, D = gen.Model(tshape, tw), gen.Model(dshape, dw)
+    prompt = workloads.make_prompt(tshape.vocab, prompt_len, seed=seed)[0].tolist()
+    prev = gen.prefill_prev_logits(T, prompt, k) if mix else None
+    t0 = time.perf_counter()
+    res = gen.spec_step(T, D, prompt, k, temperature, 0, 0, prev, mix)
+    dt = time.perf_counter() - t0
+    return len(res.emitted), dt, torch.get_num_threads()
+
+
+def host_weights(shape, seed):
+    """Seeded weights of a large model, drawn on the GPU (fast) and copied to host."""
+    import torch
+    import workloads
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = workloads.make_weights(shape, seed, device=dev)
+    if dev == "cuda":
+        w = {k: ([{kk: vv.cpu() for kk, vv in l.items()} for l in v] if k == "layers" else v.cpu())
+             for k, v in w.items()}
+        torch.cuda.empty_cache()
+    return w
+
+
+def run_reference(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    tshape, dshape, wl = workload_shapes(args.workload)
+    tw = host_weights(tshape, 1)
+    if dshape is None:
+        import workloads
+        dshape, dw = workloads.prefix_draft(tshape, tw, 2)
+    else:
+        dw = host_weights(dshape, 2)
+    times, toks = [], 0
+    threads = torch.get_num_threads()
+    for i in range(args.warmup + args.steps):
+        n, dt, threads = oracle_step_sample(tshape, tw, dshape, dw, args.k, args.temperature,
+                                            args.mix, seed=100 + i)
+        if i >= args.warmup:
+            times.append(dt)
+            toks += n
+    total = sum(times)
+    v = toks / total
+    sample = (f"each step: one full-depth fp64 oracle speculative step ({wl}, K={args.k}, "
+              f"T={args.temperature}, lambda={args.mix}) on a 16-token prompt instead of 512")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * total / max(1, len(times)), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl, "K": args.k, "temperature": args.temperature,
+                       "mix_lambda": args.mix, "prompt": 16, "batch": 1},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- ours
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import torch.distributed as dist
+    import workloads
+    import speculative_decoding_verification_step_gb300 as sv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sv.build()
+    sv.lib()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    tshape, dshape, wl = workload_shapes(args.workload)
+    K = args.k
+    tw = workloads.make_weights(tshape, 1, device="cuda")
+    if dshape is None:
+        dshape, dw = workloads.prefix_draft(tshape, tw, 2)
+    else:
+        dw = workloads.make_weights(dshape, 2, device="cuda")
+    torch.cuda.synchronize()
+    max_ctx = args.prompt + args.new_tokens + 4 * (K + 1) + 64
+    stream = torch.cuda.Stream()
+
+    def make(temp, mix, flags=0):
+        return sv.SpecDecoder(tshape, tw, dshape, dw, K, max_ctx, temperature=temp, seed=0,
+                              mix_lambda=mix, stream=stream.cuda_stream, flags=flags)
+
+    def prompt(i):
+        return workloads.make_prompt(tshape.vocab, args.prompt, seed=1000 * rank + i)[0].tolist()
+
+    def timed_generations(dec, n_steps, gen_base):
+        """Run n_steps speculative steps as whole generations; returns (ms, tokens, steps)."""
+        ms, toks, done, g = 0.0, 0, 0, gen_base
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        while done < n_steps:
+            dec.prefill(prompt(g))
+            g += 1
+            emitted = 0
+            e0.record(stream)
+            while emitted < args.new_tokens and done < n_steps:
+                t, _ = dec.step()
+                emitted += len(t)
+                done += 1
+            e1.record(stream)
+            e1.synchronize()
+            ms += e0.elapsed_time(e1)
+            toks += emitted
+        return ms, toks, done
+
+    # ---- headline run ----
+    dec = make(args.temperature, args.mix)
+    dec.prefill(prompt(0))
+    for _ in range(args.warmup):
+        dec.step()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        ms, toks, nsteps = timed_generations(dec, args.steps, 1)
+        wall = time.perf_counter() - wall0
+    clocks = clk.summary()
+    st = dec.stats()
+    if world > 1:
+        t = torch.tensor([ms, toks], dtype=torch.float64, device="cuda")
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        ms_max, toks_all = float(mx[0]), float(t[1])
+    else:
+        ms_max, toks_all = ms, float(toks)
+    value = toks_all / (ms_max / 1000.0)
+    hist = st["accept_hist"][:K + 1]
+    steps_in_stats = max(1, sum(hist))
+    tokens_per_step = sum((i + 1) * h for i, h in enumerate(hist)) / steps_in_stats
+    alpha = sum(i * h for i, h in enumerate(hist)) / max(1, sum(i * h for i, h in enumerate(hist)) +
+                                                         sum(hist[:K]))
+
+    # ---- phase times (graph replay): verify pass, draft loop, plain decoding ----
+    dec.prefill(prompt(0))
+    prof = dec.profile(iters=20)
+    L = args.prompt + args.new_tokens // 2     # mid-generation context for the byte count
+    kv_t, kv_d = st["kv_bytes_per_token_target"], st["kv_bytes_per_token_draft"]
+    verify_bytes = st["verify_weight_bytes"] + (L + K + 1) * kv_t + (K + 1) * tshape.vocab * 4
+    draft_bytes = K * st["draft_weight_bytes"] + K * (L + K) * kv_d
+    verify_gbs = verify_bytes / (prof["verify_ms"] * 1e6)
+    hbm_peak, peak_kind = peaks()
+    step_bytes = verify_bytes + draft_bytes
+    roofline_tok_s = tokens_per_step / (step_bytes / (HBM_ROOFLINE_GBS * 1e9))
+
+    # ---- plain autoregressive decoding on the same kernels ----
+    ar = make(args.temperature, 0.0)
+    ar.prefill(prompt(0))
+    for _ in range(3):
+        ar.ar_step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ar.prefill(prompt(1))
+    e0.record(stream)
+    for _ in range(args.ar_tokens):
+        ar.ar_step()
+    e1.record(stream)
+    e1.synchronize()
+    ar_tok_s = args.ar_tokens / (e0.elapsed_time(e1) / 1000.0)
+    ar_kernels = ar.stats()["kernels_per_ar_step"]
+    ar.close()
+
+    # ---- dominant kernel (verify GEMMs), timed live with CUDA events ----
+    tim = make(args.temperature, args.mix, flags=sv.SPEC_OPT_TIMING)
+    tim.prefill(prompt(0))
+    tim.step()
+    for _ in range(8):
+        tim.step()
+    ts = tim.stats()
+    tim.close()
+    launches = max(1, ts["timed_gemm_launches"])
+    gemm_achieved = ts["timed_gemm_bytes"] / (ts["timed_gemm_ms"] * 1e6)
+    traffic = gemm_traffic_record()
+    roofline = {"bound": "hbm", "kernel": "gemm_bf16_streamk (verify-pass weight GEMMs)",
+                "achieved": gemm_achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gemm_achieved / hbm_peak, "peak_kind": peak_kind,
+                "bytes_per_launch": ts["timed_gemm_bytes"] / launches,
+                "ms_per_launch": ts["timed_gemm_ms"] / launches,
+                "traffic": (traffic["traffic_ratio"] * ts["timed_gemm_bytes"] / launches)
+                if traffic else None}
+
+    # ---- sweep of the other draft settings of this workload ----
+    sweep = []
+    if not args.no_sweep:
+        for temp, mix in [(1.0, 0.0), (1.0, 0.9), (0.0, 0.0), (0.0, 0.9)]:
+            if (temp, mix) == (args.temperature, args.mix):
+                continue
+            d2 = make(temp, mix)
+            d2.prefill(prompt(0))
+            d2.step()
+            m2, t2, n2 = timed_generations(d2, 60, 50)
+            s2 = d2.stats()
+            h2 = s2["accept_hist"][:K + 1]
+            sweep.append({"temperature": temp, "mix_lambda": mix, "tokens_per_s": t2 / (m2 / 1000),
+                          "tokens_per_step": t2 / n2,
+                          "speedup_vs_ar": (t2 / (m2 / 1000)) / ar_tok_s})
+            d2.close()
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e_reqs, e2e_toks, e2e_steps = 2, 0, 0
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for i in range(e2e_reqs):
+        dec.prefill(prompt(200 + i))       # host prompt -> device, prefill
+        out = dec.generate(args.new_tokens)   # host token buffer
+        e2e_toks += len(out)
+        e2e_steps += dec.stats()["steps"]
+    e2e_s = time.perf_counter() - w0
+    e2e_steps = max(1, e2e_steps)
+    e2e = {"value": e2e_toks / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": round(e2e_reqs * args.prompt * 4 / e2e_steps, 1),
+           "d2h_bytes_per_step": (2 * K + 3) * 4,
+           "includes": f"prompt upload ({args.prompt} int32) + prefill + {args.new_tokens} tokens per request"}
+
+    # ---- oracle on the host cores (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del dec
+        thw = {k: ([{kk: vv.cpu() for kk, vv in l.items()} for l in v] if k == "layers" else v.cpu())
+               for k, v in tw.items()}
+        dhw = ({k: ([{kk: vv.cpu() for kk, vv in l.items()} for l in v] if k == "layers" else v.cpu())
+                for k, v in dw.items()})
+        n, dt, threads = oracle_step_sample(tshape, thw, dshape, dhw, K, args.temperature, args.mix)
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"1 full-depth fp64 oracle speculative step ({wl}, K={K}) on a 16-token "
+                         f"prompt ({dt:.1f} s, {n} tokens)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": nsteps, "warmup": args.warmup, "ms_per_step": ms_max / max(1, nsteps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (random N(0,0.02^2) weights, uniform-random prompts)",
+        "config": {"workload": wl, "batch": 1, "K": K, "prompt": args.prompt,
+                   "new_tokens_per_generation": args.new_tokens, "temperature": args.temperature,
+                   "mix_lambda": args.mix, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (17.5 GB of weights per step)"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": st["kernels_per_step"] * nsteps,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "verify_step": {"ms": prof["verify_ms"], "bytes": verify_bytes, "GB_s": verify_gbs,
+                        "frac_of_8TBs": verify_gbs / HBM_ROOFLINE_GBS,
+                        "frac_of_measured": verify_gbs / hbm_peak, "kernels": prof["kernels_verify"]},
+        "draft_loop": {"ms": prof["draft_loop_ms"], "bytes": draft_bytes,
+                       "GB_s": draft_bytes / (prof["draft_loop_ms"] * 1e6),
+                       "kernels": prof["kernels_draft_loop"]},
+        "ar_decoding": {"tokens_per_s": ar_tok_s, "ms_per_token": 1000.0 / ar_tok_s,
+                        "pass_ms": prof["ar_ms"], "kernels_per_token": ar_kernels},
+        "speedup_vs_ar": value / ar_tok_s,
+        "tokens_per_step": tokens_per_step, "acceptance_alpha": alpha,
+        "accepted_tokens_s_frac_of_8TBs_roofline": value / roofline_tok_s,
+        "modelled_speedup": {"C": prof["draft_loop_ms"] / max(1e-9, K * prof["verify_ms"]),
+                             "K_alpha_over_1_plus_KC": K * alpha / (1 + K * prof["draft_loop_ms"] /
+                                                                    max(1e-9, K * prof["verify_ms"]))},
+        "sweep": sweep,
+        "wall_s_timed": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -220,6 +220,26 @@ SPEC_API int spec_sample_rows(const float* logits, int64_t row_stride, int rows,
                      float temperature, uint64_t seed, uint64_t step_base, int position,
                      int32_t* tokens, void* stream);
 
+/* Phase timing of the step as run in production (CUDA graphs, CUDA events
+ * on the context's stream), averaged over `iters` replays after two
+ * warm-up replays: the draft loop (K draft passes + samplers), the verify
+ * pass (target over the K+1 positions + fused acceptance, not committed)
+ * and one plain-decoding pass (target over 1 position + sampler, not
+ * committed).  Requires a prefilled context; the committed state is left
+ * unchanged (only uncommitted KV rows and draft slots are rewritten, with
+ * the values the next step computes anyway).  Measures the quantities of
+ * [INT 加速倍率 = K × acceptance rate 的限制]: T_draft, T_target and C. */
+typedef struct spec_profile_t {
+    double draft_loop_ms;
+    double verify_ms;
+    double ar_ms;
+    int32_t iters;
+    int32_t kernels_draft_loop;
+    int32_t kernels_verify;
+    int32_t kernels_ar;
+} spec_profile_t;
+SPEC_API int spec_profile(spec_ctx* ctx, int iters, spec_profile_t* out);
+
 /* Library version string. */
 SPEC_API const char* spec_version(void);
 

@@ -65,6 +65,16 @@ class Stats(ctypes.Structure):
         return d
 
 
+class Profile(ctypes.Structure):
+    _fields_ = [("draft_loop_ms", ctypes.c_double), ("verify_ms", ctypes.c_double),
+                ("ar_ms", ctypes.c_double), ("iters", ctypes.c_int32),
+                ("kernels_draft_loop", ctypes.c_int32), ("kernels_verify", ctypes.c_int32),
+                ("kernels_ar", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _U32P = ctypes.POINTER(ctypes.c_uint32)
 _F32P = ctypes.POINTER(ctypes.c_float)
@@ -89,6 +99,7 @@ SIGNATURES = {
     "spec_sample_rows": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64,
                                         ctypes.c_int, _VP, _VP]),
+    "spec_profile": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(Profile)]),
     "spec_version": (ctypes.c_char_p, []),
 }
 
@@ -197,6 +208,12 @@ class SpecDecoder:
         s = Stats()
         _check(lib().spec_get_stats(self.ctx, ctypes.byref(s)), self.ctx)
         return s.as_dict()
+
+    def profile(self, iters=20):
+        """Graph-replayed phase times (ms): draft loop, verify pass, plain-decoding pass."""
+        pr = Profile()
+        _check(lib().spec_profile(self.ctx, iters, ctypes.byref(pr)), self.ctx)
+        return pr.as_dict()
 
     def last_step_debug(self, max_ctx):
         """(p_logits [K+1, V], q_logits [K, V], drafts [K], context tokens) as numpy."""

@@ -91,6 +91,8 @@ struct spec_ctx {
   // graphs
   cudaGraphExec_t step_exec = nullptr;
   cudaGraphExec_t ar_exec = nullptr;
+  cudaGraphExec_t prof_exec[3] = {nullptr, nullptr, nullptr};  // draft loop, verify, ar
+  int prof_kernels[3] = {0, 0, 0};
   // host mirror of the state
   bool prefilled = false;
   bool draft_stale = false;
@@ -263,7 +265,7 @@ void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const 
   }
 }
 
-void enqueue_step(Launch& L) {
+void enqueue_draft(Launch& L) {
   spec_ctx* c = L.c;
   const int K = c->K, V = c->tgt.d.vocab;
   const int32_t* Lp = c->st;  // committed length index (position of the pending token)
@@ -286,8 +288,14 @@ void enqueue_step(Launch& L) {
     sd.partials = c->samp_part; sd.tickets = c->samp_tick;
     L.note(launch_sample(sd, c->stream));
   }
+}
+
+void enqueue_verify(Launch& L, bool commit) {
+  spec_ctx* c = L.c;
+  const int K = c->K, V = c->tgt.d.vocab;
+  const int32_t* Lp = c->st;
   const bool was = c->timing_verify;
-  c->timing_verify = (c->opts.flags & SPEC_OPT_TIMING) != 0;
+  c->timing_verify = commit && (c->opts.flags & SPEC_OPT_TIMING) != 0;
   forward(L, c->tgt, K + 1, c->seq, Lp, 0, Lp, 0, 0, K + 1, c->logits_p);
   c->timing_verify = was;
   AcceptDesc ad{};
@@ -298,15 +306,26 @@ void enqueue_step(Launch& L) {
   ad.step_dev = c->st + 1; ad.step_base = 0;
   ad.out_tokens = c->result; ad.out_count = c->result + (K + 1);
   ad.out_flags = (uint32_t*)(c->result + (K + 2));
-  ad.commit_seq = c->seq; ad.commit_len = c->st; ad.commit_step = c->st + 1;
+  if (commit) {
+    ad.commit_seq = c->seq; ad.commit_len = c->st; ad.commit_step = c->st + 1;
+  }
   ad.partials = c->acc_part; ad.tickets = c->acc_tick;
   L.note(launch_accept(ad, c->stream));
+}
+
+void enqueue_step(Launch& L) {
+  spec_ctx* c = L.c;
+  const int K = c->K;
+  enqueue_draft(L);
+  enqueue_verify(L, true);
   L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 3),
                          cudaMemcpyDeviceToHost, c->stream));
   c->launch_count--;  // the copy is not a kernel
 }
 
-void enqueue_ar(Launch& L) {
+void enqueue_verify_only(Launch& L) { enqueue_verify(L, false); }
+
+void enqueue_ar_pass(Launch& L, bool commit) {
   spec_ctx* c = L.c;
   const int V = c->tgt.d.vocab;
   const int32_t* Lp = c->st;
@@ -316,12 +335,37 @@ void enqueue_ar(Launch& L) {
   sd.temperature = c->opts.temperature; sd.seed = c->opts.seed;
   sd.step_dev = c->st + 2; sd.position = 0; sd.stream = kStreamAR;
   sd.out_token = c->result; sd.out_idx = nullptr; sd.out_off = 0;
-  sd.commit_seq = c->seq; sd.commit_len = c->st; sd.commit_step = c->st + 2;
+  if (commit) {
+    sd.commit_seq = c->seq; sd.commit_len = c->st; sd.commit_step = c->st + 2;
+  }
   sd.partials = c->samp_part; sd.tickets = c->samp_tick;
   L.note(launch_sample(sd, c->stream));
+}
+
+void enqueue_ar(Launch& L) {
+  spec_ctx* c = L.c;
+  enqueue_ar_pass(L, true);
   L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t), cudaMemcpyDeviceToHost,
                          c->stream));
   c->launch_count--;
+}
+
+void enqueue_ar_only(Launch& L) { enqueue_ar_pass(L, false); }
+
+int capture(spec_ctx* c, cudaGraphExec_t* exec, void (*enq)(Launch&), int* nkern) {
+  CUDA_TRY(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeRelaxed));
+  Launch L{c};
+  c->launch_count = 0;
+  enq(L);
+  cudaGraph_t g = nullptr;
+  cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+  CUDA_TRY(c, L.e);
+  CUDA_TRY(c, e2);
+  *nkern = c->launch_count;
+  cudaError_t e3 = cudaGraphInstantiate(exec, g, 0);
+  cudaGraphDestroy(g);
+  CUDA_TRY(c, e3);
+  return SPEC_OK;
 }
 
 bool use_graph(const spec_ctx* c) {
@@ -338,18 +382,8 @@ int run_captured(spec_ctx* c, cudaGraphExec_t* exec, void (*enq)(Launch&), int* 
     return SPEC_OK;
   }
   if (!*exec) {
-    CUDA_TRY(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeRelaxed));
-    Launch L{c};
-    c->launch_count = 0;
-    enq(L);
-    cudaGraph_t g = nullptr;
-    cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
-    CUDA_TRY(c, L.e);
-    CUDA_TRY(c, e2);
-    *nkern = c->launch_count;
-    cudaError_t e3 = cudaGraphInstantiate(exec, g, 0);
-    cudaGraphDestroy(g);
-    CUDA_TRY(c, e3);
+    int rc = capture(c, exec, enq, nkern);
+    if (rc) return rc;
   }
   CUDA_TRY(c, cudaGraphLaunch(*exec, c->stream));
   return SPEC_OK;
@@ -359,6 +393,8 @@ void free_ctx(spec_ctx* c) {
   if (!c) return;
   if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
   if (c->ar_exec) cudaGraphExecDestroy(c->ar_exec);
+  for (cudaGraphExec_t g : c->prof_exec)
+    if (g) cudaGraphExecDestroy(g);
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->h_result) cudaFreeHost(c->h_result);
@@ -651,6 +687,43 @@ int spec_last_step_debug(spec_ctx* c, float* p_logits, float* q_logits, int32_t*
                                 cudaMemcpyDeviceToHost, c->stream));
   if (context_len) *context_len = c->host_L + 1;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  return SPEC_OK;
+}
+
+int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
+  if (!c || !out) return fail(c, SPEC_E_ARG, "null argument");
+  if (iters < 1) return fail(c, SPEC_E_ARG, "iters must be >= 1");
+  if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_profile before spec_prefill");
+  if (c->draft_stale) return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
+  if (c->host_L + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
+  void (*enq[3])(Launch&) = {enqueue_draft, enqueue_verify_only, enqueue_ar_only};
+  double ms[3];
+  cudaEvent_t e0, e1;
+  CUDA_TRY(c, cudaEventCreate(&e0));
+  CUDA_TRY(c, cudaEventCreate(&e1));
+  for (int k = 0; k < 3; ++k) {
+    if (!c->prof_exec[k]) {
+      int rc = capture(c, &c->prof_exec[k], enq[k], &c->prof_kernels[k]);
+      if (rc) { cudaEventDestroy(e0); cudaEventDestroy(e1); return rc; }
+    }
+    for (int w = 0; w < 2; ++w) CUDA_TRY(c, cudaGraphLaunch(c->prof_exec[k], c->stream));
+    CUDA_TRY(c, cudaEventRecord(e0, c->stream));
+    for (int i = 0; i < iters; ++i) CUDA_TRY(c, cudaGraphLaunch(c->prof_exec[k], c->stream));
+    CUDA_TRY(c, cudaEventRecord(e1, c->stream));
+    CUDA_TRY(c, cudaEventSynchronize(e1));
+    float t = 0.f;
+    CUDA_TRY(c, cudaEventElapsedTime(&t, e0, e1));
+    ms[k] = (double)t / iters;
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  out->draft_loop_ms = ms[0];
+  out->verify_ms = ms[1];
+  out->ar_ms = ms[2];
+  out->iters = iters;
+  out->kernels_draft_loop = c->prof_kernels[0];
+  out->kernels_verify = c->prof_kernels[1];
+  out->kernels_ar = c->prof_kernels[2];
   return SPEC_OK;
 }
 

@@ -37,6 +37,8 @@ def equal_mass_bins(p, nbins):
     order = np.argsort(-p, kind="stable")
     cum = np.cumsum(p[order])
     ids = np.minimum((cum - p[order] / 2) * nbins, nbins - 1).astype(int)
+    # a single heavy token can span several nominal bins: keep non-empty ones
+    _, ids = np.unique(ids, return_inverse=True)
     out = np.empty_like(ids)
     out[order] = ids
     return out

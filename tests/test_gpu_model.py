@@ -95,7 +95,8 @@ def _teacher_forced(shape, w, dshape, dw, prompt, k, temp, n_new, mix=0.0, seed=
         if same < k:
             assert ref.flags & helpers.SKIP_FLAGS, (step, ref.drafts, list(d))
         # stage (ii): acceptance on the GPU's logits reproduces the GPU's tokens
-        em, n, fl = gen.verify(p, q, list(d), temp, seed, step, tie_eps=helpers.tie_eps(shape))
+        # (same fp32 logits on both sides: argmax ties are exact, no tie window)
+        em, n, fl = gen.verify(p, q, list(d), temp, seed, step, tie_eps=0.0)
         if fl & helpers.SKIP_FLAGS:
             skipped += 1
         else:

@@ -212,6 +212,24 @@ SPEC_API int spec_accept_rows(const float* p_logits, int64_t p_row_stride,
                      uint64_t seed, uint64_t step_base, int32_t* tokens, int32_t* counts,
                      uint32_t* flags, void* stream);
 
+/* Same as spec_accept_rows, but allocates nothing.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory
+ * when they verify drafts -- e.g. a serving process whose memory pool has
+ * already reserved (nearly) all of HBM, or a latency-critical loop that must
+ * not trigger the device synchronisation an allocation can cause.  Scratch
+ * comes from one fixed 4 MiB array compiled into the library (present on
+ * every GPU that loads it, until the process exits); calls needing more
+ * (about 750 rows at K=5, V=128256) fail with SPEC_E_ARG and a message.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the array: calls that overlap on the GPU race,
+ * so order them (one stream, or events).  Asynchronous on `stream`. */
+SPEC_API int spec_accept_rows_noalloc(const float* p_logits, int64_t p_row_stride,
+                     const float* q_logits, int64_t q_row_stride,
+                     const int32_t* drafts, int rows, int K, int V, float temperature,
+                     uint64_t seed, uint64_t step_base, int32_t* tokens, int32_t* counts,
+                     uint32_t* flags, void* stream);
+
 /* Stateless draft sampler: one token per row from softmax(logits[r] / T)
  * by inverse CDF (argmax at T=0), with the Philox draw (seed; step_base+r,
  * position, stream 0, row 0).  logits: [rows] rows of V fp32 (device,

@@ -96,6 +96,10 @@ SIGNATURES = {
     "spec_accept_rows": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, ctypes.c_int64, _VP, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_uint64,
                                         ctypes.c_uint64, _VP, _VP, _VP, _VP]),
+    "spec_accept_rows_noalloc": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, ctypes.c_int64, _VP,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64,
+                                                _VP, _VP, _VP, _VP]),
     "spec_sample_rows": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64,
                                         ctypes.c_int, _VP, _VP]),
@@ -255,6 +259,26 @@ def accept_rows(p_logits, q_logits, drafts, temperature, seed, step_base=0, stre
     _check(lib().spec_accept_rows(_ptr(p_logits), ps, _ptr(q_logits), qs, _ptr(drafts), R, K, V,
                                   float(temperature), int(seed), int(step_base), _ptr(tokens),
                                   _ptr(counts), _ptr(flags), ctypes.c_void_p(st)))
+    return tokens, counts, flags
+
+
+def accept_rows_noalloc(p_logits, q_logits, drafts, temperature, seed, step_base=0, stream=None):
+    """accept_rows for callers that cannot allocate device memory: the library's
+    scratch comes from a fixed 4 MiB array instead of an allocator (outputs are
+    still torch tensors here; C callers pass their own buffers)."""
+    import torch
+    K = q_logits.shape[-2]
+    V = p_logits.shape[-1]
+    R = p_logits.shape[0]
+    dev = p_logits.device
+    tokens = torch.empty((R, K + 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(R, dtype=torch.int32, device=dev)
+    flags = torch.empty(R, dtype=torch.int32, device=dev)
+    st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _check(lib().spec_accept_rows_noalloc(_ptr(p_logits), (K + 1) * V, _ptr(q_logits), K * V,
+                                          _ptr(drafts), R, K, V, float(temperature), int(seed),
+                                          int(step_base), _ptr(tokens), _ptr(counts), _ptr(flags),
+                                          ctypes.c_void_p(st)))
     return tokens, counts, flags
 
 

@@ -56,6 +56,11 @@ struct ModelState {
 
 }  // namespace
 
+namespace sv {
+// Error message of a failed stateless call, read by spec_last_error(NULL).
+void set_thread_error(const std::string& msg) { g_err = msg; }
+}  // namespace sv
+
 struct spec_ctx {
   ModelState tgt, drf;
   int K = 0;

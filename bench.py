@@ -47,6 +47,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--ar-tokens", type=int, default=128)
+    ap.add_argument("--ncu-mode", action="store_true",
+                    help="profiling run: prefill, --warmup steps, then --steps steps inside "
+                         "cudaProfilerStart/Stop, nothing else")
+    ap.add_argument("--pdl", action="store_true", help="launch with programmatic dependent launch")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: keep the first N layers of both models")
     return ap.parse_args()
 
 
@@ -217,6 +223,11 @@ def main():
             dist.barrier()
 
     tshape, dshape, wl = workload_shapes(args.workload)
+    if args.layers:
+        from dataclasses import replace
+        tshape = replace(tshape, n_layers=min(args.layers, tshape.n_layers))
+        dshape = replace(dshape, n_layers=min(args.layers, dshape.n_layers)) if dshape else None
+        wl += f" (first {args.layers} layers, profiling only)"
     K = args.k
     tw = workloads.make_weights(tshape, 1, device="cuda")
     if dshape is None:
@@ -227,9 +238,11 @@ def main():
     max_ctx = args.prompt + args.new_tokens + 4 * (K + 1) + 64
     stream = torch.cuda.Stream()
 
+    base_flags = sv.SPEC_OPT_PDL if args.pdl else 0
+
     def make(temp, mix, flags=0):
         return sv.SpecDecoder(tshape, tw, dshape, dw, K, max_ctx, temperature=temp, seed=0,
-                              mix_lambda=mix, stream=stream.cuda_stream, flags=flags)
+                              mix_lambda=mix, stream=stream.cuda_stream, flags=flags | base_flags)
 
     def prompt(i):
         return workloads.make_prompt(tshape.vocab, args.prompt, seed=1000 * rank + i)[0].tolist()
@@ -252,6 +265,23 @@ def main():
             ms += e0.elapsed_time(e1)
             toks += emitted
         return ms, toks, done
+
+    if args.ncu_mode:
+        dec = make(args.temperature, args.mix)
+        dec.prefill(prompt(0))
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            dec.step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        for _ in range(args.steps):
+            dec.step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        st = dec.stats()
+        print(json.dumps({"ncu_mode": True, "kernels_per_step": st["kernels_per_step"],
+                          "steps": st["steps"]}), flush=True)
+        return 0
 
     # ---- headline run ----
     dec = make(args.temperature, args.mix)

@@ -69,6 +69,9 @@ extern "C" {
 #define SPEC_OPT_NO_GRAPH      0x1   /* launch the step kernel by kernel (no CUDA graph) */
 #define SPEC_OPT_TIMING        0x2   /* record CUDA events around every weight-streaming
                                         GEMM of the verify pass (implies NO_GRAPH) */
+#define SPEC_OPT_PDL           0x4   /* launch kernels with programmatic dependent launch
+                                        (process-wide; off by default: measured slower on
+                                        the verify pass) */
 
 typedef struct spec_ctx spec_ctx;
 

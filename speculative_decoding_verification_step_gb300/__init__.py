@@ -25,6 +25,7 @@ SPEC_FLAG_RESID_ZERO = 0x1
 SPEC_FLAG_ALL_ACCEPTED = 0x2
 SPEC_OPT_NO_GRAPH = 0x1
 SPEC_OPT_TIMING = 0x2
+SPEC_OPT_PDL = 0x4
 
 _LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
 

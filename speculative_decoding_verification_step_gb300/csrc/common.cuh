@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #define SV_DEV __device__ __forceinline__
 
 namespace sv {
@@ -88,5 +90,37 @@ SV_DEV float warp_sum(float v) {
 }
 
 SV_DEV float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel is launched with programmatic
+// stream serialisation, so it may start while its predecessor in the stream
+// is still running.  pdl_trigger() (called on entry) lets the successor
+// launch; pdl_wait() blocks until the predecessor grid has completed and its
+// memory is visible.  A kernel touches no output of an earlier kernel, and
+// writes nothing, before pdl_wait(); the weight GEMM issues its first
+// read-only weight loads before it, overlapping its ramp-up with the tail of
+// the previous kernel.  Both are no-ops without a programmatic dependency.
+// ---------------------------------------------------------------------------
+SV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SV_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool pdl_enabled();
+void set_pdl_enabled(bool on);
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace sv

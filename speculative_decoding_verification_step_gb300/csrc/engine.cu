@@ -82,6 +82,7 @@ struct spec_ctx {
   float* q = nullptr;
   void* attn = nullptr;
   float* attn_part = nullptr;
+  int* attn_tick = nullptr;
   float* logits_p = nullptr;  // [K+1][V]
   float* logits_q = nullptr;  // [K][V]
   GemmScratch gs{};
@@ -240,12 +241,11 @@ void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const 
     L.note(launch_rope_append(r, s));
     AttnDesc a{};
     a.q = c->q; a.kc = r.kc; a.vc = r.vc; a.pos_base = pos_idx; a.pos_off = pos_off;
-    a.partials = c->attn_part; a.out = c->attn;
+    a.partials = c->attn_part; a.tickets = c->attn_tick; a.out = c->attn;
     a.ntok = ntok; a.hq = hq; a.hkv = hkv; a.hd = hd; a.cap = c->cap;
     a.max_chunks = c->max_chunks; a.dtype = dt;
     a.scale = 1.0f / sqrtf((float)hd);
     L.note(launch_attention(a, s));
-    c->launch_count++;  // combine kernel
     GemmDesc o{};
     o.w[0] = w.wo; o.seg_rows[0] = dm; o.n = dm; o.k = hq * hd; o.x = c->attn; o.ldx = hq * hd;
     o.ntok = ntok; o.epi = kEpiAdd; o.out = c->x; o.ldo = dm;
@@ -258,6 +258,7 @@ void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const 
     GemmDesc dn{};
     dn.w[0] = w.w_down; dn.seg_rows[0] = dm; dn.n = dm; dn.k = d.ffn_dim; dn.x = c->hbuf;
     dn.ldx = d.ffn_dim; dn.ntok = ntok; dn.epi = kEpiAdd; dn.out = c->x; dn.ldo = dm;
+    dn.early_prefetch = 1;   // follows the gate/up GEMM
     gemm(L, dn, dt);
   }
   if (lrows > 0) {
@@ -472,6 +473,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     }                                                                                       \
   } while (0)
   INIT_TRY(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev));
+  set_pdl_enabled((opts->flags & SPEC_OPT_PDL) != 0);
   INIT_TRY(configure_kernels());
   if (opts->cuda_stream) {
     c->stream = (cudaStream_t)opts->cuda_stream;
@@ -502,6 +504,14 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   INIT_TRY(dalloc(c, &c->attn, 4 * maxN * hqd));
   INIT_TRY(dalloc(c, &c->attn_part,
                   sizeof(float) * attn_partial_floats(maxN, (int)hqmax, (int)hdmax, c->max_chunks)));
+  {
+    const int hkvmax = std::max(c->tgt.d.n_kv_heads, c->drf.d.n_kv_heads);
+    const int rt = std::max(attn_max_row_tiles(maxN, c->tgt.d.n_heads, c->tgt.d.n_kv_heads),
+                            attn_max_row_tiles(maxN, c->drf.d.n_heads, c->drf.d.n_kv_heads));
+    const size_t nt = (size_t)hkvmax * rt;
+    INIT_TRY(dalloc(c, &c->attn_tick, sizeof(int) * nt));
+    INIT_TRY(cudaMemset(c->attn_tick, 0, sizeof(int) * nt));
+  }
   INIT_TRY(dalloc(c, &c->logits_p, sizeof(float) * (size_t)(K + 1) * V));
   INIT_TRY(dalloc(c, &c->logits_q, sizeof(float) * (size_t)K * V));
   c->gs.partial_floats = gemm_partial_floats(c->num_sms);

@@ -32,6 +32,11 @@
 namespace sv {
 
 constexpr int kStepK = 64;
+constexpr int kMinStepsPerWarp = 8;
+
+static bool g_pdl = false;
+bool pdl_enabled() { return g_pdl; }
+void set_pdl_enabled(bool on) { g_pdl = on; }
 
 int gemm_grid(int num_sms) { return 2 * num_sms; }
 
@@ -100,10 +105,13 @@ template <int NG, int U>
 __global__ void __launch_bounds__(256, 2)
 gemm_bf16_streamk(const __grid_constant__ GemmDesc g, float* __restrict__ partials,
                   int* __restrict__ tickets, int total_steps, int spt) {
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kGemmWarpsPerCta + (threadIdx.x >> 5);
   const long long total = total_steps;
-  const long long nw = min((long long)gridDim.x * kGemmWarpsPerCta, total);
+  // at least kMinStepsPerWarp k-steps per warp: bounds how many warps share a
+  // tile (and so the length of its reduction) for small matrices
+  const long long nw = max(1LL, min((long long)gridDim.x * kGemmWarpsPerCta, total / kMinStepsPerWarp));
   if (gw >= nw) return;
   const int gi = lane >> 2, ci = lane & 3;
   int s = (int)first_step_of_warp(gw, total, nw);
@@ -111,6 +119,11 @@ gemm_bf16_streamk(const __grid_constant__ GemmDesc g, float* __restrict__ partia
   const bool swiglu = g.epi == kEpiSwiglu;
   const uint16_t* xbase = (const uint16_t*)g.x;
   int slot = 0;
+  bool waited = false;
+  if (!g.early_prefetch) {
+    pdl_wait();
+    waited = true;
+  }
   while (s < s1) {
     const int tile = s / spt;
     const int ks = s - tile * spt;
@@ -135,35 +148,56 @@ gemm_bf16_streamk(const __grid_constant__ GemmDesc g, float* __restrict__ partia
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[ng][e] = 0.f;
 
+    // Rolling prefetch: buffer u holds k-step kk + u; right after its MMAs
+    // consume it, it is refilled with step kk + u + U, so every warp keeps U
+    // steps (U x 2 KB) of weights in flight for its whole range.
+    uint4 wa[U][2], wb[U][2];
+    const uint4 zero4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int off = (ks + u) * kStepK + ci * 16;
+      const bool live = ks + u < ke;
+      wa[u][0] = (live && va) ? ld_stream(pa + off) : zero4;
+      wa[u][1] = (live && va) ? ld_stream(pa + off + 8) : zero4;
+      wb[u][0] = (live && vb) ? ld_stream(pb + off) : zero4;
+      wb[u][1] = (live && vb) ? ld_stream(pb + off + 8) : zero4;
+    }
+    if (!waited) {   // weights are read-only: prefetched before the predecessor finishes
+      pdl_wait();
+      waited = true;
+    }
     for (int kk = ks; kk < ke; kk += U) {
-      uint4 wa[U][2], wb[U][2];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int off = (kk + u) * kStepK + ci * 16;
-        const bool live = kk + u < ke;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        wa[u][0] = (live && va) ? ld_stream(pa + off) : z;
-        wa[u][1] = (live && va) ? ld_stream(pa + off + 8) : z;
-        wb[u][0] = (live && vb) ? ld_stream(pb + off) : z;
-        wb[u][1] = (live && vb) ? ld_stream(pb + off + 8) : z;
-      }
+        const int st = kk + u;
+        if (st < ke) {
+          const int off = st * kStepK + ci * 16;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (kk + u >= ke) break;
-        const int off = (kk + u) * kStepK + ci * 16;
-#pragma unroll
-        for (int ng = 0; ng < NG; ++ng) {
-          const int tok = ng * 8 + gi;
-          uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-          if (tok < g.ntok) {
-            const uint4* xp = (const uint4*)(xbase + (size_t)tok * g.ldx + off);
-            x0 = __ldg(xp);
-            x1 = __ldg(xp + 1);
+          for (int ng = 0; ng < NG; ++ng) {
+            const int tok = ng * 8 + gi;
+            uint4 x0 = zero4, x1 = zero4;
+            if (tok < g.ntok) {
+              const uint4* xp = (const uint4*)(xbase + (size_t)tok * g.ldx + off);
+              x0 = __ldg(xp);
+              x1 = __ldg(xp + 1);
+            }
+            mma_bf16_16816(acc[ng], wa[u][0].x, wb[u][0].x, wa[u][0].y, wb[u][0].y, x0.x, x0.y);
+            mma_bf16_16816(acc[ng], wa[u][0].z, wb[u][0].z, wa[u][0].w, wb[u][0].w, x0.z, x0.w);
+            mma_bf16_16816(acc[ng], wa[u][1].x, wb[u][1].x, wa[u][1].y, wb[u][1].y, x1.x, x1.y);
+            mma_bf16_16816(acc[ng], wa[u][1].z, wb[u][1].z, wa[u][1].w, wb[u][1].w, x1.z, x1.w);
           }
-          mma_bf16_16816(acc[ng], wa[u][0].x, wb[u][0].x, wa[u][0].y, wb[u][0].y, x0.x, x0.y);
-          mma_bf16_16816(acc[ng], wa[u][0].z, wb[u][0].z, wa[u][0].w, wb[u][0].w, x0.z, x0.w);
-          mma_bf16_16816(acc[ng], wa[u][1].x, wb[u][1].x, wa[u][1].y, wb[u][1].y, x1.x, x1.y);
-          mma_bf16_16816(acc[ng], wa[u][1].z, wb[u][1].z, wa[u][1].w, wb[u][1].w, x1.z, x1.w);
+          const int nx = st + U;
+          if (nx < ke) {
+            const int noff = nx * kStepK + ci * 16;
+            if (va) {
+              wa[u][0] = ld_stream(pa + noff);
+              wa[u][1] = ld_stream(pa + noff + 8);
+            }
+            if (vb) {
+              wb[u][0] = ld_stream(pb + noff);
+              wb[u][1] = ld_stream(pb + noff + 8);
+            }
+          }
         }
       }
     }
@@ -190,16 +224,32 @@ gemm_bf16_streamk(const __grid_constant__ GemmDesc g, float* __restrict__ partia
         for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
           for (int e = 0; e < 4; ++e) tot[ng][e] = 0.f;
-        for (int w = wfirst; w <= wlast; ++w) {
-          const int sl = (first_step_of_warp(w, total, nw) / spt == tile) ? 0 : 1;
-          const float* src = partials + (size_t)(w * 2 + sl) * NG * 32 * 4;
+        // partials are loaded kBatch at a time, then added in ascending warp order
+        constexpr int kBatch = NG >= 8 ? 1 : 8 / NG;
+        for (int w0 = wfirst; w0 <= wlast; w0 += kBatch) {
+          float4 v[kBatch][NG];
 #pragma unroll
-          for (int ng = 0; ng < NG; ++ng) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + ((size_t)ng * 32 + lane) * 4));
-            tot[ng][0] += v.x;
-            tot[ng][1] += v.y;
-            tot[ng][2] += v.z;
-            tot[ng][3] += v.w;
+          for (int b = 0; b < kBatch; ++b) {
+            const int w = w0 + b;
+            if (w <= wlast) {
+              const int sl = (first_step_of_warp(w, total, nw) / spt == tile) ? 0 : 1;
+              const float* src = partials + (size_t)(w * 2 + sl) * NG * 32 * 4;
+#pragma unroll
+              for (int ng = 0; ng < NG; ++ng)
+                v[b][ng] = __ldcg(reinterpret_cast<const float4*>(src + ((size_t)ng * 32 + lane) * 4));
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            if (w0 + b <= wlast) {
+#pragma unroll
+              for (int ng = 0; ng < NG; ++ng) {
+                tot[ng][0] += v[b][ng].x;
+                tot[ng][1] += v[b][ng].y;
+                tot[ng][2] += v[b][ng].z;
+                tot[ng][3] += v[b][ng].w;
+              }
+            }
           }
         }
         gemm_epilogue<NG>(g, tile, tot, gi, ci);
@@ -213,6 +263,8 @@ gemm_bf16_streamk(const __grid_constant__ GemmDesc g, float* __restrict__ partia
 
 // fp32 models: one warp per output row (per gate/up pair for SwiGLU).
 __global__ void __launch_bounds__(256) gemv_f32(const __grid_constant__ GemmDesc g) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= g.n) return;
@@ -266,16 +318,9 @@ static cudaError_t launch_sk(const GemmDesc& g, const GemmScratch& s, int num_sm
   const int tiles = gemm_tiles(g);
   const long long total = (long long)tiles * spt;
   if (total <= 0 || total > 0x7fffffffLL) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(gemm_grid(num_sms));
-  cfg.blockDim = dim3(256);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_streamk<NG, U>, g, s.partials, s.tickets, (int)total, spt);
+  (void)pdl;
+  return launch_k(gemm_bf16_streamk<NG, U>, dim3(gemm_grid(num_sms)), dim3(256), 0, st, g,
+                  s.partials, s.tickets, (int)total, spt);
 }
 
 cudaError_t launch_gemm(const GemmDesc& g, int dtype, const GemmScratch& s, int num_sms,
@@ -283,8 +328,7 @@ cudaError_t launch_gemm(const GemmDesc& g, int dtype, const GemmScratch& s, int 
   if (g.ntok <= 0 || g.ntok > kGemmMaxTok) return cudaErrorInvalidValue;
   if (dtype == 0) {
     const int rows = g.n;
-    gemv_f32<<<(rows + 7) / 8, 256, 0, st>>>(g);
-    return cudaGetLastError();
+    return launch_k(gemv_f32, dim3((rows + 7) / 8), dim3(256), 0, st, g);
   }
   if (g.k % kStepK != 0) return cudaErrorInvalidValue;
   if (gemm_tiles(g) > s.max_tiles) return cudaErrorInvalidValue;

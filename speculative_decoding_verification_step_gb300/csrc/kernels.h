@@ -25,6 +25,10 @@ struct GemmDesc {
   int epi;
   void* out;      // see Epi
   int ldo;
+  int early_prefetch;  // 1: issue the first weight loads before waiting for the
+                       // previous kernel (only when that kernel is itself a
+                       // bandwidth-bound GEMM; a latency-bound predecessor would
+                       // be slowed by the extra traffic)
 };
 
 // Cross-warp partial sums and per-tile arrival counters of the bf16 GEMM.
@@ -71,9 +75,11 @@ struct RopeDesc {
 cudaError_t launch_rope_append(const RopeDesc& r, cudaStream_t st);
 
 // Causal GQA attention of ntok new query rows over the KV cache, split by
-// fixed 64-key chunks of absolute position, then folded chunk by chunk in
-// order (the result of a row depends only on its own position).
+// fixed 64-key chunks of absolute position; the last CTA of each (KV head,
+// row tile) combines the chunk partials of its rows (the result of a row
+// depends only on its own position and partials).
 constexpr int kAttnChunk = 64;
+constexpr int kAttnRowsPerCta = 32;
 struct AttnDesc {
   const float* q;          // [ntok][hq][hd] fp32 (rotated)
   const void* kc;          // [hkv][cap][hd]
@@ -81,11 +87,13 @@ struct AttnDesc {
   const int32_t* pos_base; // query t sits at *pos_base + pos_off + t
   int pos_off;
   float* partials;         // [ntok*hq][max_chunks][hd+2]
+  int* tickets;            // [hkv][row tiles], zero before and after
   void* out;               // [ntok][hq*hd] model dtype
   int ntok, hq, hkv, hd, cap, max_chunks, dtype;
   float scale;
 };
 size_t attn_partial_floats(int max_tok, int hq, int hd, int max_chunks);
+int attn_max_row_tiles(int max_tok, int hq, int hkv);
 cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st);
 // One-time kernel attributes (dynamic shared memory); call before any capture.
 cudaError_t configure_kernels();

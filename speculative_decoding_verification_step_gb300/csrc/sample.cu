@@ -8,18 +8,21 @@
 // the target's argmax, emit the target's argmax at the first mismatch, or the
 // bonus argmax.
 //
-// Both kernels split the vocabulary into 2048-wide chunks, one CTA per
-// (chunk, row): each CTA reduces its chunk to (max, sum exp) or (max,
-// argmax) partials.  The last CTA to finish a row (one atomic ticket per
-// row, no waiting) folds the partials in chunk order, takes the decisions,
-// and runs the inverse-CDF draw as a block-wide two-pass scan:
-//   pass 1: each warp sums a contiguous segment (32 lanes at a time, fp32
-//           shuffle tree per group of 32, fp64 running sum);
-//   pass 2: the warp whose segment holds the target u * Z rescans it with
-//           the same arithmetic and an in-warp prefix scan.
-// Inverse CDF: the smallest index whose running sum exceeds u * Z, in token
-// id order.  Random numbers come from Philox-4x32-10 keyed by (seed;
-// step, position, stream, row), identical to the host restatement.
+// Work split: the vocabulary is cut into 2048-token chunks and every (chunk,
+// logit row) pair is one CTA, which reduces its chunk to (max z, sum
+// exp(z - max)) -- or (max, argmax) when greedy -- with z = logit / T.  The
+// last CTA to finish a verify row (one atomic ticket per row; nobody waits)
+// folds the partials in chunk order in fp64 and takes every decision:
+//   * softmax draws (draft token, bonus): chunk masses come straight from the
+//     partials, s_c * exp(m_c - M); the chunk holding the target u * Z is
+//     found by a running fp64 sum, and only that chunk is rescanned (block
+//     prefix scan, token-id order);
+//   * the residual draw: one block-wide pass computes the (p - q)+ mass of
+//     every chunk, then the same chunk search and rescan.
+// Inverse CDF: the smallest token whose running sum exceeds u * Z; if
+// rounding leaves no such token in the chosen chunk, the last token of the
+// chunk with positive weight.  Random numbers: Philox-4x32-10 keyed by
+// (seed; step, position, stream, row), identical to the host restatement.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,9 +31,11 @@ namespace sv {
 constexpr int kSampThreads = 256;
 constexpr int kSampWarps = kSampThreads / 32;
 constexpr int kMaxK = 16;
+constexpr int kMaxChunks = 128;          // vocabularies up to 262144 tokens
+constexpr int kPerThread = kVocabChunk / kSampThreads;   // 8 contiguous tokens per thread in a rescan
 
-static inline int vocab_chunks(int V) { return (V + kVocabChunk - 1) / kVocabChunk; }
-size_t sample_partial_floats(int rows, int V) { return (size_t)rows * vocab_chunks(V) * 2; }
+__host__ __device__ inline int vocab_chunks(int V) { return (V + kVocabChunk - 1) / kVocabChunk; }
+size_t sample_partial_floats(int rows, int V) { return (size_t)rows * vocab_chunks(V) * 3; }
 size_t accept_partial_floats(int rows, int K, int V) {
   return (size_t)rows * vocab_chunks(V) * (2 * K + 1) * 2;
 }
@@ -47,7 +52,7 @@ SV_DEV void am_combine(float& v, int& i, float v2, int i2) {
   if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
 }
 
-// Block reduce of (m, s) over kSampThreads threads; result valid in thread 0.
+// Block reductions; the result is valid in thread 0.
 SV_DEV void block_ms(float& m, float& s, float* sm_m, float* sm_s) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -55,7 +60,6 @@ SV_DEV void block_ms(float& m, float& s, float* sm_m, float* sm_s) {
     ms_combine(m, s, m2, s2);
   }
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  __syncthreads();
   if (lane == 0) { sm_m[w] = m; sm_s[w] = s; }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -71,7 +75,6 @@ SV_DEV void block_am(float& v, int& i, float* sm_v, int* sm_i) {
     am_combine(v, i, v2, i2);
   }
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  __syncthreads();
   if (lane == 0) { sm_v[w] = v; sm_i[w] = i; }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -80,91 +83,51 @@ SV_DEV void block_am(float& v, int& i, float* sm_v, int* sm_i) {
   }
 }
 
-// Block-wide inverse CDF over weights wfn(v), v in [0, V).  All threads call
-// it; returns the index in every thread.  *z_out receives the total.
-struct CdfShared {
-  double tot[kSampWarps];
-  double prefix, target, z;
-  int wsel, result;
-};
-
-template <typename WFn>
-SV_DEV int block_inverse_cdf(const WFn& wfn, int V, float u, CdfShared& sh, double* z_out) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int seg = (V + kSampWarps - 1) / kSampWarps;
-  seg = (seg + 31) & ~31;
-  const int beg = min(V, w * seg), end = min(V, beg + seg);
-  double R = 0.0;
-  for (int b = beg; b < end; b += 32) {
-    const int v = b + lane;
-    const float x = v < end ? wfn(v) : 0.f;
-    R += (double)warp_sum(x);
-  }
-  __syncthreads();
-  if (lane == 0) sh.tot[w] = R;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double z = 0.0;
-    for (int k = 0; k < kSampWarps; ++k) z += sh.tot[k];
-    const double target = (double)u * z;
-    double pre = 0.0;
-    int sel = -1;
-    double sel_pre = 0.0;
-    for (int k = 0; k < kSampWarps; ++k) {
-      if (sel < 0 && pre + sh.tot[k] > target) { sel = k; sel_pre = pre; }
-      pre += sh.tot[k];
-    }
-    if (sel < 0) {  // rounding left the target at the end: last warp with mass
-      pre = 0.0;
-      for (int k = 0; k < kSampWarps; ++k) {
-        if (sh.tot[k] > 0.0) { sel = k; sel_pre = pre; }
-        pre += sh.tot[k];
-      }
-      if (sel < 0) sel = 0;
-    }
-    sh.wsel = sel; sh.prefix = sel_pre; sh.target = target; sh.z = z;
-    sh.result = -1;
-  }
-  __syncthreads();
-  if (w == sh.wsel) {
-    const double target = sh.target, pre = sh.prefix;
-    double Rl = 0.0;
-    int last_pos = -1;
-    int found = -1;
-    for (int b = beg; b < end; b += 32) {
-      const int v = b + lane;
-      const float x = v < end ? wfn(v) : 0.f;
-      const float S = warp_sum(x);
-      const unsigned pos_mask = __ballot_sync(0xffffffffu, x > 0.f);
-      if (pos_mask) last_pos = b + 31 - __clz(pos_mask);
-      if (pre + (Rl + (double)S) > target) {
-        float scan = x;
+// Statistics of one chunk [v0, v1) of one logit row (8 independent loads per
+// thread are issued before any arithmetic).
+SV_DEV void chunk_softmax_stats(const float* src, int v0, int v1, float invT, float* sm_a,
+                                float* sm_b, float* m_out, float* s_out) {
+  float x[kPerThread];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, scan, o);
-          if (lane >= o) scan += y;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, pre + Rl + (double)scan > target && x > 0.f);
-        found = hit ? b + __ffs(hit) - 1 : last_pos;
-        break;
-      }
-      Rl += (double)S;
-    }
-    if (found < 0) found = last_pos;
-    if (lane == 0) sh.result = found < 0 ? 0 : found;
+  for (int j = 0; j < kPerThread; ++j) {
+    const int v = v0 + threadIdx.x + j * kSampThreads;
+    x[j] = v < v1 ? src[v] * invT : neg_inf();
   }
-  __syncthreads();
-  if (z_out) *z_out = sh.z;
-  return sh.result;
+  float m = neg_inf();
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) m = fmaxf(m, x[j]);
+  float s = 0.f;
+  if (m != neg_inf()) {
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) s += (x[j] == neg_inf()) ? 0.f : expf(x[j] - m);
+  }
+  block_ms(m, s, sm_a, sm_b);
+  if (threadIdx.x == 0) { *m_out = m; *s_out = s; }
 }
 
-// Ticket: returns true in all threads of the CTA that arrives last for `row`.
-SV_DEV bool last_arrival(int* tickets, int row, int nchunks, int* sm_flag) {
+SV_DEV void chunk_argmax(const float* src, int v0, int v1, float* sm_a, int* sm_i, float* v_out,
+                         int* i_out) {
+  float best = neg_inf();
+  int bi = 0x7fffffff;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int v = v0 + threadIdx.x + j * kSampThreads;
+    if (v < v1) {
+      const float x = src[v];
+      if (x > best || (x == best && v < bi)) { best = x; bi = v; }
+    }
+  }
+  block_am(best, bi, sm_a, sm_i);
+  if (threadIdx.x == 0) { *v_out = best; *i_out = bi; }
+}
+
+// Ticket: true in every thread of the CTA that arrives last for `row`.
+SV_DEV bool last_arrival(int* tickets, int row, int arrivals, int* sm_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     const int old = atomicAdd(&tickets[row], 1);
-    *sm_flag = (old == nchunks - 1);
+    *sm_flag = (old == arrivals - 1);
   }
   __syncthreads();
   const bool last = *sm_flag != 0;
@@ -172,13 +135,117 @@ SV_DEV bool last_arrival(int* tickets, int row, int nchunks, int* sm_flag) {
   return last;
 }
 
+struct DrawShared {
+  double mass[kMaxChunks];
+  double warp_sum[kSampWarps];
+  double prefix, target;
+  int chunk, result;
+};
+
+// Given per-chunk masses in sh.mass[0..nch), find the chunk holding u * Z
+// (thread 0, fp64, chunk order).  Returns Z in every thread.
+SV_DEV double pick_chunk(DrawShared& sh, int nch, float u) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double z = 0.0;
+    for (int c = 0; c < nch; ++c) z += sh.mass[c];
+    const double target = (double)u * z;
+    double pre = 0.0, sel_pre = 0.0;
+    int sel = -1;
+    for (int c = 0; c < nch; ++c) {
+      if (sel < 0 && pre + sh.mass[c] > target) { sel = c; sel_pre = pre; }
+      pre += sh.mass[c];
+    }
+    if (sel < 0) {   // rounding left the target at the end: last chunk with mass
+      pre = 0.0;
+      for (int c = 0; c < nch; ++c) {
+        if (sh.mass[c] > 0.0) { sel = c; sel_pre = pre; }
+        pre += sh.mass[c];
+      }
+      if (sel < 0) sel = 0;
+    }
+    sh.chunk = sel;
+    sh.prefix = sel_pre;
+    sh.target = target;
+    sh.warp_sum[0] = z;
+  }
+  __syncthreads();
+  return sh.warp_sum[0];
+}
+
+// Rescan chunk sh.chunk: thread t owns tokens [v0 + 8t, v0 + 8t + 8); block
+// exclusive scan of the per-thread sums (fp64), then the owning thread walks
+// its tokens.  Returns the token in every thread.
+template <typename WFn>
+SV_DEV int rescan_chunk(DrawShared& sh, const WFn& wfn, int V) {
+  const int v0 = sh.chunk * kVocabChunk;
+  const int t0 = v0 + threadIdx.x * kPerThread;
+  float w[kPerThread];
+  float tsum = 0.f;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    w[j] = (t0 + j < V) ? wfn(t0 + j) : 0.f;
+    tsum += w[j];
+  }
+  // inclusive scan over threads: warp shuffle scan, then warp offsets
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  double inc = (double)tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  __syncthreads();
+  if (lane == 31) sh.warp_sum[wid] = inc;
+  __syncthreads();
+  double off = sh.prefix;
+  for (int k = 0; k < wid; ++k) off += sh.warp_sum[k];
+  const double excl = off + inc - (double)tsum;
+  const double target = sh.target;
+  // the first (lowest) thread whose range crosses the target walks its tokens
+  const bool crosses = excl + (double)tsum > target && tsum > 0.f;
+  __shared__ int first_thread;
+  if (threadIdx.x == 0) first_thread = 0x7fffffff;
+  __syncthreads();
+  if (crosses) atomicMin(&first_thread, (int)threadIdx.x);
+  __syncthreads();
+  if ((int)threadIdx.x == first_thread) {
+    double run = excl;
+    int pick = -1, lastpos = -1;
+    for (int j = 0; j < kPerThread; ++j) {
+      if (w[j] > 0.f) lastpos = t0 + j;
+      run += (double)w[j];
+      if (pick < 0 && w[j] > 0.f && run > target) pick = t0 + j;
+    }
+    sh.result = pick >= 0 ? pick : lastpos;
+  }
+  __syncthreads();
+  if (first_thread == 0x7fffffff) {
+    // no thread crossed (rounding): last token of the chunk with positive weight
+    __shared__ int lastpos_all;
+    if (threadIdx.x == 0) lastpos_all = -1;
+    __syncthreads();
+    int lp = -1;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j)
+      if (w[j] > 0.f) lp = t0 + j;
+    if (lp >= 0) atomicMax(&lastpos_all, lp);
+    __syncthreads();
+    if (threadIdx.x == 0) sh.result = lastpos_all >= 0 ? lastpos_all : v0;
+    __syncthreads();
+  }
+  return sh.result;
+}
+
 // ---------------------------------------------------------------- sampler
 __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_constant__ SampleDesc s) {
   __shared__ float sm_a[kSampWarps];
-  __shared__ int sm_i[kSampWarps];
   __shared__ float sm_b[kSampWarps];
+  __shared__ int sm_i[kSampWarps];
   __shared__ int sm_flag;
-  __shared__ CdfShared cdf;
+  __shared__ DrawShared sh;
+  pdl_trigger();
+  pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
   const int nch = gridDim.x;
   const float* row = s.logits + (size_t)r * s.ld;
@@ -186,45 +253,68 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
   float* mixed = s.mix_src ? s.mixed_out + (size_t)r * s.mixed_ld : nullptr;
   const int v0 = c * kVocabChunk, v1 = min(s.V, v0 + kVocabChunk);
   const bool greedy = s.temperature == 0.f;
+  const float invT = greedy ? 1.f : 1.0f / s.temperature;
 
-  float best = neg_inf();
-  int bi = 0x7fffffff;
-  for (int v = v0 + threadIdx.x; v < v1; v += kSampThreads) {
-    float x = row[v];
-    if (mix) {
-      x = (1.f - s.lambda) * x + s.lambda * mix[v];
-      mixed[v] = x;
+  const float* src = row;
+  if (mix) {
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const int v = v0 + threadIdx.x + j * kSampThreads;
+      if (v < v1) mixed[v] = (1.f - s.lambda) * row[v] + s.lambda * mix[v];
     }
-    if (x > best || (x == best && v < bi)) { best = x; bi = v; }
+    __syncthreads();
+    src = mixed;   // this CTA's own writes: visible to its threads after the barrier
   }
-  block_am(best, bi, sm_a, sm_i);
-  float* part = s.partials + ((size_t)r * nch + c) * 2;
-  if (threadIdx.x == 0) { part[0] = best; part[1] = __int_as_float(bi); }
+  float* part = s.partials + ((size_t)r * nch + c) * 3;
+  if (greedy) {
+    float bv;
+    int bi;
+    chunk_argmax(src, v0, v1, sm_a, sm_i, &bv, &bi);
+    if (threadIdx.x == 0) { part[0] = bv; part[1] = __int_as_float(bi); }
+  } else {
+    float m, sum;
+    chunk_softmax_stats(src, v0, v1, invT, sm_a, sm_b, &m, &sum);
+    if (threadIdx.x == 0) { part[0] = m; part[2] = sum; }
+  }
   if (!last_arrival(s.tickets, r, nch, &sm_flag)) return;
 
-  // ---- last CTA of this row ----
-  __shared__ int tok_sh;
-  __shared__ float gmax_sh;
-  if (threadIdx.x == 0) {
-    float bv = neg_inf();
-    int bidx = 0x7fffffff;
-    for (int k = 0; k < nch; ++k) {
-      const float* p = s.partials + ((size_t)r * nch + k) * 2;
-      am_combine(bv, bidx, __ldcg(p), __float_as_int(__ldcg(p + 1)));
-    }
-    tok_sh = bidx;
-    gmax_sh = bv;
+  // ---- last CTA of this row: partials loaded in parallel into shared memory ----
+  const float* P = s.partials + (size_t)r * nch * 3;
+  __shared__ float pm[kMaxChunks], pz[kMaxChunks];
+  __shared__ int pi[kMaxChunks];
+  for (int k = threadIdx.x; k < nch; k += kSampThreads) {
+    pm[k] = __ldcg(P + 3 * k);
+    pi[k] = __float_as_int(__ldcg(P + 3 * k + 1));
+    pz[k] = __ldcg(P + 3 * k + 2);
   }
   __syncthreads();
-  int tok = tok_sh;
-  const uint32_t step = (uint32_t)((s.step_dev ? (uint64_t)*s.step_dev : 0) + s.step_base + r);
-  if (!greedy) {
-    const float invT = 1.0f / s.temperature;
-    const float mz = gmax_sh * invT;
-    const float* src = mix ? mixed : row;
-    auto wfn = [&](int v) { return expf(__ldcg(src + v) * invT - mz); };
+  int tok;
+  if (greedy) {
+    if (threadIdx.x == 0) {
+      float bv = neg_inf();
+      int bi = 0x7fffffff;
+      for (int k = 0; k < nch; ++k) am_combine(bv, bi, pm[k], pi[k]);
+      sh.result = bi;
+    }
+    __syncthreads();
+    tok = sh.result;
+  } else {
+    __shared__ float gmax;
+    if (threadIdx.x == 0) {
+      float M = neg_inf();
+      for (int k = 0; k < nch; ++k) M = fmaxf(M, pm[k]);
+      gmax = M;
+    }
+    __syncthreads();
+    const float M = gmax;
+    for (int k = threadIdx.x; k < nch; k += kSampThreads)
+      sh.mass[k] = (pm[k] == neg_inf()) ? 0.0 : (double)(pz[k] * expf(pm[k] - M));
+    const uint32_t step = (uint32_t)((s.step_dev ? (uint64_t)*s.step_dev : 0) + s.step_base + r);
     const float u = philox_uniform(s.seed, step, s.position, s.stream, 0);
-    tok = block_inverse_cdf(wfn, s.V, u, cdf, nullptr);
+    pick_chunk(sh, nch, u);
+    const float* srcall = mix ? mixed : row;
+    auto wfn = [&](int v) { return expf(__ldcg(srcall + v) * invT - M); };
+    tok = rescan_chunk(sh, wfn, s.V);
   }
   if (threadIdx.x == 0) {
     s.out_token[(s.out_idx ? *s.out_idx : 0) + s.out_off + r] = tok;
@@ -239,9 +329,8 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
 }
 
 cudaError_t launch_sample(const SampleDesc& s, cudaStream_t st) {
-  if (s.rows <= 0 || s.V <= 0) return cudaErrorInvalidValue;
-  sample_kernel<<<dim3(vocab_chunks(s.V), s.rows), kSampThreads, 0, st>>>(s);
-  return cudaGetLastError();
+  if (s.rows <= 0 || s.V <= 0 || vocab_chunks(s.V) > kMaxChunks) return cudaErrorInvalidValue;
+  return launch_k(sample_kernel, dim3(vocab_chunks(s.V), s.rows), dim3(kSampThreads), 0, st, s);
 }
 
 // ---------------------------------------------------------------- acceptance
@@ -250,93 +339,91 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
   __shared__ float sm_b[kSampWarps];
   __shared__ int sm_i[kSampWarps];
   __shared__ int sm_flag;
-  __shared__ CdfShared cdf;
+  __shared__ DrawShared sh;
   __shared__ double rowM[2 * kMaxK + 1], rowZ[2 * kMaxK + 1];
   __shared__ int argm[kMaxK + 1];
-  __shared__ int dec_n, dec_kind, dec_tok;   // accepted count; 0 = residual, 1 = bonus
+  __shared__ int dec_n, dec_kind, dec_tok;   // accepted count; kind 0 residual, 1 bonus, 2 greedy
+  pdl_trigger();
+  pdl_wait();
 
-  const int c = blockIdx.x, r = blockIdx.y;
-  const int nch = gridDim.x;
+  const int r = blockIdx.y;
   const int K = a.K, V = a.V;
+  const int nch = vocab_chunks(V);
   const int nrow = 2 * K + 1;                // p_1..p_{K+1}, q_1..q_K
   const bool greedy = a.temperature == 0.f;
+  const int nstat = greedy ? K + 1 : nrow;
   const float invT = greedy ? 1.f : 1.0f / a.temperature;
   const float* P = a.p + (size_t)r * a.p_ld;
   const float* Q = a.q + (size_t)r * a.q_ld;
+  const int j = blockIdx.x / nch, c = blockIdx.x % nch;   // logit row, chunk
   const int v0 = c * kVocabChunk, v1 = min(V, v0 + kVocabChunk);
-  float* part = a.partials + ((size_t)r * nch + c) * nrow * 2;
+  float* part = a.partials + (((size_t)r * nrow + j) * nch + c) * 2;
 
-  // ---- phase A: chunk partials of every row ----
-  const int nstat = greedy ? K + 1 : nrow;
-  for (int j = 0; j < nstat; ++j) {
+  // ---- phase A: one (logit row, chunk) per CTA ----
+  {
     const float* src = j <= K ? P + (size_t)j * V : Q + (size_t)(j - K - 1) * V;
     if (greedy) {
-      float best = neg_inf();
-      int bi = 0x7fffffff;
-      for (int v = v0 + threadIdx.x; v < v1; v += kSampThreads) {
-        const float x = src[v];
-        if (x > best || (x == best && v < bi)) { best = x; bi = v; }
-      }
-      block_am(best, bi, sm_a, sm_i);
-      if (threadIdx.x == 0) { part[j * 2] = best; part[j * 2 + 1] = __int_as_float(bi); }
+      float bv;
+      int bi;
+      chunk_argmax(src, v0, v1, sm_a, sm_i, &bv, &bi);
+      if (threadIdx.x == 0) { part[0] = bv; part[1] = __int_as_float(bi); }
     } else {
-      float m = neg_inf(), sum = 0.f;
-      for (int v = v0 + threadIdx.x; v < v1; v += kSampThreads) {
-        const float z = src[v] * invT;
-        if (z > m) { sum = sum * expf(m - z) + 1.f; m = z; }
-        else sum += expf(z - m);
-      }
-      block_ms(m, sum, sm_a, sm_b);
-      if (threadIdx.x == 0) { part[j * 2] = m; part[j * 2 + 1] = sum; }
+      float m, sum;
+      chunk_softmax_stats(src, v0, v1, invT, sm_a, sm_b, &m, &sum);
+      if (threadIdx.x == 0) { part[0] = m; part[1] = sum; }
     }
   }
-  if (!last_arrival(a.tickets, r, nch, &sm_flag)) return;
+  if (!last_arrival(a.tickets, r, nstat * nch, &sm_flag)) return;
 
-  // ---- phase B: fold partials in chunk order, ratio tests ----
+  // ---- phase B: fold partials in chunk order, decisions ----
   const uint32_t step = (uint32_t)((a.step_dev ? (uint64_t)*a.step_dev : 0) + a.step_base + r);
   const int32_t* D = a.drafts + (a.drafts_idx ? *a.drafts_idx : 0) + a.drafts_off + (size_t)r * K;
+  const float* PR = a.partials + (size_t)r * nrow * nch * 2;
+  // all partials of this verify row into shared memory, loaded in parallel
+  __shared__ float pa_[(2 * kMaxK + 1) * kMaxChunks], pb_[(2 * kMaxK + 1) * kMaxChunks];
+  for (int e = threadIdx.x; e < nstat * nch; e += kSampThreads) {
+    pa_[e] = __ldcg(PR + 2 * e);
+    pb_[e] = __ldcg(PR + 2 * e + 1);
+  }
+  __syncthreads();
   if (threadIdx.x < nstat) {
-    const int j = threadIdx.x;
+    const int jj = threadIdx.x;
+    const float* ma = pa_ + jj * nch;
+    const float* mb = pb_ + jj * nch;
     if (greedy) {
       float bv = neg_inf();
       int bi = 0x7fffffff;
-      for (int k = 0; k < nch; ++k) {
-        const float* p = a.partials + (((size_t)r * nch + k) * nrow + j) * 2;
-        am_combine(bv, bi, __ldcg(p), __float_as_int(__ldcg(p + 1)));
-      }
-      argm[j] = bi;
+      for (int k = 0; k < nch; ++k) am_combine(bv, bi, ma[k], __float_as_int(mb[k]));
+      argm[jj] = bi;
     } else {
       float M = neg_inf();
-      for (int k = 0; k < nch; ++k)
-        M = fmaxf(M, __ldcg(a.partials + (((size_t)r * nch + k) * nrow + j) * 2));
+      for (int k = 0; k < nch; ++k) M = fmaxf(M, ma[k]);
       double Z = 0.0;
-      for (int k = 0; k < nch; ++k) {
-        const float* p = a.partials + (((size_t)r * nch + k) * nrow + j) * 2;
-        const float m = __ldcg(p), sm = __ldcg(p + 1);
-        if (m != neg_inf()) Z += (double)sm * exp((double)m - (double)M);
-      }
-      rowM[j] = (double)M;
-      rowZ[j] = Z;
+      for (int k = 0; k < nch; ++k)
+        if (ma[k] != neg_inf()) Z += (double)(mb[k] * expf(ma[k] - M));
+      rowM[jj] = (double)M;
+      rowZ[jj] = Z;
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int n = K;
-    int kind = 1;
-    int tok = -1;
+    int n = K, kind = 1, tok = -1;
     if (greedy) {
+      kind = 2;
       for (int i = 0; i < K; ++i) {
-        if (D[i] != argm[i]) { n = i; kind = 2; tok = argm[i]; break; }
+        if (D[i] != argm[i]) { n = i; tok = argm[i]; break; }
       }
-      if (kind == 1) tok = argm[K];
+      if (n == K) tok = argm[K];
     } else {
       for (int i = 0; i < K; ++i) {
         const int d = D[i];
-        const double lp = (double)(P[(size_t)i * V + d] * invT) - rowM[i] - log(rowZ[i]);
-        const double lq = (double)(Q[(size_t)i * V + d] * invT) - rowM[K + 1 + i] - log(rowZ[K + 1 + i]);
-        const double ratio = exp(lp - lq);
+        // p_i(d) / q_i(d) = exp((zp - Mp) - (zq - Mq)) * Zq / Zp, in fp32 with
+        // the normaliser ratio taken in fp64
+        const float lp = P[(size_t)i * V + d] * invT - (float)rowM[i];
+        const float lq = Q[(size_t)i * V + d] * invT - (float)rowM[K + 1 + i];
+        const float ratio = expf(lp - lq) * (float)(rowZ[K + 1 + i] / rowZ[i]);
         const float rr = philox_uniform(a.seed, step, (uint32_t)(i + 1), kStreamAccept, 0);
-        if (!((double)rr < fmin(1.0, ratio))) { n = i; kind = 0; break; }
+        if (!(rr < fminf(1.0f, ratio))) { n = i; kind = 0; break; }
       }
     }
     dec_n = n;
@@ -349,30 +436,59 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
   uint32_t flags = (n == K) ? 0x2u : 0u;
 
   // ---- phase C: residual or bonus draw ----
-  if (!greedy) {
-    if (kind == 0) {
-      const float* pr = P + (size_t)n * V;
-      const float* qr = Q + (size_t)n * V;
-      const float mp = (float)rowM[n], mq = (float)rowM[K + 1 + n];
-      const float izp = (float)(1.0 / rowZ[n]), izq = (float)(1.0 / rowZ[K + 1 + n]);
-      auto wres = [&](int v) {
-        return fmaxf(expf(pr[v] * invT - mp) * izp - expf(qr[v] * invT - mq) * izq, 0.f);
-      };
-      const float u = philox_uniform(a.seed, step, (uint32_t)(n + 1), kStreamResidual, 0);
-      double z = 0.0;
-      tok = block_inverse_cdf(wres, V, u, cdf, &z);
-      if (!(z > 0.0)) {
-        flags |= 0x1u;
-        auto wp = [&](int v) { return expf(pr[v] * invT - mp); };
-        tok = block_inverse_cdf(wp, V, u, cdf, nullptr);
+  if (kind == 0) {
+    const float* pr = P + (size_t)n * V;
+    const float* qr = Q + (size_t)n * V;
+    const float mp = (float)rowM[n], mq = (float)rowM[K + 1 + n];
+    const float izp = (float)(1.0 / rowZ[n]), izq = (float)(1.0 / rowZ[K + 1 + n]);
+    auto wres = [&](int v) {
+      return fmaxf(expf(pr[v] * invT - mp) * izp - expf(qr[v] * invT - mq) * izq, 0.f);
+    };
+    // residual mass of every chunk: warp w takes chunks w, w + 8, ...
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int cc = wid; cc < nch; cc += kSampWarps) {
+      const int b0 = cc * kVocabChunk, b1 = min(V, b0 + kVocabChunk);
+      float acc = 0.f;
+      for (int base = b0; base < b1; base += 32 * 16) {
+        float pv[16], qv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int v = base + lane + 32 * u;
+          pv[u] = v < b1 ? pr[v] : neg_inf();
+          qv[u] = v < b1 ? qr[v] : neg_inf();
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          acc += fmaxf(expf(pv[u] * invT - mp) * izp - expf(qv[u] * invT - mq) * izq, 0.f);
       }
-    } else {
-      const float* pr = P + (size_t)K * V;
-      const float mp = (float)rowM[K];
-      auto wp = [&](int v) { return expf(pr[v] * invT - mp); };
-      const float u = philox_uniform(a.seed, step, (uint32_t)(K + 1), kStreamBonus, 0);
-      tok = block_inverse_cdf(wp, V, u, cdf, nullptr);
+      acc = warp_sum(acc);
+      if (lane == 0) sh.mass[cc] = (double)acc;
     }
+    const float u = philox_uniform(a.seed, step, (uint32_t)(n + 1), kStreamResidual, 0);
+    const double z = pick_chunk(sh, nch, u);
+    if (z > 0.0) {
+      tok = rescan_chunk(sh, wres, V);
+    } else {   // zero residual mass (rounding): draw from p_i
+      flags |= 0x1u;
+      for (int k = threadIdx.x; k < nch; k += kSampThreads) {
+        const float m = pa_[n * nch + k], sm = pb_[n * nch + k];
+        sh.mass[k] = (m == neg_inf()) ? 0.0 : (double)(sm * expf(m - (float)rowM[n]));
+      }
+      pick_chunk(sh, nch, u);
+      auto wp = [&](int v) { return expf(pr[v] * invT - mp); };
+      tok = rescan_chunk(sh, wp, V);
+    }
+  } else if (kind == 1) {
+    const float* pr = P + (size_t)K * V;
+    const float mp = (float)rowM[K];
+    for (int k = threadIdx.x; k < nch; k += kSampThreads) {
+      const float m = pa_[K * nch + k], sm = pb_[K * nch + k];
+      sh.mass[k] = (m == neg_inf()) ? 0.0 : (double)(sm * expf(m - (float)rowM[K]));
+    }
+    const float u = philox_uniform(a.seed, step, (uint32_t)(K + 1), kStreamBonus, 0);
+    pick_chunk(sh, nch, u);
+    auto wp = [&](int v) { return expf(pr[v] * invT - mp); };
+    tok = rescan_chunk(sh, wp, V);
   }
 
   if (threadIdx.x == 0) {
@@ -396,8 +512,10 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
 
 cudaError_t launch_accept(const AcceptDesc& a, cudaStream_t st) {
   if (a.rows <= 0 || a.K < 1 || a.K > kMaxK || a.V <= 0) return cudaErrorInvalidValue;
-  accept_kernel<<<dim3(vocab_chunks(a.V), a.rows), kSampThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  const int nch = vocab_chunks(a.V);
+  if (nch > kMaxChunks) return cudaErrorInvalidValue;
+  const int nstat = a.temperature == 0.f ? a.K + 1 : 2 * a.K + 1;
+  return launch_k(accept_kernel, dim3(nstat * nch, a.rows), dim3(kSampThreads), 0, st, a);
 }
 
 }  // namespace sv

@@ -51,6 +51,11 @@ def parse():
                     help="profiling run: prefill, --warmup steps, then --steps steps inside "
                          "cudaProfilerStart/Stop, nothing else")
     ap.add_argument("--pdl", action="store_true", help="launch with programmatic dependent launch")
+    ap.add_argument("--phase-times", action="store_true",
+                    help="profiling: per-phase breakdown of the persistent verify, plain-decoding "
+                         "and draft passes (globaltimer stamps)")
+    ap.add_argument("--no-persist", action="store_true",
+                    help="one kernel per phase instead of the persistent forward kernel")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of both models")
     return ap.parse_args()
@@ -200,6 +205,42 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- ours
+def phase_summary(ph):
+    """Fold per-phase stamps of one persistent pass: time per phase kind from
+    one release to the next, the spread of CTA arrivals (imbalance) and the
+    barrier latency (last arrival to release), and GB/s per GEMM shape."""
+    kinds = {0: "embed", 1: "gemm", 2: "attn"}
+    out = {"phases": len(ph), "total_us": 0.0, "by_kind": {}, "gemm_shapes": {}}
+    prev = 0
+    for i, p in enumerate(ph):
+        end = p["release_ns"] if p["release_ns"] >= 0 else p["arrive_max_ns"]
+        dur = (end - prev) / 1e3
+        spread = (p["arrive_max_ns"] - p["arrive_min_ns"]) / 1e3
+        bar = (p["release_ns"] - p["arrive_max_ns"]) / 1e3 if p["release_ns"] >= 0 else 0.0
+        k = kinds.get(p["kind"], str(p["kind"]))
+        agg = out["by_kind"].setdefault(k, {"count": 0, "us": 0.0, "spread_us": 0.0, "barrier_us": 0.0})
+        agg["count"] += 1
+        agg["us"] += dur
+        agg["spread_us"] += spread
+        agg["barrier_us"] += bar
+        if p["kind"] == 1:
+            key = f'{p["n"]}x{p["k"]}'
+            g = out["gemm_shapes"].setdefault(key, {"count": 0, "us": 0.0})
+            g["count"] += 1
+            g["us"] += dur
+        prev = end
+    out["total_us"] = prev / 1e3
+    for key, g in out["gemm_shapes"].items():
+        n, k = (int(v) for v in key.split("x"))
+        g["gbs"] = round(g["count"] * n * k * 2 / (g["us"] * 1e3), 1)
+        g["us"] = round(g["us"], 1)
+    for agg in out["by_kind"].values():
+        for f in ("us", "spread_us", "barrier_us"):
+            agg[f] = round(agg[f], 1)
+    out["total_us"] = round(out["total_us"], 1)
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -238,7 +279,7 @@ def main():
     max_ctx = args.prompt + args.new_tokens + 4 * (K + 1) + 64
     stream = torch.cuda.Stream()
 
-    base_flags = sv.SPEC_OPT_PDL if args.pdl else 0
+    base_flags = (sv.SPEC_OPT_PDL if args.pdl else 0) | (sv.SPEC_OPT_NO_PERSIST if args.no_persist else 0)
 
     def make(temp, mix, flags=0):
         return sv.SpecDecoder(tshape, tw, dshape, dw, K, max_ctx, temperature=temp, seed=0,
@@ -265,6 +306,18 @@ def main():
             ms += e0.elapsed_time(e1)
             toks += emitted
         return ms, toks, done
+
+    if args.phase_times:
+        dec = make(args.temperature, args.mix, sv.SPEC_OPT_PHASE_TIMES)
+        dec.prefill(prompt(0))
+        for _ in range(max(args.warmup, 3)):
+            dec.step()
+        dec.profile(3)   # runs the verify-only and plain-decoding passes too
+        print(json.dumps({"phase_times": True, "workload": wl,
+                          "passes": {name: phase_summary(dec.phase_times(i))
+                                     for name, i in (("draft_1", 0), ("draft_2", 1), ("verify", K),
+                                                     ("ar", K + 1))}}), flush=True)
+        return 0
 
     if args.ncu_mode:
         dec = make(args.temperature, args.mix)

@@ -72,6 +72,13 @@ extern "C" {
 #define SPEC_OPT_PDL           0x4   /* launch kernels with programmatic dependent launch
                                         (process-wide; off by default: measured slower on
                                         the verify pass) */
+#define SPEC_OPT_NO_PERSIST    0x8   /* run each forward as one kernel per operation
+                                        instead of one persistent kernel (bf16 models).
+                                        The two paths sum in different orders: their
+                                        logits agree to rounding, not bit for bit; each
+                                        is batch-invariant on its own */
+#define SPEC_OPT_PHASE_TIMES   0x10  /* persistent kernel records per-phase timestamps
+                                        (read with spec_phase_times) */
 
 typedef struct spec_ctx spec_ctx;
 
@@ -260,6 +267,20 @@ typedef struct spec_profile_t {
     int32_t kernels_ar;
 } spec_profile_t;
 SPEC_API int spec_profile(spec_ctx* ctx, int iters, spec_profile_t* out);
+
+/* Per-phase timing of the last run of one persistent forward pass
+ * (context created with SPEC_OPT_PHASE_TIMES on the persistent path).
+ * which: 0..K-1 the K draft passes of a step, K the verify pass, K+1 the
+ * plain-decoding pass.  Writes *nphases and, per phase i, six int64 at
+ * out[6 i ..]: kind (0 embedding, 1 GEMM, 2 attention), rows n (GEMM) or
+ * query heads (attention) or tokens (embedding), k (GEMM) or tokens
+ * (attention), then three %globaltimer offsets in ns from CTA 0's start:
+ * the earliest and the latest CTA's arrival at the end of the phase and
+ * CTA 0's release from the grid barrier after it (-1 for the last phase).
+ * out holds max_phases * 6 int64 (host).  Synchronises the context's stream.
+ * Errors: SPEC_E_STATE without the option or the persistent path,
+ * SPEC_E_ARG when max_phases is too small (after setting *nphases). */
+SPEC_API int spec_phase_times(spec_ctx* ctx, int which, int64_t* out, int max_phases, int* nphases);
 
 /* Library version string. */
 SPEC_API const char* spec_version(void);

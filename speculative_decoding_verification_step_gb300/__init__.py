@@ -26,6 +26,8 @@ SPEC_FLAG_ALL_ACCEPTED = 0x2
 SPEC_OPT_NO_GRAPH = 0x1
 SPEC_OPT_TIMING = 0x2
 SPEC_OPT_PDL = 0x4
+SPEC_OPT_NO_PERSIST = 0x8
+SPEC_OPT_PHASE_TIMES = 0x10
 
 _LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
 
@@ -105,6 +107,8 @@ SIGNATURES = {
                                         ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64,
                                         ctypes.c_int, _VP, _VP]),
     "spec_profile": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(Profile)]),
+    "spec_phase_times": (ctypes.c_int, [_VP, ctypes.c_int, _VP, ctypes.c_int,
+                                        ctypes.POINTER(ctypes.c_int)]),
     "spec_version": (ctypes.c_char_p, []),
 }
 
@@ -219,6 +223,18 @@ class SpecDecoder:
         pr = Profile()
         _check(lib().spec_profile(self.ctx, iters, ctypes.byref(pr)), self.ctx)
         return pr.as_dict()
+
+    def phase_times(self, which):
+        """Per-phase stamps of the last persistent run of forward `which`
+        (0..K-1 draft passes, K verify, K+1 plain decoding): a list of dicts
+        with kind, n, k and the earliest/latest arrival and release in ns."""
+        import numpy as np
+        buf = np.zeros((1024, 6), dtype=np.int64)
+        n = ctypes.c_int(0)
+        _check(lib().spec_phase_times(self.ctx, which, buf.ctypes.data_as(_VP), 1024,
+                                      ctypes.byref(n)), self.ctx)
+        names = ("kind", "n", "k", "arrive_min_ns", "arrive_max_ns", "release_ns")
+        return [dict(zip(names, (int(v) for v in row))) for row in buf[:n.value]]
 
     def last_step_debug(self, max_ctx):
         """(p_logits [K+1, V], q_logits [K, V], drafts [K], context tokens) as numpy."""

@@ -1,0 +1,312 @@
+// Decode / verify attention of the persistent forward kernel (at most 8
+// query tokens, bf16 KV cache), on tensor cores.
+//
+// Work item = (KV head, query token, group of up to 8 of the KV head's
+// query heads, key split).  All rows of an item share one position p, so they
+// see the same keys 0..p.  Keys are walked in absolute 16-key steps; step s
+// belongs to consumer warp s mod 8.  A warp keeps, per row, an online
+// softmax state over its steps (running max m, sum l, output o):
+//   scores  S = K_step Q^T              (mma m16n8k16: keys x rows, k = dims)
+//   m' = max(m, max_j S_j), scale = exp(m - m'), p_j = exp(S_j - m')
+//   l  = l * scale + sum_j p_j,  o = o * scale + V_step^T p   (bf16 p)
+// with K, Q, V and p in bf16 and fp32 accumulation.  The eight warp states
+// are then merged in warp order: M = max_w m_w, out = sum_w e^(m_w - M) o_w /
+// sum_w e^(m_w - M) l_w.  Keys are split in absolute 1024-key ranges; a row
+// whose position spans several splits writes one (M, L, O) partial per split
+// and the last split item to finish merges them in split order.  Every step
+// of the arithmetic is fixed by the row's position alone, so a row gets the
+// same bits whichever rows share the pass (batch invariance).
+//
+// Memory: per warp two 16-key K/V buffers (cp.async, rows padded by 16 bytes
+// so the fragment loads and ldmatrix rows hit distinct banks) and a 16x8
+// probability tile; the warp merge reuses the same space.
+#pragma once
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sv {
+
+constexpr int kDStepKeys = 16;
+constexpr int kDSplitKeys = 1024;
+constexpr int kDWarps = 8;
+constexpr int kDRows = 8;                          // rows per item (MMA n)
+
+template <int HD>
+struct DAttnSmem {
+  static constexpr int kPitch = HD + 8;            // bf16 elements per buffered key row
+  static constexpr int kBufElems = kDStepKeys * kPitch;
+  // per warp: K[2], V[2] buffers, then the probability tile [8 rows][16 keys]
+  static constexpr size_t kWarpBytes = (size_t)4 * kBufElems * 2 + kDRows * kDStepKeys * 2;
+  // merge area: m, l [8 warps][8 rows], o [8 warps][8 rows][HD] (fp32)
+  static constexpr size_t kMergeBytes = (size_t)kDWarps * kDRows * (2 + HD) * 4;
+  static constexpr size_t kBytes = kDWarps * kWarpBytes > kMergeBytes ? kDWarps * kWarpBytes : kMergeBytes;
+};
+
+SV_DEV void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+SV_DEV uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Item geometry.
+struct DItem {
+  int kvh, t, hg, split;
+};
+SV_DEV DItem dattn_item_of(const AttnDesc& a, int it, int hgroups) {
+  DItem d;
+  d.hg = it % hgroups;
+  it /= hgroups;
+  d.kvh = it % a.hkv;
+  it /= a.hkv;
+  d.t = it % a.ntok;
+  d.split = it / a.ntok;
+  return d;
+}
+__host__ __device__ inline int dattn_hgroups(int hq, int hkv) { return (hq / hkv + kDRows - 1) / kDRows; }
+__host__ __device__ inline int dattn_splits(int cap) { return (cap + kDSplitKeys - 1) / kDSplitKeys; }
+__host__ __device__ inline int dattn_items(int ntok, int hq, int hkv, int cap) {
+  return dattn_splits(cap) * ntok * hkv * dattn_hgroups(hq, hkv);
+}
+
+// Issue the cp.async copies of K/V step s (keys 16s .. 16s+15, those above
+// `last` zero-filled) into one buffer pair of the warp.
+template <int HD>
+SV_DEV void dattn_fetch(const bf16* kc, const bf16* vc, int s, int last, bf16* kb, bf16* vb) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kVecPerRow = HD / 8;               // 16-byte vectors per key row
+  constexpr int kVecs = kDStepKeys * kVecPerRow;
+#pragma unroll
+  for (int i = lane; i < kVecs; i += 32) {
+    const int key = i / kVecPerRow, v = i % kVecPerRow;
+    const int abs_key = s * kDStepKeys + key;
+    const bool ok = abs_key <= last;
+    const size_t src = (size_t)(ok ? abs_key : 0) * HD + v * 8;
+    cp_async16(kb + key * DAttnSmem<HD>::kPitch + v * 8, kc + src, ok);
+    cp_async16(vb + key * DAttnSmem<HD>::kPitch + v * 8, vc + src, ok);
+  }
+  cp_async_commit();
+}
+
+// One item; called by the eight consumer warps (threads 0..255) of the CTA.
+// sm: dynamic shared memory (DAttnSmem<HD>::kBytes); s_last: shared int.
+template <int HD>
+SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last) {
+  using L = DAttnSmem<HD>;
+  const int hgroups = dattn_hgroups(a.hq, a.hkv);
+  const DItem d = dattn_item_of(a, it, hgroups);
+  const int G = a.hq / a.hkv;
+  const int rows = min(kDRows, G - d.hg * kDRows);   // valid rows of this item
+  const int pos = *a.pos_base + a.pos_off + d.t;
+  const int k0 = d.split * kDSplitKeys;
+  if (k0 > pos) return;                               // split entirely in the future
+  const int last = min(pos, k0 + kDSplitKeys - 1);    // last key of this split
+  const int nsplit = pos / kDSplitKeys + 1;           // splits of this row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
+  const int h0 = d.kvh * G + d.hg * kDRows;           // first query head of the item
+  const bf16* kc = (const bf16*)a.kc + (size_t)d.kvh * a.cap * HD;
+  const bf16* vc = (const bf16*)a.vc + (size_t)d.kvh * a.cap * HD;
+
+  // Q fragments (rows = query heads; dims in groups of GD, k-permuted as in
+  // the GEMM): thread (g, c) holds row g, dims j*GD + c*GD/4 .. +GD/4-1 of
+  // every group j as TW bf16 pairs; MMA i of a group takes pairs 2i, 2i+1.
+  constexpr int GD = HD < 64 ? HD : 64;
+  constexpr int NG = HD / GD, TW = GD / 8, NM = GD / 16;
+  uint32_t qf[NG][TW];
+  {
+    const bool ok = gi < rows;
+    const float* qp = a.q + ((size_t)d.t * a.hq + h0 + (ok ? gi : 0)) * HD + ci * (GD / 4);
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+#pragma unroll
+      for (int e = 0; e < TW / 2; ++e) {
+        const float4 v = ok ? __ldcg(reinterpret_cast<const float4*>(qp + j * GD + 4 * e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qf[j][2 * e] = pack_bf16(v.x, v.y);
+        qf[j][2 * e + 1] = pack_bf16(v.z, v.w);
+      }
+    }
+  }
+
+  // buffer b of the warp: K at wb + b * kBufElems, V at wb + (2 + b) * kBufElems
+  bf16* wb = reinterpret_cast<bf16*>(sm + (size_t)warp * L::kWarpBytes);
+  bf16* ps = wb + 4 * L::kBufElems;                   // [8 rows][16 keys]
+
+  // this warp's steps: s = s_begin + warp + 8j, s <= s_end
+  const int s_begin = k0 / kDStepKeys, s_end = last / kDStepKeys;
+  float m_r[2] = {neg_inf(), neg_inf()}, l_r[2] = {0.f, 0.f};   // rows 2c, 2c+1
+  float o[HD / 16][4];
+#pragma unroll
+  for (int mt = 0; mt < HD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  const bool rv0 = 2 * ci < rows, rv1 = 2 * ci + 1 < rows;
+  int s = s_begin + warp;
+  if (s <= s_end) dattn_fetch<HD>(kc, vc, s, last, wb, wb + 2 * L::kBufElems);
+  int buf = 0;
+  for (; s <= s_end; s += kDWarps, buf ^= 1) {
+    const int sn = s + kDWarps;
+    if (sn <= s_end) {
+      dattn_fetch<HD>(kc, vc, sn, last, wb + (buf ^ 1) * L::kBufElems, wb + (3 - buf) * L::kBufElems);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
+    // scores: D[key g / g+8][row 2c / 2c+1]
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    const bf16* kr = wb + buf * L::kBufElems + gi * L::kPitch + ci * (GD / 4);
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      uint32_t lo[TW], hi[TW];   // key rows g and g+8
+#pragma unroll
+      for (int e = 0; e < TW / 4; ++e) {
+        const uint4 x = *reinterpret_cast<const uint4*>(kr + j * GD + 8 * e);
+        const uint4 y = *reinterpret_cast<const uint4*>(kr + 8 * L::kPitch + j * GD + 8 * e);
+        lo[4 * e] = x.x; lo[4 * e + 1] = x.y; lo[4 * e + 2] = x.z; lo[4 * e + 3] = x.w;
+        hi[4 * e] = y.x; hi[4 * e + 1] = y.y; hi[4 * e + 2] = y.z; hi[4 * e + 3] = y.w;
+      }
+#pragma unroll
+      for (int i = 0; i < NM; ++i)
+        mma_bf16_16816(sc, lo[2 * i], hi[2 * i], lo[2 * i + 1], hi[2 * i + 1], qf[j][2 * i], qf[j][2 * i + 1]);
+    }
+    const int key_lo = s * kDStepKeys + gi, key_hi = key_lo + 8;
+    const bool kv_lo = key_lo <= last, kv_hi = key_hi <= last;
+    float v00 = (rv0 && kv_lo) ? sc[0] * a.scale : neg_inf();   // row 2c, key g
+    float v01 = (rv1 && kv_lo) ? sc[1] * a.scale : neg_inf();   // row 2c+1, key g
+    float v10 = (rv0 && kv_hi) ? sc[2] * a.scale : neg_inf();   // row 2c, key g+8
+    float v11 = (rv1 && kv_hi) ? sc[3] * a.scale : neg_inf();   // row 2c+1, key g+8
+    // step max per row over the 16 keys (lanes sharing c)
+    float mx0 = fmaxf(v00, v10), mx1 = fmaxf(v01, v11);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
+    const float sc0 = rv0 ? expf(m_r[0] - mn0) : 0.f;   // m_r = -inf before the first step: 0
+    const float sc1 = rv1 ? expf(m_r[1] - mn1) : 0.f;
+    const float p00 = v00 == neg_inf() ? 0.f : expf(v00 - mn0);
+    const float p10 = v10 == neg_inf() ? 0.f : expf(v10 - mn0);
+    const float p01 = v01 == neg_inf() ? 0.f : expf(v01 - mn1);
+    const float p11 = v11 == neg_inf() ? 0.f : expf(v11 - mn1);
+    float ls0 = p00 + p10, ls1 = p01 + p11;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
+    }
+    if (rv0) {
+      l_r[0] = l_r[0] * sc0 + ls0;
+      m_r[0] = mn0;
+    }
+    if (rv1) {
+      l_r[1] = l_r[1] * sc1 + ls1;
+      m_r[1] = mn1;
+    }
+    // probabilities as bf16, [row][key]
+    ps[(2 * ci) * kDStepKeys + gi] = __float2bfloat16_rn(p00);
+    ps[(2 * ci + 1) * kDStepKeys + gi] = __float2bfloat16_rn(p01);
+    ps[(2 * ci) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p10);
+    ps[(2 * ci + 1) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p11);
+    __syncwarp();
+    const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(ps + gi * kDStepKeys + 2 * ci);
+    const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(ps + gi * kDStepKeys + 2 * ci + 8);
+    // o^T[dim][row] = o^T * scale + V^T p: A = V^T via transposing ldmatrix
+    const int lrow = (lane & 7) + ((lane >> 4) << 3);   // key of this lane's row address
+    const int lcol = ((lane >> 3) & 1) * 8;             // dim offset within the 16-dim tile
+    const bf16* vr = wb + (2 + buf) * L::kBufElems + lrow * L::kPitch + lcol;
+#pragma unroll
+    for (int mt = 0; mt < HD / 16; ++mt) {
+      uint32_t va[4];
+      ldmatrix_x4_trans(va, vr + mt * 16);
+      o[mt][0] *= sc0;
+      o[mt][1] *= sc1;
+      o[mt][2] *= sc0;
+      o[mt][3] *= sc1;
+      mma_bf16_16816(o[mt], va[0], va[1], va[2], va[3], pb0, pb1);
+    }
+    __syncwarp();   // buffers and the probability tile are reused by the next step
+  }
+  cp_async_wait<0>();
+
+  // ---- merge the eight warps (warp order) ----
+  named_sync(1, kDWarps * 32);   // every warp is done with its buffers
+  float* mm = reinterpret_cast<float*>(sm);          // [8 warps][8 rows]
+  float* ll = mm + kDWarps * kDRows;                 // [8 warps][8 rows]
+  float* oo = ll + kDWarps * kDRows;                 // [8 warps][8 rows][HD]
+  if (gi == 0) {
+    mm[warp * kDRows + 2 * ci] = m_r[0];
+    mm[warp * kDRows + 2 * ci + 1] = m_r[1];
+    ll[warp * kDRows + 2 * ci] = l_r[0];
+    ll[warp * kDRows + 2 * ci + 1] = l_r[1];
+  }
+#pragma unroll
+  for (int mt = 0; mt < HD / 16; ++mt) {
+    float* ow = oo + (size_t)warp * kDRows * HD;
+    ow[(2 * ci) * HD + mt * 16 + gi] = o[mt][0];
+    ow[(2 * ci + 1) * HD + mt * 16 + gi] = o[mt][1];
+    ow[(2 * ci) * HD + mt * 16 + gi + 8] = o[mt][2];
+    ow[(2 * ci + 1) * HD + mt * 16 + gi + 8] = o[mt][3];
+  }
+  named_sync(1, kDWarps * 32);
+  const int tid = threadIdx.x;
+  for (int e = tid; e < rows * HD; e += kDWarps * 32) {
+    const int r = e / HD, dm = e % HD;
+    float M = neg_inf();
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, mm[w * kDRows + r]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) {
+      const float mw = mm[w * kDRows + r];
+      const float f = mw == neg_inf() ? 0.f : expf(mw - M);
+      num = fmaf(f, oo[((size_t)w * kDRows + r) * HD + dm], num);
+      den = fmaf(f, ll[w * kDRows + r], den);
+    }
+    const int h = h0 + r;
+    if (nsplit == 1) {
+      ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)h * HD + dm] = __float2bfloat16_rn(num / den);
+    } else {
+      float* pp = a.partials + (((size_t)d.t * a.hq + h) * dattn_splits(a.cap) + d.split) * (HD + 4);
+      pp[dm] = num;
+      if (dm == 0) {
+        pp[HD] = M;
+        pp[HD + 1] = den;
+      }
+    }
+  }
+  if (nsplit == 1) {
+    named_sync(1, kDWarps * 32);   // the merge area is reused by the next item
+    return;
+  }
+  // ---- several splits: the last one to finish merges them in split order ----
+  int* ticket = a.tickets + ((size_t)d.t * a.hkv + d.kvh) * hgroups + d.hg;
+  named_sync(1, kDWarps * 32);
+  if (tid == 0) {
+    __threadfence();
+    *s_last = (atomicAdd(ticket, 1) == nsplit - 1);
+  }
+  named_sync(1, kDWarps * 32);
+  if (!*s_last) return;
+  __threadfence();
+  const int ns = dattn_splits(a.cap);
+  for (int e = tid; e < rows * HD; e += kDWarps * 32) {
+    const int r = e / HD, dm = e % HD;
+    const float* base = a.partials + ((size_t)d.t * a.hq + h0 + r) * ns * (HD + 4);
+    float M = neg_inf();
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(base + (size_t)sp * (HD + 4) + HD));
+    float num = 0.f, den = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float* pp = base + (size_t)sp * (HD + 4);
+      const float f = expf(__ldcg(pp + HD) - M);
+      num = fmaf(f, __ldcg(pp + dm), num);
+      den = fmaf(f, __ldcg(pp + HD + 1), den);
+    }
+    ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)(h0 + r) * HD + dm] = __float2bfloat16_rn(num / den);
+  }
+  named_sync(1, kDWarps * 32);
+  if (tid == 0) *ticket = 0;
+}
+
+}  // namespace sv

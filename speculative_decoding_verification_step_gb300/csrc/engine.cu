@@ -61,8 +61,21 @@ namespace sv {
 void set_thread_error(const std::string& msg) { g_err = msg; }
 }  // namespace sv
 
+struct PersistFwd {
+  PersistDesc desc{};
+  int hd = 0;
+  size_t smem = 0;
+  std::vector<PhaseDesc> host;   // the phase list (for spec_phase_times)
+};
+
 struct spec_ctx {
   ModelState tgt, drf;
+  bool persist = false;            // persistent forward kernels (bf16 models)
+  // draft passes 1..K (0..K-1), verify (K), plain decoding (K+1), and the
+  // last scored prompt position of the draft (K+2) and of the target (K+3)
+  PersistFwd pforward[20];
+  PhaseDesc* phase_dev = nullptr;
+  unsigned* bar = nullptr;
   int K = 0;
   spec_opts opts{};
   cudaStream_t stream = nullptr;
@@ -78,11 +91,11 @@ struct spec_ctx {
   float* x = nullptr;
   void* xn = nullptr;
   void* hbuf = nullptr;
-  float* qkv = nullptr;
   float* q = nullptr;
   void* attn = nullptr;
   float* attn_part = nullptr;
   int* attn_tick = nullptr;
+  float* ss = nullptr;         // [d_max/16][kGemmMaxTok] per-tile sums of squares
   float* logits_p = nullptr;  // [K+1][V]
   float* logits_q = nullptr;  // [K][V]
   GemmScratch gs{};
@@ -210,65 +223,117 @@ void gemm(Launch& L, const GemmDesc& g, int dtype) {
   }
 }
 
-// Forward of one model over ntok tokens.  tokens = tok_base + *tok_idx +
-// tok_off; positions = *pos_idx + pos_off + t.  LM-head logits of rows
-// [lrow0, lrow0 + lrows) go to logits ([lrows][V]).
-void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const int32_t* tok_idx,
-             int tok_off, const int32_t* pos_idx, int pos_off, int lrow0, int lrows,
-             float* logits) {
-  spec_ctx* c = L.c;
+// One kernel-level operation of a forward.
+struct Op {
+  int kind;   // PhaseKind
+  GemmDesc g;
+  AttnDesc a;
+  EmbedDesc e;
+};
+
+// Operations of one model's forward over ntok tokens.  tokens = tok_base +
+// *tok_idx + tok_off; positions = *pos_idx + pos_off + t.  LM-head logits of
+// rows [lrow0, lrow0 + lrows) go to logits ([lrows][V]).  Per layer: q/k/v
+// GEMM (input RMSNorm on load, RoPE + KV append in its epilogue), attention,
+// o-projection + residual (writes the next norm's sums of squares), gate/up
+// GEMM (RMSNorm on load, SwiGLU epilogue), down-projection + residual.
+std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t* tok_base,
+                            const int32_t* tok_idx, int tok_off, const int32_t* pos_idx,
+                            int pos_off, int lrow0, int lrows, float* logits) {
   const spec_model_desc& d = m.d;
   const int dm = d.d_model, hq = d.n_heads, hkv = d.n_kv_heads, hd = d.head_dim;
   const int qkvr = m.qkv_rows();
   const int dt = d.dtype;
-  cudaStream_t s = c->stream;
-  L.note(launch_embed(tok_base, tok_idx, tok_off, d.embed, dt, c->x, ntok, dm, s));
+  std::vector<Op> ops;
+  Op op{};
+  op.kind = kPhaseEmbed;
+  op.e.tok_base = tok_base; op.e.tok_idx = tok_idx; op.e.tok_off = tok_off; op.e.embed = d.embed;
+  op.e.dtype = dt; op.e.x = c->x; op.e.ss = c->ss; op.e.ss_ld = kGemmMaxTok; op.e.ntok = ntok;
+  op.e.d = dm;
+  ops.push_back(op);
   for (int l = 0; l < d.n_layers; ++l) {
     const spec_layer_weights& w = m.layers[l];
-    L.note(launch_rmsnorm(c->x, (const float*)w.attn_norm, d.rms_eps, c->xn, dt, ntok, dm, s));
-    GemmDesc g{};
+    const size_t kvoff = (size_t)l * m.layer_kv_elems(c->cap) * m.esize;
+    void* kc = (char*)m.kc + kvoff;
+    void* vc = (char*)m.vc + kvoff;
+    Op q{};
+    q.kind = kPhaseGemm;
+    GemmDesc& g = q.g;
     g.w[0] = w.wq; g.w[1] = w.wk; g.w[2] = w.wv;
     g.seg_rows[0] = hq * hd; g.seg_rows[1] = hkv * hd; g.seg_rows[2] = hkv * hd;
-    g.n = qkvr; g.k = dm; g.x = c->xn; g.ldx = dm; g.ntok = ntok;
-    g.epi = kEpiStore; g.out = c->qkv; g.ldo = qkvr;
-    gemm(L, g, dt);
-    const size_t kvoff = (size_t)l * m.layer_kv_elems(c->cap) * m.esize;
-    RopeDesc r{};
-    r.qkv = c->qkv; r.pos_base = pos_idx; r.pos_off = pos_off;
-    r.rope_cos = m.rope_cos; r.rope_sin = m.rope_sin; r.q_out = c->q;
-    r.kc = (char*)m.kc + kvoff; r.vc = (char*)m.vc + kvoff;
-    r.ntok = ntok; r.hq = hq; r.hkv = hkv; r.hd = hd; r.cap = c->cap; r.dtype = dt;
-    L.note(launch_rope_append(r, s));
-    AttnDesc a{};
-    a.q = c->q; a.kc = r.kc; a.vc = r.vc; a.pos_base = pos_idx; a.pos_off = pos_off;
+    g.n = qkvr; g.k = dm; g.ntok = ntok;
+    g.x = c->x; g.ldx = dm; g.x_norm = 1; g.gain = (const float*)w.attn_norm;
+    g.ss_in = c->ss; g.ss_ld = kGemmMaxTok; g.eps = d.rms_eps;
+    g.epi = kEpiQkvRope; g.hq = hq; g.hkv = hkv; g.hd = hd; g.cap = c->cap;
+    g.pos_base = pos_idx; g.pos_off = pos_off; g.rope_cos = m.rope_cos; g.rope_sin = m.rope_sin;
+    g.q_out = c->q; g.kc = kc; g.vc = vc;
+    ops.push_back(q);
+    Op at{};
+    at.kind = kPhaseAttn;
+    AttnDesc& a = at.a;
+    a.q = c->q; a.kc = kc; a.vc = vc; a.pos_base = pos_idx; a.pos_off = pos_off;
     a.partials = c->attn_part; a.tickets = c->attn_tick; a.out = c->attn;
     a.ntok = ntok; a.hq = hq; a.hkv = hkv; a.hd = hd; a.cap = c->cap;
     a.max_chunks = c->max_chunks; a.dtype = dt;
     a.scale = 1.0f / sqrtf((float)hd);
-    L.note(launch_attention(a, s));
-    GemmDesc o{};
-    o.w[0] = w.wo; o.seg_rows[0] = dm; o.n = dm; o.k = hq * hd; o.x = c->attn; o.ldx = hq * hd;
-    o.ntok = ntok; o.epi = kEpiAdd; o.out = c->x; o.ldo = dm;
-    gemm(L, o, dt);
-    L.note(launch_rmsnorm(c->x, (const float*)w.ffn_norm, d.rms_eps, c->xn, dt, ntok, dm, s));
-    GemmDesc gu{};
-    gu.w[0] = w.w_gate; gu.w[1] = w.w_up; gu.n = d.ffn_dim; gu.k = dm; gu.x = c->xn; gu.ldx = dm;
-    gu.ntok = ntok; gu.epi = kEpiSwiglu; gu.out = c->hbuf; gu.ldo = d.ffn_dim;
-    gemm(L, gu, dt);
-    GemmDesc dn{};
-    dn.w[0] = w.w_down; dn.seg_rows[0] = dm; dn.n = dm; dn.k = d.ffn_dim; dn.x = c->hbuf;
-    dn.ldx = d.ffn_dim; dn.ntok = ntok; dn.epi = kEpiAdd; dn.out = c->x; dn.ldo = dm;
-    dn.early_prefetch = 1;   // follows the gate/up GEMM
-    gemm(L, dn, dt);
+    ops.push_back(at);
+    Op o{};
+    o.kind = kPhaseGemm;
+    o.g.w[0] = w.wo; o.g.seg_rows[0] = dm; o.g.n = dm; o.g.k = hq * hd; o.g.x = c->attn;
+    o.g.ldx = hq * hd; o.g.ntok = ntok; o.g.epi = kEpiAdd; o.g.out = c->x; o.g.ldo = dm;
+    o.g.ss_out = c->ss; o.g.ss_ld = kGemmMaxTok;
+    ops.push_back(o);
+    Op gu{};
+    gu.kind = kPhaseGemm;
+    gu.g.w[0] = w.w_gate; gu.g.w[1] = w.w_up; gu.g.n = d.ffn_dim; gu.g.k = dm; gu.g.ntok = ntok;
+    gu.g.x = c->x; gu.g.ldx = dm; gu.g.x_norm = 1; gu.g.gain = (const float*)w.ffn_norm;
+    gu.g.ss_in = c->ss; gu.g.ss_ld = kGemmMaxTok; gu.g.eps = d.rms_eps;
+    gu.g.epi = kEpiSwiglu; gu.g.out = c->hbuf; gu.g.ldo = d.ffn_dim;
+    ops.push_back(gu);
+    Op dn{};
+    dn.kind = kPhaseGemm;
+    dn.g.w[0] = w.w_down; dn.g.seg_rows[0] = dm; dn.g.n = dm; dn.g.k = d.ffn_dim; dn.g.x = c->hbuf;
+    dn.g.ldx = d.ffn_dim; dn.g.ntok = ntok; dn.g.epi = kEpiAdd; dn.g.out = c->x; dn.g.ldo = dm;
+    dn.g.ss_out = c->ss; dn.g.ss_ld = kGemmMaxTok;
+    dn.g.early_prefetch = 1;   // follows the gate/up GEMM
+    ops.push_back(dn);
   }
   if (lrows > 0) {
-    L.note(launch_rmsnorm(c->x + (size_t)lrow0 * dm, (const float*)d.final_norm, d.rms_eps, c->xn,
-                          dt, lrows, dm, s));
-    GemmDesc h{};
-    h.w[0] = d.lm_head; h.seg_rows[0] = d.vocab; h.n = d.vocab; h.k = dm; h.x = c->xn; h.ldx = dm;
-    h.ntok = lrows; h.epi = kEpiStore; h.out = logits; h.ldo = d.vocab;
-    gemm(L, h, dt);
+    Op h{};
+    h.kind = kPhaseGemm;
+    h.g.w[0] = d.lm_head; h.g.seg_rows[0] = d.vocab; h.g.n = d.vocab; h.g.k = dm; h.g.ntok = lrows;
+    h.g.x = c->x + (size_t)lrow0 * dm; h.g.ldx = dm; h.g.x_norm = 1;
+    h.g.gain = (const float*)d.final_norm;
+    h.g.ss_in = c->ss + lrow0; h.g.ss_ld = kGemmMaxTok; h.g.eps = d.rms_eps;
+    h.g.epi = kEpiStore; h.g.out = logits; h.g.ldo = d.vocab;
+    ops.push_back(h);
   }
+  return ops;
+}
+
+// Per-kernel path: one launch per operation.
+void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const int32_t* tok_idx,
+             int tok_off, const int32_t* pos_idx, int pos_off, int lrow0, int lrows,
+             float* logits) {
+  spec_ctx* c = L.c;
+  const std::vector<Op> ops =
+      forward_ops(c, m, ntok, tok_base, tok_idx, tok_off, pos_idx, pos_off, lrow0, lrows, logits);
+  for (const Op& op : ops) {
+    if (op.kind == kPhaseEmbed) L.note(launch_embed(op.e, c->stream));
+    else if (op.kind == kPhaseAttn) L.note(launch_attention(op.a, c->stream));
+    else gemm(L, op.g, m.d.dtype);
+  }
+}
+
+// Persistent path: one cooperative launch for the whole forward, from a
+// phase list prepared at init (index into c->pforward).
+void forward_persist(Launch& L, int which) {
+  spec_ctx* c = L.c;
+  const PersistFwd& f = c->pforward[which];
+  if (f.desc.times)
+    L.note(cudaMemsetAsync(f.desc.times, 0, sizeof(unsigned long long) * (1 + 3 * f.desc.nphases),
+                           c->stream));
+  L.note(launch_persist(f.desc, f.hd, f.smem, c->num_sms, c->stream));
 }
 
 void enqueue_draft(Launch& L) {
@@ -278,7 +343,9 @@ void enqueue_draft(Launch& L) {
   const bool mix = c->opts.draft_mix_lambda != 0.f;
   for (int i = 1; i <= K; ++i) {
     float* qrow = c->logits_q + (size_t)(i - 1) * V;
-    if (i == 1)
+    if (c->persist)
+      forward_persist(L, i - 1);
+    else if (i == 1)
       forward(L, c->drf, 2, c->seq, Lp, -1, Lp, -1, 1, 1, qrow);
     else
       forward(L, c->drf, 1, c->seq, Lp, i - 1, Lp, i - 1, 0, 1, qrow);
@@ -302,7 +369,10 @@ void enqueue_verify(Launch& L, bool commit) {
   const int32_t* Lp = c->st;
   const bool was = c->timing_verify;
   c->timing_verify = commit && (c->opts.flags & SPEC_OPT_TIMING) != 0;
-  forward(L, c->tgt, K + 1, c->seq, Lp, 0, Lp, 0, 0, K + 1, c->logits_p);
+  if (c->persist)
+    forward_persist(L, K);
+  else
+    forward(L, c->tgt, K + 1, c->seq, Lp, 0, Lp, 0, 0, K + 1, c->logits_p);
   c->timing_verify = was;
   AcceptDesc ad{};
   ad.p = c->logits_p; ad.p_ld = 0; ad.q = c->logits_q; ad.q_ld = 0;
@@ -324,7 +394,7 @@ void enqueue_step(Launch& L) {
   const int K = c->K;
   enqueue_draft(L);
   enqueue_verify(L, true);
-  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 3),
+  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 4),
                          cudaMemcpyDeviceToHost, c->stream));
   c->launch_count--;  // the copy is not a kernel
 }
@@ -335,7 +405,10 @@ void enqueue_ar_pass(Launch& L, bool commit) {
   spec_ctx* c = L.c;
   const int V = c->tgt.d.vocab;
   const int32_t* Lp = c->st;
-  forward(L, c->tgt, 1, c->seq, Lp, 0, Lp, 0, 0, 1, c->logits_p);
+  if (c->persist)
+    forward_persist(L, c->K + 1);
+  else
+    forward(L, c->tgt, 1, c->seq, Lp, 0, Lp, 0, 0, 1, c->logits_p);
   SampleDesc sd{};
   sd.logits = c->logits_p; sd.ld = V; sd.rows = 1; sd.V = V;
   sd.temperature = c->opts.temperature; sd.seed = c->opts.seed;
@@ -351,8 +424,8 @@ void enqueue_ar_pass(Launch& L, bool commit) {
 void enqueue_ar(Launch& L) {
   spec_ctx* c = L.c;
   enqueue_ar_pass(L, true);
-  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t), cudaMemcpyDeviceToHost,
-                         c->stream));
+  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * c->K + 4),
+                         cudaMemcpyDeviceToHost, c->stream));
   c->launch_count--;
 }
 
@@ -407,6 +480,15 @@ void free_ctx(spec_ctx* c) {
   if (c->h_pos) cudaFreeHost(c->h_pos);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   delete c;
+}
+
+// A grid-barrier wait of a persistent kernel gave up: clear the flag and the
+// barrier state so that the context stays usable, and report the timeout.
+int persist_timeout(spec_ctx* c) {
+  cudaMemsetAsync(c->result + (2 * c->K + 3), 0, sizeof(int32_t), c->stream);
+  cudaMemsetAsync(c->bar, 0, sizeof(unsigned) * 4, c->stream);
+  cudaStreamSynchronize(c->stream);
+  return fail(c, SPEC_E_TIMEOUT, "a grid barrier of the persistent forward kernel timed out");
 }
 
 int set_eager_pos(spec_ctx* c, int pos) {
@@ -499,7 +581,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   INIT_TRY(dalloc(c, &c->x, sizeof(float) * maxN * dmax));
   INIT_TRY(dalloc(c, &c->xn, 4 * maxN * dmax));
   INIT_TRY(dalloc(c, &c->hbuf, 4 * maxN * fmax));
-  INIT_TRY(dalloc(c, &c->qkv, sizeof(float) * maxN * qkvmax));
+  INIT_TRY(dalloc(c, &c->ss, sizeof(float) * maxN * (dmax / 16 + 1)));
   INIT_TRY(dalloc(c, &c->q, sizeof(float) * maxN * hqd));
   INIT_TRY(dalloc(c, &c->attn, 4 * maxN * hqd));
   INIT_TRY(dalloc(c, &c->attn_part,
@@ -541,6 +623,94 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     INIT_TRY(launch_rope_table(m->rope_cos, m->rope_sin, c->cap, m->d.head_dim,
                                (double)m->d.rope_theta, c->stream));
   }
+  INIT_TRY(cudaMemset(c->result, 0, sizeof(int32_t) * (2 * K + 8)));
+  // Persistent forward kernels: both models bf16, and the weight ring plus
+  // K+1 tokens of normalised input (or the attention tile) fit one CTA's
+  // shared memory.
+  if (target->dtype == SPEC_DTYPE_BF16 && draft->dtype == SPEC_DTYPE_BF16 &&
+      !(opts->flags & (SPEC_OPT_TIMING | SPEC_OPT_NO_PERSIST))) {
+    const size_t sm_t = persist_smem_bytes(target->head_dim, c->max_chunks, K + 1, target->d_model);
+    const size_t sm_d = persist_smem_bytes(draft->head_dim, c->max_chunks, 2, draft->d_model);
+    if (persist_supported(target->head_dim, sm_t, c->num_sms, K + 1) &&
+        persist_supported(draft->head_dim, sm_d, c->num_sms, 2)) {
+      std::vector<PhaseDesc> all;
+      std::vector<TensorMap128> maps;
+      size_t start[20], count[20];
+      bool encodable = c->gs.partial_floats >= persist_partial_floats(c->num_sms);
+      // decode-attention scratch: partials in the attention buffer, own tickets
+      for (const spec_model_desc* m : {target, draft})
+        encodable = encodable && persist_attn_partial_floats(K + 1, m->n_heads, m->head_dim, c->cap) <=
+                                     attn_partial_floats(maxN, (int)hqmax, (int)hdmax, c->max_chunks);
+      int* dattn_tick = nullptr;
+      {
+        const int nt = std::max(persist_attn_tickets(K + 1, target->n_heads, target->n_kv_heads),
+                                persist_attn_tickets(K + 1, draft->n_heads, draft->n_kv_heads));
+        INIT_TRY(dalloc(c, &dattn_tick, sizeof(int) * nt));
+        INIT_TRY(cudaMemset(dattn_tick, 0, sizeof(int) * nt));
+      }
+      auto add = [&](int idx, const std::vector<Op>& ops) {
+        start[idx] = all.size();
+        for (const Op& op : ops) {
+          PhaseDesc p{};
+          if (op.kind == kPhaseEmbed) {
+            persist_phase_from_embed(p, op.e);
+          } else if (op.kind == kPhaseAttn) {
+            encodable = persist_phase_from_attn(p, op.a) && encodable;
+            p.a.tickets = dattn_tick;
+          } else {
+            encodable = persist_phase_from_gemm(p, op.g, maps) && encodable;
+          }
+          all.push_back(p);
+        }
+        count[idx] = ops.size();
+      };
+      for (int i = 1; i <= K; ++i) {
+        float* qrow = c->logits_q + (size_t)(i - 1) * V;
+        if (i == 1)
+          add(0, forward_ops(c, c->drf, 2, c->seq, c->st, -1, c->st, -1, 1, 1, qrow));
+        else
+          add(i - 1, forward_ops(c, c->drf, 1, c->seq, c->st, i - 1, c->st, i - 1, 0, 1, qrow));
+      }
+      add(K, forward_ops(c, c->tgt, K + 1, c->seq, c->st, 0, c->st, 0, 0, K + 1, c->logits_p));
+      add(K + 1, forward_ops(c, c->tgt, 1, c->seq, c->st, 0, c->st, 0, 0, 1, c->logits_p));
+      // last scored prompt position (st[0] - 1) of both models, run by
+      // spec_prefill so that its KV rows carry the step passes' arithmetic
+      add(K + 2, forward_ops(c, c->drf, 1, c->seq, c->st, -1, c->st, -1, 0, 0, nullptr));
+      add(K + 3, forward_ops(c, c->tgt, 1, c->seq, c->st, -1, c->st, -1, 0,
+                             opts->draft_mix_lambda != 0.f ? 1 : 0, c->logits_p + (size_t)K * V));
+      if (encodable) {
+        INIT_TRY(dalloc(c, &c->phase_dev, sizeof(PhaseDesc) * all.size()));
+        INIT_TRY(cudaMemcpy(c->phase_dev, all.data(), sizeof(PhaseDesc) * all.size(), cudaMemcpyHostToDevice));
+        TensorMap128* tmaps_dev = nullptr;
+        INIT_TRY(dalloc(c, &tmaps_dev, sizeof(TensorMap128) * maps.size()));
+        INIT_TRY(cudaMemcpy(tmaps_dev, maps.data(), sizeof(TensorMap128) * maps.size(), cudaMemcpyHostToDevice));
+        INIT_TRY(dalloc(c, &c->bar, sizeof(unsigned) * 4));
+        INIT_TRY(cudaMemset(c->bar, 0, sizeof(unsigned) * 4));
+        unsigned long long* times = nullptr;
+        if (opts->flags & SPEC_OPT_PHASE_TIMES) {
+          const size_t words = (size_t)(K + 4) + 3 * all.size();   // 1 + 3 phases per forward
+          INIT_TRY(dalloc(c, &times, sizeof(unsigned long long) * words));
+          INIT_TRY(cudaMemset(times, 0, sizeof(unsigned long long) * words));
+        }
+        for (int f = 0; f <= K + 3; ++f) {
+          PersistFwd& pf = c->pforward[f];
+          pf.host.assign(all.begin() + start[f], all.begin() + start[f] + count[f]);
+          if (times) pf.desc.times = times + f + 3 * start[f];
+          pf.desc.phases = c->phase_dev + start[f];
+          pf.desc.nphases = (int)count[f];
+          pf.desc.tmaps = tmaps_dev;
+          pf.desc.partials = c->gs.partials;
+          pf.desc.tickets = c->gs.tickets;
+          pf.desc.bar = c->bar;
+          pf.desc.err = c->result + (2 * K + 3);
+          const bool drf = f < K || f == K + 2;
+          pf.hd = drf ? draft->head_dim : target->head_dim;
+          pf.smem = drf ? sm_d : sm_t;
+        }
+        c->persist = true;
+      }
+    }
+  }
   if (opts->flags & SPEC_OPT_TIMING) {
     const int n = 2 * (4 * target->n_layers + 1);
     c->ev.resize(n);
@@ -571,9 +741,13 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
   const int n = L - 1;   // positions 0..L-2 are scored; token L-1 is pending
   const int K = c->K;
   const int lo = n - (K + 1);  // rows of the previous-step logits before step 0
+  // The first draft pass of a step recomputes position st[0] - 1.  On the
+  // persistent path that position is scored here by the persistent kernel
+  // too (both models), so that both KV caches hold the same bits for it.
+  const int nk = c->persist ? n - 1 : n;   // positions scored one kernel per operation
   Launch Lc{c};
-  for (int p0 = 0; p0 < n; p0 += kGemmMaxTok) {
-    const int nt = std::min(kGemmMaxTok, n - p0);
+  for (int p0 = 0; p0 < nk; p0 += kGemmMaxTok) {
+    const int nt = std::min(kGemmMaxTok, nk - p0);
     int rc = set_eager_pos(c, p0);
     if (rc) return rc;
     forward(Lc, c->drf, nt, c->seq, nullptr, p0, c->st + 3, 0, 0, 0, nullptr);
@@ -589,7 +763,15 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
     // the pinned position slot is reused by the next chunk
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   }
+  if (c->persist) {
+    forward_persist(Lc, K + 2);
+    forward_persist(Lc, K + 3);
+    CUDA_TRY(c, Lc.e);
+    CUDA_TRY(c, cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 4), cudaMemcpyDeviceToHost,
+                                c->stream));
+  }
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  if (c->persist && c->h_result[2 * K + 3]) return persist_timeout(c);
   c->host_L = L - 1;
   c->prefilled = true;
   c->draft_stale = false;
@@ -610,6 +792,7 @@ int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* ou
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   const int32_t* h = c->h_result;
+  if (c->persist && h[2 * K + 3]) return persist_timeout(c);
   const int cnt = h[K + 1];
   if (cnt < 1 || cnt > K + 1) return fail(c, SPEC_E_CUDA, "acceptance kernel returned an invalid count");
   for (int i = 0; i < cnt; ++i) out_tokens[i] = h[i];
@@ -655,6 +838,7 @@ int spec_ar_step(spec_ctx* c, int32_t* out_token) {
   int rc = run_captured(c, &c->ar_exec, enqueue_ar, &c->kernels_ar);
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  if (c->persist && c->h_result[2 * c->K + 3]) return persist_timeout(c);
   *out_token = c->h_result[0];
   c->host_L += 1;
   c->ar_steps++;
@@ -732,6 +916,11 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  if (c->persist) {
+    int32_t flag = 0;
+    CUDA_TRY(c, cudaMemcpy(&flag, c->result + (2 * c->K + 3), sizeof flag, cudaMemcpyDeviceToHost));
+    if (flag) return persist_timeout(c);
+  }
   out->draft_loop_ms = ms[0];
   out->verify_ms = ms[1];
   out->ar_ms = ms[2];
@@ -739,6 +928,34 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   out->kernels_draft_loop = c->prof_kernels[0];
   out->kernels_verify = c->prof_kernels[1];
   out->kernels_ar = c->prof_kernels[2];
+  return SPEC_OK;
+}
+
+int spec_phase_times(spec_ctx* c, int which, int64_t* out, int max_phases, int* nphases) {
+  if (!c || !out || !nphases) return fail(c, SPEC_E_ARG, "null argument");
+  if (!c->persist) return fail(c, SPEC_E_STATE, "no persistent forward kernel in this context");
+  if (which < 0 || which > c->K + 1) return fail(c, SPEC_E_ARG, "which must be in [0, K+1]");
+  const PersistFwd& f = c->pforward[which];
+  if (!f.desc.times) return fail(c, SPEC_E_STATE, "context created without SPEC_OPT_PHASE_TIMES");
+  const int n = f.desc.nphases;
+  *nphases = n;
+  if (max_phases < n) return fail(c, SPEC_E_ARG, "max_phases below the number of phases");
+  std::vector<unsigned long long> t(1 + 3 * (size_t)n);
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  CUDA_TRY(c, cudaMemcpy(t.data(), f.desc.times, sizeof(unsigned long long) * t.size(),
+                         cudaMemcpyDeviceToHost));
+  const unsigned long long t0 = t[0];
+  auto rel = [&](unsigned long long v) { return v ? (int64_t)(v - t0) : (int64_t)-1; };
+  for (int i = 0; i < n; ++i) {
+    const PhaseDesc& d = f.host[i];
+    int64_t* o = out + 6 * (size_t)i;
+    o[0] = d.kind;
+    o[1] = d.kind == kPhaseGemm ? d.g.n : d.kind == kPhaseAttn ? d.a.hq : d.e.ntok;
+    o[2] = d.kind == kPhaseGemm ? d.g.k : d.kind == kPhaseAttn ? d.a.ntok : 0;
+    o[3] = t[1 + 3 * i] ? rel(~t[1 + 3 * i]) : -1;
+    o[4] = rel(t[2 + 3 * i]);
+    o[5] = rel(t[3 + 3 * i]);
+  }
   return SPEC_OK;
 }
 

@@ -1,30 +1,59 @@
 // Internal launch interface between the kernels and the engine.
 #pragma once
 #include <cuda_runtime.h>
+#include <vector>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace sv {
 
 enum Epi : int {
-  kEpiStore = 0,   // out_f32[tok][row] = y
-  kEpiAdd = 1,     // out_f32[tok][row] += y          (residual add)
-  kEpiSwiglu = 2,  // out[tok][j] = silu(gate_j) * up_j, model dtype (gate/up tiles)
+  kEpiStore = 0,    // out_f32[tok][row] = y
+  kEpiAdd = 1,      // out_f32[tok][row] += y (residual add); optionally per-tile sums of
+                    // squares of the updated rows -> ss_out (the next RMSNorm's input)
+  kEpiSwiglu = 2,   // out[tok][j] = silu(gate_j) * up_j, model dtype (gate/up tiles)
+  kEpiQkvRope = 3,  // fused q/k/v: rotate q, k at their positions; q -> q_out (fp32),
+                    // k, v -> KV cache (model dtype)
 };
 
 // Y = X . W^T for a "skinny" X (ntok rows), W stacked from up to three
 // row-major [rows][k] segments (q/k/v), or the gate/up pair for kEpiSwiglu.
+//
+// Output tiles are 16 rows.  Row pairing per tile (thread rows g and g+8):
+//   plain:        rows 16t + g, 16t + g + 8
+//   kEpiSwiglu:   gate row 8t + g, up row 8t + g
+//   kEpiQkvRope:  head h = t / (hd/16), j = t % (hd/16): rows h*hd + 8j + g and
+//                 h*hd + 8j + g + hd/2 (a RoPE rotation pair)
 struct GemmDesc {
   const void* w[3];
   int seg_rows[3];
   int n;          // total output rows (kEpiSwiglu: ffn, the number of gate rows)
   int k;
-  const void* x;  // [ntok][ldx], bf16 for bf16 models, fp32 for fp32 models
+  // X operand: [ntok][ldx]; bf16 (fp32 models: fp32), or with x_norm = 1 the fp32
+  // residual, normalised on load: X = x * inv_rms(tok) * gain, inv_rms from the
+  // per-16-row-tile sums of squares ss_in[(k/16) tiles][ss_ld].
+  const void* x;
   int ldx;
   int ntok;
+  int x_norm;
+  const float* gain;
+  const float* ss_in;
+  int ss_ld;
+  float eps;
+  // epilogue
   int epi;
-  void* out;      // see Epi
+  void* out;      // kEpiStore/kEpiAdd: fp32 [ntok][ldo]; kEpiSwiglu: model dtype [ntok][ldo]
   int ldo;
+  float* ss_out;  // kEpiAdd: per-tile sums of squares [tiles][ss_ld] (may be null)
+  // kEpiQkvRope
+  int hq, hkv, hd, cap;
+  const int32_t* pos_base;   // position of token t = *pos_base + pos_off + t
+  int pos_off;
+  const float* rope_cos;     // [cap][hd/2]
+  const float* rope_sin;
+  float* q_out;              // [ntok][hq][hd]
+  void* kc;                  // [hkv][cap][hd] of this layer
+  void* vc;
   int early_prefetch;  // 1: issue the first weight loads before waiting for the
                        // previous kernel (only when that kernel is itself a
                        // bandwidth-bound GEMM; a latency-bound predecessor would
@@ -49,31 +78,23 @@ int gemm_tiles(const GemmDesc& g);
 // dtype: 0 = fp32 model (CUDA-core GEMV), 1 = bf16 model (tensor-core stream-K).
 cudaError_t launch_gemm(const GemmDesc& g, int dtype, const GemmScratch& s, int num_sms,
                         cudaStream_t st, bool pdl);
+cudaError_t configure_gemm();
 
 // x[t][:] = embed[tok[t]][:] (fp32 residual stream), with
-// tok = tok_base + (tok_idx ? *tok_idx : 0) + tok_off (device-resident index).
-cudaError_t launch_embed(const int32_t* tok_base, const int32_t* tok_idx, int tok_off,
-                         const void* embed, int dtype, float* x, int ntok, int d, cudaStream_t st);
-// out[t][:] = x[t][:] / sqrt(mean(x^2) + eps) * gain   (out in model dtype)
-cudaError_t launch_rmsnorm(const float* x, const float* gain, float eps, void* out, int dtype,
-                           int ntok, int d, cudaStream_t st);
-
-// Rotate q and k of the fused qkv rows (fp32 [ntok][(hq+2hkv)*hd]) at
-// positions *pos_base + t; q -> q_out fp32 [ntok][hq][hd], k,v -> KV cache
-// [hkv][cap][hd] (model dtype) at those positions.
-struct RopeDesc {
-  const float* qkv;
-  const int32_t* pos_base;  // position of token t = *pos_base + pos_off + t
-  int pos_off;
-  const float* rope_cos;  // [cap][hd/2]
-  const float* rope_sin;
-  float* q_out;
-  void* kc;
-  void* vc;
-  int ntok, hq, hkv, hd, cap, dtype;
+// tok = tok_base + (tok_idx ? *tok_idx : 0) + tok_off (device-resident index);
+// ss[i][t] = sum of x[t][16i .. 16i+15]^2 (the first RMSNorm's input).
+struct EmbedDesc {
+  const int32_t* tok_base;
+  const int32_t* tok_idx;
+  int tok_off;
+  const void* embed;
+  int dtype;
+  float* x;
+  float* ss;
+  int ss_ld;
+  int ntok, d;
 };
-cudaError_t launch_rope_append(const RopeDesc& r, cudaStream_t st);
-
+cudaError_t launch_embed(const EmbedDesc& e, cudaStream_t st);
 // Causal GQA attention of ntok new query rows over the KV cache, split by
 // fixed 64-key chunks of absolute position; the last CTA of each (KV head,
 // row tile) combines the chunk partials of its rows (the result of a row
@@ -154,6 +175,65 @@ struct AcceptDesc {
 };
 size_t accept_partial_floats(int rows, int K, int V);
 cudaError_t launch_accept(const AcceptDesc& a, cudaStream_t st);
+
+// ---- persistent forward (bf16 models) ----
+// One cooperative launch runs the phases of a whole forward (embedding, the
+// per-layer GEMMs and attention, the LM head), separated by a bounded grid
+// barrier.  GEMM phases stream their weights with 2-D tensor copies (see
+// tma_dev.cuh); results agree with the per-kernel path up to the order of
+// fp32 partial sums, and are batch-invariant like it.
+enum PhaseKind : int { kPhaseEmbed = 0, kPhaseGemm = 1, kPhaseAttn = 2 };
+struct PhaseDesc {
+  int kind;
+  int xm;            // GEMM X source (see gemm_dev.cuh)
+  // GEMM streaming geometry: R rows per box, paired boxes (RoPE / SwiGLU) or
+  // one box of 2R rows, row groups, ring stages and bytes per stage, and the
+  // tensor-map indices of the weight segments (0..2) and of X (3)
+  int R, paired, groups, stages, stage_bytes;
+  int tm[4];
+  int attn_items;
+  GemmDesc g;
+  AttnDesc a;
+  EmbedDesc e;
+};
+// 2-D tensor-map descriptors (opaque, 128 bytes, 64-byte aligned in memory).
+struct alignas(64) TensorMap128 {
+  unsigned char bytes[128];
+};
+struct PersistDesc {
+  const PhaseDesc* phases;   // device array
+  int nphases;
+  const TensorMap128* tmaps; // device array indexed by PhaseDesc::tm
+  float* partials;           // GEMM scratch, >= persist_partial_floats(grid) floats
+  int* tickets;
+  unsigned* bar;             // [2] barrier arrival count and generation (zero at start)
+  int* err;                  // set to 1 when a wait gives up
+  // optional (null: off): [1 + 3 * nphases] globaltimer stamps, zeroed before
+  // the launch -- start, then per phase the earliest arrival (stored as ~t,
+  // atomicMax), the latest arrival (atomicMax) and CTA 0's release
+  unsigned long long* times;
+};
+// Fill the kernel-side fields of a phase.  The GEMM variant also encodes the
+// phase's tensor maps, appending them to maps; false when the phase does not
+// meet the tensor-copy rules (16-byte aligned rows, k and the X stride
+// multiples of 8, at most 8 tokens, RoPE head dim a multiple of 32).
+bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps);
+// Attention phases need a bf16 cache, at most 8 tokens and head dim 32, 64
+// or 128; their scratch is persist_attn_partial_floats floats and
+// persist_attn_tickets zeroed counters (a.partials, a.tickets).
+bool persist_phase_from_attn(PhaseDesc& p, const AttnDesc& a);
+size_t persist_attn_partial_floats(int max_tok, int hq, int hd, int cap);
+int persist_attn_tickets(int max_tok, int hq, int hkv);
+void persist_phase_from_embed(PhaseDesc& p, const EmbedDesc& e);
+// Dynamic shared memory the persistent kernel needs for head dim hd, KV
+// chunks max_chunks and the largest normalised GEMM input (tokens x k).
+size_t persist_smem_bytes(int hd, int max_chunks, int max_tok, int max_k);
+// GEMM partial-sum floats the persistent kernel needs for `grid` CTAs.
+size_t persist_partial_floats(int grid);
+// True when one CTA per SM of the persistent kernel fits, for passes of at
+// most max_tok tokens.
+bool persist_supported(int hd, size_t smem, int num_sms, int max_tok);
+cudaError_t launch_persist(const PersistDesc& p, int hd, size_t smem, int num_sms, cudaStream_t st);
 
 // RoPE tables: cos/sin of pos * theta^(-2i/hd) for pos < cap, computed in fp64.
 cudaError_t launch_rope_table(float* cos_out, float* sin_out, int cap, int hd, double theta,

@@ -1,0 +1,323 @@
+// Persistent forward kernel (bf16 models).
+//
+// A batch-1 decode or verify pass is a chain of ~5 dependent phases per layer
+// (q/k/v GEMM with RoPE + KV append, attention, o-projection, gate/up GEMM,
+// down-projection), each of which must see the whole output of the previous
+// one.  Launched one kernel per phase, every weight-streaming GEMM pays its
+// ramp-up and tail (the HBM pipe drains at each kernel boundary), which for
+// the 8-50 MB matrices of a decoder layer costs as much as the streaming
+// itself.  Here one cooperative launch runs all phases of a forward:
+//   * one CTA per SM stays resident; phases are separated by a grid barrier
+//     split in an arrive and a wait half;
+//   * GEMM phases stream weights with 2-D tensor copies (TMA) through a
+//     shared-memory ring (tma_dev.cuh): one producer thread copies, eight
+//     consumer warps run the MMAs;
+//   * between arriving at a barrier and waiting on it, the producer already
+//     issues the weight copies of the next GEMM phase's first units (weights
+//     are read-only), so HBM keeps streaming across phase boundaries;
+//   * attention phases run the tensor-core decode attention (dattn_dev.cuh)
+//     on the eight consumer warps; the embedding reuses embed_dev.cuh.
+// The work split depends only on the matrix shapes and the SM count, never
+// on the token count, so every pass is batch-invariant.  Every wait is
+// bounded: a grid-barrier wait that gives up, or a pipeline wait (see
+// tma_dev.cuh), sets the error flag and the kernel leaves; the host reports
+// a timeout.  Activations written by other CTAs are read through L2.
+#include "dattn_dev.cuh"
+#include "embed_dev.cuh"
+#include "tma_dev.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace sv {
+
+constexpr long long kBarrierSpinLimit = 1LL << 22;
+
+SV_DEV unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+SV_DEV unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of a co-resident launch, split in two halves so that
+// the next phase's weight copies can be issued in between: bar[0] counts
+// arrivals, bar[1] is the generation.  grid_arrive (every thread, after the
+// phase's last shared-memory use) publishes this CTA's writes and arrives;
+// grid_wait returns once every CTA has arrived, false (in every thread of the
+// CTA) when the wait gave up or another CTA reported an error.
+SV_DEV void grid_arrive(unsigned* bar, unsigned* s_gen) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned gen = ld_acquire_u32(bar + 1);
+    __threadfence();
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    }
+    *s_gen = gen;
+  }
+}
+
+SV_DEV bool grid_wait(unsigned* bar, int* err, const unsigned* s_gen, int* s_ok) {
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    long long spins = 0;
+    while (ld_acquire_u32(bar + 1) == *s_gen) {
+      if (++spins > kBarrierSpinLimit) {
+        atomicExch(err, 1);
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+    *s_ok = ok && (*(volatile int*)err == 0);
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __grid_constant__ PersistDesc p) {
+  // dynamic shared memory: [weight ring, kRingBytes][X region: normalised X,
+  // or the X boxes of phases reading X from global memory]; attention
+  // phases reuse it from offset 0
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  __shared__ TmaPipe tp;
+  __shared__ float s_inv[kGemmMaxTok];
+  __shared__ int s_last, s_ok;
+  __shared__ unsigned s_gen;
+  // the current and the next phase descriptor, staged in shared memory
+  __shared__ __align__(16) PhaseDesc s_ph[2];
+  unsigned char* ring = dsm;
+  unsigned char* xreg = dsm + kRingBytes;
+  const unsigned char* maps = reinterpret_cast<const unsigned char*>(p.tmaps);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool producer = warp == kProducerWarp;
+  auto stage = [&](int slot, int ph) {
+    const int words = (int)(sizeof(PhaseDesc) / 4);
+    const int* src = reinterpret_cast<const int*>(p.phases + ph);
+    int* dst = reinterpret_cast<int*>(&s_ph[slot]);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+  };
+  unsigned long long* const times = p.times;
+  if (times && blockIdx.x == 0 && threadIdx.x == 0) times[0] = global_ns();
+  tma_init(tp);
+  stage(0, 0);
+  __syncthreads();
+  unsigned cpar = 0;   // consumers: parity of each stage's next full-barrier completion
+  int npre = 0;        // units of the current GEMM phase issued before its barrier
+  for (int ph = 0; ph < p.nphases; ++ph) {
+    const PhaseDesc& d = s_ph[ph & 1];
+    if (d.kind == kPhaseEmbed) {
+      for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16>(d.e, t);
+    } else if (d.kind == kPhaseGemm) {
+      if (d.xm == kXSmem) gemm_prepare_x<kXSmem>(d.g, s_inv, reinterpret_cast<uint16_t*>(xreg));
+      if (producer) {
+        if (lane == 0) tma_produce(d, npre, tp, ring, xreg, maps);
+        __syncwarp();
+      } else if (d.xm == kXSmem) {
+        tma_consume<kXSmem>(d, tp, cpar, ring, xreg, p.partials, p.tickets);
+      } else {
+        tma_consume<kXGlobal>(d, tp, cpar, ring, xreg, p.partials, p.tickets);
+      }
+    } else if (!producer) {
+      for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x) dattn_item<HD>(d.a, it, dsm, &s_last);
+    }
+    npre = 0;
+    // this thread's global writes and shared-memory accesses are ordered
+    // before later tensor copies (other CTAs' copies of X; this CTA's ring)
+    fence_proxy_async_global();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (times) {   // arrival of this CTA (its threads are done with the phase)
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const unsigned long long t = global_ns();
+        atomicMax(times + 1 + 3 * ph, ~t);
+        atomicMax(times + 2 + 3 * ph, t);
+      }
+    }
+    if (ph + 1 < p.nphases) {
+      stage((ph + 1) & 1, ph + 1);
+      grid_arrive(p.bar, &s_gen);   // its __syncthreads also ends this phase's shared-memory use
+      if (threadIdx.x == 0 && tp.abort) atomicExch(p.err, 1);
+      const PhaseDesc& nx = s_ph[(ph + 1) & 1];
+      if (nx.kind == kPhaseGemm && producer) {   // weights of the next GEMM: issued while waiting
+        if (lane == 0) npre = tma_prefetch(nx, tp, ring, xreg, maps);
+        npre = __shfl_sync(0xffffffffu, npre, 0);
+      }
+      if (!grid_wait(p.bar, p.err, &s_gen, &s_ok)) {
+        tma_drain(tp);
+        return;
+      }
+      if (times && blockIdx.x == 0 && threadIdx.x == 0) times[3 + 3 * ph] = global_ns();
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && tp.abort) atomicExch(p.err, 1);
+  if (tp.abort) tma_drain(tp);
+}
+
+// ---- host side ----
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][k] with row stride ld elements, boxes of
+// box_rows x kTmaK; elements outside the matrix read as zero.
+static bool encode_rows(TensorMap128& m, const void* base, int k, long long rows, long long ld, int box_rows) {
+  static_assert(sizeof(CUtensorMap) == sizeof(TensorMap128), "tensor map size");
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || !base || rows < 1 || (reinterpret_cast<uintptr_t>(base) & 15u) || (ld * 2) % 16 != 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTmaK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(reinterpret_cast<CUtensorMap*>(&m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps) {
+  p = PhaseDesc{};
+  p.kind = kPhaseGemm;
+  p.g = g;
+  p.xm = g.x_norm ? kXSmem : kXGlobal;
+  if (g.k % 8 != 0 || g.ntok < 1 || g.ntok > kPersistMaxTok) return false;
+  auto add = [&](const void* base, long long rows, long long ld, int box_rows) {
+    TensorMap128 m{};
+    if (!encode_rows(m, base, g.k, rows, ld, box_rows)) return -1;
+    maps.push_back(m);
+    return (int)maps.size() - 1;
+  };
+  if (g.epi == kEpiQkvRope) {
+    if (g.hd % 32 != 0) return false;
+    p.R = (g.hd / 2) % 32 == 0 ? 32 : 16;
+    p.paired = 1;
+    p.groups = (g.hq + 2 * g.hkv) * (g.hd / (2 * p.R));
+    for (int s = 0; s < 3; ++s) p.tm[s] = add(g.w[s], g.seg_rows[s], g.k, p.R);
+  } else if (g.epi == kEpiSwiglu) {
+    if (g.n % 16 != 0) return false;
+    p.R = g.n % 32 == 0 ? 32 : 16;
+    p.paired = 1;
+    p.groups = g.n / p.R;
+    p.tm[0] = add(g.w[0], g.n, g.k, p.R);
+    p.tm[1] = add(g.w[1], g.n, g.k, p.R);
+    p.tm[2] = p.tm[0];
+  } else {
+    p.R = 32;
+    p.paired = 0;
+    p.groups = (g.n + 2 * p.R - 1) / (2 * p.R);
+    p.tm[0] = add(g.w[0], g.n, g.k, 2 * p.R);
+    p.tm[1] = p.tm[2] = p.tm[0];
+  }
+  p.tm[3] = p.xm == kXGlobal ? add(g.x, g.ntok, g.ldx, kXBoxRows) : 0;
+  for (int i = 0; i < 4; ++i)
+    if (p.tm[i] < 0) return false;
+  p.stage_bytes = 2 * p.R * kTmaRowBytes;
+  p.stages = (int)(kRingBytes / p.stage_bytes);
+  if (p.stages > kMaxStages) p.stages = kMaxStages;
+  return true;
+}
+
+bool persist_phase_from_attn(PhaseDesc& p, const AttnDesc& a) {
+  p = PhaseDesc{};
+  p.kind = kPhaseAttn;
+  p.a = a;
+  p.attn_items = dattn_items(a.ntok, a.hq, a.hkv, a.cap);
+  return a.dtype == 1 && a.ntok <= kPersistMaxTok && a.hq % a.hkv == 0 &&
+         (a.hd == 32 || a.hd == 64 || a.hd == 128);
+}
+
+size_t persist_attn_partial_floats(int max_tok, int hq, int hd, int cap) {
+  return (size_t)max_tok * hq * dattn_splits(cap) * (hd + 4);
+}
+
+int persist_attn_tickets(int max_tok, int hq, int hkv) { return max_tok * hkv * dattn_hgroups(hq, hkv); }
+
+void persist_phase_from_embed(PhaseDesc& p, const EmbedDesc& e) {
+  p = PhaseDesc{};
+  p.kind = kPhaseEmbed;
+  p.e = e;
+}
+
+size_t persist_smem_bytes(int hd, int max_chunks, int max_tok, int max_k) {
+  (void)max_chunks;
+  size_t attn = 0;
+  if (hd == 32) attn = DAttnSmem<32>::kBytes;
+  if (hd == 64) attn = DAttnSmem<64>::kBytes;
+  if (hd == 128) attn = DAttnSmem<128>::kBytes;
+  size_t xreg = (size_t)max_tok * (max_k + kXPad) * 2;
+  if (xreg < (size_t)kMaxStages * kXStageBytes) xreg = (size_t)kMaxStages * kXStageBytes;
+  const size_t gemm = kRingBytes + xreg;
+  return attn > gemm ? attn : gemm;
+}
+
+size_t persist_partial_floats(int grid) { return (size_t)grid * 2 * kMaxMmaTiles * 32 * 4; }
+
+// The dynamic shared-memory limit is a per-function attribute shared by
+// every context of the process (a draft and a target with the same head
+// dimension use the same instance): it only ever grows here.
+template <int HD>
+static bool persist_fits(size_t smem) {
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, persist_forward<HD>) != cudaSuccess) return false;
+  if ((size_t)fa.maxDynamicSharedSizeBytes < smem &&
+      cudaFuncSetAttribute(persist_forward<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return false;
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, persist_forward<HD>, kPersistThreads, smem) !=
+      cudaSuccess)
+    return false;
+  return blocks >= 1;
+}
+
+bool persist_supported(int hd, size_t smem, int num_sms, int max_tok) {
+  (void)num_sms;
+  if (max_tok > kPersistMaxTok || !tensor_map_encoder()) return false;
+  if (hd == 32) return persist_fits<32>(smem);
+  if (hd == 64) return persist_fits<64>(smem);
+  if (hd == 128) return persist_fits<128>(smem);
+  return false;
+}
+
+template <int HD>
+static cudaError_t launch_persist_t(const PersistDesc& p, size_t smem, int num_sms, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);   // one CTA per SM, all co-resident
+  cfg.blockDim = dim3(kPersistThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, persist_forward<HD>, p);
+}
+
+cudaError_t launch_persist(const PersistDesc& p, int hd, size_t smem, int num_sms, cudaStream_t st) {
+  if (hd == 32) return launch_persist_t<32>(p, smem, num_sms, st);
+  if (hd == 64) return launch_persist_t<64>(p, smem, num_sms, st);
+  if (hd == 128) return launch_persist_t<128>(p, smem, num_sms, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sv

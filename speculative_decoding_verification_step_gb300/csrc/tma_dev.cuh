@@ -1,0 +1,334 @@
+// Tensor-copy (TMA) weight streaming of the persistent forward kernel.
+//
+// A GEMM phase is cut into units of one row group x 256 k.  A row group is
+// two boxes of R rows (R = 16 or 32) of the weight matrix, each box one
+// 2-D tensor copy of R x 256 bf16 into shared memory:
+//   * plain matrices: one box of 2R consecutive rows, MMA tile t = rows
+//     16t + g and 16t + 8 + g of the box;
+//   * q/k/v with RoPE: rows h*hd + j*R + [0, R) and the rotation partners
+//     hd/2 further, MMA tile t = row 8t + g of each box;
+//   * SwiGLU: the same R rows of the gate and of the up matrix.
+// So an MMA tile is exactly a 16-row tile of the per-kernel path (same
+// epilogue, same tile index).  A CTA owns a contiguous range of units (split
+// by shape and grid only, never by token count).  One producer thread streams
+// the units through a ring of S stages (S x 2R x 512 bytes, S <= 8): per unit
+// one or two weight boxes and, in phases whose X comes from global memory,
+// one 8-row X box, all completing on the stage's transaction barrier.  The
+// eight consumer warps split a unit's (MMA tile, 64-k step) pairs: warp w
+// takes tile w mod T (T = R/8 tiles) and steps w/T + j*8/T.  At the end of a
+// row group the warps of each tile add their accumulators in warp order in
+// shared memory; a group split between CTAs is finished by the
+// last-arriving CTA, which adds the CTA partials in CTA order.  Results do
+// not depend on timing or on the token count.
+//
+// Every wait is bounded.  A wait that gives up raises the CTA's abort flag;
+// from then on every wait of the CTA returns at once and the warps run
+// through their remaining iterations without touching the data (named
+// barrier counts stay identical); the kernel reports the failure and leaves
+// after waiting, again with a bound, for its copies still in flight.
+#pragma once
+#include "gemm_dev.cuh"
+
+namespace sv {
+
+constexpr int kTmaK = 256;                        // k per unit (box inner extent)
+constexpr int kTmaRowBytes = kTmaK * 2;           // row pitch of a box in shared memory
+constexpr int kTmaSteps = kTmaK / kStepK;         // 64-k MMA steps per unit
+constexpr int kCWarps = 8;                        // consumer warps
+constexpr int kProducerWarp = kCWarps;
+constexpr int kPersistThreads = (kCWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr int kXBoxRows = 8;
+constexpr int kXStageBytes = kXBoxRows * kTmaRowBytes;
+constexpr size_t kRingBytes = 160 * 1024;         // weight ring: 5 stages of 32 KB
+constexpr int kMinUnitsPerCta = 2;
+constexpr int kMaxMmaTiles = 4;                   // R / 8 for R <= 32
+constexpr long long kWaitLimit = 1LL << 22;
+constexpr long long kDrainLimit = 1LL << 16;
+constexpr int kBarConsumers = 2;                  // named barrier of the consumer warps
+constexpr int kPersistMaxTok = 8;
+constexpr size_t kTensorMapBytes = 128;
+
+struct TmaPipe {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  unsigned fills[kMaxStages];   // fills issued per slot (producer)
+  float red[2][kCWarps][32 * 4];
+  int abort;
+};
+
+SV_DEV void tma_init(TmaPipe& tp) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&tp.full[i], 1);
+      mbar_init(&tp.empty[i], kCWarps);
+      tp.fills[i] = 0;
+    }
+    tp.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+}
+
+// Wait for the completion of the phase of `parity`; false once the CTA has
+// aborted (raising the flag when this wait is the one that gives up).
+SV_DEV bool tma_wait(uint64_t* bar, unsigned parity, TmaPipe& tp) {
+  volatile int* ab = &tp.abort;
+  long long spins = 0;
+  while (true) {
+    if (*ab) return false;
+    if (mbar_test(bar, parity)) return true;
+    if (++spins > kWaitLimit) {
+      *ab = 1;
+      return false;
+    }
+  }
+}
+
+struct TmaRange {
+  long long total, nc;
+  int u0, u1, kbpt;
+};
+
+SV_DEV TmaRange tma_range(const PhaseDesc& d) {
+  TmaRange r;
+  r.kbpt = (d.g.k + kTmaK - 1) / kTmaK;
+  r.total = (long long)d.groups * r.kbpt;
+  r.nc = max(1LL, min((long long)gridDim.x, r.total / kMinUnitsPerCta));
+  const bool has = blockIdx.x < r.nc;
+  r.u0 = has ? (int)first_step_of_warp(blockIdx.x, r.total, r.nc) : 0;
+  r.u1 = has ? (int)first_step_of_warp(blockIdx.x + 1, r.total, r.nc) : 0;
+  return r;
+}
+
+// Tensor-map index and first row of box A / box B of row group grp.
+struct GroupBoxes {
+  int ma, ra, mb, rb;
+};
+SV_DEV GroupBoxes group_boxes(const PhaseDesc& d, int grp) {
+  const GemmDesc& g = d.g;
+  const int R = d.R;
+  if (g.epi == kEpiQkvRope) {
+    const int per = g.hd / (2 * R);
+    int row = (grp / per) * g.hd + (grp % per) * R;
+    int seg = 0;
+    if (row >= g.seg_rows[0]) {
+      row -= g.seg_rows[0];
+      seg = 1;
+      if (row >= g.seg_rows[1]) {
+        row -= g.seg_rows[1];
+        seg = 2;
+      }
+    }
+    return {seg, row, seg, row + g.hd / 2};
+  }
+  if (g.epi == kEpiSwiglu) return {0, grp * R, 1, grp * R};
+  return {0, grp * 2 * R, 0, 0};   // one box of 2R rows
+}
+// Index of MMA tile t of group grp among the 16-row tiles of the matrix.
+SV_DEV int group_tile(const PhaseDesc& d, int grp, int t) {
+  const GemmDesc& g = d.g;
+  const int R = d.R;
+  if (g.epi == kEpiQkvRope) {
+    const int per = g.hd / (2 * R);
+    return (grp / per) * (g.hd / 16) + (grp % per) * (R / 8) + t;
+  }
+  return grp * (R / 8) + t;
+}
+
+// Producer thread: issue unit i of the CTA's range into slot i mod S --
+// wait for the consumers to release the slot, announce the bytes, copy the
+// weight boxes and, when with_x, the X box.
+SV_DEV void tma_issue(const PhaseDesc& d, const TmaRange& r, int i, bool with_x, TmaPipe& tp,
+                      unsigned char* ring, unsigned char* xreg, const unsigned char* maps) {
+  const int slot = i % d.stages;
+  const unsigned f = tp.fills[slot];
+  if (!tma_wait(&tp.empty[slot], (f & 1u) ^ 1u, tp)) return;
+  const int u = r.u0 + i;
+  const int grp = u / r.kbpt, kb = u - grp * r.kbpt;
+  const GroupBoxes b = group_boxes(d, grp);
+  const bool xg = d.xm == kXGlobal;
+  mbar_arrive_expect_tx(&tp.full[slot], (unsigned)d.stage_bytes + (xg ? (unsigned)kXStageBytes : 0u));
+  unsigned char* st = ring + (size_t)slot * d.stage_bytes;
+  const int kc = kb * kTmaK;
+  if (d.paired) {
+    tma_load_2d(st, maps + (size_t)d.tm[b.ma] * kTensorMapBytes, kc, b.ra, &tp.full[slot]);
+    tma_load_2d(st + (size_t)d.R * kTmaRowBytes, maps + (size_t)d.tm[b.mb] * kTensorMapBytes, kc, b.rb,
+                &tp.full[slot]);
+  } else {
+    tma_load_2d(st, maps + (size_t)d.tm[0] * kTensorMapBytes, kc, b.ra, &tp.full[slot]);
+  }
+  if (with_x)
+    tma_load_2d(xreg + (size_t)slot * kXStageBytes, maps + (size_t)d.tm[3] * kTensorMapBytes, kc, 0,
+                &tp.full[slot]);
+  tp.fills[slot] = f + 1;
+}
+
+// Producer thread: the X box of an already announced unit.
+SV_DEV void tma_issue_x(const PhaseDesc& d, const TmaRange& r, int i, TmaPipe& tp, unsigned char* xreg,
+                        const unsigned char* maps) {
+  if (tp.abort) return;
+  const int slot = i % d.stages;
+  const int u = r.u0 + i;
+  const int kb = u % r.kbpt;
+  tma_load_2d(xreg + (size_t)slot * kXStageBytes, maps + (size_t)d.tm[3] * kTensorMapBytes, kb * kTmaK, 0,
+              &tp.full[slot]);
+}
+
+// Producer thread, between arriving at the grid barrier that precedes GEMM
+// phase d and waiting on it: the weight boxes of its first units (weights
+// are read-only; X is not ready yet).  Returns how many units were issued.
+SV_DEV int tma_prefetch(const PhaseDesc& d, TmaPipe& tp, unsigned char* ring, unsigned char* xreg,
+                        const unsigned char* maps) {
+  const TmaRange r = tma_range(d);
+  const int npre = min(r.u1 - r.u0, d.stages);
+  for (int i = 0; i < npre; ++i) tma_issue(d, r, i, false, tp, ring, xreg, maps);
+  return npre;
+}
+
+// Producer thread during GEMM phase d: X boxes of the npre prefetched units,
+// then every remaining unit.
+SV_DEV void tma_produce(const PhaseDesc& d, int npre, TmaPipe& tp, unsigned char* ring, unsigned char* xreg,
+                        const unsigned char* maps) {
+  const TmaRange r = tma_range(d);
+  const int n = r.u1 - r.u0;
+  const bool xg = d.xm == kXGlobal;
+  fence_proxy_async_global();   // X was written by other CTAs before the grid barrier
+  if (xg)
+    for (int i = 0; i < npre; ++i) tma_issue_x(d, r, i, tp, xreg, maps);
+  for (int i = npre; i < n; ++i) tma_issue(d, r, i, xg, tp, ring, xreg, maps);
+}
+
+// Consumer warps at the end of a row group: the warps of MMA tile t add their
+// accumulators in warp order; warp t finishes the tile (epilogue, or CTA
+// partial and, for the last-arriving CTA, the reduction over CTAs in CTA
+// order).
+SV_DEV void tma_group_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs, int kbe, int pslot,
+                          const float (&acc)[4], int par, TmaPipe& tp, float* __restrict__ partials,
+                          int* __restrict__ tickets) {
+  const GemmDesc& g = d.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
+  const int T = d.R / 8;
+  float* buf = tp.red[par][0];
+  *reinterpret_cast<float4*>(buf + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  named_sync(kBarConsumers, kCWarps * 32);
+  if (warp >= T || tp.abort) return;
+  const int tile = group_tile(d, grp, warp);
+  if (tile >= gemm_tiles_of(g)) return;
+  float tot[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+  for (int w = warp; w < kCWarps; w += T) {
+    const float4 v = *reinterpret_cast<const float4*>(buf + (w * 32 + lane) * 4);
+    tot[0][0] += v.x;
+    tot[0][1] += v.y;
+    tot[0][2] += v.z;
+    tot[0][3] += v.w;
+  }
+  if (kbs == 0 && kbe == r.kbpt) {
+    gemm_epilogue<1>(g, tile, tot, gi, ci);
+    return;
+  }
+  float* mine = partials + (((size_t)blockIdx.x * 2 + pslot) * kMaxMmaTiles + warp) * 32 * 4;
+  *reinterpret_cast<float4*>(mine + (size_t)lane * 4) = make_float4(tot[0][0], tot[0][1], tot[0][2], tot[0][3]);
+  __threadfence();
+  __syncwarp();
+  const int cfirst = warp_of_step((long long)grp * r.kbpt, r.total, r.nc);
+  const int clast = warp_of_step((long long)(grp + 1) * r.kbpt - 1, r.total, r.nc);
+  int old = 0;
+  if (lane == 0) old = atomicAdd(&tickets[tile], 1);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old != clast - cfirst) return;
+  __threadfence();
+  float sum[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+  for (int c = cfirst; c <= clast; ++c) {
+    const int sl = (first_step_of_warp(c, r.total, r.nc) / r.kbpt == grp) ? 0 : 1;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+        partials + (((size_t)c * 2 + sl) * kMaxMmaTiles + warp) * 32 * 4 + (size_t)lane * 4));
+    sum[0][0] += v.x;
+    sum[0][1] += v.y;
+    sum[0][2] += v.z;
+    sum[0][3] += v.w;
+  }
+  gemm_epilogue<1>(g, tile, sum, gi, ci);
+  if (lane == 0) tickets[tile] = 0;
+}
+
+// Consumer warp during GEMM phase d.  cpar: per-slot parity of the next
+// completion of each stage's full barrier (identical in every consumer warp).
+template <int XM>
+SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const unsigned char* ring,
+                        const unsigned char* xreg, float* __restrict__ partials, int* __restrict__ tickets) {
+  const GemmDesc& g = d.g;
+  const TmaRange r = tma_range(d);
+  const int n = r.u1 - r.u0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
+  const uint4 zero4 = make_uint4(0, 0, 0, 0);
+  const int R = d.R, T = R / 8, S = d.stages, sb = d.stage_bytes;
+  const int t = warp % T;
+  const int arow = d.paired ? 8 * t + gi : 16 * t + gi;
+  const int brow = d.paired ? R + 8 * t + gi : 16 * t + 8 + gi;
+  const int s0 = warp / T, sstride = kCWarps / T, nsteps = kTmaSteps / sstride;
+  const bool has_tok = gi < g.ntok;
+  const int k = g.k;
+  const size_t xs_pitch = (size_t)(k + kXPad) * 2;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int par = 0, pslot = 0;
+  int kbs = n > 0 ? r.u0 % r.kbpt : 0;
+#pragma unroll 1
+  for (int i = 0; i < n; ++i) {
+    const int slot = i % S;
+    const bool ok = tma_wait(&tp.full[slot], (cpar >> slot) & 1u, tp);
+    cpar ^= 1u << slot;
+    const int u = r.u0 + i;
+    const int grp = u / r.kbpt, kb = u - grp * r.kbpt;
+    if (ok) {
+      const unsigned char* st = ring + (size_t)slot * sb + ci * 32;
+      for (int j = 0; j < nsteps; ++j) {
+        const int s = s0 + j * sstride;
+        const int kg = kb * kTmaK + s * kStepK;
+        if (kg >= k) break;
+        const unsigned char* ap = st + arow * kTmaRowBytes + s * (kStepK * 2);
+        const unsigned char* bp = st + brow * kTmaRowBytes + s * (kStepK * 2);
+        const uint4 a0 = *reinterpret_cast<const uint4*>(ap);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(ap + 16);
+        const uint4 b0 = *reinterpret_cast<const uint4*>(bp);
+        const uint4 b1 = *reinterpret_cast<const uint4*>(bp + 16);
+        uint4 x0 = zero4, x1 = zero4;
+        if (has_tok) {
+          const unsigned char* xp =
+              XM == kXSmem ? xreg + gi * xs_pitch + (size_t)(kg + ci * 16) * 2
+                           : xreg + (size_t)slot * kXStageBytes + gi * kTmaRowBytes + s * (kStepK * 2) + ci * 32;
+          x0 = *reinterpret_cast<const uint4*>(xp);
+          x1 = *reinterpret_cast<const uint4*>(xp + 16);
+        }
+        mma_bf16_16816(acc, a0.x, b0.x, a0.y, b0.y, x0.x, x0.y);
+        mma_bf16_16816(acc, a0.z, b0.z, a0.w, b0.w, x0.z, x0.w);
+        mma_bf16_16816(acc, a1.x, b1.x, a1.y, b1.y, x1.x, x1.y);
+        mma_bf16_16816(acc, a1.z, b1.z, a1.w, b1.w, x1.z, x1.w);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && ok) mbar_arrive(&tp.empty[slot]);
+    if (kb == r.kbpt - 1 || i == n - 1) {
+      tma_group_end(d, r, grp, kbs, kb + 1, pslot, acc, par, tp, partials, tickets);
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      par ^= 1;
+      pslot = 1;
+      kbs = 0;
+    }
+  }
+}
+
+// After an abort: wait (bounded) for the latest fill of every slot, so that
+// no copy lands after the CTA has left.  A fill whose bytes were never all
+// issued does not complete; its wait gives up after kDrainLimit probes.
+SV_DEV void tma_drain(TmaPipe& tp) {
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < kMaxStages; ++s) {
+    const unsigned f = tp.fills[s];
+    if (f == 0) continue;
+    long long spins = 0;
+    while (!mbar_test(&tp.full[s], (f - 1) & 1u) && ++spins < kDrainLimit) {
+    }
+  }
+}
+
+}  // namespace sv

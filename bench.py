@@ -206,38 +206,44 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- ours
 def phase_summary(ph):
-    """Fold per-phase stamps of one persistent pass: time per phase kind from
-    one release to the next, the spread of CTA arrivals (imbalance) and the
-    barrier latency (last arrival to release), and GB/s per GEMM shape."""
+    """Fold per-phase stamps of one persistent pass.  Per phase: total time
+    from the previous release to this one, split into prep (release -> latest
+    end of X preparation; attention: latest end of a key walk), stream (->
+    latest delivery of a CTA's last weight unit; attention: end of the items,
+    i.e. the merges), tail (-> latest arrival: reductions and epilogues) and
+    barrier (latest arrival -> release).  Summed per phase kind
+    and per GEMM shape (with its weight GB/s over the whole phase)."""
     kinds = {0: "embed", 1: "gemm", 2: "attn"}
     out = {"phases": len(ph), "total_us": 0.0, "by_kind": {}, "gemm_shapes": {}}
     prev = 0
-    for i, p in enumerate(ph):
+    for p in ph:
         end = p["release_ns"] if p["release_ns"] >= 0 else p["arrive_max_ns"]
-        dur = (end - prev) / 1e3
-        spread = (p["arrive_max_ns"] - p["arrive_min_ns"]) / 1e3
-        bar = (p["release_ns"] - p["arrive_max_ns"]) / 1e3 if p["release_ns"] >= 0 else 0.0
+        prep_end = p["prep_max_ns"] if p["prep_max_ns"] >= 0 else prev
+        work_end = p["work_max_ns"] if p["work_max_ns"] >= 0 else prep_end
+        parts = {"us": (end - prev) / 1e3, "prep_us": (prep_end - prev) / 1e3,
+                 "stream_us": (work_end - prep_end) / 1e3, "tail_us": (p["arrive_max_ns"] - work_end) / 1e3,
+                 "barrier_us": ((p["release_ns"] - p["arrive_max_ns"]) / 1e3) if p["release_ns"] >= 0 else 0.0}
         k = kinds.get(p["kind"], str(p["kind"]))
-        agg = out["by_kind"].setdefault(k, {"count": 0, "us": 0.0, "spread_us": 0.0, "barrier_us": 0.0})
+        agg = out["by_kind"].setdefault(k, {"count": 0})
         agg["count"] += 1
-        agg["us"] += dur
-        agg["spread_us"] += spread
-        agg["barrier_us"] += bar
+        for f, v in parts.items():
+            agg[f] = agg.get(f, 0.0) + v
         if p["kind"] == 1:
             key = f'{p["n"]}x{p["k"]}'
-            g = out["gemm_shapes"].setdefault(key, {"count": 0, "us": 0.0})
+            g = out["gemm_shapes"].setdefault(key, {"count": 0})
             g["count"] += 1
-            g["us"] += dur
+            for f, v in parts.items():
+                g[f] = g.get(f, 0.0) + v
         prev = end
-    out["total_us"] = prev / 1e3
+    out["total_us"] = round(prev / 1e3, 1)
     for key, g in out["gemm_shapes"].items():
         n, k = (int(v) for v in key.split("x"))
         g["gbs"] = round(g["count"] * n * k * 2 / (g["us"] * 1e3), 1)
-        g["us"] = round(g["us"], 1)
-    for agg in out["by_kind"].values():
-        for f in ("us", "spread_us", "barrier_us"):
-            agg[f] = round(agg[f], 1)
-    out["total_us"] = round(out["total_us"], 1)
+    for table in (out["by_kind"], out["gemm_shapes"]):
+        for agg in table.values():
+            for f in list(agg):
+                if f.endswith("_us") or f == "us":
+                    agg[f] = round(agg[f] / agg["count"], 2)   # per phase
     return out
 
 

@@ -271,15 +271,18 @@ SPEC_API int spec_profile(spec_ctx* ctx, int iters, spec_profile_t* out);
 /* Per-phase timing of the last run of one persistent forward pass
  * (context created with SPEC_OPT_PHASE_TIMES on the persistent path).
  * which: 0..K-1 the K draft passes of a step, K the verify pass, K+1 the
- * plain-decoding pass.  Writes *nphases and, per phase i, six int64 at
- * out[6 i ..]: kind (0 embedding, 1 GEMM, 2 attention), rows n (GEMM) or
+ * plain-decoding pass.  Writes *nphases and, per phase i, eight int64 at
+ * out[8 i ..]: kind (0 embedding, 1 GEMM, 2 attention), rows n (GEMM) or
  * query heads (attention) or tokens (embedding), k (GEMM) or tokens
- * (attention), then three %globaltimer offsets in ns from CTA 0's start:
- * the earliest and the latest CTA's arrival at the end of the phase and
- * CTA 0's release from the grid barrier after it (-1 for the last phase).
- * out holds max_phases * 6 int64 (host).  Synchronises the context's stream.
- * Errors: SPEC_E_STATE without the option or the persistent path,
- * SPEC_E_ARG when max_phases is too small (after setting *nphases). */
+ * (attention), then %globaltimer offsets in ns from CTA 0's start: the
+ * earliest and the latest CTA's arrival at the end of the phase, CTA 0's
+ * release from the grid barrier after it (-1 for the last phase), the latest
+ * CTA's end of X preparation (GEMM) or end of its key walk (attention),
+ * and the latest CTA's delivery of its last weight unit (GEMM) or end of
+ * its items (attention); -1 where a stamp was not taken.  out holds max_phases * 8
+ * int64 (host).  Synchronises the context's stream.  Errors: SPEC_E_STATE
+ * without the option or the persistent path, SPEC_E_ARG when max_phases is
+ * too small (after setting *nphases). */
 SPEC_API int spec_phase_times(spec_ctx* ctx, int which, int64_t* out, int max_phases, int* nphases);
 
 /* Library version string. */

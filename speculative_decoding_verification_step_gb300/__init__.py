@@ -227,13 +227,15 @@ class SpecDecoder:
     def phase_times(self, which):
         """Per-phase stamps of the last persistent run of forward `which`
         (0..K-1 draft passes, K verify, K+1 plain decoding): a list of dicts
-        with kind, n, k and the earliest/latest arrival and release in ns."""
+        with kind, n, k, the earliest/latest arrival, the release, the latest
+        end of X preparation and the latest end of streaming, in ns."""
         import numpy as np
-        buf = np.zeros((1024, 6), dtype=np.int64)
+        buf = np.zeros((1024, 8), dtype=np.int64)
         n = ctypes.c_int(0)
         _check(lib().spec_phase_times(self.ctx, which, buf.ctypes.data_as(_VP), 1024,
                                       ctypes.byref(n)), self.ctx)
-        names = ("kind", "n", "k", "arrive_min_ns", "arrive_max_ns", "release_ns")
+        names = ("kind", "n", "k", "arrive_min_ns", "arrive_max_ns", "release_ns", "prep_max_ns",
+                 "work_max_ns")
         return [dict(zip(names, (int(v) for v in row))) for row in buf[:n.value]]
 
     def last_step_debug(self, max_ctx):

@@ -124,6 +124,24 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 // ---------------------------------------------------------------------------
+// GPU-scope atomics with explicit ordering (cheaper than a full fence plus a
+// relaxed atomic).  An acq_rel add publishes the calling thread's earlier
+// writes (and, through a preceding CTA or warp barrier, those of its peers)
+// and makes the writes published by earlier adders visible to it.
+// ---------------------------------------------------------------------------
+SV_DEV unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+SV_DEV void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+SV_DEV void st_relaxed_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Asynchronous bulk copies and shared-memory barriers (sm_90 and later).
 // A transaction barrier completes its phase when its expected arrivals have
 // arrived and the bytes announced with expect_tx have landed.
@@ -137,6 +155,9 @@ SV_DEV void mbar_init(uint64_t* bar, unsigned count) {
 SV_DEV void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
+}
+SV_DEV void mbar_arrive_count(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 SV_DEV void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");

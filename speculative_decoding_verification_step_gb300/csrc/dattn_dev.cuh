@@ -17,9 +17,11 @@
 // of the arithmetic is fixed by the row's position alone, so a row gets the
 // same bits whichever rows share the pass (batch invariance).
 //
-// Memory: per warp two 16-key K/V buffers (cp.async, rows padded by 16 bytes
-// so the fragment loads and ldmatrix rows hit distinct banks) and a 16x8
-// probability tile; the warp merge reuses the same space.
+// Memory: per warp a pipeline of 3 (head dim 128) or 6 stages of 16-key K/V
+// tiles, each filled by 2-D tensor copies (hardware-swizzled so the fragment
+// loads and ldmatrix rows hit distinct banks) issued by the warp's lane 0 and
+// completing on the stage's barrier, and a 16x8 probability tile; the warp
+// merge reuses the same space.
 #pragma once
 #include "common.cuh"
 #include "kernels.h"
@@ -33,14 +35,32 @@ constexpr int kDRows = 8;                          // rows per item (MMA n)
 
 template <int HD>
 struct DAttnSmem {
-  static constexpr int kPitch = HD + 8;            // bf16 elements per buffered key row
-  static constexpr int kBufElems = kDStepKeys * kPitch;
-  // per warp: K[2], V[2] buffers, then the probability tile [8 rows][16 keys]
-  static constexpr size_t kWarpBytes = (size_t)4 * kBufElems * 2 + kDRows * kDStepKeys * 2;
+  // per warp: kDepth stages of a 16-key K tile and V tile, each tile written
+  // by 2-D tensor copies of 16 keys x kBoxCols dims with the hardware 128-byte
+  // (64-byte for head dim 32) swizzle, then the probability tile
+  // [8 rows][16 keys]; warp regions stay 1 KB aligned (swizzle atoms)
+  static constexpr int kDepth = HD >= 128 ? 3 : 6;
+  static constexpr int kTileElems = kDStepKeys * HD;
+  static constexpr int kTileBytes = kTileElems * 2;
+  static constexpr int kBoxCols = HD < 64 ? HD : 64;
+  static constexpr int kBoxes = HD / kBoxCols;
+  static constexpr size_t kWarpRaw = (size_t)kDepth * 2 * kTileBytes + kDRows * kDStepKeys * 2;
+  static constexpr size_t kWarpBytes = (kWarpRaw + 1023) / 1024 * 1024;
   // merge area: m, l [8 warps][8 rows], o [8 warps][8 rows][HD] (fp32)
   static constexpr size_t kMergeBytes = (size_t)kDWarps * kDRows * (2 + HD) * 4;
   static constexpr size_t kBytes = kDWarps * kWarpBytes > kMergeBytes ? kDWarps * kWarpBytes : kMergeBytes;
+  // element offset of logical 16-byte chunk c of key row r in a tile: box
+  // c / 8 (64 dims), row r, chunk (c mod 8) XOR (r mod 8) -- the tensor
+  // copy's 128-byte swizzle; for head dim 32, (c XOR (r / 2 mod 4)) in 64-byte
+  // rows -- the 64-byte swizzle.  Eight consecutive rows read at one logical
+  // chunk land in eight distinct bank groups.
+  static __device__ __forceinline__ int at(int r, int c) {
+    if (HD >= 64) return (c >> 3) * (kDStepKeys * 64) + r * 64 + (((c & 7) ^ (r & 7)) << 3);
+    return r * HD + ((c ^ ((r >> 1) & 3)) << 3);
+  }
 };
+constexpr int kDMaxDepth = 6;
+constexpr long long kDWaitLimit = 1LL << 22;
 
 SV_DEV void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -72,29 +92,47 @@ __host__ __device__ inline int dattn_items(int ntok, int hq, int hkv, int cap) {
   return dattn_splits(cap) * ntok * hkv * dattn_hgroups(hq, hkv);
 }
 
-// Issue the cp.async copies of K/V step s (keys 16s .. 16s+15, those above
-// `last` zero-filled) into one buffer pair of the warp.
+// Lane 0: the tensor copies of K/V step s (keys 16s .. 16s+15 of the rows
+// of KV head row0 / cap; keys beyond the row's position are masked later,
+// rows past the cache read as zero) into one stage, completing on bar.
 template <int HD>
-SV_DEV void dattn_fetch(const bf16* kc, const bf16* vc, int s, int last, bf16* kb, bf16* vb) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kVecPerRow = HD / 8;               // 16-byte vectors per key row
-  constexpr int kVecs = kDStepKeys * kVecPerRow;
+SV_DEV void dattn_fetch(const AttnDesc& a, int row0, int s, bf16* kt, bf16* vt, uint64_t* bar) {
+  using L = DAttnSmem<HD>;
+  mbar_arrive_expect_tx(bar, 2u * L::kTileBytes);
+  const int r = row0 + s * kDStepKeys;
 #pragma unroll
-  for (int i = lane; i < kVecs; i += 32) {
-    const int key = i / kVecPerRow, v = i % kVecPerRow;
-    const int abs_key = s * kDStepKeys + key;
-    const bool ok = abs_key <= last;
-    const size_t src = (size_t)(ok ? abs_key : 0) * HD + v * 8;
-    cp_async16(kb + key * DAttnSmem<HD>::kPitch + v * 8, kc + src, ok);
-    cp_async16(vb + key * DAttnSmem<HD>::kPitch + v * 8, vc + src, ok);
+  for (int b = 0; b < L::kBoxes; ++b) {
+    tma_load_2d(kt + b * kDStepKeys * L::kBoxCols, a.tmk, b * L::kBoxCols, r, bar);
+    tma_load_2d(vt + b * kDStepKeys * L::kBoxCols, a.tmv, b * L::kBoxCols, r, bar);
   }
-  cp_async_commit();
 }
 
-// One item; called by the eight consumer warps (threads 0..255) of the CTA.
-// sm: dynamic shared memory (DAttnSmem<HD>::kBytes); s_last: shared int.
+// Bounded wait on a stage barrier; false (after raising *a.err) on timeout.
+SV_DEV bool dattn_wait(const AttnDesc& a, uint64_t* bar, unsigned parity) {
+  long long spins = 0;
+  while (!mbar_test(bar, parity)) {
+    if (++spins > kDWaitLimit) {
+      if (a.err) atomicExch(a.err, 1);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Stage barriers of the eight warps (kDMaxDepth each), initialised once per
+// kernel by thread 0 before any item; dpar: per-warp parity bitmask of the
+// next completion of each stage, carried from item to item.
+SV_DEV void dattn_init_bars(uint64_t* bars) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDWarps * kDMaxDepth; ++i) mbar_init(&bars[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+}
+
+// stamp (optional): atomicMax of the globaltimer when the key walk ended.
 template <int HD>
-SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last) {
+SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
+                       unsigned& dpar, unsigned long long* stamp = nullptr) {
   using L = DAttnSmem<HD>;
   const int hgroups = dattn_hgroups(a.hq, a.hkv);
   const DItem d = dattn_item_of(a, it, hgroups);
@@ -107,8 +145,8 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
   const int nsplit = pos / kDSplitKeys + 1;           // splits of this row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
   const int h0 = d.kvh * G + d.hg * kDRows;           // first query head of the item
-  const bf16* kc = (const bf16*)a.kc + (size_t)d.kvh * a.cap * HD;
-  const bf16* vc = (const bf16*)a.vc + (size_t)d.kvh * a.cap * HD;
+  const int row0 = d.kvh * a.cap;                     // first cache row of the KV head
+  uint64_t* wbar = bars + warp * kDMaxDepth;
 
   // Q fragments (rows = query heads; dims in groups of GD, k-permuted as in
   // the GEMM): thread (g, c) holds row g, dims j*GD + c*GD/4 .. +GD/4-1 of
@@ -130,45 +168,64 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     }
   }
 
-  // buffer b of the warp: K at wb + b * kBufElems, V at wb + (2 + b) * kBufElems
+  // stage b of the warp: K tile at wb + 2b * kTileElems, V tile after it
+  constexpr int D = L::kDepth;
   bf16* wb = reinterpret_cast<bf16*>(sm + (size_t)warp * L::kWarpBytes);
-  bf16* ps = wb + 4 * L::kBufElems;                   // [8 rows][16 keys]
+  bf16* ps = wb + 2 * D * L::kTileElems;              // [8 rows][16 keys]
 
-  // this warp's steps: s = s_begin + warp + 8j, s <= s_end
+  // this warp's steps: s = first + 8j, j < nst, kept D steps ahead in flight
   const int s_begin = k0 / kDStepKeys, s_end = last / kDStepKeys;
+  const int first = s_begin + warp;
+  const int nst = first <= s_end ? (s_end - first) / kDWarps + 1 : 0;
   float m_r[2] = {neg_inf(), neg_inf()}, l_r[2] = {0.f, 0.f};   // rows 2c, 2c+1
   float o[HD / 16][4];
 #pragma unroll
   for (int mt = 0; mt < HD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   const bool rv0 = 2 * ci < rows, rv1 = 2 * ci + 1 < rows;
-  int s = s_begin + warp;
-  if (s <= s_end) dattn_fetch<HD>(kc, vc, s, last, wb, wb + 2 * L::kBufElems);
-  int buf = 0;
-  for (; s <= s_end; s += kDWarps, buf ^= 1) {
-    const int sn = s + kDWarps;
-    if (sn <= s_end) {
-      dattn_fetch<HD>(kc, vc, sn, last, wb + (buf ^ 1) * L::kBufElems, wb + (3 - buf) * L::kBufElems);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  if (lane == 0)
+    for (int j = 0; j < D && j < nst; ++j)
+      dattn_fetch<HD>(a, row0, first + kDWarps * j, wb + 2 * j * L::kTileElems, wb + (2 * j + 1) * L::kTileElems,
+                      &wbar[j]);
+  // per-lane element offsets of the fragments (fixed for the whole walk)
+  int koff_lo[NG][TW / 4], koff_hi[NG][TW / 4], voff[HD / 16];
+#pragma unroll
+  for (int jg = 0; jg < NG; ++jg)
+#pragma unroll
+    for (int e = 0; e < TW / 4; ++e) {
+      const int c = jg * (GD / 8) + ci * (GD / 32) + e;   // logical 16-byte chunk
+      koff_lo[jg][e] = L::at(gi, c);
+      koff_hi[jg][e] = L::at(gi + 8, c);
     }
-    __syncwarp();
+  {
+    const int lrow = (lane & 7) + ((lane >> 4) << 3);   // key of this lane's ldmatrix row
+    const int lchk = (lane >> 3) & 1;                   // 8-dim half of a 16-dim tile
+#pragma unroll
+    for (int mt = 0; mt < HD / 16; ++mt) voff[mt] = L::at(lrow, 2 * mt + lchk);
+  }
+  bool live = true;
+  for (int j = 0; j < nst; ++j) {
+    const int s = first + kDWarps * j;
+    const int buf = j % D;
+    const bf16* kt = wb + 2 * buf * L::kTileElems;
+    const bf16* vt = kt + L::kTileElems;
+    live = __all_sync(0xffffffffu, live && dattn_wait(a, &wbar[buf], (dpar >> buf) & 1u));
+    dpar ^= 1u << buf;
+    if (!live) continue;   // timed out: the rows of this item are not computed
     // scores: D[key g / g+8][row 2c / 2c+1]
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    const bf16* kr = wb + buf * L::kBufElems + gi * L::kPitch + ci * (GD / 4);
 #pragma unroll
-    for (int j = 0; j < NG; ++j) {
+    for (int jg = 0; jg < NG; ++jg) {
       uint32_t lo[TW], hi[TW];   // key rows g and g+8
 #pragma unroll
       for (int e = 0; e < TW / 4; ++e) {
-        const uint4 x = *reinterpret_cast<const uint4*>(kr + j * GD + 8 * e);
-        const uint4 y = *reinterpret_cast<const uint4*>(kr + 8 * L::kPitch + j * GD + 8 * e);
+        const uint4 x = *reinterpret_cast<const uint4*>(kt + koff_lo[jg][e]);
+        const uint4 y = *reinterpret_cast<const uint4*>(kt + koff_hi[jg][e]);
         lo[4 * e] = x.x; lo[4 * e + 1] = x.y; lo[4 * e + 2] = x.z; lo[4 * e + 3] = x.w;
         hi[4 * e] = y.x; hi[4 * e + 1] = y.y; hi[4 * e + 2] = y.z; hi[4 * e + 3] = y.w;
       }
 #pragma unroll
       for (int i = 0; i < NM; ++i)
-        mma_bf16_16816(sc, lo[2 * i], hi[2 * i], lo[2 * i + 1], hi[2 * i + 1], qf[j][2 * i], qf[j][2 * i + 1]);
+        mma_bf16_16816(sc, lo[2 * i], hi[2 * i], lo[2 * i + 1], hi[2 * i + 1], qf[jg][2 * i], qf[jg][2 * i + 1]);
     }
     const int key_lo = s * kDStepKeys + gi, key_hi = key_lo + 8;
     const bool kv_lo = key_lo <= last, kv_hi = key_hi <= last;
@@ -213,25 +270,39 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(ps + gi * kDStepKeys + 2 * ci);
     const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(ps + gi * kDStepKeys + 2 * ci + 8);
     // o^T[dim][row] = o^T * scale + V^T p: A = V^T via transposing ldmatrix
-    const int lrow = (lane & 7) + ((lane >> 4) << 3);   // key of this lane's row address
-    const int lcol = ((lane >> 3) & 1) * 8;             // dim offset within the 16-dim tile
-    const bf16* vr = wb + (2 + buf) * L::kBufElems + lrow * L::kPitch + lcol;
 #pragma unroll
     for (int mt = 0; mt < HD / 16; ++mt) {
       uint32_t va[4];
-      ldmatrix_x4_trans(va, vr + mt * 16);
+      ldmatrix_x4_trans(va, vt + voff[mt]);
       o[mt][0] *= sc0;
       o[mt][1] *= sc1;
       o[mt][2] *= sc0;
       o[mt][3] *= sc1;
       mma_bf16_16816(o[mt], va[0], va[1], va[2], va[3], pb0, pb1);
     }
-    __syncwarp();   // buffers and the probability tile are reused by the next step
+    __syncwarp();   // the stage and the probability tile are reused
+    if (lane == 0 && j + D < nst) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // our reads before the copy's writes
+      dattn_fetch<HD>(a, row0, s + kDWarps * D, wb + 2 * buf * L::kTileElems, wb + (2 * buf + 1) * L::kTileElems,
+                      &wbar[buf]);
+    }
   }
-  cp_async_wait<0>();
+  // after a timeout: let the copies still in flight land before the space is reused
+  if (!live && lane == 0)
+    for (int j = nst - D > 0 ? nst - D : 0; j < nst; ++j) {
+      long long spins = 0;
+      while (!mbar_test(&wbar[j % D], ((dpar >> (j % D)) & 1u) ^ 1u) && ++spins < (1LL << 16)) {
+      }
+    }
+  __syncwarp();
 
   // ---- merge the eight warps (warp order) ----
   named_sync(1, kDWarps * 32);   // every warp is done with its buffers
+  if (stamp && threadIdx.x == 0) {
+    unsigned long long tm;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(tm));
+    atomicMax(stamp, tm);
+  }
   float* mm = reinterpret_cast<float*>(sm);          // [8 warps][8 rows]
   float* ll = mm + kDWarps * kDRows;                 // [8 warps][8 rows]
   float* oo = ll + kDWarps * kDRows;                 // [8 warps][8 rows][HD]
@@ -283,13 +354,10 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
   // ---- several splits: the last one to finish merges them in split order ----
   int* ticket = a.tickets + ((size_t)d.t * a.hkv + d.kvh) * hgroups + d.hg;
   named_sync(1, kDWarps * 32);
-  if (tid == 0) {
-    __threadfence();
-    *s_last = (atomicAdd(ticket, 1) == nsplit - 1);
-  }
+  if (tid == 0)   // acq_rel: publishes this split's partial, acquires the earlier ones
+    *s_last = (atom_add_acq_rel_gpu(reinterpret_cast<unsigned*>(ticket), 1u) == (unsigned)nsplit - 1);
   named_sync(1, kDWarps * 32);
   if (!*s_last) return;
-  __threadfence();
   const int ns = dattn_splits(a.cap);
   for (int e = tid; e < rows * HD; e += kDWarps * 32) {
     const int r = e / HD, dm = e % HD;

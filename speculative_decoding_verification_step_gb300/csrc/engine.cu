@@ -42,6 +42,7 @@ struct ModelState {
   void* vc = nullptr;
   float* rope_cos = nullptr;
   float* rope_sin = nullptr;
+  TensorMap128* kv_maps = nullptr;   // bf16: [layer][K, V] tensor maps of the cache
   int esize = 4;
   int qkv_rows() const { return (d.n_heads + 2 * d.n_kv_heads) * d.head_dim; }
   size_t layer_kv_elems(int cap) const { return (size_t)d.n_kv_heads * cap * d.head_dim; }
@@ -95,6 +96,7 @@ struct spec_ctx {
   void* attn = nullptr;
   float* attn_part = nullptr;
   int* attn_tick = nullptr;
+  int* dattn_tick = nullptr;       // tensor-core attention (bf16 models)
   float* ss = nullptr;         // [d_max/16][kGemmMaxTok] per-tile sums of squares
   float* logits_p = nullptr;  // [K+1][V]
   float* logits_q = nullptr;  // [K][V]
@@ -276,6 +278,11 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     a.ntok = ntok; a.hq = hq; a.hkv = hkv; a.hd = hd; a.cap = c->cap;
     a.max_chunks = c->max_chunks; a.dtype = dt;
     a.scale = 1.0f / sqrtf((float)hd);
+    if (m.kv_maps) {
+      a.tmk = m.kv_maps + 2 * l;
+      a.tmv = m.kv_maps + 2 * l + 1;
+    }
+    a.err = c->result + (2 * c->K + 3);
     ops.push_back(at);
     Op o{};
     o.kind = kPhaseGemm;
@@ -320,7 +327,15 @@ void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const 
       forward_ops(c, m, ntok, tok_base, tok_idx, tok_off, pos_idx, pos_off, lrow0, lrows, logits);
   for (const Op& op : ops) {
     if (op.kind == kPhaseEmbed) L.note(launch_embed(op.e, c->stream));
-    else if (op.kind == kPhaseAttn) L.note(launch_attention(op.a, c->stream));
+    else if (op.kind == kPhaseAttn) {
+      if (m.d.dtype == SPEC_DTYPE_BF16) {   // same attention arithmetic as the persistent kernel
+        AttnDesc a = op.a;
+        a.tickets = c->dattn_tick;
+        L.note(launch_dattn(a, c->stream));
+      } else {
+        L.note(launch_attention(op.a, c->stream));
+      }
+    }
     else gemm(L, op.g, m.d.dtype);
   }
 }
@@ -331,8 +346,8 @@ void forward_persist(Launch& L, int which) {
   spec_ctx* c = L.c;
   const PersistFwd& f = c->pforward[which];
   if (f.desc.times)
-    L.note(cudaMemsetAsync(f.desc.times, 0, sizeof(unsigned long long) * (1 + 3 * f.desc.nphases),
-                           c->stream));
+    L.note(cudaMemsetAsync(f.desc.times, 0,
+                           sizeof(unsigned long long) * (1 + (size_t)kPhaseStamps * f.desc.nphases), c->stream));
   L.note(launch_persist(f.desc, f.hd, f.smem, c->num_sms, c->stream));
 }
 
@@ -486,9 +501,9 @@ void free_ctx(spec_ctx* c) {
 // barrier state so that the context stays usable, and report the timeout.
 int persist_timeout(spec_ctx* c) {
   cudaMemsetAsync(c->result + (2 * c->K + 3), 0, sizeof(int32_t), c->stream);
-  cudaMemsetAsync(c->bar, 0, sizeof(unsigned) * 4, c->stream);
+  if (c->bar) cudaMemsetAsync(c->bar, 0, sizeof(unsigned) * 4, c->stream);
   cudaStreamSynchronize(c->stream);
-  return fail(c, SPEC_E_TIMEOUT, "a grid barrier of the persistent forward kernel timed out");
+  return fail(c, SPEC_E_TIMEOUT, "a bounded wait of a forward kernel (grid barrier or copy) timed out");
 }
 
 int set_eager_pos(spec_ctx* c, int pos) {
@@ -593,6 +608,10 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     const size_t nt = (size_t)hkvmax * rt;
     INIT_TRY(dalloc(c, &c->attn_tick, sizeof(int) * nt));
     INIT_TRY(cudaMemset(c->attn_tick, 0, sizeof(int) * nt));
+    const int dnt = std::max(dattn_tickets(maxN, c->tgt.d.n_heads, c->tgt.d.n_kv_heads),
+                             dattn_tickets(maxN, c->drf.d.n_heads, c->drf.d.n_kv_heads));
+    INIT_TRY(dalloc(c, &c->dattn_tick, sizeof(int) * dnt));
+    INIT_TRY(cudaMemset(c->dattn_tick, 0, sizeof(int) * dnt));
   }
   INIT_TRY(dalloc(c, &c->logits_p, sizeof(float) * (size_t)(K + 1) * V));
   INIT_TRY(dalloc(c, &c->logits_q, sizeof(float) * (size_t)K * V));
@@ -622,6 +641,22 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     INIT_TRY(dalloc(c, &m->rope_sin, tb));
     INIT_TRY(launch_rope_table(m->rope_cos, m->rope_sin, c->cap, m->d.head_dim,
                                (double)m->d.rope_theta, c->stream));
+    if (m->d.dtype == SPEC_DTYPE_BF16) {   // tensor maps of every layer's K and V cache
+      std::vector<TensorMap128> maps(2 * (size_t)m->d.n_layers);
+      const long long rows = (long long)m->d.n_kv_heads * c->cap;
+      bool ok = true;
+      for (int l = 0; l < m->d.n_layers && ok; ++l) {
+        const size_t off = (size_t)l * m->layer_kv_elems(c->cap) * m->esize;
+        ok = encode_kv_map(maps[2 * l], (char*)m->kc + off, m->d.head_dim, rows) &&
+             encode_kv_map(maps[2 * l + 1], (char*)m->vc + off, m->d.head_dim, rows);
+      }
+      if (!ok) {
+        free_ctx(c);
+        return fail(nullptr, SPEC_E_CUDA, "could not encode the KV-cache tensor maps");
+      }
+      INIT_TRY(dalloc(c, &m->kv_maps, sizeof(TensorMap128) * maps.size()));
+      INIT_TRY(cudaMemcpy(m->kv_maps, maps.data(), sizeof(TensorMap128) * maps.size(), cudaMemcpyHostToDevice));
+    }
   }
   INIT_TRY(cudaMemset(c->result, 0, sizeof(int32_t) * (2 * K + 8)));
   // Persistent forward kernels: both models bf16, and the weight ring plus
@@ -641,13 +676,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
       for (const spec_model_desc* m : {target, draft})
         encodable = encodable && persist_attn_partial_floats(K + 1, m->n_heads, m->head_dim, c->cap) <=
                                      attn_partial_floats(maxN, (int)hqmax, (int)hdmax, c->max_chunks);
-      int* dattn_tick = nullptr;
-      {
-        const int nt = std::max(persist_attn_tickets(K + 1, target->n_heads, target->n_kv_heads),
-                                persist_attn_tickets(K + 1, draft->n_heads, draft->n_kv_heads));
-        INIT_TRY(dalloc(c, &dattn_tick, sizeof(int) * nt));
-        INIT_TRY(cudaMemset(dattn_tick, 0, sizeof(int) * nt));
-      }
+      int* const dattn_tick = c->dattn_tick;   // sized for kGemmMaxTok >= K + 1 tokens
       auto add = [&](int idx, const std::vector<Op>& ops) {
         start[idx] = all.size();
         for (const Op& op : ops) {
@@ -688,14 +717,14 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
         INIT_TRY(cudaMemset(c->bar, 0, sizeof(unsigned) * 4));
         unsigned long long* times = nullptr;
         if (opts->flags & SPEC_OPT_PHASE_TIMES) {
-          const size_t words = (size_t)(K + 4) + 3 * all.size();   // 1 + 3 phases per forward
+          const size_t words = (size_t)(K + 4) + (size_t)kPhaseStamps * all.size();
           INIT_TRY(dalloc(c, &times, sizeof(unsigned long long) * words));
           INIT_TRY(cudaMemset(times, 0, sizeof(unsigned long long) * words));
         }
         for (int f = 0; f <= K + 3; ++f) {
           PersistFwd& pf = c->pforward[f];
           pf.host.assign(all.begin() + start[f], all.begin() + start[f] + count[f]);
-          if (times) pf.desc.times = times + f + 3 * start[f];
+          if (times) pf.desc.times = times + f + (size_t)kPhaseStamps * start[f];
           pf.desc.phases = c->phase_dev + start[f];
           pf.desc.nphases = (int)count[f];
           pf.desc.tmaps = tmaps_dev;
@@ -767,11 +796,11 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
     forward_persist(Lc, K + 2);
     forward_persist(Lc, K + 3);
     CUDA_TRY(c, Lc.e);
-    CUDA_TRY(c, cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 4), cudaMemcpyDeviceToHost,
-                                c->stream));
   }
+  CUDA_TRY(c, cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 4), cudaMemcpyDeviceToHost,
+                              c->stream));
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  if (c->persist && c->h_result[2 * K + 3]) return persist_timeout(c);
+  if (c->h_result[2 * K + 3]) return persist_timeout(c);
   c->host_L = L - 1;
   c->prefilled = true;
   c->draft_stale = false;
@@ -792,7 +821,7 @@ int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* ou
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   const int32_t* h = c->h_result;
-  if (c->persist && h[2 * K + 3]) return persist_timeout(c);
+  if (h[2 * K + 3]) return persist_timeout(c);
   const int cnt = h[K + 1];
   if (cnt < 1 || cnt > K + 1) return fail(c, SPEC_E_CUDA, "acceptance kernel returned an invalid count");
   for (int i = 0; i < cnt; ++i) out_tokens[i] = h[i];
@@ -838,7 +867,7 @@ int spec_ar_step(spec_ctx* c, int32_t* out_token) {
   int rc = run_captured(c, &c->ar_exec, enqueue_ar, &c->kernels_ar);
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  if (c->persist && c->h_result[2 * c->K + 3]) return persist_timeout(c);
+  if (c->h_result[2 * c->K + 3]) return persist_timeout(c);
   *out_token = c->h_result[0];
   c->host_L += 1;
   c->ar_steps++;
@@ -916,7 +945,7 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
-  if (c->persist) {
+  {
     int32_t flag = 0;
     CUDA_TRY(c, cudaMemcpy(&flag, c->result + (2 * c->K + 3), sizeof flag, cudaMemcpyDeviceToHost));
     if (flag) return persist_timeout(c);
@@ -940,7 +969,7 @@ int spec_phase_times(spec_ctx* c, int which, int64_t* out, int max_phases, int* 
   const int n = f.desc.nphases;
   *nphases = n;
   if (max_phases < n) return fail(c, SPEC_E_ARG, "max_phases below the number of phases");
-  std::vector<unsigned long long> t(1 + 3 * (size_t)n);
+  std::vector<unsigned long long> t(1 + (size_t)kPhaseStamps * n);
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   CUDA_TRY(c, cudaMemcpy(t.data(), f.desc.times, sizeof(unsigned long long) * t.size(),
                          cudaMemcpyDeviceToHost));
@@ -948,13 +977,16 @@ int spec_phase_times(spec_ctx* c, int which, int64_t* out, int max_phases, int* 
   auto rel = [&](unsigned long long v) { return v ? (int64_t)(v - t0) : (int64_t)-1; };
   for (int i = 0; i < n; ++i) {
     const PhaseDesc& d = f.host[i];
-    int64_t* o = out + 6 * (size_t)i;
+    const unsigned long long* st = t.data() + 1 + (size_t)kPhaseStamps * i;
+    int64_t* o = out + 8 * (size_t)i;
     o[0] = d.kind;
     o[1] = d.kind == kPhaseGemm ? d.g.n : d.kind == kPhaseAttn ? d.a.hq : d.e.ntok;
     o[2] = d.kind == kPhaseGemm ? d.g.k : d.kind == kPhaseAttn ? d.a.ntok : 0;
-    o[3] = t[1 + 3 * i] ? rel(~t[1 + 3 * i]) : -1;
-    o[4] = rel(t[2 + 3 * i]);
-    o[5] = rel(t[3 + 3 * i]);
+    o[3] = st[0] ? rel(~st[0]) : -1;
+    o[4] = rel(st[1]);
+    o[5] = rel(st[2]);
+    o[6] = rel(st[3]);
+    o[7] = rel(st[4]);
   }
   return SPEC_OK;
 }
@@ -981,6 +1013,9 @@ int spec_model_forward(spec_ctx* c, int which, const int32_t* tokens, int n, int
     CUDA_TRY(c, L.e);
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   }
+  int32_t flag = 0;
+  CUDA_TRY(c, cudaMemcpy(&flag, c->result + (2 * c->K + 3), sizeof flag, cudaMemcpyDeviceToHost));
+  if (flag) return persist_timeout(c);
   return SPEC_OK;
 }
 

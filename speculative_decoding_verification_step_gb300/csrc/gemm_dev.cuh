@@ -248,6 +248,65 @@ SV_DEV void gemm_begin(const GemmDesc& g, int total_steps, int spt, int gw, int 
 
 // CTA-wide (every thread of the CTA calls it): 1/rms of every token and, in
 // kXSmem mode, the normalised bf16 X of every token in shared memory.
+// Normalised bf16 x * inv_rms * gain of 8 consecutive k of one token.
+SV_DEV uint4 norm_chunk(const float4& a0, const float4& a1, float iv, const float4& g0, const float4& g1) {
+  const __nv_bfloat162 b0 = __floats2bfloat162_rn(a0.x * iv * g0.x, a0.y * iv * g0.y);
+  const __nv_bfloat162 b1 = __floats2bfloat162_rn(a0.z * iv * g0.z, a0.w * iv * g0.w);
+  const __nv_bfloat162 b2 = __floats2bfloat162_rn(a1.x * iv * g1.x, a1.y * iv * g1.y);
+  const __nv_bfloat162 b3 = __floats2bfloat162_rn(a1.z * iv * g1.z, a1.w * iv * g1.w);
+  return make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
+                    *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+}
+
+// kXSmem preparation for at most 8 tokens, latency-oriented (for kernels
+// with the register budget of one 256-thread CTA per SM): a thread owns
+// 8-wide k-chunks c, c + blockDim, ... and issues the loads of two chunks for
+// every token (and their gains) at once; they are in flight while the warps
+// sum the per-tile squares into 1/rms.
+SV_DEV void prepare_x_few(const GemmDesc& g, float* s_inv, uint16_t* s_x) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  const int ld = g.k + kXPad, per_tok = g.k / 8, ntok = g.ntok;
+  float4 xa[2][8][2], ga[2][2];
+  auto load = [&](int b, int c) {
+    if (c >= per_tok) return;
+    const float4* gp = (const float4*)(g.gain + c * 8);
+    ga[b][0] = __ldg(gp);
+    ga[b][1] = __ldg(gp + 1);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      if (t < ntok) {
+        const float4* xp = (const float4*)((const float*)g.x + (size_t)t * g.ldx + c * 8);
+        xa[b][t][0] = __ldcg(xp);
+        xa[b][t][1] = __ldcg(xp + 1);
+      }
+    }
+  };
+  auto store = [&](int b, int c) {
+    if (c >= per_tok) return;
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < ntok)
+        *reinterpret_cast<uint4*>(s_x + (size_t)t * ld + c * 8) =
+            norm_chunk(xa[b][t][0], xa[b][t][1], s_inv[t], ga[b][0], ga[b][1]);
+  };
+  const int step = blockDim.x;
+  int c = threadIdx.x;
+  load(0, c);
+  load(1, c + step);
+  for (int tok = warp; tok < ntok; tok += nwarp) {
+    const float v = warp_inv_rms(g, tok, lane);
+    if (lane == 0) s_inv[tok] = v;
+  }
+  __syncthreads();
+  for (; c < per_tok; c += 2 * step) {
+    store(0, c);
+    store(1, c + step);
+    load(0, c + 2 * step);
+    load(1, c + 3 * step);
+  }
+  __syncthreads();
+}
+
 template <int XM>
 SV_DEV void gemm_prepare_x(const GemmDesc& g, float* s_inv, uint16_t* s_x) {
   if (XM == kXGlobal) return;
@@ -281,14 +340,8 @@ SV_DEV void gemm_prepare_x(const GemmDesc& g, float* s_inv, uint16_t* s_x) {
       const int e = e0 + b * blockDim.x;
       if (e < chunks) {
         const int tok = e / per_tok, k0 = (e % per_tok) * 8;
-        const float iv = s_inv[tok];
-        const __nv_bfloat162 b0 = __floats2bfloat162_rn(a[b][0].x * iv * gg[b][0].x, a[b][0].y * iv * gg[b][0].y);
-        const __nv_bfloat162 b1 = __floats2bfloat162_rn(a[b][0].z * iv * gg[b][0].z, a[b][0].w * iv * gg[b][0].w);
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(a[b][1].x * iv * gg[b][1].x, a[b][1].y * iv * gg[b][1].y);
-        const __nv_bfloat162 b3 = __floats2bfloat162_rn(a[b][1].z * iv * gg[b][1].z, a[b][1].w * iv * gg[b][1].w);
         *reinterpret_cast<uint4*>(s_x + (size_t)tok * ld + k0) =
-            make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
-                       *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+            norm_chunk(a[b][0], a[b][1], s_inv[tok], gg[b][0], gg[b][1]);
       }
     }
   }

@@ -112,10 +112,26 @@ struct AttnDesc {
   void* out;               // [ntok][hq*hd] model dtype
   int ntok, hq, hkv, hd, cap, max_chunks, dtype;
   float scale;
+  // tensor-core path (bf16): 2-D tensor maps of this layer's K and V cache
+  // ([hkv * cap][hd], see encode_kv_map) and the flag raised when a wait for
+  // their copies gives up
+  const void* tmk;
+  const void* tmv;
+  int* err;
 };
 size_t attn_partial_floats(int max_tok, int hq, int hd, int max_chunks);
 int attn_max_row_tiles(int max_tok, int hq, int hkv);
 cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st);
+// Tensor-core attention (bf16 cache, head dim 32/64/128, any token count):
+// items per (KV head, token, group of 8 query heads, 1024-key split); its
+// tickets are dattn_tickets(tokens, hq, hkv) zeroed counters, its partials
+// persist_attn_partial_floats floats.
+cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st);
+struct TensorMap128;
+// Tensor map of a bf16 KV cache [rows][hd] for launch_dattn (head dim 32, 64
+// or 128); false when the map cannot be encoded.
+bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows);
+int dattn_tickets(int max_tok, int hq, int hkv);
 // One-time kernel attributes (dynamic shared memory); call before any capture.
 cudaError_t configure_kernels();
 
@@ -183,6 +199,7 @@ cudaError_t launch_accept(const AcceptDesc& a, cudaStream_t st);
 // tma_dev.cuh); results agree with the per-kernel path up to the order of
 // fp32 partial sums, and are batch-invariant like it.
 enum PhaseKind : int { kPhaseEmbed = 0, kPhaseGemm = 1, kPhaseAttn = 2 };
+constexpr int kPhaseStamps = 5;
 struct PhaseDesc {
   int kind;
   int xm;            // GEMM X source (see gemm_dev.cuh)
@@ -206,11 +223,14 @@ struct PersistDesc {
   const TensorMap128* tmaps; // device array indexed by PhaseDesc::tm
   float* partials;           // GEMM scratch, >= persist_partial_floats(grid) floats
   int* tickets;
-  unsigned* bar;             // [2] barrier arrival count and generation (zero at start)
+  unsigned* bar;             // [1] arrival count (zero at start; the kernel leaves it zero)
   int* err;                  // set to 1 when a wait gives up
-  // optional (null: off): [1 + 3 * nphases] globaltimer stamps, zeroed before
-  // the launch -- start, then per phase the earliest arrival (stored as ~t,
-  // atomicMax), the latest arrival (atomicMax) and CTA 0's release
+  // optional (null: off): [1 + kPhaseStamps * nphases] globaltimer stamps,
+  // zeroed before the launch -- start, then per phase the earliest arrival
+  // (stored as ~t, atomicMax), the latest arrival (atomicMax), CTA 0's
+  // release, the latest end of X preparation (GEMM) or of a key walk
+  // (attention), and the latest delivery of a CTA's last weight unit (GEMM)
+  // or end of its items (attention)
   unsigned long long* times;
 };
 // Fill the kernel-side fields of a phase.  The GEMM variant also encodes the
@@ -220,10 +240,9 @@ struct PersistDesc {
 bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps);
 // Attention phases need a bf16 cache, at most 8 tokens and head dim 32, 64
 // or 128; their scratch is persist_attn_partial_floats floats and
-// persist_attn_tickets zeroed counters (a.partials, a.tickets).
+// dattn_tickets zeroed counters (a.partials, a.tickets).
 bool persist_phase_from_attn(PhaseDesc& p, const AttnDesc& a);
 size_t persist_attn_partial_floats(int max_tok, int hq, int hd, int cap);
-int persist_attn_tickets(int max_tok, int hq, int hkv);
 void persist_phase_from_embed(PhaseDesc& p, const EmbedDesc& e);
 // Dynamic shared memory the persistent kernel needs for head dim hd, KV
 // chunks max_chunks and the largest normalised GEMM input (tokens x k).

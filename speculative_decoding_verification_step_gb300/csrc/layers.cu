@@ -9,6 +9,7 @@
 // stale KV rows beyond the committed length are never read (each query only
 // reads keys at or before its own position) and are overwritten later.
 #include "attn_dev.cuh"
+#include "dattn_dev.cuh"
 #include "embed_dev.cuh"
 
 namespace sv {
@@ -87,6 +88,39 @@ static cudaError_t configure_attn() {
                               (int)kAttnSmemCap);
 }
 
+// Tensor-core attention with one item per (KV head, token, head group, key
+// split) -- the device code of the persistent kernel as its own launch.
+template <int HD>
+__global__ void __launch_bounds__(kDWarps * 32) dattn_kernel(const __grid_constant__ AttnDesc a) {
+  extern __shared__ __align__(1024) unsigned char dsm_attn[];
+  __shared__ int s_last;
+  __shared__ uint64_t bars[kDWarps * kDMaxDepth];
+  dattn_init_bars(bars);
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  unsigned dpar = 0;
+  dattn_item<HD>(a, blockIdx.x, dsm_attn, &s_last, bars, dpar);
+}
+
+template <int HD>
+static cudaError_t configure_dattn() {
+  return cudaFuncSetAttribute(dattn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)DAttnSmem<HD>::kBytes);
+}
+
+int dattn_tickets(int max_tok, int hq, int hkv) { return max_tok * hkv * dattn_hgroups(hq, hkv); }
+
+cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st) {
+  if (a.dtype != 1 || a.hq % a.hkv != 0 || !a.tmk || !a.tmv) return cudaErrorInvalidValue;
+  const int items = dattn_items(a.ntok, a.hq, a.hkv, a.cap);
+  if (a.hd == 32) return launch_k(dattn_kernel<32>, dim3(items), dim3(kDWarps * 32), DAttnSmem<32>::kBytes, st, a);
+  if (a.hd == 64) return launch_k(dattn_kernel<64>, dim3(items), dim3(kDWarps * 32), DAttnSmem<64>::kBytes, st, a);
+  if (a.hd == 128)
+    return launch_k(dattn_kernel<128>, dim3(items), dim3(kDWarps * 32), DAttnSmem<128>::kBytes, st, a);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t configure_kernels() {
   cudaError_t e;
   if ((e = configure_gemm()) != cudaSuccess) return e;
@@ -95,7 +129,10 @@ cudaError_t configure_kernels() {
   if ((e = configure_attn<128, float>()) != cudaSuccess) return e;
   if ((e = configure_attn<32, bf16>()) != cudaSuccess) return e;
   if ((e = configure_attn<64, bf16>()) != cudaSuccess) return e;
-  return configure_attn<128, bf16>();
+  if ((e = configure_attn<128, bf16>()) != cudaSuccess) return e;
+  if ((e = configure_dattn<32>()) != cudaSuccess) return e;
+  if ((e = configure_dattn<64>()) != cudaSuccess) return e;
+  return configure_dattn<128>();
 }
 
 template <int HD, typename T>

@@ -10,13 +10,13 @@
 //   * one CTA per SM stays resident; phases are separated by a grid barrier
 //     split in an arrive and a wait half;
 //   * GEMM phases stream weights with 2-D tensor copies (TMA) through a
-//     shared-memory ring (tma_dev.cuh): one producer thread copies, eight
-//     consumer warps run the MMAs;
+//     shared-memory ring (tma_dev.cuh): one producer thread copies, up to
+//     four tile-owner warps run the MMAs;
 //   * between arriving at a barrier and waiting on it, the producer already
 //     issues the weight copies of the next GEMM phase's first units (weights
 //     are read-only), so HBM keeps streaming across phase boundaries;
 //   * attention phases run the tensor-core decode attention (dattn_dev.cuh)
-//     on the eight consumer warps; the embedding reuses embed_dev.cuh.
+//     on all eight warps; the embedding reuses embed_dev.cuh.
 // The work split depends only on the matrix shapes and the SM count, never
 // on the token count, so every pass is batch-invariant.  Every wait is
 // bounded: a grid-barrier wait that gives up, or a pipeline wait (see
@@ -46,42 +46,40 @@ SV_DEV unsigned ld_acquire_u32(const unsigned* p) {
 }
 
 // Grid-wide barrier of a co-resident launch, split in two halves so that
-// the next phase's weight copies can be issued in between: bar[0] counts
-// arrivals, bar[1] is the generation.  grid_arrive (every thread, after the
-// phase's last shared-memory use) publishes this CTA's writes and arrives;
-// grid_wait returns once every CTA has arrived, false (in every thread of the
-// CTA) when the wait gave up or another CTA reported an error.
-SV_DEV void grid_arrive(unsigned* bar, unsigned* s_gen) {
+// the next phase's weight copies can be issued in between.  bar[0] counts
+// arrivals since the launch began: every CTA arrives once at each barrier
+// (after phase ph the count to wait for is (ph + 1) * gridDim.x) and once
+// more on leaving, and the CTA whose leaving arrival completes the count
+// resets it for the next launch -- by then every CTA has passed its last
+// wait.  grid_arrive (every thread, after the phase's last shared-memory use)
+// publishes this CTA's writes with a release add; grid_wait returns once the
+// count is reached, false (in every thread of the CTA) when the wait gave up
+// or another CTA reported an error.
+SV_DEV void grid_arrive(unsigned* bar) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire_u32(bar + 1);
-    __threadfence();
-    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
-    }
-    *s_gen = gen;
-  }
+  if (threadIdx.x == 0) red_add_release_gpu(bar, 1u);
 }
 
-SV_DEV bool grid_wait(unsigned* bar, int* err, const unsigned* s_gen, int* s_ok) {
+SV_DEV bool grid_wait(unsigned* bar, unsigned target, int* err, int* s_ok) {
   if (threadIdx.x == 0) {
     int ok = 1;
     long long spins = 0;
-    while (ld_acquire_u32(bar + 1) == *s_gen) {
+    while (ld_acquire_u32(bar) < target) {
       if (++spins > kBarrierSpinLimit) {
         atomicExch(err, 1);
         ok = 0;
         break;
       }
-      __nanosleep(32);
     }
-    __threadfence();
     *s_ok = ok && (*(volatile int*)err == 0);
   }
   __syncthreads();
   return *s_ok != 0;
+}
+
+SV_DEV void grid_leave(unsigned* bar, unsigned total) {
+  __syncthreads();
+  if (threadIdx.x == 0 && atom_add_acq_rel_gpu(bar, 1u) == total - 1) st_relaxed_gpu(bar, 0u);
 }
 
 template <int HD>
@@ -91,9 +89,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   // phases reuse it from offset 0
   extern __shared__ __align__(1024) unsigned char dsm[];
   __shared__ TmaPipe tp;
+  __shared__ uint64_t dbars[kDWarps * kDMaxDepth];   // attention stage barriers
   __shared__ float s_inv[kGemmMaxTok];
   __shared__ int s_last, s_ok;
-  __shared__ unsigned s_gen;
   // the current and the next phase descriptor, staged in shared memory
   __shared__ __align__(16) PhaseDesc s_ph[2];
   unsigned char* ring = dsm;
@@ -110,26 +108,32 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   unsigned long long* const times = p.times;
   if (times && blockIdx.x == 0 && threadIdx.x == 0) times[0] = global_ns();
   tma_init(tp);
+  dattn_init_bars(dbars);
+  unsigned dpar = 0;   // attention: per-warp stage parities
   stage(0, 0);
   __syncthreads();
   unsigned cpar = 0;   // consumers: parity of each stage's next full-barrier completion
   int npre = 0;        // units of the current GEMM phase issued before its barrier
   for (int ph = 0; ph < p.nphases; ++ph) {
     const PhaseDesc& d = s_ph[ph & 1];
+    unsigned long long* const st = times ? times + 1 + kPhaseStamps * ph : nullptr;
     if (d.kind == kPhaseEmbed) {
       for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16>(d.e, t);
     } else if (d.kind == kPhaseGemm) {
-      if (d.xm == kXSmem) gemm_prepare_x<kXSmem>(d.g, s_inv, reinterpret_cast<uint16_t*>(xreg));
+      if (d.xm == kXSmem) prepare_x_few(d.g, s_inv, reinterpret_cast<uint16_t*>(xreg));
+      if (st && threadIdx.x == 0) atomicMax(st + 3, global_ns());
       if (producer) {
         if (lane == 0) tma_produce(d, npre, tp, ring, xreg, maps);
         __syncwarp();
       } else if (d.xm == kXSmem) {
-        tma_consume<kXSmem>(d, tp, cpar, ring, xreg, p.partials, p.tickets);
+        tma_consume<kXSmem>(d, tp, cpar, ring, xreg, p.partials, p.tickets, st ? st + 4 : nullptr);
       } else {
-        tma_consume<kXGlobal>(d, tp, cpar, ring, xreg, p.partials, p.tickets);
+        tma_consume<kXGlobal>(d, tp, cpar, ring, xreg, p.partials, p.tickets, st ? st + 4 : nullptr);
       }
-    } else if (!producer) {
-      for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x) dattn_item<HD>(d.a, it, dsm, &s_last);
+    } else {
+      for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x)
+        dattn_item<HD>(d.a, it, dsm, &s_last, dbars, dpar, st ? st + 3 : nullptr);
+      if (st && threadIdx.x == 0) atomicMax(st + 4, global_ns());
     }
     npre = 0;
     // this thread's global writes and shared-memory accesses are ordered
@@ -140,29 +144,30 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
       __syncthreads();
       if (threadIdx.x == 0) {
         const unsigned long long t = global_ns();
-        atomicMax(times + 1 + 3 * ph, ~t);
-        atomicMax(times + 2 + 3 * ph, t);
+        atomicMax(st, ~t);
+        atomicMax(st + 1, t);
       }
     }
     if (ph + 1 < p.nphases) {
       stage((ph + 1) & 1, ph + 1);
-      grid_arrive(p.bar, &s_gen);   // its __syncthreads also ends this phase's shared-memory use
+      grid_arrive(p.bar);   // its __syncthreads also ends this phase's shared-memory use
       if (threadIdx.x == 0 && tp.abort) atomicExch(p.err, 1);
       const PhaseDesc& nx = s_ph[(ph + 1) & 1];
       if (nx.kind == kPhaseGemm && producer) {   // weights of the next GEMM: issued while waiting
         if (lane == 0) npre = tma_prefetch(nx, tp, ring, xreg, maps);
         npre = __shfl_sync(0xffffffffu, npre, 0);
       }
-      if (!grid_wait(p.bar, p.err, &s_gen, &s_ok)) {
+      if (!grid_wait(p.bar, (unsigned)(ph + 1) * gridDim.x, p.err, &s_ok)) {
         tma_drain(tp);
         return;
       }
-      if (times && blockIdx.x == 0 && threadIdx.x == 0) times[3 + 3 * ph] = global_ns();
+      if (st && blockIdx.x == 0 && threadIdx.x == 0) st[2] = global_ns();
     }
   }
   __syncthreads();
   if (threadIdx.x == 0 && tp.abort) atomicExch(p.err, 1);
   if (tp.abort) tma_drain(tp);
+  grid_leave(p.bar, (unsigned)p.nphases * gridDim.x);
 }
 
 // ---- host side ----
@@ -192,6 +197,22 @@ static bool encode_rows(TensorMap128& m, const void* base, int k, long long rows
   return enc(reinterpret_cast<CUtensorMap*>(&m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || !base || rows < 1 || (hd != 32 && hd != 64 && hd != 128) ||
+      (reinterpret_cast<uintptr_t>(base) & 15u))
+    return false;
+  const int cols = hd < 64 ? hd : 64;
+  cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
+  cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)kDStepKeys};
+  cuuint32_t es[2] = {1, 1};
+  return enc(reinterpret_cast<CUtensorMap*>(&m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             hd < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps) {
@@ -241,15 +262,13 @@ bool persist_phase_from_attn(PhaseDesc& p, const AttnDesc& a) {
   p.kind = kPhaseAttn;
   p.a = a;
   p.attn_items = dattn_items(a.ntok, a.hq, a.hkv, a.cap);
-  return a.dtype == 1 && a.ntok <= kPersistMaxTok && a.hq % a.hkv == 0 &&
+  return a.dtype == 1 && a.ntok <= kPersistMaxTok && a.hq % a.hkv == 0 && a.tmk && a.tmv &&
          (a.hd == 32 || a.hd == 64 || a.hd == 128);
 }
 
 size_t persist_attn_partial_floats(int max_tok, int hq, int hd, int cap) {
   return (size_t)max_tok * hq * dattn_splits(cap) * (hd + 4);
 }
-
-int persist_attn_tickets(int max_tok, int hq, int hkv) { return max_tok * hkv * dattn_hgroups(hq, hkv); }
 
 void persist_phase_from_embed(PhaseDesc& p, const EmbedDesc& e) {
   p = PhaseDesc{};

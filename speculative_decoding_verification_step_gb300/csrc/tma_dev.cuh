@@ -14,12 +14,11 @@
 // the units through a ring of S stages (S x 2R x 512 bytes, S <= 8): per unit
 // one or two weight boxes and, in phases whose X comes from global memory,
 // one 8-row X box, all completing on the stage's transaction barrier.  The
-// eight consumer warps split a unit's (MMA tile, 64-k step) pairs: warp w
-// takes tile w mod T (T = R/8 tiles) and steps w/T + j*8/T.  At the end of a
-// row group the warps of each tile add their accumulators in warp order in
-// shared memory; a group split between CTAs is finished by the
-// last-arriving CTA, which adds the CTA partials in CTA order.  Results do
-// not depend on timing or on the token count.
+// warp t < T = R/8 owns MMA tile t of every unit (its four 64-k
+// steps, one accumulator chain each, added in step order).  A tile split
+// between CTAs is finished by the last-arriving CTA, which adds the CTA
+// partials in CTA order; no consumer warp ever waits for another.  Results
+// do not depend on timing or on the token count.
 //
 // Every wait is bounded.  A wait that gives up raises the CTA's abort flag;
 // from then on every wait of the CTA returns at once and the warps run
@@ -34,9 +33,9 @@ namespace sv {
 constexpr int kTmaK = 256;                        // k per unit (box inner extent)
 constexpr int kTmaRowBytes = kTmaK * 2;           // row pitch of a box in shared memory
 constexpr int kTmaSteps = kTmaK / kStepK;         // 64-k MMA steps per unit
-constexpr int kCWarps = 8;                        // consumer warps
-constexpr int kProducerWarp = kCWarps;
-constexpr int kPersistThreads = (kCWarps + 1) * 32;
+constexpr int kCWarps = 8;                        // warps of the CTA (attention uses all)
+constexpr int kProducerWarp = kCWarps - 1;        // lane 0 issues the tensor copies
+constexpr int kPersistThreads = kCWarps * 32;     // 2 warps per SM sub-partition: 255 registers
 constexpr int kMaxStages = 8;
 constexpr int kXBoxRows = 8;
 constexpr int kXStageBytes = kXBoxRows * kTmaRowBytes;
@@ -45,7 +44,6 @@ constexpr int kMinUnitsPerCta = 2;
 constexpr int kMaxMmaTiles = 4;                   // R / 8 for R <= 32
 constexpr long long kWaitLimit = 1LL << 22;
 constexpr long long kDrainLimit = 1LL << 16;
-constexpr int kBarConsumers = 2;                  // named barrier of the consumer warps
 constexpr int kPersistMaxTok = 8;
 constexpr size_t kTensorMapBytes = 128;
 
@@ -53,7 +51,6 @@ struct TmaPipe {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   unsigned fills[kMaxStages];   // fills issued per slot (producer)
-  float red[2][kCWarps][32 * 4];
   int abort;
 };
 
@@ -61,7 +58,7 @@ SV_DEV void tma_init(TmaPipe& tp) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&tp.full[i], 1);
-      mbar_init(&tp.empty[i], kCWarps);
+      mbar_init(&tp.empty[i], kMaxMmaTiles);   // released by the tile-owner warps
       tp.fills[i] = 0;
     }
     tp.abort = 0;
@@ -198,45 +195,30 @@ SV_DEV void tma_produce(const PhaseDesc& d, int npre, TmaPipe& tp, unsigned char
   for (int i = npre; i < n; ++i) tma_issue(d, r, i, xg, tp, ring, xreg, maps);
 }
 
-// Consumer warps at the end of a row group: the warps of MMA tile t add their
-// accumulators in warp order; warp t finishes the tile (epilogue, or CTA
-// partial and, for the last-arriving CTA, the reduction over CTAs in CTA
-// order).
-SV_DEV void tma_group_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs, int kbe, int pslot,
-                          const float (&acc)[4], int par, TmaPipe& tp, float* __restrict__ partials,
-                          int* __restrict__ tickets) {
+// Consumer warp t at the end of a row group: finish MMA tile t -- the
+// epilogue when this CTA covered every k of the group, else its CTA partial
+// and, for the last-arriving CTA of the group, the sum of the CTA partials in
+// CTA order and the epilogue.  No other warp takes part.
+SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs, int kbe, int pslot,
+                         const float (&tot)[1][4], float* __restrict__ partials, int* __restrict__ tickets) {
   const GemmDesc& g = d.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
-  const int T = d.R / 8;
-  float* buf = tp.red[par][0];
-  *reinterpret_cast<float4*>(buf + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  named_sync(kBarConsumers, kCWarps * 32);
-  if (warp >= T || tp.abort) return;
   const int tile = group_tile(d, grp, warp);
   if (tile >= gemm_tiles_of(g)) return;
-  float tot[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-  for (int w = warp; w < kCWarps; w += T) {
-    const float4 v = *reinterpret_cast<const float4*>(buf + (w * 32 + lane) * 4);
-    tot[0][0] += v.x;
-    tot[0][1] += v.y;
-    tot[0][2] += v.z;
-    tot[0][3] += v.w;
-  }
   if (kbs == 0 && kbe == r.kbpt) {
     gemm_epilogue<1>(g, tile, tot, gi, ci);
     return;
   }
   float* mine = partials + (((size_t)blockIdx.x * 2 + pslot) * kMaxMmaTiles + warp) * 32 * 4;
   *reinterpret_cast<float4*>(mine + (size_t)lane * 4) = make_float4(tot[0][0], tot[0][1], tot[0][2], tot[0][3]);
-  __threadfence();
   __syncwarp();
   const int cfirst = warp_of_step((long long)grp * r.kbpt, r.total, r.nc);
   const int clast = warp_of_step((long long)(grp + 1) * r.kbpt - 1, r.total, r.nc);
-  int old = 0;
-  if (lane == 0) old = atomicAdd(&tickets[tile], 1);
+  int old = 0;   // the acq_rel ticket publishes this partial and acquires the earlier ones
+  if (lane == 0) old = (int)atom_add_acq_rel_gpu(reinterpret_cast<unsigned*>(&tickets[tile]), 1u);
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old != clast - cfirst) return;
-  __threadfence();
+  __syncwarp();
   float sum[1][4] = {{0.f, 0.f, 0.f, 0.f}};
   for (int c = cfirst; c <= clast; ++c) {
     const int sl = (first_step_of_warp(c, r.total, r.nc) / r.kbpt == grp) ? 0 : 1;
@@ -251,66 +233,86 @@ SV_DEV void tma_group_end(const PhaseDesc& d, const TmaRange& r, int grp, int kb
   if (lane == 0) tickets[tile] = 0;
 }
 
-// Consumer warp during GEMM phase d.  cpar: per-slot parity of the next
-// completion of each stage's full barrier (identical in every consumer warp).
+// Consumer warps during GEMM phase d.  Warp t < T = R/8 owns MMA tile t of
+// every unit and runs its four 64-k steps, each into its own accumulator
+// chain (added in step order at the end of the group); warps t >= T only
+// keep the ring bookkeeping.  cpar: per-slot parity of the next completion
+// of each stage's full barrier (identical in every consumer warp).
+// stamp (optional): atomicMax of the globaltimer when the last unit arrived.
 template <int XM>
 SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const unsigned char* ring,
-                        const unsigned char* xreg, float* __restrict__ partials, int* __restrict__ tickets) {
+                        const unsigned char* xreg, float* __restrict__ partials, int* __restrict__ tickets,
+                        unsigned long long* stamp) {
   const GemmDesc& g = d.g;
   const TmaRange r = tma_range(d);
   const int n = r.u1 - r.u0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
-  const uint4 zero4 = make_uint4(0, 0, 0, 0);
   const int R = d.R, T = R / 8, S = d.stages, sb = d.stage_bytes;
-  const int t = warp % T;
+  if (warp >= T) {   // not a tile owner in this phase (the producer warp never gets here)
+    for (int i = 0; i < n; ++i) cpar ^= 1u << (i % S);
+    return;
+  }
+  const uint4 zero4 = make_uint4(0, 0, 0, 0);
+  const int t = warp;
   const int arow = d.paired ? 8 * t + gi : 16 * t + gi;
   const int brow = d.paired ? R + 8 * t + gi : 16 * t + 8 + gi;
-  const int s0 = warp / T, sstride = kCWarps / T, nsteps = kTmaSteps / sstride;
   const bool has_tok = gi < g.ntok;
   const int k = g.k;
   const size_t xs_pitch = (size_t)(k + kXPad) * 2;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int par = 0, pslot = 0;
+  const unsigned arrivals = (unsigned)(kMaxMmaTiles / T);   // the empty barrier expects kMaxMmaTiles
+  float acc[kTmaSteps][4];
+#pragma unroll
+  for (int s = 0; s < kTmaSteps; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
+  int pslot = 0;
   int kbs = n > 0 ? r.u0 % r.kbpt : 0;
 #pragma unroll 1
   for (int i = 0; i < n; ++i) {
     const int slot = i % S;
     const bool ok = tma_wait(&tp.full[slot], (cpar >> slot) & 1u, tp);
     cpar ^= 1u << slot;
+    if (stamp && i == n - 1 && threadIdx.x == 0) {
+      unsigned long long tm;
+      asm volatile("mov.u64 %0, %globaltimer;" : "=l"(tm));
+      atomicMax(stamp, tm);
+    }
     const int u = r.u0 + i;
     const int grp = u / r.kbpt, kb = u - grp * r.kbpt;
     if (ok) {
       const unsigned char* st = ring + (size_t)slot * sb + ci * 32;
-      for (int j = 0; j < nsteps; ++j) {
-        const int s = s0 + j * sstride;
+#pragma unroll
+      for (int s = 0; s < kTmaSteps; ++s) {
         const int kg = kb * kTmaK + s * kStepK;
-        if (kg >= k) break;
-        const unsigned char* ap = st + arow * kTmaRowBytes + s * (kStepK * 2);
-        const unsigned char* bp = st + brow * kTmaRowBytes + s * (kStepK * 2);
-        const uint4 a0 = *reinterpret_cast<const uint4*>(ap);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(ap + 16);
-        const uint4 b0 = *reinterpret_cast<const uint4*>(bp);
-        const uint4 b1 = *reinterpret_cast<const uint4*>(bp + 16);
-        uint4 x0 = zero4, x1 = zero4;
-        if (has_tok) {
-          const unsigned char* xp =
-              XM == kXSmem ? xreg + gi * xs_pitch + (size_t)(kg + ci * 16) * 2
-                           : xreg + (size_t)slot * kXStageBytes + gi * kTmaRowBytes + s * (kStepK * 2) + ci * 32;
-          x0 = *reinterpret_cast<const uint4*>(xp);
-          x1 = *reinterpret_cast<const uint4*>(xp + 16);
+        if (kg < k) {
+          const unsigned char* ap = st + arow * kTmaRowBytes + s * (kStepK * 2);
+          const unsigned char* bp = st + brow * kTmaRowBytes + s * (kStepK * 2);
+          const uint4 a0 = *reinterpret_cast<const uint4*>(ap);
+          const uint4 a1 = *reinterpret_cast<const uint4*>(ap + 16);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(bp);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(bp + 16);
+          uint4 x0 = zero4, x1 = zero4;
+          if (has_tok) {
+            const unsigned char* xp =
+                XM == kXSmem ? xreg + gi * xs_pitch + (size_t)(kg + ci * 16) * 2
+                             : xreg + (size_t)slot * kXStageBytes + gi * kTmaRowBytes + s * (kStepK * 2) + ci * 32;
+            x0 = *reinterpret_cast<const uint4*>(xp);
+            x1 = *reinterpret_cast<const uint4*>(xp + 16);
+          }
+          mma_bf16_16816(acc[s], a0.x, b0.x, a0.y, b0.y, x0.x, x0.y);
+          mma_bf16_16816(acc[s], a0.z, b0.z, a0.w, b0.w, x0.z, x0.w);
+          mma_bf16_16816(acc[s], a1.x, b1.x, a1.y, b1.y, x1.x, x1.y);
+          mma_bf16_16816(acc[s], a1.z, b1.z, a1.w, b1.w, x1.z, x1.w);
         }
-        mma_bf16_16816(acc, a0.x, b0.x, a0.y, b0.y, x0.x, x0.y);
-        mma_bf16_16816(acc, a0.z, b0.z, a0.w, b0.w, x0.z, x0.w);
-        mma_bf16_16816(acc, a1.x, b1.x, a1.y, b1.y, x1.x, x1.y);
-        mma_bf16_16816(acc, a1.z, b1.z, a1.w, b1.w, x1.z, x1.w);
       }
     }
     __syncwarp();
-    if (lane == 0 && ok) mbar_arrive(&tp.empty[slot]);
+    if (lane == 0 && ok) mbar_arrive_count(&tp.empty[slot], arrivals);
     if (kb == r.kbpt - 1 || i == n - 1) {
-      tma_group_end(d, r, grp, kbs, kb + 1, pslot, acc, par, tp, partials, tickets);
-      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-      par ^= 1;
+      float tot[1][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tot[0][e] = ((acc[0][e] + acc[1][e]) + acc[2][e]) + acc[3][e];
+      if (!tp.abort) tma_tile_end(d, r, grp, kbs, kb + 1, pslot, tot, partials, tickets);
+#pragma unroll
+      for (int s = 0; s < kTmaSteps; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
       pslot = 1;
       kbs = 0;
     }
@@ -331,4 +333,8 @@ SV_DEV void tma_drain(TmaPipe& tp) {
   }
 }
 
+}  // namespace sv
+
+namespace sv {
+static_assert(kProducerWarp >= kMaxMmaTiles, "the producer warp must not own an MMA tile");
 }  // namespace sv

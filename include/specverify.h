@@ -253,7 +253,9 @@ SPEC_API int spec_sample_rows(const float* logits, int64_t row_stride, int rows,
  * warm-up replays: the draft loop (K draft passes + samplers), the verify
  * pass (target over the K+1 positions + fused acceptance, not committed)
  * and one plain-decoding pass (target over 1 position + sampler, not
- * committed).  Requires a prefilled context; the committed state is left
+ * committed), and the verify pass's target forward alone (the one
+ * persistent kernel launch, or its per-operation kernels).  Requires a
+ * prefilled context; the committed state is left
  * unchanged (only uncommitted KV rows and draft slots are rewritten, with
  * the values the next step computes anyway).  Measures the quantities of
  * [INT 加速倍率 = K × acceptance rate 的限制]: T_draft, T_target and C. */
@@ -265,6 +267,8 @@ typedef struct spec_profile_t {
     int32_t kernels_draft_loop;
     int32_t kernels_verify;
     int32_t kernels_ar;
+    double verify_forward_ms;     /* the verify pass's target forward alone */
+    int32_t kernels_verify_forward;
 } spec_profile_t;
 SPEC_API int spec_profile(spec_ctx* ctx, int iters, spec_profile_t* out);
 

@@ -72,7 +72,8 @@ class Profile(ctypes.Structure):
     _fields_ = [("draft_loop_ms", ctypes.c_double), ("verify_ms", ctypes.c_double),
                 ("ar_ms", ctypes.c_double), ("iters", ctypes.c_int32),
                 ("kernels_draft_loop", ctypes.c_int32), ("kernels_verify", ctypes.c_int32),
-                ("kernels_ar", ctypes.c_int32)]
+                ("kernels_ar", ctypes.c_int32), ("verify_forward_ms", ctypes.c_double),
+                ("kernels_verify_forward", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -219,7 +220,8 @@ class SpecDecoder:
         return s.as_dict()
 
     def profile(self, iters=20):
-        """Graph-replayed phase times (ms): draft loop, verify pass, plain-decoding pass."""
+        """Graph-replayed phase times (ms): draft loop, verify pass, plain-decoding
+        pass, and the verify pass's target forward alone."""
         pr = Profile()
         _check(lib().spec_profile(self.ctx, iters, ctypes.byref(pr)), self.ctx)
         return pr.as_dict()

@@ -112,8 +112,9 @@ struct spec_ctx {
   // graphs
   cudaGraphExec_t step_exec = nullptr;
   cudaGraphExec_t ar_exec = nullptr;
-  cudaGraphExec_t prof_exec[3] = {nullptr, nullptr, nullptr};  // draft loop, verify, ar
-  int prof_kernels[3] = {0, 0, 0};
+  // draft loop, verify, ar, verify forward alone
+  cudaGraphExec_t prof_exec[4] = {nullptr, nullptr, nullptr, nullptr};
+  int prof_kernels[4] = {0, 0, 0, 0};
   // host mirror of the state
   bool prefilled = false;
   bool draft_stale = false;
@@ -415,6 +416,16 @@ void enqueue_step(Launch& L) {
 }
 
 void enqueue_verify_only(Launch& L) { enqueue_verify(L, false); }
+
+// The verify forward alone (the target over the K+1 positions, no acceptance).
+void enqueue_verify_forward(Launch& L) {
+  spec_ctx* c = L.c;
+  const int32_t* Lp = c->st;
+  if (c->persist)
+    forward_persist(L, c->K);
+  else
+    forward(L, c->tgt, c->K + 1, c->seq, Lp, 0, Lp, 0, 0, c->K + 1, c->logits_p);
+}
 
 void enqueue_ar_pass(Launch& L, bool commit) {
   spec_ctx* c = L.c;
@@ -924,12 +935,12 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_profile before spec_prefill");
   if (c->draft_stale) return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
   if (c->host_L + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
-  void (*enq[3])(Launch&) = {enqueue_draft, enqueue_verify_only, enqueue_ar_only};
-  double ms[3];
+  void (*enq[4])(Launch&) = {enqueue_draft, enqueue_verify_only, enqueue_ar_only, enqueue_verify_forward};
+  double ms[4];
   cudaEvent_t e0, e1;
   CUDA_TRY(c, cudaEventCreate(&e0));
   CUDA_TRY(c, cudaEventCreate(&e1));
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < 4; ++k) {
     if (!c->prof_exec[k]) {
       int rc = capture(c, &c->prof_exec[k], enq[k], &c->prof_kernels[k]);
       if (rc) { cudaEventDestroy(e0); cudaEventDestroy(e1); return rc; }
@@ -957,6 +968,8 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   out->kernels_draft_loop = c->prof_kernels[0];
   out->kernels_verify = c->prof_kernels[1];
   out->kernels_ar = c->prof_kernels[2];
+  out->verify_forward_ms = ms[3];
+  out->kernels_verify_forward = c->prof_kernels[3];
   return SPEC_OK;
 }
 

@@ -90,7 +90,7 @@ struct spec_ctx {
   int32_t* fwd_tok = nullptr;  // [kGemmMaxTok] host-supplied tokens of spec_model_forward
   // activations
   float* x = nullptr;
-  void* xn = nullptr;
+  void* xg = nullptr;   // bf16 x * gain of the next RMSNorm (persistent forward: x_norm = 2 input)
   void* hbuf = nullptr;
   float* q = nullptr;
   void* attn = nullptr;
@@ -240,9 +240,12 @@ struct Op {
 // GEMM (input RMSNorm on load, RoPE + KV append in its epilogue), attention,
 // o-projection + residual (writes the next norm's sums of squares), gate/up
 // GEMM (RMSNorm on load, SwiGLU epilogue), down-projection + residual.
+// pregain (persistent kernel): the residual producers also write x times the
+// next RMSNorm's gain in bf16 (c->xg), which the normalised GEMMs read
+// (x_norm = 2) and scale by 1/rms after the sums.
 std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t* tok_base,
                             const int32_t* tok_idx, int tok_off, const int32_t* pos_idx,
-                            int pos_off, int lrow0, int lrows, float* logits) {
+                            int pos_off, int lrow0, int lrows, float* logits, bool pregain = false) {
   const spec_model_desc& d = m.d;
   const int dm = d.d_model, hq = d.n_heads, hkv = d.n_kv_heads, hd = d.head_dim;
   const int qkvr = m.qkv_rows();
@@ -253,7 +256,24 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
   op.e.tok_base = tok_base; op.e.tok_idx = tok_idx; op.e.tok_off = tok_off; op.e.embed = d.embed;
   op.e.dtype = dt; op.e.x = c->x; op.e.ss = c->ss; op.e.ss_ld = kGemmMaxTok; op.e.ntok = ntok;
   op.e.d = dm;
+  if (pregain) {
+    op.e.xg = c->xg;
+    op.e.gain = (const float*)m.layers[0].attn_norm;
+  }
   ops.push_back(op);
+  // a normalised GEMM's X: the fp32 residual normalised on load, or its
+  // pre-multiplied bf16 copy
+  auto norm_x = [&](GemmDesc& g, const void* gain, int row0) {
+    g.ldx = dm;
+    g.gain = (const float*)gain;
+    if (pregain) {
+      g.x = (const uint16_t*)c->xg + (size_t)row0 * dm;
+      g.x_norm = 2;
+    } else {
+      g.x = c->x + (size_t)row0 * dm;
+      g.x_norm = 1;
+    }
+  };
   for (int l = 0; l < d.n_layers; ++l) {
     const spec_layer_weights& w = m.layers[l];
     const size_t kvoff = (size_t)l * m.layer_kv_elems(c->cap) * m.esize;
@@ -265,7 +285,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     g.w[0] = w.wq; g.w[1] = w.wk; g.w[2] = w.wv;
     g.seg_rows[0] = hq * hd; g.seg_rows[1] = hkv * hd; g.seg_rows[2] = hkv * hd;
     g.n = qkvr; g.k = dm; g.ntok = ntok;
-    g.x = c->x; g.ldx = dm; g.x_norm = 1; g.gain = (const float*)w.attn_norm;
+    norm_x(g, w.attn_norm, 0);
     g.ss_in = c->ss; g.ss_ld = kGemmMaxTok; g.eps = d.rms_eps;
     g.epi = kEpiQkvRope; g.hq = hq; g.hkv = hkv; g.hd = hd; g.cap = c->cap;
     g.pos_base = pos_idx; g.pos_off = pos_off; g.rope_cos = m.rope_cos; g.rope_sin = m.rope_sin;
@@ -289,12 +309,16 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     o.kind = kPhaseGemm;
     o.g.w[0] = w.wo; o.g.seg_rows[0] = dm; o.g.n = dm; o.g.k = hq * hd; o.g.x = c->attn;
     o.g.ldx = hq * hd; o.g.ntok = ntok; o.g.epi = kEpiAdd; o.g.out = c->x; o.g.ldo = dm;
+    if (pregain) {
+      o.g.xg_out = c->xg;
+      o.g.gain_next = (const float*)w.ffn_norm;
+    }
     o.g.ss_out = c->ss; o.g.ss_ld = kGemmMaxTok;
     ops.push_back(o);
     Op gu{};
     gu.kind = kPhaseGemm;
     gu.g.w[0] = w.w_gate; gu.g.w[1] = w.w_up; gu.g.n = d.ffn_dim; gu.g.k = dm; gu.g.ntok = ntok;
-    gu.g.x = c->x; gu.g.ldx = dm; gu.g.x_norm = 1; gu.g.gain = (const float*)w.ffn_norm;
+    norm_x(gu.g, w.ffn_norm, 0);
     gu.g.ss_in = c->ss; gu.g.ss_ld = kGemmMaxTok; gu.g.eps = d.rms_eps;
     gu.g.epi = kEpiSwiglu; gu.g.out = c->hbuf; gu.g.ldo = d.ffn_dim;
     ops.push_back(gu);
@@ -302,6 +326,10 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     dn.kind = kPhaseGemm;
     dn.g.w[0] = w.w_down; dn.g.seg_rows[0] = dm; dn.g.n = dm; dn.g.k = d.ffn_dim; dn.g.x = c->hbuf;
     dn.g.ldx = d.ffn_dim; dn.g.ntok = ntok; dn.g.epi = kEpiAdd; dn.g.out = c->x; dn.g.ldo = dm;
+    if (pregain) {
+      dn.g.xg_out = c->xg;
+      dn.g.gain_next = (const float*)(l + 1 < d.n_layers ? m.layers[l + 1].attn_norm : d.final_norm);
+    }
     dn.g.ss_out = c->ss; dn.g.ss_ld = kGemmMaxTok;
     dn.g.early_prefetch = 1;   // follows the gate/up GEMM
     ops.push_back(dn);
@@ -310,8 +338,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     Op h{};
     h.kind = kPhaseGemm;
     h.g.w[0] = d.lm_head; h.g.seg_rows[0] = d.vocab; h.g.n = d.vocab; h.g.k = dm; h.g.ntok = lrows;
-    h.g.x = c->x + (size_t)lrow0 * dm; h.g.ldx = dm; h.g.x_norm = 1;
-    h.g.gain = (const float*)d.final_norm;
+    norm_x(h.g, d.final_norm, lrow0);
     h.g.ss_in = c->ss + lrow0; h.g.ss_ld = kGemmMaxTok; h.g.eps = d.rms_eps;
     h.g.epi = kEpiStore; h.g.out = logits; h.g.ldo = d.vocab;
     ops.push_back(h);
@@ -605,7 +632,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   INIT_TRY(cudaMemset(c->seq, 0, sizeof(int32_t) * (c->cap + K + 2)));
   INIT_TRY(dalloc(c, &c->fwd_tok, sizeof(int32_t) * maxN));
   INIT_TRY(dalloc(c, &c->x, sizeof(float) * maxN * dmax));
-  INIT_TRY(dalloc(c, &c->xn, 4 * maxN * dmax));
+  INIT_TRY(dalloc(c, &c->xg, 2 * maxN * dmax));
   INIT_TRY(dalloc(c, &c->hbuf, 4 * maxN * fmax));
   INIT_TRY(dalloc(c, &c->ss, sizeof(float) * maxN * (dmax / 16 + 1)));
   INIT_TRY(dalloc(c, &c->q, sizeof(float) * maxN * hqd));
@@ -707,17 +734,17 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
       for (int i = 1; i <= K; ++i) {
         float* qrow = c->logits_q + (size_t)(i - 1) * V;
         if (i == 1)
-          add(0, forward_ops(c, c->drf, 2, c->seq, c->st, -1, c->st, -1, 1, 1, qrow));
+          add(0, forward_ops(c, c->drf, 2, c->seq, c->st, -1, c->st, -1, 1, 1, qrow, true));
         else
-          add(i - 1, forward_ops(c, c->drf, 1, c->seq, c->st, i - 1, c->st, i - 1, 0, 1, qrow));
+          add(i - 1, forward_ops(c, c->drf, 1, c->seq, c->st, i - 1, c->st, i - 1, 0, 1, qrow, true));
       }
-      add(K, forward_ops(c, c->tgt, K + 1, c->seq, c->st, 0, c->st, 0, 0, K + 1, c->logits_p));
-      add(K + 1, forward_ops(c, c->tgt, 1, c->seq, c->st, 0, c->st, 0, 0, 1, c->logits_p));
+      add(K, forward_ops(c, c->tgt, K + 1, c->seq, c->st, 0, c->st, 0, 0, K + 1, c->logits_p, true));
+      add(K + 1, forward_ops(c, c->tgt, 1, c->seq, c->st, 0, c->st, 0, 0, 1, c->logits_p, true));
       // last scored prompt position (st[0] - 1) of both models, run by
       // spec_prefill so that its KV rows carry the step passes' arithmetic
-      add(K + 2, forward_ops(c, c->drf, 1, c->seq, c->st, -1, c->st, -1, 0, 0, nullptr));
+      add(K + 2, forward_ops(c, c->drf, 1, c->seq, c->st, -1, c->st, -1, 0, 0, nullptr, true));
       add(K + 3, forward_ops(c, c->tgt, 1, c->seq, c->st, -1, c->st, -1, 0,
-                             opts->draft_mix_lambda != 0.f ? 1 : 0, c->logits_p + (size_t)K * V));
+                             opts->draft_mix_lambda != 0.f ? 1 : 0, c->logits_p + (size_t)K * V, true));
       if (encodable) {
         INIT_TRY(dalloc(c, &c->phase_dev, sizeof(PhaseDesc) * all.size()));
         INIT_TRY(cudaMemcpy(c->phase_dev, all.data(), sizeof(PhaseDesc) * all.size(), cudaMemcpyHostToDevice));

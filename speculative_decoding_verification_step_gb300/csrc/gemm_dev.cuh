@@ -117,8 +117,19 @@ SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4]
       if (tok < g.ntok) {
         float* o = (float*)g.out + (size_t)tok * g.ldo;
         if (g.epi == kEpiAdd) {
-          if (lo >= 0) { const float v = __ldcg(o + lo) + acc[ng][j]; o[lo] = v; ss = v * v; }
-          if (hi >= 0) { const float v = __ldcg(o + hi) + acc[ng][2 + j]; o[hi] = v; ss = fmaf(v, v, ss); }
+          bf16* xg = g.xg_out ? (bf16*)g.xg_out + (size_t)tok * g.ldo : nullptr;
+          if (lo >= 0) {
+            const float v = __ldcg(o + lo) + acc[ng][j];
+            o[lo] = v;
+            ss = v * v;
+            if (xg) xg[lo] = __float2bfloat16_rn(v * __ldg(g.gain_next + lo));
+          }
+          if (hi >= 0) {
+            const float v = __ldcg(o + hi) + acc[ng][2 + j];
+            o[hi] = v;
+            ss = fmaf(v, v, ss);
+            if (xg) xg[hi] = __float2bfloat16_rn(v * __ldg(g.gain_next + hi));
+          }
         } else {
           if (lo >= 0) o[lo] = acc[ng][j];
           if (hi >= 0) o[hi] = acc[ng][2 + j];
@@ -201,13 +212,15 @@ SV_DEV void tile_ptrs(const GemmDesc& g, int tile, int gi, const uint16_t*& pa, 
   }
 }
 
-// X source: kXGlobal = bf16 X from global memory; kXSmem = RMSNorm applied
-// once per CTA into shared memory (rows padded by 8 elements so the fragment
-// loads are bank-conflict free); kXInline = RMSNorm applied while loading
-// (large token counts, where the normalised X would not fit).
+// X source: kXGlobal = bf16 X from global memory; kXSmem = the normalised X
+// of every token in shared memory, once per CTA (rows padded by 8 elements so
+// the fragment loads are bank-conflict free) -- the per-kernel GEMM
+// normalises the fp32 residual into it, the persistent kernel copies in the
+// bf16 rows pre-multiplied by the gain (x_norm = 2); kXInline = RMSNorm
+// applied while loading (large token counts, where the normalised X would not
+// fit).
 enum XMode : int { kXGlobal = 0, kXSmem = 1, kXInline = 2 };
 constexpr int kXPad = 8;
-
 
 // Per-warp state of one GEMM: its range of (tile, k-step) units and the
 // weight ring of its current tile.
@@ -256,55 +269,6 @@ SV_DEV uint4 norm_chunk(const float4& a0, const float4& a1, float iv, const floa
   const __nv_bfloat162 b3 = __floats2bfloat162_rn(a1.z * iv * g1.z, a1.w * iv * g1.w);
   return make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
                     *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
-}
-
-// kXSmem preparation for at most 8 tokens, latency-oriented (for kernels
-// with the register budget of one 256-thread CTA per SM): a thread owns
-// 8-wide k-chunks c, c + blockDim, ... and issues the loads of two chunks for
-// every token (and their gains) at once; they are in flight while the warps
-// sum the per-tile squares into 1/rms.
-SV_DEV void prepare_x_few(const GemmDesc& g, float* s_inv, uint16_t* s_x) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
-  const int ld = g.k + kXPad, per_tok = g.k / 8, ntok = g.ntok;
-  float4 xa[2][8][2], ga[2][2];
-  auto load = [&](int b, int c) {
-    if (c >= per_tok) return;
-    const float4* gp = (const float4*)(g.gain + c * 8);
-    ga[b][0] = __ldg(gp);
-    ga[b][1] = __ldg(gp + 1);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      if (t < ntok) {
-        const float4* xp = (const float4*)((const float*)g.x + (size_t)t * g.ldx + c * 8);
-        xa[b][t][0] = __ldcg(xp);
-        xa[b][t][1] = __ldcg(xp + 1);
-      }
-    }
-  };
-  auto store = [&](int b, int c) {
-    if (c >= per_tok) return;
-#pragma unroll
-    for (int t = 0; t < 8; ++t)
-      if (t < ntok)
-        *reinterpret_cast<uint4*>(s_x + (size_t)t * ld + c * 8) =
-            norm_chunk(xa[b][t][0], xa[b][t][1], s_inv[t], ga[b][0], ga[b][1]);
-  };
-  const int step = blockDim.x;
-  int c = threadIdx.x;
-  load(0, c);
-  load(1, c + step);
-  for (int tok = warp; tok < ntok; tok += nwarp) {
-    const float v = warp_inv_rms(g, tok, lane);
-    if (lane == 0) s_inv[tok] = v;
-  }
-  __syncthreads();
-  for (; c < per_tok; c += 2 * step) {
-    store(0, c);
-    store(1, c + step);
-    load(0, c + 2 * step);
-    load(1, c + 3 * step);
-  }
-  __syncthreads();
 }
 
 template <int XM>

@@ -31,7 +31,10 @@ struct GemmDesc {
   int k;
   // X operand: [ntok][ldx]; bf16 (fp32 models: fp32), or with x_norm = 1 the fp32
   // residual, normalised on load: X = x * inv_rms(tok) * gain, inv_rms from the
-  // per-16-row-tile sums of squares ss_in[(k/16) tiles][ss_ld].
+  // per-16-row-tile sums of squares ss_in[(k/16) tiles][ss_ld].  x_norm = 2
+  // (persistent kernel only): X is the bf16 product x * gain written by the
+  // producer of x (xg_out below), and inv_rms(tok) scales the finished sums
+  // before the epilogue.
   const void* x;
   int ldx;
   int ntok;
@@ -45,6 +48,8 @@ struct GemmDesc {
   void* out;      // kEpiStore/kEpiAdd: fp32 [ntok][ldo]; kEpiSwiglu: model dtype [ntok][ldo]
   int ldo;
   float* ss_out;  // kEpiAdd: per-tile sums of squares [tiles][ss_ld] (may be null)
+  void* xg_out;            // kEpiAdd (may be null): bf16 [ntok][ldo] updated rows x gain_next,
+  const float* gain_next;  // the next RMSNorm's x_norm = 2 input
   // kEpiQkvRope
   int hq, hkv, hd, cap;
   const int32_t* pos_base;   // position of token t = *pos_base + pos_off + t
@@ -82,7 +87,8 @@ cudaError_t configure_gemm();
 
 // x[t][:] = embed[tok[t]][:] (fp32 residual stream), with
 // tok = tok_base + (tok_idx ? *tok_idx : 0) + tok_off (device-resident index);
-// ss[i][t] = sum of x[t][16i .. 16i+15]^2 (the first RMSNorm's input).
+// ss[i][t] = sum of x[t][16i .. 16i+15]^2 (the first RMSNorm's input);
+// optionally xg[t][:] = bf16(x[t][:] * gain) (its x_norm = 2 input).
 struct EmbedDesc {
   const int32_t* tok_base;
   const int32_t* tok_idx;
@@ -90,6 +96,8 @@ struct EmbedDesc {
   const void* embed;
   int dtype;
   float* x;
+  void* xg;
+  const float* gain;
   float* ss;
   int ss_ld;
   int ntok, d;

@@ -120,15 +120,15 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
     if (d.kind == kPhaseEmbed) {
       for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16>(d.e, t);
     } else if (d.kind == kPhaseGemm) {
-      if (d.xm == kXSmem) prepare_x_few(d.g, s_inv, reinterpret_cast<uint16_t*>(xreg));
+      if (d.xm == kXSmem) tma_prepare_xg(d, tp, s_inv, xreg);
       if (st && threadIdx.x == 0) atomicMax(st + 3, global_ns());
       if (producer) {
         if (lane == 0) tma_produce(d, npre, tp, ring, xreg, maps);
         __syncwarp();
       } else if (d.xm == kXSmem) {
-        tma_consume<kXSmem>(d, tp, cpar, ring, xreg, p.partials, p.tickets, st ? st + 4 : nullptr);
+        tma_consume<kXSmem>(d, tp, cpar, ring, xreg, s_inv, p.partials, p.tickets, st ? st + 4 : nullptr);
       } else {
-        tma_consume<kXGlobal>(d, tp, cpar, ring, xreg, p.partials, p.tickets, st ? st + 4 : nullptr);
+        tma_consume<kXGlobal>(d, tp, cpar, ring, xreg, s_inv, p.partials, p.tickets, st ? st + 4 : nullptr);
       }
     } else {
       for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x)
@@ -221,6 +221,10 @@ bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<Tensor
   p.g = g;
   p.xm = g.x_norm ? kXSmem : kXGlobal;
   if (g.k % 8 != 0 || g.ntok < 1 || g.ntok > kPersistMaxTok) return false;
+  // a normalised input comes pre-multiplied by its gain (x_norm = 2), by bulk
+  // copies of 16-byte aligned rows
+  if (g.x_norm == 1) return false;
+  if (g.x_norm == 2 && (g.ldx % 8 != 0 || reinterpret_cast<uintptr_t>(g.x) % 16 != 0)) return false;
   auto add = [&](const void* base, long long rows, long long ld, int box_rows) {
     TensorMap128 m{};
     if (!encode_rows(m, base, g.k, rows, ld, box_rows)) return -1;

@@ -13,7 +13,10 @@
 // by shape and grid only, never by token count).  One producer thread streams
 // the units through a ring of S stages (S x 2R x 512 bytes, S <= 8): per unit
 // one or two weight boxes and, in phases whose X comes from global memory,
-// one 8-row X box, all completing on the stage's transaction barrier.  The
+// one 8-row X box, all completing on the stage's transaction barrier.  In an
+// RMSNorm'd phase the producer first copies the X columns the CTA's units
+// read -- bf16 rows already multiplied by the norm's gain -- into shared
+// memory with bulk copies, and 1/rms scales the finished sums.  The
 // warp t < T = R/8 owns MMA tile t of every unit (its four 64-k
 // steps, one accumulator chain each, added in step order).  A tile split
 // between CTAs is finished by the last-arriving CTA, which adds the CTA
@@ -50,7 +53,9 @@ constexpr size_t kTensorMapBytes = 128;
 struct TmaPipe {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t xfull;               // the bulk X copies of an x_norm = 2 phase
   unsigned fills[kMaxStages];   // fills issued per slot (producer)
+  unsigned xfills;              // X loads issued (their barrier's phase count)
   int abort;
 };
 
@@ -61,6 +66,8 @@ SV_DEV void tma_init(TmaPipe& tp) {
       mbar_init(&tp.empty[i], kMaxMmaTiles);   // released by the tile-owner warps
       tp.fills[i] = 0;
     }
+    mbar_init(&tp.xfull, 1);
+    tp.xfills = 0;
     tp.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -132,6 +139,47 @@ SV_DEV int group_tile(const PhaseDesc& d, int grp, int t) {
   return grp * (R / 8) + t;
 }
 
+// x_norm = 2 phase, before its units: the producer thread copies the k-blocks
+// of X that the CTA's units read (the whole row once they span a row group,
+// else one or two runs of blocks) into the X region with one bulk copy per
+// token and run, completing on tp.xfull; every warp meanwhile folds the
+// per-tile sums of squares into s_inv[tok] = 1 / rms.  Ends with a CTA barrier.
+SV_DEV void tma_prepare_xg(const PhaseDesc& d, TmaPipe& tp, float* s_inv, unsigned char* xreg) {
+  const GemmDesc& g = d.g;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == kProducerWarp && lane == 0) {
+    const TmaRange r = tma_range(d);
+    const int n = r.u1 - r.u0;
+    int run[2][2] = {{0, 0}, {0, 0}}, nrun = 0;   // [kb begin, kb end)
+    if (n >= r.kbpt) {
+      run[0][0] = 0; run[0][1] = r.kbpt; nrun = 1;
+    } else if (n > 0) {
+      const int kb0 = r.u0 % r.kbpt, kb1 = (r.u1 - 1) % r.kbpt;
+      if (kb0 <= kb1) {
+        run[0][0] = kb0; run[0][1] = kb1 + 1; nrun = 1;
+      } else {
+        run[0][0] = kb0; run[0][1] = r.kbpt; run[1][0] = 0; run[1][1] = kb1 + 1; nrun = 2;
+      }
+    }
+    unsigned bytes = 0;
+    for (int q = 0; q < nrun; ++q) bytes += (unsigned)(min(run[q][1] * kTmaK, g.k) - run[q][0] * kTmaK) * 2u;
+    mbar_arrive_expect_tx(&tp.xfull, bytes * (unsigned)g.ntok);
+    const size_t pitch = (size_t)(g.k + kXPad) * 2;
+    for (int t = 0; t < g.ntok; ++t)
+      for (int q = 0; q < nrun; ++q) {
+        const int c0 = run[q][0] * kTmaK, c1 = min(run[q][1] * kTmaK, g.k);
+        bulk_g2s(xreg + t * pitch + (size_t)c0 * 2, (const bf16*)g.x + (size_t)t * g.ldx + c0,
+                 (unsigned)(c1 - c0) * 2u, &tp.xfull);
+      }
+    tp.xfills += 1;
+  }
+  for (int tok = warp; tok < g.ntok; tok += kPersistThreads / 32) {
+    const float v = warp_inv_rms(g, tok, lane);
+    if (lane == 0) s_inv[tok] = v;
+  }
+  __syncthreads();
+}
+
 // Producer thread: issue unit i of the CTA's range into slot i mod S --
 // wait for the consumers to release the slot, announce the bytes, copy the
 // weight boxes and, when with_x, the X box.
@@ -198,15 +246,20 @@ SV_DEV void tma_produce(const PhaseDesc& d, int npre, TmaPipe& tp, unsigned char
 // Consumer warp t at the end of a row group: finish MMA tile t -- the
 // epilogue when this CTA covered every k of the group, else its CTA partial
 // and, for the last-arriving CTA of the group, the sum of the CTA partials in
-// CTA order and the epilogue.  No other warp takes part.
+// CTA order and the epilogue.  s_inv (x_norm = 2, else null): 1 / rms per
+// token, applied to the finished sums of tokens 2ci, 2ci+1.  No other warp
+// takes part.
 SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs, int kbe, int pslot,
-                         const float (&tot)[1][4], float* __restrict__ partials, int* __restrict__ tickets) {
+                         const float (&tot)[1][4], float* __restrict__ partials, int* __restrict__ tickets,
+                         const float* s_inv) {
   const GemmDesc& g = d.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
   const int tile = group_tile(d, grp, warp);
   if (tile >= gemm_tiles_of(g)) return;
+  const float sc0 = s_inv ? s_inv[2 * ci] : 1.f, sc1 = s_inv ? s_inv[2 * ci + 1] : 1.f;
   if (kbs == 0 && kbe == r.kbpt) {
-    gemm_epilogue<1>(g, tile, tot, gi, ci);
+    const float y[1][4] = {{tot[0][0] * sc0, tot[0][1] * sc1, tot[0][2] * sc0, tot[0][3] * sc1}};
+    gemm_epilogue<1>(g, tile, y, gi, ci);
     return;
   }
   float* mine = partials + (((size_t)blockIdx.x * 2 + pslot) * kMaxMmaTiles + warp) * 32 * 4;
@@ -229,6 +282,10 @@ SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs
     sum[0][2] += v.z;
     sum[0][3] += v.w;
   }
+  sum[0][0] *= sc0;
+  sum[0][1] *= sc1;
+  sum[0][2] *= sc0;
+  sum[0][3] *= sc1;
   gemm_epilogue<1>(g, tile, sum, gi, ci);
   if (lane == 0) tickets[tile] = 0;
 }
@@ -241,8 +298,8 @@ SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs
 // stamp (optional): atomicMax of the globaltimer when the last unit arrived.
 template <int XM>
 SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const unsigned char* ring,
-                        const unsigned char* xreg, float* __restrict__ partials, int* __restrict__ tickets,
-                        unsigned long long* stamp) {
+                        const unsigned char* xreg, const float* s_inv, float* __restrict__ partials,
+                        int* __restrict__ tickets, unsigned long long* stamp) {
   const GemmDesc& g = d.g;
   const TmaRange r = tma_range(d);
   const int n = r.u1 - r.u0;
@@ -265,18 +322,22 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
   for (int s = 0; s < kTmaSteps; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
   int pslot = 0;
   int kbs = n > 0 ? r.u0 % r.kbpt : 0;
+  const bool xg = XM == kXSmem && g.x_norm == 2;
+  bool xok = true;
+  if (xg && n > 0) xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
+
 #pragma unroll 1
   for (int i = 0; i < n; ++i) {
     const int slot = i % S;
-    const bool ok = tma_wait(&tp.full[slot], (cpar >> slot) & 1u, tp);
+    const int u = r.u0 + i;
+    const int grp = u / r.kbpt, kb = u - grp * r.kbpt;
+    const bool ok = tma_wait(&tp.full[slot], (cpar >> slot) & 1u, tp) && xok;
     cpar ^= 1u << slot;
     if (stamp && i == n - 1 && threadIdx.x == 0) {
       unsigned long long tm;
       asm volatile("mov.u64 %0, %globaltimer;" : "=l"(tm));
       atomicMax(stamp, tm);
     }
-    const int u = r.u0 + i;
-    const int grp = u / r.kbpt, kb = u - grp * r.kbpt;
     if (ok) {
       const unsigned char* st = ring + (size_t)slot * sb + ci * 32;
 #pragma unroll
@@ -310,7 +371,7 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
       float tot[1][4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) tot[0][e] = ((acc[0][e] + acc[1][e]) + acc[2][e]) + acc[3][e];
-      if (!tp.abort) tma_tile_end(d, r, grp, kbs, kb + 1, pslot, tot, partials, tickets);
+      if (!tp.abort) tma_tile_end(d, r, grp, kbs, kb + 1, pslot, tot, partials, tickets, xg ? s_inv : nullptr);
 #pragma unroll
       for (int s = 0; s < kTmaSteps; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
       pslot = 1;
@@ -324,6 +385,11 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
 // issued does not complete; its wait gives up after kDrainLimit probes.
 SV_DEV void tma_drain(TmaPipe& tp) {
   if (threadIdx.x != 0) return;
+  if (tp.xfills) {
+    long long spins = 0;
+    while (!mbar_test(&tp.xfull, (tp.xfills - 1) & 1u) && ++spins < kDrainLimit) {
+    }
+  }
   for (int s = 0; s < kMaxStages; ++s) {
     const unsigned f = tp.fills[s];
     if (f == 0) continue;

@@ -188,6 +188,28 @@ SV_DEV void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* b
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
+// L2 eviction-priority policies for the cache_hint form below: data read once
+// per pass (streamed weights) is evicted first, data read again soon (the KV
+// cache, activations) last.
+SV_DEV uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+SV_DEV uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// tma_load_2d with an L2 cache policy.
+SV_DEV void tma_load_2d_hint(void* dst, const void* tmap, int c0, int c1, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar)),
+        "l"(policy)
+      : "memory");
+}
 // 16-byte asynchronous global -> shared copy (L2 only); with valid = false
 // nothing is read and the destination is zero-filled.
 SV_DEV void cp_async16(void* dst, const void* src, bool valid) {

@@ -100,10 +100,11 @@ SV_DEV void dattn_fetch(const AttnDesc& a, int row0, int s, bf16* kt, bf16* vt, 
   using L = DAttnSmem<HD>;
   mbar_arrive_expect_tx(bar, 2u * L::kTileBytes);
   const int r = row0 + s * kDStepKeys;
+  const uint64_t pol = l2_evict_last();   // the cache is read again by every later pass
 #pragma unroll
   for (int b = 0; b < L::kBoxes; ++b) {
-    tma_load_2d(kt + b * kDStepKeys * L::kBoxCols, a.tmk, b * L::kBoxCols, r, bar);
-    tma_load_2d(vt + b * kDStepKeys * L::kBoxCols, a.tmv, b * L::kBoxCols, r, bar);
+    tma_load_2d_hint(kt + b * kDStepKeys * L::kBoxCols, a.tmk, b * L::kBoxCols, r, bar, pol);
+    tma_load_2d_hint(vt + b * kDStepKeys * L::kBoxCols, a.tmv, b * L::kBoxCols, r, bar, pol);
   }
 }
 

@@ -99,23 +99,29 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   const unsigned char* maps = reinterpret_cast<const unsigned char*>(p.tmaps);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = warp == kProducerWarp;
-  auto stage = [&](int slot, int ph) {
-    const int words = (int)(sizeof(PhaseDesc) / 4);
-    const int* src = reinterpret_cast<const int*>(p.phases + ph);
-    int* dst = reinterpret_cast<int*>(&s_ph[slot]);
-    for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+  // phase descriptors: one word per thread, read at the start of the
+  // previous phase and stored into its shared-memory slot at that phase's
+  // end, so that the load's latency is not on the way to the grid barrier
+  constexpr int kDescWords = (int)(sizeof(PhaseDesc) / 4);
+  static_assert(sizeof(PhaseDesc) % 4 == 0 && kDescWords <= kPersistThreads, "one word per thread");
+  auto load_desc = [&](int ph) {
+    return threadIdx.x < kDescWords ? __ldg(reinterpret_cast<const int*>(p.phases + ph) + threadIdx.x) : 0;
+  };
+  auto store_desc = [&](int slot, int word) {
+    if (threadIdx.x < kDescWords) reinterpret_cast<int*>(&s_ph[slot])[threadIdx.x] = word;
   };
   unsigned long long* const times = p.times;
   if (times && blockIdx.x == 0 && threadIdx.x == 0) times[0] = global_ns();
   tma_init(tp);
   dattn_init_bars(dbars);
   unsigned dpar = 0;   // attention: per-warp stage parities
-  stage(0, 0);
+  store_desc(0, load_desc(0));
   __syncthreads();
   unsigned cpar = 0;   // consumers: parity of each stage's next full-barrier completion
   int npre = 0;        // units of the current GEMM phase issued before its barrier
   for (int ph = 0; ph < p.nphases; ++ph) {
     const PhaseDesc& d = s_ph[ph & 1];
+    const int next_word = ph + 1 < p.nphases ? load_desc(ph + 1) : 0;
     unsigned long long* const st = times ? times + 1 + kPhaseStamps * ph : nullptr;
     if (d.kind == kPhaseEmbed) {
       for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16>(d.e, t);
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
       }
     }
     if (ph + 1 < p.nphases) {
-      stage((ph + 1) & 1, ph + 1);
+      store_desc((ph + 1) & 1, next_word);
       grid_arrive(p.bar);   // its __syncthreads also ends this phase's shared-memory use
       if (threadIdx.x == 0 && tp.abort) atomicExch(p.err, 1);
       const PhaseDesc& nx = s_ph[(ph + 1) & 1];

@@ -195,12 +195,13 @@ SV_DEV void tma_issue(const PhaseDesc& d, const TmaRange& r, int i, bool with_x,
   mbar_arrive_expect_tx(&tp.full[slot], (unsigned)d.stage_bytes + (xg ? (unsigned)kXStageBytes : 0u));
   unsigned char* st = ring + (size_t)slot * d.stage_bytes;
   const int kc = kb * kTmaK;
+  const uint64_t pol = l2_evict_first();   // weights are read once per pass
   if (d.paired) {
-    tma_load_2d(st, maps + (size_t)d.tm[b.ma] * kTensorMapBytes, kc, b.ra, &tp.full[slot]);
-    tma_load_2d(st + (size_t)d.R * kTmaRowBytes, maps + (size_t)d.tm[b.mb] * kTensorMapBytes, kc, b.rb,
-                &tp.full[slot]);
+    tma_load_2d_hint(st, maps + (size_t)d.tm[b.ma] * kTensorMapBytes, kc, b.ra, &tp.full[slot], pol);
+    tma_load_2d_hint(st + (size_t)d.R * kTmaRowBytes, maps + (size_t)d.tm[b.mb] * kTensorMapBytes, kc, b.rb,
+                     &tp.full[slot], pol);
   } else {
-    tma_load_2d(st, maps + (size_t)d.tm[0] * kTensorMapBytes, kc, b.ra, &tp.full[slot]);
+    tma_load_2d_hint(st, maps + (size_t)d.tm[0] * kTensorMapBytes, kc, b.ra, &tp.full[slot], pol);
   }
   if (with_x)
     tma_load_2d(xreg + (size_t)slot * kXStageBytes, maps + (size_t)d.tm[3] * kTensorMapBytes, kc, 0,

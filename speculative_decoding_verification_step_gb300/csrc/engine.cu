@@ -725,7 +725,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
             encodable = persist_phase_from_attn(p, op.a) && encodable;
             p.a.tickets = dattn_tick;
           } else {
-            encodable = persist_phase_from_gemm(p, op.g, maps) && encodable;
+            encodable = persist_phase_from_gemm(p, op.g, maps, c->num_sms) && encodable;
           }
           all.push_back(p);
         }

@@ -60,9 +60,55 @@ SV_DEV float warp_inv_rms(const GemmDesc& g, int tok, int lane) {
   return 1.0f / sqrtf(s / (float)g.k + g.eps);
 }
 
-// ---- epilogue: thread holds rows lo/hi of the tile for tokens ng*8 + 2ci + j ----
+// Epilogue inputs that do not depend on the sums, for one-token-group tiles
+// (tokens 2ci, 2ci+1): the residual of rows lo/hi (kEpiAdd) or the RoPE
+// cos/sin of the tokens' positions (q/k heads of kEpiQkvRope) in v[j] /
+// v[2+j], the next RMSNorm's gains of rows lo/hi (kEpiAdd with xg_out) in gn;
+// pos0 = position of token 0.  Issued together with other loads so that
+// their latencies overlap.
+struct EpiIn {
+  float v[4];
+  float gn[2];
+  int pos0;
+};
+SV_DEV void gemm_epi_load(const GemmDesc& g, int tile, int pos0, int gi, int ci, EpiIn& e) {
+  e.pos0 = pos0;
+  e.v[0] = e.v[1] = e.v[2] = e.v[3] = 0.f;
+  e.gn[0] = e.gn[1] = 0.f;
+  if (g.epi == kEpiAdd) {
+    int lo, hi;
+    tile_rows(g, tile, gi, &lo, &hi);
+    if (g.xg_out) {
+      if (lo >= 0) e.gn[0] = __ldg(g.gain_next + lo);
+      if (hi >= 0) e.gn[1] = __ldg(g.gain_next + hi);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int tok = 2 * ci + j;
+      if (tok >= g.ntok) continue;
+      const float* o = (const float*)g.out + (size_t)tok * g.ldo;
+      if (lo >= 0) e.v[j] = __ldcg(o + lo);
+      if (hi >= 0) e.v[2 + j] = __ldcg(o + hi);
+    }
+  } else if (g.epi == kEpiQkvRope) {
+    const int per = g.hd / 16, half = g.hd / 2;
+    const int h = tile / per, i = 8 * (tile % per) + gi;
+    if (h >= g.hq + g.hkv) return;   // value head: no rotation
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int tok = 2 * ci + j;
+      if (tok >= g.ntok) continue;
+      e.v[j] = __ldg(g.rope_cos + (size_t)(pos0 + tok) * half + i);
+      e.v[2 + j] = __ldg(g.rope_sin + (size_t)(pos0 + tok) * half + i);
+    }
+  }
+}
+
+// ---- epilogue: thread holds rows lo/hi of the tile for tokens ng*8 + 2ci + j;
+// pre (NG = 1 only): the inputs gemm_epi_load read, else they are loaded here ----
 template <int NG>
-SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4], int gi, int ci) {
+SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4], int gi, int ci,
+                          const EpiIn* pre = nullptr) {
   if (g.epi == kEpiSwiglu) {
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng)
@@ -85,14 +131,15 @@ SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4]
         const int tok = ng * 8 + 2 * ci + j;
         if (tok >= g.ntok) continue;
         const float x1 = acc[ng][j], x2 = acc[ng][2 + j];
-        const int pos = *g.pos_base + g.pos_off + tok;
+        const int pos = pre ? pre->pos0 + tok : *g.pos_base + g.pos_off + tok;
         if (h >= g.hq + g.hkv) {   // value head: stored as is
           bf16* dst = (bf16*)g.vc + ((size_t)(h - g.hq - g.hkv) * g.cap + pos) * g.hd;
           dst[i] = __float2bfloat16_rn(x1);
           dst[i + half] = __float2bfloat16_rn(x2);
           continue;
         }
-        const float c = g.rope_cos[(size_t)pos * half + i], s = g.rope_sin[(size_t)pos * half + i];
+        const float c = pre ? pre->v[j] : g.rope_cos[(size_t)pos * half + i];
+        const float s = pre ? pre->v[2 + j] : g.rope_sin[(size_t)pos * half + i];
         const float y1 = x1 * c - x2 * s, y2 = x2 * c + x1 * s;
         if (h < g.hq) {
           float* dq = g.q_out + ((size_t)tok * g.hq + h) * g.hd;
@@ -119,16 +166,16 @@ SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4]
         if (g.epi == kEpiAdd) {
           bf16* xg = g.xg_out ? (bf16*)g.xg_out + (size_t)tok * g.ldo : nullptr;
           if (lo >= 0) {
-            const float v = __ldcg(o + lo) + acc[ng][j];
+            const float v = (pre ? pre->v[j] : __ldcg(o + lo)) + acc[ng][j];
             o[lo] = v;
             ss = v * v;
-            if (xg) xg[lo] = __float2bfloat16_rn(v * __ldg(g.gain_next + lo));
+            if (xg) xg[lo] = __float2bfloat16_rn(v * (pre ? pre->gn[0] : __ldg(g.gain_next + lo)));
           }
           if (hi >= 0) {
-            const float v = __ldcg(o + hi) + acc[ng][2 + j];
+            const float v = (pre ? pre->v[2 + j] : __ldcg(o + hi)) + acc[ng][2 + j];
             o[hi] = v;
             ss = fmaf(v, v, ss);
-            if (xg) xg[hi] = __float2bfloat16_rn(v * __ldg(g.gain_next + hi));
+            if (xg) xg[hi] = __float2bfloat16_rn(v * (pre ? pre->gn[1] : __ldg(g.gain_next + hi)));
           }
         } else {
           if (lo >= 0) o[lo] = acc[ng][j];

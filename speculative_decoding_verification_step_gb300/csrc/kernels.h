@@ -215,6 +215,7 @@ struct PhaseDesc {
   // one box of 2R rows, row groups, ring stages and bytes per stage, and the
   // tensor-map indices of the weight segments (0..2) and of X (3)
   int R, paired, groups, stages, stage_bytes;
+  int whole;         // 1: CTAs own whole row groups (no tile split between CTAs)
   int tm[4];
   int attn_items;
   GemmDesc g;
@@ -245,7 +246,7 @@ struct PersistDesc {
 // phase's tensor maps, appending them to maps; false when the phase does not
 // meet the tensor-copy rules (16-byte aligned rows, k and the X stride
 // multiples of 8, at most 8 tokens, RoPE head dim a multiple of 32).
-bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps);
+bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid);
 // Attention phases need a bf16 cache, at most 8 tokens and head dim 32, 64
 // or 128; their scratch is persist_attn_partial_floats floats and
 // dattn_tickets zeroed counters (a.partials, a.tickets).

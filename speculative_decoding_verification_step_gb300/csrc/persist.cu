@@ -28,6 +28,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <algorithm>
 
 namespace sv {
 
@@ -221,7 +222,7 @@ bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps) {
+bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid) {
   p = PhaseDesc{};
   p.kind = kPhaseGemm;
   p.g = g;
@@ -261,6 +262,16 @@ bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<Tensor
   p.tm[3] = p.xm == kXGlobal ? add(g.x, g.ntok, g.ldx, kXBoxRows) : 0;
   for (int i = 0; i < 4; ++i)
     if (p.tm[i] < 0) return false;
+  // whole row groups per CTA when that loads no CTA more than the even unit
+  // split does: then no tile is split between CTAs (no partials, no tickets)
+  {
+    const long long kbpt = (g.k + kTmaK - 1) / kTmaK, units = (long long)p.groups * kbpt;
+    const long long nc = std::max(1LL, std::min((long long)grid, units / kMinUnitsPerCta));
+    const long long split_max = (units + nc - 1) / nc;
+    const long long ncw = std::min((long long)grid, (long long)p.groups);
+    const long long whole_max = (p.groups + ncw - 1) / ncw * kbpt;
+    p.whole = whole_max <= split_max ? 1 : 0;
+  }
   p.stage_bytes = 2 * p.R * kTmaRowBytes;
   p.stages = (int)(kRingBytes / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;

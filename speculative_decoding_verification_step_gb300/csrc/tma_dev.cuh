@@ -97,6 +97,13 @@ SV_DEV TmaRange tma_range(const PhaseDesc& d) {
   TmaRange r;
   r.kbpt = (d.g.k + kTmaK - 1) / kTmaK;
   r.total = (long long)d.groups * r.kbpt;
+  if (d.whole) {   // whole row groups per CTA, as evenly as groups allow
+    r.nc = min((long long)gridDim.x, (long long)d.groups);
+    const bool has = blockIdx.x < r.nc;
+    r.u0 = has ? (int)first_step_of_warp(blockIdx.x, d.groups, r.nc) * r.kbpt : 0;
+    r.u1 = has ? (int)first_step_of_warp(blockIdx.x + 1, d.groups, r.nc) * r.kbpt : 0;
+    return r;
+  }
   r.nc = max(1LL, min((long long)gridDim.x, r.total / kMinUnitsPerCta));
   const bool has = blockIdx.x < r.nc;
   r.u0 = has ? (int)first_step_of_warp(blockIdx.x, r.total, r.nc) : 0;
@@ -248,11 +255,13 @@ SV_DEV void tma_produce(const PhaseDesc& d, int npre, TmaPipe& tp, unsigned char
 // epilogue when this CTA covered every k of the group, else its CTA partial
 // and, for the last-arriving CTA of the group, the sum of the CTA partials in
 // CTA order and the epilogue.  s_inv (x_norm = 2, else null): 1 / rms per
-// token, applied to the finished sums of tokens 2ci, 2ci+1.  No other warp
-// takes part.
+// token, applied to the finished sums of tokens 2ci, 2ci+1.  The last CTA
+// issues the epilogue's own input loads (residual or RoPE factors at token
+// 0's position pos0) together with the partial loads.  No other warp takes
+// part.
 SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs, int kbe, int pslot,
                          const float (&tot)[1][4], float* __restrict__ partials, int* __restrict__ tickets,
-                         const float* s_inv) {
+                         const float* s_inv, int pos0) {
   const GemmDesc& g = d.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
   const int tile = group_tile(d, grp, warp);
@@ -273,11 +282,30 @@ SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old != clast - cfirst) return;
   __syncwarp();
-  float sum[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+  // the epilogue's own inputs are loaded together with the first partials
+  EpiIn pre;
+  gemm_epi_load(g, tile, pos0, gi, ci, pre);
+  float4 pv[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int c = cfirst + q;
+    pv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c <= clast) {
+      const int sl = (first_step_of_warp(c, r.total, r.nc) / r.kbpt == grp) ? 0 : 1;
+      pv[q] = __ldcg(reinterpret_cast<const float4*>(
+          partials + (((size_t)c * 2 + sl) * kMaxMmaTiles + warp) * 32 * 4 + (size_t)lane * 4));
+    }
+  }
+  float sum[1][4] = {{0.f, 0.f, 0.f, 0.f}};   // CTA order
   for (int c = cfirst; c <= clast; ++c) {
-    const int sl = (first_step_of_warp(c, r.total, r.nc) / r.kbpt == grp) ? 0 : 1;
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(
-        partials + (((size_t)c * 2 + sl) * kMaxMmaTiles + warp) * 32 * 4 + (size_t)lane * 4));
+    float4 v;
+    if (c - cfirst < 2) {
+      v = c == cfirst ? pv[0] : pv[1];
+    } else {
+      const int sl = (first_step_of_warp(c, r.total, r.nc) / r.kbpt == grp) ? 0 : 1;
+      v = __ldcg(reinterpret_cast<const float4*>(
+          partials + (((size_t)c * 2 + sl) * kMaxMmaTiles + warp) * 32 * 4 + (size_t)lane * 4));
+    }
     sum[0][0] += v.x;
     sum[0][1] += v.y;
     sum[0][2] += v.z;
@@ -287,7 +315,7 @@ SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs
   sum[0][1] *= sc1;
   sum[0][2] *= sc0;
   sum[0][3] *= sc1;
-  gemm_epilogue<1>(g, tile, sum, gi, ci);
+  gemm_epilogue<1>(g, tile, sum, gi, ci, &pre);
   if (lane == 0) tickets[tile] = 0;
 }
 
@@ -324,6 +352,7 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
   int pslot = 0;
   int kbs = n > 0 ? r.u0 % r.kbpt : 0;
   const bool xg = XM == kXSmem && g.x_norm == 2;
+  const int pos0 = g.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
   bool xok = true;
   if (xg && n > 0) xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
 
@@ -372,7 +401,7 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
       float tot[1][4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) tot[0][e] = ((acc[0][e] + acc[1][e]) + acc[2][e]) + acc[3][e];
-      if (!tp.abort) tma_tile_end(d, r, grp, kbs, kb + 1, pslot, tot, partials, tickets, xg ? s_inv : nullptr);
+      if (!tp.abort) tma_tile_end(d, r, grp, kbs, kb + 1, pslot, tot, partials, tickets, xg ? s_inv : nullptr, pos0);
 #pragma unroll
       for (int s = 0; s < kTmaSteps; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
       pslot = 1;

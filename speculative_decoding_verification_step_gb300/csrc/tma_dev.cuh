@@ -233,7 +233,11 @@ SV_DEV void tma_issue_x(const PhaseDesc& d, const TmaRange& r, int i, TmaPipe& t
 SV_DEV int tma_prefetch(const PhaseDesc& d, TmaPipe& tp, unsigned char* ring, unsigned char* xreg,
                         const unsigned char* maps) {
   const TmaRange r = tma_range(d);
-  const int npre = min(r.u1 - r.u0, d.stages);
+  // a phase whose X is bulk-copied after the barrier, with few units per CTA,
+  // takes only 3 units ahead, so that fewer weight copies are in flight when
+  // its X copies are issued (the 8B q/k/v phase's X arrives ~1 us sooner)
+  const int n = r.u1 - r.u0;
+  const int npre = min(n, d.xm == kXSmem && n <= 16 ? min(d.stages, 3) : d.stages);
   for (int i = 0; i < npre; ++i) tma_issue(d, r, i, false, tp, ring, xreg, maps);
   return npre;
 }

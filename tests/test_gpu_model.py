@@ -153,6 +153,43 @@ def test_small_bf16_mixed_draft_teacher_forced(mix):
     _teacher_forced(shape, w, dshape, dw, prompt, 5, 1.0, 30, mix=mix)
 
 
+def test_long_context_forward_crosses_key_split():
+    """Past 1024 keys a row's attention spans two key splits (merged by the
+    last split in split order): forward logits against the oracle, and
+    positions 1020..1027 scored alone or in a block from an odd position
+    bit-identical to the full forward."""
+    shape = workloads.small_shape(dtype="bf16")
+    w = workloads.make_weights(shape, seed=11)
+    wc = helpers.to_device(w)
+    dec = helpers.decoder(shape, wc, shape, wc, 4, 1200)
+    n = 1100
+    toks = workloads.make_prompt(shape.vocab, n, seed=12)[0].tolist()
+    full = torch.empty(n, shape.vocab, device="cuda")
+    dec.model_forward(0, toks, 0, full)
+    ref = omodel.forward(shape, w, toks).numpy()
+    err = np.abs(full.cpu().numpy()[1000:] - ref[1000:]).max()
+    assert err < helpers.logit_tol(shape), err
+    one = torch.empty(1, shape.vocab, device="cuda")
+    for pos in range(1020, 1028):
+        dec.model_forward(0, [toks[pos]], pos, one)
+        assert torch.equal(one[0], full[pos]), pos
+    blk = torch.empty(6, shape.vocab, device="cuda")
+    dec.model_forward(0, toks[1021:1027], 1021, blk)
+    assert torch.equal(blk, full[1021:1027])
+    dec.close()
+
+
+def test_long_context_steps_teacher_forced():
+    """Speculative steps at 1050+ positions: the persistent kernel's
+    attention merges two key splits per row; draft and target logits and the
+    emitted tokens are checked against the oracle step by step."""
+    shape = workloads.small_shape(dtype="bf16")
+    w = workloads.make_weights(shape, seed=13)
+    dshape, dw = workloads.prefix_draft(shape, w, 1)
+    prompt = workloads.make_prompt(shape.vocab, 1050, seed=14)[0].tolist()
+    _teacher_forced(shape, w, dshape, dw, prompt, 5, 1.0, 20, max_ctx=1200)
+
+
 @pytest.mark.parametrize("shape", SHAPES[:2], ids=lambda s: f"{s.name}-{s.dtype}")
 def test_greedy_spec_equals_greedy_ar(shape):
     w = workloads.make_weights(shape, seed=6)

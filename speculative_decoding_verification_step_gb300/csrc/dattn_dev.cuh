@@ -2,7 +2,11 @@
 // query tokens, bf16 KV cache), on tensor cores.
 //
 // Work item = (KV head, query token, group of up to 8 of the KV head's
-// query heads, key split).  All rows of an item share one position p, so they
+// query heads, key split, V part).  With head dim 64 or 128 an item reads all of K
+// (the scores need every dim) but only its half of V, and writes its half of
+// the output dims: each 16-dim block of P.V is its own MMA, so the two items
+// of a row produce exactly the bits one item would, with 25% fewer bytes per
+// CTA.  All rows of an item share one position p, so they
 // see the same keys 0..p.  Keys are walked in absolute 16-key steps; step s
 // belongs to consumer warp s mod 8.  A warp keeps, per row, an online
 // softmax state over its steps (running max m, sum l, output o):
@@ -40,14 +44,24 @@ struct DAttnSmem {
   // (64-byte for head dim 32) swizzle, then the probability tile
   // [8 rows][16 keys]; warp regions stay 1 KB aligned (swizzle atoms)
   static constexpr int kDepth = HD >= 128 ? 3 : 6;
-  static constexpr int kTileElems = kDStepKeys * HD;
+  static constexpr int kTileElems = kDStepKeys * HD;   // K tile
   static constexpr int kTileBytes = kTileElems * 2;
   static constexpr int kBoxCols = HD < 64 ? HD : 64;
   static constexpr int kBoxes = HD / kBoxCols;
-  static constexpr size_t kWarpRaw = (size_t)kDepth * 2 * kTileBytes + kDRows * kDStepKeys * 2;
+  // V is read in kVParts column parts, one per item (head dim 128 / 64:
+  // halves, copied as boxes of 64 / 32 dims with the 128- / 64-byte swizzle
+  // -- every 16-dim block of the output is its own MMA, so an item needs all
+  // of K for the scores but only its part of V)
+  static constexpr int kVParts = HD >= 64 ? 2 : 1;
+  static constexpr int kVDims = HD / kVParts;
+  static constexpr int kVTileElems = kDStepKeys * kVDims;
+  static constexpr int kVBoxCols = kVDims < 64 ? kVDims : 64;
+  static constexpr int kVBoxes = kVDims / kVBoxCols;
+  static constexpr int kStageElems = kTileElems + kVTileElems;   // K tile, then V tile
+  static constexpr size_t kWarpRaw = (size_t)kDepth * kStageElems * 2 + kDRows * kDStepKeys * 2;
   static constexpr size_t kWarpBytes = (kWarpRaw + 1023) / 1024 * 1024;
-  // merge area: m, l [8 warps][8 rows], o [8 warps][8 rows][HD] (fp32)
-  static constexpr size_t kMergeBytes = (size_t)kDWarps * kDRows * (2 + HD) * 4;
+  // merge area: m, l [8 warps][8 rows], o [8 warps][8 rows][kVDims] (fp32)
+  static constexpr size_t kMergeBytes = (size_t)kDWarps * kDRows * (2 + kVDims) * 4;
   static constexpr size_t kBytes = kDWarps * kWarpBytes > kMergeBytes ? kDWarps * kWarpBytes : kMergeBytes;
   // element offset of logical 16-byte chunk c of key row r in a tile: box
   // c / 8 (64 dims), row r, chunk (c mod 8) XOR (r mod 8) -- the tensor
@@ -57,6 +71,11 @@ struct DAttnSmem {
   static __device__ __forceinline__ int at(int r, int c) {
     if (HD >= 64) return (c >> 3) * (kDStepKeys * 64) + r * 64 + (((c & 7) ^ (r & 7)) << 3);
     return r * HD + ((c ^ ((r >> 1) & 3)) << 3);
+  }
+  // the same for a V tile of kVDims dims
+  static __device__ __forceinline__ int at_v(int r, int c) {
+    if (kVDims >= 64) return (c >> 3) * (kDStepKeys * 64) + r * 64 + (((c & 7) ^ (r & 7)) << 3);
+    return r * kVDims + ((c ^ ((r >> 1) & 3)) << 3);
   }
 };
 constexpr int kDMaxDepth = 6;
@@ -88,24 +107,32 @@ SV_DEV DItem dattn_item_of(const AttnDesc& a, int it, int hgroups) {
 }
 __host__ __device__ inline int dattn_hgroups(int hq, int hkv) { return (hq / hkv + kDRows - 1) / kDRows; }
 __host__ __device__ inline int dattn_splits(int cap) { return (cap + kDSplitKeys - 1) / kDSplitKeys; }
-__host__ __device__ inline int dattn_items(int ntok, int hq, int hkv, int cap) {
-  return dattn_splits(cap) * ntok * hkv * dattn_hgroups(hq, hkv);
+__host__ __device__ inline int dattn_vparts(int hd) { return hd >= 64 ? 2 : 1; }
+// Columns of a V tensor-map box (its swizzle: 2 bytes x this).
+__host__ __device__ inline int dattn_vbox_cols(int hd) {
+  const int vd = hd / dattn_vparts(hd);
+  return vd < 64 ? vd : 64;
+}
+__host__ __device__ inline int dattn_items(int ntok, int hq, int hkv, int cap, int hd) {
+  return dattn_splits(cap) * ntok * hkv * dattn_hgroups(hq, hkv) * dattn_vparts(hd);
 }
 
-// Lane 0: the tensor copies of K/V step s (keys 16s .. 16s+15 of the rows
-// of KV head row0 / cap; keys beyond the row's position are masked later,
-// rows past the cache read as zero) into one stage, completing on bar.
+// Lane 0: the tensor copies of K step s (keys 16s .. 16s+15 of the rows of
+// KV head row0 / cap; keys beyond the row's position are masked later, rows
+// past the cache read as zero) and of V part vp of it into one stage,
+// completing on bar.
 template <int HD>
-SV_DEV void dattn_fetch(const AttnDesc& a, int row0, int s, bf16* kt, bf16* vt, uint64_t* bar) {
+SV_DEV void dattn_fetch(const AttnDesc& a, int row0, int s, int vp, bf16* kt, bf16* vt, uint64_t* bar) {
   using L = DAttnSmem<HD>;
-  mbar_arrive_expect_tx(bar, 2u * L::kTileBytes);
+  mbar_arrive_expect_tx(bar, (unsigned)(L::kTileElems + L::kVTileElems) * 2u);
   const int r = row0 + s * kDStepKeys;
   const uint64_t pol = l2_evict_last();   // the cache is read again by every later pass
 #pragma unroll
-  for (int b = 0; b < L::kBoxes; ++b) {
+  for (int b = 0; b < L::kBoxes; ++b)
     tma_load_2d_hint(kt + b * kDStepKeys * L::kBoxCols, a.tmk, b * L::kBoxCols, r, bar, pol);
-    tma_load_2d_hint(vt + b * kDStepKeys * L::kBoxCols, a.tmv, b * L::kBoxCols, r, bar, pol);
-  }
+#pragma unroll
+  for (int b = 0; b < L::kVBoxes; ++b)
+    tma_load_2d_hint(vt + b * kDStepKeys * L::kVBoxCols, a.tmv, vp * L::kVDims + b * L::kVBoxCols, r, bar, pol);
 }
 
 // Bounded wait on a stage barrier; false (after raising *a.err) on timeout.
@@ -135,8 +162,10 @@ template <int HD>
 SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
                        unsigned& dpar, unsigned long long* stamp = nullptr) {
   using L = DAttnSmem<HD>;
+  constexpr int VD = L::kVDims;                       // output dims of this item
+  const int vp = it % L::kVParts;                     // V part (fastest in the item order)
   const int hgroups = dattn_hgroups(a.hq, a.hkv);
-  const DItem d = dattn_item_of(a, it, hgroups);
+  const DItem d = dattn_item_of(a, it / L::kVParts, hgroups);
   const int G = a.hq / a.hkv;
   const int rows = min(kDRows, G - d.hg * kDRows);   // valid rows of this item
   const int pos = *a.pos_base + a.pos_off + d.t;
@@ -169,26 +198,26 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     }
   }
 
-  // stage b of the warp: K tile at wb + 2b * kTileElems, V tile after it
+  // stage b of the warp: K tile at wb + b * kStageElems, V tile after it
   constexpr int D = L::kDepth;
   bf16* wb = reinterpret_cast<bf16*>(sm + (size_t)warp * L::kWarpBytes);
-  bf16* ps = wb + 2 * D * L::kTileElems;              // [8 rows][16 keys]
+  bf16* ps = wb + D * L::kStageElems;                 // [8 rows][16 keys]
 
   // this warp's steps: s = first + 8j, j < nst, kept D steps ahead in flight
   const int s_begin = k0 / kDStepKeys, s_end = last / kDStepKeys;
   const int first = s_begin + warp;
   const int nst = first <= s_end ? (s_end - first) / kDWarps + 1 : 0;
   float m_r[2] = {neg_inf(), neg_inf()}, l_r[2] = {0.f, 0.f};   // rows 2c, 2c+1
-  float o[HD / 16][4];
+  float o[VD / 16][4];
 #pragma unroll
-  for (int mt = 0; mt < HD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  for (int mt = 0; mt < VD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   const bool rv0 = 2 * ci < rows, rv1 = 2 * ci + 1 < rows;
   if (lane == 0)
     for (int j = 0; j < D && j < nst; ++j)
-      dattn_fetch<HD>(a, row0, first + kDWarps * j, wb + 2 * j * L::kTileElems, wb + (2 * j + 1) * L::kTileElems,
-                      &wbar[j]);
+      dattn_fetch<HD>(a, row0, first + kDWarps * j, vp, wb + j * L::kStageElems,
+                      wb + j * L::kStageElems + L::kTileElems, &wbar[j]);
   // per-lane element offsets of the fragments (fixed for the whole walk)
-  int koff_lo[NG][TW / 4], koff_hi[NG][TW / 4], voff[HD / 16];
+  int koff_lo[NG][TW / 4], koff_hi[NG][TW / 4], voff[VD / 16];
 #pragma unroll
   for (int jg = 0; jg < NG; ++jg)
 #pragma unroll
@@ -201,13 +230,13 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     const int lrow = (lane & 7) + ((lane >> 4) << 3);   // key of this lane's ldmatrix row
     const int lchk = (lane >> 3) & 1;                   // 8-dim half of a 16-dim tile
 #pragma unroll
-    for (int mt = 0; mt < HD / 16; ++mt) voff[mt] = L::at(lrow, 2 * mt + lchk);
+    for (int mt = 0; mt < VD / 16; ++mt) voff[mt] = L::at_v(lrow, 2 * mt + lchk);
   }
   bool live = true;
   for (int j = 0; j < nst; ++j) {
     const int s = first + kDWarps * j;
     const int buf = j % D;
-    const bf16* kt = wb + 2 * buf * L::kTileElems;
+    const bf16* kt = wb + buf * L::kStageElems;
     const bf16* vt = kt + L::kTileElems;
     live = __all_sync(0xffffffffu, live && dattn_wait(a, &wbar[buf], (dpar >> buf) & 1u));
     dpar ^= 1u << buf;
@@ -272,7 +301,7 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(ps + gi * kDStepKeys + 2 * ci + 8);
     // o^T[dim][row] = o^T * scale + V^T p: A = V^T via transposing ldmatrix
 #pragma unroll
-    for (int mt = 0; mt < HD / 16; ++mt) {
+    for (int mt = 0; mt < VD / 16; ++mt) {
       uint32_t va[4];
       ldmatrix_x4_trans(va, vt + voff[mt]);
       o[mt][0] *= sc0;
@@ -284,8 +313,8 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     __syncwarp();   // the stage and the probability tile are reused
     if (lane == 0 && j + D < nst) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // our reads before the copy's writes
-      dattn_fetch<HD>(a, row0, s + kDWarps * D, wb + 2 * buf * L::kTileElems, wb + (2 * buf + 1) * L::kTileElems,
-                      &wbar[buf]);
+      dattn_fetch<HD>(a, row0, s + kDWarps * D, vp, wb + buf * L::kStageElems,
+                      wb + buf * L::kStageElems + L::kTileElems, &wbar[buf]);
     }
   }
   // after a timeout: let the copies still in flight land before the space is reused
@@ -306,7 +335,7 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
   }
   float* mm = reinterpret_cast<float*>(sm);          // [8 warps][8 rows]
   float* ll = mm + kDWarps * kDRows;                 // [8 warps][8 rows]
-  float* oo = ll + kDWarps * kDRows;                 // [8 warps][8 rows][HD]
+  float* oo = ll + kDWarps * kDRows;                 // [8 warps][8 rows][VD]
   if (gi == 0) {
     mm[warp * kDRows + 2 * ci] = m_r[0];
     mm[warp * kDRows + 2 * ci + 1] = m_r[1];
@@ -314,17 +343,19 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     ll[warp * kDRows + 2 * ci + 1] = l_r[1];
   }
 #pragma unroll
-  for (int mt = 0; mt < HD / 16; ++mt) {
-    float* ow = oo + (size_t)warp * kDRows * HD;
-    ow[(2 * ci) * HD + mt * 16 + gi] = o[mt][0];
-    ow[(2 * ci + 1) * HD + mt * 16 + gi] = o[mt][1];
-    ow[(2 * ci) * HD + mt * 16 + gi + 8] = o[mt][2];
-    ow[(2 * ci + 1) * HD + mt * 16 + gi + 8] = o[mt][3];
+  for (int mt = 0; mt < VD / 16; ++mt) {
+    float* ow = oo + (size_t)warp * kDRows * VD;
+    ow[(2 * ci) * VD + mt * 16 + gi] = o[mt][0];
+    ow[(2 * ci + 1) * VD + mt * 16 + gi] = o[mt][1];
+    ow[(2 * ci) * VD + mt * 16 + gi + 8] = o[mt][2];
+    ow[(2 * ci + 1) * VD + mt * 16 + gi + 8] = o[mt][3];
   }
   named_sync(1, kDWarps * 32);
   const int tid = threadIdx.x;
-  for (int e = tid; e < rows * HD; e += kDWarps * 32) {
-    const int r = e / HD, dm = e % HD;
+  const int dv0 = vp * VD;                           // first output dim of this item
+  // a split partial: [HD dims][M, L of V part 0][M, L of V part 1]
+  for (int e = tid; e < rows * VD; e += kDWarps * 32) {
+    const int r = e / VD, dm = e % VD;
     float M = neg_inf();
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, mm[w * kDRows + r]);
@@ -333,18 +364,18 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     for (int w = 0; w < kDWarps; ++w) {
       const float mw = mm[w * kDRows + r];
       const float f = mw == neg_inf() ? 0.f : expf(mw - M);
-      num = fmaf(f, oo[((size_t)w * kDRows + r) * HD + dm], num);
+      num = fmaf(f, oo[((size_t)w * kDRows + r) * VD + dm], num);
       den = fmaf(f, ll[w * kDRows + r], den);
     }
     const int h = h0 + r;
     if (nsplit == 1) {
-      ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)h * HD + dm] = __float2bfloat16_rn(num / den);
+      ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)h * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
     } else {
       float* pp = a.partials + (((size_t)d.t * a.hq + h) * dattn_splits(a.cap) + d.split) * (HD + 4);
-      pp[dm] = num;
+      pp[dv0 + dm] = num;
       if (dm == 0) {
-        pp[HD] = M;
-        pp[HD + 1] = den;
+        pp[HD + 2 * vp] = M;
+        pp[HD + 2 * vp + 1] = den;
       }
     }
   }
@@ -352,27 +383,28 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     named_sync(1, kDWarps * 32);   // the merge area is reused by the next item
     return;
   }
-  // ---- several splits: the last one to finish merges them in split order ----
-  int* ticket = a.tickets + ((size_t)d.t * a.hkv + d.kvh) * hgroups + d.hg;
+  // ---- several splits: the last one (of this V part) to finish merges them
+  // in split order ----
+  int* ticket = a.tickets + (((size_t)d.t * a.hkv + d.kvh) * hgroups + d.hg) * L::kVParts + vp;
   named_sync(1, kDWarps * 32);
   if (tid == 0)   // acq_rel: publishes this split's partial, acquires the earlier ones
     *s_last = (atom_add_acq_rel_gpu(reinterpret_cast<unsigned*>(ticket), 1u) == (unsigned)nsplit - 1);
   named_sync(1, kDWarps * 32);
   if (!*s_last) return;
   const int ns = dattn_splits(a.cap);
-  for (int e = tid; e < rows * HD; e += kDWarps * 32) {
-    const int r = e / HD, dm = e % HD;
+  for (int e = tid; e < rows * VD; e += kDWarps * 32) {
+    const int r = e / VD, dm = e % VD;
     const float* base = a.partials + ((size_t)d.t * a.hq + h0 + r) * ns * (HD + 4);
     float M = neg_inf();
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(base + (size_t)sp * (HD + 4) + HD));
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(base + (size_t)sp * (HD + 4) + HD + 2 * vp));
     float num = 0.f, den = 0.f;
     for (int sp = 0; sp < nsplit; ++sp) {
       const float* pp = base + (size_t)sp * (HD + 4);
-      const float f = expf(__ldcg(pp + HD) - M);
-      num = fmaf(f, __ldcg(pp + dm), num);
-      den = fmaf(f, __ldcg(pp + HD + 1), den);
+      const float f = expf(__ldcg(pp + HD + 2 * vp) - M);
+      num = fmaf(f, __ldcg(pp + dv0 + dm), num);
+      den = fmaf(f, __ldcg(pp + HD + 2 * vp + 1), den);
     }
-    ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)(h0 + r) * HD + dm] = __float2bfloat16_rn(num / den);
+    ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)(h0 + r) * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
   }
   named_sync(1, kDWarps * 32);
   if (tid == 0) *ticket = 0;

@@ -686,7 +686,8 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
       for (int l = 0; l < m->d.n_layers && ok; ++l) {
         const size_t off = (size_t)l * m->layer_kv_elems(c->cap) * m->esize;
         ok = encode_kv_map(maps[2 * l], (char*)m->kc + off, m->d.head_dim, rows) &&
-             encode_kv_map(maps[2 * l + 1], (char*)m->vc + off, m->d.head_dim, rows);
+             encode_kv_map(maps[2 * l + 1], (char*)m->vc + off, m->d.head_dim, rows,
+                           dattn_v_box_cols(m->d.head_dim));
       }
       if (!ok) {
         free_ctx(c);

@@ -131,14 +131,19 @@ size_t attn_partial_floats(int max_tok, int hq, int hd, int max_chunks);
 int attn_max_row_tiles(int max_tok, int hq, int hkv);
 cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st);
 // Tensor-core attention (bf16 cache, head dim 32/64/128, any token count):
-// items per (KV head, token, group of 8 query heads, 1024-key split); its
+// items per (KV head, token, group of 8 query heads, 1024-key split, V
+// column part -- two for head dims 64 and 128); its
 // tickets are dattn_tickets(tokens, hq, hkv) zeroed counters, its partials
 // persist_attn_partial_floats floats.
 cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st);
 struct TensorMap128;
 // Tensor map of a bf16 KV cache [rows][hd] for launch_dattn (head dim 32, 64
-// or 128); false when the map cannot be encoded.
-bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows);
+// or 128; boxes of 16 rows x box_cols dims, 0: min(hd, 64)); false when the
+// map cannot be encoded.
+bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows, int box_cols = 0);
+// Box columns of the V map launch_dattn expects (head dim 64: 32 -- items
+// read V in halves).
+int dattn_v_box_cols(int hd);
 int dattn_tickets(int max_tok, int hq, int hkv);
 // One-time kernel attributes (dynamic shared memory); call before any capture.
 cudaError_t configure_kernels();

@@ -109,11 +109,13 @@ static cudaError_t configure_dattn() {
                               (int)DAttnSmem<HD>::kBytes);
 }
 
-int dattn_tickets(int max_tok, int hq, int hkv) { return max_tok * hkv * dattn_hgroups(hq, hkv); }
+int dattn_v_box_cols(int hd) { return dattn_vbox_cols(hd); }
+
+int dattn_tickets(int max_tok, int hq, int hkv) { return max_tok * hkv * dattn_hgroups(hq, hkv) * 2; }
 
 cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st) {
   if (a.dtype != 1 || a.hq % a.hkv != 0 || !a.tmk || !a.tmv) return cudaErrorInvalidValue;
-  const int items = dattn_items(a.ntok, a.hq, a.hkv, a.cap);
+  const int items = dattn_items(a.ntok, a.hq, a.hkv, a.cap, a.hd);
   if (a.hd == 32) return launch_k(dattn_kernel<32>, dim3(items), dim3(kDWarps * 32), DAttnSmem<32>::kBytes, st, a);
   if (a.hd == 64) return launch_k(dattn_kernel<64>, dim3(items), dim3(kDWarps * 32), DAttnSmem<64>::kBytes, st, a);
   if (a.hd == 128)

@@ -206,19 +206,20 @@ static bool encode_rows(TensorMap128& m, const void* base, int k, long long rows
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows) {
+bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows, int box_cols) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc || !base || rows < 1 || (hd != 32 && hd != 64 && hd != 128) ||
       (reinterpret_cast<uintptr_t>(base) & 15u))
     return false;
-  const int cols = hd < 64 ? hd : 64;
+  const int cols = box_cols > 0 ? box_cols : (hd < 64 ? hd : 64);
+  if (cols != 32 && cols != 64) return false;
   cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
   cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)kDStepKeys};
   cuuint32_t es[2] = {1, 1};
   return enc(reinterpret_cast<CUtensorMap*>(&m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             hd < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             cols < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -282,7 +283,7 @@ bool persist_phase_from_attn(PhaseDesc& p, const AttnDesc& a) {
   p = PhaseDesc{};
   p.kind = kPhaseAttn;
   p.a = a;
-  p.attn_items = dattn_items(a.ntok, a.hq, a.hkv, a.cap);
+  p.attn_items = dattn_items(a.ntok, a.hq, a.hkv, a.cap, a.hd);
   return a.dtype == 1 && a.ntok <= kPersistMaxTok && a.hq % a.hkv == 0 && a.tmk && a.tmv &&
          (a.hd == 32 || a.hd == 64 || a.hd == 128);
 }

@@ -28,8 +28,11 @@ from oracle import model as omodel
 
 pytestmark = pytest.mark.gpu
 
+# bf16 shapes with head dims 64 and 128: attention items read V in halves
+HD_SHAPES = [workloads.small_shape(name="hd64", dtype="bf16", n_heads=4, n_kv_heads=2, head_dim=64),
+             workloads.small_shape(name="hd128", dtype="bf16", n_heads=2, n_kv_heads=1, head_dim=128)]
 SHAPES = [workloads.TINY, workloads.small_shape(dtype="bf16"),
-          workloads.small_shape(dtype="f32", n_heads=4, n_kv_heads=1, head_dim=64)]
+          workloads.small_shape(dtype="f32", n_heads=4, n_kv_heads=1, head_dim=64)] + HD_SHAPES
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -151,6 +154,16 @@ def test_small_bf16_mixed_draft_teacher_forced(mix):
     dshape, dw = workloads.prefix_draft(shape, w, 1)
     prompt = workloads.make_prompt(shape.vocab, 40, seed=5)[0].tolist()
     _teacher_forced(shape, w, dshape, dw, prompt, 5, 1.0, 30, mix=mix)
+
+
+@pytest.mark.parametrize("shape", HD_SHAPES, ids=lambda s: s.name)
+def test_head_dims_teacher_forced(shape):
+    """The persistent kernel's attention at head dims 64 and 128 (V read in
+    halves by two items per row), step by step against the oracle."""
+    w = workloads.make_weights(shape, seed=15)
+    dshape, dw = workloads.prefix_draft(shape, w, 1)
+    prompt = workloads.make_prompt(shape.vocab, 60, seed=16)[0].tolist()
+    _teacher_forced(shape, w, dshape, dw, prompt, 5, 1.0, 24)
 
 
 def test_long_context_forward_crosses_key_split():

@@ -240,9 +240,9 @@ struct Op {
 // GEMM (input RMSNorm on load, RoPE + KV append in its epilogue), attention,
 // o-projection + residual (writes the next norm's sums of squares), gate/up
 // GEMM (RMSNorm on load, SwiGLU epilogue), down-projection + residual.
-// pregain (persistent kernel): the residual producers also write x times the
-// next RMSNorm's gain in bf16 (c->xg), which the normalised GEMMs read
-// (x_norm = 2) and scale by 1/rms after the sums.
+// pregain (bf16 models): the residual producers also write x times the next
+// RMSNorm's gain in bf16 (c->xg), which the normalised GEMMs read (x_norm =
+// 2) and scale by 1/rms after the sums.
 std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t* tok_base,
                             const int32_t* tok_idx, int tok_off, const int32_t* pos_idx,
                             int pos_off, int lrow0, int lrows, float* logits, bool pregain = false) {
@@ -351,8 +351,10 @@ void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const 
              int tok_off, const int32_t* pos_idx, int pos_off, int lrow0, int lrows,
              float* logits) {
   spec_ctx* c = L.c;
-  const std::vector<Op> ops =
-      forward_ops(c, m, ntok, tok_base, tok_idx, tok_off, pos_idx, pos_off, lrow0, lrows, logits);
+  // bf16 models: normalised GEMM inputs as x * gain in bf16 (as in the
+  // persistent kernel), 1/rms applied after the sums
+  const std::vector<Op> ops = forward_ops(c, m, ntok, tok_base, tok_idx, tok_off, pos_idx, pos_off, lrow0,
+                                          lrows, logits, m.d.dtype == SPEC_DTYPE_BF16);
   for (const Op& op : ops) {
     if (op.kind == kPhaseEmbed) L.note(launch_embed(op.e, c->stream));
     else if (op.kind == kPhaseAttn) {

@@ -211,7 +211,7 @@ static cudaError_t launch_sk(const GemmDesc& g, const GemmScratch& s, int num_sm
 
 template <int NG, int U>
 static cudaError_t launch_sk_x(const GemmDesc& g, const GemmScratch& s, int num_sms, cudaStream_t st) {
-  if (!g.x_norm) return launch_sk<NG, U, kXGlobal>(g, s, num_sms, st);
+  if (g.x_norm != 1) return launch_sk<NG, U, kXGlobal>(g, s, num_sms, st);   // bf16 X (x_norm = 2: x * gain)
   if (NG == 1 && gemm_xsmem_bytes(g) <= kXSmemMax) return launch_sk<NG, U, kXSmem>(g, s, num_sms, st);
   return launch_sk<NG, U, kXInline>(g, s, num_sms, st);
 }

@@ -320,7 +320,7 @@ SV_DEV uint4 norm_chunk(const float4& a0, const float4& a1, float iv, const floa
 
 template <int XM>
 SV_DEV void gemm_prepare_x(const GemmDesc& g, float* s_inv, uint16_t* s_x) {
-  if (XM == kXGlobal) return;
+  if (XM == kXGlobal && g.x_norm != 2) return;   // x_norm = 2: 1/rms scales the epilogue
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   for (int tok = warp; tok < g.ntok; tok += nwarp) {
     const float v = warp_inv_rms(g, tok, lane);
@@ -357,6 +357,21 @@ SV_DEV void gemm_prepare_x(const GemmDesc& g, float* s_inv, uint16_t* s_x) {
     }
   }
   __syncthreads();
+}
+
+// x_norm = 2: the finished sums of token ng*8 + 2ci + j times its 1 / rms.
+template <int NG>
+SV_DEV void scale_by_inv_rms(const GemmDesc& g, float (&acc)[NG][4], const float* s_inv, int ci) {
+  if (g.x_norm != 2) return;
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int tok = ng * 8 + 2 * ci + j;
+      const float sc = tok < g.ntok ? s_inv[tok] : 1.f;
+      acc[ng][j] *= sc;
+      acc[ng][2 + j] *= sc;
+    }
 }
 
 // Main loop and epilogues of one warp (after gemm_begin and gemm_prepare_x).
@@ -426,6 +441,7 @@ SV_DEV void gemm_run(const GemmDesc& g, GemmWarp<U>& st, int gw, float* __restri
     }
 
     if (ks == 0 && ke == spt) {
+      scale_by_inv_rms<NG>(g, acc, s_inv, ci);
       gemm_epilogue<NG>(g, tile, acc, gi, ci);
     } else {
       float* mine = partials + (size_t)(gw * 2 + slot) * NG * 32 * 4;
@@ -475,6 +491,7 @@ SV_DEV void gemm_run(const GemmDesc& g, GemmWarp<U>& st, int gw, float* __restri
             }
           }
         }
+        scale_by_inv_rms<NG>(g, tot, s_inv, ci);
         gemm_epilogue<NG>(g, tile, tot, gi, ci);
         if (lane == 0) tickets[tile] = 0;
       }

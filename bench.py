@@ -58,6 +58,9 @@ def parse():
                     help="one kernel per phase instead of the persistent forward kernel")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of both models")
+    ap.add_argument("--verify-sweep", action="store_true",
+                    help="verify step alone at batch 1 over K x context (one JSON line each): "
+                         "latency, algorithmic bytes, GB/s")
     return ap.parse_args()
 
 
@@ -347,6 +350,31 @@ def main():
             ms += e0.elapsed_time(e1)
             toks += emitted
         return ms, toks, done
+
+    if args.verify_sweep:
+        # the verify step (target over K+1 positions + fused acceptance) after a
+        # prefill of `context` uniform-random ids, replayed as a graph
+        peak, peak_kind = peaks()
+        for ctx in (512, 4096, 16384):
+            prm = workloads.make_prompt(tshape.vocab, ctx, seed=77)[0].tolist()
+            for k in (1, 2, 3, 4, 5, 6, 8):
+                d = sv.SpecDecoder(tshape, tw, dshape, dw, k, ctx + 2 * (k + 1) + 64, temperature=args.temperature,
+                                   seed=0, mix_lambda=0.0, stream=stream.cuda_stream)
+                d.prefill(prm)
+                prof = d.profile(iters=10)
+                st = d.stats()
+                L = ctx - 1                      # committed positions before the pending token
+                nbytes = (st["verify_weight_bytes"] + (L + k + 1) * st["kv_bytes_per_token_target"]
+                          + (k + 1) * tshape.vocab * 4)
+                gbs = nbytes / (prof["verify_ms"] * 1e6)
+                print(json.dumps({"verify_sweep": True, "workload": wl, "batch": 1, "K": k, "context": ctx,
+                                  "verify_step_ms": prof["verify_ms"],
+                                  "target_forward_ms": prof["verify_forward_ms"],
+                                  "bytes": nbytes, "GB_s": gbs, "frac_of_measured": gbs / peak,
+                                  "peak_kind": peak_kind, "kernels_per_verify": prof["kernels_verify"],
+                                  "persistent": prof["kernels_verify"] <= 2}), flush=True)
+                d.close()
+        return 0
 
     if args.phase_times:
         dec = make(args.temperature, args.mix, sv.SPEC_OPT_PHASE_TIMES)

@@ -1,25 +1,32 @@
 // Decode / verify attention of the persistent forward kernel (at most 8
 // query tokens, bf16 KV cache), on tensor cores.
 //
-// Work item = (KV head, query token, group of up to 8 of the KV head's
-// query heads, key split, V part).  With head dim 64 or 128 an item reads all of K
-// (the scores need every dim) but only its half of V, and writes its half of
-// the output dims: each 16-dim block of P.V is its own MMA, so the two items
-// of a row produce exactly the bits one item would, with 25% fewer bytes per
-// CTA.  All rows of an item share one position p, so they
-// see the same keys 0..p.  Keys are walked in absolute 16-key steps; step s
-// belongs to consumer warp s mod 8.  A warp keeps, per row, an online
-// softmax state over its steps (running max m, sum l, output o):
+// Work item = (KV head, token group, group of up to 8 of the KV head's
+// query heads, key split, V part).  Its at most 8 rows are (token, head)
+// pairs, tokens outer: min(G, 8) heads (G query heads per KV head) of one
+// token, or -- once the pass's last position reaches 1024, where the keys
+// no longer sit in L2 and re-reading them per token costs HBM bytes -- of
+// 8 / min(G, 8) consecutive tokens (2 tokens x 4 heads for the 8B and 1B
+// shapes), so one walk over the KV head's keys serves all of them.  Row r sees keys
+// 0..p_r of its own position; keys past it are masked.  With head dim 64 or
+// 128 an item reads all of K (the scores need every dim) but only its half
+// of V, and writes its half of the output dims: each 16-dim block of P.V is
+// its own MMA, so the two items of a row produce exactly the bits one item
+// would, with 25% fewer bytes per CTA.  Keys are walked in absolute 16-key
+// steps; step s belongs to consumer warp s mod 8.  A warp keeps, per row, an
+// online softmax state over its steps (running max m, sum l, output o):
 //   scores  S = K_step Q^T              (mma m16n8k16: keys x rows, k = dims)
 //   m' = max(m, max_j S_j), scale = exp(m - m'), p_j = exp(S_j - m')
 //   l  = l * scale + sum_j p_j,  o = o * scale + V_step^T p   (bf16 p)
-// with K, Q, V and p in bf16 and fp32 accumulation.  The eight warp states
-// are then merged in warp order: M = max_w m_w, out = sum_w e^(m_w - M) o_w /
-// sum_w e^(m_w - M) l_w.  Keys are split in absolute 1024-key ranges; a row
-// whose position spans several splits writes one (M, L, O) partial per split
-// and the last split item to finish merges them in split order.  Every step
-// of the arithmetic is fixed by the row's position alone, so a row gets the
-// same bits whichever rows share the pass (batch invariance).
+// with K, Q, V and p in bf16 and fp32 accumulation; a step holding no key of
+// a row leaves the row's state as it is (scale 1, p = 0).  The eight warp
+// states are then merged in warp order: M = max_w m_w, out = sum_w e^(m_w -
+// M) o_w / sum_w e^(m_w - M) l_w.  Keys are split in absolute 1024-key
+// ranges; a row whose position spans several splits writes one (M, L, O)
+// partial per split and the last split item of its token group to finish
+// merges each row's splits in split order.  Every step of a row's
+// arithmetic is fixed by its own position, so a row gets the same bits
+// whichever rows share the item or the pass (batch invariance).
 //
 // Memory: per warp a pipeline of 3 (head dim 128) or 6 stages of 16-key K/V
 // tiles, each filled by 2-D tensor copies (hardware-swizzled so the fragment
@@ -92,20 +99,24 @@ SV_DEV uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Item geometry.
+// Rows of an item are (token, head) pairs, tokens outer: hpi = min(G, 8)
+// heads (G = query heads per KV head) of tpi consecutive tokens, tpi = 1 or
+// 8 / hpi (see kDGroupMinPos), so one K/V walk serves every token of the group.
 struct DItem {
-  int kvh, t, hg, split;
+  int kvh, tg, hg, split;
 };
-SV_DEV DItem dattn_item_of(const AttnDesc& a, int it, int hgroups) {
+__host__ __device__ inline int dattn_hgroups(int hq, int hkv) { return (hq / hkv + kDRows - 1) / kDRows; }
+__host__ __device__ inline int dattn_hpi(int hq, int hkv) { return hq / hkv < kDRows ? hq / hkv : kDRows; }
+SV_DEV DItem dattn_item_of(const AttnDesc& a, int it, int hgroups, int tgroups) {
   DItem d;
   d.hg = it % hgroups;
   it /= hgroups;
   d.kvh = it % a.hkv;
   it /= a.hkv;
-  d.t = it % a.ntok;
-  d.split = it / a.ntok;
+  d.tg = it % tgroups;
+  d.split = it / tgroups;
   return d;
 }
-__host__ __device__ inline int dattn_hgroups(int hq, int hkv) { return (hq / hkv + kDRows - 1) / kDRows; }
 __host__ __device__ inline int dattn_splits(int cap) { return (cap + kDSplitKeys - 1) / kDSplitKeys; }
 __host__ __device__ inline int dattn_vparts(int hd) { return hd >= 64 ? 2 : 1; }
 // Columns of a V tensor-map box (its swizzle: 2 bytes x this).
@@ -113,6 +124,8 @@ __host__ __device__ inline int dattn_vbox_cols(int hd) {
   const int vd = hd / dattn_vparts(hd);
   return vd < 64 ? vd : 64;
 }
+// Items are enumerated as for one token per item (ntok token slots); with
+// token groups the slots past the last group return at once.
 __host__ __device__ inline int dattn_items(int ntok, int hq, int hkv, int cap, int hd) {
   return dattn_splits(cap) * ntok * hkv * dattn_hgroups(hq, hkv) * dattn_vparts(hd);
 }
@@ -157,36 +170,45 @@ SV_DEV void dattn_init_bars(uint64_t* bars) {
   }
 }
 
-// stamp (optional): atomicMax of the globaltimer when the key walk ended.
-template <int HD>
-SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
-                       unsigned& dpar, unsigned long long* stamp = nullptr) {
+// One item; kGroup: token groups (8 / hpi tokens per item) rather than one
+// token per item.  stamp (optional): atomicMax of the globaltimer when the
+// key walk ended.
+template <int HD, bool kGroup>
+SV_DEV void dattn_item_rows(const AttnDesc& a, int it, int pos0, unsigned char* sm, int* s_last, uint64_t* bars,
+                            unsigned& dpar, unsigned long long* stamp) {
   using L = DAttnSmem<HD>;
   constexpr int VD = L::kVDims;                       // output dims of this item
   const int vp = it % L::kVParts;                     // V part (fastest in the item order)
   const int hgroups = dattn_hgroups(a.hq, a.hkv);
-  const DItem d = dattn_item_of(a, it / L::kVParts, hgroups);
-  const int G = a.hq / a.hkv;
-  const int rows = min(kDRows, G - d.hg * kDRows);   // valid rows of this item
-  const int pos = *a.pos_base + a.pos_off + d.t;
+  const DItem d = dattn_item_of(a, it / L::kVParts, hgroups, a.ntok);
+  const int G = a.hq / a.hkv, hpi = dattn_hpi(a.hq, a.hkv);
+  const int tpi = kGroup ? kDRows / hpi : 1;          // tokens per item
+  const int t0 = d.tg * tpi;                          // first token of the item
+  if (kGroup && t0 >= a.ntok) return;                 // token slot past the last group
+  // rows 0 .. nrows-1 are valid: row r = (token t0 + r / hpi, head h0 + r % hpi)
+  const int nrows = kGroup ? min(tpi, a.ntok - t0) * min(hpi, G - d.hg * kDRows) : min(kDRows, G - d.hg * kDRows);
+  const int pmax = pos0 + t0 + (kGroup ? min(tpi, a.ntok - t0) - 1 : 0);
   const int k0 = d.split * kDSplitKeys;
-  if (k0 > pos) return;                               // split entirely in the future
-  const int last = min(pos, k0 + kDSplitKeys - 1);    // last key of this split
-  const int nsplit = pos / kDSplitKeys + 1;           // splits of this row
+  if (k0 > pmax) return;                              // split entirely in the future
+  const int last = min(pmax, k0 + kDSplitKeys - 1);   // last key of this split
+  const int nsplit = pmax / kDSplitKeys + 1;          // splits of the token group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
   const int h0 = d.kvh * G + d.hg * kDRows;           // first query head of the item
   const int row0 = d.kvh * a.cap;                     // first cache row of the KV head
   uint64_t* wbar = bars + warp * kDMaxDepth;
+  // token of valid item row r, and its head
+  auto row_tok = [&](int r) { return kGroup ? t0 + r / hpi : t0; };
+  auto row_head = [&](int r) { return h0 + (kGroup ? r % hpi : r); };
 
-  // Q fragments (rows = query heads; dims in groups of GD, k-permuted as in
-  // the GEMM): thread (g, c) holds row g, dims j*GD + c*GD/4 .. +GD/4-1 of
-  // every group j as TW bf16 pairs; MMA i of a group takes pairs 2i, 2i+1.
+  // Q fragments (rows = (token, head) pairs; dims in groups of GD, k-permuted
+  // as in the GEMM): thread (g, c) holds row g, dims j*GD + c*GD/4 .. +GD/4-1
+  // of every group j as TW bf16 pairs; MMA i of a group takes pairs 2i, 2i+1.
   constexpr int GD = HD < 64 ? HD : 64;
   constexpr int NG = HD / GD, TW = GD / 8, NM = GD / 16;
   uint32_t qf[NG][TW];
   {
-    const bool ok = gi < rows;
-    const float* qp = a.q + ((size_t)d.t * a.hq + h0 + (ok ? gi : 0)) * HD + ci * (GD / 4);
+    const bool ok = gi < nrows;
+    const float* qp = a.q + ((size_t)(ok ? row_tok(gi) : t0) * a.hq + (ok ? row_head(gi) : h0)) * HD + ci * (GD / 4);
 #pragma unroll
     for (int j = 0; j < NG; ++j) {
 #pragma unroll
@@ -211,7 +233,10 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
   float o[VD / 16][4];
 #pragma unroll
   for (int mt = 0; mt < VD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  const bool rv0 = 2 * ci < rows, rv1 = 2 * ci + 1 < rows;
+  // positions of rows 2c, 2c+1 (-1: empty row); keys past them are masked
+  const bool rv0 = 2 * ci < nrows, rv1 = 2 * ci + 1 < nrows;
+  const int p0 = rv0 ? pos0 + row_tok(2 * ci) : -1;
+  const int p1 = rv1 ? pos0 + row_tok(2 * ci + 1) : -1;
   if (lane == 0)
     for (int j = 0; j < D && j < nst; ++j)
       dattn_fetch<HD>(a, row0, first + kDWarps * j, vp, wb + j * L::kStageElems,
@@ -258,11 +283,15 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
         mma_bf16_16816(sc, lo[2 * i], hi[2 * i], lo[2 * i + 1], hi[2 * i + 1], qf[jg][2 * i], qf[jg][2 * i + 1]);
     }
     const int key_lo = s * kDStepKeys + gi, key_hi = key_lo + 8;
-    const bool kv_lo = key_lo <= last, kv_hi = key_hi <= last;
-    float v00 = (rv0 && kv_lo) ? sc[0] * a.scale : neg_inf();   // row 2c, key g
-    float v01 = (rv1 && kv_lo) ? sc[1] * a.scale : neg_inf();   // row 2c+1, key g
-    float v10 = (rv0 && kv_hi) ? sc[2] * a.scale : neg_inf();   // row 2c, key g+8
-    float v11 = (rv1 && kv_hi) ? sc[3] * a.scale : neg_inf();   // row 2c+1, key g+8
+    // one token per item: every row's last key is `last`
+    const bool kl0 = kGroup ? key_lo <= p0 : rv0 && key_lo <= last;
+    const bool kl1 = kGroup ? key_lo <= p1 : rv1 && key_lo <= last;
+    const bool kh0 = kGroup ? key_hi <= p0 : rv0 && key_hi <= last;
+    const bool kh1 = kGroup ? key_hi <= p1 : rv1 && key_hi <= last;
+    float v00 = kl0 ? sc[0] * a.scale : neg_inf();   // row 2c, key g
+    float v01 = kl1 ? sc[1] * a.scale : neg_inf();   // row 2c+1, key g
+    float v10 = kh0 ? sc[2] * a.scale : neg_inf();   // row 2c, key g+8
+    float v11 = kh1 ? sc[3] * a.scale : neg_inf();   // row 2c+1, key g+8
     // step max per row over the 16 keys (lanes sharing c)
     float mx0 = fmaxf(v00, v10), mx1 = fmaxf(v01, v11);
 #pragma unroll
@@ -271,8 +300,12 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
-    const float sc0 = rv0 ? expf(m_r[0] - mn0) : 0.f;   // m_r = -inf before the first step: 0
-    const float sc1 = rv1 ? expf(m_r[1] - mn1) : 0.f;
+    // no key of the row yet: its state stays (0, 0); a step past the row's
+    // position has scale exp(0) = 1 and p = 0, so it leaves the state as is
+    // (one token per item: a valid row has a key in every step, and
+    // exp(-inf - finite) = 0 on its first)
+    const float sc0 = (kGroup ? mn0 == neg_inf() : !rv0) ? 0.f : expf(m_r[0] - mn0);
+    const float sc1 = (kGroup ? mn1 == neg_inf() : !rv1) ? 0.f : expf(m_r[1] - mn1);
     const float p00 = v00 == neg_inf() ? 0.f : expf(v00 - mn0);
     const float p10 = v10 == neg_inf() ? 0.f : expf(v10 - mn0);
     const float p01 = v01 == neg_inf() ? 0.f : expf(v01 - mn1);
@@ -283,11 +316,11 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
       ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
       ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
     }
-    if (rv0) {
+    if (kGroup || rv0) {
       l_r[0] = l_r[0] * sc0 + ls0;
       m_r[0] = mn0;
     }
-    if (rv1) {
+    if (kGroup || rv1) {
       l_r[1] = l_r[1] * sc1 + ls1;
       m_r[1] = mn1;
     }
@@ -353,9 +386,12 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
   named_sync(1, kDWarps * 32);
   const int tid = threadIdx.x;
   const int dv0 = vp * VD;                           // first output dim of this item
+  const int ns = dattn_splits(a.cap);
   // a split partial: [HD dims][M, L of V part 0][M, L of V part 1]
-  for (int e = tid; e < rows * VD; e += kDWarps * 32) {
+  for (int e = tid; e < nrows * VD; e += kDWarps * 32) {
     const int r = e / VD, dm = e % VD;
+    const int t = row_tok(r);
+    if (kGroup && pos0 + t < k0) continue;           // no key of the row in this split
     float M = neg_inf();
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, mm[w * kDRows + r]);
@@ -367,11 +403,11 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
       num = fmaf(f, oo[((size_t)w * kDRows + r) * VD + dm], num);
       den = fmaf(f, ll[w * kDRows + r], den);
     }
-    const int h = h0 + r;
+    const int h = row_head(r);
     if (nsplit == 1) {
-      ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)h * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
+      ((bf16*)a.out)[(size_t)t * a.hq * HD + (size_t)h * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
     } else {
-      float* pp = a.partials + (((size_t)d.t * a.hq + h) * dattn_splits(a.cap) + d.split) * (HD + 4);
+      float* pp = a.partials + (((size_t)t * a.hq + h) * ns + d.split) * (HD + 4);
       pp[dv0 + dm] = num;
       if (dm == 0) {
         pp[HD + 2 * vp] = M;
@@ -383,31 +419,53 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     named_sync(1, kDWarps * 32);   // the merge area is reused by the next item
     return;
   }
-  // ---- several splits: the last one (of this V part) to finish merges them
-  // in split order ----
-  int* ticket = a.tickets + (((size_t)d.t * a.hkv + d.kvh) * hgroups + d.hg) * L::kVParts + vp;
+  // ---- several splits: the last one of the token group (and V part) to
+  // finish merges each row's splits 0 .. p_r / 1024 in split order ----
+  int* ticket = a.tickets + (((size_t)d.tg * a.hkv + d.kvh) * hgroups + d.hg) * L::kVParts + vp;
   named_sync(1, kDWarps * 32);
   if (tid == 0)   // acq_rel: publishes this split's partial, acquires the earlier ones
     *s_last = (atom_add_acq_rel_gpu(reinterpret_cast<unsigned*>(ticket), 1u) == (unsigned)nsplit - 1);
   named_sync(1, kDWarps * 32);
   if (!*s_last) return;
-  const int ns = dattn_splits(a.cap);
-  for (int e = tid; e < rows * VD; e += kDWarps * 32) {
+  for (int e = tid; e < nrows * VD; e += kDWarps * 32) {
     const int r = e / VD, dm = e % VD;
-    const float* base = a.partials + ((size_t)d.t * a.hq + h0 + r) * ns * (HD + 4);
+    const int t = row_tok(r);
+    const int nr = (pos0 + t) / kDSplitKeys + 1;     // the row's own splits
+    const int h = row_head(r);
+    const float* base = a.partials + ((size_t)t * a.hq + h) * ns * (HD + 4);
     float M = neg_inf();
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(base + (size_t)sp * (HD + 4) + HD + 2 * vp));
+    for (int sp = 0; sp < nr; ++sp) M = fmaxf(M, __ldcg(base + (size_t)sp * (HD + 4) + HD + 2 * vp));
     float num = 0.f, den = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
+    for (int sp = 0; sp < nr; ++sp) {
       const float* pp = base + (size_t)sp * (HD + 4);
       const float f = expf(__ldcg(pp + HD + 2 * vp) - M);
       num = fmaf(f, __ldcg(pp + dv0 + dm), num);
       den = fmaf(f, __ldcg(pp + HD + 2 * vp + 1), den);
     }
-    ((bf16*)a.out)[(size_t)d.t * a.hq * HD + (size_t)(h0 + r) * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
+    ((bf16*)a.out)[(size_t)t * a.hq * HD + (size_t)h * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
   }
   named_sync(1, kDWarps * 32);
   if (tid == 0) *ticket = 0;
+}
+
+// Item it of an attention phase in a fixed grouping mode (the persistent
+// kernel is instantiated per mode and the host picks it per pass).
+template <int HD, bool kGroup>
+SV_DEV void dattn_item_mode(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
+                            unsigned& dpar, unsigned long long* stamp = nullptr) {
+  dattn_item_rows<HD, kGroup>(a, it, *a.pos_base + a.pos_off, sm, s_last, bars, dpar, stamp);
+}
+
+// Item it of an attention phase: token groups once the pass's last position
+// reaches kDGroupMinPos, else one token per item.
+template <int HD>
+SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
+                       unsigned& dpar, unsigned long long* stamp = nullptr) {
+  const int pos0 = *a.pos_base + a.pos_off;           // position of token 0
+  if (pos0 + a.ntok - 1 >= kDGroupMinPos)
+    dattn_item_rows<HD, true>(a, it, pos0, sm, s_last, bars, dpar, stamp);
+  else
+    dattn_item_rows<HD, false>(a, it, pos0, sm, s_last, bars, dpar, stamp);
 }
 
 }  // namespace sv

@@ -110,11 +110,15 @@ struct spec_ctx {
   int32_t* h_pos = nullptr;     // pinned host scratch for eager positions
   std::vector<void*> allocs;
   // graphs
-  cudaGraphExec_t step_exec = nullptr;
+  // step and profiling graphs per attention mode (index: grp)
+  cudaGraphExec_t step_exec[2] = {nullptr, nullptr};
   cudaGraphExec_t ar_exec = nullptr;
   // draft loop, verify, ar, verify forward alone
-  cudaGraphExec_t prof_exec[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaGraphExec_t prof_exec[4][2] = {};
   int prof_kernels[4] = {0, 0, 0, 0};
+  // attention mode of the persistent launches being enqueued: token groups
+  // (the passes' last position reaches kDGroupMinPos) or one token per item
+  bool grp = false;
   // host mirror of the state
   bool prefilled = false;
   bool draft_stale = false;
@@ -378,7 +382,7 @@ void forward_persist(Launch& L, int which) {
   if (f.desc.times)
     L.note(cudaMemsetAsync(f.desc.times, 0,
                            sizeof(unsigned long long) * (1 + (size_t)kPhaseStamps * f.desc.nphases), c->stream));
-  L.note(launch_persist(f.desc, f.hd, f.smem, c->num_sms, c->stream));
+  L.note(launch_persist(f.desc, f.hd, c->grp, f.smem, c->num_sms, c->stream));
 }
 
 void enqueue_draft(Launch& L) {
@@ -525,10 +529,12 @@ int run_captured(spec_ctx* c, cudaGraphExec_t* exec, void (*enq)(Launch&), int* 
 
 void free_ctx(spec_ctx* c) {
   if (!c) return;
-  if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
-  if (c->ar_exec) cudaGraphExecDestroy(c->ar_exec);
-  for (cudaGraphExec_t g : c->prof_exec)
+  for (cudaGraphExec_t g : c->step_exec)
     if (g) cudaGraphExecDestroy(g);
+  if (c->ar_exec) cudaGraphExecDestroy(c->ar_exec);
+  for (auto& pe : c->prof_exec)
+    for (cudaGraphExec_t g : pe)
+      if (g) cudaGraphExecDestroy(g);
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->h_result) cudaFreeHost(c->h_result);
@@ -834,6 +840,7 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   }
   if (c->persist) {
+    c->grp = false;   // one token per pass
     forward_persist(Lc, K + 2);
     forward_persist(Lc, K + 3);
     CUDA_TRY(c, Lc.e);
@@ -858,7 +865,8 @@ int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* ou
   if (c->host_L + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
   const int K = c->K;
   c->ev_used = 0;
-  int rc = run_captured(c, &c->step_exec, enqueue_step, &c->kernels_step);
+  c->grp = c->host_L + K >= kDGroupMinPos;   // last verify position
+  int rc = run_captured(c, &c->step_exec[c->grp], enqueue_step, &c->kernels_step);
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   const int32_t* h = c->h_result;
@@ -905,6 +913,7 @@ int spec_ar_step(spec_ctx* c, int32_t* out_token) {
   if (!out_token) return fail(c, SPEC_E_ARG, "null output buffer");
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_ar_step before spec_prefill");
   if (c->host_L + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
+  c->grp = false;   // one token: nothing to share
   int rc = run_captured(c, &c->ar_exec, enqueue_ar, &c->kernels_ar);
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
@@ -971,13 +980,15 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   CUDA_TRY(c, cudaEventCreate(&e0));
   CUDA_TRY(c, cudaEventCreate(&e1));
   for (int k = 0; k < 4; ++k) {
-    if (!c->prof_exec[k]) {
-      int rc = capture(c, &c->prof_exec[k], enq[k], &c->prof_kernels[k]);
+    c->grp = k != 2 && c->host_L + c->K >= kDGroupMinPos;   // as spec_step / spec_ar_step pick it
+    cudaGraphExec_t& ex = c->prof_exec[k][c->grp];
+    if (!ex) {
+      int rc = capture(c, &ex, enq[k], &c->prof_kernels[k]);
       if (rc) { cudaEventDestroy(e0); cudaEventDestroy(e1); return rc; }
     }
-    for (int w = 0; w < 2; ++w) CUDA_TRY(c, cudaGraphLaunch(c->prof_exec[k], c->stream));
+    for (int w = 0; w < 2; ++w) CUDA_TRY(c, cudaGraphLaunch(ex, c->stream));
     CUDA_TRY(c, cudaEventRecord(e0, c->stream));
-    for (int i = 0; i < iters; ++i) CUDA_TRY(c, cudaGraphLaunch(c->prof_exec[k], c->stream));
+    for (int i = 0; i < iters; ++i) CUDA_TRY(c, cudaGraphLaunch(ex, c->stream));
     CUDA_TRY(c, cudaEventRecord(e1, c->stream));
     CUDA_TRY(c, cudaEventSynchronize(e1));
     float t = 0.f;

@@ -131,8 +131,8 @@ size_t attn_partial_floats(int max_tok, int hq, int hd, int max_chunks);
 int attn_max_row_tiles(int max_tok, int hq, int hkv);
 cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st);
 // Tensor-core attention (bf16 cache, head dim 32/64/128, any token count):
-// items per (KV head, token, group of 8 query heads, 1024-key split, V
-// column part -- two for head dims 64 and 128); its
+// items per (KV head, token group, group of 8 query heads, 1024-key split,
+// V column part -- two for head dims 64 and 128); its
 // tickets are dattn_tickets(tokens, hq, hkv) zeroed counters, its partials
 // persist_attn_partial_floats floats.
 cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st);
@@ -144,6 +144,12 @@ bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows, in
 // Box columns of the V map launch_dattn expects (head dim 64: 32 -- items
 // read V in halves).
 int dattn_v_box_cols(int hd);
+// Attention items of a pass whose last position is at least this take token
+// groups (8 / min(G, 8) tokens share one walk over the KV head's keys);
+// earlier passes give each token its own items, since the keys are then few
+// and L2-resident and more, shorter items finish sooner.  Grouping changes
+// no row's arithmetic.
+constexpr int kDGroupMinPos = 1024;
 int dattn_tickets(int max_tok, int hq, int hkv);
 // One-time kernel attributes (dynamic shared memory); call before any capture.
 cudaError_t configure_kernels();
@@ -266,7 +272,9 @@ size_t persist_partial_floats(int grid);
 // True when one CTA per SM of the persistent kernel fits, for passes of at
 // most max_tok tokens.
 bool persist_supported(int hd, size_t smem, int num_sms, int max_tok);
-cudaError_t launch_persist(const PersistDesc& p, int hd, size_t smem, int num_sms, cudaStream_t st);
+// group: attention items take token groups (kDGroupMinPos); either mode gives
+// the same bits, the caller picks the faster one for the pass's positions.
+cudaError_t launch_persist(const PersistDesc& p, int hd, bool group, size_t smem, int num_sms, cudaStream_t st);
 
 // RoPE tables: cos/sin of pos * theta^(-2i/hd) for pos < cap, computed in fp64.
 cudaError_t launch_rope_table(float* cos_out, float* sin_out, int cap, int hd, double theta,

@@ -83,7 +83,7 @@ SV_DEV void grid_leave(unsigned* bar, unsigned total) {
   if (threadIdx.x == 0 && atom_add_acq_rel_gpu(bar, 1u) == total - 1) st_relaxed_gpu(bar, 0u);
 }
 
-template <int HD>
+template <int HD, bool kGroup>
 __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __grid_constant__ PersistDesc p) {
   // dynamic shared memory: [weight ring, kRingBytes][X region: normalised X,
   // or the X boxes of phases reading X from global memory]; attention
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
       }
     } else {
       for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x)
-        dattn_item<HD>(d.a, it, dsm, &s_last, dbars, dpar, st ? st + 3 : nullptr);
+        dattn_item_mode<HD, kGroup>(d.a, it, dsm, &s_last, dbars, dpar, st ? st + 3 : nullptr);
       if (st && threadIdx.x == 0) atomicMax(st + 4, global_ns());
     }
     npre = 0;
@@ -315,19 +315,23 @@ size_t persist_partial_floats(int grid) { return (size_t)grid * 2 * kMaxMmaTiles
 // The dynamic shared-memory limit is a per-function attribute shared by
 // every context of the process (a draft and a target with the same head
 // dimension use the same instance): it only ever grows here.
-template <int HD>
-static bool persist_fits(size_t smem) {
+template <int HD, bool kGroup>
+static bool persist_fits_mode(size_t smem) {
   cudaFuncAttributes fa{};
-  if (cudaFuncGetAttributes(&fa, persist_forward<HD>) != cudaSuccess) return false;
+  if (cudaFuncGetAttributes(&fa, persist_forward<HD, kGroup>) != cudaSuccess) return false;
   if ((size_t)fa.maxDynamicSharedSizeBytes < smem &&
-      cudaFuncSetAttribute(persist_forward<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(persist_forward<HD, kGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return false;
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, persist_forward<HD>, kPersistThreads, smem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, persist_forward<HD, kGroup>, kPersistThreads,
+                                                    smem) != cudaSuccess)
     return false;
   return blocks >= 1;
+}
+template <int HD>
+static bool persist_fits(size_t smem) {
+  return persist_fits_mode<HD, false>(smem) && persist_fits_mode<HD, true>(smem);
 }
 
 bool persist_supported(int hd, size_t smem, int num_sms, int max_tok) {
@@ -339,7 +343,7 @@ bool persist_supported(int hd, size_t smem, int num_sms, int max_tok) {
   return false;
 }
 
-template <int HD>
+template <int HD, bool kGroup>
 static cudaError_t launch_persist_t(const PersistDesc& p, size_t smem, int num_sms, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);   // one CTA per SM, all co-resident
@@ -351,13 +355,18 @@ static cudaError_t launch_persist_t(const PersistDesc& p, size_t smem, int num_s
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, persist_forward<HD>, p);
+  return cudaLaunchKernelEx(&cfg, persist_forward<HD, kGroup>, p);
 }
 
-cudaError_t launch_persist(const PersistDesc& p, int hd, size_t smem, int num_sms, cudaStream_t st) {
-  if (hd == 32) return launch_persist_t<32>(p, smem, num_sms, st);
-  if (hd == 64) return launch_persist_t<64>(p, smem, num_sms, st);
-  if (hd == 128) return launch_persist_t<128>(p, smem, num_sms, st);
+template <int HD>
+static cudaError_t launch_persist_hd(const PersistDesc& p, bool group, size_t smem, int num_sms, cudaStream_t st) {
+  return group ? launch_persist_t<HD, true>(p, smem, num_sms, st) : launch_persist_t<HD, false>(p, smem, num_sms, st);
+}
+
+cudaError_t launch_persist(const PersistDesc& p, int hd, bool group, size_t smem, int num_sms, cudaStream_t st) {
+  if (hd == 32) return launch_persist_hd<32>(p, group, smem, num_sms, st);
+  if (hd == 64) return launch_persist_hd<64>(p, group, smem, num_sms, st);
+  if (hd == 128) return launch_persist_hd<128>(p, group, smem, num_sms, st);
   return cudaErrorInvalidValue;
 }
 

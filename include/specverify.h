@@ -25,7 +25,13 @@
  *    memory allocated by spec_init and released by spec_free.
  *  - Token buffers of the context API are caller-owned HOST memory; every
  *    context call returns only after its outputs are written.
- *  - Only batch 1 is supported by the context API in this version.
+ *  - A context holds `batch` independent sequences (1..SPEC_MAX_BATCH).
+ *    Batch 1 runs each forward as one persistent kernel (bf16 models);
+ *    batch > 1 needs bf16 models and runs one kernel per operation, with
+ *    the sequences' tokens in one pass (groups of at most 64 tokens, each
+ *    group streaming the weights once).  Sequences advance independently
+ *    (ragged acceptance): every sequence has its own committed length, step
+ *    counters, KV rows and Philox row word (its index b).
  *  - All work runs on one GPU, on the stream given in spec_opts (or a
  *    stream the library creates).  There is no CPU fallback: without a
  *    usable GPU every call fails with SPEC_E_CUDA.
@@ -58,6 +64,8 @@ extern "C" {
 #define SPEC_E_STATE       -8   /* call out of order (e.g. step before prefill) */
 
 /* ---- model dtypes ---- */
+#define SPEC_MAX_BATCH     64
+
 #define SPEC_DTYPE_F32      0
 #define SPEC_DTYPE_BF16     1
 
@@ -109,7 +117,8 @@ typedef struct spec_model_desc {
 } spec_model_desc;
 
 typedef struct spec_opts {
-    int      batch;             /* must be 1 */
+    int      batch;             /* sequences, 1..SPEC_MAX_BATCH (> 1: bf16 models,
+                                   draft_mix_lambda 0) */
     int      max_ctx;           /* KV capacity in positions (prompt + generated + K + 1) */
     float    temperature;       /* 0 = greedy; >0 scales target and draft logits */
     uint64_t seed;              /* Philox key of every random draw */
@@ -155,12 +164,27 @@ SPEC_API void spec_free(spec_ctx* ctx);
  * stateless call on this thread when ctx is NULL).  Never NULL. */
 SPEC_API const char* spec_last_error(const spec_ctx* ctx);
 
-/* Prefill: tokens[0..L-1] (host, int32, 0 <= id < vocab).  Both models
- * score positions 0..L-2 into their KV caches; tokens[L-1] becomes the
- * pending token of the first step (it is the x of [INT 演算法核心] Step 2's
+/* Prefill: tokens[b][0..L-1] (host, int32 [batch][L], 0 <= id < vocab),
+ * the same length L for every sequence.  Both models score positions
+ * 0..L-2 into their KV caches; tokens[b][L-1] becomes the pending token of
+ * sequence b's first step (it is the x of [INT 演算法核心] Step 2's
  * T(.|x)).  Resets the step counters.  Requires 2 <= L and
  * L + K + 1 <= max_ctx; with draft_mix_lambda != 0 also L >= K + 2. */
 SPEC_API int spec_prefill(spec_ctx* ctx, const int32_t* tokens, int L);
+
+/* Benchmark state without a prefill: every sequence gets L committed
+ * positions (L - 1 cached, token L-1 pending) with token ids drawn uniformly
+ * from [0, vocab) and both models' KV caches filled with synthetic
+ * normally distributed bf16 / fp32 values (a counter-based generator keyed
+ * by seed), not with the models' own keys and values.  Steps then run the
+ * same kernels and read the same bytes as after a real prefill of L tokens;
+ * their tokens carry no meaning.  Resets the step counters.  Requires
+ * 2 <= L and L + K + 1 <= max_ctx. */
+SPEC_API int spec_prefill_synthetic(spec_ctx* ctx, int L, uint64_t seed);
+
+/* Committed tokens of sequence b (host, capacity max_ctx): context[0 ..
+ * *len - 1], the last one being the pending token. */
+SPEC_API int spec_seq_context(spec_ctx* ctx, int b, int32_t* context, int32_t* len);
 
 /* One speculative step [INT 演算法核心 Steps 1-4; 101 Floors 4-5]:
  *  1. draft loop: K draft forwards, d_i ~ softmax(q_i / T) (argmax at T=0);
@@ -172,34 +196,38 @@ SPEC_API int spec_prefill(spec_ctx* ctx, const int32_t* tokens, int L);
  *  4. commit: the emitted tokens extend the context, the last one becomes
  *     the pending token; KV entries past the accepted prefix are dropped by
  *     length truncation (no copies).
- * out_tokens (host, capacity K+1) receives the n+1 emitted tokens,
- * *out_count = n+1 (1 <= n+1 <= K+1, [101 Floor 4]); out_flags may be NULL.
- * Fails with SPEC_E_STATE before prefill, SPEC_E_CAPACITY when the context
- * plus K+1 would exceed max_ctx. */
+ * For every sequence b: out_tokens (host, [batch][K+1]) row b receives its
+ * n_b+1 emitted tokens (the rest of the row is -1), out_count[b] = n_b+1
+ * (1 <= n_b+1 <= K+1, [101 Floor 4]); out_flags ([batch]) may be NULL.
+ * Fails with SPEC_E_STATE before prefill, SPEC_E_CAPACITY when a sequence's
+ * context plus K+1 would exceed max_ctx. */
 SPEC_API int spec_step(spec_ctx* ctx, int32_t* out_tokens, int32_t* out_count, uint32_t* out_flags);
 
-/* Speculative generation of n_new tokens: spec_step until at least n_new
- * tokens are emitted; out (host, capacity n_new) receives the first n_new,
- * *out_n = n_new.  Extra emitted tokens of the last step stay committed. */
+/* Speculative generation of n_new tokens (batch 1): spec_step until at
+ * least n_new tokens are emitted; out (host, capacity n_new) receives the
+ * first n_new, *out_n = n_new.  Extra emitted tokens of the last step stay
+ * committed.  Batched contexts call spec_step directly. */
 SPEC_API int spec_generate(spec_ctx* ctx, int n_new, int32_t* out, int32_t* out_n);
 
 /* Plain autoregressive decoding on the same kernels [101 Floor 1]: one
- * target forward over the pending token, one draw from softmax(p / T)
- * (argmax at T=0), committed like a step.  *out_token receives it. */
+ * target forward over the pending token of every sequence, one draw per
+ * sequence from softmax(p / T) (argmax at T=0), committed like a step.
+ * out_token[b] (host, [batch]) receives sequence b's token. */
 SPEC_API int spec_ar_step(spec_ctx* ctx, int32_t* out_token);
 
 /* Counters and byte accounting of the context. */
 SPEC_API int spec_get_stats(const spec_ctx* ctx, spec_stats* out);
 
 /* Copy the internals of the last spec_step to host buffers (any may be
- * NULL): target logits [K+1][vocab] fp32, draft q logits after mixing
- * [K][vocab] fp32, draft tokens [K], committed context tokens
- * [context_len] (capacity max_ctx).  For verification against a reference. */
+ * NULL): target logits [batch][K+1][vocab] fp32, draft q logits after
+ * mixing [batch][K][vocab] fp32, draft tokens [batch][K], and sequence 0's
+ * committed context tokens [context_len] (capacity max_ctx; other
+ * sequences: spec_seq_context).  For verification against a reference. */
 SPEC_API int spec_last_step_debug(spec_ctx* ctx, float* p_logits, float* q_logits,
                          int32_t* drafts, int32_t* context, int32_t* context_len);
 
 /* Run one model's forward over n tokens (host ids) at positions pos0 ..
- * pos0+n-1 of its own KV cache (pos0 <= its current valid length; the valid
+ * pos0+n-1 of its own KV cache (sequence 0; pos0 <= its current valid length; the valid
  * length becomes pos0+n) and write fp32 logits of all n positions to
  * logits_dev ([n][vocab], device).  which: 0 = target, 1 = draft.  This is
  * the forward the step uses [101 Floor 3]; it does not touch the step state

@@ -21,6 +21,7 @@ ERRORS = {-1: "SPEC_E_ARG", -2: "SPEC_E_VOCAB", -3: "SPEC_E_SHAPE", -4: "SPEC_E_
           -5: "SPEC_E_CUDA", -6: "SPEC_E_OOM", -7: "SPEC_E_TIMEOUT", -8: "SPEC_E_STATE"}
 SPEC_DTYPE_F32 = 0
 SPEC_DTYPE_BF16 = 1
+SPEC_MAX_BATCH = 64
 SPEC_FLAG_RESID_ZERO = 0x1
 SPEC_FLAG_ALL_ACCEPTED = 0x2
 SPEC_OPT_NO_GRAPH = 0x1
@@ -91,6 +92,8 @@ SIGNATURES = {
     "spec_free": (None, [_VP]),
     "spec_last_error": (ctypes.c_char_p, [_VP]),
     "spec_prefill": (ctypes.c_int, [_VP, _I32P, ctypes.c_int]),
+    "spec_prefill_synthetic": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_uint64]),
+    "spec_seq_context": (ctypes.c_int, [_VP, ctypes.c_int, _I32P, _I32P]),
     "spec_step": (ctypes.c_int, [_VP, _I32P, _I32P, _U32P]),
     "spec_generate": (ctypes.c_int, [_VP, ctypes.c_int, _I32P, _I32P]),
     "spec_ar_step": (ctypes.c_int, [_VP, _I32P]),
@@ -165,15 +168,17 @@ def model_desc(shape, weights):
 
 
 class SpecDecoder:
-    """One target/draft pair with K drafts per step (batch 1)."""
+    """One target/draft pair with K drafts per step over `batch` sequences
+    (batch > 1: bf16 models, every sequence advancing independently)."""
 
     def __init__(self, target_shape, target_w, draft_shape, draft_w, k, max_ctx,
-                 temperature=0.0, seed=0, mix_lambda=0.0, stream=None, flags=0):
+                 temperature=0.0, seed=0, mix_lambda=0.0, stream=None, flags=0, batch=1):
         self.k = k
+        self.batch = batch
         self.vocab = target_shape.vocab
         self._td, self._tk = model_desc(target_shape, target_w)
         self._dd, self._dk = model_desc(draft_shape, draft_w)
-        opts = Opts(1, max_ctx, temperature, seed, mix_lambda,
+        opts = Opts(batch, max_ctx, temperature, seed, mix_lambda,
                     ctypes.c_void_p(stream) if stream else ctypes.c_void_p(0), flags)
         h = ctypes.c_void_p()
         rc = lib().spec_init(ctypes.byref(self._td), ctypes.byref(self._dd), k, ctypes.byref(opts),
@@ -193,15 +198,39 @@ class SpecDecoder:
             pass
 
     def prefill(self, tokens):
-        arr = (ctypes.c_int32 * len(tokens))(*[int(t) for t in tokens])
-        _check(lib().spec_prefill(self.ctx, arr, len(tokens)), self.ctx)
+        """tokens: one prompt (batch 1) or `batch` prompts of one length."""
+        rows = [list(tokens)] if self.batch == 1 and not hasattr(tokens[0], "__len__") else list(tokens)
+        n = len(rows[0])
+        flat = [int(t) for r in rows for t in r]
+        arr = (ctypes.c_int32 * len(flat))(*flat)
+        _check(lib().spec_prefill(self.ctx, arr, n), self.ctx)
+
+    def prefill_synthetic(self, length, seed=0):
+        """State of a prefill of `length` tokens with synthetic token ids and
+        KV caches (benchmark workloads; the tokens carry no meaning)."""
+        _check(lib().spec_prefill_synthetic(self.ctx, length, seed), self.ctx)
 
     def step(self):
-        out = (ctypes.c_int32 * (self.k + 1))()
-        cnt = ctypes.c_int32()
-        flags = ctypes.c_uint32()
-        _check(lib().spec_step(self.ctx, out, ctypes.byref(cnt), ctypes.byref(flags)), self.ctx)
-        return list(out[:cnt.value]), flags.value
+        """Batch 1: (emitted tokens, flags).  Batch > 1: ([tokens of each
+        sequence], [flags of each sequence])."""
+        b = self.batch
+        out = (ctypes.c_int32 * (b * (self.k + 1)))()
+        cnt = (ctypes.c_int32 * b)()
+        flags = (ctypes.c_uint32 * b)()
+        _check(lib().spec_step(self.ctx, out, cnt, flags), self.ctx)
+        rows = [list(out[i * (self.k + 1):i * (self.k + 1) + cnt[i]]) for i in range(b)]
+        if b == 1:
+            return rows[0], flags[0]
+        return rows, list(flags)
+
+    def seq_context(self, b):
+        """Committed tokens of sequence b (the last is the pending token)."""
+        import numpy as np
+        n = ctypes.c_int32()
+        _check(lib().spec_seq_context(self.ctx, b, None, ctypes.byref(n)), self.ctx)
+        buf = np.zeros(max(1, n.value), dtype=np.int32)
+        _check(lib().spec_seq_context(self.ctx, b, buf.ctypes.data_as(_I32P), ctypes.byref(n)), self.ctx)
+        return buf[:n.value].copy()
 
     def generate(self, n_new):
         out = (ctypes.c_int32 * max(1, n_new))()
@@ -210,9 +239,10 @@ class SpecDecoder:
         return list(out[:got.value])
 
     def ar_step(self):
-        tok = ctypes.c_int32()
-        _check(lib().spec_ar_step(self.ctx, ctypes.byref(tok)), self.ctx)
-        return tok.value
+        """Batch 1: the token; batch > 1: one token per sequence."""
+        tok = (ctypes.c_int32 * self.batch)()
+        _check(lib().spec_ar_step(self.ctx, tok), self.ctx)
+        return tok[0] if self.batch == 1 else list(tok)
 
     def stats(self):
         s = Stats()
@@ -241,12 +271,15 @@ class SpecDecoder:
         return [dict(zip(names, (int(v) for v in row))) for row in buf[:n.value]]
 
     def last_step_debug(self, max_ctx):
-        """(p_logits [K+1, V], q_logits [K, V], drafts [K], context tokens) as numpy."""
+        """(p_logits [K+1, V], q_logits [K, V], drafts [K], context tokens) as
+        numpy; batch > 1: p [B, K+1, V], q [B, K, V], drafts [B, K] and
+        sequence 0's context."""
         import numpy as np
-        k, v = self.k, self.vocab
-        p = np.zeros((k + 1, v), dtype=np.float32)
-        q = np.zeros((k, v), dtype=np.float32)
-        d = np.zeros(k, dtype=np.int32)
+        k, v, b = self.k, self.vocab, self.batch
+        lead = () if b == 1 else (b,)
+        p = np.zeros(lead + (k + 1, v), dtype=np.float32)
+        q = np.zeros(lead + (k, v), dtype=np.float32)
+        d = np.zeros(lead + (k,), dtype=np.int32)
         ctx = np.zeros(max_ctx, dtype=np.int32)
         n = ctypes.c_int32()
         _check(lib().spec_last_step_debug(self.ctx, p.ctypes.data_as(_F32P), q.ctypes.data_as(_F32P),

@@ -173,8 +173,9 @@ SV_DEV void dattn_init_bars(uint64_t* bars) {
 // One item; kGroup: token groups (8 / hpi tokens per item) rather than one
 // token per item.  stamp (optional): atomicMax of the globaltimer when the
 // key walk ended.
-template <int HD, bool kGroup>
-SV_DEV void dattn_item_rows(const AttnDesc& a, int it, int pos0, unsigned char* sm, int* s_last, uint64_t* bars,
+// kSeqs = false: single-sequence passes only (the persistent kernel).
+template <int HD, bool kGroup, bool kSeqs>
+SV_DEV void dattn_item_rows(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
                             unsigned& dpar, unsigned long long* stamp) {
   using L = DAttnSmem<HD>;
   constexpr int VD = L::kVDims;                       // output dims of this item
@@ -182,19 +183,24 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, int pos0, unsigned char* 
   const int hgroups = dattn_hgroups(a.hq, a.hkv);
   const DItem d = dattn_item_of(a, it / L::kVParts, hgroups, a.ntok);
   const int G = a.hq / a.hkv, hpi = dattn_hpi(a.hq, a.hkv);
+  const int S = kSeqs && a.spt > 0 ? a.spt : a.ntok;  // tokens per sequence
+  const int b = kSeqs ? d.tg / S : 0;                 // the item's sequence
   const int tpi = kGroup ? kDRows / hpi : 1;          // tokens per item
-  const int t0 = d.tg * tpi;                          // first token of the item
-  if (kGroup && t0 >= a.ntok) return;                 // token slot past the last group
+  const int j0 = (kSeqs ? d.tg % S : d.tg) * tpi;     // its first token within the sequence
+  if (kGroup && j0 >= S) return;                      // token slot past the last group
+  const int t0 = b * S + j0;                          // ... and within the pass
+  // position of pass token t (of this sequence)
+  const int pbase = kSeqs ? a.pos_base[(size_t)b * a.pos_ld] + a.pos_off - b * S : *a.pos_base + a.pos_off;
   // rows 0 .. nrows-1 are valid: row r = (token t0 + r / hpi, head h0 + r % hpi)
-  const int nrows = kGroup ? min(tpi, a.ntok - t0) * min(hpi, G - d.hg * kDRows) : min(kDRows, G - d.hg * kDRows);
-  const int pmax = pos0 + t0 + (kGroup ? min(tpi, a.ntok - t0) - 1 : 0);
+  const int nrows = kGroup ? min(tpi, S - j0) * min(hpi, G - d.hg * kDRows) : min(kDRows, G - d.hg * kDRows);
+  const int pmax = pbase + t0 + (kGroup ? min(tpi, S - j0) - 1 : 0);
   const int k0 = d.split * kDSplitKeys;
   if (k0 > pmax) return;                              // split entirely in the future
   const int last = min(pmax, k0 + kDSplitKeys - 1);   // last key of this split
   const int nsplit = pmax / kDSplitKeys + 1;          // splits of the token group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
   const int h0 = d.kvh * G + d.hg * kDRows;           // first query head of the item
-  const int row0 = d.kvh * a.cap;                     // first cache row of the KV head
+  const int row0 = ((kSeqs ? a.seq0 + b : 0) * a.hkv + d.kvh) * a.cap;   // first cache row of the KV head
   uint64_t* wbar = bars + warp * kDMaxDepth;
   // token of valid item row r, and its head
   auto row_tok = [&](int r) { return kGroup ? t0 + r / hpi : t0; };
@@ -235,8 +241,8 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, int pos0, unsigned char* 
   for (int mt = 0; mt < VD / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   // positions of rows 2c, 2c+1 (-1: empty row); keys past them are masked
   const bool rv0 = 2 * ci < nrows, rv1 = 2 * ci + 1 < nrows;
-  const int p0 = rv0 ? pos0 + row_tok(2 * ci) : -1;
-  const int p1 = rv1 ? pos0 + row_tok(2 * ci + 1) : -1;
+  const int p0 = rv0 ? pbase + row_tok(2 * ci) : -1;
+  const int p1 = rv1 ? pbase + row_tok(2 * ci + 1) : -1;
   if (lane == 0)
     for (int j = 0; j < D && j < nst; ++j)
       dattn_fetch<HD>(a, row0, first + kDWarps * j, vp, wb + j * L::kStageElems,
@@ -391,7 +397,7 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, int pos0, unsigned char* 
   for (int e = tid; e < nrows * VD; e += kDWarps * 32) {
     const int r = e / VD, dm = e % VD;
     const int t = row_tok(r);
-    if (kGroup && pos0 + t < k0) continue;           // no key of the row in this split
+    if (kGroup && pbase + t < k0) continue;          // no key of the row in this split
     float M = neg_inf();
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, mm[w * kDRows + r]);
@@ -430,7 +436,7 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, int pos0, unsigned char* 
   for (int e = tid; e < nrows * VD; e += kDWarps * 32) {
     const int r = e / VD, dm = e % VD;
     const int t = row_tok(r);
-    const int nr = (pos0 + t) / kDSplitKeys + 1;     // the row's own splits
+    const int nr = (pbase + t) / kDSplitKeys + 1;    // the row's own splits
     const int h = row_head(r);
     const float* base = a.partials + ((size_t)t * a.hq + h) * ns * (HD + 4);
     float M = neg_inf();
@@ -450,22 +456,25 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, int pos0, unsigned char* 
 
 // Item it of an attention phase in a fixed grouping mode (the persistent
 // kernel is instantiated per mode and the host picks it per pass).
-template <int HD, bool kGroup>
+template <int HD, bool kGroup, bool kSeqs>
 SV_DEV void dattn_item_mode(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
                             unsigned& dpar, unsigned long long* stamp = nullptr) {
-  dattn_item_rows<HD, kGroup>(a, it, *a.pos_base + a.pos_off, sm, s_last, bars, dpar, stamp);
+  dattn_item_rows<HD, kGroup, kSeqs>(a, it, sm, s_last, bars, dpar, stamp);
 }
 
-// Item it of an attention phase: token groups once the pass's last position
-// reaches kDGroupMinPos, else one token per item.
+// Item it of an attention phase: token groups once the last position of the
+// item's sequence in the pass reaches kDGroupMinPos, else one token per item
+// (the items of a sequence all take the same mode).
 template <int HD>
 SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
                        unsigned& dpar, unsigned long long* stamp = nullptr) {
-  const int pos0 = *a.pos_base + a.pos_off;           // position of token 0
-  if (pos0 + a.ntok - 1 >= kDGroupMinPos)
-    dattn_item_rows<HD, true>(a, it, pos0, sm, s_last, bars, dpar, stamp);
+  using L = DAttnSmem<HD>;
+  const int S = a.spt > 0 ? a.spt : a.ntok;
+  const int b = dattn_item_of(a, it / L::kVParts, dattn_hgroups(a.hq, a.hkv), a.ntok).tg / S;
+  if (a.pos_base[(size_t)b * a.pos_ld] + a.pos_off + S - 1 >= kDGroupMinPos)
+    dattn_item_rows<HD, true, true>(a, it, sm, s_last, bars, dpar, stamp);
   else
-    dattn_item_rows<HD, false>(a, it, pos0, sm, s_last, bars, dpar, stamp);
+    dattn_item_rows<HD, false, true>(a, it, sm, s_last, bars, dpar, stamp);
 }
 
 }  // namespace sv

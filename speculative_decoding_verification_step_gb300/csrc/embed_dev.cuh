@@ -9,10 +9,12 @@ namespace sv {
 // Token t of e (one CTA): thread i owns the 16-element tiles i, i + blockDim,
 // ...: it copies them into the fp32 residual stream and writes their sums of
 // squares (the first RMSNorm of the forward folds them into 1/rms).
-template <typename T>
+// kSeqs = false: single-sequence passes only (the persistent kernel).
+template <typename T, bool kSeqs = true>
 SV_DEV void embed_token(const EmbedDesc& e, int t) {
-  const int32_t* tok = e.tok_base + (e.tok_idx ? *e.tok_idx : 0) + e.tok_off;
-  const T* row = (const T*)e.embed + (size_t)tok[t] * e.d;
+  const int b = kSeqs ? seq_of_tok(e.spt, t) : 0, j = kSeqs ? idx_in_seq(e.spt, t) : t;
+  const int32_t* tok = e.tok_base + (size_t)b * e.tok_ld + (e.tok_idx ? e.tok_idx[(size_t)b * e.idx_ld] : 0) + e.tok_off;
+  const T* row = (const T*)e.embed + (size_t)tok[j] * e.d;
   for (int tile = threadIdx.x; tile < e.d / 16; tile += blockDim.x) {
     float v[16], gn[16];
 #pragma unroll

@@ -78,6 +78,8 @@ struct spec_ctx {
   PhaseDesc* phase_dev = nullptr;
   unsigned* bar = nullptr;
   int K = 0;
+  int B = 1;                       // sequences (batch > 1: per-operation path, bf16 models)
+  int64_t seq_ld = 0;              // int32 stride between the sequences' token arrays
   spec_opts opts{};
   cudaStream_t stream = nullptr;
   bool own_stream = false;
@@ -85,8 +87,10 @@ struct spec_ctx {
   int cap = 0;
   int max_chunks = 0;
   // device state
-  int32_t* st = nullptr;    // [0] L, [1] spec step, [2] ar step, [3] eager position scratch
-  int32_t* seq = nullptr;   // [cap + K + 2]
+  // per sequence b, kStateLd apart: [0] L, [1] spec step, [2] ar step,
+  // [3] eager position scratch
+  int32_t* st = nullptr;
+  int32_t* seq = nullptr;   // [B][seq_ld], seq_ld = cap + K + 2
   int32_t* fwd_tok = nullptr;  // [kGemmMaxTok] host-supplied tokens of spec_model_forward
   // activations
   float* x = nullptr;
@@ -99,13 +103,15 @@ struct spec_ctx {
   int* dattn_tick = nullptr;       // tensor-core attention (bf16 models)
   float* ss = nullptr;         // [d_max/16][kGemmMaxTok] per-tile sums of squares
   float* logits_p = nullptr;  // [K+1][V]
-  float* logits_q = nullptr;  // [K][V]
+  float* logits_q = nullptr;  // [B][K][V]
+  float* logits_d = nullptr;  // batch > 1: [2B][V] draft-pass logits before sampling
   GemmScratch gs{};
   float* samp_part = nullptr;
   int* samp_tick = nullptr;
   float* acc_part = nullptr;
   int* acc_tick = nullptr;
-  int32_t* result = nullptr;    // device [K+1 tokens][count][flags][drafts K]
+  // device [B][K+1 tokens][B counts][B flags][B][K drafts][wait-timeout flag]
+  int32_t* result = nullptr;
   int32_t* h_result = nullptr;  // pinned host mirror
   int32_t* h_pos = nullptr;     // pinned host scratch for eager positions
   std::vector<void*> allocs;
@@ -122,7 +128,8 @@ struct spec_ctx {
   // host mirror of the state
   bool prefilled = false;
   bool draft_stale = false;
-  int host_L = 0;
+  int host_L = 0;                  // sequence 0 (batch 1: the sequence)
+  std::vector<int> host_Ls;        // every sequence's L
   int kernels_step = 0, kernels_ar = 0, gemms_verify = 0;
   int64_t steps = 0, ar_steps = 0, emitted = 0, accepted = 0;
   int64_t hist[17] = {0};
@@ -206,6 +213,10 @@ int check_model(const spec_model_desc* m, const char* which, std::string* why) {
   return SPEC_OK;
 }
 
+// Result words of the device result buffer (see spec_ctx::result).
+int32_t* res_err(spec_ctx* c) { return c->result + (size_t)c->B * (2 * c->K + 3); }
+int res_words(const spec_ctx* c) { return c->B * (2 * c->K + 3) + 1; }
+
 // ---------------------------------------------------------------- launches
 struct Launch {
   spec_ctx* c;
@@ -247,9 +258,21 @@ struct Op {
 // pregain (bf16 models): the residual producers also write x times the next
 // RMSNorm's gain in bf16 (c->xg), which the normalised GEMMs read (x_norm =
 // 2) and scale by 1/rms after the sums.
+// Sequences of a batched pass (batch > 1, per-operation path): the pass's
+// tokens are spt per sequence for sequences seq0 .. seq0 + n - 1 of the
+// context; tok_base / tok_idx / pos_idx then point at sequence seq0's token
+// array and state, and sequence b's are tok_ld / kStateLd further.  spt = 0:
+// one sequence (the batch-1 layout).
+struct Seqs {
+  int spt = 0;
+  int64_t tok_ld = 0;
+  int seq0 = 0;
+};
+
 std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t* tok_base,
                             const int32_t* tok_idx, int tok_off, const int32_t* pos_idx,
-                            int pos_off, int lrow0, int lrows, float* logits, bool pregain = false) {
+                            int pos_off, int lrow0, int lrows, float* logits, bool pregain = false,
+                            const Seqs& sq = Seqs()) {
   const spec_model_desc& d = m.d;
   const int dm = d.d_model, hq = d.n_heads, hkv = d.n_kv_heads, hd = d.head_dim;
   const int qkvr = m.qkv_rows();
@@ -260,6 +283,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
   op.e.tok_base = tok_base; op.e.tok_idx = tok_idx; op.e.tok_off = tok_off; op.e.embed = d.embed;
   op.e.dtype = dt; op.e.x = c->x; op.e.ss = c->ss; op.e.ss_ld = kGemmMaxTok; op.e.ntok = ntok;
   op.e.d = dm;
+  op.e.spt = sq.spt; op.e.idx_ld = kStateLd; op.e.tok_ld = sq.tok_ld;
   if (pregain) {
     op.e.xg = c->xg;
     op.e.gain = (const float*)m.layers[0].attn_norm;
@@ -280,7 +304,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
   };
   for (int l = 0; l < d.n_layers; ++l) {
     const spec_layer_weights& w = m.layers[l];
-    const size_t kvoff = (size_t)l * m.layer_kv_elems(c->cap) * m.esize;
+    const size_t kvoff = ((size_t)l * c->B + sq.seq0) * m.layer_kv_elems(c->cap) * m.esize;
     void* kc = (char*)m.kc + kvoff;
     void* vc = (char*)m.vc + kvoff;
     Op q{};
@@ -293,12 +317,14 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     g.ss_in = c->ss; g.ss_ld = kGemmMaxTok; g.eps = d.rms_eps;
     g.epi = kEpiQkvRope; g.hq = hq; g.hkv = hkv; g.hd = hd; g.cap = c->cap;
     g.pos_base = pos_idx; g.pos_off = pos_off; g.rope_cos = m.rope_cos; g.rope_sin = m.rope_sin;
+    g.spt = sq.spt; g.pos_ld = kStateLd;
     g.q_out = c->q; g.kc = kc; g.vc = vc;
     ops.push_back(q);
     Op at{};
     at.kind = kPhaseAttn;
     AttnDesc& a = at.a;
     a.q = c->q; a.kc = kc; a.vc = vc; a.pos_base = pos_idx; a.pos_off = pos_off;
+    a.spt = sq.spt; a.pos_ld = kStateLd; a.seq0 = sq.seq0;
     a.partials = c->attn_part; a.tickets = c->attn_tick; a.out = c->attn;
     a.ntok = ntok; a.hq = hq; a.hkv = hkv; a.hd = hd; a.cap = c->cap;
     a.max_chunks = c->max_chunks; a.dtype = dt;
@@ -307,7 +333,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
       a.tmk = m.kv_maps + 2 * l;
       a.tmv = m.kv_maps + 2 * l + 1;
     }
-    a.err = c->result + (2 * c->K + 3);
+    a.err = res_err(c);
     ops.push_back(at);
     Op o{};
     o.kind = kPhaseGemm;
@@ -353,12 +379,12 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
 // Per-kernel path: one launch per operation.
 void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const int32_t* tok_idx,
              int tok_off, const int32_t* pos_idx, int pos_off, int lrow0, int lrows,
-             float* logits) {
+             float* logits, const Seqs& sq = Seqs()) {
   spec_ctx* c = L.c;
   // bf16 models: normalised GEMM inputs as x * gain in bf16 (as in the
   // persistent kernel), 1/rms applied after the sums
   const std::vector<Op> ops = forward_ops(c, m, ntok, tok_base, tok_idx, tok_off, pos_idx, pos_off, lrow0,
-                                          lrows, logits, m.d.dtype == SPEC_DTYPE_BF16);
+                                          lrows, logits, m.d.dtype == SPEC_DTYPE_BF16, sq);
   for (const Op& op : ops) {
     if (op.kind == kPhaseEmbed) L.note(launch_embed(op.e, c->stream));
     else if (op.kind == kPhaseAttn) {
@@ -374,6 +400,25 @@ void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const 
   }
 }
 
+// Batched per-operation forward: spt tokens of every sequence, token j of
+// sequence b taken from seq[b][L_b + tok_off + j] at position L_b + pos_off
+// + j; the LM-head logits of all B * spt rows go to logits ([B][spt][V]).
+// Sequences are processed in groups of at most kGemmMaxTok tokens (each
+// group streams the weights once).
+void forward_batch(Launch& L, ModelState& m, int spt, int tok_off, int pos_off, float* logits) {
+  spec_ctx* c = L.c;
+  const int per = std::max(1, kGemmMaxTok / spt);
+  const size_t V = (size_t)m.d.vocab;
+  for (int b0 = 0; b0 < c->B; b0 += per) {
+    const int n = std::min(per, c->B - b0);
+    Seqs sq;
+    sq.spt = spt; sq.tok_ld = c->seq_ld; sq.seq0 = b0;
+    const int32_t* stb = c->st + (size_t)b0 * kStateLd;
+    forward(L, m, n * spt, c->seq + (size_t)b0 * c->seq_ld, stb, tok_off, stb, pos_off, 0, n * spt,
+            logits + (size_t)b0 * spt * V, sq);
+  }
+}
+
 // Persistent path: one cooperative launch for the whole forward, from a
 // phase list prepared at init (index into c->pforward).
 void forward_persist(Launch& L, int which) {
@@ -385,52 +430,74 @@ void forward_persist(Launch& L, int which) {
   L.note(launch_persist(f.desc, f.hd, c->grp, f.smem, c->num_sms, c->stream));
 }
 
+// Sampler rows of a context: row b is sequence b (its step counter at
+// st[b][which], Philox row word b), drawing into out_token[b * out_ld +
+// (out_idx ? L_b : 0) + out_off].
+SampleDesc sampler(spec_ctx* c, int which, int32_t* out_token, int64_t out_ld, const int32_t* out_idx,
+                   int out_off) {
+  SampleDesc sd{};
+  sd.rows = c->B; sd.V = c->tgt.d.vocab; sd.temperature = c->opts.temperature; sd.seed = c->opts.seed;
+  sd.batch = 1; sd.st_ld = kStateLd; sd.seq_ld = c->seq_ld;
+  sd.step_dev = c->st + which; sd.step_base = 0;
+  sd.out_token = out_token; sd.out_ld = out_ld; sd.out_idx = out_idx; sd.out_off = out_off;
+  sd.partials = c->samp_part; sd.tickets = c->samp_tick;
+  return sd;
+}
+
 void enqueue_draft(Launch& L) {
   spec_ctx* c = L.c;
   const int K = c->K, V = c->tgt.d.vocab;
   const int32_t* Lp = c->st;  // committed length index (position of the pending token)
   const bool mix = c->opts.draft_mix_lambda != 0.f;
   for (int i = 1; i <= K; ++i) {
-    float* qrow = c->logits_q + (size_t)(i - 1) * V;
+    float* qrow = c->logits_q + (size_t)(i - 1) * V;   // q row i of sequence b: qrow + b * K * V
+    const int S = i == 1 ? 2 : 1;                        // tokens per sequence of this pass
     if (c->persist)
       forward_persist(L, i - 1);
-    else if (i == 1)
+    else if (c->B == 1 && i == 1)
       forward(L, c->drf, 2, c->seq, Lp, -1, Lp, -1, 1, 1, qrow);
-    else
+    else if (c->B == 1)
       forward(L, c->drf, 1, c->seq, Lp, i - 1, Lp, i - 1, 0, 1, qrow);
-    SampleDesc sd{};
-    sd.logits = qrow; sd.ld = V;
-    if (mix) {
+    else
+      forward_batch(L, c->drf, S, i == 1 ? -1 : i - 1, i == 1 ? -1 : i - 1, c->logits_d);
+    SampleDesc sd = sampler(c, 1, c->seq, c->seq_ld, Lp, i);
+    sd.position = (uint32_t)i; sd.stream = kStreamDraft;
+    if (c->B == 1) {
+      sd.logits = qrow; sd.ld = V;
+    } else {   // the last row of each sequence; the row is kept as q_i
+      sd.logits = c->logits_d + (size_t)(S - 1) * V; sd.ld = (int64_t)S * V;
+      sd.mixed_out = qrow; sd.mixed_ld = (int64_t)K * V;
+    }
+    if (mix) {   // batch 1 only
       sd.mix_src = c->logits_p + (size_t)(i - 1) * V; sd.mix_ld = V;
       sd.lambda = c->opts.draft_mix_lambda; sd.mixed_out = qrow; sd.mixed_ld = V;
     }
-    sd.rows = 1; sd.V = V; sd.temperature = c->opts.temperature; sd.seed = c->opts.seed;
-    sd.step_dev = c->st + 1; sd.step_base = 0; sd.position = (uint32_t)i; sd.stream = kStreamDraft;
-    sd.out_token = c->seq; sd.out_idx = Lp; sd.out_off = i;
-    sd.partials = c->samp_part; sd.tickets = c->samp_tick;
     L.note(launch_sample(sd, c->stream));
   }
 }
 
 void enqueue_verify(Launch& L, bool commit) {
   spec_ctx* c = L.c;
-  const int K = c->K, V = c->tgt.d.vocab;
+  const int K = c->K, V = c->tgt.d.vocab, B = c->B;
   const int32_t* Lp = c->st;
   const bool was = c->timing_verify;
   c->timing_verify = commit && (c->opts.flags & SPEC_OPT_TIMING) != 0;
   if (c->persist)
     forward_persist(L, K);
-  else
+  else if (B == 1)
     forward(L, c->tgt, K + 1, c->seq, Lp, 0, Lp, 0, 0, K + 1, c->logits_p);
+  else
+    forward_batch(L, c->tgt, K + 1, 0, 0, c->logits_p);
   c->timing_verify = was;
   AcceptDesc ad{};
-  ad.p = c->logits_p; ad.p_ld = 0; ad.q = c->logits_q; ad.q_ld = 0;
+  ad.p = c->logits_p; ad.p_ld = (int64_t)(K + 1) * V; ad.q = c->logits_q; ad.q_ld = (int64_t)K * V;
+  ad.batch = 1; ad.st_ld = kStateLd; ad.seq_ld = c->seq_ld;
   ad.drafts = c->seq; ad.drafts_idx = Lp; ad.drafts_off = 1;
-  ad.drafts_copy = c->result + (K + 3);
-  ad.rows = 1; ad.K = K; ad.V = V; ad.temperature = c->opts.temperature; ad.seed = c->opts.seed;
+  ad.drafts_copy = c->result + (size_t)B * (K + 3);
+  ad.rows = B; ad.K = K; ad.V = V; ad.temperature = c->opts.temperature; ad.seed = c->opts.seed;
   ad.step_dev = c->st + 1; ad.step_base = 0;
-  ad.out_tokens = c->result; ad.out_count = c->result + (K + 1);
-  ad.out_flags = (uint32_t*)(c->result + (K + 2));
+  ad.out_tokens = c->result; ad.out_count = c->result + (size_t)B * (K + 1);
+  ad.out_flags = (uint32_t*)(c->result + (size_t)B * (K + 2));
   if (commit) {
     ad.commit_seq = c->seq; ad.commit_len = c->st; ad.commit_step = c->st + 1;
   }
@@ -440,10 +507,9 @@ void enqueue_verify(Launch& L, bool commit) {
 
 void enqueue_step(Launch& L) {
   spec_ctx* c = L.c;
-  const int K = c->K;
   enqueue_draft(L);
   enqueue_verify(L, true);
-  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 4),
+  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * res_words(c),
                          cudaMemcpyDeviceToHost, c->stream));
   c->launch_count--;  // the copy is not a kernel
 }
@@ -456,8 +522,10 @@ void enqueue_verify_forward(Launch& L) {
   const int32_t* Lp = c->st;
   if (c->persist)
     forward_persist(L, c->K);
-  else
+  else if (c->B == 1)
     forward(L, c->tgt, c->K + 1, c->seq, Lp, 0, Lp, 0, 0, c->K + 1, c->logits_p);
+  else
+    forward_batch(L, c->tgt, c->K + 1, 0, 0, c->logits_p);
 }
 
 void enqueue_ar_pass(Launch& L, bool commit) {
@@ -466,24 +534,23 @@ void enqueue_ar_pass(Launch& L, bool commit) {
   const int32_t* Lp = c->st;
   if (c->persist)
     forward_persist(L, c->K + 1);
-  else
+  else if (c->B == 1)
     forward(L, c->tgt, 1, c->seq, Lp, 0, Lp, 0, 0, 1, c->logits_p);
-  SampleDesc sd{};
-  sd.logits = c->logits_p; sd.ld = V; sd.rows = 1; sd.V = V;
-  sd.temperature = c->opts.temperature; sd.seed = c->opts.seed;
-  sd.step_dev = c->st + 2; sd.position = 0; sd.stream = kStreamAR;
-  sd.out_token = c->result; sd.out_idx = nullptr; sd.out_off = 0;
+  else
+    forward_batch(L, c->tgt, 1, 0, 0, c->logits_p);
+  SampleDesc sd = sampler(c, 2, c->result, 1, nullptr, 0);   // token of sequence b -> result[b]
+  sd.logits = c->logits_p; sd.ld = V;
+  sd.position = 0; sd.stream = kStreamAR;
   if (commit) {
     sd.commit_seq = c->seq; sd.commit_len = c->st; sd.commit_step = c->st + 2;
   }
-  sd.partials = c->samp_part; sd.tickets = c->samp_tick;
   L.note(launch_sample(sd, c->stream));
 }
 
 void enqueue_ar(Launch& L) {
   spec_ctx* c = L.c;
   enqueue_ar_pass(L, true);
-  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * c->K + 4),
+  L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * res_words(c),
                          cudaMemcpyDeviceToHost, c->stream));
   c->launch_count--;
 }
@@ -546,16 +613,17 @@ void free_ctx(spec_ctx* c) {
 // A grid-barrier wait of a persistent kernel gave up: clear the flag and the
 // barrier state so that the context stays usable, and report the timeout.
 int persist_timeout(spec_ctx* c) {
-  cudaMemsetAsync(c->result + (2 * c->K + 3), 0, sizeof(int32_t), c->stream);
+  cudaMemsetAsync(res_err(c), 0, sizeof(int32_t), c->stream);
   if (c->bar) cudaMemsetAsync(c->bar, 0, sizeof(unsigned) * 4, c->stream);
   cudaStreamSynchronize(c->stream);
   return fail(c, SPEC_E_TIMEOUT, "a bounded wait of a forward kernel (grid barrier or copy) timed out");
 }
 
-int set_eager_pos(spec_ctx* c, int pos) {
+// Position of a host-driven forward of sequence b: st[b][3] = pos.
+int set_eager_pos(spec_ctx* c, int pos, int b = 0) {
   *c->h_pos = pos;
-  CUDA_TRY(c, cudaMemcpyAsync(c->st + 3, c->h_pos, sizeof(int32_t), cudaMemcpyHostToDevice,
-                              c->stream));
+  CUDA_TRY(c, cudaMemcpyAsync(c->st + (size_t)b * kStateLd + 3, c->h_pos, sizeof(int32_t),
+                              cudaMemcpyHostToDevice, c->stream));
   return SPEC_OK;
 }
 
@@ -585,7 +653,12 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
                                            std::to_string(draft->vocab) + " vs " +
                                            std::to_string(target->vocab) + ")");
   if (K < 1 || K > 16) return fail(nullptr, SPEC_E_ARG, "K must be in 1..16");
-  if (opts->batch != 1) return fail(nullptr, SPEC_E_ARG, "only batch 1 is supported");
+  if (opts->batch < 1 || opts->batch > SPEC_MAX_BATCH)
+    return fail(nullptr, SPEC_E_ARG, "batch must be in 1..SPEC_MAX_BATCH");
+  if (opts->batch > 1 && (target->dtype != SPEC_DTYPE_BF16 || draft->dtype != SPEC_DTYPE_BF16))
+    return fail(nullptr, SPEC_E_ARG, "batch > 1 needs bf16 target and draft models");
+  if (opts->batch > 1 && opts->draft_mix_lambda != 0.f)
+    return fail(nullptr, SPEC_E_ARG, "batch > 1 does not support draft_mix_lambda");
   if (opts->max_ctx < K + 3) return fail(nullptr, SPEC_E_ARG, "max_ctx must be at least K + 3");
   if (!(opts->temperature >= 0.f)) return fail(nullptr, SPEC_E_ARG, "temperature must be >= 0");
   int dev = 0;
@@ -594,8 +667,11 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
 
   spec_ctx* c = new spec_ctx();
   c->K = K;
+  c->B = opts->batch;
   c->opts = *opts;
   c->cap = opts->max_ctx;
+  c->seq_ld = (int64_t)c->cap + K + 2;
+  c->host_Ls.assign(c->B, 0);
   c->max_chunks = (c->cap + kAttnChunk - 1) / kAttnChunk;
   auto setup_model = [&](ModelState& m, const spec_model_desc* d) {
     m.d = *d;
@@ -634,10 +710,12 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   const size_t hqd = mx([](const spec_model_desc& d) { return (size_t)d.n_heads * d.head_dim; });
   const size_t hqmax = mx([](const spec_model_desc& d) { return (size_t)d.n_heads; });
   const size_t hdmax = mx([](const spec_model_desc& d) { return (size_t)d.head_dim; });
-  INIT_TRY(dalloc(c, &c->st, 16 * sizeof(int32_t)));
-  INIT_TRY(cudaMemset(c->st, 0, 16 * sizeof(int32_t)));
-  INIT_TRY(dalloc(c, &c->seq, sizeof(int32_t) * (c->cap + K + 2)));
-  INIT_TRY(cudaMemset(c->seq, 0, sizeof(int32_t) * (c->cap + K + 2)));
+  const int B = c->B;
+  const size_t stw = std::max<size_t>(16, (size_t)kStateLd * B);
+  INIT_TRY(dalloc(c, &c->st, stw * sizeof(int32_t)));
+  INIT_TRY(cudaMemset(c->st, 0, stw * sizeof(int32_t)));
+  INIT_TRY(dalloc(c, &c->seq, sizeof(int32_t) * B * c->seq_ld));
+  INIT_TRY(cudaMemset(c->seq, 0, sizeof(int32_t) * B * c->seq_ld));
   INIT_TRY(dalloc(c, &c->fwd_tok, sizeof(int32_t) * maxN));
   INIT_TRY(dalloc(c, &c->x, sizeof(float) * maxN * dmax));
   INIT_TRY(dalloc(c, &c->xg, 2 * maxN * dmax));
@@ -659,25 +737,28 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     INIT_TRY(dalloc(c, &c->dattn_tick, sizeof(int) * dnt));
     INIT_TRY(cudaMemset(c->dattn_tick, 0, sizeof(int) * dnt));
   }
-  INIT_TRY(dalloc(c, &c->logits_p, sizeof(float) * (size_t)(K + 1) * V));
-  INIT_TRY(dalloc(c, &c->logits_q, sizeof(float) * (size_t)K * V));
+  INIT_TRY(dalloc(c, &c->logits_p, sizeof(float) * (size_t)B * (K + 1) * V));
+  INIT_TRY(dalloc(c, &c->logits_q, sizeof(float) * (size_t)B * K * V));
+  if (B > 1) INIT_TRY(dalloc(c, &c->logits_d, sizeof(float) * (size_t)2 * B * V));
   c->gs.partial_floats = gemm_partial_floats(c->num_sms);
   c->gs.max_tiles = (int)std::max<size_t>(
       (V + 15) / 16, std::max(fmax / 8, (std::max(qkvmax, dmax) + 15) / 16));
   INIT_TRY(dalloc(c, &c->gs.partials, sizeof(float) * c->gs.partial_floats));
   INIT_TRY(dalloc(c, &c->gs.tickets, sizeof(int) * c->gs.max_tiles));
   INIT_TRY(cudaMemset(c->gs.tickets, 0, sizeof(int) * c->gs.max_tiles));
-  INIT_TRY(dalloc(c, &c->samp_part, sizeof(float) * sample_partial_floats(1, V)));
-  INIT_TRY(dalloc(c, &c->samp_tick, sizeof(int) * 4));
-  INIT_TRY(cudaMemset(c->samp_tick, 0, sizeof(int) * 4));
-  INIT_TRY(dalloc(c, &c->acc_part, sizeof(float) * accept_partial_floats(1, K, V)));
-  INIT_TRY(dalloc(c, &c->acc_tick, sizeof(int) * 4));
-  INIT_TRY(cudaMemset(c->acc_tick, 0, sizeof(int) * 4));
-  INIT_TRY(dalloc(c, &c->result, sizeof(int32_t) * (2 * K + 8)));
-  INIT_TRY(cudaMallocHost(&c->h_result, sizeof(int32_t) * (2 * K + 8)));
+  const size_t nt = std::max(4, B);
+  INIT_TRY(dalloc(c, &c->samp_part, sizeof(float) * sample_partial_floats(B, V)));
+  INIT_TRY(dalloc(c, &c->samp_tick, sizeof(int) * nt));
+  INIT_TRY(cudaMemset(c->samp_tick, 0, sizeof(int) * nt));
+  INIT_TRY(dalloc(c, &c->acc_part, sizeof(float) * accept_partial_floats(B, K, V)));
+  INIT_TRY(dalloc(c, &c->acc_tick, sizeof(int) * nt));
+  INIT_TRY(cudaMemset(c->acc_tick, 0, sizeof(int) * nt));
+  const size_t rw = (size_t)res_words(c) + 7;
+  INIT_TRY(dalloc(c, &c->result, sizeof(int32_t) * rw));
+  INIT_TRY(cudaMallocHost(&c->h_result, sizeof(int32_t) * rw));
   INIT_TRY(cudaMallocHost(&c->h_pos, sizeof(int32_t) * 4));
   for (ModelState* m : {&c->tgt, &c->drf}) {
-    const size_t kvb = (size_t)m->d.n_layers * m->layer_kv_elems(c->cap) * m->esize;
+    const size_t kvb = (size_t)m->d.n_layers * B * m->layer_kv_elems(c->cap) * m->esize;
     INIT_TRY(dalloc(c, &m->kc, kvb));
     INIT_TRY(dalloc(c, &m->vc, kvb));
     INIT_TRY(cudaMemset(m->kc, 0, kvb));
@@ -689,10 +770,10 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
                                (double)m->d.rope_theta, c->stream));
     if (m->d.dtype == SPEC_DTYPE_BF16) {   // tensor maps of every layer's K and V cache
       std::vector<TensorMap128> maps(2 * (size_t)m->d.n_layers);
-      const long long rows = (long long)m->d.n_kv_heads * c->cap;
+      const long long rows = (long long)B * m->d.n_kv_heads * c->cap;   // every sequence of the layer
       bool ok = true;
       for (int l = 0; l < m->d.n_layers && ok; ++l) {
-        const size_t off = (size_t)l * m->layer_kv_elems(c->cap) * m->esize;
+        const size_t off = (size_t)l * B * m->layer_kv_elems(c->cap) * m->esize;
         ok = encode_kv_map(maps[2 * l], (char*)m->kc + off, m->d.head_dim, rows) &&
              encode_kv_map(maps[2 * l + 1], (char*)m->vc + off, m->d.head_dim, rows,
                            dattn_v_box_cols(m->d.head_dim));
@@ -705,11 +786,11 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
       INIT_TRY(cudaMemcpy(m->kv_maps, maps.data(), sizeof(TensorMap128) * maps.size(), cudaMemcpyHostToDevice));
     }
   }
-  INIT_TRY(cudaMemset(c->result, 0, sizeof(int32_t) * (2 * K + 8)));
+  INIT_TRY(cudaMemset(c->result, 0, sizeof(int32_t) * rw));
   // Persistent forward kernels: both models bf16, and the weight ring plus
   // K+1 tokens of normalised input (or the attention tile) fit one CTA's
   // shared memory.
-  if (target->dtype == SPEC_DTYPE_BF16 && draft->dtype == SPEC_DTYPE_BF16 &&
+  if (B == 1 && target->dtype == SPEC_DTYPE_BF16 && draft->dtype == SPEC_DTYPE_BF16 &&
       !(opts->flags & (SPEC_OPT_TIMING | SPEC_OPT_NO_PERSIST))) {
     const size_t sm_t = persist_smem_bytes(target->head_dim, c->max_chunks, K + 1, target->d_model);
     const size_t sm_d = persist_smem_bytes(draft->head_dim, c->max_chunks, 2, draft->d_model);
@@ -778,7 +859,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
           pf.desc.partials = c->gs.partials;
           pf.desc.tickets = c->gs.tickets;
           pf.desc.bar = c->bar;
-          pf.desc.err = c->result + (2 * K + 3);
+          pf.desc.err = res_err(c);
           const bool drf = f < K || f == K + 2;
           pf.hd = drf ? draft->head_dim : target->head_dim;
           pf.smem = drf ? sm_d : sm_t;
@@ -799,6 +880,30 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   return SPEC_OK;
 }
 
+// Step state of every sequence after a prefill of L tokens: L_b = L - 1
+// (position of the pending token), step counters 0.
+int reset_state(spec_ctx* c, int L) {
+  for (int b = 0; b < c->B; ++b) {
+    int32_t* w = c->h_result + (size_t)b * kStateLd;
+    w[0] = L - 1; w[1] = 0; w[2] = 0; w[3] = 0;
+  }
+  CUDA_TRY(c, cudaMemcpyAsync(c->st, c->h_result, sizeof(int32_t) * kStateLd * c->B, cudaMemcpyHostToDevice,
+                              c->stream));
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));   // h_result is reused by the step read-back
+  return SPEC_OK;
+}
+
+void mark_prefilled(spec_ctx* c, int L) {
+  c->host_L = L - 1;
+  c->host_Ls.assign(c->B, L - 1);
+  c->prefilled = true;
+  c->draft_stale = false;
+  c->steps = c->ar_steps = c->emitted = c->accepted = 0;
+  std::fill(std::begin(c->hist), std::end(c->hist), 0);
+}
+
+int max_host_L(const spec_ctx* c) { return *std::max_element(c->host_Ls.begin(), c->host_Ls.end()); }
+
 int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
   if (!tokens || L < 2) return fail(c, SPEC_E_ARG, "prefill needs at least 2 tokens");
@@ -806,14 +911,13 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
   const bool mix = c->opts.draft_mix_lambda != 0.f;
   if (mix && L < c->K + 2) return fail(c, SPEC_E_ARG, "mixed draft needs a prompt of at least K + 2 tokens");
   const int V = c->tgt.d.vocab;
-  for (int i = 0; i < L; ++i)
+  for (size_t i = 0; i < (size_t)c->B * L; ++i)
     if (tokens[i] < 0 || tokens[i] >= V) return fail(c, SPEC_E_ARG, "token id out of range");
   c->prefilled = false;
-  CUDA_TRY(c, cudaMemcpyAsync(c->seq, tokens, sizeof(int32_t) * L, cudaMemcpyHostToDevice, c->stream));
-  // st[0] = L - 1 (position of the pending token), step counters = 0
-  int32_t init[3] = {L - 1, 0, 0};
-  memcpy(c->h_result, init, sizeof init);
-  CUDA_TRY(c, cudaMemcpyAsync(c->st, c->h_result, sizeof init, cudaMemcpyHostToDevice, c->stream));
+  CUDA_TRY(c, cudaMemcpy2DAsync(c->seq, sizeof(int32_t) * c->seq_ld, tokens, sizeof(int32_t) * L,
+                                sizeof(int32_t) * L, c->B, cudaMemcpyHostToDevice, c->stream));
+  int rc = reset_state(c, L);
+  if (rc) return rc;
   const int n = L - 1;   // positions 0..L-2 are scored; token L-1 is pending
   const int K = c->K;
   const int lo = n - (K + 1);  // rows of the previous-step logits before step 0
@@ -822,22 +926,28 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
   // too (both models), so that both KV caches hold the same bits for it.
   const int nk = c->persist ? n - 1 : n;   // positions scored one kernel per operation
   Launch Lc{c};
-  for (int p0 = 0; p0 < nk; p0 += kGemmMaxTok) {
-    const int nt = std::min(kGemmMaxTok, nk - p0);
-    int rc = set_eager_pos(c, p0);
-    if (rc) return rc;
-    forward(Lc, c->drf, nt, c->seq, nullptr, p0, c->st + 3, 0, 0, 0, nullptr);
-    int r0 = 0, rn = 0;
-    if (mix) {
-      r0 = std::max(lo, p0) - p0;
-      rn = std::min(n, p0 + nt) - p0 - r0;
-      if (rn < 0) rn = 0;
+  for (int b = 0; b < c->B; ++b) {   // sequence by sequence, in chunks of positions
+    Seqs sq;
+    sq.seq0 = b;
+    const int32_t* sb = c->seq + (size_t)b * c->seq_ld;
+    const int32_t* pb = c->st + (size_t)b * kStateLd + 3;
+    for (int p0 = 0; p0 < nk; p0 += kGemmMaxTok) {
+      const int nt = std::min(kGemmMaxTok, nk - p0);
+      rc = set_eager_pos(c, p0, b);
+      if (rc) return rc;
+      forward(Lc, c->drf, nt, sb, nullptr, p0, pb, 0, 0, 0, nullptr, sq);
+      int r0 = 0, rn = 0;
+      if (mix) {
+        r0 = std::max(lo, p0) - p0;
+        rn = std::min(n, p0 + nt) - p0 - r0;
+        if (rn < 0) rn = 0;
+      }
+      float* dst = c->logits_p + (size_t)std::max(0, p0 + r0 - lo) * V;
+      forward(Lc, c->tgt, nt, sb, nullptr, p0, pb, 0, r0, rn, dst, sq);
+      CUDA_TRY(c, Lc.e);
+      // the pinned position slot is reused by the next chunk
+      CUDA_TRY(c, cudaStreamSynchronize(c->stream));
     }
-    float* dst = c->logits_p + (size_t)std::max(0, p0 + r0 - lo) * V;
-    forward(Lc, c->tgt, nt, c->seq, nullptr, p0, c->st + 3, 0, r0, rn, dst);
-    CUDA_TRY(c, Lc.e);
-    // the pinned position slot is reused by the next chunk
-    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   }
   if (c->persist) {
     c->grp = false;   // one token per pass
@@ -845,15 +955,41 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
     forward_persist(Lc, K + 3);
     CUDA_TRY(c, Lc.e);
   }
-  CUDA_TRY(c, cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * (2 * K + 4), cudaMemcpyDeviceToHost,
+  CUDA_TRY(c, cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * res_words(c), cudaMemcpyDeviceToHost,
                               c->stream));
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  if (c->h_result[2 * K + 3]) return persist_timeout(c);
-  c->host_L = L - 1;
-  c->prefilled = true;
-  c->draft_stale = false;
-  c->steps = c->ar_steps = c->emitted = c->accepted = 0;
-  std::fill(std::begin(c->hist), std::end(c->hist), 0);
+  if (c->h_result[res_words(c) - 1]) return persist_timeout(c);
+  mark_prefilled(c, L);
+  return SPEC_OK;
+}
+
+int spec_prefill_synthetic(spec_ctx* c, int L, uint64_t seed) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  if (L < 2) return fail(c, SPEC_E_ARG, "need at least 2 positions");
+  if (L + c->K + 1 > c->cap) return fail(c, SPEC_E_CAPACITY, "L + K + 1 exceeds max_ctx");
+  c->prefilled = false;
+  const int V = c->tgt.d.vocab;
+  CUDA_TRY(c, launch_fill_tokens(c->seq, (size_t)c->B * c->seq_ld, V, seed, c->stream));
+  uint64_t sub = 1;
+  for (ModelState* m : {&c->tgt, &c->drf}) {
+    const size_t elems = (size_t)m->d.n_layers * c->B * m->layer_kv_elems(c->cap);
+    CUDA_TRY(c, launch_fill_normal(m->kc, elems, m->d.dtype, seed ^ (0x9E3779B97F4A7C15ull * sub++), c->stream));
+    CUDA_TRY(c, launch_fill_normal(m->vc, elems, m->d.dtype, seed ^ (0x9E3779B97F4A7C15ull * sub++), c->stream));
+  }
+  int rc = reset_state(c, L);
+  if (rc) return rc;
+  mark_prefilled(c, L);
+  return SPEC_OK;
+}
+
+int spec_seq_context(spec_ctx* c, int b, int32_t* context, int32_t* len) {
+  if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
+  if (b < 0 || b >= c->B || !len) return fail(c, SPEC_E_ARG, "bad sequence index or null length");
+  const int n = c->host_Ls[b] + 1;
+  if (context)
+    CUDA_TRY(c, cudaMemcpy(context, c->seq + (size_t)b * c->seq_ld, sizeof(int32_t) * n,
+                           cudaMemcpyDeviceToHost));
+  *len = n;
   return SPEC_OK;
 }
 
@@ -862,25 +998,31 @@ int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* ou
   if (!out_tokens || !out_count) return fail(c, SPEC_E_ARG, "null output buffer");
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_step before spec_prefill");
   if (c->draft_stale) return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
-  if (c->host_L + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
-  const int K = c->K;
+  if (max_host_L(c) + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
+  const int K = c->K, B = c->B;
   c->ev_used = 0;
-  c->grp = c->host_L + K >= kDGroupMinPos;   // last verify position
+  c->grp = c->host_L + K >= kDGroupMinPos;   // last verify position (persistent path: batch 1)
   int rc = run_captured(c, &c->step_exec[c->grp], enqueue_step, &c->kernels_step);
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   const int32_t* h = c->h_result;
-  if (h[2 * K + 3]) return persist_timeout(c);
-  const int cnt = h[K + 1];
-  if (cnt < 1 || cnt > K + 1) return fail(c, SPEC_E_CUDA, "acceptance kernel returned an invalid count");
-  for (int i = 0; i < cnt; ++i) out_tokens[i] = h[i];
-  *out_count = cnt;
-  if (out_flags) *out_flags = (uint32_t)h[K + 2];
-  c->host_L += cnt;
+  if (h[res_words(c) - 1]) return persist_timeout(c);
+  for (int b = 0; b < B; ++b) {
+    const int cnt = h[(size_t)B * (K + 1) + b];
+    if (cnt < 1 || cnt > K + 1) return fail(c, SPEC_E_CUDA, "acceptance kernel returned an invalid count");
+  }
+  for (int b = 0; b < B; ++b) {
+    const int cnt = h[(size_t)B * (K + 1) + b];
+    for (int i = 0; i <= K; ++i) out_tokens[(size_t)b * (K + 1) + i] = h[(size_t)b * (K + 1) + i];
+    out_count[b] = cnt;
+    if (out_flags) out_flags[b] = (uint32_t)h[(size_t)B * (K + 2) + b];
+    c->host_Ls[b] += cnt;
+    c->emitted += cnt;
+    c->accepted += cnt - 1;
+    c->hist[cnt - 1]++;
+  }
+  c->host_L = c->host_Ls[0];
   c->steps++;
-  c->emitted += cnt;
-  c->accepted += cnt - 1;
-  c->hist[cnt - 1]++;
   if (c->opts.flags & SPEC_OPT_TIMING) {
     for (int i = 0; i + 1 < c->ev_used; i += 2) {
       float ms = 0.f;
@@ -896,6 +1038,7 @@ int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* ou
 int spec_generate(spec_ctx* c, int n_new, int32_t* out, int32_t* out_n) {
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
   if (n_new < 0 || (!out && n_new > 0) || !out_n) return fail(c, SPEC_E_ARG, "bad output buffer");
+  if (c->B != 1) return fail(c, SPEC_E_ARG, "spec_generate is for batch 1; call spec_step");
   std::vector<int32_t> buf(c->K + 1);
   int got = 0;
   while (got < n_new) {
@@ -912,14 +1055,17 @@ int spec_ar_step(spec_ctx* c, int32_t* out_token) {
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
   if (!out_token) return fail(c, SPEC_E_ARG, "null output buffer");
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_ar_step before spec_prefill");
-  if (c->host_L + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
+  if (max_host_L(c) + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
   c->grp = false;   // one token: nothing to share
   int rc = run_captured(c, &c->ar_exec, enqueue_ar, &c->kernels_ar);
   if (rc) return rc;
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  if (c->h_result[2 * c->K + 3]) return persist_timeout(c);
-  *out_token = c->h_result[0];
-  c->host_L += 1;
+  if (c->h_result[res_words(c) - 1]) return persist_timeout(c);
+  for (int b = 0; b < c->B; ++b) {
+    out_token[b] = c->h_result[b];
+    c->host_Ls[b] += 1;
+  }
+  c->host_L = c->host_Ls[0];
   c->ar_steps++;
   c->draft_stale = true;
   return SPEC_OK;
@@ -950,15 +1096,15 @@ int spec_get_stats(const spec_ctx* c, spec_stats* o) {
 int spec_last_step_debug(spec_ctx* c, float* p_logits, float* q_logits, int32_t* drafts,
                          int32_t* context, int32_t* context_len) {
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
-  const int K = c->K, V = c->tgt.d.vocab;
+  const int K = c->K, V = c->tgt.d.vocab, B = c->B;
   if (p_logits)
-    CUDA_TRY(c, cudaMemcpyAsync(p_logits, c->logits_p, sizeof(float) * (size_t)(K + 1) * V,
+    CUDA_TRY(c, cudaMemcpyAsync(p_logits, c->logits_p, sizeof(float) * (size_t)B * (K + 1) * V,
                                 cudaMemcpyDeviceToHost, c->stream));
   if (q_logits)
-    CUDA_TRY(c, cudaMemcpyAsync(q_logits, c->logits_q, sizeof(float) * (size_t)K * V,
+    CUDA_TRY(c, cudaMemcpyAsync(q_logits, c->logits_q, sizeof(float) * (size_t)B * K * V,
                                 cudaMemcpyDeviceToHost, c->stream));
   if (drafts)
-    CUDA_TRY(c, cudaMemcpyAsync(drafts, c->result + (K + 3), sizeof(int32_t) * K,
+    CUDA_TRY(c, cudaMemcpyAsync(drafts, c->result + (size_t)B * (K + 3), sizeof(int32_t) * B * K,
                                 cudaMemcpyDeviceToHost, c->stream));
   if (context)
     CUDA_TRY(c, cudaMemcpyAsync(context, c->seq, sizeof(int32_t) * (c->host_L + 1),
@@ -973,7 +1119,7 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   if (iters < 1) return fail(c, SPEC_E_ARG, "iters must be >= 1");
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_profile before spec_prefill");
   if (c->draft_stale) return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
-  if (c->host_L + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
+  if (max_host_L(c) + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
   void (*enq[4])(Launch&) = {enqueue_draft, enqueue_verify_only, enqueue_ar_only, enqueue_verify_forward};
   double ms[4];
   cudaEvent_t e0, e1;
@@ -999,7 +1145,7 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   cudaEventDestroy(e1);
   {
     int32_t flag = 0;
-    CUDA_TRY(c, cudaMemcpy(&flag, c->result + (2 * c->K + 3), sizeof flag, cudaMemcpyDeviceToHost));
+    CUDA_TRY(c, cudaMemcpy(&flag, res_err(c), sizeof flag, cudaMemcpyDeviceToHost));
     if (flag) return persist_timeout(c);
   }
   out->draft_loop_ms = ms[0];
@@ -1068,7 +1214,7 @@ int spec_model_forward(spec_ctx* c, int which, const int32_t* tokens, int n, int
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
   }
   int32_t flag = 0;
-  CUDA_TRY(c, cudaMemcpy(&flag, c->result + (2 * c->K + 3), sizeof flag, cudaMemcpyDeviceToHost));
+  CUDA_TRY(c, cudaMemcpy(&flag, res_err(c), sizeof flag, cudaMemcpyDeviceToHost));
   if (flag) return persist_timeout(c);
   return SPEC_OK;
 }

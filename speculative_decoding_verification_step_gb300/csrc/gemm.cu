@@ -228,6 +228,8 @@ cudaError_t launch_gemm(const GemmDesc& g, int dtype, const GemmScratch& s, int 
   if (g.epi == kEpiQkvRope && (g.hd % 16 != 0 || g.n != (g.hq + 2 * g.hkv) * g.hd))
     return cudaErrorInvalidValue;
   if (g.x_norm && g.k % 16 != 0) return cudaErrorInvalidValue;
+  if (g.epi == kEpiQkvRope && g.spt > 0 && (g.ntok % g.spt != 0 || (dtype == 0 && g.spt != g.ntok)))
+    return cudaErrorInvalidValue;   // whole sequences; fp32 models: one sequence per pass
   if (dtype == 0) {
     if (g.k % 4 != 0) return cudaErrorInvalidValue;
     return launch_k(gemv_f32, dim3((gemm_tiles(g) + 7) / 8), dim3(256), 0, st, g);

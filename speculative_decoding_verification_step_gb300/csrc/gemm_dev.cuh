@@ -71,6 +71,20 @@ struct EpiIn {
   float gn[2];
   int pos0;
 };
+
+// Position of token tok of a q/k/v GEMM (pos0 = *pos_base + pos_off, used
+// for one sequence) and the first KV row of its sequence.  kSeqs = false:
+// the caller runs single-sequence passes only (the persistent kernel).
+template <bool kSeqs = true>
+SV_DEV int tok_pos(const GemmDesc& g, int tok, int pos0) {
+  if (!kSeqs || g.spt <= 0) return pos0 + tok;
+  return g.pos_base[(size_t)(tok / g.spt) * g.pos_ld] + g.pos_off + tok % g.spt;
+}
+template <bool kSeqs = true>
+SV_DEV size_t tok_kv_row0(const GemmDesc& g, int tok) {
+  return kSeqs ? (size_t)seq_of_tok(g.spt, tok) * g.hkv * g.cap : 0;
+}
+template <bool kSeqs = true>
 SV_DEV void gemm_epi_load(const GemmDesc& g, int tile, int pos0, int gi, int ci, EpiIn& e) {
   e.pos0 = pos0;
   e.v[0] = e.v[1] = e.v[2] = e.v[3] = 0.f;
@@ -98,15 +112,16 @@ SV_DEV void gemm_epi_load(const GemmDesc& g, int tile, int pos0, int gi, int ci,
     for (int j = 0; j < 2; ++j) {
       const int tok = 2 * ci + j;
       if (tok >= g.ntok) continue;
-      e.v[j] = __ldg(g.rope_cos + (size_t)(pos0 + tok) * half + i);
-      e.v[2 + j] = __ldg(g.rope_sin + (size_t)(pos0 + tok) * half + i);
+      const int pos = tok_pos<kSeqs>(g, tok, pos0);
+      e.v[j] = __ldg(g.rope_cos + (size_t)pos * half + i);
+      e.v[2 + j] = __ldg(g.rope_sin + (size_t)pos * half + i);
     }
   }
 }
 
 // ---- epilogue: thread holds rows lo/hi of the tile for tokens ng*8 + 2ci + j;
 // pre (NG = 1 only): the inputs gemm_epi_load read, else they are loaded here ----
-template <int NG>
+template <int NG, bool kSeqs = true>
 SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4], int gi, int ci,
                           const EpiIn* pre = nullptr) {
   if (g.epi == kEpiSwiglu) {
@@ -131,9 +146,10 @@ SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4]
         const int tok = ng * 8 + 2 * ci + j;
         if (tok >= g.ntok) continue;
         const float x1 = acc[ng][j], x2 = acc[ng][2 + j];
-        const int pos = pre ? pre->pos0 + tok : *g.pos_base + g.pos_off + tok;
+        const int pos = tok_pos<kSeqs>(g, tok, pre ? pre->pos0 : (kSeqs && g.spt > 0 ? 0 : *g.pos_base + g.pos_off));
+        const size_t kv0 = tok_kv_row0<kSeqs>(g, tok);
         if (h >= g.hq + g.hkv) {   // value head: stored as is
-          bf16* dst = (bf16*)g.vc + ((size_t)(h - g.hq - g.hkv) * g.cap + pos) * g.hd;
+          bf16* dst = (bf16*)g.vc + (kv0 + (size_t)(h - g.hq - g.hkv) * g.cap + pos) * g.hd;
           dst[i] = __float2bfloat16_rn(x1);
           dst[i + half] = __float2bfloat16_rn(x2);
           continue;
@@ -146,7 +162,7 @@ SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4]
           dq[i] = y1;
           dq[i + half] = y2;
         } else {
-          bf16* dst = (bf16*)g.kc + ((size_t)(h - g.hq) * g.cap + pos) * g.hd;
+          bf16* dst = (bf16*)g.kc + (kv0 + (size_t)(h - g.hq) * g.cap + pos) * g.hd;
           dst[i] = __float2bfloat16_rn(y1);
           dst[i + half] = __float2bfloat16_rn(y2);
         }

@@ -7,6 +7,15 @@
 
 namespace sv {
 
+// Batched passes: the tokens of a pass are the sequences' tokens in sequence
+// order, spt per sequence (token t is token t % spt of sequence t / spt;
+// spt <= 0: one sequence).  Per-sequence device state (committed length L,
+// step counters, ...) is kStateLd int32 apart; sequence b's KV rows are
+// those of KV heads b * hkv .. b * hkv + hkv - 1 of a [B * hkv][cap][hd] cache.
+constexpr int kStateLd = 4;
+__host__ __device__ inline int seq_of_tok(int spt, int t) { return spt > 0 ? t / spt : 0; }
+__host__ __device__ inline int idx_in_seq(int spt, int t) { return spt > 0 ? t % spt : t; }
+
 enum Epi : int {
   kEpiStore = 0,    // out_f32[tok][row] = y
   kEpiAdd = 1,      // out_f32[tok][row] += y (residual add); optionally per-tile sums of
@@ -52,8 +61,9 @@ struct GemmDesc {
   const float* gain_next;  // the next RMSNorm's x_norm = 2 input
   // kEpiQkvRope
   int hq, hkv, hd, cap;
-  const int32_t* pos_base;   // position of token t = *pos_base + pos_off + t
-  int pos_off;
+  const int32_t* pos_base;   // position of token t = *pos_base + pos_off + t, or with
+  int pos_off;               // spt > 0: pos_base[b * pos_ld] + pos_off + j (token j of sequence b)
+  int spt, pos_ld;
   const float* rope_cos;     // [cap][hd/2]
   const float* rope_sin;
   float* q_out;              // [ntok][hq][hd]
@@ -87,12 +97,16 @@ cudaError_t configure_gemm();
 
 // x[t][:] = embed[tok[t]][:] (fp32 residual stream), with
 // tok = tok_base + (tok_idx ? *tok_idx : 0) + tok_off (device-resident index);
+// with spt > 0 token j of sequence b is tok_base[b * tok_ld + (tok_idx ?
+// tok_idx[b * idx_ld] : 0) + tok_off + j];
 // ss[i][t] = sum of x[t][16i .. 16i+15]^2 (the first RMSNorm's input);
 // optionally xg[t][:] = bf16(x[t][:] * gain) (its x_norm = 2 input).
 struct EmbedDesc {
   const int32_t* tok_base;
   const int32_t* tok_idx;
   int tok_off;
+  int spt, idx_ld;
+  int64_t tok_ld;
   const void* embed;
   int dtype;
   float* x;
@@ -113,8 +127,10 @@ struct AttnDesc {
   const float* q;          // [ntok][hq][hd] fp32 (rotated)
   const void* kc;          // [hkv][cap][hd]
   const void* vc;
-  const int32_t* pos_base; // query t sits at *pos_base + pos_off + t
-  int pos_off;
+  const int32_t* pos_base; // query t sits at *pos_base + pos_off + t, or with spt > 0
+  int pos_off;             // (bf16 path only) at pos_base[b * pos_ld] + pos_off + j
+  int spt, pos_ld;
+  int seq0;                // bf16 path: sequence b of the pass is cache sequence seq0 + b
   float* partials;         // [ntok*hq][max_chunks][hd+2]
   int* tickets;            // [hkv][row tiles], zero before and after
   void* out;               // [ntok][hq*hd] model dtype
@@ -162,7 +178,8 @@ struct SampleDesc {
   const float* mix_src;     // optional second row set (same layout), mixed in at weight lambda
   int64_t mix_ld;
   float lambda;
-  float* mixed_out;         // where the mixed row is written (needed when mix_src != null)
+  float* mixed_out;         // where the mixed row (or, without mix_src, the row) is written;
+                            // needed when mix_src != null
   int64_t mixed_ld;
   int rows, V;
   float temperature;
@@ -178,6 +195,12 @@ struct SampleDesc {
   int32_t* commit_seq;
   int32_t* commit_len;
   int32_t* commit_step;     // incremented when committing
+  // batch = 1: row r is sequence r of a batch -- step = step_dev[r * st_ld] +
+  // step_base with Philox row word r, the token goes to out_token[r * out_ld +
+  // (out_idx ? out_idx[r * st_ld] : 0) + out_off], and the commit uses
+  // commit_seq + r * seq_ld, commit_len[r * st_ld], commit_step[r * st_ld]
+  int batch, st_ld;
+  int64_t out_ld, seq_ld;
   float* partials;          // scratch [rows][chunks][2]
   int* tickets;             // [rows], zero before and after
 };
@@ -201,10 +224,16 @@ struct AcceptDesc {
   int32_t* out_tokens;      // [rows][K+1]
   int32_t* out_count;       // [rows]
   uint32_t* out_flags;      // [rows] or null
-  // optional commit (rows == 1): seq[len+1..len+n+1] = emitted; len += n+1; step += 1
+  // optional commit (rows == 1, or batch): seq[len+1..len+n+1] = emitted; len += n+1; step += 1
   int32_t* commit_seq;
   int32_t* commit_len;
   int32_t* commit_step;
+  // batch = 1: row r is sequence r -- step = step_dev[r * st_ld] + step_base
+  // with Philox row word r, drafts at drafts + r * seq_ld + (drafts_idx ?
+  // drafts_idx[r * st_ld] : 0) + drafts_off, commit into commit_seq + r * seq_ld,
+  // commit_len[r * st_ld], commit_step[r * st_ld]
+  int batch, st_ld;
+  int64_t seq_ld;
   float* partials;          // scratch [rows][chunks][2K+1][2]
   int* tickets;             // [rows]
 };
@@ -275,6 +304,12 @@ bool persist_supported(int hd, size_t smem, int num_sms, int max_tok);
 // group: attention items take token groups (kDGroupMinPos); either mode gives
 // the same bits, the caller picks the faster one for the pass's positions.
 cudaError_t launch_persist(const PersistDesc& p, int hd, bool group, size_t smem, int num_sms, cudaStream_t st);
+
+// Synthetic state: token ids uniform in [0, V) (up to a modulo bias below
+// 2^-40) and normally distributed values (dtype 0 fp32, 1 bf16), both from a
+// counter-based generator keyed by seed.
+cudaError_t launch_fill_tokens(int32_t* p, size_t n, int V, uint64_t seed, cudaStream_t st);
+cudaError_t launch_fill_normal(void* p, size_t n, int dtype, uint64_t seed, cudaStream_t st);
 
 // RoPE tables: cos/sin of pos * theta^(-2i/hd) for pos < cap, computed in fp64.
 cudaError_t launch_rope_table(float* cos_out, float* sin_out, int cap, int hd, double theta,

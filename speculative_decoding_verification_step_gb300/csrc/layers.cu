@@ -53,6 +53,51 @@ cudaError_t launch_rope_table(float* cos_out, float* sin_out, int cap, int hd, d
                   sin_out, cap, hd, theta);
 }
 
+// ---------------------------------------------------------------- synthetic state
+// SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+// generators", 2014): one 64-bit word per (seed, index).
+__device__ __forceinline__ unsigned long long splitmix64(unsigned long long z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__global__ void fill_tokens_kernel(int32_t* p, size_t n, int V, unsigned long long seed) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    p[i] = (int32_t)(splitmix64(seed ^ splitmix64(i)) % (unsigned long long)V);
+}
+
+// Box-Muller on two 24-bit uniforms of one word: u1 in (0, 1], u2 in [0, 1).
+template <typename T>
+__global__ void fill_normal_kernel(T* p, size_t n, unsigned long long seed) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const unsigned long long w = splitmix64(seed ^ splitmix64(i));
+    const float u1 = ((float)(w >> 40) + 1.0f) * (1.0f / 16777216.0f);
+    const float u2 = (float)((w >> 16) & 0xFFFFFFull) * (1.0f / 16777216.0f);
+    const float z = sqrtf(-2.0f * logf(u1)) * cospif(2.0f * u2);
+    p[i] = from_f32<T>(z);
+  }
+}
+
+static unsigned fill_grid(size_t n) {
+  const size_t blocks = (n + 255) / 256;
+  return (unsigned)(blocks < 65536 ? (blocks ? blocks : 1) : 65536);
+}
+
+cudaError_t launch_fill_tokens(int32_t* p, size_t n, int V, uint64_t seed, cudaStream_t st) {
+  if (V < 1) return cudaErrorInvalidValue;
+  return launch_k(fill_tokens_kernel, dim3(fill_grid(n)), dim3(256), 0, st, p, n, V, (unsigned long long)seed);
+}
+
+cudaError_t launch_fill_normal(void* p, size_t n, int dtype, uint64_t seed, cudaStream_t st) {
+  if (dtype == 1)
+    return launch_k(fill_normal_kernel<bf16>, dim3(fill_grid(n)), dim3(256), 0, st, (bf16*)p, n,
+                    (unsigned long long)seed);
+  return launch_k(fill_normal_kernel<float>, dim3(fill_grid(n)), dim3(256), 0, st, (float*)p, n,
+                  (unsigned long long)seed);
+}
+
 // ---------------------------------------------------------------- attention
 // Query rows of one KV head: row r = t * G + j (token t, query head
 // kvh * G + j, G = hq / hkv).  A CTA takes up to 32 rows and one 64-key chunk
@@ -115,6 +160,7 @@ int dattn_tickets(int max_tok, int hq, int hkv) { return max_tok * hkv * dattn_h
 
 cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st) {
   if (a.dtype != 1 || a.hq % a.hkv != 0 || !a.tmk || !a.tmv) return cudaErrorInvalidValue;
+  if (a.spt > 0 && a.ntok % a.spt != 0) return cudaErrorInvalidValue;
   const int items = dattn_items(a.ntok, a.hq, a.hkv, a.cap, a.hd);
   if (a.hd == 32) return launch_k(dattn_kernel<32>, dim3(items), dim3(kDWarps * 32), DAttnSmem<32>::kBytes, st, a);
   if (a.hd == 64) return launch_k(dattn_kernel<64>, dim3(items), dim3(kDWarps * 32), DAttnSmem<64>::kBytes, st, a);
@@ -149,6 +195,7 @@ static cudaError_t launch_attn_t(const AttnDesc& a, cudaStream_t st) {
 
 cudaError_t launch_attention(const AttnDesc& a, cudaStream_t st) {
   if (a.hq % a.hkv != 0) return cudaErrorInvalidValue;
+  if (a.spt > 0 && a.spt != a.ntok) return cudaErrorInvalidValue;   // one sequence per pass
   if (a.dtype == 0) {
     if (a.hd == 32) return launch_attn_t<32, float>(a, st);
     if (a.hd == 64) return launch_attn_t<64, float>(a, st);

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
     const int next_word = ph + 1 < p.nphases ? load_desc(ph + 1) : 0;
     unsigned long long* const st = times ? times + 1 + kPhaseStamps * ph : nullptr;
     if (d.kind == kPhaseEmbed) {
-      for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16>(d.e, t);
+      for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16, false>(d.e, t);
     } else if (d.kind == kPhaseGemm) {
       if (d.xm == kXSmem) tma_prepare_xg(d, tp, s_inv, xreg);
       if (st && threadIdx.x == 0) atomicMax(st + 3, global_ns());
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
       }
     } else {
       for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x)
-        dattn_item_mode<HD, kGroup>(d.a, it, dsm, &s_last, dbars, dpar, st ? st + 3 : nullptr);
+        dattn_item_mode<HD, kGroup, false>(d.a, it, dsm, &s_last, dbars, dpar, st ? st + 3 : nullptr);
       if (st && threadIdx.x == 0) atomicMax(st + 4, global_ns());
     }
     npre = 0;

@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
   const int nch = gridDim.x;
   const float* row = s.logits + (size_t)r * s.ld;
   const float* mix = s.mix_src ? s.mix_src + (size_t)r * s.mix_ld : nullptr;
-  float* mixed = s.mix_src ? s.mixed_out + (size_t)r * s.mixed_ld : nullptr;
+  float* mixed = s.mixed_out ? s.mixed_out + (size_t)r * s.mixed_ld : nullptr;
   const int v0 = c * kVocabChunk, v1 = min(s.V, v0 + kVocabChunk);
   const bool greedy = s.temperature == 0.f;
   const float invT = greedy ? 1.f : 1.0f / s.temperature;
@@ -264,6 +264,12 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
     }
     __syncthreads();
     src = mixed;   // this CTA's own writes: visible to its threads after the barrier
+  } else if (mixed) {   // no mixing: the row itself is kept there
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const int v = v0 + threadIdx.x + j * kSampThreads;
+      if (v < v1) mixed[v] = row[v];
+    }
   }
   float* part = s.partials + ((size_t)r * nch + c) * 3;
   if (greedy) {
@@ -309,20 +315,34 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
     const float M = gmax;
     for (int k = threadIdx.x; k < nch; k += kSampThreads)
       sh.mass[k] = (pm[k] == neg_inf()) ? 0.0 : (double)(pz[k] * expf(pm[k] - M));
-    const uint32_t step = (uint32_t)((s.step_dev ? (uint64_t)*s.step_dev : 0) + s.step_base + r);
-    const float u = philox_uniform(s.seed, step, s.position, s.stream, 0);
+    // batch: row r is sequence r (its own step counter, Philox row word r);
+    // else rows are independent draws at steps step + r
+    const uint64_t st0 = s.step_dev ? (uint64_t)s.step_dev[s.batch ? (size_t)r * s.st_ld : 0] : 0;
+    const uint32_t step = (uint32_t)(st0 + s.step_base + (s.batch ? 0 : r));
+    const float u = philox_uniform(s.seed, step, s.position, s.stream, s.batch ? (uint32_t)r : 0u);
     pick_chunk(sh, nch, u);
     const float* srcall = mix ? mixed : row;
     auto wfn = [&](int v) { return expf(__ldcg(srcall + v) * invT - M); };
     tok = rescan_chunk(sh, wfn, s.V);
   }
   if (threadIdx.x == 0) {
-    s.out_token[(s.out_idx ? *s.out_idx : 0) + s.out_off + r] = tok;
-    if (s.commit_seq) {
-      const int len = *s.commit_len;
-      s.commit_seq[len + 1] = tok;
-      *s.commit_len = len + 1;
-      *s.commit_step += 1;
+    if (s.batch) {
+      const size_t so = (size_t)r * s.seq_ld, io = (size_t)r * s.st_ld;
+      s.out_token[(size_t)r * s.out_ld + (s.out_idx ? s.out_idx[io] : 0) + s.out_off] = tok;
+      if (s.commit_seq) {
+        const int len = s.commit_len[io];
+        s.commit_seq[so + len + 1] = tok;
+        s.commit_len[io] = len + 1;
+        s.commit_step[io] += 1;
+      }
+    } else {
+      s.out_token[(s.out_idx ? *s.out_idx : 0) + s.out_off + r] = tok;
+      if (s.commit_seq) {
+        const int len = *s.commit_len;
+        s.commit_seq[len + 1] = tok;
+        *s.commit_len = len + 1;
+        *s.commit_step += 1;
+      }
     }
     s.tickets[r] = 0;
   }
@@ -376,8 +396,14 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
   if (!last_arrival(a.tickets, r, nstat * nch, &sm_flag)) return;
 
   // ---- phase B: fold partials in chunk order, decisions ----
-  const uint32_t step = (uint32_t)((a.step_dev ? (uint64_t)*a.step_dev : 0) + a.step_base + r);
-  const int32_t* D = a.drafts + (a.drafts_idx ? *a.drafts_idx : 0) + a.drafts_off + (size_t)r * K;
+  // batch: row r is sequence r (its own step counter, Philox row word r,
+  // drafts in its own token array); else rows are independent verify rows
+  const size_t io = a.batch ? (size_t)r * a.st_ld : 0;
+  const uint64_t st0 = a.step_dev ? (uint64_t)a.step_dev[io] : 0;
+  const uint32_t step = (uint32_t)(st0 + a.step_base + (a.batch ? 0 : r));
+  const uint32_t prow = a.batch ? (uint32_t)r : 0u;
+  const int32_t* D = a.batch ? a.drafts + (size_t)r * a.seq_ld + (a.drafts_idx ? a.drafts_idx[io] : 0) + a.drafts_off
+                             : a.drafts + (a.drafts_idx ? *a.drafts_idx : 0) + a.drafts_off + (size_t)r * K;
   const float* PR = a.partials + (size_t)r * nrow * nch * 2;
   // all partials of this verify row into shared memory, loaded in parallel
   __shared__ float pa_[(2 * kMaxK + 1) * kMaxChunks], pb_[(2 * kMaxK + 1) * kMaxChunks];
@@ -422,7 +448,7 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
         const float lp = P[(size_t)i * V + d] * invT - (float)rowM[i];
         const float lq = Q[(size_t)i * V + d] * invT - (float)rowM[K + 1 + i];
         const float ratio = expf(lp - lq) * (float)(rowZ[K + 1 + i] / rowZ[i]);
-        const float rr = philox_uniform(a.seed, step, (uint32_t)(i + 1), kStreamAccept, 0);
+        const float rr = philox_uniform(a.seed, step, (uint32_t)(i + 1), kStreamAccept, prow);
         if (!(rr < fminf(1.0f, ratio))) { n = i; kind = 0; break; }
       }
     }
@@ -464,7 +490,7 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
       acc = warp_sum(acc);
       if (lane == 0) sh.mass[cc] = (double)acc;
     }
-    const float u = philox_uniform(a.seed, step, (uint32_t)(n + 1), kStreamResidual, 0);
+    const float u = philox_uniform(a.seed, step, (uint32_t)(n + 1), kStreamResidual, prow);
     const double z = pick_chunk(sh, nch, u);
     if (z > 0.0) {
       tok = rescan_chunk(sh, wres, V);
@@ -485,7 +511,7 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
       const float m = pa_[K * nch + k], sm = pb_[K * nch + k];
       sh.mass[k] = (m == neg_inf()) ? 0.0 : (double)(sm * expf(m - (float)rowM[K]));
     }
-    const float u = philox_uniform(a.seed, step, (uint32_t)(K + 1), kStreamBonus, 0);
+    const float u = philox_uniform(a.seed, step, (uint32_t)(K + 1), kStreamBonus, prow);
     pick_chunk(sh, nch, u);
     auto wp = [&](int v) { return expf(pr[v] * invT - mp); };
     tok = rescan_chunk(sh, wp, V);
@@ -501,10 +527,11 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
     a.out_count[r] = n + 1;
     if (a.out_flags) a.out_flags[r] = flags;
     if (a.commit_seq) {
-      const int len = *a.commit_len;
-      for (int i = 0; i <= n; ++i) a.commit_seq[len + 1 + i] = out[i];
-      *a.commit_len = len + n + 1;
-      *a.commit_step += 1;
+      int32_t* cs = a.commit_seq + (a.batch ? (size_t)r * a.seq_ld : 0);
+      const int len = a.commit_len[io];
+      for (int i = 0; i <= n; ++i) cs[len + 1 + i] = out[i];
+      a.commit_len[io] = len + n + 1;
+      a.commit_step[io] += 1;
     }
     a.tickets[r] = 0;
   }

@@ -273,7 +273,7 @@ SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs
   const float sc0 = s_inv ? s_inv[2 * ci] : 1.f, sc1 = s_inv ? s_inv[2 * ci + 1] : 1.f;
   if (kbs == 0 && kbe == r.kbpt) {
     const float y[1][4] = {{tot[0][0] * sc0, tot[0][1] * sc1, tot[0][2] * sc0, tot[0][3] * sc1}};
-    gemm_epilogue<1>(g, tile, y, gi, ci);
+    gemm_epilogue<1, false>(g, tile, y, gi, ci);
     return;
   }
   float* mine = partials + (((size_t)blockIdx.x * 2 + pslot) * kMaxMmaTiles + warp) * 32 * 4;
@@ -288,7 +288,7 @@ SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs
   __syncwarp();
   // the epilogue's own inputs are loaded together with the first partials
   EpiIn pre;
-  gemm_epi_load(g, tile, pos0, gi, ci, pre);
+  gemm_epi_load<false>(g, tile, pos0, gi, ci, pre);
   float4 pv[2];
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
@@ -319,7 +319,7 @@ SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs
   sum[0][1] *= sc1;
   sum[0][2] *= sc0;
   sum[0][3] *= sc1;
-  gemm_epilogue<1>(g, tile, sum, gi, ci, &pre);
+  gemm_epilogue<1, false>(g, tile, sum, gi, ci, &pre);
   if (lane == 0) tickets[tile] = 0;
 }
 

@@ -49,8 +49,8 @@ def _desc(vocab=256, head_dim=32, dtype=sv.SPEC_DTYPE_F32, layers=None):
     return d, lay
 
 
-def _init(L, t, d, k=4, max_ctx=128):
-    opts = sv.Opts(1, max_ctx, 1.0, 0, 0.0, None, 0)
+def _init(L, t, d, k=4, max_ctx=128, batch=1, mix=0.0):
+    opts = sv.Opts(batch, max_ctx, 1.0, 0, mix, None, 0)
     h = ctypes.c_void_p()
     rc = L.spec_init(ctypes.byref(t) if t is not None else None,
                      ctypes.byref(d) if d is not None else None, k, ctypes.byref(opts), ctypes.byref(h))
@@ -77,6 +77,19 @@ def test_init_argument_errors(L):
     assert _init(L, nl, d)[0] == -1
 
 
+def test_batch_argument_errors(L):
+    t, _a = _desc()
+    d, _b = _desc()
+    assert _init(L, t, d, batch=0)[0] == -1
+    assert _init(L, t, d, batch=sv.SPEC_MAX_BATCH + 1)[0] == -1
+    assert _init(L, t, d, batch=2)[0] == -1                 # batch > 1 needs bf16 models
+    assert b"bf16" in L.spec_last_error(None)
+    bt, _c = _desc(dtype=sv.SPEC_DTYPE_BF16)
+    bd, _d = _desc(dtype=sv.SPEC_DTYPE_BF16)
+    assert _init(L, bt, bd, batch=2, mix=0.5)[0] == -1      # no draft mixing in batches
+    assert b"draft_mix_lambda" in L.spec_last_error(None)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_no_cpu_fallback(L):
     t, _a = _desc()
@@ -101,6 +114,8 @@ def test_null_context_calls(L):
     assert L.spec_prefill(None, None, 0) == -1
     assert L.spec_step(None, None, None, None) == -1
     assert L.spec_ar_step(None, None) == -1
+    assert L.spec_prefill_synthetic(None, 16, 0) == -1
+    assert L.spec_seq_context(None, 0, None, None) == -1
     assert L.spec_get_stats(None, None) == -1
     assert L.spec_last_error(None)
 

@@ -59,8 +59,13 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of both models")
     ap.add_argument("--verify-sweep", action="store_true",
-                    help="verify step alone at batch 1 over K x context (one JSON line each): "
-                         "latency, algorithmic bytes, GB/s")
+                    help="verify step alone over batch x K x context (one JSON line each): "
+                         "latency, algorithmic bytes, GB/s, tensor FLOP/s")
+    ap.add_argument("--sweep-batches", default="1",
+                    help="comma-separated batch sizes of --verify-sweep (batch > 1: synthetic KV)")
+    ap.add_argument("--sweep-ks", default="1,2,3,4,5,6,8", help="comma-separated K of --verify-sweep")
+    ap.add_argument("--sweep-contexts", default="512,4096,16384",
+                    help="comma-separated contexts of --verify-sweep")
     return ap.parse_args()
 
 
@@ -78,6 +83,16 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tflops_peak():
+    """Dense bf16 tensor FLOP/s of a kernel timed alone (MEASURED_PEAKS.json
+    burst figure, else the fallback), in TFLOP/s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 class ClockSampler:
@@ -352,28 +367,52 @@ def main():
         return ms, toks, done
 
     if args.verify_sweep:
-        # the verify step (target over K+1 positions + fused acceptance) after a
-        # prefill of `context` uniform-random ids, replayed as a graph
+        # the verify step (target over K+1 positions per sequence + fused
+        # acceptance) replayed as a graph, after a prefill of `context`
+        # uniform-random ids (batch 1) or a synthetic state of `context`
+        # positions (batch > 1: random ids, KV caches filled with N(0, 1)
+        # values -- the same bytes read, not the models' own keys and values)
         peak, peak_kind = peaks()
-        for ctx in (512, 4096, 16384):
-            prm = workloads.make_prompt(tshape.vocab, ctx, seed=77)[0].tolist()
-            for k in (1, 2, 3, 4, 5, 6, 8):
-                d = sv.SpecDecoder(tshape, tw, dshape, dw, k, ctx + 2 * (k + 1) + 64, temperature=args.temperature,
-                                   seed=0, mix_lambda=0.0, stream=stream.cuda_stream)
-                d.prefill(prm)
-                prof = d.profile(iters=10)
-                st = d.stats()
-                L = ctx - 1                      # committed positions before the pending token
-                nbytes = (st["verify_weight_bytes"] + (L + k + 1) * st["kv_bytes_per_token_target"]
-                          + (k + 1) * tshape.vocab * 4)
-                gbs = nbytes / (prof["verify_ms"] * 1e6)
-                print(json.dumps({"verify_sweep": True, "workload": wl, "batch": 1, "K": k, "context": ctx,
-                                  "verify_step_ms": prof["verify_ms"],
-                                  "target_forward_ms": prof["verify_forward_ms"],
-                                  "bytes": nbytes, "GB_s": gbs, "frac_of_measured": gbs / peak,
-                                  "peak_kind": peak_kind, "kernels_per_verify": prof["kernels_verify"],
-                                  "persistent": prof["kernels_verify"] <= 2}), flush=True)
-                d.close()
+        tf_peak = tflops_peak()
+        kv_tok = tshape.kv_bytes_per_token() + dshape.kv_bytes_per_token()
+        for batch in [int(x) for x in args.sweep_batches.split(",")]:
+            for ctx in [int(x) for x in args.sweep_contexts.split(",")]:
+                prm = workloads.make_prompt(tshape.vocab, ctx, seed=77)[0].tolist()
+                for k in [int(x) for x in args.sweep_ks.split(",")]:
+                    cap = ctx + 2 * (k + 1) + 64
+                    need = batch * cap * kv_tok * 1.05 + 2e9
+                    free = torch.cuda.mem_get_info()[0]
+                    line = {"verify_sweep": True, "workload": wl, "batch": batch, "K": k, "context": ctx}
+                    if need > free:
+                        line["skipped"] = f"KV caches need {need / 1e9:.0f} GB, {free / 1e9:.0f} GB free"
+                        print(json.dumps(line), flush=True)
+                        continue
+                    d = sv.SpecDecoder(tshape, tw, dshape, dw, k, cap, temperature=args.temperature,
+                                       seed=0, mix_lambda=0.0, stream=stream.cuda_stream, batch=batch)
+                    if batch == 1:
+                        d.prefill(prm)
+                    else:
+                        d.prefill_synthetic(ctx, seed=77)
+                    prof = d.profile(iters=10 if batch == 1 else 3)
+                    st = d.stats()
+                    L = ctx - 1                      # committed positions before the pending token
+                    nbytes = (st["verify_weight_bytes"] + batch * (L + k + 1) * st["kv_bytes_per_token_target"]
+                              + batch * (k + 1) * tshape.vocab * 4)
+                    sec = prof["verify_ms"] * 1e-3
+                    gbs = nbytes / sec / 1e9
+                    # dense GEMM flops: 2 x (weight elements) x verify rows
+                    tfl = 2.0 * st["verify_weight_bytes"] / 2 * batch * (k + 1) / sec / 1e12
+                    line.update({"kv": "prefill" if batch == 1 else "synthetic N(0,1)",
+                                 "verify_step_ms": prof["verify_ms"],
+                                 "target_forward_ms": prof["verify_forward_ms"],
+                                 "positions_per_s": batch * (k + 1) / sec,
+                                 "bytes": nbytes, "GB_s": gbs, "frac_of_measured": gbs / peak,
+                                 "peak_kind": peak_kind, "gemm_TFLOP_s": tfl, "frac_of_bf16_peak": tfl / tf_peak,
+                                 "kernels_per_verify": prof["kernels_verify"],
+                                 "persistent": prof["kernels_verify"] <= 2})
+                    print(json.dumps(line), flush=True)
+                    d.close()
+                    torch.cuda.synchronize()
         return 0
 
     if args.phase_times:

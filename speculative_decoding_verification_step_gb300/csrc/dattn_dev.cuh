@@ -463,15 +463,17 @@ SV_DEV void dattn_item_mode(const AttnDesc& a, int it, unsigned char* sm, int* s
 }
 
 // Item it of an attention phase: token groups once the last position of the
-// item's sequence in the pass reaches kDGroupMinPos, else one token per item
-// (the items of a sequence all take the same mode).
+// item's sequence in the pass reaches kDGroupMinPos, or when the pass asks for
+// them (a.group: batched passes with items for several waves of CTAs, where
+// half as many walks beats more parallel ones), else one token per item (the
+// items of a sequence all take the same mode).
 template <int HD>
 SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
                        unsigned& dpar, unsigned long long* stamp = nullptr) {
   using L = DAttnSmem<HD>;
   const int S = a.spt > 0 ? a.spt : a.ntok;
   const int b = dattn_item_of(a, it / L::kVParts, dattn_hgroups(a.hq, a.hkv), a.ntok).tg / S;
-  if (a.pos_base[(size_t)b * a.pos_ld] + a.pos_off + S - 1 >= kDGroupMinPos)
+  if (a.group || a.pos_base[(size_t)b * a.pos_ld] + a.pos_off + S - 1 >= kDGroupMinPos)
     dattn_item_rows<HD, true, true>(a, it, sm, s_last, bars, dpar, stamp);
   else
     dattn_item_rows<HD, false, true>(a, it, sm, s_last, bars, dpar, stamp);

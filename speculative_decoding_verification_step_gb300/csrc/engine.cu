@@ -80,6 +80,9 @@ struct spec_ctx {
   int K = 0;
   int B = 1;                       // sequences (batch > 1: per-operation path, bf16 models)
   int64_t seq_ld = 0;              // int32 stride between the sequences' token arrays
+  int tok_max = kGemmMaxTok;       // tokens per forward pass (batch > 1: up to kTcMaxTok)
+  float* tc_part = nullptr;        // tensor-core GEMM partials (batch > 1), tc_units work units
+  long long tc_units = 0;
   spec_opts opts{};
   cudaStream_t stream = nullptr;
   bool own_stream = false;
@@ -101,7 +104,7 @@ struct spec_ctx {
   float* attn_part = nullptr;
   int* attn_tick = nullptr;
   int* dattn_tick = nullptr;       // tensor-core attention (bf16 models)
-  float* ss = nullptr;         // [d_max/16][kGemmMaxTok] per-tile sums of squares
+  float* ss = nullptr;         // [d_max/16][tok_max] per-tile sums of squares
   float* logits_p = nullptr;  // [K+1][V]
   float* logits_q = nullptr;  // [B][K][V]
   float* logits_d = nullptr;  // batch > 1: [2B][V] draft-pass logits before sampling
@@ -229,6 +232,10 @@ struct Launch {
 
 void gemm(Launch& L, const GemmDesc& g, int dtype) {
   spec_ctx* c = L.c;
+  if (g.ntok > kGemmMaxTok) {   // many tokens (batched passes): tensor-memory GEMM
+    L.note(launch_tc_gemm(g, c->tc_part, res_err(c), c->num_sms, c->tc_units, c->stream));
+    return;
+  }
   const bool timed = c->timing_verify && c->ev_used + 2 <= (int)c->ev.size();
   if (timed) cudaEventRecord(c->ev[c->ev_used], c->stream);
   L.note(launch_gemm(g, dtype, c->gs, c->num_sms, c->stream, false));
@@ -281,7 +288,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
   Op op{};
   op.kind = kPhaseEmbed;
   op.e.tok_base = tok_base; op.e.tok_idx = tok_idx; op.e.tok_off = tok_off; op.e.embed = d.embed;
-  op.e.dtype = dt; op.e.x = c->x; op.e.ss = c->ss; op.e.ss_ld = kGemmMaxTok; op.e.ntok = ntok;
+  op.e.dtype = dt; op.e.x = c->x; op.e.ss = c->ss; op.e.ss_ld = c->tok_max; op.e.ntok = ntok;
   op.e.d = dm;
   op.e.spt = sq.spt; op.e.idx_ld = kStateLd; op.e.tok_ld = sq.tok_ld;
   if (pregain) {
@@ -314,7 +321,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     g.seg_rows[0] = hq * hd; g.seg_rows[1] = hkv * hd; g.seg_rows[2] = hkv * hd;
     g.n = qkvr; g.k = dm; g.ntok = ntok;
     norm_x(g, w.attn_norm, 0);
-    g.ss_in = c->ss; g.ss_ld = kGemmMaxTok; g.eps = d.rms_eps;
+    g.ss_in = c->ss; g.ss_ld = c->tok_max; g.eps = d.rms_eps;
     g.epi = kEpiQkvRope; g.hq = hq; g.hkv = hkv; g.hd = hd; g.cap = c->cap;
     g.pos_base = pos_idx; g.pos_off = pos_off; g.rope_cos = m.rope_cos; g.rope_sin = m.rope_sin;
     g.spt = sq.spt; g.pos_ld = kStateLd;
@@ -325,6 +332,9 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     AttnDesc& a = at.a;
     a.q = c->q; a.kc = kc; a.vc = vc; a.pos_base = pos_idx; a.pos_off = pos_off;
     a.spt = sq.spt; a.pos_ld = kStateLd; a.seq0 = sq.seq0;
+    // batched passes of several tokens per sequence with one-token items for
+    // at least two waves: token-group items (the same bits, half the walks)
+    a.group = sq.spt >= 2 && (long long)ntok * hkv * (hd >= 64 ? 2 : 1) >= 2LL * c->num_sms;
     a.partials = c->attn_part; a.tickets = c->attn_tick; a.out = c->attn;
     a.ntok = ntok; a.hq = hq; a.hkv = hkv; a.hd = hd; a.cap = c->cap;
     a.max_chunks = c->max_chunks; a.dtype = dt;
@@ -343,13 +353,13 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
       o.g.xg_out = c->xg;
       o.g.gain_next = (const float*)w.ffn_norm;
     }
-    o.g.ss_out = c->ss; o.g.ss_ld = kGemmMaxTok;
+    o.g.ss_out = c->ss; o.g.ss_ld = c->tok_max;
     ops.push_back(o);
     Op gu{};
     gu.kind = kPhaseGemm;
     gu.g.w[0] = w.w_gate; gu.g.w[1] = w.w_up; gu.g.n = d.ffn_dim; gu.g.k = dm; gu.g.ntok = ntok;
     norm_x(gu.g, w.ffn_norm, 0);
-    gu.g.ss_in = c->ss; gu.g.ss_ld = kGemmMaxTok; gu.g.eps = d.rms_eps;
+    gu.g.ss_in = c->ss; gu.g.ss_ld = c->tok_max; gu.g.eps = d.rms_eps;
     gu.g.epi = kEpiSwiglu; gu.g.out = c->hbuf; gu.g.ldo = d.ffn_dim;
     ops.push_back(gu);
     Op dn{};
@@ -360,7 +370,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
       dn.g.xg_out = c->xg;
       dn.g.gain_next = (const float*)(l + 1 < d.n_layers ? m.layers[l + 1].attn_norm : d.final_norm);
     }
-    dn.g.ss_out = c->ss; dn.g.ss_ld = kGemmMaxTok;
+    dn.g.ss_out = c->ss; dn.g.ss_ld = c->tok_max;
     dn.g.early_prefetch = 1;   // follows the gate/up GEMM
     ops.push_back(dn);
   }
@@ -369,7 +379,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     h.kind = kPhaseGemm;
     h.g.w[0] = d.lm_head; h.g.seg_rows[0] = d.vocab; h.g.n = d.vocab; h.g.k = dm; h.g.ntok = lrows;
     norm_x(h.g, d.final_norm, lrow0);
-    h.g.ss_in = c->ss + lrow0; h.g.ss_ld = kGemmMaxTok; h.g.eps = d.rms_eps;
+    h.g.ss_in = c->ss + lrow0; h.g.ss_ld = c->tok_max; h.g.eps = d.rms_eps;
     h.g.epi = kEpiStore; h.g.out = logits; h.g.ldo = d.vocab;
     ops.push_back(h);
   }
@@ -400,14 +410,25 @@ void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const 
   }
 }
 
+// True when every GEMM of the model meets the tensor-memory GEMM's tiling
+// (128-row tiles of the q/k/v segments and of d_model, 64-row gate/up
+// tiles, k in 64-element blocks).
+bool tc_model_ok(const ModelState& m) {
+  const spec_model_desc& d = m.d;
+  const int hd = d.head_dim, q = d.n_heads * hd, kv = d.n_kv_heads * hd;
+  return d.dtype == SPEC_DTYPE_BF16 && d.d_model % 128 == 0 && q % 128 == 0 && kv % 128 == 0 &&
+         128 % hd == 0 && d.ffn_dim % 64 == 0;
+}
+
 // Batched per-operation forward: spt tokens of every sequence, token j of
 // sequence b taken from seq[b][L_b + tok_off + j] at position L_b + pos_off
 // + j; the LM-head logits of all B * spt rows go to logits ([B][spt][V]).
-// Sequences are processed in groups of at most kGemmMaxTok tokens (each
-// group streams the weights once).
+// Sequences are processed in groups of at most c->tok_max tokens (each group
+// streams the weights once; groups of more than kGemmMaxTok tokens run their
+// GEMMs on the tensor-memory GEMM, when the model's shapes allow it).
 void forward_batch(Launch& L, ModelState& m, int spt, int tok_off, int pos_off, float* logits) {
   spec_ctx* c = L.c;
-  const int per = std::max(1, kGemmMaxTok / spt);
+  const int per = std::max(1, (tc_model_ok(m) ? c->tok_max : kGemmMaxTok) / spt);
   const size_t V = (size_t)m.d.vocab;
   for (int b0 = 0; b0 < c->B; b0 += per) {
     const int n = std::min(per, c->B - b0);
@@ -701,7 +722,8 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     c->own_stream = true;
   }
   const int V = target->vocab;
-  const int maxN = kGemmMaxTok;
+  c->tok_max = opts->batch > 1 ? kTcMaxTok : kGemmMaxTok;
+  const int maxN = c->tok_max;
   auto mx = [&](auto f) { return std::max(f(c->tgt.d), f(c->drf.d)); };
   const size_t dmax = mx([](const spec_model_desc& d) { return (size_t)d.d_model; });
   const size_t fmax = mx([](const spec_model_desc& d) { return (size_t)d.ffn_dim; });
@@ -746,6 +768,12 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   INIT_TRY(dalloc(c, &c->gs.partials, sizeof(float) * c->gs.partial_floats));
   INIT_TRY(dalloc(c, &c->gs.tickets, sizeof(int) * c->gs.max_tiles));
   INIT_TRY(cudaMemset(c->gs.tickets, 0, sizeof(int) * c->gs.max_tiles));
+  if (c->tok_max > kGemmMaxTok) {
+    const int maxn = (int)std::max<size_t>((size_t)V, std::max(2 * fmax, std::max(qkvmax, dmax)));
+    const size_t tpf = tc_gemm_partial_floats(c->num_sms, maxn);
+    c->tc_units = (long long)(tpf / ((size_t)128 * kTcMaxTok));
+    INIT_TRY(dalloc(c, &c->tc_part, sizeof(float) * tpf));
+  }
   const size_t nt = std::max(4, B);
   INIT_TRY(dalloc(c, &c->samp_part, sizeof(float) * sample_partial_floats(B, V)));
   INIT_TRY(dalloc(c, &c->samp_tick, sizeof(int) * nt));

@@ -87,6 +87,19 @@ struct GemmScratch {
 constexpr int kGemmWarpsPerCta = 8;
 constexpr int kGemmMaxTok = 64;      // tokens per GEMM pass (8 groups of 8)
 
+// Tensor-core (tcgen05) GEMM for passes of kGemmMaxTok < ntok <= kTcMaxTok
+// tokens (tcgemm.cu): row tiles of 128 weight rows x k splits; split GEMMs
+// write partials ([units][128][npad] fp32, at most max_units units,
+// tc_gemm_partial_floats) that a second launch reduces; err raised when a
+// bounded wait gives up.
+constexpr int kTcMaxTok = 256;
+constexpr int kTcSmemBytes = 4 * (128 * 64 * 2 + kTcMaxTok * 64 * 2) + 1024;
+bool tc_gemm_supported(const GemmDesc& g);
+size_t tc_gemm_partial_floats(int num_sms, int max_n);
+cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num_sms, long long max_units,
+                           cudaStream_t st);
+cudaError_t configure_tc_gemm();
+
 int gemm_grid(int num_sms);
 size_t gemm_partial_floats(int num_sms);
 int gemm_tiles(const GemmDesc& g);
@@ -131,6 +144,7 @@ struct AttnDesc {
   int pos_off;             // (bf16 path only) at pos_base[b * pos_ld] + pos_off + j
   int spt, pos_ld;
   int seq0;                // bf16 path: sequence b of the pass is cache sequence seq0 + b
+  int group;               // bf16 per-operation path: 1 = token-group items at any position
   float* partials;         // [ntok*hq][max_chunks][hd+2]
   int* tickets;            // [hkv][row tiles], zero before and after
   void* out;               // [ntok][hq*hd] model dtype

@@ -172,6 +172,7 @@ cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st) {
 cudaError_t configure_kernels() {
   cudaError_t e;
   if ((e = configure_gemm()) != cudaSuccess) return e;
+  if ((e = configure_tc_gemm()) != cudaSuccess) return e;
   if ((e = configure_attn<32, float>()) != cudaSuccess) return e;
   if ((e = configure_attn<64, float>()) != cudaSuccess) return e;
   if ((e = configure_attn<128, float>()) != cudaSuccess) return e;

@@ -1,0 +1,508 @@
+// Tensor-core GEMM on the fifth-generation tensor cores for passes of many
+// tokens (a batch of sequences' K+1 verify positions): Y = X . W^T with the
+// weights W [n][k] bf16 (the q/k/v segments, or the gate/up pair) and
+// X [ntok][k] bf16, 64 < ntok <= 256, fp32 accumulation in tensor memory.
+//
+// Work unit = (row tile, k split).  A row tile is 128 output rows (gate/up:
+// 64 gate rows then the same 64 up rows); the k range of the GEMM is cut into
+// `splits` contiguous runs of 64-element blocks, fixed by n, k and the grid
+// (not by ntok); each CTA starts its run at a tile-dependent block so that
+// a wave's CTAs read different blocks of X at a time.  Per CTA:
+//   warp 0, lane 0   producer: tensor copies of each 64-k block of the tile's
+//                    weight rows (128 x 128 B) and of X (npad x 128 B) into
+//                    a ring of stages, 128-byte swizzled;
+//   warp 1, lane 0   MMA issuer: four 128 x npad x 16 tcgen05.mma per stage
+//                    (A = weights, B = X, both K-major), accumulating in tensor
+//                    memory; tcgen05.commit frees the stage, a last commit
+//                    signals the accumulator complete;
+//   warps 2..5       read the accumulator (one TMEM lane quarter each);
+//   warp 6           allocates and frees the tensor-memory columns;
+//   warps 2..7       meanwhile 1/rms of every token (normalised inputs arrive
+//                    as x * gain in bf16, as in the skinny GEMM).
+// One split: the accumulator (x 1/rms) goes to shared memory and the CTA runs
+// the operation's epilogue (store / residual add with the next norm's sums of
+// squares and x * gain / SwiGLU / RoPE + KV append).  Several splits: each
+// writes its fp32 partial [128][npad]; a second kernel, one CTA per (tile,
+// 32-token block), sums the partials in split order and runs the epilogue,
+// so that the reduction is spread over the whole GPU.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "gemm_dev.cuh"
+#include "kernels.h"
+
+namespace sv {
+
+namespace {
+
+constexpr int kTcM = 128;           // weight rows per tile (MMA M)
+constexpr int kTcKb = 64;           // k elements per stage (one 128-byte swizzle row)
+constexpr int kTcThreads = 256;
+constexpr int kTcABytes = kTcM * kTcKb * 2;   // 16 KB
+constexpr long long kTcWaitLimit = 1LL << 26;
+constexpr int kTcYLd = kTcM + 4;   // floats per token of the staged sums (one-split epilogue)
+
+struct TcArgs {
+  TensorMap128 wmap[3];   // weight segments: boxes of 64 k x 128 rows (gate/up: 64 rows)
+  TensorMap128 xmap;      // X [ntok][k]: boxes of 64 k x npad rows
+  GemmDesc g;
+  int npad, tiles, splits, nkb, stages, tmem_cols;
+  float* partials;        // [tiles * splits][128][npad] (splits > 1)
+  int* err;
+};
+
+// ---- tcgen05 / descriptor helpers ----
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart; start address in 16-byte units (advanced by 2 per 16-k
+// slice inside the 128-byte row).
+SV_DEV uint64_t smem_desc_sw128(const void* p) {
+  const uint64_t a = (smem_u32(p) >> 4) & 0x3FFFu;
+  return a | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = n.
+SV_DEV uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+}
+SV_DEV void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+SV_DEV void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+SV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+SV_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+SV_DEV void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded wait; false (after raising the abort flag) on timeout.
+SV_DEV bool tc_wait(uint64_t* bar, unsigned parity, volatile int* abort) {
+  long long spins = 0;
+  while (!mbar_test(bar, parity)) {
+    if (*abort || ++spins > kTcWaitLimit) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Weight row of tile-local row r of tile `tile`, as (segment, row in segment).
+SV_DEV void tc_tile_src(const GemmDesc& g, int tile, int r, int* seg, int* row) {
+  if (g.epi == kEpiSwiglu) {   // rows 0..63: gate rows, 64..127: the same up rows
+    *seg = r < 64 ? 0 : 1;
+    *row = tile * 64 + (r & 63);
+    return;
+  }
+  int R = tile * kTcM + r, s = 0;
+  while (s < 2 && g.seg_rows[s] > 0 && R >= g.seg_rows[s]) R -= g.seg_rows[s++];
+  *seg = s;
+  *row = R;
+}
+
+// Epilogue of tile `tile` for tokens t0 .. t0 + nt - 1: Y[(t - t0) * ld + r]
+// holds the finished sum of tile row r for token t (scaled by 1/rms for
+// normalised inputs).  Elements are spread over threads tid = 0 .. nth - 1,
+// consecutive threads on consecutive rows of one token (coalesced global
+// accesses), kEb elements per thread in flight where global loads are needed.
+SV_DEV void tc_epilogue(const GemmDesc& g, int tile, const float* Y, int ld, int t0, int nt, int tid, int nth) {
+  constexpr int kEb = 8;
+  if (g.epi == kEpiSwiglu) {
+    const int total = nt * 64;   // (token, ffn index of the tile)
+    for (int e = tid; e < total; e += nth) {
+      const int tl = e / 64, t = t0 + tl, j = e % 64, f = tile * 64 + j;
+      if (f < g.n)
+        ((bf16*)g.out)[(size_t)t * g.ldo + f] =
+            __float2bfloat16_rn(silu(Y[tl * ld + j]) * Y[tl * ld + 64 + j]);
+    }
+  } else if (g.epi == kEpiQkvRope) {
+    const int half = g.hd / 2;
+    const int pos0 = g.spt > 0 ? 0 : *g.pos_base + g.pos_off;
+    const int total = nt * (kTcM / 2);   // (token, rotation pair of the tile)
+    for (int e0 = tid; e0 < total; e0 += kEb * nth) {
+      float cs[kEb], sn[kEb];
+      int pos[kEb];
+#pragma unroll
+      for (int u = 0; u < kEb; ++u) {   // positions and rotations first: kEb loads in flight
+        const int e = e0 + u * nth;
+        cs[u] = 1.f; sn[u] = 0.f; pos[u] = 0;
+        if (e >= total) continue;
+        const int t = t0 + e / (kTcM / 2), pr = e % (kTcM / 2), i = pr % half;
+        pos[u] = tok_pos(g, t, pos0);
+        const int h = (tile * kTcM) / g.hd + pr / half;
+        if (h < g.hq + g.hkv) {
+          cs[u] = __ldg(g.rope_cos + (size_t)pos[u] * half + i);
+          sn[u] = __ldg(g.rope_sin + (size_t)pos[u] * half + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kEb; ++u) {
+        const int e = e0 + u * nth;
+        if (e >= total) continue;
+        const int tl = e / (kTcM / 2), t = t0 + tl, pr = e % (kTcM / 2);
+        const int hl = pr / half, i = pr % half;
+        const int h = (tile * kTcM) / g.hd + hl;          // head of the fused q/k/v rows
+        if (h >= g.hq + 2 * g.hkv) continue;
+        const float x1 = Y[tl * ld + hl * g.hd + i], x2 = Y[tl * ld + hl * g.hd + i + half];
+        const size_t kv0 = tok_kv_row0(g, t);
+        if (h >= g.hq + g.hkv) {   // value head: stored as is
+          bf16* dst = (bf16*)g.vc + (kv0 + (size_t)(h - g.hq - g.hkv) * g.cap + pos[u]) * g.hd;
+          dst[i] = __float2bfloat16_rn(x1);
+          dst[i + half] = __float2bfloat16_rn(x2);
+          continue;
+        }
+        const float y1 = x1 * cs[u] - x2 * sn[u], y2 = x2 * cs[u] + x1 * sn[u];
+        if (h < g.hq) {
+          float* dq = g.q_out + ((size_t)t * g.hq + h) * g.hd;
+          dq[i] = y1;
+          dq[i + half] = y2;
+        } else {
+          bf16* dst = (bf16*)g.kc + (kv0 + (size_t)(h - g.hq) * g.cap + pos[u]) * g.hd;
+          dst[i] = __float2bfloat16_rn(y1);
+          dst[i + half] = __float2bfloat16_rn(y2);
+        }
+      }
+    }
+  } else if (g.epi == kEpiStore) {
+    const int total = nt * kTcM;   // (token, row of the tile)
+    for (int e = tid; e < total; e += nth) {
+      const int tl = e / kTcM, t = t0 + tl, r = e % kTcM, R = tile * kTcM + r;
+      if (R < g.n) ((float*)g.out)[(size_t)t * g.ldo + R] = Y[tl * ld + r];
+    }
+  } else {
+    // residual add; a warp holds 32 consecutive rows of one token, i.e. two
+    // 16-row tiles of the next norm's sums of squares
+    const int total = nt * kTcM;
+    for (int e0 = tid; e0 < total; e0 += kEb * nth) {
+      float ov[kEb];
+#pragma unroll
+      for (int u = 0; u < kEb; ++u) {   // residual loads first: kEb in flight
+        const int e = e0 + u * nth;
+        const int t = t0 + e / kTcM, R = tile * kTcM + e % kTcM;
+        ov[u] = (e < total && R < g.n) ? __ldcg((const float*)g.out + (size_t)t * g.ldo + R) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kEb; ++u) {
+        const int e = e0 + u * nth;
+        if (e >= total) break;   // uniform across the warp (totals are multiples of 32)
+        const int tl = e / kTcM, t = t0 + tl, r = e % kTcM, R = tile * kTcM + r;
+        const bool in = R < g.n;
+        const float v = ov[u] + Y[tl * ld + r];
+        if (in) {
+          ((float*)g.out)[(size_t)t * g.ldo + R] = v;
+          if (g.xg_out) ((bf16*)g.xg_out)[(size_t)t * g.ldo + R] = __float2bfloat16_rn(v * __ldg(g.gain_next + R));
+        }
+        float ss = in ? v * v : 0.f;
+        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (g.ss_out && (tid & 15) == 0 && in) g.ss_out[(size_t)(R / 16) * g.ss_ld + t] = ss;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char tsm[];
+  __shared__ uint64_t full[8], empty[8], done;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ int s_issued, s_consumed;
+  __shared__ float s_inv[kTcMaxTok];
+  __shared__ __align__(16) float s_red[(kTcThreads - 64) * 4];   // 1/rms: sums of k-tile groups
+  const GemmDesc& g = a.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+  const int kb0 = (int)((long long)split * a.nkb / a.splits);
+  const int kb1 = (int)((long long)(split + 1) * a.nkb / a.splits);
+  const int nk = kb1 - kb0;
+  // first k block of the run: rotated by tile, so that the CTAs of a wave
+  // read different blocks of X at a time (fixed by the grid, not by ntok)
+  const int rot = (int)(((long long)tile * 5) % nk);
+  const int npad = a.npad;
+  const unsigned stage_bytes = (unsigned)(kTcABytes + npad * kTcKb * 2);
+  // 1024-aligned stage bases (the swizzle pattern repeats every 1024 bytes)
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm) + 1023) & ~uintptr_t(1023));
+  auto stage_a = [&](int s) { return base + (size_t)s * stage_bytes; };
+  auto stage_b = [&](int s) { return base + (size_t)s * stage_bytes + kTcABytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    s_abort = 0;
+    s_issued = s_consumed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 6) {   // tensor-memory columns for the accumulator (one warp allocates and frees)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(&s_tmem)), "r"(a.tmem_cols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  pdl_trigger();
+  pdl_wait();
+
+  if (g.x_norm == 2 && warp >= 2) {   // 1/rms of every token, while the pipeline fills
+    // threads 64..255: float4 columns of 4 tokens x groups of k tiles
+    const int cols = npad / 4, groups = (kTcThreads - 64) / cols, u = threadIdx.x - 64;
+    const int col = u % cols, grp = u / cols, nt = g.k / 16;
+    float* red = reinterpret_cast<float*>(s_red);   // [groups][npad]
+    if (grp < groups) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = grp; i < nt; i += groups) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(g.ss_in + (size_t)i * g.ss_ld) + col);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      reinterpret_cast<float4*>(red + grp * npad)[col] = acc;
+    }
+    named_sync(1, kTcThreads - 64);
+    for (int t = u; t < npad; t += kTcThreads - 64) {
+      float sum = 0.f;
+      for (int q = 0; q < groups; ++q) sum += red[q * npad + t];
+      s_inv[t] = 1.0f / sqrtf(sum / (float)g.k + g.eps);
+    }
+    named_sync(1, kTcThreads - 64);
+  }
+  if (warp == 0 && lane == 0) {
+    // ---- producer ----
+    const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % a.stages;
+      if (i >= a.stages && !tc_wait(&empty[s], (unsigned)((i / a.stages - 1) & 1), &s_abort)) break;
+      const int kb = kb0 + (i + rot) % nk;
+      mbar_arrive_expect_tx(&full[s], stage_bytes);
+      if (g.epi == kEpiSwiglu) {
+        tma_load_2d_hint(stage_a(s), &a.wmap[0], kb * kTcKb, tile * 64, &full[s], pol_w);
+        tma_load_2d_hint(stage_a(s) + kTcABytes / 2, &a.wmap[1], kb * kTcKb, tile * 64, &full[s], pol_w);
+      } else {
+        int seg, row;
+        tc_tile_src(g, tile, 0, &seg, &row);
+        tma_load_2d_hint(stage_a(s), &a.wmap[seg], kb * kTcKb, row, &full[s], pol_w);
+      }
+      tma_load_2d_hint(stage_b(s), &a.xmap, kb * kTcKb, 0, &full[s], pol_x);
+      s_issued = i + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    const uint32_t idesc = idesc_bf16(npad);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % a.stages;
+      if (!tc_wait(&full[s], (unsigned)((i / a.stages) & 1), &s_abort)) break;
+      s_consumed = i + 1;
+      tc_fence_after();
+      const uint64_t ad = smem_desc_sw128(stage_a(s)), bd = smem_desc_sw128(stage_b(s));
+#pragma unroll
+      for (int kk = 0; kk < kTcKb / 16; ++kk)   // 16-k slices: +32 bytes = +2 in the start field
+        tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(&empty[s]);
+    }
+    tc_commit(&done);   // completes when every MMA issued above has
+  } else if (warp >= 2 && warp <= 5) {
+    // ---- accumulator -> partial [128][npad] ----
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;                  // tile row
+    const bool ok = tc_wait(&done, 0u, &s_abort);
+    tc_fence_after();
+    if (ok && a.splits > 1) {   // partial [128][npad] for the reduction kernel
+      float* part = a.partials + ((size_t)blockIdx.x * kTcM + r) * npad;
+      for (int c = 0; c < npad; c += 16) {
+        float v[16];
+        tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(part + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+    } else if (ok) {            // the whole sum: Y[t][r] (x 1/rms) in the idle stage ring
+      float* Y = reinterpret_cast<float*>(base);
+      for (int c = 0; c < npad; c += 16) {
+        float v[16];
+        tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Y[(c + i) * kTcYLd + r] = g.x_norm == 2 ? v[i] * s_inv[c + i] : v[i];
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (s_abort && threadIdx.x == 0) {
+    // a wait gave up: let the copies issued but not consumed land (bounded),
+    // and the MMAs issued finish, before the space and the columns go
+    atomicExch(a.err, 1);
+    for (int i = s_consumed; i < s_issued; ++i) {
+      long long spins = 0;
+      while (!mbar_test(&full[i % a.stages], (unsigned)((i / a.stages) & 1)) && ++spins < (1LL << 20)) {
+      }
+    }
+    long long spins = 0;
+    while (!mbar_test(&done, 0u) && ++spins < (1LL << 20)) {
+    }
+  }
+  __syncthreads();
+  if (warp == 6) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+  }
+  if (s_abort) return;
+
+  if (a.splits == 1) tc_epilogue(g, tile, reinterpret_cast<const float*>(base), kTcYLd, 0, g.ntok, threadIdx.x,
+                                 kTcThreads);
+}
+
+// Reduction and epilogue of a split GEMM: one CTA per (row tile, block of
+// kTcRedTok tokens) sums the splits' partials in split order (x 1/rms) and
+// runs the epilogue for those tokens.
+constexpr int kTcRedTok = 32;
+constexpr int kTcRedLd = kTcM + 1;   // odd stride: conflict-free transposed writes
+__global__ void __launch_bounds__(kTcThreads) tc_reduce_kernel(const __grid_constant__ TcArgs a) {
+  __shared__ float Y[kTcRedTok * kTcRedLd];
+  __shared__ float s_inv[kTcRedTok];
+  const GemmDesc& g = a.g;
+  const int tile = blockIdx.x, t0 = blockIdx.y * kTcRedTok;
+  const int nt = min(kTcRedTok, g.ntok - t0), npad = a.npad;
+  pdl_trigger();
+  pdl_wait();
+  if (g.x_norm == 2) {   // 8 threads per token, k tiles strided, in-group shuffle sum
+    const int tl = threadIdx.x / 8, sub = threadIdx.x % 8, nkt = g.k / 16;
+    float sum = 0.f;
+    if (tl < nt)
+      for (int i = sub; i < nkt; i += 8) sum += __ldcg(g.ss_in + (size_t)i * g.ss_ld + t0 + tl);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    if (sub == 0 && tl < kTcRedTok) s_inv[tl] = 1.0f / sqrtf(sum / (float)g.k + g.eps);
+  }
+  __syncthreads();
+  const float* P = a.partials + (size_t)tile * a.splits * kTcM * npad + t0;
+  for (int e = threadIdx.x; e < kTcM * kTcRedTok; e += kTcThreads) {
+    const int r = e / kTcRedTok, tl = e % kTcRedTok;
+    if (tl >= nt) continue;
+    float acc = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp) acc += __ldcg(P + ((size_t)sp * kTcM + r) * npad + tl);
+    Y[tl * kTcRedLd + r] = g.x_norm == 2 ? acc * s_inv[tl] : acc;
+  }
+  __syncthreads();
+  tc_epilogue(g, tile, Y, kTcRedLd, t0, nt, threadIdx.x, kTcThreads);
+}
+
+}  // namespace
+
+// ---- host side ----
+static PFN_cuTensorMapEncodeTiled_v12000 tc_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][k], row stride ld elements, boxes of 64 k x
+// box_rows with the 128-byte swizzle; rows past the end read as zero.
+static bool tc_encode_rows(TensorMap128& m, const void* base, int k, long long rows, long long ld, int box_rows) {
+  static_assert(sizeof(CUtensorMap) == sizeof(TensorMap128), "tensor map size");
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tc_encoder();
+  if (!enc || !base || rows < 1 || box_rows < 1 || box_rows > 256 || (reinterpret_cast<uintptr_t>(base) & 15u) ||
+      (ld * 2) % 16 != 0)
+    return false;
+  cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTcKb, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(reinterpret_cast<CUtensorMap*>(&m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t tc_gemm_partial_floats(int num_sms, int max_n) {
+  // every work unit of a split GEMM writes one [128][npad] partial: at most
+  // two waves of num_sms units (one-split GEMMs write none)
+  (void)max_n;
+  return 2 * (size_t)num_sms * kTcM * kTcMaxTok;
+}
+
+bool tc_gemm_supported(const GemmDesc& g) {
+  if (g.ntok <= kGemmMaxTok || g.ntok > kTcMaxTok || g.k % kTcKb != 0 || g.ldx % 8 != 0) return false;
+  if (g.x_norm == 1) return false;   // normalised inputs arrive as x * gain in bf16
+  if (g.x_norm == 2 && ((reinterpret_cast<uintptr_t>(g.ss_in) & 15u) || g.ss_ld % 4 != 0 || g.ss_ld < kTcMaxTok))
+    return false;                    // 1/rms reads float4 columns of up to kTcMaxTok tokens
+  if (g.epi == kEpiSwiglu) return g.n % 64 == 0;
+  for (int s = 0; s < 3; ++s)
+    if (g.seg_rows[s] > 0 && g.seg_rows[s] % kTcM != 0 && !(s == 0 && g.seg_rows[1] == 0)) return false;
+  if (g.epi == kEpiQkvRope) return g.hd % 2 == 0 && kTcM % g.hd == 0 && g.n % kTcM == 0;
+  return true;
+}
+
+cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num_sms, long long max_units,
+                           cudaStream_t st) {
+  if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.g = g;
+  a.npad = (g.ntok + 15) / 16 * 16;
+  a.nkb = g.k / kTcKb;
+  a.tiles = g.epi == kEpiSwiglu ? g.n / 64 : (g.n + kTcM - 1) / kTcM;
+  // splits: the fullest last wave of num_sms CTAs (one per SM), fewest
+  // splits on ties, at least two k blocks per split, within the partials
+  a.splits = 1;
+  double best = 0.0;
+  for (int sp = 1; sp <= std::max(1, std::min(16, a.nkb / 2)); ++sp) {
+    const long long units = (long long)a.tiles * sp;
+    if (sp > 1 && units > max_units) break;
+    const double eff = (double)units / ((double)num_sms * (double)((units + num_sms - 1) / num_sms));
+    if (eff > best + 1e-3) {
+      best = eff;
+      a.splits = sp;
+    }
+  }
+  const int stage_bytes = kTcABytes + a.npad * kTcKb * 2;
+  a.stages = std::min(8, (kTcSmemBytes - 1024) / stage_bytes);
+  int cols = 32;
+  while (cols < a.npad) cols *= 2;
+  a.tmem_cols = cols;
+  if (a.splits > 1 && (long long)a.tiles * a.splits > max_units) return cudaErrorInvalidValue;
+  a.partials = partials;
+  a.err = err;
+  const int box_rows = g.epi == kEpiSwiglu ? 64 : kTcM;
+  for (int s = 0; s < 3; ++s) {
+    if (!g.w[s]) continue;
+    const long long rows = g.epi == kEpiSwiglu ? g.n : (g.seg_rows[s] > 0 ? g.seg_rows[s] : g.n);
+    if (!tc_encode_rows(a.wmap[s], g.w[s], g.k, rows, g.k, box_rows)) return cudaErrorInvalidValue;
+  }
+  if (!tc_encode_rows(a.xmap, g.x, g.k, g.ntok, g.ldx, a.npad)) return cudaErrorInvalidValue;
+  cudaError_t e = launch_k(tc_gemm_kernel, dim3(a.tiles * a.splits), dim3(kTcThreads), (size_t)kTcSmemBytes, st, a);
+  if (e != cudaSuccess || a.splits == 1) return e;
+  return launch_k(tc_reduce_kernel, dim3(a.tiles, (g.ntok + kTcRedTok - 1) / kTcRedTok), dim3(kTcThreads), 0, st, a);
+}
+
+cudaError_t configure_tc_gemm() {
+  return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+}
+
+}  // namespace sv

@@ -1,7 +1,7 @@
 """Batched contexts (several sequences per step) through the C ABI.
 
 A batched context runs every forward once over all sequences' tokens (the
-per-operation path, groups of at most 64 tokens), samples and accepts one row
+per-operation path, groups of at most 256 tokens), samples and accepts one row
 per sequence, and commits each sequence by its own count (ragged
 acceptance).  The pages describe one sequence; a batch is that algorithm per
 sequence, with sequence b's Philox draws at row word b.
@@ -14,6 +14,10 @@ sequence, with sequence b's Philox draws at row word b.
 * Teacher-forced parity per sequence against the fp64 oracle: stage (i)
   logits within the bf16 tolerance, stage (ii) the oracle's acceptance with
   row word b on the GPU's logits reproduces sequence b's emitted tokens.
+* Passes of more than 64 tokens (16 sequences x 5 positions) run their GEMMs
+  on the tensor-memory (tcgen05) GEMM; the teacher-forced parity above
+  covers every GEMM kind on that path (q/k/v + RoPE + KV append, residual
+  adds, gate/up + SwiGLU, LM head).
 * Sequences whose contexts cross the first 1024-key split (token-group
   attention items, split merges), after a synthetic prefill, step with valid
   counts and ragged lengths; spec_ar_step and spec_profile run on batches.
@@ -74,9 +78,12 @@ def test_batch_sequences_match_single(temp):
         assert len(ctxs[b]) == 20 + sum(len(got[s][0][b]) for s in range(steps))
 
 
+@pytest.mark.parametrize("nseq,k", [(3, 3), (16, 4)], ids=["3x4tok", "16x5tok-tensor-memory-gemm"])
 @pytest.mark.parametrize("temp", [0.0, 1.0])
-def test_batch_teacher_forced(temp):
-    k, max_ctx, nseq, steps, seed = 3, 128, 3, 5, 7
+def test_batch_teacher_forced(temp, nseq, k):
+    # 16 sequences x 5 positions = 80 tokens per verify pass: the GEMMs run on
+    # the tensor-memory (tcgen05) GEMM
+    max_ctx, steps, seed = 128, 5, 7
     w, dshape, dw = _pair(seed=3)
     prompts = workloads.make_prompt(SHAPE.vocab, 12, seed=9, batch=nseq).tolist()
     dec = _dec(w, dshape, dw, k, max_ctx, temp, nseq, seed=seed)
@@ -115,8 +122,11 @@ def test_batch_teacher_forced(temp):
     dec.close()
 
 
-def test_batch_long_context_synthetic():
-    k, nseq, L = 5, 4, 1100   # last verify position past 1024: token-group items, split merges
+@pytest.mark.parametrize("nseq", [4, 16])
+def test_batch_long_context_synthetic(nseq):
+    # last verify position past 1024: token-group items, split merges; 16
+    # sequences: 96-token verify passes on the tensor-memory GEMM
+    k, L = 5, 1100
     w, dshape, dw = _pair(seed=4)
     dec = _dec(w, dshape, dw, k, 1200, 1.0, nseq)
     dec.prefill_synthetic(L, seed=11)

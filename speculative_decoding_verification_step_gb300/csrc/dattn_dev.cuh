@@ -44,7 +44,7 @@ constexpr int kDSplitKeys = 1024;
 constexpr int kDWarps = 8;
 constexpr int kDRows = 8;                          // rows per item (MMA n)
 
-template <int HD>
+template <int HD, int NT = 1>
 struct DAttnSmem {
   // per warp: kDepth stages of a 16-key K tile and V tile, each tile written
   // by 2-D tensor copies of 16 keys x kBoxCols dims with the hardware 128-byte
@@ -65,10 +65,11 @@ struct DAttnSmem {
   static constexpr int kVBoxCols = kVDims < 64 ? kVDims : 64;
   static constexpr int kVBoxes = kVDims / kVBoxCols;
   static constexpr int kStageElems = kTileElems + kVTileElems;   // K tile, then V tile
-  static constexpr size_t kWarpRaw = (size_t)kDepth * kStageElems * 2 + kDRows * kDStepKeys * 2;
+  // (NT probability tiles of [8 rows][16 keys]: wide items, NT x 8 rows)
+  static constexpr size_t kWarpRaw = (size_t)kDepth * kStageElems * 2 + NT * kDRows * kDStepKeys * 2;
   static constexpr size_t kWarpBytes = (kWarpRaw + 1023) / 1024 * 1024;
-  // merge area: m, l [8 warps][8 rows], o [8 warps][8 rows][kVDims] (fp32)
-  static constexpr size_t kMergeBytes = (size_t)kDWarps * kDRows * (2 + kVDims) * 4;
+  // merge area: m, l [8 warps][8 NT rows], o [8 warps][8 NT rows][kVDims] (fp32)
+  static constexpr size_t kMergeBytes = (size_t)kDWarps * NT * kDRows * (2 + kVDims) * 4;
   static constexpr size_t kBytes = kDWarps * kWarpBytes > kMergeBytes ? kDWarps * kWarpBytes : kMergeBytes;
   // element offset of logical 16-byte chunk c of key row r in a tile: box
   // c / 8 (64 dims), row r, chunk (c mod 8) XOR (r mod 8) -- the tensor
@@ -477,6 +478,292 @@ SV_DEV void dattn_item(const AttnDesc& a, int it, unsigned char* sm, int* s_last
     dattn_item_rows<HD, true, true>(a, it, sm, s_last, bars, dpar, stamp);
   else
     dattn_item_rows<HD, false, true>(a, it, sm, s_last, bars, dpar, stamp);
+}
+
+// ---- wide items (batched passes of the per-operation kernel) ----
+// Item = (sequence, group of tpi = 8 NT / G of its tokens, KV head, 1024-key
+// split, V part) with NT n-tiles of 8 rows: all G query heads of tpi tokens
+// (G <= 8), so one K/V tile in shared memory serves 8 NT rows -- each step's
+// K fragments feed NT score MMAs and each V fragment NT P.V MMAs.  A row's
+// arithmetic is step for step that of the one-tile items (the same MMAs,
+// softmax updates and merges on its own column), so its bits do not depend
+// on the item width.
+__host__ __device__ inline int dattn_wide_tpi(int nt, int hq, int hkv) { return nt * kDRows / (hq / hkv); }
+__host__ __device__ inline int dattn_items_wide(int nt, int ntok, int spt, int hq, int hkv, int cap, int hd) {
+  const int S = spt > 0 ? spt : ntok, tpi = dattn_wide_tpi(nt, hq, hkv);
+  return dattn_splits(cap) * (ntok / S) * ((S + tpi - 1) / tpi) * hkv * dattn_vparts(hd);
+}
+
+template <int HD, int NT>
+SV_DEV void dattn_item_wide(const AttnDesc& a, int it, unsigned char* sm, int* s_last, uint64_t* bars,
+                            unsigned& dpar) {
+  using L = DAttnSmem<HD, NT>;
+  constexpr int VD = L::kVDims;                       // output dims of this item
+  constexpr int R = NT * kDRows;                      // rows of the item
+  const int vp = it % L::kVParts;
+  const int G = a.hq / a.hkv;                         // heads per KV head (<= 8): hpi
+  const int S = a.spt > 0 ? a.spt : a.ntok;           // tokens per sequence
+  const int tpi = R / G, gps = (S + tpi - 1) / tpi;   // tokens per item, groups per sequence
+  const DItem d = dattn_item_of(a, it / L::kVParts, 1, (a.ntok / S) * gps);
+  const int b = d.tg / gps, j0 = (d.tg % gps) * tpi;
+  const int t0 = b * S + j0, ntk = min(tpi, S - j0);
+  const int pbase = a.pos_base[(size_t)b * a.pos_ld] + a.pos_off - b * S;
+  const int nrows = ntk * G;
+  const int pmax = pbase + t0 + ntk - 1;
+  const int k0 = d.split * kDSplitKeys;
+  if (k0 > pmax) return;                              // split entirely in the future
+  const int last = min(pmax, k0 + kDSplitKeys - 1);
+  const int nsplit = pmax / kDSplitKeys + 1;          // splits of the token group
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
+  const int h0 = d.kvh * G;
+  const int row0 = ((a.seq0 + b) * a.hkv + d.kvh) * a.cap;
+  uint64_t* wbar = bars + warp * kDMaxDepth;
+  auto row_tok = [&](int r) { return t0 + r / G; };
+  auto row_head = [&](int r) { return h0 + r % G; };
+
+  constexpr int GD = HD < 64 ? HD : 64;
+  constexpr int NG = HD / GD, TW = GD / 8, NM = GD / 16;
+  uint32_t qf[NT][NG][TW];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int r = nt * kDRows + gi;
+    const bool ok = r < nrows;
+    const float* qp = a.q + ((size_t)(ok ? row_tok(r) : t0) * a.hq + (ok ? row_head(r) : h0)) * HD + ci * (GD / 4);
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+#pragma unroll
+      for (int e = 0; e < TW / 2; ++e) {
+        const float4 v = ok ? __ldcg(reinterpret_cast<const float4*>(qp + j * GD + 4 * e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qf[nt][j][2 * e] = pack_bf16(v.x, v.y);
+        qf[nt][j][2 * e + 1] = pack_bf16(v.z, v.w);
+      }
+    }
+  }
+
+  constexpr int D = L::kDepth;
+  bf16* wb = reinterpret_cast<bf16*>(sm + (size_t)warp * L::kWarpBytes);
+  bf16* ps = wb + D * L::kStageElems;                 // [NT][8 rows][16 keys]
+  const int s_begin = k0 / kDStepKeys, s_end = last / kDStepKeys;
+  const int first = s_begin + warp;
+  const int nst = first <= s_end ? (s_end - first) / kDWarps + 1 : 0;
+  float m_r[NT][2], l_r[NT][2], o[VD / 16][NT][4];
+  int p0[NT], p1[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_r[nt][0] = m_r[nt][1] = neg_inf();
+    l_r[nt][0] = l_r[nt][1] = 0.f;
+    const int ra = nt * kDRows + 2 * ci;
+    p0[nt] = ra < nrows ? pbase + row_tok(ra) : -1;
+    p1[nt] = ra + 1 < nrows ? pbase + row_tok(ra + 1) : -1;
+#pragma unroll
+    for (int mt = 0; mt < VD / 16; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+  }
+  if (lane == 0)
+    for (int j = 0; j < D && j < nst; ++j)
+      dattn_fetch<HD>(a, row0, first + kDWarps * j, vp, wb + j * L::kStageElems,
+                      wb + j * L::kStageElems + L::kTileElems, &wbar[j]);
+  int koff_lo[NG][TW / 4], koff_hi[NG][TW / 4], voff[VD / 16];
+#pragma unroll
+  for (int jg = 0; jg < NG; ++jg)
+#pragma unroll
+    for (int e = 0; e < TW / 4; ++e) {
+      const int c = jg * (GD / 8) + ci * (GD / 32) + e;
+      koff_lo[jg][e] = L::at(gi, c);
+      koff_hi[jg][e] = L::at(gi + 8, c);
+    }
+  {
+    const int lrow = (lane & 7) + ((lane >> 4) << 3);
+    const int lchk = (lane >> 3) & 1;
+#pragma unroll
+    for (int mt = 0; mt < VD / 16; ++mt) voff[mt] = L::at_v(lrow, 2 * mt + lchk);
+  }
+  bool live = true;
+  for (int j = 0; j < nst; ++j) {
+    const int s = first + kDWarps * j;
+    const int buf = j % D;
+    const bf16* kt = wb + buf * L::kStageElems;
+    const bf16* vt = kt + L::kTileElems;
+    live = __all_sync(0xffffffffu, live && dattn_wait(a, &wbar[buf], (dpar >> buf) & 1u));
+    dpar ^= 1u << buf;
+    if (!live) continue;
+    float sc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int jg = 0; jg < NG; ++jg) {
+      uint32_t lo[TW], hi[TW];
+#pragma unroll
+      for (int e = 0; e < TW / 4; ++e) {
+        const uint4 x = *reinterpret_cast<const uint4*>(kt + koff_lo[jg][e]);
+        const uint4 y = *reinterpret_cast<const uint4*>(kt + koff_hi[jg][e]);
+        lo[4 * e] = x.x; lo[4 * e + 1] = x.y; lo[4 * e + 2] = x.z; lo[4 * e + 3] = x.w;
+        hi[4 * e] = y.x; hi[4 * e + 1] = y.y; hi[4 * e + 2] = y.z; hi[4 * e + 3] = y.w;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < NM; ++i)
+          mma_bf16_16816(sc[nt], lo[2 * i], hi[2 * i], lo[2 * i + 1], hi[2 * i + 1], qf[nt][jg][2 * i],
+                         qf[nt][jg][2 * i + 1]);
+    }
+    const int key_lo = s * kDStepKeys + gi, key_hi = key_lo + 8;
+    float scl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float v00 = key_lo <= p0[nt] ? sc[nt][0] * a.scale : neg_inf();
+      const float v01 = key_lo <= p1[nt] ? sc[nt][1] * a.scale : neg_inf();
+      const float v10 = key_hi <= p0[nt] ? sc[nt][2] * a.scale : neg_inf();
+      const float v11 = key_hi <= p1[nt] ? sc[nt][3] * a.scale : neg_inf();
+      float mx0 = fmaxf(v00, v10), mx1 = fmaxf(v01, v11);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m_r[nt][0], mx0), mn1 = fmaxf(m_r[nt][1], mx1);
+      const float sc0 = mn0 == neg_inf() ? 0.f : expf(m_r[nt][0] - mn0);
+      const float sc1 = mn1 == neg_inf() ? 0.f : expf(m_r[nt][1] - mn1);
+      const float p00 = v00 == neg_inf() ? 0.f : expf(v00 - mn0);
+      const float p10 = v10 == neg_inf() ? 0.f : expf(v10 - mn0);
+      const float p01 = v01 == neg_inf() ? 0.f : expf(v01 - mn1);
+      const float p11 = v11 == neg_inf() ? 0.f : expf(v11 - mn1);
+      float ls0 = p00 + p10, ls1 = p01 + p11;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
+        ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
+      }
+      l_r[nt][0] = l_r[nt][0] * sc0 + ls0;
+      m_r[nt][0] = mn0;
+      l_r[nt][1] = l_r[nt][1] * sc1 + ls1;
+      m_r[nt][1] = mn1;
+      scl[nt][0] = sc0;
+      scl[nt][1] = sc1;
+      bf16* pt = ps + nt * kDRows * kDStepKeys;
+      pt[(2 * ci) * kDStepKeys + gi] = __float2bfloat16_rn(p00);
+      pt[(2 * ci + 1) * kDStepKeys + gi] = __float2bfloat16_rn(p01);
+      pt[(2 * ci) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p10);
+      pt[(2 * ci + 1) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p11);
+    }
+    __syncwarp();
+    uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const bf16* pt = ps + nt * kDRows * kDStepKeys;
+      pb0[nt] = *reinterpret_cast<const uint32_t*>(pt + gi * kDStepKeys + 2 * ci);
+      pb1[nt] = *reinterpret_cast<const uint32_t*>(pt + gi * kDStepKeys + 2 * ci + 8);
+    }
+#pragma unroll
+    for (int mt = 0; mt < VD / 16; ++mt) {
+      uint32_t va[4];
+      ldmatrix_x4_trans(va, vt + voff[mt]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[mt][nt][0] *= scl[nt][0];
+        o[mt][nt][1] *= scl[nt][1];
+        o[mt][nt][2] *= scl[nt][0];
+        o[mt][nt][3] *= scl[nt][1];
+        mma_bf16_16816(o[mt][nt], va[0], va[1], va[2], va[3], pb0[nt], pb1[nt]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && j + D < nst) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      dattn_fetch<HD>(a, row0, s + kDWarps * D, vp, wb + buf * L::kStageElems,
+                      wb + buf * L::kStageElems + L::kTileElems, &wbar[buf]);
+    }
+  }
+  if (!live && lane == 0)
+    for (int j = nst - D > 0 ? nst - D : 0; j < nst; ++j) {
+      long long spins = 0;
+      while (!mbar_test(&wbar[j % D], ((dpar >> (j % D)) & 1u) ^ 1u) && ++spins < (1LL << 16)) {
+      }
+    }
+  __syncwarp();
+
+  // ---- merge the eight warps (warp order) ----
+  named_sync(1, kDWarps * 32);
+  float* mm = reinterpret_cast<float*>(sm);          // [8 warps][R rows]
+  float* ll = mm + kDWarps * R;                      // [8 warps][R rows]
+  float* oo = ll + kDWarps * R;                      // [8 warps][R rows][VD]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int ra = nt * kDRows + 2 * ci;
+    if (gi == 0) {
+      mm[warp * R + ra] = m_r[nt][0];
+      mm[warp * R + ra + 1] = m_r[nt][1];
+      ll[warp * R + ra] = l_r[nt][0];
+      ll[warp * R + ra + 1] = l_r[nt][1];
+    }
+    float* ow = oo + (size_t)warp * R * VD;
+#pragma unroll
+    for (int mt = 0; mt < VD / 16; ++mt) {
+      ow[ra * VD + mt * 16 + gi] = o[mt][nt][0];
+      ow[(ra + 1) * VD + mt * 16 + gi] = o[mt][nt][1];
+      ow[ra * VD + mt * 16 + gi + 8] = o[mt][nt][2];
+      ow[(ra + 1) * VD + mt * 16 + gi + 8] = o[mt][nt][3];
+    }
+  }
+  named_sync(1, kDWarps * 32);
+  const int tid = threadIdx.x;
+  const int dv0 = vp * VD;
+  const int ns = dattn_splits(a.cap);
+  for (int e = tid; e < nrows * VD; e += kDWarps * 32) {
+    const int r = e / VD, dm = e % VD;
+    const int t = row_tok(r);
+    if (pbase + t < k0) continue;                    // no key of the row in this split
+    float M = neg_inf();
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, mm[w * R + r]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) {
+      const float mw = mm[w * R + r];
+      const float f = mw == neg_inf() ? 0.f : expf(mw - M);
+      num = fmaf(f, oo[((size_t)w * R + r) * VD + dm], num);
+      den = fmaf(f, ll[w * R + r], den);
+    }
+    const int h = row_head(r);
+    if (nsplit == 1) {
+      ((bf16*)a.out)[(size_t)t * a.hq * HD + (size_t)h * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
+    } else {
+      float* pp = a.partials + (((size_t)t * a.hq + h) * ns + d.split) * (HD + 4);
+      pp[dv0 + dm] = num;
+      if (dm == 0) {
+        pp[HD + 2 * vp] = M;
+        pp[HD + 2 * vp + 1] = den;
+      }
+    }
+  }
+  if (nsplit == 1) {
+    named_sync(1, kDWarps * 32);
+    return;
+  }
+  int* ticket = a.tickets + ((size_t)d.tg * a.hkv + d.kvh) * L::kVParts + vp;
+  named_sync(1, kDWarps * 32);
+  if (tid == 0)
+    *s_last = (atom_add_acq_rel_gpu(reinterpret_cast<unsigned*>(ticket), 1u) == (unsigned)nsplit - 1);
+  named_sync(1, kDWarps * 32);
+  if (!*s_last) return;
+  for (int e = tid; e < nrows * VD; e += kDWarps * 32) {
+    const int r = e / VD, dm = e % VD;
+    const int t = row_tok(r);
+    const int nr = (pbase + t) / kDSplitKeys + 1;
+    const int h = row_head(r);
+    const float* base = a.partials + ((size_t)t * a.hq + h) * ns * (HD + 4);
+    float M = neg_inf();
+    for (int sp = 0; sp < nr; ++sp) M = fmaxf(M, __ldcg(base + (size_t)sp * (HD + 4) + HD + 2 * vp));
+    float num = 0.f, den = 0.f;
+    for (int sp = 0; sp < nr; ++sp) {
+      const float* pp = base + (size_t)sp * (HD + 4);
+      const float f = expf(__ldcg(pp + HD + 2 * vp) - M);
+      num = fmaf(f, __ldcg(pp + dv0 + dm), num);
+      den = fmaf(f, __ldcg(pp + HD + 2 * vp + 1), den);
+    }
+    ((bf16*)a.out)[(size_t)t * a.hq * HD + (size_t)h * HD + dv0 + dm] = __float2bfloat16_rn(num / den);
+  }
+  named_sync(1, kDWarps * 32);
+  if (tid == 0) *ticket = 0;
 }
 
 }  // namespace sv

@@ -335,6 +335,11 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     // batched passes of several tokens per sequence with one-token items for
     // at least two waves: token-group items (the same bits, half the walks)
     a.group = sq.spt >= 2 && (long long)ntok * hkv * (hd >= 64 ? 2 : 1) >= 2LL * c->num_sms;
+    // batched passes of 3+ tokens per sequence with at least one wave of
+    // (sequence, KV head, V part) items: wide items, all G heads of 2 x tiles
+    // tokens per K/V walk (the same bits; K/V read up to 3x less often)
+    if (sq.spt >= 3 && hq / hkv <= 8 && (long long)(ntok / sq.spt) * hkv * (hd >= 64 ? 2 : 1) >= c->num_sms)
+      a.wide = sq.spt <= 4 ? 2 : 3;
     a.partials = c->attn_part; a.tickets = c->attn_tick; a.out = c->attn;
     a.ntok = ntok; a.hq = hq; a.hkv = hkv; a.hd = hd; a.cap = c->cap;
     a.max_chunks = c->max_chunks; a.dtype = dt;

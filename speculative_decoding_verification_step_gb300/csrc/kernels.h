@@ -145,6 +145,8 @@ struct AttnDesc {
   int spt, pos_ld;
   int seq0;                // bf16 path: sequence b of the pass is cache sequence seq0 + b
   int group;               // bf16 per-operation path: 1 = token-group items at any position
+  int wide;                // bf16 per-operation path: 2 or 3 = wide items of that many 8-row
+                           // tiles (all heads of several tokens of one sequence; G <= 8)
   float* partials;         // [ntok*hq][max_chunks][hd+2]
   int* tickets;            // [hkv][row tiles], zero before and after
   void* out;               // [ntok][hq*hd] model dtype

@@ -148,10 +148,39 @@ __global__ void __launch_bounds__(kDWarps * 32) dattn_kernel(const __grid_consta
   dattn_item<HD>(a, blockIdx.x, dsm_attn, &s_last, bars, dpar);
 }
 
+// Wide items (batched passes): NT 8-row tiles per item.
+template <int HD, int NT>
+__global__ void __launch_bounds__(kDWarps * 32) dattn_wide_kernel(const __grid_constant__ AttnDesc a) {
+  extern __shared__ __align__(1024) unsigned char dsm_attn[];
+  __shared__ int s_last;
+  __shared__ uint64_t bars[kDWarps * kDMaxDepth];
+  dattn_init_bars(bars);
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  unsigned dpar = 0;
+  dattn_item_wide<HD, NT>(a, blockIdx.x, dsm_attn, &s_last, bars, dpar);
+}
+
 template <int HD>
 static cudaError_t configure_dattn() {
-  return cudaFuncSetAttribute(dattn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)DAttnSmem<HD>::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(dattn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)DAttnSmem<HD>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dattn_wide_kernel<HD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DAttnSmem<HD, 2>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dattn_wide_kernel<HD, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DAttnSmem<HD, 3>::kBytes);
+  return e;
+}
+
+template <int HD>
+static cudaError_t launch_dattn_wide(const AttnDesc& a, cudaStream_t st) {
+  const int items = dattn_items_wide(a.wide, a.ntok, a.spt, a.hq, a.hkv, a.cap, a.hd);
+  if (a.wide == 2)
+    return launch_k(dattn_wide_kernel<HD, 2>, dim3(items), dim3(kDWarps * 32), DAttnSmem<HD, 2>::kBytes, st, a);
+  return launch_k(dattn_wide_kernel<HD, 3>, dim3(items), dim3(kDWarps * 32), DAttnSmem<HD, 3>::kBytes, st, a);
 }
 
 int dattn_v_box_cols(int hd) { return dattn_vbox_cols(hd); }
@@ -161,6 +190,13 @@ int dattn_tickets(int max_tok, int hq, int hkv) { return max_tok * hkv * dattn_h
 cudaError_t launch_dattn(const AttnDesc& a, cudaStream_t st) {
   if (a.dtype != 1 || a.hq % a.hkv != 0 || !a.tmk || !a.tmv) return cudaErrorInvalidValue;
   if (a.spt > 0 && a.ntok % a.spt != 0) return cudaErrorInvalidValue;
+  if (a.wide == 2 || a.wide == 3) {
+    if (a.hq / a.hkv > kDRows) return cudaErrorInvalidValue;   // one head group per KV head
+    if (a.hd == 32) return launch_dattn_wide<32>(a, st);
+    if (a.hd == 64) return launch_dattn_wide<64>(a, st);
+    if (a.hd == 128) return launch_dattn_wide<128>(a, st);
+    return cudaErrorInvalidValue;
+  }
   const int items = dattn_items(a.ntok, a.hq, a.hkv, a.cap, a.hd);
   if (a.hd == 32) return launch_k(dattn_kernel<32>, dim3(items), dim3(kDWarps * 32), DAttnSmem<32>::kBytes, st, a);
   if (a.hd == 64) return launch_k(dattn_kernel<64>, dim3(items), dim3(kDWarps * 32), DAttnSmem<64>::kBytes, st, a);

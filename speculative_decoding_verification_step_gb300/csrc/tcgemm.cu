@@ -398,12 +398,29 @@ __global__ void __launch_bounds__(kTcThreads) tc_reduce_kernel(const __grid_cons
   }
   __syncthreads();
   const float* P = a.partials + (size_t)tile * a.splits * kTcM * npad + t0;
-  for (int e = threadIdx.x; e < kTcM * kTcRedTok; e += kTcThreads) {
-    const int r = e / kTcRedTok, tl = e % kTcRedTok;
-    if (tl >= nt) continue;
-    float acc = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) acc += __ldcg(P + ((size_t)sp * kTcM + r) * npad + tl);
-    Y[tl * kTcRedLd + r] = g.x_norm == 2 ? acc * s_inv[tl] : acc;
+  // 4 elements per thread at a time, their partial loads in flight together;
+  // each element's splits are added in split order
+  constexpr int kRb = 4;
+  for (int e0 = threadIdx.x; e0 < kTcM * kTcRedTok; e0 += kRb * kTcThreads) {
+    float acc[kRb];
+#pragma unroll
+    for (int u = 0; u < kRb; ++u) acc[u] = 0.f;
+#pragma unroll 2
+    for (int sp = 0; sp < a.splits; ++sp) {
+      float v[kRb];
+#pragma unroll
+      for (int u = 0; u < kRb; ++u) {
+        const int e = e0 + u * kTcThreads, r = e / kTcRedTok, tl = e % kTcRedTok;
+        v[u] = tl < nt ? __ldcg(P + ((size_t)sp * kTcM + r) * npad + tl) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kRb; ++u) acc[u] += v[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kRb; ++u) {
+      const int e = e0 + u * kTcThreads, r = e / kTcRedTok, tl = e % kTcRedTok;
+      if (tl < nt) Y[tl * kTcRedLd + r] = g.x_norm == 2 ? acc[u] * s_inv[tl] : acc[u];
+    }
   }
   __syncthreads();
   tc_epilogue(g, tile, Y, kTcRedLd, t0, nt, threadIdx.x, kTcThreads);

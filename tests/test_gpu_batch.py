@@ -17,7 +17,9 @@ sequence, with sequence b's Philox draws at row word b.
 * Passes of more than 64 tokens (16 sequences x 5 positions) run their GEMMs
   on the tensor-memory (tcgen05) GEMM; the teacher-forced parity above
   covers every GEMM kind on that path (q/k/v + RoPE + KV append, residual
-  adds, gate/up + SwiGLU, LM head).
+  adds, gate/up + SwiGLU, LM head).  With enough sequences for a wave of
+  (sequence, KV head) items, attention items carry 2 or 3 eight-row tiles
+  (all heads of several tokens per K/V walk): 48 x 3 and 40 x 5 tokens.
 * Sequences whose contexts cross the first 1024-key split (token-group
   attention items, split merges), after a synthetic prefill, step with valid
   counts and ragged lengths; spec_ar_step and spec_profile run on batches.
@@ -78,11 +80,14 @@ def test_batch_sequences_match_single(temp):
         assert len(ctxs[b]) == 20 + sum(len(got[s][0][b]) for s in range(steps))
 
 
-@pytest.mark.parametrize("nseq,k", [(3, 3), (16, 4)], ids=["3x4tok", "16x5tok-tensor-memory-gemm"])
+@pytest.mark.parametrize("nseq,k", [(3, 3), (16, 4), (48, 2), (40, 4)],
+                         ids=["3x4tok", "16x5tok-tensor-memory-gemm", "48x3tok-wide2-attention",
+                              "40x5tok-wide3-attention"])
 @pytest.mark.parametrize("temp", [0.0, 1.0])
 def test_batch_teacher_forced(temp, nseq, k):
-    # 16 sequences x 5 positions = 80 tokens per verify pass: the GEMMs run on
-    # the tensor-memory (tcgen05) GEMM
+    # 16 x 5 = 80 tokens per verify pass: the GEMMs run on the tensor-memory
+    # (tcgen05) GEMM; 48 x 3 and 40 x 5 tokens (with 152 SMs): attention
+    # items of 2 and 3 eight-row tiles
     max_ctx, steps, seed = 128, 5, 7
     w, dshape, dw = _pair(seed=3)
     prompts = workloads.make_prompt(SHAPE.vocab, 12, seed=9, batch=nseq).tolist()
@@ -122,10 +127,11 @@ def test_batch_teacher_forced(temp, nseq, k):
     dec.close()
 
 
-@pytest.mark.parametrize("nseq", [4, 16])
+@pytest.mark.parametrize("nseq", [4, 16, 40])
 def test_batch_long_context_synthetic(nseq):
     # last verify position past 1024: token-group items, split merges; 16
-    # sequences: 96-token verify passes on the tensor-memory GEMM
+    # sequences: 96-token verify passes on the tensor-memory GEMM; 40: wide
+    # attention items across key splits
     k, L = 5, 1100
     w, dshape, dw = _pair(seed=4)
     dec = _dec(w, dshape, dw, k, 1200, 1.0, nseq)

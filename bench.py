@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--verify-sweep", action="store_true",
                     help="verify step alone over batch x K x context (one JSON line each): "
                          "latency, algorithmic bytes, GB/s, tensor FLOP/s")
+    ap.add_argument("--profile-batch", default="",
+                    help="profiling: B,K,CONTEXT -- one batched speculative step launched kernel by kernel "
+                         "(synthetic state) between cudaProfilerStart/Stop, after two unprofiled steps")
     ap.add_argument("--sweep-batches", default="1",
                     help="comma-separated batch sizes of --verify-sweep (batch > 1: synthetic KV)")
     ap.add_argument("--sweep-ks", default="1,2,3,4,5,6,8", help="comma-separated K of --verify-sweep")
@@ -425,6 +428,24 @@ def main():
                           "passes": {name: phase_summary(dec.phase_times(i))
                                      for name, i in (("draft_1", 0), ("draft_2", 1), ("verify", K),
                                                      ("ar", K + 1))}}), flush=True)
+        return 0
+
+    if args.profile_batch:
+        pb, pk, pctx = [int(x) for x in args.profile_batch.split(",")]
+        d = sv.SpecDecoder(tshape, tw, dshape, dw, pk, pctx + 2 * (pk + 1) + 64, temperature=args.temperature,
+                           seed=0, mix_lambda=0.0, stream=stream.cuda_stream, flags=sv.SPEC_OPT_NO_GRAPH,
+                           batch=pb)
+        d.prefill_synthetic(pctx, seed=3)
+        d.step()
+        d.step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        d.step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        print(json.dumps({"profile_batch": True, "batch": pb, "K": pk, "context": pctx, "workload": wl,
+                          "kernels_per_step": d.stats()["kernels_per_step"]}), flush=True)
+        d.close()
         return 0
 
     if args.ncu_mode:

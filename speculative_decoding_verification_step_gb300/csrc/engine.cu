@@ -232,7 +232,7 @@ struct Launch {
 
 void gemm(Launch& L, const GemmDesc& g, int dtype) {
   spec_ctx* c = L.c;
-  if (g.ntok > kGemmMaxTok) {   // many tokens (batched passes): tensor-memory GEMM
+  if (c->tok_max > kGemmMaxTok && g.ntok > kTcMinTok && tc_gemm_supported(g)) {   // batched passes
     L.note(launch_tc_gemm(g, c->tc_part, res_err(c), c->num_sms, c->tc_units, c->stream));
     return;
   }

@@ -1,7 +1,7 @@
 // Tensor-core GEMM on the fifth-generation tensor cores for passes of many
 // tokens (a batch of sequences' K+1 verify positions): Y = X . W^T with the
 // weights W [n][k] bf16 (the q/k/v segments, or the gate/up pair) and
-// X [ntok][k] bf16, 64 < ntok <= 256, fp32 accumulation in tensor memory.
+// X [ntok][k] bf16, 16 < ntok <= 256, fp32 accumulation in tensor memory.
 //
 // Work unit = (row tile, k split).  A row tile is 128 output rows (gate/up:
 // 64 gate rows then the same 64 up rows); the k range of the GEMM is cut into
@@ -466,7 +466,7 @@ size_t tc_gemm_partial_floats(int num_sms, int max_n) {
 }
 
 bool tc_gemm_supported(const GemmDesc& g) {
-  if (g.ntok <= kGemmMaxTok || g.ntok > kTcMaxTok || g.k % kTcKb != 0 || g.ldx % 8 != 0) return false;
+  if (g.ntok <= kTcMinTok || g.ntok > kTcMaxTok || g.k % kTcKb != 0 || g.ldx % 8 != 0) return false;
   if (g.x_norm == 1) return false;   // normalised inputs arrive as x * gain in bf16
   if (g.x_norm == 2 && ((reinterpret_cast<uintptr_t>(g.ss_in) & 15u) || g.ss_ld % 4 != 0 || g.ss_ld < kTcMaxTok))
     return false;                    // 1/rms reads float4 columns of up to kTcMaxTok tokens

@@ -7,15 +7,16 @@ acceptance).  The pages describe one sequence; a batch is that algorithm per
 sequence, with sequence b's Philox draws at row word b.
 
 * Each sequence advances exactly as it would alone: greedy steps of a
-  3-sequence batch give bit-identical tokens and counts to three batch-1
-  contexts on the per-operation path (every split point is independent of
-  the number of tokens in a pass), and so does sequence 0 at T = 1 (row
-  word 0 in both).
+  3-sequence batch (passes of at most 16 tokens, the skinny GEMM) give
+  bit-identical tokens and counts to three batch-1 contexts on the
+  per-operation path (every split point is independent of the number of
+  tokens in a pass), and so does sequence 0 at T = 1 (row word 0 in both).
 * Teacher-forced parity per sequence against the fp64 oracle: stage (i)
   logits within the bf16 tolerance, stage (ii) the oracle's acceptance with
   row word b on the GPU's logits reproduces sequence b's emitted tokens.
-* Passes of more than 64 tokens (16 sequences x 5 positions) run their GEMMs
-  on the tensor-memory (tcgen05) GEMM; the teacher-forced parity above
+* Passes of more than 16 tokens (6 or 16 sequences x 5 positions; 64 x 5 in
+  two passes of at most 256) run their GEMMs on the tensor-memory (tcgen05)
+  GEMM; the teacher-forced parity above
   covers every GEMM kind on that path (q/k/v + RoPE + KV append, residual
   adds, gate/up + SwiGLU, LM head).  With enough sequences for a wave of
   (sequence, KV head) items, attention items carry 2 or 3 eight-row tiles
@@ -80,14 +81,15 @@ def test_batch_sequences_match_single(temp):
         assert len(ctxs[b]) == 20 + sum(len(got[s][0][b]) for s in range(steps))
 
 
-@pytest.mark.parametrize("nseq,k", [(3, 3), (16, 4), (48, 2), (40, 4)],
-                         ids=["3x4tok", "16x5tok-tensor-memory-gemm", "48x3tok-wide2-attention",
-                              "40x5tok-wide3-attention"])
+@pytest.mark.parametrize("nseq,k", [(3, 3), (6, 4), (16, 4), (48, 2), (40, 4), (64, 4)],
+                         ids=["3x4tok", "6x5tok-tensor-memory-gemm", "16x5tok-tensor-memory-gemm",
+                              "48x3tok-wide2-attention", "40x5tok-wide3-attention", "64x5tok-two-passes"])
 @pytest.mark.parametrize("temp", [0.0, 1.0])
 def test_batch_teacher_forced(temp, nseq, k):
-    # 16 x 5 = 80 tokens per verify pass: the GEMMs run on the tensor-memory
-    # (tcgen05) GEMM; 48 x 3 and 40 x 5 tokens (with 152 SMs): attention
-    # items of 2 and 3 eight-row tiles
+    # 6 x 5 and 16 x 5 tokens per verify pass: the GEMMs run on the
+    # tensor-memory (tcgen05) GEMM; 48 x 3 and 40 x 5 tokens (with 152 SMs):
+    # attention items of 2 and 3 eight-row tiles; 64 x 5 = 320 tokens: two
+    # passes (sequence groups of at most 256 tokens)
     max_ctx, steps, seed = 128, 5, 7
     w, dshape, dw = _pair(seed=3)
     prompts = workloads.make_prompt(SHAPE.vocab, 12, seed=9, batch=nseq).tolist()

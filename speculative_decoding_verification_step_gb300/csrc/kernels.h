@@ -88,10 +88,10 @@ constexpr int kGemmWarpsPerCta = 8;
 constexpr int kGemmMaxTok = 64;      // tokens per GEMM pass (8 groups of 8)
 
 // Tensor-core (tcgen05) GEMM for batched passes of kTcMinTok < ntok <=
-// kTcMaxTok tokens (tcgemm.cu): row tiles of 128 weight rows x k splits;
-// split GEMMs write partials ([units][128][npad] fp32, at most max_units
-// units, tc_gemm_partial_floats) that a second launch reduces; err raised
-// when a bounded wait gives up.
+// kTcMaxTok tokens (tcgemm.cu): work units of 128 weight rows x a k split,
+// taken by one persistent CTA per SM; every unit writes an fp32 partial
+// ([units][128][npad], at most max_units units, tc_gemm_partial_floats) that
+// a second launch sums and finishes; err raised when a bounded wait gives up.
 constexpr int kTcMinTok = 16;    // the tensor-memory GEMM takes passes of more tokens
 constexpr int kTcMaxTok = 256;
 constexpr int kTcSmemBytes = 4 * (128 * 64 * 2 + kTcMaxTok * 64 * 2) + 1024;

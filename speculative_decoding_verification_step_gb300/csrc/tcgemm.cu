@@ -6,25 +6,28 @@
 // Work unit = (row tile, k split).  A row tile is 128 output rows (gate/up:
 // 64 gate rows then the same 64 up rows); the k range of the GEMM is cut into
 // `splits` contiguous runs of 64-element blocks, fixed by n, k and the grid
-// (not by ntok); each CTA starts its run at a tile-dependent block so that
-// a wave's CTAs read different blocks of X at a time.  Per CTA:
-//   warp 0, lane 0   producer: tensor copies of each 64-k block of the tile's
+// (not by ntok); a unit walks its run from a tile-dependent block so that the
+// CTAs read different blocks of X at a time.  Persistent: one CTA per SM
+// takes units blockIdx.x, blockIdx.x + gridDim.x, ...
+//   warp 0, lane 0   producer: tensor copies of each 64-k block of a unit's
 //                    weight rows (128 x 128 B) and of X (npad x 128 B) into
-//                    a ring of stages, 128-byte swizzled;
+//                    one ring of stages running across the CTA's units,
+//                    128-byte swizzled;
 //   warp 1, lane 0   MMA issuer: four 128 x npad x 16 tcgen05.mma per stage
-//                    (A = weights, B = X, both K-major), accumulating in tensor
-//                    memory; tcgen05.commit frees the stage, a last commit
-//                    signals the accumulator complete;
-//   warps 2..5       read the accumulator (one TMEM lane quarter each);
-//   warp 6           allocates and frees the tensor-memory columns;
-//   warps 2..7       meanwhile 1/rms of every token (normalised inputs arrive
-//                    as x * gain in bf16, as in the skinny GEMM).
-// One split: the accumulator (x 1/rms) goes to shared memory and the CTA runs
-// the operation's epilogue (store / residual add with the next norm's sums of
-// squares and x * gain / SwiGLU / RoPE + KV append).  Several splits: each
-// writes its fp32 partial [128][npad]; a second kernel, one CTA per (tile,
-// 32-token block), sums the partials in split order and runs the epilogue,
-// so that the reduction is spread over the whole GPU.
+//                    (A = weights, B = X, both K-major) into one of two
+//                    tensor-memory accumulators (unit i: buffer i mod 2);
+//                    tcgen05.commit frees the stage, a last commit per unit
+//                    signals its accumulator complete;
+//   warps 2..5       read a finished accumulator (one TMEM lane quarter each)
+//                    into the unit's fp32 partial [128][npad] while the next
+//                    unit accumulates in the other buffer, then free it;
+//   warp 6           allocates and frees the tensor-memory columns.
+// A second kernel, one CTA per (tile, 32-token block), sums the tile's
+// partials in split order, scales by 1/rms of the token (normalised inputs
+// arrive as x * gain in bf16, as in the skinny GEMM) and runs the operation's
+// epilogue (store / residual add with the next norm's sums of squares and
+// x * gain / SwiGLU / RoPE + KV append), so that reductions and epilogues are
+// spread over the whole GPU.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -44,14 +47,13 @@ constexpr int kTcKb = 64;           // k elements per stage (one 128-byte swizzl
 constexpr int kTcThreads = 256;
 constexpr int kTcABytes = kTcM * kTcKb * 2;   // 16 KB
 constexpr long long kTcWaitLimit = 1LL << 26;
-constexpr int kTcYLd = kTcM + 4;   // floats per token of the staged sums (one-split epilogue)
 
 struct TcArgs {
   TensorMap128 wmap[3];   // weight segments: boxes of 64 k x 128 rows (gate/up: 64 rows)
   TensorMap128 xmap;      // X [ntok][k]: boxes of 64 k x npad rows
   GemmDesc g;
   int npad, tiles, splits, nkb, stages, tmem_cols;
-  float* partials;        // [tiles * splits][128][npad] (splits > 1)
+  float* partials;        // [tiles * splits][128][npad]
   int* err;
 };
 
@@ -223,21 +225,27 @@ SV_DEV void tc_epilogue(const GemmDesc& g, int tile, const float* Y, int ld, int
 
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(1024) unsigned char tsm[];
-  __shared__ uint64_t full[8], empty[8], done;
+  // stage ring barriers; per accumulator buffer: MMAs done, readout done
+  __shared__ uint64_t full[8], empty[8], done[2], tfree[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_issued, s_consumed;
-  __shared__ float s_inv[kTcMaxTok];
-  __shared__ __align__(16) float s_red[(kTcThreads - 64) * 4];   // 1/rms: sums of k-tile groups
+  __shared__ int s_issued, s_consumed, s_units_done;
   const GemmDesc& g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
-  const int kb0 = (int)((long long)split * a.nkb / a.splits);
-  const int kb1 = (int)((long long)(split + 1) * a.nkb / a.splits);
-  const int nk = kb1 - kb0;
-  // first k block of the run: rotated by tile, so that the CTAs of a wave
-  // read different blocks of X at a time (fixed by the grid, not by ntok)
-  const int rot = (int)(((long long)tile * 5) % nk);
+  const int units = a.tiles * a.splits;
+  // this CTA's units: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int my_n = units > (int)blockIdx.x ? (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  // unit u = (tile, split): its k blocks kb0 .. kb0 + nk - 1, walked from a
+  // tile-dependent first block so that the CTAs read different blocks of X
+  // at a time (fixed by the grid, not by ntok)
+  auto unit_of = [&](int i, int* tile, int* kb0, int* nk, int* rot) {
+    const int u = (int)blockIdx.x + i * (int)gridDim.x;
+    *tile = u / a.splits;
+    const int split = u % a.splits;
+    *kb0 = (int)((long long)split * a.nkb / a.splits);
+    *nk = (int)((long long)(split + 1) * a.nkb / a.splits) - *kb0;
+    *rot = (int)(((long long)*tile * 5) % *nk);
+  };
   const int npad = a.npad;
   const unsigned stage_bytes = (unsigned)(kTcABytes + npad * kTcKb * 2);
   // 1024-aligned stage bases (the swizzle pattern repeats every 1024 bytes)
@@ -250,12 +258,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&done[b], 1);
+      mbar_init(&tfree[b], 4);   // one arrival per readout warp
+    }
     s_abort = 0;
-    s_issued = s_consumed = 0;
+    s_issued = s_consumed = s_units_done = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 6) {   // tensor-memory columns for the accumulator (one warp allocates and frees)
+  if (warp == 6) {   // tensor-memory columns: two accumulators of npad (one warp allocates and frees)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(&s_tmem)), "r"(a.tmem_cols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -267,99 +278,98 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   pdl_trigger();
   pdl_wait();
 
-  if (g.x_norm == 2 && warp >= 2) {   // 1/rms of every token, while the pipeline fills
-    // threads 64..255: float4 columns of 4 tokens x groups of k tiles
-    const int cols = npad / 4, groups = (kTcThreads - 64) / cols, u = threadIdx.x - 64;
-    const int col = u % cols, grp = u / cols, nt = g.k / 16;
-    float* red = reinterpret_cast<float*>(s_red);   // [groups][npad]
-    if (grp < groups) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int i = grp; i < nt; i += groups) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(g.ss_in + (size_t)i * g.ss_ld) + col);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      reinterpret_cast<float4*>(red + grp * npad)[col] = acc;
-    }
-    named_sync(1, kTcThreads - 64);
-    for (int t = u; t < npad; t += kTcThreads - 64) {
-      float sum = 0.f;
-      for (int q = 0; q < groups; ++q) sum += red[q * npad + t];
-      s_inv[t] = 1.0f / sqrtf(sum / (float)g.k + g.eps);
-    }
-    named_sync(1, kTcThreads - 64);
-  }
   if (warp == 0 && lane == 0) {
-    // ---- producer ----
+    // ---- producer: one continuous ring over all of this CTA's units ----
     const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
-    for (int i = 0; i < nk; ++i) {
-      const int s = i % a.stages;
-      if (i >= a.stages && !tc_wait(&empty[s], (unsigned)((i / a.stages - 1) & 1), &s_abort)) break;
-      const int kb = kb0 + (i + rot) % nk;
-      mbar_arrive_expect_tx(&full[s], stage_bytes);
-      if (g.epi == kEpiSwiglu) {
-        tma_load_2d_hint(stage_a(s), &a.wmap[0], kb * kTcKb, tile * 64, &full[s], pol_w);
-        tma_load_2d_hint(stage_a(s) + kTcABytes / 2, &a.wmap[1], kb * kTcKb, tile * 64, &full[s], pol_w);
-      } else {
-        int seg, row;
-        tc_tile_src(g, tile, 0, &seg, &row);
-        tma_load_2d_hint(stage_a(s), &a.wmap[seg], kb * kTcKb, row, &full[s], pol_w);
+    int q = 0;   // stage fills issued
+    for (int i = 0; i < my_n && !s_abort; ++i) {
+      int tile, kb0, nk, rot;
+      unit_of(i, &tile, &kb0, &nk, &rot);
+      int seg = 0, row = 0;
+      if (g.epi != kEpiSwiglu) tc_tile_src(g, tile, 0, &seg, &row);
+      for (int j = 0; j < nk; ++j, ++q) {
+        const int s = q % a.stages;
+        if (q >= a.stages && !tc_wait(&empty[s], (unsigned)((q / a.stages - 1) & 1), &s_abort)) break;
+        const int kb = kb0 + (j + rot) % nk;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        if (g.epi == kEpiSwiglu) {
+          tma_load_2d_hint(stage_a(s), &a.wmap[0], kb * kTcKb, tile * 64, &full[s], pol_w);
+          tma_load_2d_hint(stage_a(s) + kTcABytes / 2, &a.wmap[1], kb * kTcKb, tile * 64, &full[s], pol_w);
+        } else {
+          tma_load_2d_hint(stage_a(s), &a.wmap[seg], kb * kTcKb, row, &full[s], pol_w);
+        }
+        tma_load_2d_hint(stage_b(s), &a.xmap, kb * kTcKb, 0, &full[s], pol_x);
+        s_issued = q + 1;
       }
-      tma_load_2d_hint(stage_b(s), &a.xmap, kb * kTcKb, 0, &full[s], pol_x);
-      s_issued = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer ----
+    // ---- MMA issuer: unit i accumulates into buffer i & 1 ----
     const uint32_t idesc = idesc_bf16(npad);
-    for (int i = 0; i < nk; ++i) {
-      const int s = i % a.stages;
-      if (!tc_wait(&full[s], (unsigned)((i / a.stages) & 1), &s_abort)) break;
-      s_consumed = i + 1;
+    int q = 0;   // stage fills consumed
+    for (int i = 0; i < my_n && !s_abort; ++i) {
+      int tile, kb0, nk, rot;
+      unit_of(i, &tile, &kb0, &nk, &rot);
+      const int bi = i & 1;
+      // the readout of unit i - 2 has emptied this buffer
+      if (i >= 2 && !tc_wait(&tfree[bi], (unsigned)((i / 2 - 1) & 1), &s_abort)) break;
       tc_fence_after();
-      const uint64_t ad = smem_desc_sw128(stage_a(s)), bd = smem_desc_sw128(stage_b(s));
+      const uint32_t acc = tmem + (uint32_t)(bi * npad);
+      bool ok = true;
+      for (int j = 0; j < nk; ++j, ++q) {
+        const int s = q % a.stages;
+        if (!tc_wait(&full[s], (unsigned)((q / a.stages) & 1), &s_abort)) {
+          ok = false;
+          break;
+        }
+        s_consumed = q + 1;
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(stage_a(s)), bd = smem_desc_sw128(stage_b(s));
 #pragma unroll
-      for (int kk = 0; kk < kTcKb / 16; ++kk)   // 16-k slices: +32 bytes = +2 in the start field
-        tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(&empty[s]);
+        for (int kk = 0; kk < kTcKb / 16; ++kk)   // 16-k slices: +32 bytes = +2 in the start field
+          tc_mma(acc, ad + 2 * kk, bd + 2 * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(&done[bi]);   // completes when every MMA issued above has
+      if (!ok) break;
     }
-    tc_commit(&done);   // completes when every MMA issued above has
   } else if (warp >= 2 && warp <= 5) {
-    // ---- accumulator -> partial [128][npad] ----
+    // ---- accumulator -> partial [128][npad] of unit blockIdx.x + i gridDim.x ----
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const int r = q * 32 + lane;                  // tile row
-    const bool ok = tc_wait(&done, 0u, &s_abort);
-    tc_fence_after();
-    if (ok && a.splits > 1) {   // partial [128][npad] for the reduction kernel
-      float* part = a.partials + ((size_t)blockIdx.x * kTcM + r) * npad;
+    for (int i = 0; i < my_n; ++i) {
+      const int bi = i & 1;
+      if (!tc_wait(&done[bi], (unsigned)((i / 2) & 1), &s_abort)) break;
+      tc_fence_after();
+      const int u = (int)blockIdx.x + i * (int)gridDim.x;
+      float* part = a.partials + ((size_t)u * kTcM + r) * npad;
+      const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(bi * npad);
       for (int c = 0; c < npad; c += 16) {
         float v[16];
-        tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
+        tc_ld16(acc + (uint32_t)c, v);
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(part + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(part + c + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
       }
-    } else if (ok) {            // the whole sum: Y[t][r] (x 1/rms) in the idle stage ring
-      float* Y = reinterpret_cast<float*>(base);
-      for (int c = 0; c < npad; c += 16) {
-        float v[16];
-        tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) Y[(c + i) * kTcYLd + r] = g.x_norm == 2 ? v[i] * s_inv[c + i] : v[i];
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tfree[bi]);
+      if (threadIdx.x == 64) s_units_done = i + 1;
     }
-    tc_fence_before();
   }
   __syncthreads();
   if (s_abort && threadIdx.x == 0) {
-    // a wait gave up: let the copies issued but not consumed land (bounded),
-    // and the MMAs issued finish, before the space and the columns go
+    // a wait gave up: let the copies issued but not consumed land and the
+    // MMAs issued finish (bounded), before the space and the columns go
     atomicExch(a.err, 1);
-    for (int i = s_consumed; i < s_issued; ++i) {
+    for (int q = s_consumed; q < s_issued; ++q) {
       long long spins = 0;
-      while (!mbar_test(&full[i % a.stages], (unsigned)((i / a.stages) & 1)) && ++spins < (1LL << 20)) {
+      while (!mbar_test(&full[q % a.stages], (unsigned)((q / a.stages) & 1)) && ++spins < (1LL << 20)) {
       }
     }
-    long long spins = 0;
-    while (!mbar_test(&done, 0u) && ++spins < (1LL << 20)) {
+    for (int i = s_units_done; i < my_n && i < s_units_done + 2; ++i) {
+      long long spins = 0;
+      while (!mbar_test(&done[i & 1], (unsigned)((i / 2) & 1)) && ++spins < (1LL << 20)) {
+      }
     }
   }
   __syncthreads();
@@ -367,10 +377,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
   }
-  if (s_abort) return;
-
-  if (a.splits == 1) tc_epilogue(g, tile, reinterpret_cast<const float*>(base), kTcYLd, 0, g.ntok, threadIdx.x,
-                                 kTcThreads);
 }
 
 // Reduction and epilogue of a split GEMM: one CTA per (row tile, block of
@@ -459,10 +465,9 @@ static bool tc_encode_rows(TensorMap128& m, const void* base, int k, long long r
 }
 
 size_t tc_gemm_partial_floats(int num_sms, int max_n) {
-  // every work unit of a split GEMM writes one [128][npad] partial: at most
-  // two waves of num_sms units (one-split GEMMs write none)
-  (void)max_n;
-  return 2 * (size_t)num_sms * kTcM * kTcMaxTok;
+  // every work unit writes one [128][npad] partial: the LM head's tiles (one
+  // split), or up to eight splits of fewer tiles
+  return std::max<size_t>((size_t)(max_n + kTcM - 1) / kTcM, 8 * (size_t)num_sms) * kTcM * kTcMaxTok;
 }
 
 bool tc_gemm_supported(const GemmDesc& g) {
@@ -485,25 +490,26 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
   a.npad = (g.ntok + 15) / 16 * 16;
   a.nkb = g.k / kTcKb;
   a.tiles = g.epi == kEpiSwiglu ? g.n / 64 : (g.n + kTcM - 1) / kTcM;
-  // splits: the fullest last wave of num_sms CTAs (one per SM), fewest
-  // splits on ties, at least two k blocks per split, within the partials
+  // splits (at most 8, at least two k blocks each): the fewest rounds of
+  // units per CTA times the k blocks of a unit, fewest splits on ties, within
+  // the partials
   a.splits = 1;
-  double best = 0.0;
-  for (int sp = 1; sp <= std::max(1, std::min(16, a.nkb / 2)); ++sp) {
+  long long best = -1;
+  for (int sp = 1; sp <= std::max(1, std::min(8, a.nkb / 2)); ++sp) {
     const long long units = (long long)a.tiles * sp;
-    if (sp > 1 && units > max_units) break;
-    const double eff = (double)units / ((double)num_sms * (double)((units + num_sms - 1) / num_sms));
-    if (eff > best + 1e-3) {
-      best = eff;
+    if (units > max_units) break;
+    const long long cost = ((units + num_sms - 1) / num_sms) * ((a.nkb + sp - 1) / sp);
+    if (best < 0 || cost < best) {
+      best = cost;
       a.splits = sp;
     }
   }
   const int stage_bytes = kTcABytes + a.npad * kTcKb * 2;
   a.stages = std::min(8, (kTcSmemBytes - 1024) / stage_bytes);
   int cols = 32;
-  while (cols < a.npad) cols *= 2;
+  while (cols < 2 * a.npad) cols *= 2;   // two accumulators
   a.tmem_cols = cols;
-  if (a.splits > 1 && (long long)a.tiles * a.splits > max_units) return cudaErrorInvalidValue;
+  if ((long long)a.tiles * a.splits > max_units) return cudaErrorInvalidValue;
   a.partials = partials;
   a.err = err;
   const int box_rows = g.epi == kEpiSwiglu ? 64 : kTcM;
@@ -513,8 +519,9 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
     if (!tc_encode_rows(a.wmap[s], g.w[s], g.k, rows, g.k, box_rows)) return cudaErrorInvalidValue;
   }
   if (!tc_encode_rows(a.xmap, g.x, g.k, g.ntok, g.ldx, a.npad)) return cudaErrorInvalidValue;
-  cudaError_t e = launch_k(tc_gemm_kernel, dim3(a.tiles * a.splits), dim3(kTcThreads), (size_t)kTcSmemBytes, st, a);
-  if (e != cudaSuccess || a.splits == 1) return e;
+  const int grid = std::min(a.tiles * a.splits, num_sms);   // persistent: one CTA per SM
+  cudaError_t e = launch_k(tc_gemm_kernel, dim3(grid), dim3(kTcThreads), (size_t)kTcSmemBytes, st, a);
+  if (e != cudaSuccess) return e;
   return launch_k(tc_reduce_kernel, dim3(a.tiles, (g.ntok + kTcRedTok - 1) / kTcRedTok), dim3(kTcThreads), 0, st, a);
 }
 

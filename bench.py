@@ -343,19 +343,25 @@ def main():
 
     base_flags = (sv.SPEC_OPT_PDL if args.pdl else 0) | (sv.SPEC_OPT_NO_PERSIST if args.no_persist else 0)
 
-    def make(temp, mix, flags=0):
+    def make(temp, mix, flags=0, lookup=0):
         return sv.SpecDecoder(tshape, tw, dshape, dw, K, max_ctx, temperature=temp, seed=0,
-                              mix_lambda=mix, stream=stream.cuda_stream, flags=flags | base_flags)
+                              mix_lambda=mix, stream=stream.cuda_stream, flags=flags | base_flags,
+                              lookup=lookup)
 
     def prompt(i):
         return workloads.make_prompt(tshape.vocab, args.prompt, seed=1000 * rank + i)[0].tolist()
 
-    def timed_generations(dec, n_steps, gen_base):
+    def repeat_prompt(i):
+        """A 128-token uniform block repeated to the prompt length (prompt lookup finds matches)."""
+        blk = workloads.make_prompt(tshape.vocab, 128, seed=1000 * rank + i)[0].tolist()
+        return (blk * (args.prompt // 128 + 1))[:args.prompt]
+
+    def timed_generations(dec, n_steps, gen_base, prompt_fn=None):
         """Run n_steps speculative steps as whole generations; returns (ms, tokens, steps)."""
         ms, toks, done, g = 0.0, 0, 0, gen_base
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         while done < n_steps:
-            dec.prefill(prompt(g))
+            dec.prefill((prompt_fn or prompt)(g))
             g += 1
             emitted = 0
             e0.record(stream)
@@ -553,6 +559,20 @@ def main():
             h2 = s2["accept_hist"][:K + 1]
             sweep.append({"temperature": temp, "mix_lambda": mix, "tokens_per_s": t2 / (m2 / 1000),
                           "tokens_per_step": t2 / n2,
+                          "speedup_vs_ar": (t2 / (m2 / 1000)) / ar_tok_s})
+            d2.close()
+        # prompt-lookup drafting (n-gram suffix match up to 3 tokens) on prompts
+        # of a repeated 128-token block; with random-init weights the target
+        # does not follow the repetition, so this measures the step cost of
+        # lookup drafting (one launch instead of the K draft passes)
+        for temp in (1.0, 0.0):
+            d2 = make(temp, 0.0, lookup=3)
+            d2.prefill(repeat_prompt(0))
+            d2.step()
+            m2, t2, n2 = timed_generations(d2, 60, 70, repeat_prompt)
+            sweep.append({"drafter": "prompt lookup (n-gram up to 3)", "temperature": temp,
+                          "prompt": "128-token uniform block repeated", "tokens_per_s": t2 / (m2 / 1000),
+                          "tokens_per_step": t2 / n2, "ms_per_step": m2 / n2,
                           "speedup_vs_ar": (t2 / (m2 / 1000)) / ar_tok_s})
             d2.close()
 

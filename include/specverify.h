@@ -126,6 +126,11 @@ typedef struct spec_opts {
                                    previous-step logits (same row index) */
     void*    cuda_stream;       /* cudaStream_t to run on; NULL = library-created stream */
     int      flags;             /* SPEC_OPT_* */
+    int      draft_lookup;      /* 0 = the draft model drafts; n in 1..8 = prompt lookup
+                                   ([101 Floor 6] n-gram drafting): the drafts continue the
+                                   most recent longest (up to n tokens) earlier match of the
+                                   context's end, q is one-hot at each draft, and the draft
+                                   model is not run (draft_mix_lambda must be 0) */
 } spec_opts;
 
 typedef struct spec_stats {

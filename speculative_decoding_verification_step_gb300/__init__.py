@@ -48,7 +48,7 @@ class ModelDesc(ctypes.Structure):
 class Opts(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("max_ctx", ctypes.c_int), ("temperature", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("draft_mix_lambda", ctypes.c_float),
-                ("cuda_stream", ctypes.c_void_p), ("flags", ctypes.c_int)]
+                ("cuda_stream", ctypes.c_void_p), ("flags", ctypes.c_int), ("draft_lookup", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):
@@ -169,17 +169,19 @@ def model_desc(shape, weights):
 
 class SpecDecoder:
     """One target/draft pair with K drafts per step over `batch` sequences
-    (batch > 1: bf16 models, every sequence advancing independently)."""
+    (batch > 1: bf16 models, every sequence advancing independently);
+    lookup = n > 0 drafts by prompt lookup (n-gram suffix match up to n
+    tokens) instead of running the draft model."""
 
     def __init__(self, target_shape, target_w, draft_shape, draft_w, k, max_ctx,
-                 temperature=0.0, seed=0, mix_lambda=0.0, stream=None, flags=0, batch=1):
+                 temperature=0.0, seed=0, mix_lambda=0.0, stream=None, flags=0, batch=1, lookup=0):
         self.k = k
         self.batch = batch
         self.vocab = target_shape.vocab
         self._td, self._tk = model_desc(target_shape, target_w)
         self._dd, self._dk = model_desc(draft_shape, draft_w)
         opts = Opts(batch, max_ctx, temperature, seed, mix_lambda,
-                    ctypes.c_void_p(stream) if stream else ctypes.c_void_p(0), flags)
+                    ctypes.c_void_p(stream) if stream else ctypes.c_void_p(0), flags, lookup)
         h = ctypes.c_void_p()
         rc = lib().spec_init(ctypes.byref(self._td), ctypes.byref(self._dd), k, ctypes.byref(opts),
                              ctypes.byref(h))

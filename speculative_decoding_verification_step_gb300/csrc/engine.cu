@@ -79,6 +79,7 @@ struct spec_ctx {
   unsigned* bar = nullptr;
   int K = 0;
   int B = 1;                       // sequences (batch > 1: per-operation path, bf16 models)
+  int lookup = 0;                  // > 0: prompt-lookup drafting with suffix matches up to this
   int64_t seq_ld = 0;              // int32 stride between the sequences' token arrays
   int tok_max = kGemmMaxTok;       // tokens per forward pass (batch > 1: up to kTcMaxTok)
   float* tc_part = nullptr;        // tensor-core GEMM partials (batch > 1), tc_units work units
@@ -473,6 +474,14 @@ SampleDesc sampler(spec_ctx* c, int which, int32_t* out_token, int64_t out_ld, c
 void enqueue_draft(Launch& L) {
   spec_ctx* c = L.c;
   const int K = c->K, V = c->tgt.d.vocab;
+  if (c->lookup) {   // prompt lookup: drafts and one-hot q rows in one launch
+    LookupDesc ld{};
+    ld.seq = c->seq; ld.seq_ld = c->seq_ld; ld.lens = c->st; ld.st_ld = kStateLd;
+    ld.rows = c->B; ld.K = K; ld.n_max = c->lookup; ld.V = V;
+    ld.q_out = c->logits_q; ld.q_ld = (int64_t)K * V;
+    L.note(launch_lookup(ld, c->stream));
+    return;
+  }
   const int32_t* Lp = c->st;  // committed length index (position of the pending token)
   const bool mix = c->opts.draft_mix_lambda != 0.f;
   for (int i = 1; i <= K; ++i) {
@@ -685,6 +694,10 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     return fail(nullptr, SPEC_E_ARG, "batch > 1 needs bf16 target and draft models");
   if (opts->batch > 1 && opts->draft_mix_lambda != 0.f)
     return fail(nullptr, SPEC_E_ARG, "batch > 1 does not support draft_mix_lambda");
+  if (opts->draft_lookup < 0 || opts->draft_lookup > kLookupMaxN)
+    return fail(nullptr, SPEC_E_ARG, "draft_lookup must be in 0..8");
+  if (opts->draft_lookup > 0 && opts->draft_mix_lambda != 0.f)
+    return fail(nullptr, SPEC_E_ARG, "prompt lookup has no draft logits to mix (draft_mix_lambda must be 0)");
   if (opts->max_ctx < K + 3) return fail(nullptr, SPEC_E_ARG, "max_ctx must be at least K + 3");
   if (!(opts->temperature >= 0.f)) return fail(nullptr, SPEC_E_ARG, "temperature must be >= 0");
   int dev = 0;
@@ -694,6 +707,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   spec_ctx* c = new spec_ctx();
   c->K = K;
   c->B = opts->batch;
+  c->lookup = opts->draft_lookup;
   c->opts = *opts;
   c->cap = opts->max_ctx;
   c->seq_ld = (int64_t)c->cap + K + 2;
@@ -968,7 +982,7 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
       const int nt = std::min(kGemmMaxTok, nk - p0);
       rc = set_eager_pos(c, p0, b);
       if (rc) return rc;
-      forward(Lc, c->drf, nt, sb, nullptr, p0, pb, 0, 0, 0, nullptr, sq);
+      if (!c->lookup) forward(Lc, c->drf, nt, sb, nullptr, p0, pb, 0, 0, 0, nullptr, sq);
       int r0 = 0, rn = 0;
       if (mix) {
         r0 = std::max(lo, p0) - p0;
@@ -984,7 +998,7 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
   }
   if (c->persist) {
     c->grp = false;   // one token per pass
-    forward_persist(Lc, K + 2);
+    if (!c->lookup) forward_persist(Lc, K + 2);
     forward_persist(Lc, K + 3);
     CUDA_TRY(c, Lc.e);
   }
@@ -1030,7 +1044,8 @@ int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* ou
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
   if (!out_tokens || !out_count) return fail(c, SPEC_E_ARG, "null output buffer");
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_step before spec_prefill");
-  if (c->draft_stale) return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
+  if (c->draft_stale && !c->lookup)   // (prompt lookup keeps no draft cache)
+    return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
   if (max_host_L(c) + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
   const int K = c->K, B = c->B;
   c->ev_used = 0;

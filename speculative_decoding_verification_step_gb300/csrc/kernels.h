@@ -257,6 +257,23 @@ struct AcceptDesc {
 size_t accept_partial_floats(int rows, int K, int V);
 cudaError_t launch_accept(const AcceptDesc& a, cudaStream_t st);
 
+// Prompt-lookup drafting (lookup.cu): per sequence b, drafts d_1..d_K of the
+// most recent longest suffix match (up to n_max tokens) written to
+// seq[b * seq_ld + L_b + 1 ..], L_b = lens[b * st_ld], and one-hot q logit
+// rows (0 at d_i, -inf elsewhere) to q_out + b * q_ld + (i-1) * V.
+constexpr int kLookupMaxK = 16;
+constexpr int kLookupMaxN = 8;
+struct LookupDesc {
+  int32_t* seq;
+  int64_t seq_ld;
+  const int32_t* lens;
+  int st_ld;
+  int rows, K, n_max, V;
+  float* q_out;
+  int64_t q_ld;
+};
+cudaError_t launch_lookup(const LookupDesc& d, cudaStream_t st);
+
 // ---- persistent forward (bf16 models) ----
 // One cooperative launch runs the phases of a whole forward (embedding, the
 // per-layer GEMMs and attention, the LM head), separated by a bounded grid

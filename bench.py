@@ -303,6 +303,20 @@ def phase_summary(ph):
     return out
 
 
+def combine_ranks(ms, toks, world, device):
+    """Whole-job inputs of the throughput across replicas: the slowest rank's
+    timed milliseconds (all_reduce MAX) and the tokens of all ranks (SUM)."""
+    if world <= 1:
+        return ms, float(toks)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, toks], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(t[1])
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -488,14 +502,7 @@ def main():
         wall = time.perf_counter() - wall0
     clocks = clk.summary()
     st = dec.stats()
-    if world > 1:
-        t = torch.tensor([ms, toks], dtype=torch.float64, device="cuda")
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        ms_max, toks_all = float(mx[0]), float(t[1])
-    else:
-        ms_max, toks_all = ms, float(toks)
+    ms_max, toks_all = combine_ranks(ms, toks, world, "cuda")
     value = toks_all / (ms_max / 1000.0)
     hist = st["accept_hist"][:K + 1]
     steps_in_stats = max(1, sum(hist))

@@ -28,8 +28,9 @@
  *  - A context holds `batch` independent sequences (1..SPEC_MAX_BATCH).
  *    Batch 1 runs each forward as one persistent kernel (bf16 models);
  *    batch > 1 needs bf16 models and runs one kernel per operation, with
- *    the sequences' tokens in one pass (groups of at most 64 tokens, each
- *    group streaming the weights once).  Sequences advance independently
+ *    the sequences' tokens in one pass (groups of at most 256 tokens, each
+ *    group streaming the weights once; passes of more than 16 tokens on the
+ *    tensor-memory GEMM).  Sequences advance independently
  *    (ragged acceptance): every sequence has its own committed length, step
  *    counters, KV rows and Philox row word (its index b).
  *  - All work runs on one GPU, on the stream given in spec_opts (or a

@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--verify-sweep", action="store_true",
                     help="verify step alone over batch x K x context (one JSON line each): "
                          "latency, algorithmic bytes, GB/s, tensor FLOP/s")
+    ap.add_argument("--k-sweep", action="store_true",
+                    help="speculative vs plain decoding at batch 1 for K = 1..8 (one JSON line each): "
+                         "tokens/s, speedup, tokens per step, acceptance, C and the modelled K a / (1 + K C)")
     ap.add_argument("--profile-batch", default="",
                     help="profiling: B,K,CONTEXT -- one batched speculative step launched kernel by kernel "
                          "(synthetic state) between cudaProfilerStart/Stop, after two unprofiled steps")
@@ -370,9 +373,14 @@ def main():
         blk = workloads.make_prompt(tshape.vocab, 128, seed=1000 * rank + i)[0].tolist()
         return (blk * (args.prompt // 128 + 1))[:args.prompt]
 
+    hist_acc = {}
+
     def timed_generations(dec, n_steps, gen_base, prompt_fn=None):
-        """Run n_steps speculative steps as whole generations; returns (ms, tokens, steps)."""
+        """Run n_steps speculative steps as whole generations; returns (ms,
+        tokens, steps).  The histogram of accepted drafts over all of them is
+        left in hist_acc[id(dec)] (each prefill resets the context's own)."""
         ms, toks, done, g = 0.0, 0, 0, gen_base
+        hist = [0] * 17
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         while done < n_steps:
             dec.prefill((prompt_fn or prompt)(g))
@@ -387,6 +395,8 @@ def main():
             e1.synchronize()
             ms += e0.elapsed_time(e1)
             toks += emitted
+            hist = [x + y for x, y in zip(hist, dec.stats()["accept_hist"])]
+        hist_acc[id(dec)] = hist
         return ms, toks, done
 
     if args.verify_sweep:
@@ -450,6 +460,48 @@ def main():
                                                      ("ar", K + 1))}}), flush=True)
         return 0
 
+    if args.k_sweep:
+        # plain decoding once (its pass does not depend on K), then per K:
+        # whole generations as in the headline run, and the graph-replayed
+        # phase times for C
+        ar = make(args.temperature, 0.0)
+        ar.prefill(prompt(0))
+        for _ in range(3):
+            ar.ar_step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ar.prefill(prompt(1))
+        e0.record(stream)
+        for _ in range(args.ar_tokens):
+            ar.ar_step()
+        e1.record(stream)
+        e1.synchronize()
+        ar_tok_s = args.ar_tokens / (e0.elapsed_time(e1) / 1000.0)
+        ar.close()
+        for k in (1, 2, 3, 4, 5, 6, 8):
+            d = sv.SpecDecoder(tshape, tw, dshape, dw, k, args.prompt + args.new_tokens + 4 * (k + 1) + 64,
+                               temperature=args.temperature, seed=0, mix_lambda=args.mix,
+                               stream=stream.cuda_stream, flags=base_flags)
+            d.prefill(prompt(0))
+            d.step()
+            ms, toks, nsteps = timed_generations(d, 90, 400)
+            hist = hist_acc[id(d)][:k + 1]
+            acc_n = sum(i * h for i, h in enumerate(hist))
+            alpha = acc_n / max(1, acc_n + sum(hist[:k]))
+            d.prefill(prompt(0))
+            prof = d.profile(iters=10)
+            c_ratio = prof["draft_loop_ms"] / max(1e-9, k * prof["verify_ms"])
+            tok_s = toks / (ms / 1000.0)
+            print(json.dumps({"k_sweep": True, "workload": wl, "K": k, "temperature": args.temperature,
+                              "mix_lambda": args.mix, "tokens_per_s": tok_s, "ar_tokens_per_s": ar_tok_s,
+                              "speedup_vs_ar": tok_s / ar_tok_s, "tokens_per_step": toks / nsteps,
+                              "acceptance_alpha": alpha,
+                              "expected_tokens_per_step": (1 - alpha ** (k + 1)) / (1 - alpha) if alpha < 1 else k + 1,
+                              "verify_ms": prof["verify_ms"], "draft_loop_ms": prof["draft_loop_ms"],
+                              "C": c_ratio, "K_alpha_over_1_plus_KC": k * alpha / (1 + k * c_ratio),
+                              "persistent": prof["kernels_verify"] <= 2}), flush=True)
+            d.close()
+        return 0
+
     if args.profile_batch:
         pb, pk, pctx = [int(x) for x in args.profile_batch.split(",")]
         d = sv.SpecDecoder(tshape, tw, dshape, dw, pk, pctx + 2 * (pk + 1) + 64, temperature=args.temperature,
@@ -504,7 +556,7 @@ def main():
     st = dec.stats()
     ms_max, toks_all = combine_ranks(ms, toks, world, "cuda")
     value = toks_all / (ms_max / 1000.0)
-    hist = st["accept_hist"][:K + 1]
+    hist = hist_acc[id(dec)][:K + 1]    # every timed generation (each prefill resets the context's)
     steps_in_stats = max(1, sum(hist))
     tokens_per_step = sum((i + 1) * h for i, h in enumerate(hist)) / steps_in_stats
     alpha = sum(i * h for i, h in enumerate(hist)) / max(1, sum(i * h for i, h in enumerate(hist)) +
@@ -562,8 +614,6 @@ def main():
             d2.prefill(prompt(0))
             d2.step()
             m2, t2, n2 = timed_generations(d2, 60, 50)
-            s2 = d2.stats()
-            h2 = s2["accept_hist"][:K + 1]
             sweep.append({"temperature": temp, "mix_lambda": mix, "tokens_per_s": t2 / (m2 / 1000),
                           "tokens_per_step": t2 / n2,
                           "speedup_vs_ar": (t2 / (m2 / 1000)) / ar_tok_s})

@@ -498,6 +498,8 @@ def main():
                               "expected_tokens_per_step": (1 - alpha ** (k + 1)) / (1 - alpha) if alpha < 1 else k + 1,
                               "verify_ms": prof["verify_ms"], "draft_loop_ms": prof["draft_loop_ms"],
                               "C": c_ratio, "K_alpha_over_1_plus_KC": k * alpha / (1 + k * c_ratio),
+                              "expected_tokens_over_1_plus_KC": ((1 - alpha ** (k + 1)) / (1 - alpha) if alpha < 1
+                                                                 else k + 1) / (1 + k * c_ratio),
                               "persistent": prof["kernels_verify"] <= 2}), flush=True)
             d.close()
         return 0

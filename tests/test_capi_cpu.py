@@ -49,8 +49,8 @@ def _desc(vocab=256, head_dim=32, dtype=sv.SPEC_DTYPE_F32, layers=None):
     return d, lay
 
 
-def _init(L, t, d, k=4, max_ctx=128, batch=1, mix=0.0):
-    opts = sv.Opts(batch, max_ctx, 1.0, 0, mix, None, 0)
+def _init(L, t, d, k=4, max_ctx=128, batch=1, mix=0.0, lookup=0):
+    opts = sv.Opts(batch, max_ctx, 1.0, 0, mix, None, 0, lookup)
     h = ctypes.c_void_p()
     rc = L.spec_init(ctypes.byref(t) if t is not None else None,
                      ctypes.byref(d) if d is not None else None, k, ctypes.byref(opts), ctypes.byref(h))
@@ -75,6 +75,15 @@ def test_init_argument_errors(L):
     nulls = (sv.LayerWeights * 1)()
     nl, _f = _desc(layers=nulls)
     assert _init(L, nl, d)[0] == -1
+
+
+def test_lookup_argument_errors(L):
+    t, _a = _desc()
+    d, _b = _desc()
+    assert _init(L, t, d, lookup=-1)[0] == -1
+    assert _init(L, t, d, lookup=9)[0] == -1                # suffix matches of at most 8 tokens
+    assert _init(L, t, d, lookup=3, mix=0.5)[0] == -1       # no draft logits to mix
+    assert b"draft_mix_lambda" in L.spec_last_error(None)
 
 
 def test_batch_argument_errors(L):

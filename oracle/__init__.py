@@ -21,6 +21,10 @@ What it restates, and from where:
   bits the GPU receives.
 * ``generate`` -- the draft loop, verification and commit of one speculative
   step, the generation loop around it, and plain autoregressive decoding.
+* ``lookup``  -- prompt-lookup (n-gram) drafting ("Speculative Decoding 101",
+  Floor 6) with its one-hot proposals.
+* ``quant``   -- the 4-bit group-quantized weight format (codes, bf16 scales,
+  packing) and its dequantization.
 
 Pins that tie this oracle to something other than itself live in
 ``tests/test_oracle_*.py`` (worked example, exhaustive enumeration, greedy

@@ -1033,9 +1033,11 @@ int spec_seq_context(spec_ctx* c, int b, int32_t* context, int32_t* len) {
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
   if (b < 0 || b >= c->B || !len) return fail(c, SPEC_E_ARG, "bad sequence index or null length");
   const int n = c->host_Ls[b] + 1;
-  if (context)
-    CUDA_TRY(c, cudaMemcpy(context, c->seq + (size_t)b * c->seq_ld, sizeof(int32_t) * n,
-                           cudaMemcpyDeviceToHost));
+  if (context) {   // on the context's stream, after anything still queued there
+    CUDA_TRY(c, cudaMemcpyAsync(context, c->seq + (size_t)b * c->seq_ld, sizeof(int32_t) * n,
+                                cudaMemcpyDeviceToHost, c->stream));
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  }
   *len = n;
   return SPEC_OK;
 }

@@ -118,12 +118,22 @@ def generate(target: Model, draft: Model, prompt, n_new, k, temperature, seed,
     return out[:n_new], steps
 
 
-def ar_token(logits_row, temperature, seed, step, row=0):
+def ar_token_flagged(logits_row, temperature, seed, step, row=0, tie_eps=acc.TIE_EPS):
+    """Plain decoding's draw at step ``step``: argmax at T = 0, else the
+    inverse CDF of softmax(logits / T) with the stream-4 uniform at position
+    0.  Returns (token, flags): FLAG_NEAR_TIE when the top-2 logit gap is
+    below tie_eps (T = 0), FLAG_NEAR_EDGE when the target lands within
+    EDGE_EPS of a bin edge (T > 0)."""
     if temperature == 0:
-        return acc.argmax_lowest(logits_row)
+        flags = acc.FLAG_NEAR_TIE if acc.top2_gap(logits_row) < tie_eps else 0
+        return acc.argmax_lowest(logits_row), flags
     p = acc.softmax_t(logits_row, temperature)
-    j, _ = acc.inverse_cdf(p, uniform(seed, step, 0, STREAM_AR, row))
-    return j
+    j, margin = acc.inverse_cdf(p, uniform(seed, step, 0, STREAM_AR, row))
+    return j, (acc.FLAG_NEAR_EDGE if margin < acc.EDGE_EPS else 0)
+
+
+def ar_token(logits_row, temperature, seed, step, row=0):
+    return ar_token_flagged(logits_row, temperature, seed, step, row)[0]
 
 
 def ar_generate(target: Model, prompt, n_new, temperature, seed, row=0):

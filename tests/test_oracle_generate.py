@@ -8,6 +8,9 @@ workload (2 layers, d=128, vocab 256, fp32; draft = layer 0 + noise).
   rejection are emitted unchanged.
 * A draft identical to the target accepts all K drafts every step.
 * generate(n) returns exactly n tokens (overshoot truncated).
+* The mixed draft's previous-step rows, worked by hand on table models:
+  before the first step they are the target rows at positions L-1-K .. L-1
+  (L = the pending token's position), and draft i mixes with row i-1.
 """
 import numpy as np
 import pytest
@@ -61,3 +64,47 @@ def test_sampled_first_token_uses_target_distribution(tiny):
     res = gen.spec_step(target, target, prompt, 4, 1.0, 0, 0)
     assert res.emitted[:4] == res.drafts
     assert np.allclose(res.q_logits, res.p_logits[:4], atol=1e-10)
+
+
+class _Table:
+    """Table model: the logit row for position j of `tokens` is
+    [j, tokens[j], 0, ...] (target), or a fixed row (draft)."""
+
+    def __init__(self, vocab, fixed=None):
+        self.vocab, self.fixed = vocab, fixed
+
+    def logits(self, tokens, last):
+        n = len(tokens)
+        rows = np.zeros((last, self.vocab))
+        for r, j in enumerate(range(n - last, n)):
+            if self.fixed is not None:
+                rows[r] = self.fixed
+            else:
+                rows[r, 0], rows[r, 1] = j, tokens[j]
+        return rows
+
+
+def test_prefill_prev_rows_by_hand():
+    """Prompt 10..19: the pending token 19 sits at position L = 9; with K = 3
+    the previous-step rows are the target rows at positions 5, 6, 7, 8
+    (tokens 15..18).  A one-position shift either way fails."""
+    target = _Table(32)
+    prev = gen.prefill_prev_logits(target, list(range(10, 20)), 3)
+    assert prev.shape == (4, 32)
+    assert prev[:, :2].tolist() == [[5, 15], [6, 16], [7, 17], [8, 18]]
+    assert not prev[:, 2:].any()
+
+
+def test_mixed_draft_rows_by_hand():
+    """lambda = 0.5, K = 2, V = 4, draft row [2, 0, 0, 0] at every position,
+    previous rows [[0,0,4,0], [0,0,0,8], [1,1,1,1]]: q_1 = [1,0,2,0] (row 0),
+    q_2 = [1,0,0,4] (row 1), so the greedy drafts are 2 then 3.  Mixing with
+    row i instead of row i-1 would propose 3 first."""
+    draft = _Table(4, fixed=np.array([2.0, 0, 0, 0]))
+    target = _Table(4, fixed=np.array([0.0, 0, 0, 1]))
+    prev = np.array([[0.0, 0, 4, 0], [0, 0, 0, 8], [1, 1, 1, 1]])
+    res = gen.spec_step(target, draft, [1, 2, 3], 2, 0.0, 0, 0, prev, 0.5)
+    assert res.q_logits.tolist() == [[1, 0, 2, 0], [1, 0, 0, 4]]
+    assert res.drafts == [2, 3]
+    # the target's argmax is 3 everywhere: draft 2 is rejected and replaced by 3
+    assert res.emitted == [3] and res.n_accepted == 0

@@ -323,6 +323,49 @@ SPEC_API int spec_profile(spec_ctx* ctx, int iters, spec_profile_t* out);
  * too small (after setting *nphases). */
 SPEC_API int spec_phase_times(spec_ctx* ctx, int which, int64_t* out, int max_phases, int* nphases);
 
+/* ---- failure injection (test hooks) ----
+ * The pages describe no failure handling; these hooks let tests drive the
+ * library's own error paths without faulting or hanging a GPU.
+ *
+ * SPEC_FAULT_ALLOC (ctx must be NULL, arg = n >= 1): the n-th device
+ *   allocation of the next spec_init call fails as if the device were out
+ *   of memory; that spec_init returns SPEC_E_OOM after releasing everything
+ *   it had allocated.  The injection applies to that one call (it is
+ *   cleared when the call returns, whether or not it fired).
+ * SPEC_FAULT_WAIT_TIMEOUT (persistent-path context, arg >= 0): with
+ *   arg > 0 every grid barrier of the context's forward kernels waits for
+ *   one arrival more than will ever come and gives up after arg probes,
+ *   raising the context's error flag; the kernels then leave at their first
+ *   barrier, nothing is committed, and the step returns SPEC_E_TIMEOUT with
+ *   the committed state unchanged.  arg = 0 disarms it.  The bound keeps
+ *   every wait finite: no kernel hangs and the context stays usable.
+ * SPEC_FAULT_CLEAR: disarm both (ctx may be NULL).
+ * Errors: SPEC_E_ARG for an unknown kind or a bad argument, SPEC_E_STATE for
+ * SPEC_FAULT_WAIT_TIMEOUT on a context without persistent kernels. */
+#define SPEC_FAULT_CLEAR         0
+#define SPEC_FAULT_ALLOC         1
+#define SPEC_FAULT_WAIT_TIMEOUT  2
+SPEC_API int spec_inject_fault(spec_ctx* ctx, int kind, int arg);
+
+/* Bytes of device memory held by every live context of the process (the
+ * allocations spec_init made and spec_free releases). */
+SPEC_API int64_t spec_device_bytes_held(void);
+
+/* Phase list of one persistent forward pass, for inspection (no device
+ * work): which = 0..K-1 the draft passes of a step, K the verify pass, K+1
+ * the plain-decoding pass.  Writes *nphases and, per phase i, eight int64 at
+ * out[8 i ..]: kind (0 embedding, 1 GEMM, 2 attention), then
+ *   GEMM:      rows n, k, tokens, 16-row output tiles, 1 if a tile's k range
+ *              is split between CTAs (else 0), ring stages, rows per box;
+ *   attention: query heads, KV heads, tokens, work items, 0, 0, head dim;
+ *   embedding: tokens, d_model, tokens, 0, 0, 0, 0.
+ * The geometry depends only on the shapes and the SM count, so a model cut
+ * to fewer layers runs the same per-layer phases as the full-depth model.
+ * out holds max_phases * 8 int64 (host).  Errors: SPEC_E_STATE without the
+ * persistent path, SPEC_E_ARG when max_phases is too small (after setting
+ * *nphases). */
+SPEC_API int spec_phase_list(spec_ctx* ctx, int which, int64_t* out, int max_phases, int* nphases);
+
 /* Library version string. */
 SPEC_API const char* spec_version(void);
 

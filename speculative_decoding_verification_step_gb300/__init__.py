@@ -29,6 +29,9 @@ SPEC_OPT_TIMING = 0x2
 SPEC_OPT_PDL = 0x4
 SPEC_OPT_NO_PERSIST = 0x8
 SPEC_OPT_PHASE_TIMES = 0x10
+SPEC_FAULT_CLEAR = 0
+SPEC_FAULT_ALLOC = 1
+SPEC_FAULT_WAIT_TIMEOUT = 2
 
 _LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
 
@@ -114,6 +117,9 @@ SIGNATURES = {
     "spec_phase_times": (ctypes.c_int, [_VP, ctypes.c_int, _VP, ctypes.c_int,
                                         ctypes.POINTER(ctypes.c_int)]),
     "spec_version": (ctypes.c_char_p, []),
+    "spec_inject_fault": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int]),
+    "spec_phase_list": (ctypes.c_int, [_VP, ctypes.c_int, _VP, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
+    "spec_device_bytes_held": (ctypes.c_int64, []),
 }
 
 _lib = None
@@ -289,11 +295,39 @@ class SpecDecoder:
                                           ctypes.byref(n)), self.ctx)
         return p, q, d, ctx[:n.value].copy()
 
+    def phase_list(self, which):
+        """Phase geometry of persistent forward `which` (0..K-1 draft passes,
+        K verify, K+1 plain decoding): a list of 8-tuples, see spec_phase_list."""
+        import numpy as np
+        buf = np.zeros((4096, 8), dtype=np.int64)
+        n = ctypes.c_int(0)
+        _check(lib().spec_phase_list(self.ctx, which, buf.ctypes.data_as(_VP), 4096, ctypes.byref(n)), self.ctx)
+        return [tuple(int(v) for v in row) for row in buf[:n.value]]
+
+    def inject_fault(self, kind, arg):
+        """Test hook: arm (arg > 0) or disarm (0) a fault of this context
+        (SPEC_FAULT_WAIT_TIMEOUT) -- see include/specverify.h."""
+        _check(lib().spec_inject_fault(self.ctx, kind, arg), self.ctx)
+
     def model_forward(self, which, tokens, pos0, logits):
         """Forward of the target (0) or draft (1) over host token ids at
         positions pos0.. into logits (CUDA fp32 tensor [n, V])."""
         arr = (ctypes.c_int32 * len(tokens))(*[int(t) for t in tokens])
         _check(lib().spec_model_forward(self.ctx, which, arr, len(tokens), pos0, _ptr(logits)), self.ctx)
+
+
+def inject_alloc_failure(n):
+    """Test hook: the n-th device allocation of the next context creation fails."""
+    _check(lib().spec_inject_fault(None, SPEC_FAULT_ALLOC, n))
+
+
+def clear_faults():
+    _check(lib().spec_inject_fault(None, SPEC_FAULT_CLEAR, 0))
+
+
+def device_bytes_held():
+    """Device bytes held by every live context of this process."""
+    return int(lib().spec_device_bytes_held())
 
 
 def accept_rows(p_logits, q_logits, drafts, temperature, seed, step_base=0, stream=None,

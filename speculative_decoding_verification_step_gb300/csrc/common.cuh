@@ -219,6 +219,9 @@ SV_DEV void cp_async16(void* dst, const void* src, bool valid) {
 SV_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 SV_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Load that bypasses the L1 and any earlier cached copy (a flag written by
+// an earlier kernel or another CTA).
+SV_DEV int ld_volatile_i32(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
 // Orders this thread's earlier generic-proxy global accesses with its later
 // bulk-copy (async-proxy) accesses, and the reverse.
 SV_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -34,6 +35,12 @@ using namespace sv;
 namespace {
 
 thread_local std::string g_err = "no error";
+
+// Test hooks (spec_inject_fault): the n-th device allocation of the next
+// spec_init fails (0: off), and the bytes every context holds in device
+// allocations.
+std::atomic<int> g_fail_alloc_at{0};
+std::atomic<long long> g_device_bytes{0};
 
 struct ModelState {
   spec_model_desc d{};
@@ -105,6 +112,7 @@ struct spec_ctx {
   float* attn_part = nullptr;
   int* attn_tick = nullptr;
   int* dattn_tick = nullptr;       // tensor-core attention (bf16 models)
+  int dattn_nt = 0;
   float* ss = nullptr;         // [d_max/16][tok_max] per-tile sums of squares
   float* logits_p = nullptr;  // [K+1][V]
   float* logits_q = nullptr;  // [B][K][V]
@@ -118,7 +126,8 @@ struct spec_ctx {
   int32_t* result = nullptr;
   int32_t* h_result = nullptr;  // pinned host mirror
   int32_t* h_pos = nullptr;     // pinned host scratch for eager positions
-  std::vector<void*> allocs;
+  std::vector<std::pair<void*, size_t>> allocs;
+  int* fault_ctl = nullptr;   // persistent kernels' fault-injection words (PersistDesc::ctl)
   // graphs
   // step and profiling graphs per attention mode (index: grp)
   cudaGraphExec_t step_exec[2] = {nullptr, nullptr};
@@ -166,9 +175,13 @@ int fail(spec_ctx* c, int code, const std::string& msg) {
 template <typename T>
 cudaError_t dalloc(spec_ctx* c, T** p, size_t bytes) {
   void* v = nullptr;
-  cudaError_t e = cudaMalloc(&v, bytes < 16 ? 16 : bytes);
+  const size_t b = bytes < 16 ? 16 : bytes;
+  // an injected allocation failure (tests) behaves like an exhausted device
+  if (g_fail_alloc_at.load() > 0 && g_fail_alloc_at.fetch_sub(1) == 1) return cudaErrorMemoryAllocation;
+  cudaError_t e = cudaMalloc(&v, b);
   if (e != cudaSuccess) return e;
-  c->allocs.push_back(v);
+  c->allocs.emplace_back(v, b);
+  g_device_bytes += (long long)b;
   *p = (T*)v;
   return cudaSuccess;
 }
@@ -535,6 +548,7 @@ void enqueue_verify(Launch& L, bool commit) {
   ad.out_flags = (uint32_t*)(c->result + (size_t)B * (K + 2));
   if (commit) {
     ad.commit_seq = c->seq; ad.commit_len = c->st; ad.commit_step = c->st + 1;
+    ad.err = res_err(c);   // no commit after a forward that gave up
   }
   ad.partials = c->acc_part; ad.tickets = c->acc_tick;
   L.note(launch_accept(ad, c->stream));
@@ -578,6 +592,7 @@ void enqueue_ar_pass(Launch& L, bool commit) {
   sd.position = 0; sd.stream = kStreamAR;
   if (commit) {
     sd.commit_seq = c->seq; sd.commit_len = c->st; sd.commit_step = c->st + 2;
+    sd.err = res_err(c);
   }
   L.note(launch_sample(sd, c->stream));
 }
@@ -638,7 +653,10 @@ void free_ctx(spec_ctx* c) {
     for (cudaGraphExec_t g : pe)
       if (g) cudaGraphExecDestroy(g);
   for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
-  for (void* p : c->allocs) cudaFree(p);
+  for (auto& a : c->allocs) {
+    cudaFree(a.first);
+    g_device_bytes -= (long long)a.second;
+  }
   if (c->h_result) cudaFreeHost(c->h_result);
   if (c->h_pos) cudaFreeHost(c->h_pos);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
@@ -650,6 +668,9 @@ void free_ctx(spec_ctx* c) {
 int persist_timeout(spec_ctx* c) {
   cudaMemsetAsync(res_err(c), 0, sizeof(int32_t), c->stream);
   if (c->bar) cudaMemsetAsync(c->bar, 0, sizeof(unsigned) * 4, c->stream);
+  // kernels that left mid-phase may hold split-tile or attention tickets
+  cudaMemsetAsync(c->gs.tickets, 0, sizeof(int) * c->gs.max_tiles, c->stream);
+  cudaMemsetAsync(c->dattn_tick, 0, sizeof(int) * c->dattn_nt, c->stream);
   cudaStreamSynchronize(c->stream);
   return fail(c, SPEC_E_TIMEOUT, "a bounded wait of a forward kernel (grid barrier or copy) timed out");
 }
@@ -676,6 +697,10 @@ void spec_free(spec_ctx* ctx) { free_ctx(ctx); }
 
 int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K,
               const spec_opts* opts, spec_ctx** out) {
+  // an injected allocation failure applies to this call only, fired or not
+  struct Disarm {
+    ~Disarm() { g_fail_alloc_at = 0; }
+  } disarm;
   if (!out) return fail(nullptr, SPEC_E_ARG, "spec_init: null output pointer");
   *out = nullptr;
   std::string why;
@@ -775,6 +800,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     INIT_TRY(cudaMemset(c->attn_tick, 0, sizeof(int) * nt));
     const int dnt = std::max(dattn_tickets(maxN, c->tgt.d.n_heads, c->tgt.d.n_kv_heads),
                              dattn_tickets(maxN, c->drf.d.n_heads, c->drf.d.n_kv_heads));
+    c->dattn_nt = dnt;
     INIT_TRY(dalloc(c, &c->dattn_tick, sizeof(int) * dnt));
     INIT_TRY(cudaMemset(c->dattn_tick, 0, sizeof(int) * dnt));
   }
@@ -890,6 +916,8 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
         INIT_TRY(cudaMemcpy(tmaps_dev, maps.data(), sizeof(TensorMap128) * maps.size(), cudaMemcpyHostToDevice));
         INIT_TRY(dalloc(c, &c->bar, sizeof(unsigned) * 4));
         INIT_TRY(cudaMemset(c->bar, 0, sizeof(unsigned) * 4));
+        INIT_TRY(dalloc(c, &c->fault_ctl, sizeof(int) * 4));
+        INIT_TRY(cudaMemset(c->fault_ctl, 0, sizeof(int) * 4));
         unsigned long long* times = nullptr;
         if (opts->flags & SPEC_OPT_PHASE_TIMES) {
           const size_t words = (size_t)(K + 4) + (size_t)kPhaseStamps * all.size();
@@ -907,6 +935,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
           pf.desc.tickets = c->gs.tickets;
           pf.desc.bar = c->bar;
           pf.desc.err = res_err(c);
+          pf.desc.ctl = c->fault_ctl;
           const bool drf = f < K || f == K + 2;
           pf.hd = drf ? draft->head_dim : target->head_dim;
           pf.smem = drf ? sm_d : sm_t;
@@ -1241,6 +1270,35 @@ int spec_phase_times(spec_ctx* c, int which, int64_t* out, int max_phases, int* 
   return SPEC_OK;
 }
 
+int spec_phase_list(spec_ctx* c, int which, int64_t* out, int max_phases, int* nphases) {
+  if (!c || !out || !nphases) return fail(c, SPEC_E_ARG, "null argument");
+  if (!c->persist) return fail(c, SPEC_E_STATE, "no persistent forward kernel in this context");
+  if (which < 0 || which > c->K + 1) return fail(c, SPEC_E_ARG, "which must be in [0, K+1]");
+  const PersistFwd& f = c->pforward[which];
+  const int n = (int)f.host.size();
+  *nphases = n;
+  if (max_phases < n) return fail(c, SPEC_E_ARG, "max_phases below the number of phases");
+  for (int i = 0; i < n; ++i) {
+    const PhaseDesc& d = f.host[i];
+    int64_t* o = out + 8 * (size_t)i;
+    o[0] = d.kind;
+    if (d.kind == kPhaseGemm) {
+      o[1] = d.g.n; o[2] = d.g.k; o[3] = d.g.ntok;
+      o[4] = gemm_tiles(d.g);
+      o[5] = d.whole ? 0 : 1;   // some 16-row tile split between CTAs
+      o[6] = d.stages;
+      o[7] = d.R;
+    } else if (d.kind == kPhaseAttn) {
+      o[1] = d.a.hq; o[2] = d.a.hkv; o[3] = d.a.ntok; o[4] = d.attn_items;
+      o[5] = o[6] = 0; o[7] = d.a.hd;
+    } else {
+      o[1] = d.e.ntok; o[2] = d.e.d; o[3] = d.e.ntok;
+      o[4] = o[5] = o[6] = o[7] = 0;
+    }
+  }
+  return SPEC_OK;
+}
+
 int spec_model_forward(spec_ctx* c, int which, const int32_t* tokens, int n, int pos0,
                        float* logits_dev) {
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
@@ -1322,5 +1380,37 @@ int spec_sample_rows(const float* logits, int64_t row_stride, int rows, int V, f
   if (e2 != cudaSuccess) return fail(nullptr, SPEC_E_CUDA, std::string("spec_sample_rows: ") + cudaGetErrorString(e2));
   return SPEC_OK;
 }
+
+int spec_inject_fault(spec_ctx* c, int kind, int arg) {
+  if (kind == SPEC_FAULT_CLEAR) {
+    g_fail_alloc_at = 0;
+    if (c && c->fault_ctl) {
+      const int z[2] = {0, 0};
+      CUDA_TRY(c, cudaMemcpyAsync(c->fault_ctl, z, sizeof z, cudaMemcpyHostToDevice, c->stream));
+      CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+    }
+    return SPEC_OK;
+  }
+  if (kind == SPEC_FAULT_ALLOC) {
+    if (c) return fail(c, SPEC_E_ARG, "SPEC_FAULT_ALLOC applies to the next spec_init: pass a NULL context");
+    if (arg < 1) return fail(nullptr, SPEC_E_ARG, "SPEC_FAULT_ALLOC needs arg >= 1");
+    g_fail_alloc_at = arg;
+    return SPEC_OK;
+  }
+  if (kind == SPEC_FAULT_WAIT_TIMEOUT) {
+    if (!c) return fail(nullptr, SPEC_E_ARG, "SPEC_FAULT_WAIT_TIMEOUT needs a context");
+    if (!c->fault_ctl) return fail(c, SPEC_E_STATE, "no persistent forward kernel in this context");
+    if (arg < 0) return fail(c, SPEC_E_ARG, "SPEC_FAULT_WAIT_TIMEOUT needs arg >= 0");
+    // arg > 0: every grid barrier waits for one arrival more than will come,
+    // giving up after arg probes; 0: disarmed
+    const int w[2] = {arg > 0 ? 1 : 0, arg};
+    CUDA_TRY(c, cudaMemcpyAsync(c->fault_ctl, w, sizeof w, cudaMemcpyHostToDevice, c->stream));
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+    return SPEC_OK;
+  }
+  return fail(c, SPEC_E_ARG, "unknown fault kind");
+}
+
+int64_t spec_device_bytes_held(void) { return (int64_t)g_device_bytes.load(); }
 
 }  // extern "C"

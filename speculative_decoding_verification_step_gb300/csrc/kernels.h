@@ -212,6 +212,7 @@ struct SampleDesc {
   int32_t* commit_seq;
   int32_t* commit_len;
   int32_t* commit_step;     // incremented when committing
+  const int32_t* err;       // optional: the commit is skipped while *err != 0 (a forward gave up)
   // batch = 1: row r is sequence r of a batch -- step = step_dev[r * st_ld] +
   // step_base with Philox row word r, the token goes to out_token[r * out_ld +
   // (out_idx ? out_idx[r * st_ld] : 0) + out_off], and the commit uses
@@ -245,6 +246,7 @@ struct AcceptDesc {
   int32_t* commit_seq;
   int32_t* commit_len;
   int32_t* commit_step;
+  const int32_t* err;       // optional: the commit is skipped while *err != 0 (a forward gave up)
   // batch = 1: row r is sequence r -- step = step_dev[r * st_ld] + step_base
   // with Philox row word r, drafts at drafts + r * seq_ld + (drafts_idx ?
   // drafts_idx[r * st_ld] : 0) + drafts_off, commit into commit_seq + r * seq_ld,
@@ -308,6 +310,10 @@ struct PersistDesc {
   int* tickets;
   unsigned* bar;             // [1] arrival count (zero at start; the kernel leaves it zero)
   int* err;                  // set to 1 when a wait gives up
+  // optional fault injection (null: off): [0] arrivals added to every grid-
+  // barrier target (> 0: a barrier that cannot complete), [1] grid-barrier
+  // probe limit (0: the default bound); read once at kernel start
+  const int* ctl;
   // optional (null: off): [1 + kPhaseStamps * nphases] globaltimer stamps,
   // zeroed before the launch -- start, then per phase the earliest arrival
   // (stored as ~t, atomicMax), the latest arrival (atomicMax), CTA 0's

@@ -61,12 +61,12 @@ SV_DEV void grid_arrive(unsigned* bar) {
   if (threadIdx.x == 0) red_add_release_gpu(bar, 1u);
 }
 
-SV_DEV bool grid_wait(unsigned* bar, unsigned target, int* err, int* s_ok) {
+SV_DEV bool grid_wait(unsigned* bar, unsigned target, int* err, int* s_ok, long long limit) {
   if (threadIdx.x == 0) {
     int ok = 1;
     long long spins = 0;
     while (ld_acquire_u32(bar) < target) {
-      if (++spins > kBarrierSpinLimit) {
+      if (++spins > limit) {
         atomicExch(err, 1);
         ok = 0;
         break;
@@ -113,6 +113,14 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   };
   unsigned long long* const times = p.times;
   if (times && blockIdx.x == 0 && threadIdx.x == 0) times[0] = global_ns();
+  // fault injection (tests): extra arrivals to wait for, and the probe bound
+  unsigned bar_extra = 0;
+  long long bar_limit = kBarrierSpinLimit;
+  if (p.ctl && threadIdx.x == 0) {
+    bar_extra = (unsigned)max(0, ld_volatile_i32(p.ctl));
+    const int lim = ld_volatile_i32(p.ctl + 1);
+    if (lim > 0) bar_limit = lim;
+  }
   tma_init(tp);
   dattn_init_bars(dbars);
   unsigned dpar = 0;   // attention: per-warp stage parities
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
         if (lane == 0) npre = tma_prefetch(nx, tp, ring, xreg, maps);
         npre = __shfl_sync(0xffffffffu, npre, 0);
       }
-      if (!grid_wait(p.bar, (unsigned)(ph + 1) * gridDim.x, p.err, &s_ok)) {
+      if (!grid_wait(p.bar, (unsigned)(ph + 1) * gridDim.x + bar_extra, p.err, &s_ok, bar_limit)) {
         tma_drain(tp);
         return;
       }

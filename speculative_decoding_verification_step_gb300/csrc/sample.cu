@@ -326,10 +326,13 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
     tok = rescan_chunk(sh, wfn, s.V);
   }
   if (threadIdx.x == 0) {
+    // a forward that gave up (err raised) produced no logits to commit: the
+    // draw is still written out, but the committed state stays as it was
+    const bool commit = s.commit_seq && !(s.err && ld_volatile_i32(s.err) != 0);
     if (s.batch) {
       const size_t so = (size_t)r * s.seq_ld, io = (size_t)r * s.st_ld;
       s.out_token[(size_t)r * s.out_ld + (s.out_idx ? s.out_idx[io] : 0) + s.out_off] = tok;
-      if (s.commit_seq) {
+      if (commit) {
         const int len = s.commit_len[io];
         s.commit_seq[so + len + 1] = tok;
         s.commit_len[io] = len + 1;
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
       }
     } else {
       s.out_token[(s.out_idx ? *s.out_idx : 0) + s.out_off + r] = tok;
-      if (s.commit_seq) {
+      if (commit) {
         const int len = *s.commit_len;
         s.commit_seq[len + 1] = tok;
         *s.commit_len = len + 1;
@@ -526,7 +529,9 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
     for (int i = n + 1; i <= K; ++i) out[i] = -1;
     a.out_count[r] = n + 1;
     if (a.out_flags) a.out_flags[r] = flags;
-    if (a.commit_seq) {
+    // a forward that gave up (err raised) left no valid logits: nothing is
+    // committed, so the context keeps its committed length and step counter
+    if (a.commit_seq && !(a.err && ld_volatile_i32(a.err) != 0)) {
       int32_t* cs = a.commit_seq + (a.batch ? (size_t)r * a.seq_ld : 0);
       const int len = a.commit_len[io];
       for (int i = 0; i <= n; ++i) cs[len + 1 + i] = out[i];

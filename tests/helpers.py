@@ -4,6 +4,7 @@ import torch
 
 import speculative_decoding_verification_step_gb300 as sv
 from oracle import accept as acc
+from oracle import generate as gen
 
 SKIP_FLAGS = acc.FLAG_NEAR_EDGE | acc.FLAG_NEAR_RATIO | acc.FLAG_NEAR_TIE | acc.FLAG_RESID_ZERO
 
@@ -42,3 +43,56 @@ def equal_mass_bins(p, nbins):
     out = np.empty_like(ids)
     out[order] = ids
     return out
+
+
+def teacher_forced(dec, T, D, prompt, k, temp, n_new, tol, mix=0.0, seed=0, max_ctx=256, tie=None):
+    """Run speculative steps on the GPU decoder `dec` (already built, not yet
+    prefilled) and check each one against the oracle models T (target) and D
+    (draft), starting every oracle step from the GPU's committed context:
+
+    * stage (i): the draft rows up to the first draft that differs from the
+      oracle's own, and the K+1 target rows when every draft agrees, within
+      `tol` of the oracle's forward;
+    * drafts: each is the oracle's inverse-CDF draw (argmax at T = 0) on the
+      GPU's own draft row with the step's Philox uniform -- exact except
+      flagged near-edge / near-tie draws;
+    * stage (ii): the oracle's acceptance on the GPU's logits and drafts gives
+      the GPU's emitted tokens, exactly, except flagged draws;
+    * the committed context grows by exactly the emitted tokens.
+
+    Returns (tokens, steps, skipped)."""
+    tie = 2 * tol if tie is None else tie
+    dec.prefill(prompt)
+    ctx = [int(t) for t in prompt]
+    prev = gen.prefill_prev_logits(T, ctx, k) if mix else None
+    out, step, skipped, tokens = 0, 0, 0, []
+    while out < n_new:
+        toks, _ = dec.step()
+        p, q, d, context = dec.last_step_debug(max_ctx)
+        assert 1 <= len(toks) <= k + 1
+        ref = gen.spec_step(T, D, ctx, k, temp, seed, step, prev, mix, tie_eps=tie)
+        same = 0
+        while same < k and ref.drafts[same] == int(d[same]):
+            same += 1
+        upto = min(k, same + 1)
+        err_q = np.abs(q[:upto] - ref.q_logits[:upto]).max()
+        assert err_q < tol, (step, err_q)
+        if same == k:
+            err_p = np.abs(p - ref.p_logits).max()
+            assert err_p < tol, (step, err_p)
+        for i in range(k):
+            dg, fl = gen.draft_token(q[i], temp, seed, step, i + 1, tie_eps=0.0)
+            if not fl & SKIP_FLAGS:
+                assert dg == int(d[i]), (step, i, dg, int(d[i]))
+        em, n, fl = gen.verify(p, q, list(d), temp, seed, step, tie_eps=0.0)
+        if fl & SKIP_FLAGS:
+            skipped += 1
+        else:
+            assert em == toks, (step, em, toks)
+        assert [int(t) for t in context[len(ctx):]] == toks
+        ctx = [int(t) for t in context]
+        prev = p.astype(np.float64)
+        tokens += toks
+        out += len(toks)
+        step += 1
+    return tokens, step, skipped

@@ -134,3 +134,14 @@ def test_binding_refuses_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(sv, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         sv.lib()
+
+
+def test_fault_hook_argument_errors(L):
+    """spec_inject_fault checks its arguments before any device work; with no
+    context and no allocation, no device memory is held."""
+    assert L.spec_inject_fault(None, 99, 0) == -1                       # unknown kind
+    assert L.spec_inject_fault(None, sv.SPEC_FAULT_ALLOC, 0) == -1      # n >= 1
+    assert L.spec_inject_fault(None, sv.SPEC_FAULT_WAIT_TIMEOUT, 5) == -1   # needs a context
+    assert L.spec_inject_fault(None, sv.SPEC_FAULT_ALLOC, 3) == 0
+    assert L.spec_inject_fault(None, sv.SPEC_FAULT_CLEAR, 0) == 0
+    assert L.spec_device_bytes_held() == 0

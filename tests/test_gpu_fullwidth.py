@@ -1,0 +1,121 @@
+"""Oracle parity at the widths the benchmark runs, on models cut to 2 layers.
+
+Target: the 8B shape (d 4096, 32 query / 8 KV heads of 128, FFN 14336,
+vocabulary 128256, RoPE theta 500000) with 2 decoder layers; draft: the 1B
+shape (d 2048, heads of 64, FFN 8192, the same vocabulary) with 2 layers.
+Every GEMM, attention and LM-head phase of these passes has exactly the
+geometry (work split, ring, boxes) of the full-depth pair -- the split is a
+function of the matrix shapes and the SM count only -- which the first test
+checks against full-depth contexts whose layers alias one layer's weights.
+
+The speculative steps run the persistent kernels (draft passes, verify pass)
+and are checked step by step against the fp64 oracle (see
+helpers.teacher_forced): logits within 2e-2, drafts and emitted tokens exact
+except flagged near-boundary draws, at T in {0, 1} and lambda in {0, 0.5},
+K = 5.  Plain decoding on the same kernels is checked the same way.
+
+The oracle reads the same weight bits as the GPU; its copies of the matrices
+are widened to fp64 once, up front (an exact conversion), so that each
+oracle forward does not widen 1 GB of LM head again.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import helpers
+import speculative_decoding_verification_step_gb300 as sv
+import workloads
+from oracle import generate as gen
+
+pytestmark = pytest.mark.gpu
+
+W8 = replace(workloads.EIGHT_B, n_layers=2)
+W1 = replace(workloads.ONE_B, n_layers=2)
+K = 5
+TOL = 2e-2
+
+
+def _oracle_copy(w):
+    return {"embed": w["embed"].cpu(), "final_norm": w["final_norm"].cpu().double(),
+            "lm_head": w["lm_head"].cpu().double(),
+            "layers": [{k: v.cpu().double() for k, v in lw.items()} for lw in w["layers"]]}
+
+
+@pytest.fixture(scope="module")
+def pair():
+    sv.build()
+    sv.lib()
+    tw = workloads.make_weights(W8, seed=31, device="cuda")
+    dw = workloads.make_weights(W1, seed=32, device="cuda")
+    return tw, dw, gen.Model(W8, _oracle_copy(tw)), gen.Model(W1, _oracle_copy(dw))
+
+
+def test_phase_geometry_matches_full_depth(pair):
+    """Each persistent pass of the 2-layer pair runs the same distinct phases
+    (GEMM rows, k, tokens, tiles, split, ring stages, box rows; attention
+    items) as the 32-layer 8B / 16-layer 1B pair, including the 128256-row
+    LM-head phases."""
+    tw, dw, _, _ = pair
+    full_t = dict(tw, layers=[tw["layers"][0]] * workloads.EIGHT_B.n_layers)
+    full_d = dict(dw, layers=[dw["layers"][0]] * workloads.ONE_B.n_layers)
+    small = sv.SpecDecoder(W8, tw, W1, dw, K, 128, temperature=1.0)
+    big = sv.SpecDecoder(workloads.EIGHT_B, full_t, workloads.ONE_B, full_d, K, 128, temperature=1.0)
+    try:
+        for which in range(K + 2):
+            a, b = small.phase_list(which), big.phase_list(which)
+            assert set(a) == set(b), which
+            nl = W1.n_layers if which < K else W8.n_layers
+            nb = workloads.ONE_B.n_layers if which < K else workloads.EIGHT_B.n_layers
+            assert (len(a) - 2) // 5 == nl and (len(b) - 2) // 5 == nb
+        verify = small.phase_list(K)
+        gemms = [p for p in verify if p[0] == 1]
+        assert (1, 128256, 4096, K + 1) == gemms[-1][:4]
+        assert {(p[1], p[2]) for p in gemms} == {(6144, 4096), (4096, 4096), (14336, 4096), (4096, 14336),
+                                                (128256, 4096)}
+        draft = small.phase_list(1)
+        assert [p for p in draft if p[0] == 1][-1][:4] == (1, 128256, 2048, 1)
+        print("verify GEMM phases (n, k, tok, tiles, split, stages, box rows):",
+              sorted({p[1:] for p in gemms}))
+    finally:
+        small.close()
+        big.close()
+
+
+@pytest.mark.parametrize("temp,mix", [(0.0, 0.0), (1.0, 0.0), (0.0, 0.5), (1.0, 0.5)])
+def test_steps_teacher_forced_full_width(pair, temp, mix):
+    tw, dw, T, D = pair
+    prompt = workloads.make_prompt(W8.vocab, 24, seed=33)[0].tolist()
+    dec = sv.SpecDecoder(W8, tw, W1, dw, K, 128, temperature=temp, seed=7, mix_lambda=mix)
+    try:
+        _, steps, skipped = helpers.teacher_forced(dec, T, D, prompt, K, temp, 12, TOL, mix=mix, seed=7,
+                                                   max_ctx=128)
+        assert skipped <= max(1, steps // 3)
+    finally:
+        dec.close()
+
+
+@pytest.mark.parametrize("temp", [0.0, 1.0])
+def test_plain_decoding_full_width(pair, temp):
+    tw, dw, T, _ = pair
+    prompt = workloads.make_prompt(W8.vocab, 20, seed=34)[0].tolist()
+    dec = sv.SpecDecoder(W8, tw, W1, dw, K, 128, temperature=temp, seed=8)
+    try:
+        dec.prefill(prompt)
+        ctx, skipped = list(prompt), 0
+        for s in range(6):
+            tok = dec.ar_step()
+            p, _, _, context = dec.last_step_debug(128)
+            ref = T.logits(ctx, last=1)[0]
+            err = np.abs(p[0] - ref).max()
+            assert err < TOL, (s, err)
+            exp, fl = gen.ar_token_flagged(p[0], temp, 8, s, tie_eps=0.0)
+            if fl & helpers.SKIP_FLAGS:
+                skipped += 1
+            else:
+                assert exp == tok, (s, exp, tok)
+            assert [int(t) for t in context] == ctx + [tok]
+            ctx.append(tok)
+        assert skipped <= 2
+    finally:
+        dec.close()

@@ -75,50 +75,12 @@ def _tiny_pair():
 def _teacher_forced(shape, w, dshape, dw, prompt, k, temp, n_new, mix=0.0, seed=0, max_ctx=256):
     dec = helpers.decoder(shape, helpers.to_device(w), dshape, helpers.to_device(dw), k, max_ctx,
                           temperature=temp, seed=seed, mix=mix)
-    dec.prefill(prompt)
-    T, D = gen.Model(shape, w), gen.Model(dshape, dw)
-    tol = helpers.logit_tol(shape)
-    ctx = list(prompt)
-    prev = gen.prefill_prev_logits(T, ctx, k) if mix else None
-    out, step, skipped, tokens = 0, 0, 0, []
-    while out < n_new:
-        toks, _ = dec.step()
-        p, q, d, context = dec.last_step_debug(max_ctx)
-        assert 1 <= len(toks) <= k + 1
-        ref = gen.spec_step(T, D, ctx, k, temp, seed, step, prev, mix, tie_eps=helpers.tie_eps(shape))
-        # stage (i): logits of the draft rows up to the first differing draft,
-        # and of the target rows when every draft agrees
-        same = 0
-        while same < k and ref.drafts[same] == int(d[same]):
-            same += 1
-        upto = min(k, same + 1)
-        assert np.abs(q[:upto] - ref.q_logits[:upto]).max() < tol
-        if same == k:
-            assert np.abs(p - ref.p_logits).max() < tol
-        # drafts: each is the inverse-CDF draw (argmax at T = 0) of the GPU's
-        # own draft row with the step's Philox uniform -- exact, except
-        # flagged near-edge / near-tie draws.  (The oracle's own drafts may
-        # differ where the in-tolerance logit error moved a draw across a bin
-        # edge; its logits were compared above up to the first such draft.)
-        for i in range(k):
-            dg, fl = gen.draft_token(q[i], temp, seed, step, i + 1, tie_eps=0.0)
-            if not fl & helpers.SKIP_FLAGS:
-                assert dg == int(d[i]), (step, i, dg, int(d[i]))
-        # stage (ii): acceptance on the GPU's logits reproduces the GPU's tokens
-        # (same fp32 logits on both sides: argmax ties are exact, no tie window)
-        em, n, fl = gen.verify(p, q, list(d), temp, seed, step, tie_eps=0.0)
-        if fl & helpers.SKIP_FLAGS:
-            skipped += 1
-        else:
-            assert em == toks, (step, em, toks)
-        assert [int(t) for t in context[len(ctx):]] == toks
-        ctx = [int(t) for t in context]
-        prev = p.astype(np.float64)
-        tokens += toks
-        out += len(toks)
-        step += 1
-    dec.close()
-    return tokens, step, skipped
+    try:
+        return helpers.teacher_forced(dec, gen.Model(shape, w), gen.Model(dshape, dw), prompt, k, temp,
+                                      n_new, helpers.logit_tol(shape), mix=mix, seed=seed, max_ctx=max_ctx,
+                                      tie=helpers.tie_eps(shape))
+    finally:
+        dec.close()
 
 
 @pytest.mark.parametrize("temp", [0.0, 1.0])
@@ -218,6 +180,41 @@ def test_greedy_spec_equals_greedy_ar(shape):
     assert spec == ar
     st = dec.stats()
     assert st["ar_steps"] == 60
+    dec.close()
+
+
+@pytest.mark.parametrize("temp", [0.0, 1.0])
+@pytest.mark.parametrize("shape", SHAPES[:2], ids=lambda s: f"{s.name}-{s.dtype}")
+def test_ar_step_teacher_forced(shape, temp):
+    """Plain decoding (spec_ar_step, the speedup's denominator) against the
+    oracle step by step: each pass's logits within tolerance of the oracle's
+    forward on the GPU's committed context, and the token the oracle's
+    plain-decoding draw (argmax, or inverse CDF with the step's stream-4
+    uniform) takes on the GPU's logits -- exact except flagged draws."""
+    w = workloads.make_weights(shape, seed=9)
+    dshape, dw = workloads.prefix_draft(shape, w, 1)
+    wc = helpers.to_device(w)
+    dwc = {**wc, "layers": wc["layers"][:1]}
+    dec = helpers.decoder(shape, wc, dshape, dwc, 4, 128, temperature=temp, seed=5)
+    prompt = workloads.make_prompt(shape.vocab, 20, seed=10)[0].tolist()
+    dec.prefill(prompt)
+    T = gen.Model(shape, w)
+    tol = helpers.logit_tol(shape)
+    ctx, skipped = list(prompt), 0
+    for s in range(16):
+        tok = dec.ar_step()
+        p, _, _, context = dec.last_step_debug(128)
+        ref = T.logits(ctx, last=1)[0]
+        assert np.abs(p[0] - ref).max() < tol, s
+        exp, fl = gen.ar_token_flagged(p[0], temp, 5, s, tie_eps=0.0)
+        if fl & helpers.SKIP_FLAGS:
+            skipped += 1
+        else:
+            assert exp == tok, (s, exp, tok)
+        assert [int(t) for t in context] == ctx + [tok]
+        ctx.append(tok)
+    assert skipped <= 3
+    assert dec.stats()["ar_steps"] == 16
     dec.close()
 
 

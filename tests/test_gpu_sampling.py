@@ -123,7 +123,8 @@ def test_accept_worked_example():
 @pytest.mark.parametrize("sigma", [0.25, 0.5, 1.0, 2.0])
 def test_accept_full_vocab_1024_rows(sigma):
     """Acceptance-kernel workload at full size: 1024 rows, V = 128256, K = 5.
-    The oracle checks a sample of rows one by one; every count is in 1..K+1."""
+    The oracle checks every row (tokens and counts exact except flagged
+    near-boundary draws); every count is in 1..K+1."""
     R, K, V = 1024, 5, 128256
     pc, qc = workloads.make_accept_rows(R, K, V, sigma, seed=int(sigma * 100), device="cuda")
     d = _draft_tokens(qc, 1.0, seed=11)
@@ -131,18 +132,20 @@ def test_accept_full_vocab_1024_rows(sigma):
     torch.cuda.synchronize()
     cn = counts.cpu().numpy()
     assert cn.min() >= 1 and cn.max() <= K + 1
-    sample = np.random.default_rng(0).choice(R, 24, replace=False)
-    idx = torch.as_tensor(sample, device="cuda")
-    ps, qs = pc[idx].double().cpu().numpy(), qc[idx].double().cpu().numpy()
-    ds, ts, cs = d[idx].cpu().numpy(), tokens[idx].cpu().numpy(), counts[idx].cpu().numpy()
+    ds, ts = d.cpu().numpy(), tokens.cpu().numpy()
     skipped = 0
-    for j, r in enumerate(sample):
-        em, n, fl = gen.verify(ps[j], qs[j], list(ds[j]), 1.0, 11, int(r), tie_eps=0.0)
-        if fl & helpers.SKIP_FLAGS:
-            skipped += 1
-            continue
-        assert list(ts[j][:cs[j]]) == em
-    assert skipped <= 6
+    for c0 in range(0, R, 64):   # host copies in chunks of 64 rows
+        ps = pc[c0:c0 + 64].cpu().numpy()
+        qs = qc[c0:c0 + 64].cpu().numpy()
+        for j in range(ps.shape[0]):
+            r = c0 + j
+            em, n, fl = gen.verify(ps[j], qs[j], list(ds[r]), 1.0, 11, r, tie_eps=0.0)
+            if fl & helpers.SKIP_FLAGS:
+                skipped += 1
+                continue
+            assert int(cn[r]) == n + 1, (r, int(cn[r]), n)
+            assert list(ts[r][:cn[r]]) == em, r
+    assert skipped <= R // 20
     alpha = (cn - 1).sum() / (cn - 1 + (cn <= K)).sum()
     print(f"sigma={sigma}: per-draft acceptance {alpha:.3f}, mean tokens/step {cn.mean():.3f}")
 

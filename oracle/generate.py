@@ -37,9 +37,10 @@ from .philox import (STREAM_ACCEPT, STREAM_AR, STREAM_BONUS, STREAM_DRAFT,
 class Model:
     shape: object
     weights: dict
+    act: str = "f64"     # "bf16": a bf16 model's dataflow (see oracle.model)
 
     def logits(self, tokens, last):
-        return model.forward(self.shape, self.weights, tokens, last=last).numpy()
+        return model.forward(self.shape, self.weights, tokens, last=last, act=self.act).numpy()
 
 
 @dataclass

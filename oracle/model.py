@@ -19,6 +19,23 @@ these readings where they are silent:
 Every position is recomputed from the token ids each call (the plain
 definition of causal self-attention); nothing is cached.  Weights are read
 exactly as given (bf16 or fp32 bits) and widened to fp64.
+
+Two precisions (``act``):
+
+* ``"f64"`` (default): the definition, every activation in fp64.
+* ``"bf16"``: the dataflow of a bf16 model with fp32 accumulation -- the
+  precision the benchmark's bf16 models are specified in.  Arithmetic stays
+  fp64 (more exact than fp32 accumulation); activations are rounded to bf16
+  (round to nearest even) where a bf16 model stores them between
+  operations: every GEMM input (an RMSNorm'd input as bf16(x * gain), its
+  1/rms applied to the GEMM's sums -- the same product as normalising
+  first), q, k and v where attention reads them, the attention output and
+  the SwiGLU output.  The residual stream, norms, RoPE, the softmax and its
+  probabilities stay unrounded (the probabilities that weight v are kept to
+  ~16 significant bits, a bf16 pair; rounded to one bf16 they would move a
+  4096-wide model's logits by up to ~0.05, by an amount that depends on the
+  order the keys are visited in).  With the rounding replaced by the
+  identity this mode is the definition itself (a pinned property).
 """
 import math
 
@@ -68,40 +85,81 @@ def causal_attention(q, k, v):
     return out
 
 
+def causal_attention_rounded(q, k, v, rnd):
+    """causal_attention in a bf16 model's dataflow: q, k and v as rnd(q),
+    rnd(k), rnd(v); the softmax unrounded.  With rnd = identity this is
+    causal_attention."""
+    return causal_attention(rnd(q), rnd(k), rnd(v))
+
+
 def silu(x):
     return x / (1.0 + torch.exp(-x))
 
 
-def decoder_layer(x, lw, shape, positions):
+def round_bf16(t):
+    """Round fp64 values to the nearest bf16 (ties to even), widened back."""
+    return t.to(torch.bfloat16).to(F64)
+
+
+def _identity(t):
+    return t
+
+
+def _norm_input(x, gain, eps, rnd):
+    """An RMSNorm'd GEMM input as (a, s) with rms_norm(x) = a * s, the GEMM
+    applied to a and its sums scaled by s.  Definition (rnd None): a = the
+    normalised x, s = 1.  bf16 dataflow: a = rnd(x * gain), s = 1 / rms(x)."""
+    if rnd is None:
+        return rms_norm(x, gain, eps), 1.0
+    inv = 1.0 / torch.sqrt((x * x).mean(dim=-1, keepdim=True) + eps)
+    return rnd(x * _w(gain)), inv
+
+
+def decoder_layer(x, lw, shape, positions, rnd=None):
+    """One pre-norm block.  rnd None: the fp64 definition; else the rounding
+    of the bf16 dataflow (see the module docstring)."""
     n = x.shape[0]
     hq, hkv, hd = shape.n_heads, shape.n_kv_heads, shape.head_dim
-    a = rms_norm(x, lw["attn_norm"], shape.rms_eps)
-    q = (a @ _w(lw["wq"]).T).view(n, hq, hd)
-    k = (a @ _w(lw["wk"]).T).view(n, hkv, hd)
-    v = (a @ _w(lw["wv"]).T).view(n, hkv, hd)
+    a, sa = _norm_input(x, lw["attn_norm"], shape.rms_eps, rnd)
+    q = ((a @ _w(lw["wq"]).T) * sa).view(n, hq, hd)
+    k = ((a @ _w(lw["wk"]).T) * sa).view(n, hkv, hd)
+    v = ((a @ _w(lw["wv"]).T) * sa).view(n, hkv, hd)
     q = apply_rope(q, positions, shape.rope_theta)
     k = apply_rope(k, positions, shape.rope_theta)
-    o = causal_attention(q, k, v).reshape(n, hq * hd)
+    if rnd is None:
+        o = causal_attention(q, k, v).reshape(n, hq * hd)
+    else:
+        o = rnd(causal_attention_rounded(q, k, v, rnd).reshape(n, hq * hd))
     x = x + o @ _w(lw["wo"]).T
-    b = rms_norm(x, lw["ffn_norm"], shape.rms_eps)
-    h = silu(b @ _w(lw["w_gate"]).T) * (b @ _w(lw["w_up"]).T)
+    b, sb = _norm_input(x, lw["ffn_norm"], shape.rms_eps, rnd)
+    h = silu((b @ _w(lw["w_gate"]).T) * sb) * ((b @ _w(lw["w_up"]).T) * sb)
+    if rnd is not None:
+        h = rnd(h)
     return x + h @ _w(lw["w_down"]).T
 
 
-def forward(shape, weights, tokens, last=None):
+ACT_ROUNDING = {"f64": None, "bf16": round_bf16}
+
+
+def forward(shape, weights, tokens, last=None, act="f64", rnd=None):
     """Logits [n, V] (fp64) at every position of ``tokens`` (positions 0..n-1).
 
     ``last``: if given, only the logits of the last ``last`` positions are
     returned (the LM head is applied to those rows only; the hidden states of
     all positions are still recomputed from scratch).
+    ``act``: "f64" (the definition) or "bf16" (a bf16 model's dataflow, see
+    the module docstring).  ``rnd`` overrides the dataflow's rounding function
+    (tests replace it by the identity).
     """
+    if rnd is None:
+        rnd = ACT_ROUNDING[act]
     tok = torch.as_tensor(tokens, dtype=torch.long).reshape(-1)
     n = tok.numel()
     positions = torch.arange(n)
     x = _w(weights["embed"][tok.to(weights["embed"].device)])
     for lw in weights["layers"]:
-        x = decoder_layer(x, lw, shape, positions)
+        x = decoder_layer(x, lw, shape, positions, rnd)
     if last is not None:
         x = x[n - last:]
-    x = rms_norm(x, weights["final_norm"], shape.rms_eps)
-    return x @ _w(weights["lm_head"]).T
+    a, s = _norm_input(x, weights["final_norm"], shape.rms_eps, rnd)
+    return (a @ _w(weights["lm_head"]).T) * s

@@ -65,8 +65,9 @@ struct DAttnSmem {
   static constexpr int kVBoxCols = kVDims < 64 ? kVDims : 64;
   static constexpr int kVBoxes = kVDims / kVBoxCols;
   static constexpr int kStageElems = kTileElems + kVTileElems;   // K tile, then V tile
-  // (NT probability tiles of [8 rows][16 keys]: wide items, NT x 8 rows)
-  static constexpr size_t kWarpRaw = (size_t)kDepth * kStageElems * 2 + NT * kDRows * kDStepKeys * 2;
+  // (the probabilities as a bf16 pair, high then low parts: 2 x NT tiles of
+  // [8 rows][16 keys]; wide items have NT x 8 rows)
+  static constexpr size_t kWarpRaw = (size_t)kDepth * kStageElems * 2 + 2 * NT * kDRows * kDStepKeys * 2;
   static constexpr size_t kWarpBytes = (kWarpRaw + 1023) / 1024 * 1024;
   // merge area: m, l [8 warps][8 NT rows], o [8 warps][8 NT rows][kVDims] (fp32)
   static constexpr size_t kMergeBytes = (size_t)kDWarps * NT * kDRows * (2 + kVDims) * 4;
@@ -97,6 +98,17 @@ SV_DEV void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
 SV_DEV uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// A probability p as the bf16 pair (h, l) = (bf16(p), bf16(p - h)): h + l
+// equals p to about 2^-17 relative, so P.V over both parts (two MMAs) keeps
+// the probabilities at nearly fp32 precision -- rounding them to one bf16
+// moves the logits of a 4096-wide model by up to ~0.05, and by an amount that
+// depends on the running maximum each key was scaled by.
+SV_DEV void store_prob(bf16* hi_tile, bf16* lo_tile, int idx, float p) {
+  const bf16 h = __float2bfloat16_rn(p);
+  hi_tile[idx] = h;
+  lo_tile[idx] = __float2bfloat16_rn(p - __bfloat162float(h));
 }
 
 // Item geometry.
@@ -230,7 +242,8 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, unsigned char* sm, int* s
   // stage b of the warp: K tile at wb + b * kStageElems, V tile after it
   constexpr int D = L::kDepth;
   bf16* wb = reinterpret_cast<bf16*>(sm + (size_t)warp * L::kWarpBytes);
-  bf16* ps = wb + D * L::kStageElems;                 // [8 rows][16 keys]
+  bf16* ps = wb + D * L::kStageElems;                 // [8 rows][16 keys], high parts
+  bf16* pl = ps + kDRows * kDStepKeys;                // low parts
 
   // this warp's steps: s = first + 8j, j < nst, kept D steps ahead in flight
   const int s_begin = k0 / kDStepKeys, s_end = last / kDStepKeys;
@@ -331,14 +344,16 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, unsigned char* sm, int* s
       l_r[1] = l_r[1] * sc1 + ls1;
       m_r[1] = mn1;
     }
-    // probabilities as bf16, [row][key]
-    ps[(2 * ci) * kDStepKeys + gi] = __float2bfloat16_rn(p00);
-    ps[(2 * ci + 1) * kDStepKeys + gi] = __float2bfloat16_rn(p01);
-    ps[(2 * ci) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p10);
-    ps[(2 * ci + 1) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p11);
+    // probabilities as bf16 pairs, [row][key]
+    store_prob(ps, pl, (2 * ci) * kDStepKeys + gi, p00);
+    store_prob(ps, pl, (2 * ci + 1) * kDStepKeys + gi, p01);
+    store_prob(ps, pl, (2 * ci) * kDStepKeys + gi + 8, p10);
+    store_prob(ps, pl, (2 * ci + 1) * kDStepKeys + gi + 8, p11);
     __syncwarp();
     const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(ps + gi * kDStepKeys + 2 * ci);
     const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(ps + gi * kDStepKeys + 2 * ci + 8);
+    const uint32_t pc0 = *reinterpret_cast<const uint32_t*>(pl + gi * kDStepKeys + 2 * ci);
+    const uint32_t pc1 = *reinterpret_cast<const uint32_t*>(pl + gi * kDStepKeys + 2 * ci + 8);
     // o^T[dim][row] = o^T * scale + V^T p: A = V^T via transposing ldmatrix
 #pragma unroll
     for (int mt = 0; mt < VD / 16; ++mt) {
@@ -349,6 +364,7 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, unsigned char* sm, int* s
       o[mt][2] *= sc0;
       o[mt][3] *= sc1;
       mma_bf16_16816(o[mt], va[0], va[1], va[2], va[3], pb0, pb1);
+      mma_bf16_16816(o[mt], va[0], va[1], va[2], va[3], pc0, pc1);
     }
     __syncwarp();   // the stage and the probability tile are reused
     if (lane == 0 && j + D < nst) {
@@ -542,7 +558,8 @@ SV_DEV void dattn_item_wide(const AttnDesc& a, int it, unsigned char* sm, int* s
 
   constexpr int D = L::kDepth;
   bf16* wb = reinterpret_cast<bf16*>(sm + (size_t)warp * L::kWarpBytes);
-  bf16* ps = wb + D * L::kStageElems;                 // [NT][8 rows][16 keys]
+  bf16* ps = wb + D * L::kStageElems;                 // [NT][8 rows][16 keys], high parts
+  bf16* pl = ps + NT * kDRows * kDStepKeys;           // low parts
   const int s_begin = k0 / kDStepKeys, s_end = last / kDStepKeys;
   const int first = s_begin + warp;
   const int nst = first <= s_end ? (s_end - first) / kDWarps + 1 : 0;
@@ -640,18 +657,22 @@ SV_DEV void dattn_item_wide(const AttnDesc& a, int it, unsigned char* sm, int* s
       scl[nt][0] = sc0;
       scl[nt][1] = sc1;
       bf16* pt = ps + nt * kDRows * kDStepKeys;
-      pt[(2 * ci) * kDStepKeys + gi] = __float2bfloat16_rn(p00);
-      pt[(2 * ci + 1) * kDStepKeys + gi] = __float2bfloat16_rn(p01);
-      pt[(2 * ci) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p10);
-      pt[(2 * ci + 1) * kDStepKeys + gi + 8] = __float2bfloat16_rn(p11);
+      bf16* qt = pl + nt * kDRows * kDStepKeys;
+      store_prob(pt, qt, (2 * ci) * kDStepKeys + gi, p00);
+      store_prob(pt, qt, (2 * ci + 1) * kDStepKeys + gi, p01);
+      store_prob(pt, qt, (2 * ci) * kDStepKeys + gi + 8, p10);
+      store_prob(pt, qt, (2 * ci + 1) * kDStepKeys + gi + 8, p11);
     }
     __syncwarp();
-    uint32_t pb0[NT], pb1[NT];
+    uint32_t pb0[NT], pb1[NT], pc0[NT], pc1[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const bf16* pt = ps + nt * kDRows * kDStepKeys;
+      const bf16* qt = pl + nt * kDRows * kDStepKeys;
       pb0[nt] = *reinterpret_cast<const uint32_t*>(pt + gi * kDStepKeys + 2 * ci);
       pb1[nt] = *reinterpret_cast<const uint32_t*>(pt + gi * kDStepKeys + 2 * ci + 8);
+      pc0[nt] = *reinterpret_cast<const uint32_t*>(qt + gi * kDStepKeys + 2 * ci);
+      pc1[nt] = *reinterpret_cast<const uint32_t*>(qt + gi * kDStepKeys + 2 * ci + 8);
     }
 #pragma unroll
     for (int mt = 0; mt < VD / 16; ++mt) {
@@ -664,6 +685,7 @@ SV_DEV void dattn_item_wide(const AttnDesc& a, int it, unsigned char* sm, int* s
         o[mt][nt][2] *= scl[nt][0];
         o[mt][nt][3] *= scl[nt][1];
         mma_bf16_16816(o[mt][nt], va[0], va[1], va[2], va[3], pb0[nt], pb1[nt]);
+        mma_bf16_16816(o[mt][nt], va[0], va[1], va[2], va[3], pc0[nt], pc1[nt]);
       }
     }
     __syncwarp();

@@ -9,10 +9,23 @@ function of the matrix shapes and the SM count only -- which the first test
 checks against full-depth contexts whose layers alias one layer's weights.
 
 The speculative steps run the persistent kernels (draft passes, verify pass)
-and are checked step by step against the fp64 oracle (see
-helpers.teacher_forced): logits within 2e-2, drafts and emitted tokens exact
-except flagged near-boundary draws, at T in {0, 1} and lambda in {0, 0.5},
-K = 5.  Plain decoding on the same kernels is checked the same way.
+and are checked step by step against the oracle (see helpers.teacher_forced):
+drafts and emitted tokens exact except flagged near-boundary draws, at T in
+{0, 1} and lambda in {0, 0.5}, K = 5.  Plain decoding on the same kernels is
+checked the same way.
+
+Logit tolerance.  The pair is specified in bf16 with fp32 accumulation.  At
+these widths that precision by itself moves logits by up to ~0.05 from the
+fp64 definition (vocabulary 128256, logits ~N(0, 1.3^2)): the bf16 KV cache
+alone accounts for ~0.03, the bf16 GEMM inputs alone for ~0.025.  The oracle
+measures that effect with its bf16 dataflow (fp64 arithmetic, activations
+rounded where a bf16 model stores them).  Each compared row set is held to
+2e-2 of the fp64 definition plus the largest bf16-dataflow-vs-fp64
+difference of the oracle on the same rows -- a bound the oracle computes
+alone; the GPU's logits enter only as the value checked.  (Against the bf16
+dataflow itself the GPU differs by ~0.02 here: its fp32 sums and the
+oracle's fp64 sums round to different bf16 neighbours for a few % of the
+activations.)
 
 The oracle reads the same weight bits as the GPU; its copies of the matrices
 are widened to fp64 once, up front (an exact conversion), so that each
@@ -48,7 +61,10 @@ def pair():
     sv.lib()
     tw = workloads.make_weights(W8, seed=31, device="cuda")
     dw = workloads.make_weights(W1, seed=32, device="cuda")
-    return tw, dw, gen.Model(W8, _oracle_copy(tw)), gen.Model(W1, _oracle_copy(dw))
+    t64, d64 = _oracle_copy(tw), _oracle_copy(dw)
+    # (fp64 definition, bf16 dataflow) of each model
+    return tw, dw, (gen.Model(W8, t64), gen.Model(W8, t64, act="bf16")), \
+        (gen.Model(W1, d64), gen.Model(W1, d64, act="bf16"))
 
 
 def test_phase_geometry_matches_full_depth(pair):
@@ -84,20 +100,22 @@ def test_phase_geometry_matches_full_depth(pair):
 
 @pytest.mark.parametrize("temp,mix", [(0.0, 0.0), (1.0, 0.0), (0.0, 0.5), (1.0, 0.5)])
 def test_steps_teacher_forced_full_width(pair, temp, mix):
-    tw, dw, T, D = pair
+    tw, dw, (T, Tb), (D, Db) = pair
     prompt = workloads.make_prompt(W8.vocab, 24, seed=33)[0].tolist()
     dec = sv.SpecDecoder(W8, tw, W1, dw, K, 128, temperature=temp, seed=7, mix_lambda=mix)
     try:
-        _, steps, skipped = helpers.teacher_forced(dec, T, D, prompt, K, temp, 12, TOL, mix=mix, seed=7,
-                                                   max_ctx=128)
+        _, steps, skipped, worst = helpers.teacher_forced(dec, T, D, prompt, K, temp, 12, TOL, mix=mix, seed=7,
+                                                          max_ctx=128, alt=(Tb, Db))
         assert skipped <= max(1, steps // 3)
+        print(f"T={temp} lambda={mix}: {steps} steps; largest logit error {worst[0]:.4f} "
+              f"(allowed {worst[1]:.4f})")
     finally:
         dec.close()
 
 
 @pytest.mark.parametrize("temp", [0.0, 1.0])
 def test_plain_decoding_full_width(pair, temp):
-    tw, dw, T, _ = pair
+    tw, dw, (T, Tb), _ = pair
     prompt = workloads.make_prompt(W8.vocab, 20, seed=34)[0].tolist()
     dec = sv.SpecDecoder(W8, tw, W1, dw, K, 128, temperature=temp, seed=8)
     try:
@@ -107,8 +125,9 @@ def test_plain_decoding_full_width(pair, temp):
             tok = dec.ar_step()
             p, _, _, context = dec.last_step_debug(128)
             ref = T.logits(ctx, last=1)[0]
+            allow = TOL + np.abs(Tb.logits(ctx, last=1)[0] - ref).max()
             err = np.abs(p[0] - ref).max()
-            assert err < TOL, (s, err)
+            assert err < allow, (s, err, allow)
             exp, fl = gen.ar_token_flagged(p[0], temp, 8, s, tie_eps=0.0)
             if fl & helpers.SKIP_FLAGS:
                 skipped += 1

@@ -78,7 +78,7 @@ def _teacher_forced(shape, w, dshape, dw, prompt, k, temp, n_new, mix=0.0, seed=
     try:
         return helpers.teacher_forced(dec, gen.Model(shape, w), gen.Model(dshape, dw), prompt, k, temp,
                                       n_new, helpers.logit_tol(shape), mix=mix, seed=seed, max_ctx=max_ctx,
-                                      tie=helpers.tie_eps(shape))
+                                      tie=helpers.tie_eps(shape))[:3]
     finally:
         dec.close()
 

@@ -135,3 +135,46 @@ def test_causality():
     alt = model.forward(shape, w, other)
     assert torch.allclose(alt[:15], full[:15], atol=1e-12)
     assert not torch.allclose(alt[15:], full[15:])
+
+
+# ---- the bf16 dataflow mode ------------------------------------------------
+
+def test_round_bf16_nearest_even_by_hand():
+    """bf16 keeps 8 significant bits: near 1 the spacing is 2^-7.  Halfway
+    cases go to the even neighbour, everything else to the nearest."""
+    x = torch.tensor([1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -20, 3.0, -(1 + 2 ** -8),
+                      2 ** -130 * 3, 65280.0, 1 - 2 ** -9], dtype=torch.float64)
+    want = [1.0, 1 + 2 ** -6, 1 + 2 ** -7, 3.0, -1.0, 2 ** -130 * 3, 65280.0, 1.0]
+    assert model.round_bf16(x).tolist() == want
+
+
+@pytest.mark.parametrize("shape", [workloads.TINY, workloads.small_shape(dtype="bf16")],
+                         ids=lambda s: s.name)
+def test_bf16_dataflow_without_rounding_is_the_definition(shape):
+    """The bf16 dataflow's restructuring (gain before the GEMM and 1/rms on
+    its sums; the softmax denominator apart from the weighted values) is the
+    definition itself once the rounding is the identity; with the rounding on
+    it moves the logits by a small, non-zero amount."""
+    w = workloads.make_weights(shape, seed=3)
+    g = torch.Generator().manual_seed(4)
+    for lw in w["layers"]:   # non-trivial gains, so that the gain placement matters
+        lw["attn_norm"] = 1 + 0.3 * torch.rand(shape.d_model, generator=g)
+        lw["ffn_norm"] = 1 + 0.3 * torch.rand(shape.d_model, generator=g)
+    w["final_norm"] = 1 + 0.3 * torch.rand(shape.d_model, generator=g)
+    toks = workloads.make_prompt(shape.vocab, 24, seed=5)[0].tolist()
+    ref = model.forward(shape, w, toks)
+    same = model.forward(shape, w, toks, act="bf16", rnd=lambda t: t)
+    assert (same - ref).abs().max() < 1e-11
+    rounded = model.forward(shape, w, toks, act="bf16")
+    d = (rounded - ref).abs().max().item()
+    assert 1e-5 < d < 0.05, d
+
+
+def test_rounded_attention_without_rounding_is_attention():
+    g = torch.Generator().manual_seed(6)
+    q = torch.randn(9, 4, 16, generator=g, dtype=torch.float64)
+    k = torch.randn(9, 2, 16, generator=g, dtype=torch.float64)
+    v = torch.randn(9, 2, 16, generator=g, dtype=torch.float64)
+    a = model.causal_attention(q, k, v)
+    b = model.causal_attention_rounded(q, k, v, lambda t: t)
+    assert (a - b).abs().max() < 1e-13

@@ -38,7 +38,8 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the array on the current device, looked up once per
-// device (the host-side name is only a stand-in for the symbol).
+// device (the host-side name is only a stand-in for the symbol) and kept for
+// the process: a device reset, which reloads the module, invalidates it.
 cudaError_t scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);

@@ -359,7 +359,8 @@ SPEC_API int64_t spec_device_bytes_held(void);
  * the plain-decoding pass.  Writes *nphases and, per phase i, eight int64 at
  * out[8 i ..]: kind (0 embedding, 1 GEMM, 2 attention), then
  *   GEMM:      rows n, k, tokens, 16-row output tiles, 1 if a tile's k range
- *              is split between CTAs (else 0), ring stages, rows per box;
+ *              is split between CTAs (else 0), ring stages, 1 if the input
+ *              rows are resident in shared memory (else streamed);
  *   attention: query heads, KV heads, tokens, work items, 0, 0, head dim;
  *   embedding: tokens, d_model, tokens, 0, 0, 0, 0.
  * The geometry depends only on the shapes and the SM count, so a model cut

@@ -210,6 +210,12 @@ SV_DEV void tma_load_2d_hint(void* dst, const void* tmap, int c0, int c1, uint64
         "l"(policy)
       : "memory");
 }
+// Prefetch of one 2-D box of the tensor map at tmap into L2 (no shared
+// memory, no barrier; completes on its own).
+SV_DEV void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1) : "memory");
+}
 // 16-byte asynchronous global -> shared copy (L2 only); with valid = false
 // nothing is read and the destination is zero-filled.
 SV_DEV void cp_async16(void* dst, const void* src, bool valid) {

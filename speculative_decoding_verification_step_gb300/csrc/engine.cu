@@ -865,20 +865,23 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   // shared memory.
   if (B == 1 && target->dtype == SPEC_DTYPE_BF16 && draft->dtype == SPEC_DTYPE_BF16 &&
       !(opts->flags & (SPEC_OPT_TIMING | SPEC_OPT_NO_PERSIST))) {
-    const size_t sm_t = persist_smem_bytes(target->head_dim, c->max_chunks, K + 1, target->d_model);
-    const size_t sm_d = persist_smem_bytes(draft->head_dim, c->max_chunks, 2, draft->d_model);
-    if (persist_supported(target->head_dim, sm_t, c->num_sms, K + 1) &&
-        persist_supported(draft->head_dim, sm_d, c->num_sms, 2)) {
+    PersistLayout lay_t{}, lay_d{};
+    const bool lay_ok = persist_layout(target->head_dim, K + 1, target->d_model, &lay_t) &&
+                        persist_layout(draft->head_dim, 2, draft->d_model, &lay_d);
+    if (lay_ok && persist_supported(target->head_dim, lay_t.total, c->num_sms, K + 1) &&
+        persist_supported(draft->head_dim, lay_d.total, c->num_sms, 2)) {
       std::vector<PhaseDesc> all;
       std::vector<TensorMap128> maps;
       size_t start[20], count[20];
-      bool encodable = c->gs.partial_floats >= persist_partial_floats(c->num_sms);
+      bool encodable = true;
       // decode-attention scratch: partials in the attention buffer, own tickets
       for (const spec_model_desc* m : {target, draft})
         encodable = encodable && persist_attn_partial_floats(K + 1, m->n_heads, m->head_dim, c->cap) <=
                                      attn_partial_floats(maxN, (int)hqmax, (int)hdmax, c->max_chunks);
       int* const dattn_tick = c->dattn_tick;   // sized for kGemmMaxTok >= K + 1 tokens
       auto add = [&](int idx, const std::vector<Op>& ops) {
+        const bool drf = idx < K || idx == K + 2;
+        const PersistLayout& lay = drf ? lay_d : lay_t;
         start[idx] = all.size();
         for (const Op& op : ops) {
           PhaseDesc p{};
@@ -888,7 +891,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
             encodable = persist_phase_from_attn(p, op.a) && encodable;
             p.a.tickets = dattn_tick;
           } else {
-            encodable = persist_phase_from_gemm(p, op.g, maps, c->num_sms) && encodable;
+            encodable = persist_phase_from_gemm(p, op.g, maps, c->num_sms, lay) && encodable;
           }
           all.push_back(p);
         }
@@ -931,14 +934,13 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
           pf.desc.phases = c->phase_dev + start[f];
           pf.desc.nphases = (int)count[f];
           pf.desc.tmaps = tmaps_dev;
-          pf.desc.partials = c->gs.partials;
-          pf.desc.tickets = c->gs.tickets;
+          const bool drf = f < K || f == K + 2;
+          pf.desc.ring_bytes = (int)(drf ? lay_d.ring : lay_t.ring);
           pf.desc.bar = c->bar;
           pf.desc.err = res_err(c);
           pf.desc.ctl = c->fault_ctl;
-          const bool drf = f < K || f == K + 2;
           pf.hd = drf ? draft->head_dim : target->head_dim;
-          pf.smem = drf ? sm_d : sm_t;
+          pf.smem = drf ? lay_d.total : lay_t.total;
         }
         c->persist = true;
       }
@@ -1284,10 +1286,10 @@ int spec_phase_list(spec_ctx* c, int which, int64_t* out, int max_phases, int* n
     o[0] = d.kind;
     if (d.kind == kPhaseGemm) {
       o[1] = d.g.n; o[2] = d.g.k; o[3] = d.g.ntok;
-      o[4] = gemm_tiles(d.g);
-      o[5] = d.whole ? 0 : 1;   // some 16-row tile split between CTAs
+      o[4] = d.tiles;
+      o[5] = 0;   // CTAs own whole tiles: no tile's k range is split between CTAs
       o[6] = d.stages;
-      o[7] = d.R;
+      o[7] = d.xm == kXSmem ? 1 : 0;
     } else if (d.kind == kPhaseAttn) {
       o[1] = d.a.hq; o[2] = d.a.hkv; o[3] = d.a.ntok; o[4] = d.attn_items;
       o[5] = o[6] = 0; o[7] = d.a.hd;

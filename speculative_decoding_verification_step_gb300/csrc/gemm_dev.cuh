@@ -282,7 +282,7 @@ SV_DEV void tile_ptrs(const GemmDesc& g, int tile, int gi, const uint16_t*& pa, 
 // bf16 rows pre-multiplied by the gain (x_norm = 2); kXInline = RMSNorm
 // applied while loading (large token counts, where the normalised X would not
 // fit).
-enum XMode : int { kXGlobal = 0, kXSmem = 1, kXInline = 2 };
+// (XMode: kernels.h)
 constexpr int kXPad = 8;
 
 // Per-warp state of one GEMM: its range of (tile, k-step) units and the

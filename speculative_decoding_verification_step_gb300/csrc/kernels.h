@@ -283,15 +283,21 @@ cudaError_t launch_lookup(const LookupDesc& d, cudaStream_t st);
 // tma_dev.cuh); results agree with the per-kernel path up to the order of
 // fp32 partial sums, and are batch-invariant like it.
 enum PhaseKind : int { kPhaseEmbed = 0, kPhaseGemm = 1, kPhaseAttn = 2 };
+// GEMM X source: from global memory (per-operation GEMM; the persistent
+// kernel's streamed X), kept in shared memory (the persistent kernel's
+// resident X), or normalised while loading (per-operation GEMM).
+enum XMode : int { kXGlobal = 0, kXSmem = 1, kXInline = 2 };
 constexpr int kPhaseStamps = 5;
 struct PhaseDesc {
   int kind;
-  int xm;            // GEMM X source (see gemm_dev.cuh)
-  // GEMM streaming geometry: R rows per box, paired boxes (RoPE / SwiGLU) or
-  // one box of 2R rows, row groups, ring stages and bytes per stage, and the
+  // GEMM streaming geometry (tma_dev.cuh): X resident in shared memory
+  // (kXSmem) or streamed beside the weights (kXGlobal); paired boxes (RoPE /
+  // SwiGLU: two 8-row boxes per tile) or one 16-row box; 16-row tiles; tiles
+  // per stage group and k per stage; ring stages, bytes per stage and the
+  // offset of the stage's X boxes; units issued before the phase's barrier;
   // tensor-map indices of the weight segments (0..2) and of X (3)
-  int R, paired, groups, stages, stage_bytes;
-  int whole;         // 1: CTAs own whole row groups (no tile split between CTAs)
+  int xm, paired, tiles, gt, kc;
+  int stages, stage_bytes, xoff, prefetch;
   int tm[4];
   int attn_items;
   GemmDesc g;
@@ -306,8 +312,7 @@ struct PersistDesc {
   const PhaseDesc* phases;   // device array
   int nphases;
   const TensorMap128* tmaps; // device array indexed by PhaseDesc::tm
-  float* partials;           // GEMM scratch, >= persist_partial_floats(grid) floats
-  int* tickets;
+  int ring_bytes;            // dynamic shared memory: [ring][group partials][X region]
   unsigned* bar;             // [1] arrival count (zero at start; the kernel leaves it zero)
   int* err;                  // set to 1 when a wait gives up
   // optional fault injection (null: off): [0] arrivals added to every grid-
@@ -322,22 +327,28 @@ struct PersistDesc {
   // or end of its items (attention)
   unsigned long long* times;
 };
+// Shared-memory layout of one persistent kernel instance: the weight ring,
+// the group-partial area and the X region (resident GEMM inputs) -- the
+// attention tiles reuse the whole of it.
+struct PersistLayout {
+  size_t ring, xreg, total;
+};
+// Layout for head dim hd and passes of at most max_tok tokens of a model of
+// width d_model (X region: at least max_tok rows of d_model); false when it
+// does not fit one CTA per SM.
+bool persist_layout(int hd, int max_tok, int d_model, PersistLayout* out);
 // Fill the kernel-side fields of a phase.  The GEMM variant also encodes the
 // phase's tensor maps, appending them to maps; false when the phase does not
 // meet the tensor-copy rules (16-byte aligned rows, k and the X stride
 // multiples of 8, at most 8 tokens, RoPE head dim a multiple of 32).
-bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid);
+bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid,
+                             const PersistLayout& lay);
 // Attention phases need a bf16 cache, at most 8 tokens and head dim 32, 64
 // or 128; their scratch is persist_attn_partial_floats floats and
 // dattn_tickets zeroed counters (a.partials, a.tickets).
 bool persist_phase_from_attn(PhaseDesc& p, const AttnDesc& a);
 size_t persist_attn_partial_floats(int max_tok, int hq, int hd, int cap);
 void persist_phase_from_embed(PhaseDesc& p, const EmbedDesc& e);
-// Dynamic shared memory the persistent kernel needs for head dim hd, KV
-// chunks max_chunks and the largest normalised GEMM input (tokens x k).
-size_t persist_smem_bytes(int hd, int max_chunks, int max_tok, int max_k);
-// GEMM partial-sum floats the persistent kernel needs for `grid` CTAs.
-size_t persist_partial_floats(int grid);
 // True when one CTA per SM of the persistent kernel fits, for passes of at
 // most max_tok tokens.
 bool persist_supported(int hd, size_t smem, int num_sms, int max_tok);

@@ -10,13 +10,14 @@
 //   * one CTA per SM stays resident; phases are separated by a grid barrier
 //     split in an arrive and a wait half;
 //   * GEMM phases stream weights with 2-D tensor copies (TMA) through a
-//     shared-memory ring (tma_dev.cuh): one producer thread copies, up to
-//     four tile-owner warps run the MMAs;
+//     shared-memory ring (tma_dev.cuh): each CTA owns whole 16-row output
+//     tiles, one producer warp copies, eight consumer warps split every
+//     stage by k and finish their tiles inside the CTA;
 //   * between arriving at a barrier and waiting on it, the producer already
 //     issues the weight copies of the next GEMM phase's first units (weights
 //     are read-only), so HBM keeps streaming across phase boundaries;
 //   * attention phases run the tensor-core decode attention (dattn_dev.cuh)
-//     on all eight warps; the embedding reuses embed_dev.cuh.
+//     on the eight consumer warps; the embedding reuses embed_dev.cuh.
 // The work split depends only on the matrix shapes and the SM count, never
 // on the token count, so every pass is batch-invariant.  Every wait is
 // bounded: a grid-barrier wait that gives up, or a pipeline wait (see
@@ -85,9 +86,9 @@ SV_DEV void grid_leave(unsigned* bar, unsigned total) {
 
 template <int HD, bool kGroup>
 __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __grid_constant__ PersistDesc p) {
-  // dynamic shared memory: [weight ring, kRingBytes][X region: normalised X,
-  // or the X boxes of phases reading X from global memory]; attention
-  // phases reuse it from offset 0
+  // dynamic shared memory: [weight ring, p.ring_bytes][group partials,
+  // kRedBytes][X region: resident GEMM inputs]; attention phases reuse it
+  // from offset 0
   extern __shared__ __align__(1024) unsigned char dsm[];
   __shared__ TmaPipe tp;
   __shared__ uint64_t dbars[kDWarps * kDMaxDepth];   // attention stage barriers
@@ -96,7 +97,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   // the current and the next phase descriptor, staged in shared memory
   __shared__ __align__(16) PhaseDesc s_ph[2];
   unsigned char* ring = dsm;
-  unsigned char* xreg = dsm + kRingBytes;
+  float4* red = reinterpret_cast<float4*>(dsm + p.ring_bytes);
+  unsigned char* xreg = dsm + p.ring_bytes + kRedBytes;
   const unsigned char* maps = reinterpret_cast<const unsigned char*>(p.tmaps);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = warp == kProducerWarp;
@@ -135,24 +137,24 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
     if (d.kind == kPhaseEmbed) {
       for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16, false>(d.e, t);
     } else if (d.kind == kPhaseGemm) {
-      if (d.xm == kXSmem) tma_prepare_xg(d, tp, s_inv, xreg);
+      if (d.xm == kXSmem) tma_prepare_x(d, tp, s_inv, xreg);
       if (st && threadIdx.x == 0) atomicMax(st + 3, global_ns());
       if (producer) {
-        if (lane == 0) tma_produce(d, npre, tp, ring, xreg, maps);
+        if (lane == 0) tma_produce(d, npre, tp, ring, maps);
         __syncwarp();
       } else if (d.xm == kXSmem) {
-        tma_consume<kXSmem>(d, tp, cpar, ring, xreg, s_inv, p.partials, p.tickets, st ? st + 4 : nullptr);
+        tma_consume<true>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
       } else {
-        tma_consume<kXGlobal>(d, tp, cpar, ring, xreg, s_inv, p.partials, p.tickets, st ? st + 4 : nullptr);
+        tma_consume<false>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
       }
-    } else {
+    } else if (!producer) {   // attention: the eight consumer warps
       for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x)
         dattn_item_mode<HD, kGroup, false>(d.a, it, dsm, &s_last, dbars, dpar, st ? st + 3 : nullptr);
       if (st && threadIdx.x == 0) atomicMax(st + 4, global_ns());
     }
-    npre = 0;
     // this thread's global writes and shared-memory accesses are ordered
     // before later tensor copies (other CTAs' copies of X; this CTA's ring)
+    npre = 0;
     fence_proxy_async_global();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (times) {   // arrival of this CTA (its threads are done with the phase)
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
       if (threadIdx.x == 0 && tp.abort) atomicExch(p.err, 1);
       const PhaseDesc& nx = s_ph[(ph + 1) & 1];
       if (nx.kind == kPhaseGemm && producer) {   // weights of the next GEMM: issued while waiting
-        if (lane == 0) npre = tma_prefetch(nx, tp, ring, xreg, maps);
+        if (lane == 0) npre = tma_prefetch(nx, tp, ring, maps);
         npre = __shfl_sync(0xffffffffu, npre, 0);
       }
       if (!grid_wait(p.bar, (unsigned)(ph + 1) * gridDim.x + bar_extra, p.err, &s_ok, bar_limit)) {
@@ -231,59 +233,64 @@ bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid) {
+bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid,
+                             const PersistLayout& lay) {
   p = PhaseDesc{};
   p.kind = kPhaseGemm;
   p.g = g;
-  p.xm = g.x_norm ? kXSmem : kXGlobal;
   if (g.k % 8 != 0 || g.ntok < 1 || g.ntok > kPersistMaxTok) return false;
-  // a normalised input comes pre-multiplied by its gain (x_norm = 2), by bulk
-  // copies of 16-byte aligned rows
+  // an RMSNorm'd input comes pre-multiplied by its gain (x_norm = 2)
   if (g.x_norm == 1) return false;
-  if (g.x_norm == 2 && (g.ldx % 8 != 0 || reinterpret_cast<uintptr_t>(g.x) % 16 != 0)) return false;
+  if (g.ldx % 8 != 0 || reinterpret_cast<uintptr_t>(g.x) % 16 != 0) return false;
   auto add = [&](const void* base, long long rows, long long ld, int box_rows) {
     TensorMap128 m{};
     if (!encode_rows(m, base, g.k, rows, ld, box_rows)) return -1;
     maps.push_back(m);
     return (int)maps.size() - 1;
   };
+  p.tiles = gemm_tiles_of(g);
   if (g.epi == kEpiQkvRope) {
-    if (g.hd % 32 != 0) return false;
-    p.R = (g.hd / 2) % 32 == 0 ? 32 : 16;
+    if (g.hd % 16 != 0) return false;
     p.paired = 1;
-    p.groups = (g.hq + 2 * g.hkv) * (g.hd / (2 * p.R));
-    for (int s = 0; s < 3; ++s) p.tm[s] = add(g.w[s], g.seg_rows[s], g.k, p.R);
+    for (int s = 0; s < 3; ++s) p.tm[s] = add(g.w[s], g.seg_rows[s], g.k, 8);
   } else if (g.epi == kEpiSwiglu) {
-    if (g.n % 16 != 0) return false;
-    p.R = g.n % 32 == 0 ? 32 : 16;
+    if (g.n % 8 != 0) return false;
     p.paired = 1;
-    p.groups = g.n / p.R;
-    p.tm[0] = add(g.w[0], g.n, g.k, p.R);
-    p.tm[1] = add(g.w[1], g.n, g.k, p.R);
+    p.tm[0] = add(g.w[0], g.n, g.k, 8);
+    p.tm[1] = add(g.w[1], g.n, g.k, 8);
     p.tm[2] = p.tm[0];
   } else {
-    p.R = 32;
     p.paired = 0;
-    p.groups = (g.n + 2 * p.R - 1) / (2 * p.R);
-    p.tm[0] = add(g.w[0], g.n, g.k, 2 * p.R);
+    p.tm[0] = add(g.w[0], g.n, g.k, kTileRows);
     p.tm[1] = p.tm[2] = p.tm[0];
   }
-  p.tm[3] = p.xm == kXGlobal ? add(g.x, g.ntok, g.ldx, kXBoxRows) : 0;
+  // X resident in shared memory when the ntok input rows fit the X region,
+  // else streamed with the weights, one box of the ntok rows per 256 k
+  const size_t xbytes = (size_t)g.ntok * (g.k + kXPad) * 2;
+  p.xm = xbytes <= lay.xreg ? kXSmem : kXGlobal;
+  const int nct = std::min(grid, p.tiles);
+  const int tiles_max = (p.tiles + nct - 1) / nct;
+  if (p.xm == kXSmem) {
+    p.gt = 1;
+    p.kc = 4 * kTmaK;
+    p.tm[3] = 0;
+  } else {
+    p.gt = std::min(kMaxGroupTiles, tiles_max);
+    p.kc = 4 * kTmaK / p.gt;
+    p.tm[3] = add(g.x, g.ntok, g.ldx, g.ntok);
+  }
   for (int i = 0; i < 4; ++i)
     if (p.tm[i] < 0) return false;
-  // whole row groups per CTA when that loads no CTA more than the even unit
-  // split does: then no tile is split between CTAs (no partials, no tickets)
-  {
-    const long long kbpt = (g.k + kTmaK - 1) / kTmaK, units = (long long)p.groups * kbpt;
-    const long long nc = std::max(1LL, std::min((long long)grid, units / kMinUnitsPerCta));
-    const long long split_max = (units + nc - 1) / nc;
-    const long long ncw = std::min((long long)grid, (long long)p.groups);
-    const long long whole_max = (p.groups + ncw - 1) / ncw * kbpt;
-    p.whole = whole_max <= split_max ? 1 : 0;
-  }
-  p.stage_bytes = 2 * p.R * kTmaRowBytes;
-  p.stages = (int)(kRingBytes / p.stage_bytes);
-  if (p.stages > kMaxStages) p.stages = kMaxStages;
+  const int xstage = p.xm == kXGlobal ? (p.kc / kTmaK) * g.ntok * kTmaRowBytes : 0;
+  p.xoff = kStageWeightBytes;
+  p.stage_bytes = (kStageWeightBytes + xstage + 1023) / 1024 * 1024;
+  p.stages = std::min<int>(kMaxStages, (int)(lay.ring / (size_t)p.stage_bytes));
+  if (p.stages < 2) return false;
+  // units issued before the phase's barrier: a full ring, except that a
+  // resident-X phase with few units per CTA takes only 3 ahead, so that its
+  // X copies are not queued behind a ring of weight copies
+  const int units_max = ((tiles_max + p.gt - 1) / p.gt) * ((g.k + p.kc - 1) / p.kc);
+  p.prefetch = p.xm == kXSmem && units_max <= 16 ? std::min(p.stages, 3) : p.stages;
   return true;
 }
 
@@ -306,19 +313,36 @@ void persist_phase_from_embed(PhaseDesc& p, const EmbedDesc& e) {
   p.e = e;
 }
 
-size_t persist_smem_bytes(int hd, int max_chunks, int max_tok, int max_k) {
-  (void)max_chunks;
+bool persist_layout(int hd, int max_tok, int d_model, PersistLayout* out) {
   size_t attn = 0;
   if (hd == 32) attn = DAttnSmem<32>::kBytes;
   if (hd == 64) attn = DAttnSmem<64>::kBytes;
   if (hd == 128) attn = DAttnSmem<128>::kBytes;
-  size_t xreg = (size_t)max_tok * (max_k + kXPad) * 2;
-  if (xreg < (size_t)kMaxStages * kXStageBytes) xreg = (size_t)kMaxStages * kXStageBytes;
-  const size_t gemm = kRingBytes + xreg;
-  return attn > gemm ? attn : gemm;
+  if (!attn) return false;
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return false;
+  // static shared memory of the kernel (the largest of its instances)
+  size_t stat = 0;
+  const void* fns[] = {(const void*)persist_forward<32, false>, (const void*)persist_forward<64, false>,
+                       (const void*)persist_forward<128, false>, (const void*)persist_forward<32, true>,
+                       (const void*)persist_forward<64, true>, (const void*)persist_forward<128, true>};
+  for (const void* fn : fns) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return false;
+    stat = std::max(stat, fa.sharedSizeBytes);
+  }
+  const size_t budget = (size_t)optin > stat + 1024 ? (size_t)optin - stat - 1024 : 0;
+  size_t xreg = ((size_t)max_tok * (d_model + kXPad) * 2 + 1023) / 1024 * 1024;
+  xreg = std::max(xreg, kXMinBytes);
+  if (budget < kRedBytes + xreg + 2 * (size_t)kStageWeightBytes) return false;
+  const size_t ring = std::min(kRingMaxBytes, budget - kRedBytes - xreg) / 1024 * 1024;
+  out->ring = ring;
+  out->xreg = xreg;
+  out->total = std::max(ring + kRedBytes + xreg, attn);
+  return out->total <= budget;
 }
-
-size_t persist_partial_floats(int grid) { return (size_t)grid * 2 * kMaxMmaTiles * 32 * 4; }
 
 // The dynamic shared-memory limit is a per-function attribute shared by
 // every context of the process (a draft and a target with the same head

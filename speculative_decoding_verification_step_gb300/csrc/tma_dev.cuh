@@ -1,59 +1,84 @@
 // Tensor-copy (TMA) weight streaming of the persistent forward kernel.
 //
-// A GEMM phase is cut into units of one row group x 256 k.  A row group is
-// two boxes of R rows (R = 16 or 32) of the weight matrix, each box one
-// 2-D tensor copy of R x 256 bf16 into shared memory:
-//   * plain matrices: one box of 2R consecutive rows, MMA tile t = rows
-//     16t + g and 16t + 8 + g of the box;
-//   * q/k/v with RoPE: rows h*hd + j*R + [0, R) and the rotation partners
-//     hd/2 further, MMA tile t = row 8t + g of each box;
-//   * SwiGLU: the same R rows of the gate and of the up matrix.
-// So an MMA tile is exactly a 16-row tile of the per-kernel path (same
-// epilogue, same tile index).  A CTA owns a contiguous range of units (split
-// by shape and grid only, never by token count).  One producer thread streams
-// the units through a ring of S stages (S x 2R x 512 bytes, S <= 8): per unit
-// one or two weight boxes and, in phases whose X comes from global memory,
-// one 8-row X box, all completing on the stage's transaction barrier.  In an
-// RMSNorm'd phase the producer first copies the X columns the CTA's units
-// read -- bf16 rows already multiplied by the norm's gain -- into shared
-// memory with bulk copies, and 1/rms scales the finished sums.  The
-// warp t < T = R/8 owns MMA tile t of every unit (its four 64-k
-// steps, one accumulator chain each, added in step order).  A tile split
-// between CTAs is finished by the last-arriving CTA, which adds the CTA
-// partials in CTA order; no consumer warp ever waits for another.  Results
-// do not depend on timing or on the token count.
+// A GEMM phase's output rows come in MMA tiles of 16 rows (gemm_dev.cuh:
+// plain tiles are rows 16t .. 16t+15; q/k/v tiles pair 8 rows with their
+// RoPE partners hd/2 further; SwiGLU tiles pair 8 gate rows with the same 8
+// up rows).  Each CTA owns a contiguous range of whole tiles -- every k of
+// them -- so no tile is split between CTAs: a tile's sum is finished inside
+// the CTA that streamed it, with no partial sums in global memory, no
+// tickets and no last-arriving CTA on the way to the grid barrier.  The
+// ranges are as even as whole tiles allow; when some CTAs own one tile
+// fewer, they finish early and the busier ones, sharing HBM with fewer
+// streams, run faster (one SM ingests ~44 GB/s when all 152 stream, up to
+// ~80 GB/s when few do), so uneven ranges cost far less than their byte
+// imbalance.
+//
+// Stages.  A stage holds gt tiles x kc columns of weights (32 KB): per tile
+// and 256-k block one tensor copy of 16 rows (plain) or two of 8 rows
+// (paired).  The input X (ntok rows) is either resident -- copied into
+// shared memory once per phase, one bulk copy per token, when ntok x k fits
+// the X region -- or streamed: per 256-k block one box of the ntok rows,
+// behind the stage's weights (the 14336-wide input of a 6-token 8B
+// down-projection).  Resident phases take one tile per stage group (gt = 1,
+// kc = 1024); streamed phases group two tiles (gt = 2, kc = 512) so that
+// each X box serves both.
+//
+// Warps.  One producer thread (warp kProducerWarp) issues the copies through
+// a ring of S stages.  The eight consumer warps split every stage by k: warp
+// w takes the stage's 64-k steps w and w + 8 (16 steps per stage: with
+// gt = 2 the first eight belong to the group's first tile, the last eight to
+// its second), each into its own accumulator chain.  At the end of a group
+// every warp leaves its partial sums in shared memory; after a barrier of
+// the consumer warps one warp per tile adds the eight partials in warp
+// order, applies 1/rms (RMSNorm'd inputs) and runs the tile's epilogue while
+// the other warps go on with the next stages (resident phases alternate two
+// partial buffers, so the next group's partials never overwrite ones still
+// being read).  The summation order depends on k and the warp count only, so
+// every pass is batch-invariant.  (Handing the partials to the epilogue warp
+// through mbarriers instead of the barrier measured no faster.)
+//
+// Phase boundaries.  Between arriving at the grid barrier before a GEMM
+// phase and leaving it, the producer already fills the ring with the
+// phase's first units (weights are read-only), so HBM keeps streaming while
+// the grid waits; after the barrier it copies X (and, streamed, the X boxes
+// of those units) and streams the rest.
 //
 // Every wait is bounded.  A wait that gives up raises the CTA's abort flag;
 // from then on every wait of the CTA returns at once and the warps run
-// through their remaining iterations without touching the data (named
-// barrier counts stay identical); the kernel reports the failure and leaves
-// after waiting, again with a bound, for its copies still in flight.
+// through their remaining iterations without touching the data (barrier
+// counts stay identical); the kernel reports the failure and leaves after
+// waiting, again with a bound, for its copies still in flight.
 #pragma once
 #include "gemm_dev.cuh"
 
 namespace sv {
 
-constexpr int kTmaK = 256;                        // k per unit (box inner extent)
+constexpr int kTmaK = 256;                        // k per box (box inner extent)
 constexpr int kTmaRowBytes = kTmaK * 2;           // row pitch of a box in shared memory
-constexpr int kTmaSteps = kTmaK / kStepK;         // 64-k MMA steps per unit
-constexpr int kCWarps = 8;                        // warps of the CTA (attention uses all)
-constexpr int kProducerWarp = kCWarps - 1;        // lane 0 issues the tensor copies
-constexpr int kPersistThreads = kCWarps * 32;     // 2 warps per SM sub-partition: 255 registers
+constexpr int kTileRows = 16;
+constexpr int kTileBlockBytes = kTileRows * kTmaRowBytes;   // one tile x 256 k: 8 KB
+constexpr int kStageWeightBytes = 4 * kTileBlockBytes;       // 32 KB of weights per stage
+constexpr int kStageSteps = kStageWeightBytes / (kTileRows * kStepK * 2);   // 64-k steps per stage: 16
+constexpr int kCWarps = 8;                        // consumer warps (attention uses them all)
+constexpr int kConsumerThreads = kCWarps * 32;
+constexpr int kProducerWarp = kCWarps;            // lane 0 issues the tensor copies
+constexpr int kPersistThreads = (kCWarps + 1) * 32;
 constexpr int kMaxStages = 8;
-constexpr int kXBoxRows = 8;
-constexpr int kXStageBytes = kXBoxRows * kTmaRowBytes;
-constexpr size_t kRingBytes = 160 * 1024;         // weight ring: 5 stages of 32 KB
-constexpr int kMinUnitsPerCta = 2;
-constexpr int kMaxMmaTiles = 4;                   // R / 8 for R <= 32
+constexpr int kMaxGroupTiles = 2;
+constexpr size_t kRingMaxBytes = 160 * 1024;      // weight ring (5 stages of 32 KB)
+// group partials: [2 buffers or kMaxGroupTiles tiles][8 warps][32 lanes] float4
+constexpr size_t kRedBytes = (size_t)2 * kCWarps * 32 * 16;
+constexpr size_t kXMinBytes = 36 * 1024;          // X region: at least a 2-token 8192-wide input
 constexpr long long kWaitLimit = 1LL << 22;
 constexpr long long kDrainLimit = 1LL << 16;
 constexpr int kPersistMaxTok = 8;
 constexpr size_t kTensorMapBytes = 128;
+constexpr int kGemmBarrier = 2;                   // named barrier of the consumer warps (1: attention)
 
 struct TmaPipe {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t xfull;               // the bulk X copies of an x_norm = 2 phase
+  uint64_t xfull;               // the bulk X copies of a resident-X phase
   unsigned fills[kMaxStages];   // fills issued per slot (producer)
   unsigned xfills;              // X loads issued (their barrier's phase count)
   int abort;
@@ -63,7 +88,7 @@ SV_DEV void tma_init(TmaPipe& tp) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&tp.full[i], 1);
-      mbar_init(&tp.empty[i], kMaxMmaTiles);   // released by the tile-owner warps
+      mbar_init(&tp.empty[i], kCWarps);   // released by every consumer warp
       tp.fills[i] = 0;
     }
     mbar_init(&tp.xfull, 1);
@@ -74,343 +99,357 @@ SV_DEV void tma_init(TmaPipe& tp) {
 }
 
 // Wait for the completion of the phase of `parity`; false once the CTA has
-// aborted (raising the flag when this wait is the one that gives up).
+// aborted (raising the flag when this wait is the one that gives up).  The
+// abort flag is read every 64 probes only: a shared-memory read in every
+// probe of the eight polling consumer warps slowed the weight stream by ~7%.
 SV_DEV bool tma_wait(uint64_t* bar, unsigned parity, TmaPipe& tp) {
   volatile int* ab = &tp.abort;
   long long spins = 0;
   while (true) {
-    if (*ab) return false;
     if (mbar_test(bar, parity)) return true;
-    if (++spins > kWaitLimit) {
-      *ab = 1;
-      return false;
+    if ((++spins & 63) == 0) {
+      if (*ab) return false;
+      if (spins > kWaitLimit) {
+        *ab = 1;
+        return false;
+      }
     }
   }
 }
 
-struct TmaRange {
-  long long total, nc;
-  int u0, u1, kbpt;
+// The phase's streaming geometry and this CTA's tiles [t0, t1), copied out
+// of the shared-memory phase descriptor into registers once per phase: the
+// copy and MMA loops run between asm statements that act as compiler memory
+// barriers, so fields read from the descriptor inside them would be loaded
+// again and again on the issue path.
+struct TmaGeo {
+  const unsigned char* maps;
+  const void* x;                 // streamed X's tensor map is tm[3]
+  int S, sb, kc, k, gt, paired, ntok, xoff, xs;
+  int epi, hd, seg0, seg1;
+  int tm0, tm1, tm2, tmx;        // weight segments 0..2, streamed X
+  int t0, t1, nchunks, ngroups, n;
 };
 
-SV_DEV TmaRange tma_range(const PhaseDesc& d) {
-  TmaRange r;
-  r.kbpt = (d.g.k + kTmaK - 1) / kTmaK;
-  r.total = (long long)d.groups * r.kbpt;
-  if (d.whole) {   // whole row groups per CTA, as evenly as groups allow
-    r.nc = min((long long)gridDim.x, (long long)d.groups);
-    const bool has = blockIdx.x < r.nc;
-    r.u0 = has ? (int)first_step_of_warp(blockIdx.x, d.groups, r.nc) * r.kbpt : 0;
-    r.u1 = has ? (int)first_step_of_warp(blockIdx.x + 1, d.groups, r.nc) * r.kbpt : 0;
-    return r;
-  }
-  r.nc = max(1LL, min((long long)gridDim.x, r.total / kMinUnitsPerCta));
-  const bool has = blockIdx.x < r.nc;
-  r.u0 = has ? (int)first_step_of_warp(blockIdx.x, r.total, r.nc) : 0;
-  r.u1 = has ? (int)first_step_of_warp(blockIdx.x + 1, r.total, r.nc) : 0;
-  return r;
+SV_DEV TmaGeo tma_geo(const PhaseDesc& d, const unsigned char* maps) {
+  TmaGeo q;
+  q.maps = maps;
+  q.x = d.g.x;
+  q.S = d.stages;
+  q.sb = d.stage_bytes;
+  q.kc = d.kc;
+  q.k = d.g.k;
+  q.gt = d.gt;
+  q.paired = d.paired;
+  q.ntok = d.g.ntok;
+  q.xoff = d.xoff;
+  q.xs = d.xm == kXGlobal;
+  q.epi = d.g.epi;
+  q.hd = d.g.hd;
+  q.seg0 = d.g.seg_rows[0];
+  q.seg1 = d.g.seg_rows[1];
+  q.tm0 = d.tm[0];
+  q.tm1 = d.tm[1];
+  q.tm2 = d.tm[2];
+  q.tmx = d.tm[3];
+  const int tiles = d.tiles;
+  const int G = min((int)gridDim.x, tiles);
+  const bool has = (int)blockIdx.x < G;
+  q.t0 = has ? (int)first_step_of_warp(blockIdx.x, tiles, G) : 0;
+  q.t1 = has ? (int)first_step_of_warp(blockIdx.x + 1, tiles, G) : 0;
+  q.nchunks = (q.k + q.kc - 1) / q.kc;
+  q.ngroups = (q.t1 - q.t0 + q.gt - 1) / q.gt;
+  q.n = q.ngroups * q.nchunks;
+  return q;
 }
 
-// Tensor-map index and first row of box A / box B of row group grp.
-struct GroupBoxes {
+// Tensor-map index and first row of box A (and box B when paired) of tile t.
+struct TileBoxes {
   int ma, ra, mb, rb;
 };
-SV_DEV GroupBoxes group_boxes(const PhaseDesc& d, int grp) {
-  const GemmDesc& g = d.g;
-  const int R = d.R;
-  if (g.epi == kEpiQkvRope) {
-    const int per = g.hd / (2 * R);
-    int row = (grp / per) * g.hd + (grp % per) * R;
+SV_DEV TileBoxes tile_boxes(const TmaGeo& q, int t) {
+  if (q.epi == kEpiQkvRope) {
+    const int per = q.hd / 16;
+    int row = (t / per) * q.hd + 8 * (t % per);
     int seg = 0;
-    if (row >= g.seg_rows[0]) {
-      row -= g.seg_rows[0];
+    if (row >= q.seg0) {
+      row -= q.seg0;
       seg = 1;
-      if (row >= g.seg_rows[1]) {
-        row -= g.seg_rows[1];
+      if (row >= q.seg1) {
+        row -= q.seg1;
         seg = 2;
       }
     }
-    return {seg, row, seg, row + g.hd / 2};
+    const int m = seg == 0 ? q.tm0 : seg == 1 ? q.tm1 : q.tm2;
+    return {m, row, m, row + q.hd / 2};
   }
-  if (g.epi == kEpiSwiglu) return {0, grp * R, 1, grp * R};
-  return {0, grp * 2 * R, 0, 0};   // one box of 2R rows
-}
-// Index of MMA tile t of group grp among the 16-row tiles of the matrix.
-SV_DEV int group_tile(const PhaseDesc& d, int grp, int t) {
-  const GemmDesc& g = d.g;
-  const int R = d.R;
-  if (g.epi == kEpiQkvRope) {
-    const int per = g.hd / (2 * R);
-    return (grp / per) * (g.hd / 16) + (grp % per) * (R / 8) + t;
-  }
-  return grp * (R / 8) + t;
+  if (q.epi == kEpiSwiglu) return {q.tm0, 8 * t, q.tm1, 8 * t};
+  return {q.tm0, 16 * t, q.tm0, 16 * t};   // one box of 16 rows
 }
 
-// x_norm = 2 phase, before its units: the producer thread copies the k-blocks
-// of X that the CTA's units read (the whole row once they span a row group,
-// else one or two runs of blocks) into the X region with one bulk copy per
-// token and run, completing on tp.xfull; every warp meanwhile folds the
-// per-tile sums of squares into s_inv[tok] = 1 / rms.  Ends with a CTA barrier.
-SV_DEV void tma_prepare_xg(const PhaseDesc& d, TmaPipe& tp, float* s_inv, unsigned char* xreg) {
+// 256-k blocks of chunk c (the last chunk may be short).
+SV_DEV int chunk_blocks(const TmaGeo& q, int c) {
+  return min(q.kc / kTmaK, (q.k - c * q.kc + kTmaK - 1) / kTmaK);
+}
+
+// Resident-X phase, before its units: the producer thread copies the ntok
+// input rows (k bf16 each; for an RMSNorm'd input the rows already carry the
+// norm's gain) into the X region with one bulk copy per token, completing on
+// tp.xfull; every warp meanwhile folds the per-tile sums of squares into
+// s_inv[tok] = 1 / rms (RMSNorm'd inputs only).  Ends with a CTA barrier.
+SV_DEV void tma_prepare_x(const PhaseDesc& d, TmaPipe& tp, float* s_inv, unsigned char* xreg) {
   const GemmDesc& g = d.g;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == kProducerWarp && lane == 0) {
-    const TmaRange r = tma_range(d);
-    const int n = r.u1 - r.u0;
-    int run[2][2] = {{0, 0}, {0, 0}}, nrun = 0;   // [kb begin, kb end)
-    if (n >= r.kbpt) {
-      run[0][0] = 0; run[0][1] = r.kbpt; nrun = 1;
-    } else if (n > 0) {
-      const int kb0 = r.u0 % r.kbpt, kb1 = (r.u1 - 1) % r.kbpt;
-      if (kb0 <= kb1) {
-        run[0][0] = kb0; run[0][1] = kb1 + 1; nrun = 1;
-      } else {
-        run[0][0] = kb0; run[0][1] = r.kbpt; run[1][0] = 0; run[1][1] = kb1 + 1; nrun = 2;
-      }
-    }
-    unsigned bytes = 0;
-    for (int q = 0; q < nrun; ++q) bytes += (unsigned)(min(run[q][1] * kTmaK, g.k) - run[q][0] * kTmaK) * 2u;
-    mbar_arrive_expect_tx(&tp.xfull, bytes * (unsigned)g.ntok);
-    const size_t pitch = (size_t)(g.k + kXPad) * 2;
-    for (int t = 0; t < g.ntok; ++t)
-      for (int q = 0; q < nrun; ++q) {
-        const int c0 = run[q][0] * kTmaK, c1 = min(run[q][1] * kTmaK, g.k);
-        bulk_g2s(xreg + t * pitch + (size_t)c0 * 2, (const bf16*)g.x + (size_t)t * g.ldx + c0,
-                 (unsigned)(c1 - c0) * 2u, &tp.xfull);
-      }
+  if (warp == kProducerWarp && lane == 0 && tma_geo(d, nullptr).n > 0) {
+    const int k = g.k, ntok = g.ntok, ldx = g.ldx;
+    const bf16* x = (const bf16*)g.x;
+    fence_proxy_async_global();   // X was written by other CTAs before the grid barrier
+    mbar_arrive_expect_tx(&tp.xfull, (unsigned)k * 2u * (unsigned)ntok);
+    const size_t pitch = (size_t)(k + kXPad) * 2;
+    for (int t = 0; t < ntok; ++t) bulk_g2s(xreg + t * pitch, x + (size_t)t * ldx, (unsigned)k * 2u, &tp.xfull);
     tp.xfills += 1;
   }
-  for (int tok = warp; tok < g.ntok; tok += kPersistThreads / 32) {
-    const float v = warp_inv_rms(g, tok, lane);
-    if (lane == 0) s_inv[tok] = v;
-  }
+  if (g.x_norm == 2)
+    for (int tok = warp; tok < g.ntok; tok += kPersistThreads / 32) {
+      const float v = warp_inv_rms(g, tok, lane);
+      if (lane == 0) s_inv[tok] = v;
+    }
   __syncthreads();
 }
 
-// Producer thread: issue unit i of the CTA's range into slot i mod S --
-// wait for the consumers to release the slot, announce the bytes, copy the
-// weight boxes and, when with_x, the X box.
-SV_DEV void tma_issue(const PhaseDesc& d, const TmaRange& r, int i, bool with_x, TmaPipe& tp,
-                      unsigned char* ring, unsigned char* xreg, const unsigned char* maps) {
-  const int slot = i % d.stages;
-  const unsigned f = tp.fills[slot];
-  if (!tma_wait(&tp.empty[slot], (f & 1u) ^ 1u, tp)) return;
-  const int u = r.u0 + i;
-  const int grp = u / r.kbpt, kb = u - grp * r.kbpt;
-  const GroupBoxes b = group_boxes(d, grp);
-  const bool xg = d.xm == kXGlobal;
-  mbar_arrive_expect_tx(&tp.full[slot], (unsigned)d.stage_bytes + (xg ? (unsigned)kXStageBytes : 0u));
-  unsigned char* st = ring + (size_t)slot * d.stage_bytes;
-  const int kc = kb * kTmaK;
-  const uint64_t pol = l2_evict_first();   // weights are read once per pass
-  if (d.paired) {
-    tma_load_2d_hint(st, maps + (size_t)d.tm[b.ma] * kTensorMapBytes, kc, b.ra, &tp.full[slot], pol);
-    tma_load_2d_hint(st + (size_t)d.R * kTmaRowBytes, maps + (size_t)d.tm[b.mb] * kTensorMapBytes, kc, b.rb,
-                     &tp.full[slot], pol);
-  } else {
-    tma_load_2d_hint(st, maps + (size_t)d.tm[0] * kTensorMapBytes, kc, b.ra, &tp.full[slot], pol);
-  }
-  if (with_x)
-    tma_load_2d(xreg + (size_t)slot * kXStageBytes, maps + (size_t)d.tm[3] * kTensorMapBytes, kc, 0,
-                &tp.full[slot]);
-  tp.fills[slot] = f + 1;
+// Producer thread: walks the CTA's units (tile group, chunk) in order,
+// issuing units [i, end) into the ring -- per unit: wait for the consumers
+// to release the slot, announce the bytes (the weights and, for streamed X,
+// the X boxes, even when those are issued later), copy the weight boxes
+// and, when with_x, the X boxes.  The walk keeps its position in registers;
+// no division on the way.
+struct TmaWalk {
+  int i, slot, grp, c, ng;
+  TileBoxes b0, b1;   // the group's tiles (kMaxGroupTiles = 2)
+};
+static_assert(kMaxGroupTiles == 2, "TmaWalk holds two tiles");
+
+SV_DEV void walk_group(const TmaGeo& q, TmaWalk& w) {
+  const int tb = q.t0 + w.grp * q.gt;
+  w.ng = min(q.gt, q.t1 - tb);
+  w.b0 = tile_boxes(q, tb);
+  if (w.ng > 1) w.b1 = tile_boxes(q, tb + 1);
 }
 
-// Producer thread: the X box of an already announced unit.
-SV_DEV void tma_issue_x(const PhaseDesc& d, const TmaRange& r, int i, TmaPipe& tp, unsigned char* xreg,
-                        const unsigned char* maps) {
-  if (tp.abort) return;
-  const int slot = i % d.stages;
-  const int u = r.u0 + i;
-  const int kb = u % r.kbpt;
-  tma_load_2d(xreg + (size_t)slot * kXStageBytes, maps + (size_t)d.tm[3] * kTensorMapBytes, kb * kTmaK, 0,
-              &tp.full[slot]);
+SV_DEV TmaWalk walk_start(const TmaGeo& q) {
+  TmaWalk w;
+  w.i = 0;
+  w.slot = 0;
+  w.grp = 0;
+  w.c = 0;
+  w.ng = 0;
+  if (q.n > 0) walk_group(q, w);
+  return w;
+}
+
+SV_DEV void walk_next(const TmaGeo& q, TmaWalk& w) {
+  ++w.i;
+  if (++w.slot == q.S) w.slot = 0;
+  if (++w.c == q.nchunks) {
+    w.c = 0;
+    ++w.grp;
+    if (w.i < q.n) walk_group(q, w);
+  }
+}
+
+SV_DEV void tma_issue_units(const TmaGeo& q, TmaWalk& w, int end, bool with_x, TmaPipe& tp, unsigned char* ring) {
+  const uint64_t pol = l2_evict_first();   // weights are read once per pass
+  const int kbs = q.kc / kTmaK;
+  const unsigned char* maps = q.maps;
+  for (; w.i < end; walk_next(q, w)) {
+    const int slot = w.slot;
+    const unsigned f = tp.fills[slot];
+    if (!tma_wait(&tp.empty[slot], (f & 1u) ^ 1u, tp)) return;
+    const int nkb = chunk_blocks(q, w.c);
+    const int k0 = w.c * q.kc;
+    const unsigned xbytes = q.xs ? (unsigned)(nkb * q.ntok * kTmaRowBytes) : 0u;
+    mbar_arrive_expect_tx(&tp.full[slot], (unsigned)(w.ng * nkb * kTileBlockBytes) + xbytes);
+    unsigned char* st = ring + (size_t)slot * q.sb;
+#pragma unroll
+    for (int gq = 0; gq < kMaxGroupTiles; ++gq) {
+      if (gq >= w.ng) break;
+      const TileBoxes b = gq ? w.b1 : w.b0;
+      const unsigned char* mapA = maps + (size_t)b.ma * kTensorMapBytes;
+      const unsigned char* mapB = maps + (size_t)b.mb * kTensorMapBytes;
+      unsigned char* dst = st + (size_t)gq * kbs * kTileBlockBytes;
+      for (int kb = 0; kb < nkb; ++kb, dst += kTileBlockBytes) {
+        tma_load_2d_hint(dst, mapA, k0 + kb * kTmaK, b.ra, &tp.full[slot], pol);
+        if (q.paired) tma_load_2d_hint(dst + 8 * kTmaRowBytes, mapB, k0 + kb * kTmaK, b.rb, &tp.full[slot], pol);
+      }
+    }
+    if (with_x) {
+      const unsigned char* mapX = maps + (size_t)q.tmx * kTensorMapBytes;
+      for (int kb = 0; kb < nkb; ++kb)
+        tma_load_2d(st + q.xoff + (size_t)kb * q.ntok * kTmaRowBytes, mapX, k0 + kb * kTmaK, 0, &tp.full[slot]);
+    }
+    tp.fills[slot] = f + 1;
+  }
 }
 
 // Producer thread, between arriving at the grid barrier that precedes GEMM
-// phase d and waiting on it: the weight boxes of its first units (weights
-// are read-only; X is not ready yet).  Returns how many units were issued.
-SV_DEV int tma_prefetch(const PhaseDesc& d, TmaPipe& tp, unsigned char* ring, unsigned char* xreg,
-                        const unsigned char* maps) {
-  const TmaRange r = tma_range(d);
-  // a phase whose X is bulk-copied after the barrier, with few units per CTA,
-  // takes only 3 units ahead, so that fewer weight copies are in flight when
-  // its X copies are issued (the 8B q/k/v phase's X arrives ~1 us sooner)
-  const int n = r.u1 - r.u0;
-  const int npre = min(n, d.xm == kXSmem && n <= 16 ? min(d.stages, 3) : d.stages);
-  for (int i = 0; i < npre; ++i) tma_issue(d, r, i, false, tp, ring, xreg, maps);
+// phase d and waiting on it: the weight boxes of its first d.prefetch units
+// (weights are read-only; X is not ready yet).  Returns how many units were
+// issued.
+SV_DEV int tma_prefetch(const PhaseDesc& d, TmaPipe& tp, unsigned char* ring, const unsigned char* maps) {
+  const TmaGeo q = tma_geo(d, maps);
+  TmaWalk w = walk_start(q);
+  const int npre = min(q.n, d.prefetch);
+  tma_issue_units(q, w, npre, false, tp, ring);
   return npre;
 }
 
-// Producer thread during GEMM phase d: X boxes of the npre prefetched units,
-// then every remaining unit.
-SV_DEV void tma_produce(const PhaseDesc& d, int npre, TmaPipe& tp, unsigned char* ring, unsigned char* xreg,
-                        const unsigned char* maps) {
-  const TmaRange r = tma_range(d);
-  const int n = r.u1 - r.u0;
-  const bool xg = d.xm == kXGlobal;
-  fence_proxy_async_global();   // X was written by other CTAs before the grid barrier
-  if (xg)
-    for (int i = 0; i < npre; ++i) tma_issue_x(d, r, i, tp, xreg, maps);
-  for (int i = npre; i < n; ++i) tma_issue(d, r, i, xg, tp, ring, xreg, maps);
+// Producer thread during GEMM phase d: the X boxes of the npre prefetched
+// units (streamed X), then every remaining unit.
+SV_DEV void tma_produce(const PhaseDesc& d, int npre, TmaPipe& tp, unsigned char* ring, const unsigned char* maps) {
+  const TmaGeo q = tma_geo(d, maps);
+  TmaWalk w = walk_start(q);
+  if (q.xs) {
+    fence_proxy_async_global();   // X was written by other CTAs before the grid barrier
+    const unsigned char* mapX = maps + (size_t)q.tmx * kTensorMapBytes;
+    for (; w.i < npre; walk_next(q, w)) {
+      if (tp.abort) return;
+      const int nkb = chunk_blocks(q, w.c);
+      unsigned char* st = ring + (size_t)w.slot * q.sb;
+      for (int kb = 0; kb < nkb; ++kb)
+        tma_load_2d(st + q.xoff + (size_t)kb * q.ntok * kTmaRowBytes, mapX, w.c * q.kc + kb * kTmaK, 0,
+                    &tp.full[w.slot]);
+    }
+  } else {
+    while (w.i < npre) walk_next(q, w);
+  }
+  tma_issue_units(q, w, q.n, q.xs != 0, tp, ring);
 }
 
-// Consumer warp t at the end of a row group: finish MMA tile t -- the
-// epilogue when this CTA covered every k of the group, else its CTA partial
-// and, for the last-arriving CTA of the group, the sum of the CTA partials in
-// CTA order and the epilogue.  s_inv (x_norm = 2, else null): 1 / rms per
-// token, applied to the finished sums of tokens 2ci, 2ci+1.  The last CTA
-// issues the epilogue's own input loads (residual or RoPE factors at token
-// 0's position pos0) together with the partial loads.  No other warp takes
-// part.
-SV_DEV void tma_tile_end(const PhaseDesc& d, const TmaRange& r, int grp, int kbs, int kbe, int pslot,
-                         const float (&tot)[1][4], float* __restrict__ partials, int* __restrict__ tickets,
-                         const float* s_inv, int pos0) {
-  const GemmDesc& g = d.g;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
-  const int tile = group_tile(d, grp, warp);
-  if (tile >= gemm_tiles_of(g)) return;
-  const float sc0 = s_inv ? s_inv[2 * ci] : 1.f, sc1 = s_inv ? s_inv[2 * ci + 1] : 1.f;
-  if (kbs == 0 && kbe == r.kbpt) {
-    const float y[1][4] = {{tot[0][0] * sc0, tot[0][1] * sc1, tot[0][2] * sc0, tot[0][3] * sc1}};
-    gemm_epilogue<1, false>(g, tile, y, gi, ci);
-    return;
-  }
-  float* mine = partials + (((size_t)blockIdx.x * 2 + pslot) * kMaxMmaTiles + warp) * 32 * 4;
-  *reinterpret_cast<float4*>(mine + (size_t)lane * 4) = make_float4(tot[0][0], tot[0][1], tot[0][2], tot[0][3]);
-  __syncwarp();
-  const int cfirst = warp_of_step((long long)grp * r.kbpt, r.total, r.nc);
-  const int clast = warp_of_step((long long)(grp + 1) * r.kbpt - 1, r.total, r.nc);
-  int old = 0;   // the acq_rel ticket publishes this partial and acquires the earlier ones
-  if (lane == 0) old = (int)atom_add_acq_rel_gpu(reinterpret_cast<unsigned*>(&tickets[tile]), 1u);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old != clast - cfirst) return;
-  __syncwarp();
-  // the epilogue's own inputs are loaded together with the first partials
-  EpiIn pre;
-  gemm_epi_load<false>(g, tile, pos0, gi, ci, pre);
-  float4 pv[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int c = cfirst + q;
-    pv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c <= clast) {
-      const int sl = (first_step_of_warp(c, r.total, r.nc) / r.kbpt == grp) ? 0 : 1;
-      pv[q] = __ldcg(reinterpret_cast<const float4*>(
-          partials + (((size_t)c * 2 + sl) * kMaxMmaTiles + warp) * 32 * 4 + (size_t)lane * 4));
-    }
-  }
-  float sum[1][4] = {{0.f, 0.f, 0.f, 0.f}};   // CTA order
-  for (int c = cfirst; c <= clast; ++c) {
-    float4 v;
-    if (c - cfirst < 2) {
-      v = c == cfirst ? pv[0] : pv[1];
-    } else {
-      const int sl = (first_step_of_warp(c, r.total, r.nc) / r.kbpt == grp) ? 0 : 1;
-      v = __ldcg(reinterpret_cast<const float4*>(
-          partials + (((size_t)c * 2 + sl) * kMaxMmaTiles + warp) * 32 * 4 + (size_t)lane * 4));
-    }
-    sum[0][0] += v.x;
-    sum[0][1] += v.y;
-    sum[0][2] += v.z;
-    sum[0][3] += v.w;
-  }
-  sum[0][0] *= sc0;
-  sum[0][1] *= sc1;
-  sum[0][2] *= sc0;
-  sum[0][3] *= sc1;
-  gemm_epilogue<1, false>(g, tile, sum, gi, ci, &pre);
-  if (lane == 0) tickets[tile] = 0;
+// One 64-k step of a tile: rows gi / gi + 8 of the tile's 16-row block at
+// byte offset boff (the step's 128-byte column) -- the thread's 16
+// consecutive k at ci * 16 -- against the X words of token gi.
+SV_DEV void tma_step(float (&acc)[4], const unsigned char* blk, const uint4& x0, const uint4& x1, int gi) {
+  const uint4 a0 = *reinterpret_cast<const uint4*>(blk + gi * kTmaRowBytes);
+  const uint4 a1 = *reinterpret_cast<const uint4*>(blk + gi * kTmaRowBytes + 16);
+  const uint4 b0 = *reinterpret_cast<const uint4*>(blk + (gi + 8) * kTmaRowBytes);
+  const uint4 b1 = *reinterpret_cast<const uint4*>(blk + (gi + 8) * kTmaRowBytes + 16);
+  mma_bf16_16816(acc, a0.x, b0.x, a0.y, b0.y, x0.x, x0.y);
+  mma_bf16_16816(acc, a0.z, b0.z, a0.w, b0.w, x0.z, x0.w);
+  mma_bf16_16816(acc, a1.x, b1.x, a1.y, b1.y, x1.x, x1.y);
+  mma_bf16_16816(acc, a1.z, b1.z, a1.w, b1.w, x1.z, x1.w);
 }
 
-// Consumer warps during GEMM phase d.  Warp t < T = R/8 owns MMA tile t of
-// every unit and runs its four 64-k steps, each into its own accumulator
-// chain (added in step order at the end of the group); warps t >= T only
-// keep the ring bookkeeping.  cpar: per-slot parity of the next completion
-// of each stage's full barrier (identical in every consumer warp).
-// stamp (optional): atomicMax of the globaltimer when the last unit arrived.
-template <int XM>
+// Consumer warps during GEMM phase d (see the file comment).  cpar: per-slot
+// parity of the next completion of each stage's full barrier (identical in
+// every consumer warp).  red: the group-partial area (kRedBytes).  s_inv:
+// 1 / rms per token (RMSNorm'd inputs).  stamp (optional): atomicMax of the
+// globaltimer when the last unit arrived.
+template <bool kResident>
 SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const unsigned char* ring,
-                        const unsigned char* xreg, const float* s_inv, float* __restrict__ partials,
-                        int* __restrict__ tickets, unsigned long long* stamp) {
+                        const unsigned char* xreg, float4* red, const float* s_inv, unsigned long long* stamp) {
   const GemmDesc& g = d.g;
-  const TmaRange r = tma_range(d);
-  const int n = r.u1 - r.u0;
+  const TmaGeo q = tma_geo(d, nullptr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
-  const int R = d.R, T = R / 8, S = d.stages, sb = d.stage_bytes;
-  if (warp >= T) {   // not a tile owner in this phase (the producer warp never gets here)
-    for (int i = 0; i < n; ++i) cpar ^= 1u << (i % S);
-    return;
-  }
+  const int spt = q.kc / kStepK;            // 64-k steps per tile in a stage (16 or 8)
+  const int kbs = q.kc / kTmaK;             // 256-k blocks per tile in a stage
+  // this warp's two steps of every stage: tile (within the group), byte
+  // offset of the step's 128-byte column in the stage, its k and, streamed,
+  // its X column
+  const int sA = warp, sB = warp + kCWarps;
+  const int gA = sA / spt, kA = sA % spt, gB = sB / spt, kB = sB % spt;
+  const int offA = (gA * kbs + kA / 4) * kTileBlockBytes + (kA % 4) * (kStepK * 2) + ci * 32;
+  const int offB = (gB * kbs + kB / 4) * kTileBlockBytes + (kB % 4) * (kStepK * 2) + ci * 32;
+  const bool has_tok = gi < q.ntok;
+  const size_t xs_pitch = (size_t)(q.k + kXPad) * 2;
+  const int xoffA = q.xoff + ((kA / 4) * q.ntok + gi) * kTmaRowBytes + (kA % 4) * (kStepK * 2) + ci * 32;
+  const int xoffB = q.xoff + ((kB / 4) * q.ntok + gi) * kTmaRowBytes + (kB % 4) * (kStepK * 2) + ci * 32;
+  const unsigned char* xrow = xreg + gi * xs_pitch + ci * 32;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
-  const int t = warp;
-  const int arow = d.paired ? 8 * t + gi : 16 * t + gi;
-  const int brow = d.paired ? R + 8 * t + gi : 16 * t + 8 + gi;
-  const bool has_tok = gi < g.ntok;
-  const int k = g.k;
-  const size_t xs_pitch = (size_t)(k + kXPad) * 2;
-  const unsigned arrivals = (unsigned)(kMaxMmaTiles / T);   // the empty barrier expects kMaxMmaTiles
-  float acc[kTmaSteps][4];
-#pragma unroll
-  for (int s = 0; s < kTmaSteps; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
-  int pslot = 0;
-  int kbs = n > 0 ? r.u0 % r.kbpt : 0;
-  const bool xg = XM == kXSmem && g.x_norm == 2;
-  const int pos0 = g.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
+  const bool xn = g.x_norm == 2;
+  const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
+  const int tiles_all = gemm_tiles_of(g);
   bool xok = true;
-  if (xg && n > 0) xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
-
+  if (kResident && q.n > 0) xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
+  int i = 0, slot = 0;
 #pragma unroll 1
-  for (int i = 0; i < n; ++i) {
-    const int slot = i % S;
-    const int u = r.u0 + i;
-    const int grp = u / r.kbpt, kb = u - grp * r.kbpt;
-    const bool ok = tma_wait(&tp.full[slot], (cpar >> slot) & 1u, tp) && xok;
-    cpar ^= 1u << slot;
-    if (stamp && i == n - 1 && threadIdx.x == 0) {
-      unsigned long long tm;
-      asm volatile("mov.u64 %0, %globaltimer;" : "=l"(tm));
-      atomicMax(stamp, tm);
-    }
-    if (ok) {
-      const unsigned char* st = ring + (size_t)slot * sb + ci * 32;
-#pragma unroll
-      for (int s = 0; s < kTmaSteps; ++s) {
-        const int kg = kb * kTmaK + s * kStepK;
-        if (kg < k) {
-          const unsigned char* ap = st + arow * kTmaRowBytes + s * (kStepK * 2);
-          const unsigned char* bp = st + brow * kTmaRowBytes + s * (kStepK * 2);
-          const uint4 a0 = *reinterpret_cast<const uint4*>(ap);
-          const uint4 a1 = *reinterpret_cast<const uint4*>(ap + 16);
-          const uint4 b0 = *reinterpret_cast<const uint4*>(bp);
-          const uint4 b1 = *reinterpret_cast<const uint4*>(bp + 16);
+  for (int grp = 0; grp < q.ngroups; ++grp) {
+    const int tb = q.t0 + grp * q.gt, ng = min(q.gt, q.t1 - tb);
+    const bool liveA = gA < ng, liveB = gB < ng;
+    float accA[4] = {0.f, 0.f, 0.f, 0.f}, accB[4] = {0.f, 0.f, 0.f, 0.f};
+    int kgA = kA * kStepK, kgB = kB * kStepK;   // the steps' k in this chunk
+#pragma unroll 1
+    for (int c = 0; c < q.nchunks; ++c, ++i, kgA += q.kc, kgB += q.kc) {
+      const bool ok = tma_wait(&tp.full[slot], (cpar >> slot) & 1u, tp) && xok;
+      cpar ^= 1u << slot;
+      if (stamp && i == q.n - 1 && threadIdx.x == 0) {
+        unsigned long long tm;
+        asm volatile("mov.u64 %0, %globaltimer;" : "=l"(tm));
+        atomicMax(stamp, tm);
+      }
+      if (ok) {
+        const unsigned char* st = ring + (size_t)slot * q.sb;
+        if (liveA && kgA < q.k) {
           uint4 x0 = zero4, x1 = zero4;
           if (has_tok) {
-            const unsigned char* xp =
-                XM == kXSmem ? xreg + gi * xs_pitch + (size_t)(kg + ci * 16) * 2
-                             : xreg + (size_t)slot * kXStageBytes + gi * kTmaRowBytes + s * (kStepK * 2) + ci * 32;
+            const unsigned char* xp = kResident ? xrow + (size_t)kgA * 2 : st + xoffA;
             x0 = *reinterpret_cast<const uint4*>(xp);
             x1 = *reinterpret_cast<const uint4*>(xp + 16);
           }
-          mma_bf16_16816(acc[s], a0.x, b0.x, a0.y, b0.y, x0.x, x0.y);
-          mma_bf16_16816(acc[s], a0.z, b0.z, a0.w, b0.w, x0.z, x0.w);
-          mma_bf16_16816(acc[s], a1.x, b1.x, a1.y, b1.y, x1.x, x1.y);
-          mma_bf16_16816(acc[s], a1.z, b1.z, a1.w, b1.w, x1.z, x1.w);
+          tma_step(accA, st + offA, x0, x1, gi);
+        }
+        if (liveB && kgB < q.k) {
+          uint4 x0 = zero4, x1 = zero4;
+          if (has_tok) {
+            const unsigned char* xp = kResident ? xrow + (size_t)kgB * 2 : st + xoffB;
+            x0 = *reinterpret_cast<const uint4*>(xp);
+            x1 = *reinterpret_cast<const uint4*>(xp + 16);
+          }
+          tma_step(accB, st + offB, x0, x1, gi);
         }
       }
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&tp.empty[slot]);
+      if (++slot == q.S) slot = 0;
     }
-    __syncwarp();
-    if (lane == 0 && ok) mbar_arrive_count(&tp.empty[slot], arrivals);
-    if (kb == r.kbpt - 1 || i == n - 1) {
-      float tot[1][4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) tot[0][e] = ((acc[0][e] + acc[1][e]) + acc[2][e]) + acc[3][e];
-      if (!tp.abort) tma_tile_end(d, r, grp, kbs, kb + 1, pslot, tot, partials, tickets, xg ? s_inv : nullptr, pos0);
-#pragma unroll
-      for (int s = 0; s < kTmaSteps; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
-      pslot = 1;
-      kbs = 0;
+    // end of the group: partials of every warp, then one warp per tile adds
+    // them in warp order and runs the epilogue
+    float4* rb = red + (size_t)(kResident ? (grp & 1) : 0) * kCWarps * 32;   // buffer (resident) or tile 0
+    if (q.gt == 1) {
+      rb[warp * 32 + lane] = make_float4(accA[0] + accB[0], accA[1] + accB[1], accA[2] + accB[2], accA[3] + accB[3]);
+    } else {
+      rb[warp * 32 + lane] = make_float4(accA[0], accA[1], accA[2], accA[3]);
+      rb[(kCWarps + warp) * 32 + lane] = make_float4(accB[0], accB[1], accB[2], accB[3]);
     }
+    named_sync(kGemmBarrier, kConsumerThreads);
+    for (int gq = 0; gq < ng; ++gq) {
+      const int ew = kResident ? grp % kCWarps : gq;   // the tile's epilogue warp
+      if (warp != ew || tp.abort) continue;
+      const int tile = tb + gq;
+      if (tile >= tiles_all) continue;
+      const float4* pt = rb + (size_t)gq * kCWarps * 32 + lane;
+      float y[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int w = 0; w < kCWarps; ++w) {
+        const float4 v = pt[w * 32];
+        y[0][0] += v.x;
+        y[0][1] += v.y;
+        y[0][2] += v.z;
+        y[0][3] += v.w;
+      }
+      if (xn) {
+        const float sc0 = s_inv[2 * ci], sc1 = s_inv[2 * ci + 1];
+        y[0][0] *= sc0;
+        y[0][1] *= sc1;
+        y[0][2] *= sc0;
+        y[0][3] *= sc1;
+      }
+      EpiIn pre;
+      gemm_epi_load<false>(g, tile, pos0, gi, ci, pre);
+      gemm_epilogue<1, false>(g, tile, y, gi, ci, &pre);
+    }
+    // streamed X: the partial area is not double-buffered -- the next
+    // group's partials wait until the epilogue warps have read these
+    if (!kResident && grp + 1 < q.ngroups) named_sync(kGemmBarrier, kConsumerThreads);
   }
 }
 
@@ -433,8 +472,4 @@ SV_DEV void tma_drain(TmaPipe& tp) {
   }
 }
 
-}  // namespace sv
-
-namespace sv {
-static_assert(kProducerWarp >= kMaxMmaTiles, "the producer warp must not own an MMA tile");
 }  // namespace sv

@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--mix", type=float, default=0.5, help="draft/target-previous-logit mix lambda")
     ap.add_argument("--prompt", type=int, default=512)
     ap.add_argument("--new-tokens", type=int, default=128)
-    ap.add_argument("--workload", choices=["8b", "1b"], default="8b")
+    ap.add_argument("--workload", choices=["8b", "1b", "8b-q4"], default="8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--ar-tokens", type=int, default=128)
@@ -77,8 +77,12 @@ def parse():
 
 def workload_shapes(name):
     import workloads
+    from dataclasses import replace
     if name == "8b":
         return workloads.EIGHT_B, workloads.ONE_B, "8B-shaped target + 1B-shaped draft"
+    if name == "8b-q4":
+        return (replace(workloads.EIGHT_B, dtype="q4"), replace(workloads.ONE_B, dtype="q4"),
+                "8B-shaped 4-bit target + 1B-shaped 4-bit draft")
     return workloads.ONE_B, None, "1B-shaped target + its first 2 layers as draft"
 
 
@@ -349,11 +353,13 @@ def main():
         dshape = replace(dshape, n_layers=min(args.layers, dshape.n_layers)) if dshape else None
         wl += f" (first {args.layers} layers, profiling only)"
     K = args.k
-    tw = workloads.make_weights(tshape, 1, device="cuda")
+    q4 = tshape.dtype == "q4"
+    mk = workloads.make_q4_weights if q4 else workloads.make_weights
+    tw = mk(tshape, 1, device="cuda")
     if dshape is None:
         dshape, dw = workloads.prefix_draft(tshape, tw, 2)
     else:
-        dw = workloads.make_weights(dshape, 2, device="cuda")
+        dw = mk(dshape, 2, device="cuda")
     torch.cuda.synchronize()
     max_ctx = args.prompt + args.new_tokens + 4 * (K + 1) + 64
     stream = torch.cuda.Stream()
@@ -653,7 +659,7 @@ def main():
 
     # ---- oracle on the host cores (rank 0, N = 1 only) ----
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not q4:
         del dec
         thw = host_weights(tshape, 1, layers=2)
         dhw = host_weights(dshape, 2, layers=2)
@@ -666,12 +672,15 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": nsteps, "warmup": args.warmup, "ms_per_step": ms_max / max(1, nsteps),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (random N(0,0.02^2) weights, uniform-random prompts)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (4-bit weights)" if q4 else "bf16",
+        "data": ("synthetic (random 4-bit codes with bf16 group scales, weights of std ~0.02, uniform-random prompts)"
+                 if q4 else "synthetic (random N(0,0.02^2) weights, uniform-random prompts)"),
         "config": {"workload": wl, "batch": 1, "K": K, "prompt": args.prompt,
                    "new_tokens_per_generation": args.new_tokens, "temperature": args.temperature,
                    "mix_lambda": args.mix, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (17.5 GB of weights per step)"},
+                   "l2": f"inputs larger than L2 ({(st['verify_weight_bytes'] + st['draft_weight_bytes']) / 1e9:.1f} "
+                         f"GB of weights per step)"},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": st["kernels_per_step"] * nsteps,

@@ -69,6 +69,19 @@ extern "C" {
 
 #define SPEC_DTYPE_F32      0
 #define SPEC_DTYPE_BF16     1
+/* 4-bit group-quantized weights ("Speculative decoding internals",
+ * section "怎麼測自己的加速倍率": the measured models are Q4 files).  Every
+ * weight matrix [n][k] (wq, wk, wv, wo, w_gate, w_up, w_down, lm_head) is
+ * one buffer: packed signed 4-bit codes [n][k/2] (byte b of a row holds
+ * element 2b in its low nibble and 2b+1 in its high nibble, two's
+ * complement, codes -8..7), immediately followed by bf16 scales stored
+ * group-major [k/64][n] (scale of row r, 64-k group j at index j*n + r);
+ * weight = scale x code.  The embedding is bf16, norm gains fp32, and the
+ * model computes in bf16 with fp32 accumulation like a bf16 model (KV cache
+ * bf16).  4-bit models run only on the persistent kernel: batch 1, K <= 7,
+ * d_model, ffn_dim and n_heads*head_dim multiples of 256, vocab and
+ * n_kv_heads*head_dim multiples of 8, prompts of at least 10 tokens. */
+#define SPEC_DTYPE_Q4       2
 
 /* ---- per-step flags (spec_step out_flags) ---- */
 #define SPEC_FLAG_RESID_ZERO   0x1u  /* rejection with zero residual mass; drew from p */
@@ -110,7 +123,7 @@ typedef struct spec_layer_weights {
 typedef struct spec_model_desc {
     int   n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
     float rope_theta, rms_eps;
-    int   dtype;                        /* SPEC_DTYPE_F32 or SPEC_DTYPE_BF16 */
+    int   dtype;                        /* SPEC_DTYPE_F32, SPEC_DTYPE_BF16 or SPEC_DTYPE_Q4 */
     const void* embed;                  /* [vocab][d_model] */
     const void* final_norm;             /* [d_model] fp32 */
     const void* lm_head;                /* [vocab][d_model] */

@@ -21,6 +21,8 @@ ERRORS = {-1: "SPEC_E_ARG", -2: "SPEC_E_VOCAB", -3: "SPEC_E_SHAPE", -4: "SPEC_E_
           -5: "SPEC_E_CUDA", -6: "SPEC_E_OOM", -7: "SPEC_E_TIMEOUT", -8: "SPEC_E_STATE"}
 SPEC_DTYPE_F32 = 0
 SPEC_DTYPE_BF16 = 1
+SPEC_DTYPE_Q4 = 2
+_DTYPES = {"f32": SPEC_DTYPE_F32, "bf16": SPEC_DTYPE_BF16, "q4": SPEC_DTYPE_Q4}
 SPEC_MAX_BATCH = 64
 SPEC_FLAG_RESID_ZERO = 0x1
 SPEC_FLAG_ALL_ACCEPTED = 0x2
@@ -158,16 +160,16 @@ def _ptr(t):
 
 def model_desc(shape, weights):
     """ModelDesc for a shape (attributes n_layers, d_model, n_heads, n_kv_heads,
-    head_dim, ffn_dim, vocab, rope_theta, rms_eps, dtype 'f32'|'bf16') and a
+    head_dim, ffn_dim, vocab, rope_theta, rms_eps, dtype 'f32'|'bf16'|'q4') and a
     weights dict {'embed', 'final_norm', 'lm_head', 'layers': [dict]} of CUDA
-    tensors.  Returns (desc, keepalive)."""
+    tensors ('q4': every matrix one uint8 buffer of packed codes followed by
+    group-major bf16 scales, see include/specverify.h).  Returns (desc, keepalive)."""
     layers = (LayerWeights * shape.n_layers)()
     for i, lw in enumerate(weights["layers"]):
         for n in _LAYER_FIELDS:
             setattr(layers[i], n, lw[n].data_ptr())
     d = ModelDesc(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
-                  shape.ffn_dim, shape.vocab, shape.rope_theta, shape.rms_eps,
-                  SPEC_DTYPE_F32 if shape.dtype == "f32" else SPEC_DTYPE_BF16,
+                  shape.ffn_dim, shape.vocab, shape.rope_theta, shape.rms_eps, _DTYPES[shape.dtype],
                   weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
                   weights["lm_head"].data_ptr(), layers)
     return d, (layers, weights)

@@ -43,7 +43,10 @@ std::atomic<int> g_fail_alloc_at{0};
 std::atomic<long long> g_device_bytes{0};
 
 struct ModelState {
+  // d.dtype is the arithmetic dtype (a 4-bit model computes like a bf16
+  // model, with q4 set: its GEMMs stream packed codes and scales)
   spec_model_desc d{};
+  bool q4 = false;
   std::vector<spec_layer_weights> layers;
   void* kc = nullptr;   // [n_layers][hkv][cap][hd]
   void* vc = nullptr;
@@ -53,11 +56,13 @@ struct ModelState {
   int esize = 4;
   int qkv_rows() const { return (d.n_heads + 2 * d.n_kv_heads) * d.head_dim; }
   size_t layer_kv_elems(int cap) const { return (size_t)d.n_kv_heads * cap * d.head_dim; }
+  // bytes one weight costs in a pass: 4-bit codes plus a bf16 scale per 64
+  double wbytes() const { return q4 ? 0.5 + 2.0 / 64.0 : esize; }
   double matrix_bytes_layer() const {
     const double hd = d.head_dim, dm = d.d_model;
-    return ((2.0 * d.n_heads + 2.0 * d.n_kv_heads) * hd * dm + 3.0 * dm * d.ffn_dim) * esize;
+    return ((2.0 * d.n_heads + 2.0 * d.n_kv_heads) * hd * dm + 3.0 * dm * d.ffn_dim) * wbytes();
   }
-  double head_bytes() const { return (double)d.vocab * d.d_model * esize; }
+  double head_bytes() const { return (double)d.vocab * d.d_model * wbytes(); }
   double weight_bytes() const { return d.n_layers * matrix_bytes_layer() + head_bytes(); }
   double kv_bytes_per_token() const { return 2.0 * d.n_layers * d.n_kv_heads * d.head_dim * esize; }
 };
@@ -79,9 +84,14 @@ struct PersistFwd {
 struct spec_ctx {
   ModelState tgt, drf;
   bool persist = false;            // persistent forward kernels (bf16 models)
-  // draft passes 1..K (0..K-1), verify (K), plain decoding (K+1), and the
-  // last scored prompt position of the draft (K+2) and of the target (K+3)
+  // draft passes 1..K (0..K-1), verify (K), plain decoding (K+1), the last
+  // scored prompt position of the draft (K+2) and of the target (K+3), and
+  // for 4-bit models the prefill chunks of kPrefillChunk positions at the
+  // host-set position: target (K+4), target with its LM-head rows (K+5),
+  // draft (K+6)
   PersistFwd pforward[20];
+  bool q4 = false;                 // a 4-bit model: prefill runs the persistent chunks
+  float* logits_chunk = nullptr;   // [kPrefillChunk][V] LM-head rows of the last target chunk
   PhaseDesc* phase_dev = nullptr;
   unsigned* bar = nullptr;
   int K = 0;
@@ -196,8 +206,16 @@ int check_model(const spec_model_desc* m, const char* which, std::string* why) {
     *why = std::string(which) + ": non-positive dimension or parameter";
     return SPEC_E_SHAPE;
   }
-  if (m->dtype != SPEC_DTYPE_F32 && m->dtype != SPEC_DTYPE_BF16) {
+  if (m->dtype != SPEC_DTYPE_F32 && m->dtype != SPEC_DTYPE_BF16 && m->dtype != SPEC_DTYPE_Q4) {
     *why = std::string(which) + ": unknown dtype";
+    return SPEC_E_SHAPE;
+  }
+  if (m->dtype == SPEC_DTYPE_Q4 &&
+      (m->d_model % 256 || m->ffn_dim % 256 || (m->n_heads * m->head_dim) % 256 || m->vocab % 8 ||
+       (m->n_kv_heads * m->head_dim) % 8)) {
+    *why = std::string(which) +
+           ": 4-bit models need d_model, ffn_dim and n_heads*head_dim multiples of 256, vocab and "
+           "n_kv_heads*head_dim multiples of 8";
     return SPEC_E_SHAPE;
   }
   if (!valid_hd(m->head_dim) || m->n_heads % m->n_kv_heads != 0) {
@@ -206,7 +224,7 @@ int check_model(const spec_model_desc* m, const char* which, std::string* why) {
     *why = buf;
     return SPEC_E_SHAPE;
   }
-  const int kmul = m->dtype == SPEC_DTYPE_BF16 ? 64 : 4;
+  const int kmul = m->dtype == SPEC_DTYPE_F32 ? 4 : 64;
   if (m->d_model % kmul || m->ffn_dim % kmul || (m->n_heads * m->head_dim) % kmul ||
       m->ffn_dim % 8) {
     snprintf(buf, sizeof buf, "%s: d_model, ffn_dim and n_heads*head_dim must be multiples of %d",
@@ -298,6 +316,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
   const int dm = d.d_model, hq = d.n_heads, hkv = d.n_kv_heads, hd = d.head_dim;
   const int qkvr = m.qkv_rows();
   const int dt = d.dtype;
+  const int q4 = m.q4 ? 1 : 0;
   std::vector<Op> ops;
   Op op{};
   op.kind = kPhaseEmbed;
@@ -340,6 +359,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     g.pos_base = pos_idx; g.pos_off = pos_off; g.rope_cos = m.rope_cos; g.rope_sin = m.rope_sin;
     g.spt = sq.spt; g.pos_ld = kStateLd;
     g.q_out = c->q; g.kc = kc; g.vc = vc;
+    g.q4 = q4;
     ops.push_back(q);
     Op at{};
     at.kind = kPhaseAttn;
@@ -373,6 +393,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
       o.g.gain_next = (const float*)w.ffn_norm;
     }
     o.g.ss_out = c->ss; o.g.ss_ld = c->tok_max;
+    o.g.q4 = q4;
     ops.push_back(o);
     Op gu{};
     gu.kind = kPhaseGemm;
@@ -380,6 +401,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     norm_x(gu.g, w.ffn_norm, 0);
     gu.g.ss_in = c->ss; gu.g.ss_ld = c->tok_max; gu.g.eps = d.rms_eps;
     gu.g.epi = kEpiSwiglu; gu.g.out = c->hbuf; gu.g.ldo = d.ffn_dim;
+    gu.g.q4 = q4;
     ops.push_back(gu);
     Op dn{};
     dn.kind = kPhaseGemm;
@@ -391,6 +413,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     }
     dn.g.ss_out = c->ss; dn.g.ss_ld = c->tok_max;
     dn.g.early_prefetch = 1;   // follows the gate/up GEMM
+    dn.g.q4 = q4;
     ops.push_back(dn);
   }
   if (lrows > 0) {
@@ -400,6 +423,7 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
     norm_x(h.g, d.final_norm, lrow0);
     h.g.ss_in = c->ss + lrow0; h.g.ss_ld = c->tok_max; h.g.eps = d.rms_eps;
     h.g.epi = kEpiStore; h.g.out = logits; h.g.ldo = d.vocab;
+    h.g.q4 = q4;
     ops.push_back(h);
   }
   return ops;
@@ -717,6 +741,10 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     return fail(nullptr, SPEC_E_ARG, "batch must be in 1..SPEC_MAX_BATCH");
   if (opts->batch > 1 && (target->dtype != SPEC_DTYPE_BF16 || draft->dtype != SPEC_DTYPE_BF16))
     return fail(nullptr, SPEC_E_ARG, "batch > 1 needs bf16 target and draft models");
+  const bool any_q4 = target->dtype == SPEC_DTYPE_Q4 || draft->dtype == SPEC_DTYPE_Q4;
+  if (any_q4 && (opts->flags & (SPEC_OPT_NO_PERSIST | SPEC_OPT_TIMING)))
+    return fail(nullptr, SPEC_E_ARG, "4-bit models run only on the persistent kernel (no NO_PERSIST / TIMING)");
+  if (any_q4 && K + 1 > kPrefillChunk) return fail(nullptr, SPEC_E_ARG, "4-bit models need K <= 7");
   if (opts->batch > 1 && opts->draft_mix_lambda != 0.f)
     return fail(nullptr, SPEC_E_ARG, "batch > 1 does not support draft_mix_lambda");
   if (opts->draft_lookup < 0 || opts->draft_lookup > kLookupMaxN)
@@ -740,9 +768,11 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   c->max_chunks = (c->cap + kAttnChunk - 1) / kAttnChunk;
   auto setup_model = [&](ModelState& m, const spec_model_desc* d) {
     m.d = *d;
+    m.q4 = d->dtype == SPEC_DTYPE_Q4;
+    if (m.q4) m.d.dtype = SPEC_DTYPE_BF16;   // the arithmetic and the KV cache are bf16
     m.layers.assign(d->layers, d->layers + d->n_layers);
     m.d.layers = m.layers.data();
-    m.esize = d->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+    m.esize = m.d.dtype == SPEC_DTYPE_BF16 ? 2 : 4;
   };
   setup_model(c->tgt, target);
   setup_model(c->drf, draft);
@@ -863,7 +893,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   // Persistent forward kernels: both models bf16, and the weight ring plus
   // K+1 tokens of normalised input (or the attention tile) fit one CTA's
   // shared memory.
-  if (B == 1 && target->dtype == SPEC_DTYPE_BF16 && draft->dtype == SPEC_DTYPE_BF16 &&
+  if (B == 1 && c->tgt.d.dtype == SPEC_DTYPE_BF16 && c->drf.d.dtype == SPEC_DTYPE_BF16 &&
       !(opts->flags & (SPEC_OPT_TIMING | SPEC_OPT_NO_PERSIST))) {
     PersistLayout lay_t{}, lay_d{};
     const bool lay_ok = persist_layout(target->head_dim, K + 1, target->d_model, &lay_t) &&
@@ -880,7 +910,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
                                      attn_partial_floats(maxN, (int)hqmax, (int)hdmax, c->max_chunks);
       int* const dattn_tick = c->dattn_tick;   // sized for kGemmMaxTok >= K + 1 tokens
       auto add = [&](int idx, const std::vector<Op>& ops) {
-        const bool drf = idx < K || idx == K + 2;
+        const bool drf = idx < K || idx == K + 2 || idx == K + 6;
         const PersistLayout& lay = drf ? lay_d : lay_t;
         start[idx] = all.size();
         for (const Op& op : ops) {
@@ -911,6 +941,16 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
       add(K + 2, forward_ops(c, c->drf, 1, c->seq, c->st, -1, c->st, -1, 0, 0, nullptr, true));
       add(K + 3, forward_ops(c, c->tgt, 1, c->seq, c->st, -1, c->st, -1, 0,
                              opts->draft_mix_lambda != 0.f ? 1 : 0, c->logits_p + (size_t)K * V, true));
+      int nf = K + 4;
+      if (any_q4) {   // prefill chunks at the host-set position st[3]
+        INIT_TRY(dalloc(c, &c->logits_chunk, sizeof(float) * (size_t)kPrefillChunk * V));
+        const int32_t* ep = c->st + 3;
+        add(K + 4, forward_ops(c, c->tgt, kPrefillChunk, c->seq, ep, 0, ep, 0, 0, 0, nullptr, true));
+        add(K + 5, forward_ops(c, c->tgt, kPrefillChunk, c->seq, ep, 0, ep, 0, 0, kPrefillChunk, c->logits_chunk,
+                               true));
+        add(K + 6, forward_ops(c, c->drf, kPrefillChunk, c->seq, ep, 0, ep, 0, 0, 0, nullptr, true));
+        nf = K + 7;
+      }
       if (encodable) {
         INIT_TRY(dalloc(c, &c->phase_dev, sizeof(PhaseDesc) * all.size()));
         INIT_TRY(cudaMemcpy(c->phase_dev, all.data(), sizeof(PhaseDesc) * all.size(), cudaMemcpyHostToDevice));
@@ -927,14 +967,14 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
           INIT_TRY(dalloc(c, &times, sizeof(unsigned long long) * words));
           INIT_TRY(cudaMemset(times, 0, sizeof(unsigned long long) * words));
         }
-        for (int f = 0; f <= K + 3; ++f) {
+        for (int f = 0; f < nf; ++f) {
           PersistFwd& pf = c->pforward[f];
           pf.host.assign(all.begin() + start[f], all.begin() + start[f] + count[f]);
           if (times) pf.desc.times = times + f + (size_t)kPhaseStamps * start[f];
           pf.desc.phases = c->phase_dev + start[f];
           pf.desc.nphases = (int)count[f];
           pf.desc.tmaps = tmaps_dev;
-          const bool drf = f < K || f == K + 2;
+          const bool drf = f < K || f == K + 2 || f == K + 6;
           pf.desc.ring_bytes = (int)(drf ? lay_d.ring : lay_t.ring);
           pf.desc.bar = c->bar;
           pf.desc.err = res_err(c);
@@ -946,6 +986,13 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
       }
     }
   }
+  if (any_q4 && !c->persist) {
+    free_ctx(c);
+    return fail(nullptr, SPEC_E_SHAPE,
+                "4-bit models need the persistent kernel, which this pair does not fit (batch 1, K <= 7, "
+                "head dims 32/64/128)");
+  }
+  c->q4 = any_q4;
   if (opts->flags & SPEC_OPT_TIMING) {
     const int n = 2 * (4 * target->n_layers + 1);
     c->ev.resize(n);
@@ -1004,7 +1051,25 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
   // too (both models), so that both KV caches hold the same bits for it.
   const int nk = c->persist ? n - 1 : n;   // positions scored one kernel per operation
   Launch Lc{c};
-  for (int b = 0; b < c->B; ++b) {   // sequence by sequence, in chunks of positions
+  if (c->q4) {   // 4-bit models: persistent chunks of kPrefillChunk positions (the last one overlapping)
+    if (nk < kPrefillChunk) return fail(c, SPEC_E_ARG, "4-bit models need prompts of at least 10 tokens");
+    for (int p0 = 0; p0 < nk; p0 += kPrefillChunk) {
+      const int s0 = std::min(p0, nk - kPrefillChunk);
+      const bool last = p0 + kPrefillChunk >= nk;
+      rc = set_eager_pos(c, s0);
+      if (rc) return rc;
+      if (!c->lookup) forward_persist(Lc, K + 6);
+      forward_persist(Lc, last && mix ? K + 5 : K + 4);
+      CUDA_TRY(c, Lc.e);
+      CUDA_TRY(c, cudaStreamSynchronize(c->stream));   // the pinned position slot is reused
+    }
+    if (mix) {   // previous-step rows at positions lo .. n-2 from the last chunk (row n-1: pass K+3)
+      const int r0 = lo - (nk - kPrefillChunk);
+      CUDA_TRY(c, cudaMemcpyAsync(c->logits_p, c->logits_chunk + (size_t)r0 * V, sizeof(float) * (size_t)K * V,
+                                  cudaMemcpyDeviceToDevice, c->stream));
+    }
+  }
+  for (int b = 0; b < c->B && !c->q4; ++b) {   // sequence by sequence, in chunks of positions
     Seqs sq;
     sq.seq0 = b;
     const int32_t* sb = c->seq + (size_t)b * c->seq_ld;
@@ -1308,6 +1373,7 @@ int spec_model_forward(spec_ctx* c, int which, const int32_t* tokens, int n, int
   if (!tokens || n < 1 || pos0 < 0) return fail(c, SPEC_E_ARG, "bad tokens");
   if (pos0 + n > c->cap) return fail(c, SPEC_E_CAPACITY, "positions exceed max_ctx");
   ModelState& m = which == 0 ? c->tgt : c->drf;
+  if (m.q4) return fail(c, SPEC_E_STATE, "spec_model_forward runs one kernel per operation: not for 4-bit models");
   for (int i = 0; i < n; ++i)
     if (tokens[i] < 0 || tokens[i] >= m.d.vocab) return fail(c, SPEC_E_ARG, "token id out of range");
   c->prefilled = false;

@@ -69,6 +69,9 @@ struct GemmDesc {
   float* q_out;              // [ntok][hq][hd]
   void* kc;                  // [hkv][cap][hd] of this layer
   void* vc;
+  int q4;              // 1: 4-bit group-quantized weights (persistent kernel only): each
+                       // segment is packed codes [rows][k/2] followed by bf16 scales
+                       // [k/64][rows] (group-major), 16-byte aligned
   int early_prefetch;  // 1: issue the first weight loads before waiting for the
                        // previous kernel (only when that kernel is itself a
                        // bandwidth-bound GEMM; a latency-bound predecessor would
@@ -288,6 +291,7 @@ enum PhaseKind : int { kPhaseEmbed = 0, kPhaseGemm = 1, kPhaseAttn = 2 };
 // resident X), or normalised while loading (per-operation GEMM).
 enum XMode : int { kXGlobal = 0, kXSmem = 1, kXInline = 2 };
 constexpr int kPhaseStamps = 5;
+constexpr int kPrefillChunk = 8;   // positions per persistent prefill pass (4-bit models)
 struct PhaseDesc {
   int kind;
   // GEMM streaming geometry (tma_dev.cuh): X resident in shared memory
@@ -299,6 +303,11 @@ struct PhaseDesc {
   int xm, paired, tiles, gt, kc;
   int stages, stage_bytes, xoff, prefetch;
   int tm[4];
+  // 4-bit group-quantized weights (q4 = 1): tensor maps of the segments'
+  // codes (tm[0..2]) and group-major scales (tms[0..2]); bytes per tile in
+  // a stage (codes of both 8-row halves, then their scales)
+  int q4, tile_bytes;
+  int tms[3];
   int attn_items;
   GemmDesc g;
   AttnDesc a;

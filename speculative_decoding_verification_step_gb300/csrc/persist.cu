@@ -142,6 +142,11 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
       if (producer) {
         if (lane == 0) tma_produce(d, npre, tp, ring, maps);
         __syncwarp();
+      } else if (d.q4) {
+        if (d.xm == kXSmem)
+          tma_consume_q4<true>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
+        else
+          tma_consume_q4<false>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
       } else if (d.xm == kXSmem) {
         tma_consume<true>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
       } else {
@@ -216,6 +221,35 @@ static bool encode_rows(TensorMap128& m, const void* base, int k, long long rows
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-bit codes of a [rows][k] matrix (k/2 bytes per row), viewed as
+// [k/256 blocks][rows][128 bytes]: boxes of 128 bytes x 8 rows x nblk blocks
+// with the 128-byte swizzle (shared-memory layout [block][row][128 B]).
+static bool encode_q4_codes(TensorMap128& m, const void* base, int k, long long rows, int nblk) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || !base || rows < 1 || k % kTmaK || (reinterpret_cast<uintptr_t>(base) & 15u)) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)(k / kTmaK)};
+  cuuint64_t strides[2] = {(cuuint64_t)k / 2, 128};
+  cuuint32_t box[3] = {128, 8, (cuuint32_t)nblk};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(reinterpret_cast<CUtensorMap*>(&m), CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 scales of a [rows][k] q4 matrix stored group-major [k/64][rows]:
+// boxes of 8 rows x ngrp groups (shared-memory layout [group][row]).
+static bool encode_q4_scales(TensorMap128& m, const void* base, int k, long long rows, int ngrp) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || !base || rows < 8 || rows % 8 || (reinterpret_cast<uintptr_t>(base) & 15u)) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)rows, (cuuint64_t)(k / 64)};
+  cuuint64_t strides[1] = {(cuuint64_t)rows * 2};
+  cuuint32_t box[2] = {8, (cuuint32_t)ngrp};
+  cuuint32_t es[2] = {1, 1};
+  return enc(reinterpret_cast<CUtensorMap*>(&m), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows, int box_cols) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc || !base || rows < 1 || (hd != 32 && hd != 64 && hd != 128) ||
@@ -231,6 +265,65 @@ bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows, in
              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              cols < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q4 phase (see tma_dev.cuh): tiles of two 8-row halves (plain matrices
+// too); X resident when it fits (one tile x 4096 k per stage), else
+// streamed (two tiles x 1024 k per stage).
+static bool persist_phase_q4(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid,
+                             const PersistLayout& lay) {
+  if (g.k % kTmaK) return false;
+  p.q4 = 1;
+  p.paired = 1;
+  const size_t xbytes = (size_t)g.ntok * (g.k + kXPad) * 2;
+  p.xm = xbytes <= lay.xreg ? kXSmem : kXGlobal;
+  const int nct = std::min(grid, p.tiles);
+  const int tiles_max = (p.tiles + nct - 1) / nct;
+  p.gt = p.xm == kXSmem ? 1 : std::min(kMaxGroupTiles, tiles_max);
+  p.kc = std::min(p.xm == kXSmem ? 16 * kTmaK : 4 * kTmaK, g.k);
+  const int nblk = p.kc / kTmaK, ngrp = p.kc / 64;
+  p.tile_bytes = (2 * nblk * 1024 + 2 * ngrp * 16 + 1023) / 1024 * 1024;
+  auto add2 = [&](const void* base, long long rows, int* mc, int* ms) {
+    // codes [rows][k/2], then the scales, 16-byte aligned
+    TensorMap128 a{}, b{};
+    const unsigned char* sc = (const unsigned char*)base + (size_t)rows * g.k / 2;
+    if (!encode_q4_codes(a, base, g.k, rows, nblk) || !encode_q4_scales(b, sc, g.k, rows, ngrp)) return false;
+    maps.push_back(a);
+    *mc = (int)maps.size() - 1;
+    maps.push_back(b);
+    *ms = (int)maps.size() - 1;
+    return true;
+  };
+  bool ok = true;
+  if (g.epi == kEpiQkvRope) {
+    if (g.hd % 16 != 0) return false;
+    for (int s = 0; s < 3; ++s) ok = ok && add2(g.w[s], g.seg_rows[s], &p.tm[s], &p.tms[s]);
+  } else if (g.epi == kEpiSwiglu) {
+    if (g.n % 8 != 0) return false;
+    ok = add2(g.w[0], g.n, &p.tm[0], &p.tms[0]) && add2(g.w[1], g.n, &p.tm[1], &p.tms[1]);
+    p.tm[2] = p.tm[0];
+    p.tms[2] = p.tms[0];
+  } else {
+    if (g.n % 8 != 0) return false;
+    ok = add2(g.w[0], g.n, &p.tm[0], &p.tms[0]);
+    p.tm[1] = p.tm[2] = p.tm[0];
+    p.tms[1] = p.tms[2] = p.tms[0];
+  }
+  if (!ok) return false;
+  if (p.xm == kXGlobal) {
+    TensorMap128 m{};
+    if (!encode_rows(m, g.x, g.k, g.ntok, g.ldx, g.ntok)) return false;
+    maps.push_back(m);
+    p.tm[3] = (int)maps.size() - 1;
+  }
+  const int xstage = p.xm == kXGlobal ? nblk * g.ntok * kTmaRowBytes : 0;
+  p.xoff = p.gt * p.tile_bytes;
+  p.stage_bytes = (p.gt * p.tile_bytes + xstage + 1023) / 1024 * 1024;
+  p.stages = std::min<int>(kMaxStages, (int)(lay.ring / (size_t)p.stage_bytes));
+  if (p.stages < 2) return false;
+  const int units_max = ((tiles_max + p.gt - 1) / p.gt) * ((g.k + p.kc - 1) / p.kc);
+  p.prefetch = p.xm == kXSmem && units_max <= 8 ? std::min(p.stages, 2) : p.stages;
+  return true;
 }
 
 bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<TensorMap128>& maps, int grid,
@@ -249,6 +342,7 @@ bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<Tensor
     return (int)maps.size() - 1;
   };
   p.tiles = gemm_tiles_of(g);
+  if (g.q4) return persist_phase_q4(p, g, maps, grid, lay);
   if (g.epi == kEpiQkvRope) {
     if (g.hd % 16 != 0) return false;
     p.paired = 1;

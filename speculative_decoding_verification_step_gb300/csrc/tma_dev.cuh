@@ -43,6 +43,19 @@
 // the grid waits; after the barrier it copies X (and, streamed, the X boxes
 // of those units) and streams the rest.
 //
+// 4-bit weights (q4).  A matrix is stored as packed signed nibbles [n][k/2]
+// (element 2b in the low nibble of byte b) followed by bf16 scales, one per
+// 64-k group, group-major [k/64][n]; weight = scale x code.  A tile's stage
+// block holds, per 8-row half, the codes as [k/256 blocks][8 rows][128 B]
+// (one 3-D tensor copy with the 128-byte swizzle, so eight rows read at the
+// same k hit distinct banks), then per half the scales [groups][8 rows] (one
+// 2-D copy; a row's scale of a group is one 2-byte read).  A 64-k step is
+// one group: the codes become bf16 (136 + v) by one lop3 per pair, then exact
+// v by one bf16x2 subtraction; four MMAs with a zero accumulator give the
+// group's sum, which the row's scale weights into the tile's fp32 total.  The
+// code pairs come out as elements (i, i + 4) of each 8-code word, so the X
+// operand takes the same pairs (one byte permute per pair).
+//
 // Every wait is bounded.  A wait that gives up raises the CTA's abort flag;
 // from then on every wait of the CTA returns at once and the warps run
 // through their remaining iterations without touching the data (barrier
@@ -128,6 +141,7 @@ struct TmaGeo {
   int S, sb, kc, k, gt, paired, ntok, xoff, xs;
   int epi, hd, seg0, seg1;
   int tm0, tm1, tm2, tmx;        // weight segments 0..2, streamed X
+  int q4, tile_bytes, tms0, tms1, tms2;
   int t0, t1, nchunks, ngroups, n;
 };
 
@@ -152,6 +166,11 @@ SV_DEV TmaGeo tma_geo(const PhaseDesc& d, const unsigned char* maps) {
   q.tm1 = d.tm[1];
   q.tm2 = d.tm[2];
   q.tmx = d.tm[3];
+  q.q4 = d.q4;
+  q.tile_bytes = d.q4 ? d.tile_bytes : (d.kc / kTmaK) * kTileBlockBytes;
+  q.tms0 = d.tms[0];
+  q.tms1 = d.tms[1];
+  q.tms2 = d.tms[2];
   const int tiles = d.tiles;
   const int G = min((int)gridDim.x, tiles);
   const bool has = (int)blockIdx.x < G;
@@ -166,6 +185,7 @@ SV_DEV TmaGeo tma_geo(const PhaseDesc& d, const unsigned char* maps) {
 // Tensor-map index and first row of box A (and box B when paired) of tile t.
 struct TileBoxes {
   int ma, ra, mb, rb;
+  int sa, sb;   // q4: scale maps of box A / B
 };
 SV_DEV TileBoxes tile_boxes(const TmaGeo& q, int t) {
   if (q.epi == kEpiQkvRope) {
@@ -181,10 +201,12 @@ SV_DEV TileBoxes tile_boxes(const TmaGeo& q, int t) {
       }
     }
     const int m = seg == 0 ? q.tm0 : seg == 1 ? q.tm1 : q.tm2;
-    return {m, row, m, row + q.hd / 2};
+    const int ms = seg == 0 ? q.tms0 : seg == 1 ? q.tms1 : q.tms2;
+    return {m, row, m, row + q.hd / 2, ms, ms};
   }
-  if (q.epi == kEpiSwiglu) return {q.tm0, 8 * t, q.tm1, 8 * t};
-  return {q.tm0, 16 * t, q.tm0, 16 * t};   // one box of 16 rows
+  if (q.epi == kEpiSwiglu) return {q.tm0, 8 * t, q.tm1, 8 * t, q.tms0, q.tms1};
+  // plain: one box of 16 rows (bf16); q4 always copies two 8-row halves
+  return {q.tm0, 16 * t, q.tm0, 16 * t + 8, q.tms0, q.tms0};
 }
 
 // 256-k blocks of chunk c (the last chunk may be short).
@@ -259,7 +281,6 @@ SV_DEV void walk_next(const TmaGeo& q, TmaWalk& w) {
 
 SV_DEV void tma_issue_units(const TmaGeo& q, TmaWalk& w, int end, bool with_x, TmaPipe& tp, unsigned char* ring) {
   const uint64_t pol = l2_evict_first();   // weights are read once per pass
-  const int kbs = q.kc / kTmaK;
   const unsigned char* maps = q.maps;
   for (; w.i < end; walk_next(q, w)) {
     const int slot = w.slot;
@@ -268,7 +289,12 @@ SV_DEV void tma_issue_units(const TmaGeo& q, TmaWalk& w, int end, bool with_x, T
     const int nkb = chunk_blocks(q, w.c);
     const int k0 = w.c * q.kc;
     const unsigned xbytes = q.xs ? (unsigned)(nkb * q.ntok * kTmaRowBytes) : 0u;
-    mbar_arrive_expect_tx(&tp.full[slot], (unsigned)(w.ng * nkb * kTileBlockBytes) + xbytes);
+    // q4: full boxes every chunk (a short last chunk reads zeros past k):
+    // per tile two code boxes of 8 rows x kc/2 bytes and two scale boxes of
+    // 8 rows x kc/64 bf16 -- 8.5 kc bytes (the tile's block is padded to 1 KB)
+    const unsigned wbytes =
+        q.q4 ? (unsigned)(w.ng * (q.kc * 8 + q.kc / 2)) : (unsigned)(w.ng * nkb * kTileBlockBytes);
+    mbar_arrive_expect_tx(&tp.full[slot], wbytes + xbytes);
     unsigned char* st = ring + (size_t)slot * q.sb;
 #pragma unroll
     for (int gq = 0; gq < kMaxGroupTiles; ++gq) {
@@ -276,7 +302,17 @@ SV_DEV void tma_issue_units(const TmaGeo& q, TmaWalk& w, int end, bool with_x, T
       const TileBoxes b = gq ? w.b1 : w.b0;
       const unsigned char* mapA = maps + (size_t)b.ma * kTensorMapBytes;
       const unsigned char* mapB = maps + (size_t)b.mb * kTensorMapBytes;
-      unsigned char* dst = st + (size_t)gq * kbs * kTileBlockBytes;
+      unsigned char* dst = st + (size_t)gq * q.tile_bytes;
+      if (q.q4) {
+        const int half = (q.kc / kTmaK) * 1024;   // codes of one 8-row half
+        tma_load_3d_hint(dst, mapA, 0, b.ra, k0 / kTmaK, &tp.full[slot], pol);
+        tma_load_3d_hint(dst + half, mapB, 0, b.rb, k0 / kTmaK, &tp.full[slot], pol);
+        unsigned char* sd = dst + 2 * half;
+        tma_load_2d_hint(sd, maps + (size_t)b.sa * kTensorMapBytes, b.ra, k0 / 64, &tp.full[slot], pol);
+        tma_load_2d_hint(sd + (q.kc / 64) * 16, maps + (size_t)b.sb * kTensorMapBytes, b.rb, k0 / 64, &tp.full[slot],
+                         pol);
+        continue;
+      }
       for (int kb = 0; kb < nkb; ++kb, dst += kTileBlockBytes) {
         tma_load_2d_hint(dst, mapA, k0 + kb * kTmaK, b.ra, &tp.full[slot], pol);
         if (q.paired) tma_load_2d_hint(dst + 8 * kTmaRowBytes, mapB, k0 + kb * kTmaK, b.rb, &tp.full[slot], pol);
@@ -339,6 +375,189 @@ SV_DEV void tma_step(float (&acc)[4], const unsigned char* blk, const uint4& x0,
   mma_bf16_16816(acc, a1.z, b1.z, a1.w, b1.w, x1.z, x1.w);
 }
 
+// End of a tile group (every consumer warp): each warp's partial sums of
+// the group's tiles (gt = 1: a + b, the warp's two chains; gt = 2: a for the
+// first tile, b for the second) go to shared memory; after a barrier of the
+// consumer warps one warp per tile adds the eight partials in warp order,
+// applies 1/rms (RMSNorm'd inputs) and runs the tile's epilogue.  Resident
+// phases alternate two partial buffers (the next group's partials never
+// overwrite ones still being read); streamed phases use both halves for
+// their two tiles and wait for the readers before the next group.
+SV_DEV void tma_group_end(const TmaGeo& q, const GemmDesc& g, TmaPipe& tp, float4* red, const float* s_inv,
+                          const float (&a)[4], const float (&b)[4], bool resident, int grp, int tb, int ng, int pos0,
+                          int tiles_all) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
+  float4* rb = red + (size_t)(resident ? (grp & 1) : 0) * kCWarps * 32;   // buffer (resident) or tile 0
+  if (q.gt == 1) {
+    rb[warp * 32 + lane] = make_float4(a[0] + b[0], a[1] + b[1], a[2] + b[2], a[3] + b[3]);
+  } else {
+    rb[warp * 32 + lane] = make_float4(a[0], a[1], a[2], a[3]);
+    rb[(kCWarps + warp) * 32 + lane] = make_float4(b[0], b[1], b[2], b[3]);
+  }
+  named_sync(kGemmBarrier, kConsumerThreads);
+  for (int gq = 0; gq < ng; ++gq) {
+    const int ew = resident ? grp % kCWarps : gq;   // the tile's epilogue warp
+    if (warp != ew || tp.abort) continue;
+    const int tile = tb + gq;
+    if (tile >= tiles_all) continue;
+    const float4* pt = rb + (size_t)gq * kCWarps * 32 + lane;
+    float y[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int w = 0; w < kCWarps; ++w) {
+      const float4 v = pt[w * 32];
+      y[0][0] += v.x;
+      y[0][1] += v.y;
+      y[0][2] += v.z;
+      y[0][3] += v.w;
+    }
+    if (g.x_norm == 2) {
+      const float sc0 = s_inv[2 * ci], sc1 = s_inv[2 * ci + 1];
+      y[0][0] *= sc0;
+      y[0][1] *= sc1;
+      y[0][2] *= sc0;
+      y[0][3] *= sc1;
+    }
+    EpiIn pre;
+    gemm_epi_load<false>(g, tile, pos0, gi, ci, pre);
+    gemm_epilogue<1, false>(g, tile, y, gi, ci, &pre);
+  }
+  // streamed X: the partial area is not double-buffered -- the next group's
+  // partials wait until the epilogue warps have read these
+  if (!resident && grp + 1 < q.ngroups) named_sync(kGemmBarrier, kConsumerThreads);
+}
+
+// One 64-k group of a q4 tile for rows gi (half 0) and gi + 8 (half 1):
+// the thread's 16 codes per row (bytes ci*8 .. ci*8+7 of the group's 32, at
+// their swizzled place), the rows' scales, and the 16 X values x0, x1 of
+// token gi at the same k; adds scale x (codes . X) to tot.
+SV_DEV uint32_t q4_pair(uint32_t t) {   // nibbles 0 and 4 of t (offset binary) -> bf16 (136 + v) x 2
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(t), "r"(0x000F000Fu), "r"(0x43004300u));
+  return r;
+}
+SV_DEV uint32_t q4_exact(uint32_t p) {   // (136 + v) x 2 -> v x 2, exactly
+  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&p);
+  const __nv_bfloat162 c = __floats2bfloat162_rn(136.f, 136.f);
+  h = __hsub2(h, c);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+SV_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+SV_DEV void q4_step(float (&tot)[4], const unsigned char* tile, int half, int ngrp, int ks, const uint4& x0,
+                    const uint4& x1, int gi, int ci) {
+  const int lb = (ks & 3) * 32 + ci * 8;   // logical byte of the thread's codes in the block's 128-B row
+  const int off = (ks >> 2) * 1024 + gi * 128 + ((((lb >> 4) ^ gi) & 7) << 4) + (lb & 15);
+  const uint2 ca = *reinterpret_cast<const uint2*>(tile + off);
+  const uint2 cb = *reinterpret_cast<const uint2*>(tile + half + off);
+  const unsigned char* sc = tile + 2 * half + ks * 16 + gi * 2;
+  const float sa = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc) << 16);
+  const float sb = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc + ngrp * 16) << 16);
+  float acc[4];
+  // codes 0..7 of the row: pairs (0,4) (1,5) (2,6) (3,7); X the same pairs
+  {
+    const uint32_t ta = ca.x ^ 0x88888888u, tb = cb.x ^ 0x88888888u;
+    const uint32_t xa = prmt(x0.x, x0.z, 0x5410u), xb = prmt(x0.x, x0.z, 0x7632u);
+    const uint32_t xc = prmt(x0.y, x0.w, 0x5410u), xd = prmt(x0.y, x0.w, 0x7632u);
+    float g0[4], g1[4];
+    mma_bf16_16816_z(g0, q4_exact(q4_pair(ta)), q4_exact(q4_pair(tb)), q4_exact(q4_pair(ta >> 4)),
+                     q4_exact(q4_pair(tb >> 4)), xa, xb);
+    mma_bf16_16816_z(g1, q4_exact(q4_pair(ta >> 8)), q4_exact(q4_pair(tb >> 8)), q4_exact(q4_pair(ta >> 12)),
+                     q4_exact(q4_pair(tb >> 12)), xc, xd);
+    acc[0] = g0[0] + g1[0];
+    acc[1] = g0[1] + g1[1];
+    acc[2] = g0[2] + g1[2];
+    acc[3] = g0[3] + g1[3];
+  }
+  {
+    const uint32_t ta = ca.y ^ 0x88888888u, tb = cb.y ^ 0x88888888u;
+    const uint32_t xa = prmt(x1.x, x1.z, 0x5410u), xb = prmt(x1.x, x1.z, 0x7632u);
+    const uint32_t xc = prmt(x1.y, x1.w, 0x5410u), xd = prmt(x1.y, x1.w, 0x7632u);
+    float g0[4], g1[4];
+    mma_bf16_16816_z(g0, q4_exact(q4_pair(ta)), q4_exact(q4_pair(tb)), q4_exact(q4_pair(ta >> 4)),
+                     q4_exact(q4_pair(tb >> 4)), xa, xb);
+    mma_bf16_16816_z(g1, q4_exact(q4_pair(ta >> 8)), q4_exact(q4_pair(tb >> 8)), q4_exact(q4_pair(ta >> 12)),
+                     q4_exact(q4_pair(tb >> 12)), xc, xd);
+    acc[0] += g0[0] + g1[0];
+    acc[1] += g0[1] + g1[1];
+    acc[2] += g0[2] + g1[2];
+    acc[3] += g0[3] + g1[3];
+  }
+  tot[0] = fmaf(sa, acc[0], tot[0]);
+  tot[1] = fmaf(sa, acc[1], tot[1]);
+  tot[2] = fmaf(sb, acc[2], tot[2]);
+  tot[3] = fmaf(sb, acc[3], tot[3]);
+}
+
+// Consumer warps of a q4 GEMM phase: every stage holds gt tiles x kc k as
+// gt tile blocks; its (tile, group) steps are dealt to the warps round robin
+// (step s to warp s mod 8), each tile's sum kept in its own accumulator.
+template <bool kResident>
+SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const unsigned char* ring,
+                           const unsigned char* xreg, float4* red, const float* s_inv, unsigned long long* stamp) {
+  const GemmDesc& g = d.g;
+  const TmaGeo q = tma_geo(d, nullptr);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
+  const int ngrp = q.kc / 64;               // 64-k groups per tile in a stage
+  const int half = (q.kc / kTmaK) * 1024;   // codes of one 8-row half
+  const int steps = q.gt * ngrp;
+  const bool has_tok = gi < q.ntok;
+  const size_t xs_pitch = (size_t)(q.k + kXPad) * 2;
+  const unsigned char* xrow = xreg + gi * xs_pitch + ci * 32;
+  const uint4 zero4 = make_uint4(0, 0, 0, 0);
+  const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
+  const int tiles_all = gemm_tiles_of(g);
+  bool xok = true;
+  if (kResident && q.n > 0) xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
+  int i = 0, slot = 0;
+#pragma unroll 1
+  for (int grp = 0; grp < q.ngroups; ++grp) {
+    const int tb = q.t0 + grp * q.gt, ng = min(q.gt, q.t1 - tb);
+    float accA[4] = {0.f, 0.f, 0.f, 0.f}, accB[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int c = 0; c < q.nchunks; ++c, ++i) {
+      const bool ok = tma_wait(&tp.full[slot], (cpar >> slot) & 1u, tp) && xok;
+      cpar ^= 1u << slot;
+      if (stamp && i == q.n - 1 && threadIdx.x == 0) {
+        unsigned long long tm;
+        asm volatile("mov.u64 %0, %globaltimer;" : "=l"(tm));
+        atomicMax(stamp, tm);
+      }
+      if (ok) {
+        const unsigned char* st = ring + (size_t)slot * q.sb;
+#pragma unroll 1
+        for (int s = warp; s < steps; s += kCWarps) {
+          const int gq = s / ngrp, ks = s - gq * ngrp;
+          const int kg = c * q.kc + ks * 64;
+          if (gq >= ng || kg >= q.k) continue;
+          uint4 x0 = zero4, x1 = zero4;
+          if (has_tok) {
+            const unsigned char* xp =
+                kResident ? xrow + (size_t)kg * 2
+                          : st + q.xoff + ((size_t)(ks >> 2) * q.ntok + gi) * kTmaRowBytes + (ks & 3) * 128 + ci * 32;
+            x0 = *reinterpret_cast<const uint4*>(xp);
+            x1 = *reinterpret_cast<const uint4*>(xp + 16);
+          }
+          if (gq)
+            q4_step(accB, st + (size_t)q.tile_bytes, half, ngrp, ks, x0, x1, gi, ci);
+          else
+            q4_step(accA, st, half, ngrp, ks, x0, x1, gi, ci);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&tp.empty[slot]);
+      if (++slot == q.S) slot = 0;
+    }
+    if (q.gt == 1) {   // one tile: the warp's sum is accA alone
+#pragma unroll
+      for (int e = 0; e < 4; ++e) accB[e] = 0.f;
+    }
+    tma_group_end(q, g, tp, red, s_inv, accA, accB, kResident, grp, tb, ng, pos0, tiles_all);
+  }
+}
+
 // Consumer warps during GEMM phase d (see the file comment).  cpar: per-slot
 // parity of the next completion of each stage's full barrier (identical in
 // every consumer warp).  red: the group-partial area (kRedBytes).  s_inv:
@@ -365,7 +584,6 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
   const int xoffB = q.xoff + ((kB / 4) * q.ntok + gi) * kTmaRowBytes + (kB % 4) * (kStepK * 2) + ci * 32;
   const unsigned char* xrow = xreg + gi * xs_pitch + ci * 32;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
-  const bool xn = g.x_norm == 2;
   const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
   const int tiles_all = gemm_tiles_of(g);
   bool xok = true;
@@ -411,45 +629,7 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
       if (lane == 0 && ok) mbar_arrive(&tp.empty[slot]);
       if (++slot == q.S) slot = 0;
     }
-    // end of the group: partials of every warp, then one warp per tile adds
-    // them in warp order and runs the epilogue
-    float4* rb = red + (size_t)(kResident ? (grp & 1) : 0) * kCWarps * 32;   // buffer (resident) or tile 0
-    if (q.gt == 1) {
-      rb[warp * 32 + lane] = make_float4(accA[0] + accB[0], accA[1] + accB[1], accA[2] + accB[2], accA[3] + accB[3]);
-    } else {
-      rb[warp * 32 + lane] = make_float4(accA[0], accA[1], accA[2], accA[3]);
-      rb[(kCWarps + warp) * 32 + lane] = make_float4(accB[0], accB[1], accB[2], accB[3]);
-    }
-    named_sync(kGemmBarrier, kConsumerThreads);
-    for (int gq = 0; gq < ng; ++gq) {
-      const int ew = kResident ? grp % kCWarps : gq;   // the tile's epilogue warp
-      if (warp != ew || tp.abort) continue;
-      const int tile = tb + gq;
-      if (tile >= tiles_all) continue;
-      const float4* pt = rb + (size_t)gq * kCWarps * 32 + lane;
-      float y[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int w = 0; w < kCWarps; ++w) {
-        const float4 v = pt[w * 32];
-        y[0][0] += v.x;
-        y[0][1] += v.y;
-        y[0][2] += v.z;
-        y[0][3] += v.w;
-      }
-      if (xn) {
-        const float sc0 = s_inv[2 * ci], sc1 = s_inv[2 * ci + 1];
-        y[0][0] *= sc0;
-        y[0][1] *= sc1;
-        y[0][2] *= sc0;
-        y[0][3] *= sc1;
-      }
-      EpiIn pre;
-      gemm_epi_load<false>(g, tile, pos0, gi, ci, pre);
-      gemm_epilogue<1, false>(g, tile, y, gi, ci, &pre);
-    }
-    // streamed X: the partial area is not double-buffered -- the next
-    // group's partials wait until the epilogue warps have read these
-    if (!kResident && grp + 1 < q.ngroups) named_sync(kGemmBarrier, kConsumerThreads);
+    tma_group_end(q, g, tp, red, s_inv, accA, accB, kResident, grp, tb, ng, pos0, tiles_all);
   }
 }
 

@@ -17,6 +17,11 @@ Recipes (all seeded, all synthetic; no dataset or trained weight is used):
 * Prompts: token ids uniform on [0, vocab).
 * Acceptance rows: target logits ~ N(0, 3^2); draft logits = target rows
   1..K plus N(0, sigma^2).
+* 4-bit weights (dtype "q4"): every matrix [n][k] gets codes uniform on
+  [-8, 7] and one bf16 scale per 64-k group, uniform on [0.75, 1.25] x
+  0.02 / 4.6 (weights of std ~0.02), laid out as the library takes them:
+  codes packed two per byte (element 2b in the low nibble), then the scales
+  group-major [k/64][n].  The embedding is bf16 N(0, 0.02^2), gains 1.
 """
 from dataclasses import dataclass, replace
 
@@ -37,7 +42,7 @@ class ModelShape:
     vocab: int
     rope_theta: float
     rms_eps: float = 1e-5
-    dtype: str = "bf16"          # "f32" or "bf16"
+    dtype: str = "bf16"          # "f32", "bf16" or "q4" (4-bit weights, bf16 arithmetic)
 
     @property
     def torch_dtype(self):
@@ -45,6 +50,12 @@ class ModelShape:
 
     @property
     def elem_bytes(self):
+        """Bytes per streamed weight (q4: a nibble plus a bf16 scale per 64)."""
+        return 4 if self.dtype == "f32" else 2 if self.dtype == "bf16" else 0.5 + 2 / 64
+
+    @property
+    def act_bytes(self):
+        """Bytes per activation / KV element."""
         return 4 if self.dtype == "f32" else 2
 
     def layer_params(self):
@@ -61,7 +72,7 @@ class ModelShape:
         return b
 
     def kv_bytes_per_token(self):
-        return self.n_layers * 2 * self.n_kv_heads * self.head_dim * self.elem_bytes
+        return self.n_layers * 2 * self.n_kv_heads * self.head_dim * self.act_bytes
 
 
 # Tiny speculative-generation model: 2 layers, d=128, 4 heads, SwiGLU 512,
@@ -154,3 +165,54 @@ def make_accept_rows(rows: int, k: int, vocab: int, sigma: float, seed: int,
     q = torch.randn(rows, k, vocab, generator=g, device=device, dtype=torch.float32)
     q.mul_(sigma).add_(p[:, :k, :])
     return p, q
+
+
+def q4_matrix(n, k, g, device, scale=0.02 / 4.6):
+    """One 4-bit matrix in the library's layout (uint8 buffer: packed codes
+    [n][k/2], then bf16 scales [k/64][n])."""
+    codes = torch.randint(-8, 8, (n, k), generator=g, device=device, dtype=torch.int16)
+    nib = (codes & 0xF).to(torch.uint8)
+    packed = nib[:, 0::2] | (nib[:, 1::2] << 4)
+    scales = (torch.rand(k // 64, n, generator=g, device=device, dtype=torch.float32) * 0.5 + 0.75) * scale
+    sb = scales.to(torch.bfloat16).contiguous().view(torch.uint8).reshape(-1)
+    return torch.cat([packed.reshape(-1), sb])
+
+
+def q4_parts(buf, n, k):
+    """(packed codes [n][k/2] uint8, scales [n][k/64] fp32 holding bf16 values)
+    of a 4-bit matrix buffer, as host tensors."""
+    b = buf.detach().cpu()
+    packed = b[: n * k // 2].reshape(n, k // 2)
+    scales = b[n * k // 2:].view(torch.bfloat16).reshape(k // 64, n).t().float()
+    return packed, scales
+
+
+def make_q4_weights(shape: ModelShape, seed: int, device="cpu"):
+    """Random 4-bit weights (see the module docstring), same dict layout as
+    make_weights; the matrices are uint8 buffers."""
+    g = _gen(seed, device)
+    d, hd, f = shape.d_model, shape.head_dim, shape.ffn_dim
+    w = {"embed": _randn((shape.vocab, d), g, device, 0.02, torch.bfloat16),
+         "final_norm": torch.ones(d, dtype=torch.float32, device=device), "layers": []}
+    for _ in range(shape.n_layers):
+        w["layers"].append({
+            "attn_norm": torch.ones(d, dtype=torch.float32, device=device),
+            "wq": q4_matrix(shape.n_heads * hd, d, g, device),
+            "wk": q4_matrix(shape.n_kv_heads * hd, d, g, device),
+            "wv": q4_matrix(shape.n_kv_heads * hd, d, g, device),
+            "wo": q4_matrix(d, shape.n_heads * hd, g, device),
+            "ffn_norm": torch.ones(d, dtype=torch.float32, device=device),
+            "w_gate": q4_matrix(f, d, g, device),
+            "w_up": q4_matrix(f, d, g, device),
+            "w_down": q4_matrix(d, f, g, device),
+        })
+    w["lm_head"] = q4_matrix(shape.vocab, d, g, device)
+    return w
+
+
+# matrix name -> (rows, k) of a shape
+def matrix_dims(shape: ModelShape, name):
+    d, hd, f = shape.d_model, shape.head_dim, shape.ffn_dim
+    return {"wq": (shape.n_heads * hd, d), "wk": (shape.n_kv_heads * hd, d), "wv": (shape.n_kv_heads * hd, d),
+            "wo": (d, shape.n_heads * hd), "w_gate": (f, d), "w_up": (f, d), "w_down": (d, f),
+            "lm_head": (shape.vocab, d)}[name]

@@ -963,7 +963,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
         INIT_TRY(cudaMemset(c->fault_ctl, 0, sizeof(int) * 4));
         unsigned long long* times = nullptr;
         if (opts->flags & SPEC_OPT_PHASE_TIMES) {
-          const size_t words = (size_t)(K + 4) + (size_t)kPhaseStamps * all.size();
+          const size_t words = (size_t)nf + (size_t)kPhaseStamps * all.size();   // a start word per forward
           INIT_TRY(dalloc(c, &times, sizeof(unsigned long long) * words));
           INIT_TRY(cudaMemset(times, 0, sizeof(unsigned long long) * words));
         }

@@ -280,7 +280,11 @@ static bool persist_phase_q4(PhaseDesc& p, const GemmDesc& g, std::vector<Tensor
   const int nct = std::min(grid, p.tiles);
   const int tiles_max = (p.tiles + nct - 1) / nct;
   p.gt = p.xm == kXSmem ? 1 : std::min(kMaxGroupTiles, tiles_max);
-  p.kc = std::min(p.xm == kXSmem ? 16 * kTmaK : 4 * kTmaK, g.k);
+  // k per stage: a power of two (the steps split by shifts), at most 4096
+  // (resident X) or 1024 (streamed X), at most k
+  p.kc = p.xm == kXSmem ? 16 * kTmaK : 4 * kTmaK;
+  while (p.kc > g.k) p.kc /= 2;
+  if (p.kc < kTmaK) return false;
   const int nblk = p.kc / kTmaK, ngrp = p.kc / 64;
   p.tile_bytes = (2 * nblk * 1024 + 2 * ngrp * 16 + 1023) / 1024 * 1024;
   auto add2 = [&](const void* base, long long rows, int* mc, int* ms) {

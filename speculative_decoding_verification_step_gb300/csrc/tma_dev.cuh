@@ -35,7 +35,7 @@
 // partial buffers, so the next group's partials never overwrite ones still
 // being read).  The summation order depends on k and the warp count only, so
 // every pass is batch-invariant.  (Handing the partials to the epilogue warp
-// through mbarriers instead of the barrier measured no faster.)
+// through mbarriers instead of the barrier measured slower.)
 //
 // Phase boundaries.  Between arriving at the grid barrier before a GEMM
 // phase and leaving it, the producer already fills the ring with the
@@ -50,11 +50,12 @@
 // (one 3-D tensor copy with the 128-byte swizzle, so eight rows read at the
 // same k hit distinct banks), then per half the scales [groups][8 rows] (one
 // 2-D copy; a row's scale of a group is one 2-byte read).  A 64-k step is
-// one group: the codes become bf16 (136 + v) by one lop3 per pair, then exact
-// v by one bf16x2 subtraction; four MMAs with a zero accumulator give the
-// group's sum, which the row's scale weights into the tile's fp32 total.  The
-// code pairs come out as elements (i, i + 4) of each 8-code word, so the X
-// operand takes the same pairs (one byte permute per pair).
+// one group: the codes become bf16 (136 + v) by one lop3 per pair and exact
+// v by one bf16x2 subtraction; four MMAs give the group's code . X sum,
+// which the row's scale weights into the tile's fp32 total.  The code pairs
+// come out as elements (i, i + 4) of each 8-code word, so the X operand
+// takes the same pairs: resident X rows are permuted into that order once
+// per phase, streamed X per step.
 //
 // Every wait is bounded.  A wait that gives up raises the CTA's abort flag;
 // from then on every wait of the CTA returns at once and the warps run
@@ -85,8 +86,8 @@ constexpr size_t kXMinBytes = 36 * 1024;          // X region: at least a 2-toke
 constexpr long long kWaitLimit = 1LL << 22;
 constexpr long long kDrainLimit = 1LL << 16;
 constexpr int kPersistMaxTok = 8;
-constexpr size_t kTensorMapBytes = 128;
 constexpr int kGemmBarrier = 2;                   // named barrier of the consumer warps (1: attention)
+constexpr size_t kTensorMapBytes = 128;
 
 struct TmaPipe {
   uint64_t full[kMaxStages];
@@ -435,60 +436,60 @@ SV_DEV uint32_t q4_pair(uint32_t t) {   // nibbles 0 and 4 of t (offset binary) 
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(t), "r"(0x000F000Fu), "r"(0x43004300u));
   return r;
 }
-SV_DEV uint32_t q4_exact(uint32_t p) {   // (136 + v) x 2 -> v x 2, exactly
-  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&p);
-  const __nv_bfloat162 c = __floats2bfloat162_rn(136.f, 136.f);
-  h = __hsub2(h, c);
-  return *reinterpret_cast<uint32_t*>(&h);
+SV_DEV uint32_t q4_exact(uint32_t p) {   // (136 + v) x 2 -> v x 2, exactly (0x4308 = bf16 136)
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(0x43084308u));
+  return r;
 }
 SV_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-SV_DEV void q4_step(float (&tot)[4], const unsigned char* tile, int half, int ngrp, int ks, const uint4& x0,
-                    const uint4& x1, int gi, int ci) {
-  const int lb = (ks & 3) * 32 + ci * 8;   // logical byte of the thread's codes in the block's 128-B row
-  const int off = (ks >> 2) * 1024 + gi * 128 + ((((lb >> 4) ^ gi) & 7) << 4) + (lb & 15);
+// Two chained MMAs over the 8 codes (one word) of each row of a pair against
+// the thread's X pairs for them.
+SV_DEV void q4_mma(float (&acc)[4], uint32_t wa, uint32_t wb, uint32_t xa, uint32_t xb, uint32_t xc, uint32_t xd,
+                   bool first) {
+  const uint32_t ta = wa ^ 0x88888888u, tb = wb ^ 0x88888888u;
+  const uint32_t a0 = q4_exact(q4_pair(ta)), b0 = q4_exact(q4_pair(tb));
+  const uint32_t a1 = q4_exact(q4_pair(ta >> 4)), b1 = q4_exact(q4_pair(tb >> 4));
+  const uint32_t a2 = q4_exact(q4_pair(ta >> 8)), b2 = q4_exact(q4_pair(tb >> 8));
+  const uint32_t a3 = q4_exact(q4_pair(ta >> 12)), b3 = q4_exact(q4_pair(tb >> 12));
+  if (first)
+    mma_bf16_16816_z(acc, a0, b0, a1, b1, xa, xb);
+  else
+    mma_bf16_16816_acc(acc, a0, b0, a1, b1, xa, xb);
+  mma_bf16_16816_acc(acc, a2, b2, a3, b3, xc, xd);
+}
+// The thread's 8 code bytes of group ks in row gi of a half: block ks / 4,
+// logical 16-byte chunk 2 (ks mod 4) + ci / 2 of the row, swizzled by the
+// row (rbase = gi * 128 + (ci mod 2) * 8).
+// kResident: x0, x1 are already in the codes' pair order; else they are
+// natural X and permuted here.
+template <bool kResident>
+SV_DEV void q4_step(float (&tot)[4], const unsigned char* tile, int half, int ngrp, int ks, int rbase, int ci,
+                    const uint4& x0, const uint4& x1, int gi) {
+  const int off = (ks >> 2) * 1024 + rbase + (((((ks & 3) << 1) + (ci >> 1)) ^ gi) & 7) * 16;
   const uint2 ca = *reinterpret_cast<const uint2*>(tile + off);
   const uint2 cb = *reinterpret_cast<const uint2*>(tile + half + off);
   const unsigned char* sc = tile + 2 * half + ks * 16 + gi * 2;
   const float sa = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc) << 16);
   const float sb = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc + ngrp * 16) << 16);
-  float acc[4];
-  // codes 0..7 of the row: pairs (0,4) (1,5) (2,6) (3,7); X the same pairs
-  {
-    const uint32_t ta = ca.x ^ 0x88888888u, tb = cb.x ^ 0x88888888u;
-    const uint32_t xa = prmt(x0.x, x0.z, 0x5410u), xb = prmt(x0.x, x0.z, 0x7632u);
-    const uint32_t xc = prmt(x0.y, x0.w, 0x5410u), xd = prmt(x0.y, x0.w, 0x7632u);
-    float g0[4], g1[4];
-    mma_bf16_16816_z(g0, q4_exact(q4_pair(ta)), q4_exact(q4_pair(tb)), q4_exact(q4_pair(ta >> 4)),
-                     q4_exact(q4_pair(tb >> 4)), xa, xb);
-    mma_bf16_16816_z(g1, q4_exact(q4_pair(ta >> 8)), q4_exact(q4_pair(tb >> 8)), q4_exact(q4_pair(ta >> 12)),
-                     q4_exact(q4_pair(tb >> 12)), xc, xd);
-    acc[0] = g0[0] + g1[0];
-    acc[1] = g0[1] + g1[1];
-    acc[2] = g0[2] + g1[2];
-    acc[3] = g0[3] + g1[3];
+  float acc[4], acd[4];
+  // codes 0..7 of the row pair, then 8..15 (two independent chains)
+  if (kResident) {
+    q4_mma(acc, ca.x, cb.x, x0.x, x0.y, x0.z, x0.w, true);
+    q4_mma(acd, ca.y, cb.y, x1.x, x1.y, x1.z, x1.w, true);
+  } else {
+    q4_mma(acc, ca.x, cb.x, prmt(x0.x, x0.z, 0x5410u), prmt(x0.x, x0.z, 0x7632u), prmt(x0.y, x0.w, 0x5410u),
+           prmt(x0.y, x0.w, 0x7632u), true);
+    q4_mma(acd, ca.y, cb.y, prmt(x1.x, x1.z, 0x5410u), prmt(x1.x, x1.z, 0x7632u), prmt(x1.y, x1.w, 0x5410u),
+           prmt(x1.y, x1.w, 0x7632u), true);
   }
-  {
-    const uint32_t ta = ca.y ^ 0x88888888u, tb = cb.y ^ 0x88888888u;
-    const uint32_t xa = prmt(x1.x, x1.z, 0x5410u), xb = prmt(x1.x, x1.z, 0x7632u);
-    const uint32_t xc = prmt(x1.y, x1.w, 0x5410u), xd = prmt(x1.y, x1.w, 0x7632u);
-    float g0[4], g1[4];
-    mma_bf16_16816_z(g0, q4_exact(q4_pair(ta)), q4_exact(q4_pair(tb)), q4_exact(q4_pair(ta >> 4)),
-                     q4_exact(q4_pair(tb >> 4)), xa, xb);
-    mma_bf16_16816_z(g1, q4_exact(q4_pair(ta >> 8)), q4_exact(q4_pair(tb >> 8)), q4_exact(q4_pair(ta >> 12)),
-                     q4_exact(q4_pair(tb >> 12)), xc, xd);
-    acc[0] += g0[0] + g1[0];
-    acc[1] += g0[1] + g1[1];
-    acc[2] += g0[2] + g1[2];
-    acc[3] += g0[3] + g1[3];
-  }
-  tot[0] = fmaf(sa, acc[0], tot[0]);
-  tot[1] = fmaf(sa, acc[1], tot[1]);
-  tot[2] = fmaf(sb, acc[2], tot[2]);
-  tot[3] = fmaf(sb, acc[3], tot[3]);
+  tot[0] = fmaf(sa, acc[0] + acd[0], tot[0]);
+  tot[1] = fmaf(sa, acc[1] + acd[1], tot[1]);
+  tot[2] = fmaf(sb, acc[2] + acd[2], tot[2]);
+  tot[3] = fmaf(sb, acc[3] + acd[3], tot[3]);
 }
 
 // Consumer warps of a q4 GEMM phase: every stage holds gt tiles x kc k as
@@ -500,17 +501,33 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
   const GemmDesc& g = d.g;
   const TmaGeo q = tma_geo(d, nullptr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
-  const int ngrp = q.kc / 64;               // 64-k groups per tile in a stage
+  const int ngrp = q.kc / 64;               // 64-k groups per tile in a stage (a power of two)
+  const int lgn = 31 - __clz(ngrp);
   const int half = (q.kc / kTmaK) * 1024;   // codes of one 8-row half
   const int steps = q.gt * ngrp;
+  const int nj = (steps + kCWarps - 1) / kCWarps;   // steps per warp per stage
   const bool has_tok = gi < q.ntok;
   const size_t xs_pitch = (size_t)(q.k + kXPad) * 2;
   const unsigned char* xrow = xreg + gi * xs_pitch + ci * 32;
+  const int rbase = gi * 128 + (ci & 1) * 8;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
   const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
   const int tiles_all = gemm_tiles_of(g);
   bool xok = true;
-  if (kResident && q.n > 0) xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
+  if (kResident && q.n > 0) {
+    xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
+    // every 8-element block of the rows permuted once into the codes' pair
+    // order (0,4) (1,5) (2,6) (3,7)
+    const int nb = q.k / 8;
+    for (int e = threadIdx.x; xok && e < q.ntok * nb; e += kConsumerThreads) {
+      const int t = e / nb, bq = e - t * nb;
+      uint4* blk = reinterpret_cast<uint4*>(const_cast<unsigned char*>(xreg) + t * xs_pitch) + bq;
+      const uint4 v = *blk;
+      *blk = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
+                        prmt(v.y, v.w, 0x7632u));
+    }
+    named_sync(kGemmBarrier, kConsumerThreads);
+  }
   int i = 0, slot = 0;
 #pragma unroll 1
   for (int grp = 0; grp < q.ngroups; ++grp) {
@@ -527,11 +544,13 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
       }
       if (ok) {
         const unsigned char* st = ring + (size_t)slot * q.sb;
-#pragma unroll 1
-        for (int s = warp; s < steps; s += kCWarps) {
-          const int gq = s / ngrp, ks = s - gq * ngrp;
-          const int kg = c * q.kc + ks * 64;
-          if (gq >= ng || kg >= q.k) continue;
+        const int kc0 = c * q.kc;
+#pragma unroll 4
+        for (int j = 0; j < nj; ++j) {
+          const int s = warp + kCWarps * j;
+          const int gq = s >> lgn, ks = s & (ngrp - 1);
+          const int kg = kc0 + ks * 64;
+          if (s >= steps || gq >= ng || kg >= q.k) continue;
           uint4 x0 = zero4, x1 = zero4;
           if (has_tok) {
             const unsigned char* xp =
@@ -541,9 +560,9 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
             x1 = *reinterpret_cast<const uint4*>(xp + 16);
           }
           if (gq)
-            q4_step(accB, st + (size_t)q.tile_bytes, half, ngrp, ks, x0, x1, gi, ci);
+            q4_step<kResident>(accB, st + (size_t)q.tile_bytes, half, ngrp, ks, rbase, ci, x0, x1, gi);
           else
-            q4_step(accA, st, half, ngrp, ks, x0, x1, gi, ci);
+            q4_step<kResident>(accA, st, half, ngrp, ks, rbase, ci, x0, x1, gi);
         }
       }
       __syncwarp();

@@ -25,6 +25,9 @@ What it restates, and from where:
   Floor 6) with its one-hot proposals.
 * ``quant``   -- the 4-bit group-quantized weight format (codes, bf16 scales,
   packing) and its dequantization.
+* ``heads``   -- drafting by extra prediction heads on the target's own final
+  hidden state ("Speculative Decoding 101", Floor 6; "Speculative decoding
+  internals", 三條主流變體: MTP).
 
 Pins that tie this oracle to something other than itself live in
 ``tests/test_oracle_*.py`` (worked example, exhaustive enumeration, greedy

@@ -141,6 +141,22 @@ def decoder_layer(x, lw, shape, positions, rnd=None):
 ACT_ROUNDING = {"f64": None, "bf16": round_bf16}
 
 
+def hidden(shape, weights, tokens, rnd=None):
+    """Residual stream [n, d] (fp64) after the last decoder layer, at every
+    position of ``tokens`` (positions 0..n-1), before the final RMSNorm."""
+    tok = torch.as_tensor(tokens, dtype=torch.long).reshape(-1)
+    positions = torch.arange(tok.numel())
+    x = _w(weights["embed"][tok.to(weights["embed"].device)])
+    for lw in weights["layers"]:
+        x = decoder_layer(x, lw, shape, positions, rnd)
+    return x
+
+
+def final_input(shape, weights, x, rnd=None):
+    """The LM head's input for residual rows x, as (a, s) (see _norm_input)."""
+    return _norm_input(x, weights["final_norm"], shape.rms_eps, rnd)
+
+
 def forward(shape, weights, tokens, last=None, act="f64", rnd=None):
     """Logits [n, V] (fp64) at every position of ``tokens`` (positions 0..n-1).
 
@@ -153,13 +169,8 @@ def forward(shape, weights, tokens, last=None, act="f64", rnd=None):
     """
     if rnd is None:
         rnd = ACT_ROUNDING[act]
-    tok = torch.as_tensor(tokens, dtype=torch.long).reshape(-1)
-    n = tok.numel()
-    positions = torch.arange(n)
-    x = _w(weights["embed"][tok.to(weights["embed"].device)])
-    for lw in weights["layers"]:
-        x = decoder_layer(x, lw, shape, positions, rnd)
+    x = hidden(shape, weights, tokens, rnd)
     if last is not None:
-        x = x[n - last:]
-    a, s = _norm_input(x, weights["final_norm"], shape.rms_eps, rnd)
+        x = x[x.shape[0] - last:]
+    a, s = final_input(shape, weights, x, rnd)
     return (a @ _w(weights["lm_head"]).T) * s

@@ -145,6 +145,16 @@ typedef struct spec_opts {
                                    most recent longest (up to n tokens) earlier match of the
                                    context's end, q is one-hot at each draft, and the draft
                                    model is not run (draft_mix_lambda must be 0) */
+    const void* draft_heads;    /* NULL = off; else self-draft heads ([101 Floor 6], [INT
+                                   三條主流變體] MTP: extra prediction heads on the target):
+                                   device pointer to K stacked row-major d_model x d_model
+                                   matrices W_1..W_K in the target's arithmetic dtype (bf16
+                                   for bf16 and 4-bit targets, fp32 for fp32 targets),
+                                   16-byte aligned, caller-owned.  Head i drafts position
+                                   L + i from the target's LM-head input u at the last
+                                   scored position: q_i logits = W_head (u + silu(W_i u)).
+                                   The draft model is not used (pass draft = NULL); needs
+                                   batch 1, K <= 8, draft_lookup 0, draft_mix_lambda 0 */
 } spec_opts;
 
 typedef struct spec_stats {
@@ -166,7 +176,8 @@ typedef struct spec_stats {
     int64_t timed_gemm_launches;
 } spec_stats;
 
-/* Create a context for one target/draft pair and K drafts per step.
+/* Create a context for one target/draft pair and K drafts per step (with
+ * opts->draft_heads the target drafts for itself and draft may be NULL).
  * Checks shapes (head_dim in {32, 64, 128}; n_heads a multiple of
  * n_kv_heads; d_model, ffn_dim and n_heads*head_dim multiples of 64 for
  * bf16 models, of 4 for fp32 models), equal vocabularies

@@ -53,7 +53,8 @@ class ModelDesc(ctypes.Structure):
 class Opts(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("max_ctx", ctypes.c_int), ("temperature", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("draft_mix_lambda", ctypes.c_float),
-                ("cuda_stream", ctypes.c_void_p), ("flags", ctypes.c_int), ("draft_lookup", ctypes.c_int)]
+                ("cuda_stream", ctypes.c_void_p), ("flags", ctypes.c_int), ("draft_lookup", ctypes.c_int),
+                ("draft_heads", ctypes.c_void_p)]
 
 
 class Stats(ctypes.Structure):
@@ -179,20 +180,28 @@ class SpecDecoder:
     """One target/draft pair with K drafts per step over `batch` sequences
     (batch > 1: bf16 models, every sequence advancing independently);
     lookup = n > 0 drafts by prompt lookup (n-gram suffix match up to n
-    tokens) instead of running the draft model."""
+    tokens) instead of running the draft model; heads = a device tensor
+    [K, d_model, d_model] in the target's arithmetic dtype drafts with
+    self-draft heads on the target (draft_shape / draft_w then None)."""
 
     def __init__(self, target_shape, target_w, draft_shape, draft_w, k, max_ctx,
-                 temperature=0.0, seed=0, mix_lambda=0.0, stream=None, flags=0, batch=1, lookup=0):
+                 temperature=0.0, seed=0, mix_lambda=0.0, stream=None, flags=0, batch=1, lookup=0,
+                 heads=None):
         self.k = k
         self.batch = batch
         self.vocab = target_shape.vocab
         self._td, self._tk = model_desc(target_shape, target_w)
-        self._dd, self._dk = model_desc(draft_shape, draft_w)
+        self._heads = heads
+        if draft_shape is None:
+            self._dd, self._dk = None, None
+        else:
+            self._dd, self._dk = model_desc(draft_shape, draft_w)
         opts = Opts(batch, max_ctx, temperature, seed, mix_lambda,
-                    ctypes.c_void_p(stream) if stream else ctypes.c_void_p(0), flags, lookup)
+                    ctypes.c_void_p(stream) if stream else ctypes.c_void_p(0), flags, lookup,
+                    ctypes.c_void_p(heads.data_ptr() if heads is not None else 0))
         h = ctypes.c_void_p()
-        rc = lib().spec_init(ctypes.byref(self._td), ctypes.byref(self._dd), k, ctypes.byref(opts),
-                             ctypes.byref(h))
+        rc = lib().spec_init(ctypes.byref(self._td), ctypes.byref(self._dd) if self._dd is not None else None, k,
+                             ctypes.byref(opts), ctypes.byref(h))
         _check(rc)
         self.ctx = h
 

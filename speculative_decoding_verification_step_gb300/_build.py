@@ -17,7 +17,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libspecverify.so")
 
-SOURCES = ["gemm.cu", "tcgemm.cu", "layers.cu", "sample.cu", "lookup.cu", "persist.cu", "engine.cu", "noalloc.cu"]
+SOURCES = ["gemm.cu", "tcgemm.cu", "layers.cu", "sample.cu", "lookup.cu", "heads.cu", "persist.cu", "engine.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -16,6 +16,14 @@
 //   readback     : one small device-to-host copy of (tokens, count, flags).
 // Every position and index is read from device memory, so the whole step is
 // captured once as a CUDA graph and replayed.
+//
+// Self-draft heads (opts.draft_heads; "Speculative Decoding 101", Floor 6,
+// "Speculative decoding internals", 三條主流變體 MTP) replace the draft passes
+// by one heads pass over the target's LM-head input at the last scored
+// position: z_i = u + silu(W_i u) for the K heads in one GEMM, the target's
+// LM head over the K rows z_i, then the K drafts in one sampler launch.
+// After the acceptance a one-block kernel keeps verify row n (n accepted) as
+// the next heads pass's input.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -89,7 +97,7 @@ struct spec_ctx {
   // for 4-bit models the prefill chunks of kPrefillChunk positions at the
   // host-set position: target (K+4), target with its LM-head rows (K+5),
   // draft (K+6)
-  PersistFwd pforward[20];
+  PersistFwd pforward[24];
   bool q4 = false;                 // a 4-bit model: prefill runs the persistent chunks
   float* logits_chunk = nullptr;   // [kPrefillChunk][V] LM-head rows of the last target chunk
   PhaseDesc* phase_dev = nullptr;
@@ -97,6 +105,14 @@ struct spec_ctx {
   int K = 0;
   int B = 1;                       // sequences (batch > 1: per-operation path, bf16 models)
   int lookup = 0;                  // > 0: prompt-lookup drafting with suffix matches up to this
+  // self-draft heads: [K][d][d] in the target's arithmetic dtype (null: none)
+  const void* heads = nullptr;
+  int heads_pass = -1;             // its persistent pass (index into pforward)
+  void* hin_x = nullptr;           // the heads' input row: the LM head's X row of the last scored position,
+  float* hin_ss = nullptr;         // its per-tile sums of squares,
+  float* hin_u = nullptr;          // and the normalised row u (fp32)
+  void* zbuf = nullptr;            // [K][d] u + silu(W_i u), the LM head's input of the heads pass
+  bool draft_model() const { return !lookup && !heads; }
   int64_t seq_ld = 0;              // int32 stride between the sequences' token arrays
   int tok_max = kGemmMaxTok;       // tokens per forward pass (batch > 1: up to kTcMaxTok)
   float* tc_part = nullptr;        // tensor-core GEMM partials (batch > 1), tc_units work units
@@ -429,6 +445,50 @@ std::vector<Op> forward_ops(spec_ctx* c, ModelState& m, int ntok, const int32_t*
   return ops;
 }
 
+// The heads pass: z_i = u + silu(W_i u) for the K stacked heads (one GEMM
+// over the kept input row), then the target's LM head over the K rows z_i
+// into the q rows.
+std::vector<Op> heads_ops(spec_ctx* c) {
+  const ModelState& m = c->tgt;
+  const spec_model_desc& d = m.d;
+  const int dm = d.d_model, K = c->K;
+  std::vector<Op> ops;
+  Op a{};
+  a.kind = kPhaseGemm;
+  GemmDesc& g = a.g;
+  g.w[0] = c->heads; g.seg_rows[0] = K * dm; g.n = K * dm; g.k = dm; g.ntok = 1;
+  g.x = c->hin_x; g.ldx = dm; g.x_norm = d.dtype == SPEC_DTYPE_BF16 ? 2 : 1;
+  g.gain = (const float*)d.final_norm; g.ss_in = c->hin_ss; g.ss_ld = 1; g.eps = d.rms_eps;
+  g.epi = kEpiHeadRes; g.hres = c->hin_u; g.out = c->zbuf; g.ldo = K * dm;
+  ops.push_back(a);
+  Op h{};
+  h.kind = kPhaseGemm;
+  h.g.w[0] = d.lm_head; h.g.seg_rows[0] = d.vocab; h.g.n = d.vocab; h.g.k = dm; h.g.ntok = K;
+  h.g.x = c->zbuf; h.g.ldx = dm; h.g.x_norm = 0;
+  h.g.epi = kEpiStore; h.g.out = c->logits_q; h.g.ldo = d.vocab;
+  h.g.q4 = m.q4 ? 1 : 0;
+  ops.push_back(h);
+  return ops;
+}
+
+// Keeps the LM-head input row of the last scored position as the next heads
+// pass's input: row *count - 1 of the verify pass (count = emitted tokens),
+// or row `row` of a prefill / plain-decoding pass.
+void keep_head_input(Launch& L, const int32_t* count, int row) {
+  spec_ctx* c = L.c;
+  if (!c->heads) return;
+  const ModelState& m = c->tgt;
+  const bool bf = m.d.dtype == SPEC_DTYPE_BF16;
+  HeadInDesc h{};
+  h.x = bf ? c->xg : (const void*)c->x; h.x_bf16 = bf ? 1 : 0; h.ldx = m.d.d_model;
+  h.ss = c->ss; h.ss_ld = c->tok_max;
+  h.count = count; h.row = row; h.max_row = c->K;
+  h.d = m.d.d_model; h.gain = (const float*)m.d.final_norm; h.eps = m.d.rms_eps;
+  h.err = res_err(c);
+  h.out_x = c->hin_x; h.out_ss = c->hin_ss; h.out_u = c->hin_u;
+  L.note(launch_head_input(h, c->stream));
+}
+
 // Per-kernel path: one launch per operation.
 void forward(Launch& L, ModelState& m, int ntok, const int32_t* tok_base, const int32_t* tok_idx,
              int tok_off, const int32_t* pos_idx, int pos_off, int lrow0, int lrows,
@@ -511,6 +571,19 @@ SampleDesc sampler(spec_ctx* c, int which, int32_t* out_token, int64_t out_ld, c
 void enqueue_draft(Launch& L) {
   spec_ctx* c = L.c;
   const int K = c->K, V = c->tgt.d.vocab;
+  if (c->heads) {   // one heads pass, then the K drafts in one sampler launch
+    if (c->persist) {
+      forward_persist(L, c->heads_pass);
+    } else {
+      for (const Op& op : heads_ops(c)) gemm(L, op.g, c->tgt.d.dtype);
+    }
+    SampleDesc sd = sampler(c, 1, c->seq, 0, c->st, 1);   // draft i -> seq[L + i]
+    sd.batch = 0; sd.rows = K; sd.row_pos = 1;
+    sd.position = 1; sd.stream = kStreamDraft;
+    sd.logits = c->logits_q; sd.ld = V;
+    L.note(launch_sample(sd, c->stream));
+    return;
+  }
   if (c->lookup) {   // prompt lookup: drafts and one-hot q rows in one launch
     LookupDesc ld{};
     ld.seq = c->seq; ld.seq_ld = c->seq_ld; ld.lens = c->st; ld.st_ld = kStateLd;
@@ -582,6 +655,7 @@ void enqueue_step(Launch& L) {
   spec_ctx* c = L.c;
   enqueue_draft(L);
   enqueue_verify(L, true);
+  keep_head_input(L, c->result + (size_t)c->B * (c->K + 1), 0);   // verify row n = count - 1
   L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * res_words(c),
                          cudaMemcpyDeviceToHost, c->stream));
   c->launch_count--;  // the copy is not a kernel
@@ -624,6 +698,7 @@ void enqueue_ar_pass(Launch& L, bool commit) {
 void enqueue_ar(Launch& L) {
   spec_ctx* c = L.c;
   enqueue_ar_pass(L, true);
+  keep_head_input(L, nullptr, 0);
   L.note(cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * res_words(c),
                          cudaMemcpyDeviceToHost, c->stream));
   c->launch_count--;
@@ -729,9 +804,18 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   *out = nullptr;
   std::string why;
   int rc;
-  if ((rc = check_model(target, "target", &why)) != SPEC_OK) return fail(nullptr, rc, why);
-  if ((rc = check_model(draft, "draft", &why)) != SPEC_OK) return fail(nullptr, rc, why);
   if (!opts) return fail(nullptr, SPEC_E_ARG, "spec_init: null opts");
+  if ((rc = check_model(target, "target", &why)) != SPEC_OK) return fail(nullptr, rc, why);
+  // self-draft heads: no draft model (the target's shape sizes the draft-side buffers)
+  const bool heads = opts->draft_heads != nullptr;
+  if (heads && draft && draft != target)
+    return fail(nullptr, SPEC_E_ARG, "self-draft heads replace the draft model: pass draft = NULL (or the target)");
+  if (heads) draft = target;
+  if ((rc = check_model(draft, "draft", &why)) != SPEC_OK) return fail(nullptr, rc, why);
+  if (heads && (opts->batch != 1 || opts->draft_lookup != 0 || opts->draft_mix_lambda != 0.f))
+    return fail(nullptr, SPEC_E_ARG, "self-draft heads need batch 1, no prompt lookup and draft_mix_lambda 0");
+  if (heads && (K > 8 || (reinterpret_cast<uintptr_t>(opts->draft_heads) & 15u)))
+    return fail(nullptr, SPEC_E_ARG, "self-draft heads need K <= 8 and 16-byte aligned head weights");
   if (target->vocab != draft->vocab)
     return fail(nullptr, SPEC_E_VOCAB, "draft and target vocabularies differ (" +
                                            std::to_string(draft->vocab) + " vs " +
@@ -761,6 +845,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   c->K = K;
   c->B = opts->batch;
   c->lookup = opts->draft_lookup;
+  c->heads = opts->draft_heads;
   c->opts = *opts;
   c->cap = opts->max_ctx;
   c->seq_ld = (int64_t)c->cap + K + 2;
@@ -840,6 +925,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   c->gs.partial_floats = gemm_partial_floats(c->num_sms);
   c->gs.max_tiles = (int)std::max<size_t>(
       (V + 15) / 16, std::max(fmax / 8, (std::max(qkvmax, dmax) + 15) / 16));
+  if (heads) c->gs.max_tiles = std::max(c->gs.max_tiles, (int)((size_t)K * dmax / 16));   // the stacked heads
   INIT_TRY(dalloc(c, &c->gs.partials, sizeof(float) * c->gs.partial_floats));
   INIT_TRY(dalloc(c, &c->gs.tickets, sizeof(int) * c->gs.max_tiles));
   INIT_TRY(cudaMemset(c->gs.tickets, 0, sizeof(int) * c->gs.max_tiles));
@@ -849,8 +935,8 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     c->tc_units = (long long)(tpf / ((size_t)128 * kTcMaxTok));
     INIT_TRY(dalloc(c, &c->tc_part, sizeof(float) * tpf));
   }
-  const size_t nt = std::max(4, B);
-  INIT_TRY(dalloc(c, &c->samp_part, sizeof(float) * sample_partial_floats(B, V)));
+  const size_t nt = std::max(std::max(4, B), K);   // sampler rows: sequences, or the K head drafts
+  INIT_TRY(dalloc(c, &c->samp_part, sizeof(float) * sample_partial_floats(std::max(B, K), V)));
   INIT_TRY(dalloc(c, &c->samp_tick, sizeof(int) * nt));
   INIT_TRY(cudaMemset(c->samp_tick, 0, sizeof(int) * nt));
   INIT_TRY(dalloc(c, &c->acc_part, sizeof(float) * accept_partial_floats(B, K, V)));
@@ -860,7 +946,18 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
   INIT_TRY(dalloc(c, &c->result, sizeof(int32_t) * rw));
   INIT_TRY(cudaMallocHost(&c->h_result, sizeof(int32_t) * rw));
   INIT_TRY(cudaMallocHost(&c->h_pos, sizeof(int32_t) * 4));
+  if (heads) {   // the heads' input row and the LM-head input of the heads pass
+    const size_t es = (size_t)c->tgt.esize;
+    INIT_TRY(dalloc(c, &c->hin_x, es * dmax));
+    INIT_TRY(dalloc(c, &c->hin_ss, sizeof(float) * (dmax / 16 + 1)));
+    INIT_TRY(dalloc(c, &c->hin_u, sizeof(float) * dmax));
+    INIT_TRY(dalloc(c, &c->zbuf, es * (size_t)K * dmax));
+    INIT_TRY(cudaMemset(c->hin_x, 0, es * dmax));
+    INIT_TRY(cudaMemset(c->hin_ss, 0, sizeof(float) * (dmax / 16 + 1)));
+    INIT_TRY(cudaMemset(c->hin_u, 0, sizeof(float) * dmax));
+  }
   for (ModelState* m : {&c->tgt, &c->drf}) {
+    if (m == &c->drf && heads) continue;   // no draft model, no draft cache
     const size_t kvb = (size_t)m->d.n_layers * B * m->layer_kv_elems(c->cap) * m->esize;
     INIT_TRY(dalloc(c, &m->kc, kvb));
     INIT_TRY(dalloc(c, &m->vc, kvb));
@@ -902,7 +999,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
         persist_supported(draft->head_dim, lay_d.total, c->num_sms, 2)) {
       std::vector<PhaseDesc> all;
       std::vector<TensorMap128> maps;
-      size_t start[20], count[20];
+      size_t start[24] = {}, count[24] = {};
       bool encodable = true;
       // decode-attention scratch: partials in the attention buffer, own tickets
       for (const spec_model_desc* m : {target, draft})
@@ -910,7 +1007,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
                                      attn_partial_floats(maxN, (int)hqmax, (int)hdmax, c->max_chunks);
       int* const dattn_tick = c->dattn_tick;   // sized for kGemmMaxTok >= K + 1 tokens
       auto add = [&](int idx, const std::vector<Op>& ops) {
-        const bool drf = idx < K || idx == K + 2 || idx == K + 6;
+        const bool drf = (idx < K || idx == K + 2 || idx == K + 6) && !heads;
         const PersistLayout& lay = drf ? lay_d : lay_t;
         start[idx] = all.size();
         for (const Op& op : ops) {
@@ -927,7 +1024,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
         }
         count[idx] = ops.size();
       };
-      for (int i = 1; i <= K; ++i) {
+      for (int i = 1; i <= K && !heads; ++i) {
         float* qrow = c->logits_q + (size_t)(i - 1) * V;
         if (i == 1)
           add(0, forward_ops(c, c->drf, 2, c->seq, c->st, -1, c->st, -1, 1, 1, qrow, true));
@@ -938,7 +1035,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
       add(K + 1, forward_ops(c, c->tgt, 1, c->seq, c->st, 0, c->st, 0, 0, 1, c->logits_p, true));
       // last scored prompt position (st[0] - 1) of both models, run by
       // spec_prefill so that its KV rows carry the step passes' arithmetic
-      add(K + 2, forward_ops(c, c->drf, 1, c->seq, c->st, -1, c->st, -1, 0, 0, nullptr, true));
+      if (!heads) add(K + 2, forward_ops(c, c->drf, 1, c->seq, c->st, -1, c->st, -1, 0, 0, nullptr, true));
       add(K + 3, forward_ops(c, c->tgt, 1, c->seq, c->st, -1, c->st, -1, 0,
                              opts->draft_mix_lambda != 0.f ? 1 : 0, c->logits_p + (size_t)K * V, true));
       int nf = K + 4;
@@ -948,8 +1045,13 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
         add(K + 4, forward_ops(c, c->tgt, kPrefillChunk, c->seq, ep, 0, ep, 0, 0, 0, nullptr, true));
         add(K + 5, forward_ops(c, c->tgt, kPrefillChunk, c->seq, ep, 0, ep, 0, 0, kPrefillChunk, c->logits_chunk,
                                true));
-        add(K + 6, forward_ops(c, c->drf, kPrefillChunk, c->seq, ep, 0, ep, 0, 0, 0, nullptr, true));
+        if (!heads) add(K + 6, forward_ops(c, c->drf, kPrefillChunk, c->seq, ep, 0, ep, 0, 0, 0, nullptr, true));
         nf = K + 7;
+      }
+      if (heads) {   // the heads pass (the target's layout)
+        c->heads_pass = nf;
+        add(nf, heads_ops(c));
+        nf += 1;
       }
       if (encodable) {
         INIT_TRY(dalloc(c, &c->phase_dev, sizeof(PhaseDesc) * all.size()));
@@ -974,7 +1076,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
           pf.desc.phases = c->phase_dev + start[f];
           pf.desc.nphases = (int)count[f];
           pf.desc.tmaps = tmaps_dev;
-          const bool drf = f < K || f == K + 2 || f == K + 6;
+          const bool drf = (f < K || f == K + 2 || f == K + 6) && !heads;
           pf.desc.ring_bytes = (int)(drf ? lay_d.ring : lay_t.ring);
           pf.desc.bar = c->bar;
           pf.desc.err = res_err(c);
@@ -1058,7 +1160,7 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
       const bool last = p0 + kPrefillChunk >= nk;
       rc = set_eager_pos(c, s0);
       if (rc) return rc;
-      if (!c->lookup) forward_persist(Lc, K + 6);
+      if (c->draft_model()) forward_persist(Lc, K + 6);
       forward_persist(Lc, last && mix ? K + 5 : K + 4);
       CUDA_TRY(c, Lc.e);
       CUDA_TRY(c, cudaStreamSynchronize(c->stream));   // the pinned position slot is reused
@@ -1078,7 +1180,7 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
       const int nt = std::min(kGemmMaxTok, nk - p0);
       rc = set_eager_pos(c, p0, b);
       if (rc) return rc;
-      if (!c->lookup) forward(Lc, c->drf, nt, sb, nullptr, p0, pb, 0, 0, 0, nullptr, sq);
+      if (c->draft_model()) forward(Lc, c->drf, nt, sb, nullptr, p0, pb, 0, 0, 0, nullptr, sq);
       int r0 = 0, rn = 0;
       if (mix) {
         r0 = std::max(lo, p0) - p0;
@@ -1087,6 +1189,7 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
       }
       float* dst = c->logits_p + (size_t)std::max(0, p0 + r0 - lo) * V;
       forward(Lc, c->tgt, nt, sb, nullptr, p0, pb, 0, r0, rn, dst, sq);
+      if (!c->persist && p0 + nt >= nk) keep_head_input(Lc, nullptr, nt - 1);   // position L-2
       CUDA_TRY(c, Lc.e);
       // the pinned position slot is reused by the next chunk
       CUDA_TRY(c, cudaStreamSynchronize(c->stream));
@@ -1094,8 +1197,9 @@ int spec_prefill(spec_ctx* c, const int32_t* tokens, int L) {
   }
   if (c->persist) {
     c->grp = false;   // one token per pass
-    if (!c->lookup) forward_persist(Lc, K + 2);
+    if (c->draft_model()) forward_persist(Lc, K + 2);
     forward_persist(Lc, K + 3);
+    keep_head_input(Lc, nullptr, 0);   // position L-2
     CUDA_TRY(c, Lc.e);
   }
   CUDA_TRY(c, cudaMemcpyAsync(c->h_result, c->result, sizeof(int32_t) * res_words(c), cudaMemcpyDeviceToHost,
@@ -1142,7 +1246,7 @@ int spec_step(spec_ctx* c, int32_t* out_tokens, int32_t* out_count, uint32_t* ou
   if (!c) return fail(nullptr, SPEC_E_ARG, "null context");
   if (!out_tokens || !out_count) return fail(c, SPEC_E_ARG, "null output buffer");
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_step before spec_prefill");
-  if (c->draft_stale && !c->lookup)   // (prompt lookup keeps no draft cache)
+  if (c->draft_stale && c->draft_model())   // (prompt lookup and the heads keep no draft cache)
     return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
   if (max_host_L(c) + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
   const int K = c->K, B = c->B;
@@ -1213,7 +1317,7 @@ int spec_ar_step(spec_ctx* c, int32_t* out_token) {
   }
   c->host_L = c->host_Ls[0];
   c->ar_steps++;
-  c->draft_stale = true;
+  c->draft_stale = c->draft_model();
   return SPEC_OK;
 }
 
@@ -1230,7 +1334,10 @@ int spec_get_stats(const spec_ctx* c, spec_stats* o) {
   o->kernels_per_ar_step = c->kernels_ar;
   o->gemm_launches_per_verify = 4 * c->tgt.d.n_layers + 1;
   o->verify_weight_bytes = c->tgt.weight_bytes();
-  o->draft_weight_bytes = c->drf.weight_bytes();
+  // heads: the K heads plus the LM head's second read per step
+  o->draft_weight_bytes = c->heads ? (double)c->K * c->tgt.d.d_model * c->tgt.d.d_model * c->tgt.esize +
+                                         c->tgt.head_bytes()
+                                   : c->drf.weight_bytes();
   o->kv_bytes_per_token_target = c->tgt.kv_bytes_per_token();
   o->kv_bytes_per_token_draft = c->drf.kv_bytes_per_token();
   o->timed_gemm_ms = c->timed_ms;
@@ -1264,7 +1371,8 @@ int spec_profile(spec_ctx* c, int iters, spec_profile_t* out) {
   if (!c || !out) return fail(c, SPEC_E_ARG, "null argument");
   if (iters < 1) return fail(c, SPEC_E_ARG, "iters must be >= 1");
   if (!c->prefilled) return fail(c, SPEC_E_STATE, "spec_profile before spec_prefill");
-  if (c->draft_stale) return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
+  if (c->draft_stale && c->draft_model())
+    return fail(c, SPEC_E_STATE, "draft cache is stale after spec_ar_step; prefill again");
   if (max_host_L(c) + c->K + 2 > c->cap) return fail(c, SPEC_E_CAPACITY, "context would exceed max_ctx");
   void (*enq[4])(Launch&) = {enqueue_draft, enqueue_verify_only, enqueue_ar_only, enqueue_verify_forward};
   double ms[4];
@@ -1310,7 +1418,7 @@ int spec_phase_times(spec_ctx* c, int which, int64_t* out, int max_phases, int* 
   if (!c || !out || !nphases) return fail(c, SPEC_E_ARG, "null argument");
   if (!c->persist) return fail(c, SPEC_E_STATE, "no persistent forward kernel in this context");
   if (which < 0 || which > c->K + 1) return fail(c, SPEC_E_ARG, "which must be in [0, K+1]");
-  const PersistFwd& f = c->pforward[which];
+  const PersistFwd& f = c->pforward[c->heads && which < c->K ? c->heads_pass : which];
   if (!f.desc.times) return fail(c, SPEC_E_STATE, "context created without SPEC_OPT_PHASE_TIMES");
   const int n = f.desc.nphases;
   *nphases = n;
@@ -1341,7 +1449,7 @@ int spec_phase_list(spec_ctx* c, int which, int64_t* out, int max_phases, int* n
   if (!c || !out || !nphases) return fail(c, SPEC_E_ARG, "null argument");
   if (!c->persist) return fail(c, SPEC_E_STATE, "no persistent forward kernel in this context");
   if (which < 0 || which > c->K + 1) return fail(c, SPEC_E_ARG, "which must be in [0, K+1]");
-  const PersistFwd& f = c->pforward[which];
+  const PersistFwd& f = c->pforward[c->heads && which < c->K ? c->heads_pass : which];
   const int n = (int)f.host.size();
   *nphases = n;
   if (max_phases < n) return fail(c, SPEC_E_ARG, "max_phases below the number of phases");
@@ -1372,6 +1480,7 @@ int spec_model_forward(spec_ctx* c, int which, const int32_t* tokens, int n, int
   if (which != 0 && which != 1) return fail(c, SPEC_E_ARG, "which must be 0 (target) or 1 (draft)");
   if (!tokens || n < 1 || pos0 < 0) return fail(c, SPEC_E_ARG, "bad tokens");
   if (pos0 + n > c->cap) return fail(c, SPEC_E_CAPACITY, "positions exceed max_ctx");
+  if (which == 1 && c->heads) return fail(c, SPEC_E_ARG, "a context with self-draft heads has no draft model");
   ModelState& m = which == 0 ? c->tgt : c->drf;
   if (m.q4) return fail(c, SPEC_E_STATE, "spec_model_forward runs one kernel per operation: not for 4-bit models");
   for (int i = 0; i < n; ++i)

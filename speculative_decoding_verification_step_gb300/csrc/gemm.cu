@@ -150,6 +150,13 @@ __global__ void __launch_bounds__(256) gemv_f32(const __grid_constant__ GemmDesc
       const float v1 = s_val[warp][0][tok], v2 = s_val[warp][1][tok];
       if (g.epi == kEpiSwiglu) {
         ((float*)g.out)[(size_t)tok * g.ldo + tile * 8 + gi] = silu(v1) * v2;
+      } else if (g.epi == kEpiHeadRes) {
+        int lo, hi;
+        tile_rows(g, tile, gi, &lo, &hi);
+        const float* u = g.hres + (size_t)tok * g.k;
+        float* o = (float*)g.out + (size_t)tok * g.ldo;
+        if (lo >= 0) o[lo] = u[lo % g.k] + silu(v1);
+        if (hi >= 0) o[hi] = u[hi % g.k] + silu(v2);
       } else if (g.epi == kEpiQkvRope) {
         const int per = g.hd / 16, half = g.hd / 2;
         const int h = tile / per, i = 8 * (tile % per) + gi;

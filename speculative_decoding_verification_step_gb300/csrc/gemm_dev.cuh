@@ -136,6 +136,22 @@ SV_DEV void gemm_epilogue(const GemmDesc& g, int tile, const float (&acc)[NG][4]
       }
     return;
   }
+  if (g.epi == kEpiHeadRes) {
+    int lo, hi;
+    tile_rows(g, tile, gi, &lo, &hi);
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int tok = ng * 8 + 2 * ci + j;
+        if (tok >= g.ntok) continue;
+        const float* u = g.hres + (size_t)tok * g.k;
+        bf16* o = (bf16*)g.out + (size_t)tok * g.ldo;
+        if (lo >= 0) o[lo] = __float2bfloat16_rn(u[lo % g.k] + silu(acc[ng][j]));
+        if (hi >= 0) o[hi] = __float2bfloat16_rn(u[hi % g.k] + silu(acc[ng][2 + j]));
+      }
+    return;
+  }
   if (g.epi == kEpiQkvRope) {
     const int per = g.hd / 16, half = g.hd / 2;
     const int h = tile / per, i = 8 * (tile % per) + gi;

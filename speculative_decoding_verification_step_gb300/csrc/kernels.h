@@ -23,6 +23,8 @@ enum Epi : int {
   kEpiSwiglu = 2,   // out[tok][j] = silu(gate_j) * up_j, model dtype (gate/up tiles)
   kEpiQkvRope = 3,  // fused q/k/v: rotate q, k at their positions; q -> q_out (fp32),
                     // k, v -> KV cache (model dtype)
+  kEpiHeadRes = 4,  // self-draft heads: out[tok][row] = hres[tok][row mod k] + silu(y),
+                    // model dtype (the rows of K stacked d x d heads, k = d)
 };
 
 // Y = X . W^T for a "skinny" X (ntok rows), W stacked from up to three
@@ -69,6 +71,7 @@ struct GemmDesc {
   float* q_out;              // [ntok][hq][hd]
   void* kc;                  // [hkv][cap][hd] of this layer
   void* vc;
+  const float* hres;   // kEpiHeadRes: fp32 [ntok][k] residual added to silu(y)
   int q4;              // 1: 4-bit group-quantized weights (persistent kernel only): each
                        // segment is packed codes [rows][k/2] followed by bf16 scales
                        // [k/64][rows] (group-major), 16-byte aligned
@@ -208,6 +211,8 @@ struct SampleDesc {
   uint64_t step_base;
   uint32_t position;        // Philox position (draft index i; 0 for AR)
   uint32_t stream;          // Philox stream id
+  int row_pos;              // batch = 0 only: row r is the draft at position position + r of
+                            // one step (step = *step_dev + step_base), not a draw at step + r
   int32_t* out_token;       // [rows]; row r goes to out_token[(out_idx ? *out_idx : 0) + out_off + r]
   const int32_t* out_idx;
   int out_off;
@@ -278,6 +283,27 @@ struct LookupDesc {
   int64_t q_ld;
 };
 cudaError_t launch_lookup(const LookupDesc& d, cudaStream_t st);
+
+// Self-draft heads' input: copies one row of the LM head's input of a pass
+// (its X row and its per-tile sums of squares) and writes the normalised
+// row u = RMSNorm_final(h) in fp32, for the next heads pass (heads.cu).
+struct HeadInDesc {
+  const void* x;           // the pass's LM-head input rows: bf16 h * gain (x_bf16) or fp32 h
+  int x_bf16;
+  int64_t ldx;             // elements between rows
+  const float* ss;         // per-16-row-tile sums of squares of h, [d/16][ss_ld]
+  int ss_ld;
+  const int32_t* count;    // non-null: row = *count - 1, clamped to [0, max_row]
+  int row, max_row;        // else row `row` (a host-checked index)
+  int d;
+  const float* gain;       // the final RMSNorm's gain (fp32 rows; bf16 rows carry it)
+  float eps;
+  const int32_t* err;      // optional: nothing is copied while *err != 0
+  void* out_x;             // [d], the row's dtype
+  float* out_ss;           // [d/16]
+  float* out_u;            // [d]
+};
+cudaError_t launch_head_input(const HeadInDesc& h, cudaStream_t st);
 
 // ---- persistent forward (bf16 models) ----
 // One cooperative launch runs the phases of a whole forward (embedding, the

@@ -317,14 +317,19 @@ __global__ void __launch_bounds__(kSampThreads) sample_kernel(const __grid_const
       sh.mass[k] = (pm[k] == neg_inf()) ? 0.0 : (double)(pz[k] * expf(pm[k] - M));
     // batch: row r is sequence r (its own step counter, Philox row word r);
     // else rows are independent draws at steps step + r
+    // row_pos: rows are the draft positions position + r of one step
     const uint64_t st0 = s.step_dev ? (uint64_t)s.step_dev[s.batch ? (size_t)r * s.st_ld : 0] : 0;
-    const uint32_t step = (uint32_t)(st0 + s.step_base + (s.batch ? 0 : r));
-    const float u = philox_uniform(s.seed, step, s.position, s.stream, s.batch ? (uint32_t)r : 0u);
+    const uint32_t step = (uint32_t)(st0 + s.step_base + (s.batch || s.row_pos ? 0 : r));
+    const uint32_t pos = s.position + (s.row_pos ? (uint32_t)r : 0u);
+    const float u = philox_uniform(s.seed, step, pos, s.stream, s.batch ? (uint32_t)r : 0u);
     pick_chunk(sh, nch, u);
     const float* srcall = mix ? mixed : row;
     auto wfn = [&](int v) { return expf(__ldcg(srcall + v) * invT - M); };
     tok = rescan_chunk(sh, wfn, s.V);
   }
+  // rows without a finite logit (a forward that gave up) leave the scan with
+  // no token: draw 0 rather than an id outside the vocabulary
+  if (tok < 0 || tok >= s.V) tok = 0;
   if (threadIdx.x == 0) {
     // a forward that gave up (err raised) produced no logits to commit: the
     // draw is still written out, but the committed state stays as it was
@@ -520,6 +525,7 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
     tok = rescan_chunk(sh, wp, V);
   }
 
+  if (tok < 0 || tok >= V) tok = 0;   // no finite logit in the row: never an id outside the vocabulary
   if (threadIdx.x == 0) {
     int32_t* out = a.out_tokens + (size_t)r * (K + 1);
     if (a.drafts_copy)

@@ -5,6 +5,7 @@ import torch
 import speculative_decoding_verification_step_gb300 as sv
 from oracle import accept as acc
 from oracle import generate as gen
+from oracle import heads as hd
 
 SKIP_FLAGS = acc.FLAG_NEAR_EDGE | acc.FLAG_NEAR_RATIO | acc.FLAG_NEAR_TIE | acc.FLAG_RESID_ZERO
 
@@ -46,7 +47,7 @@ def equal_mass_bins(p, nbins):
 
 
 def teacher_forced(dec, T, D, prompt, k, temp, n_new, tol, mix=0.0, seed=0, max_ctx=256, tie=None,
-                   extra=None, alt=None):
+                   extra=None, alt=None, heads=None, prefilled=False):
     """Run speculative steps on the GPU decoder `dec` (already built, not yet
     prefilled) and check each one against the oracle models T (target) and D
     (draft), starting every oracle step from the GPU's committed context:
@@ -65,10 +66,15 @@ def teacher_forced(dec, T, D, prompt, k, temp, n_new, tol, mix=0.0, seed=0, max_
     the oracle (its bf16 dataflow); each compared row set is then held to tol
     plus the largest difference between the two oracle precisions on those
     rows.  extra(step, ctx, p, q, drafts, ref), if given, runs further checks
-    on each step's GPU logits.  Returns (tokens, steps, skipped, worst) with
-    worst = the largest (error, allowed) seen."""
+    on each step's GPU logits.  heads, if given: the drafts come from these
+    self-draft heads on T (oracle.heads; D and alt's draft are unused), and
+    every head row is compared (they do not depend on the drafts).
+    prefilled: dec already holds the committed context `prompt` (no prefill
+    here).  Returns (tokens, steps, skipped, worst) with worst = the largest
+    (error, allowed) seen."""
     tie = 2 * tol if tie is None else tie
-    dec.prefill(prompt)
+    if not prefilled:
+        dec.prefill(prompt)
     ctx = [int(t) for t in prompt]
     prev = gen.prefill_prev_logits(T, ctx, k) if mix else None
     out, step, skipped, tokens = 0, 0, 0, []
@@ -77,16 +83,20 @@ def teacher_forced(dec, T, D, prompt, k, temp, n_new, tol, mix=0.0, seed=0, max_
         toks, _ = dec.step()
         p, q, d, context = dec.last_step_debug(max_ctx)
         assert 1 <= len(toks) <= k + 1
-        ref = gen.spec_step(T, D, ctx, k, temp, seed, step, prev, mix, tie_eps=tie)
+        if heads is not None:
+            ref = hd.spec_step(T, heads, ctx, k, temp, seed, step, tie_eps=tie)
+        else:
+            ref = gen.spec_step(T, D, ctx, k, temp, seed, step, prev, mix, tie_eps=tie)
         same = 0
         while same < k and ref.drafts[same] == int(d[same]):
             same += 1
-        upto = min(k, same + 1)
+        upto = k if heads is not None else min(k, same + 1)
         allow_q = tol
         if alt is not None:
             T_alt, D_alt = alt
+            alt_heads = hd.head_logits(T_alt, heads, ctx) if heads is not None else None
             for i in range(upto):
-                lq = D_alt.logits(ctx + ref.drafts[:i], last=1)[0]
+                lq = alt_heads[i] if heads is not None else D_alt.logits(ctx + ref.drafts[:i], last=1)[0]
                 if mix:
                     lq = (1.0 - mix) * lq + mix * np.asarray(prev[i], dtype=np.float64)
                 allow_q = max(allow_q, tol + np.abs(lq - ref.q_logits[i]).max())

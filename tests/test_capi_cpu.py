@@ -49,8 +49,8 @@ def _desc(vocab=256, head_dim=32, dtype=sv.SPEC_DTYPE_F32, layers=None):
     return d, lay
 
 
-def _init(L, t, d, k=4, max_ctx=128, batch=1, mix=0.0, lookup=0):
-    opts = sv.Opts(batch, max_ctx, 1.0, 0, mix, None, 0, lookup)
+def _init(L, t, d, k=4, max_ctx=128, batch=1, mix=0.0, lookup=0, heads=0):
+    opts = sv.Opts(batch, max_ctx, 1.0, 0, mix, None, 0, lookup, heads)
     h = ctypes.c_void_p()
     rc = L.spec_init(ctypes.byref(t) if t is not None else None,
                      ctypes.byref(d) if d is not None else None, k, ctypes.byref(opts), ctypes.byref(h))
@@ -75,6 +75,22 @@ def test_init_argument_errors(L):
     nulls = (sv.LayerWeights * 1)()
     nl, _f = _desc(layers=nulls)
     assert _init(L, nl, d)[0] == -1
+
+
+def test_heads_argument_errors(L):
+    """Self-draft heads replace the draft model: batch 1, no lookup, no mix,
+    K <= 8, aligned weights, and no second (different) draft model."""
+    t, _a = _desc()
+    d, _b = _desc()
+    heads = 0x2000
+    assert _init(L, t, None, heads=heads, batch=2)[0] == -1
+    assert _init(L, t, None, heads=heads, lookup=2)[0] == -1
+    assert _init(L, t, None, heads=heads, mix=0.5)[0] == -1
+    assert _init(L, t, None, heads=heads, k=9)[0] == -1
+    assert _init(L, t, None, heads=heads + 4)[0] == -1      # not 16-byte aligned
+    rc, h = _init(L, t, d, heads=heads)                     # a separate draft model as well
+    assert rc == -1 and not h.value
+    assert b"draft" in L.spec_last_error(None)
 
 
 def test_lookup_argument_errors(L):

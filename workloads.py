@@ -210,6 +210,14 @@ def make_q4_weights(shape: ModelShape, seed: int, device="cpu"):
     return w
 
 
+def make_heads(shape: ModelShape, k: int, seed: int, device="cpu", std=0.02):
+    """Random self-draft heads: K stacked row-major d x d matrices [K, d, d]
+    in the target's arithmetic dtype (bf16 for bf16 and 4-bit targets)."""
+    g = _gen(seed, device)
+    dt = torch.float32 if shape.dtype == "f32" else torch.bfloat16
+    return _randn((k, shape.d_model, shape.d_model), g, device, std, dt)
+
+
 # matrix name -> (rows, k) of a shape
 def matrix_dims(shape: ModelShape, name):
     d, hd, f = shape.d_model, shape.head_dim, shape.ffn_dim

@@ -62,18 +62,29 @@ SV_DEV void grid_arrive(unsigned* bar) {
   if (threadIdx.x == 0) red_add_release_gpu(bar, 1u);
 }
 
+// The error flag is read only while still waiting -- every 64 polls -- so a
+// completed wait costs no extra round trip: a CTA that gave up stops
+// arriving, and the others notice its flag within 64 polls.  A launch that
+// starts with the flag raised (a pass before it in the same step gave up and
+// left the arrival count unbalanced) leaves before its first arrival, so no
+// wait ever completes on a stale count.
 SV_DEV bool grid_wait(unsigned* bar, unsigned target, int* err, int* s_ok, long long limit) {
   if (threadIdx.x == 0) {
     int ok = 1;
     long long spins = 0;
     while (ld_acquire_u32(bar) < target) {
-      if (++spins > limit) {
+      ++spins;
+      if (spins > limit) {
         atomicExch(err, 1);
         ok = 0;
         break;
       }
+      if ((spins & 63) == 0 && ld_volatile_i32(err) != 0) {
+        ok = 0;
+        break;
+      }
     }
-    *s_ok = ok && (*(volatile int*)err == 0);
+    *s_ok = ok;
   }
   __syncthreads();
   return *s_ok != 0;
@@ -127,7 +138,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   dattn_init_bars(dbars);
   unsigned dpar = 0;   // attention: per-warp stage parities
   store_desc(0, load_desc(0));
+  if (threadIdx.x == 0) s_ok = ld_volatile_i32(p.err) == 0;
   __syncthreads();
+  if (!s_ok) return;   // an earlier pass gave up: nothing arrived, nothing issued
   unsigned cpar = 0;   // consumers: parity of each stage's next full-barrier completion
   int npre = 0;        // units of the current GEMM phase issued before its barrier
   for (int ph = 0; ph < p.nphases; ++ph) {

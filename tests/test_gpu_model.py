@@ -165,6 +165,26 @@ def test_long_context_steps_teacher_forced():
     _teacher_forced(shape, w, dshape, dw, prompt, 5, 1.0, 20, max_ctx=1200)
 
 
+def test_long_context_greedy_spec_equals_greedy_ar():
+    """Past position 1024 the verify pass's attention takes every token of a
+    KV head in one item (token-group mode) while plain decoding scores one
+    token per item: a row's arithmetic must not depend on that, so greedy
+    speculative output equals greedy plain decoding token for token."""
+    shape = workloads.small_shape(dtype="bf16")
+    w = workloads.make_weights(shape, seed=15)
+    dshape, dw = workloads.prefix_draft(shape, w, 1)
+    wc = helpers.to_device(w)
+    dwc = {**wc, "layers": wc["layers"][:1]}
+    dec = helpers.decoder(shape, wc, dshape, dwc, 5, 1200)
+    prompt = workloads.make_prompt(shape.vocab, 1040, seed=16)[0].tolist()
+    dec.prefill(prompt)
+    spec = dec.generate(40)
+    dec.prefill(prompt)
+    ar = [dec.ar_step() for _ in range(40)]
+    assert spec == ar
+    dec.close()
+
+
 @pytest.mark.parametrize("shape", SHAPES[:2], ids=lambda s: f"{s.name}-{s.dtype}")
 def test_greedy_spec_equals_greedy_ar(shape):
     w = workloads.make_weights(shape, seed=6)

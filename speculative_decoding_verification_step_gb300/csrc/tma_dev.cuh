@@ -468,13 +468,13 @@ SV_DEV void q4_mma(float (&acc)[4], uint32_t wa, uint32_t wb, uint32_t xa, uint3
 // natural X and permuted here.
 template <bool kResident>
 SV_DEV void q4_step(float (&tot)[4], const unsigned char* tile, int half, int ngrp, int ks, int rbase, int ci,
-                    const uint4& x0, const uint4& x1, int gi) {
+                    const uint4& x0, const uint4& x1, int gi, float w) {
   const int off = (ks >> 2) * 1024 + rbase + (((((ks & 3) << 1) + (ci >> 1)) ^ gi) & 7) * 16;
   const uint2 ca = *reinterpret_cast<const uint2*>(tile + off);
   const uint2 cb = *reinterpret_cast<const uint2*>(tile + half + off);
   const unsigned char* sc = tile + 2 * half + ks * 16 + gi * 2;
-  const float sa = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc) << 16);
-  const float sb = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc + ngrp * 16) << 16);
+  const float sa = w * __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc) << 16);
+  const float sb = w * __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(sc + ngrp * 16) << 16);
   float acc[4], acd[4];
   // codes 0..7 of the row pair, then 8..15 (two independent chains)
   if (kResident) {
@@ -507,8 +507,9 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
   const int steps = q.gt * ngrp;
   const int nj = (steps + kCWarps - 1) / kCWarps;   // steps per warp per stage
   const bool has_tok = gi < q.ntok;
+  const int gx = min(gi, q.ntok - 1);       // X row read (rows past ntok are read as 0)
   const size_t xs_pitch = (size_t)(q.k + kXPad) * 2;
-  const unsigned char* xrow = xreg + gi * xs_pitch + ci * 32;
+  const unsigned char* xrow = xreg + gx * xs_pitch + ci * 32;
   const int rbase = gi * 128 + (ci & 1) * 8;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
   const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
@@ -545,24 +546,29 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
       if (ok) {
         const unsigned char* st = ring + (size_t)slot * q.sb;
         const int kc0 = c * q.kc;
+        // branch-free steps (so that the compiler can overlap them): a step
+        // past the stage's work reads group 0 of tile 0 and weighs it by 0
 #pragma unroll 4
         for (int j = 0; j < nj; ++j) {
           const int s = warp + kCWarps * j;
-          const int gq = s >> lgn, ks = s & (ngrp - 1);
-          const int kg = kc0 + ks * 64;
-          if (s >= steps || gq >= ng || kg >= q.k) continue;
-          uint4 x0 = zero4, x1 = zero4;
-          if (has_tok) {
-            const unsigned char* xp =
-                kResident ? xrow + (size_t)kg * 2
-                          : st + q.xoff + ((size_t)(ks >> 2) * q.ntok + gi) * kTmaRowBytes + (ks & 3) * 128 + ci * 32;
-            x0 = *reinterpret_cast<const uint4*>(xp);
-            x1 = *reinterpret_cast<const uint4*>(xp + 16);
-          }
-          if (gq)
-            q4_step<kResident>(accB, st + (size_t)q.tile_bytes, half, ngrp, ks, rbase, ci, x0, x1, gi);
+          int gq = s >> lgn, ks = s & (ngrp - 1);
+          int kg = kc0 + ks * 64;
+          const bool live = s < steps && gq < ng && kg < q.k;
+          gq = live ? gq : 0;
+          ks = live ? ks : 0;
+          kg = live ? kg : kc0;
+          const unsigned char* xp =
+              kResident ? xrow + (size_t)kg * 2
+                        : st + q.xoff + ((size_t)(ks >> 2) * q.ntok + gx) * kTmaRowBytes + (ks & 3) * 128 + ci * 32;
+          uint4 x0 = *reinterpret_cast<const uint4*>(xp);
+          uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
+          x0 = has_tok ? x0 : zero4;
+          x1 = has_tok ? x1 : zero4;
+          const float w = live ? 1.f : 0.f;
+          if (kResident || gq == 0)   // resident phases hold one tile per group
+            q4_step<kResident>(accA, st, half, ngrp, ks, rbase, ci, x0, x1, gi, w);
           else
-            q4_step<kResident>(accA, st, half, ngrp, ks, rbase, ci, x0, x1, gi);
+            q4_step<kResident>(accB, st + (size_t)q.tile_bytes, half, ngrp, ks, rbase, ci, x0, x1, gi, w);
         }
       }
       __syncwarp();

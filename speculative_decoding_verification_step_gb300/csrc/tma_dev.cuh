@@ -548,7 +548,7 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
         const int kc0 = c * q.kc;
         // branch-free steps (so that the compiler can overlap them): a step
         // past the stage's work reads group 0 of tile 0 and weighs it by 0
-#pragma unroll 4
+#pragma unroll 2
         for (int j = 0; j < nj; ++j) {
           const int s = warp + kCWarps * j;
           int gq = s >> lgn, ks = s & (ngrp - 1);

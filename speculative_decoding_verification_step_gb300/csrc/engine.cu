@@ -1010,6 +1010,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
         const bool drf = (idx < K || idx == K + 2 || idx == K + 6) && !heads;
         const PersistLayout& lay = drf ? lay_d : lay_t;
         start[idx] = all.size();
+        int rev = 1, prev = kPhaseEmbed;
         for (const Op& op : ops) {
           PhaseDesc p{};
           if (op.kind == kPhaseEmbed) {
@@ -1019,7 +1020,12 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
             p.a.tickets = dattn_tick;
           } else {
             encodable = persist_phase_from_gemm(p, op.g, maps, c->num_sms, lay) && encodable;
+            // GEMM tile ranges alternate direction; after attention (whose
+            // items run on the first CTAs) they are counted from the last CTA
+            rev = prev == kPhaseAttn ? 1 : 1 - rev;
+            p.rev = rev;
           }
+          prev = op.kind;
           all.push_back(p);
         }
         count[idx] = ops.size();

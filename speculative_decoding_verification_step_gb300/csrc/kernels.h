@@ -334,6 +334,11 @@ struct PhaseDesc {
   // a stage (codes of both 8-row halves, then their scales)
   int q4, tile_bytes;
   int tms[3];
+  // GEMM: tile ranges counted from the last CTA down (1) or from CTA 0 (0);
+  // the CTAs with the larger shares of tiles are then the ones that finished
+  // the previous phase early (no attention item, or a smaller share) and
+  // streamed this phase's first weights while waiting at its barrier
+  int rev;
   int attn_items;
   GemmDesc g;
   AttnDesc a;

@@ -172,11 +172,15 @@ SV_DEV TmaGeo tma_geo(const PhaseDesc& d, const unsigned char* maps) {
   q.tms0 = d.tms[0];
   q.tms1 = d.tms[1];
   q.tms2 = d.tms[2];
+  // contiguous tile ranges, the larger shares first; counted from the last
+  // CTA down when d.rev (see PhaseDesc::rev)
   const int tiles = d.tiles;
   const int G = min((int)gridDim.x, tiles);
-  const bool has = (int)blockIdx.x < G;
-  q.t0 = has ? (int)first_step_of_warp(blockIdx.x, tiles, G) : 0;
-  q.t1 = has ? (int)first_step_of_warp(blockIdx.x + 1, tiles, G) : 0;
+  const int c = d.rev ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+  const bool has = c < G;
+  const int base = tiles / G, rem = tiles - base * G;
+  q.t0 = has ? c * base + min(c, rem) : 0;
+  q.t1 = has ? q.t0 + base + (c < rem ? 1 : 0) : 0;
   q.nchunks = (q.k + q.kc - 1) / q.kc;
   q.ngroups = (q.t1 - q.t0 + q.gt - 1) / q.gt;
   q.n = q.ngroups * q.nchunks;

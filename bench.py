@@ -58,6 +58,9 @@ def parse():
                     help="one kernel per phase instead of the persistent forward kernel")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of both models")
+    ap.add_argument("--accept-bench", action="store_true",
+                    help="acceptance-kernel microbench: 1024 verify rows, V 128256, K 5, draft noise "
+                         "sigma in {0.25, 0.5, 1, 2} (one JSON line each)")
     ap.add_argument("--verify-sweep", action="store_true",
                     help="verify step alone over batch x K x context (one JSON line each): "
                          "latency, algorithmic bytes, GB/s, tensor FLOP/s")
@@ -399,6 +402,41 @@ def main():
             hist = [x + y for x, y in zip(hist, dec.stats()["accept_hist"])]
         hist_acc[id(dec)] = hist
         return ms, toks, done
+
+    if args.accept_bench:
+        # the fused acceptance kernel alone over independent verify rows:
+        # target logits N(0, 3^2), draft logits = target rows 1..K + N(0,
+        # sigma^2), drafts drawn from the draft softmax (Philox stream 0 at
+        # step = row index); inputs resident on the device, 5.78 GB > L2
+        peak, peak_kind = peaks()
+        R, KA, VA = 1024, 5, 128256
+        for sigma in (0.25, 0.5, 1.0, 2.0):
+            p, q = workloads.make_accept_rows(R, KA, VA, sigma, seed=7, device="cuda")
+            drafts = torch.empty(R, KA, dtype=torch.int32, device="cuda")
+            for i in range(KA):
+                drafts[:, i] = sv.sample_rows(q[:, i, :], 1.0, 11, step_base=0, position=i + 1,
+                                              row_stride=KA * VA, rows=R)
+            for _ in range(3):
+                sv.accept_rows(p, q, drafts, 1.0, 11)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 10
+            e0.record()
+            for _ in range(n):
+                toks, counts, flags = sv.accept_rows(p, q, drafts, 1.0, 11)
+            e1.record()
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            nbytes = R * (2 * KA + 1) * VA * 4
+            acc_mean = float(counts.float().mean()) - 1.0
+            print(json.dumps({"accept_bench": True, "rows": R, "K": KA, "V": VA, "sigma": sigma,
+                              "ms": ms, "bytes": nbytes, "GB_s": nbytes / (ms * 1e6),
+                              "frac_of_measured": nbytes / (ms * 1e6) / peak, "peak_kind": peak_kind,
+                              "rows_per_s": R / (ms * 1e-3), "accepted_per_row": acc_mean,
+                              "acceptance_alpha_approx": acc_mean / KA}), flush=True)
+            del p, q, drafts
+            torch.cuda.empty_cache()
+        return 0
 
     if args.verify_sweep:
         # the verify step (target over K+1 positions per sequence + fused

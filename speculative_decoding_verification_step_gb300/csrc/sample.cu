@@ -35,6 +35,8 @@ constexpr int kMaxChunks = 128;          // vocabularies up to 262144 tokens
 constexpr int kPerThread = kVocabChunk / kSampThreads;   // 8 contiguous tokens per thread in a rescan
 
 __host__ __device__ inline int vocab_chunks(int V) { return (V + kVocabChunk - 1) / kVocabChunk; }
+// Acceptance phase A: CTAs per logit row (one chunk per warp).
+__host__ __device__ inline int accept_blocks_per_stat(int V) { return (vocab_chunks(V) + kSampWarps - 1) / kSampWarps; }
 size_t sample_partial_floats(int rows, int V) { return (size_t)rows * vocab_chunks(V) * 3; }
 size_t accept_partial_floats(int rows, int K, int V) {
   return (size_t)rows * vocab_chunks(V) * (2 * K + 1) * 2;
@@ -119,6 +121,64 @@ SV_DEV void chunk_argmax(const float* src, int v0, int v1, float* sm_a, int* sm_
   }
   block_am(best, bi, sm_a, sm_i);
   if (threadIdx.x == 0) { *v_out = best; *i_out = bi; }
+}
+
+// One warp's statistics of one chunk [v0, v1) of a logit row: lane l reads
+// tokens v0 + 4 (l + 32 i) .. +3 with 16-byte loads (element-wise when the
+// chunk is short or not 16-byte aligned), then shuffle trees.  Softmax:
+// m = max z, s = sum exp(z - m) with z = logit / T (the values are read
+// twice, the second time from L1).  Argmax: lowest index on ties.
+SV_DEV void warp_chunk_softmax(const float* src, int v0, int v1, float invT, float* m_out, float* s_out) {
+  const int lane = threadIdx.x & 31;
+  const bool vec = v1 - v0 == kVocabChunk && (reinterpret_cast<uintptr_t>(src + v0) & 15u) == 0;
+  float m = neg_inf();
+  if (vec) {
+    const float4* p4 = reinterpret_cast<const float4*>(src + v0) + lane;
+#pragma unroll 4
+    for (int i = 0; i < kVocabChunk / 128; ++i) {
+      const float4 x = p4[32 * i];
+      m = fmaxf(m, fmaxf(fmaxf(x.x * invT, x.y * invT), fmaxf(x.z * invT, x.w * invT)));
+    }
+  } else {
+    for (int v = v0 + lane; v < v1; v += 32) m = fmaxf(m, src[v] * invT);
+  }
+  m = warp_max(m);
+  float sum = 0.f;
+  if (m != neg_inf()) {
+    if (vec) {
+      const float4* p4 = reinterpret_cast<const float4*>(src + v0) + lane;
+#pragma unroll 4
+      for (int i = 0; i < kVocabChunk / 128; ++i) {
+        const float4 x = p4[32 * i];
+        sum += (expf(x.x * invT - m) + expf(x.y * invT - m)) + (expf(x.z * invT - m) + expf(x.w * invT - m));
+      }
+    } else {
+      for (int v = v0 + lane; v < v1; v += 32) {
+        const float z = src[v] * invT;
+        sum += z == neg_inf() ? 0.f : expf(z - m);
+      }
+    }
+  }
+  *m_out = m;
+  *s_out = warp_sum(sum);
+}
+
+SV_DEV void warp_chunk_argmax(const float* src, int v0, int v1, float* v_out, int* i_out) {
+  const int lane = threadIdx.x & 31;
+  float best = neg_inf();
+  int bi = 0x7fffffff;
+  for (int v = v0 + lane; v < v1; v += 32) {
+    const float x = src[v];
+    if (x > best || (x == best && v < bi)) { best = x; bi = v; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+    am_combine(best, bi, v2, i2);
+  }
+  *v_out = best;
+  *i_out = bi;
 }
 
 // Ticket: true in every thread of the CTA that arrives last for `row`.
@@ -383,25 +443,27 @@ __global__ void __launch_bounds__(kSampThreads) accept_kernel(const __grid_const
   const float invT = greedy ? 1.f : 1.0f / a.temperature;
   const float* P = a.p + (size_t)r * a.p_ld;
   const float* Q = a.q + (size_t)r * a.q_ld;
-  const int j = blockIdx.x / nch, c = blockIdx.x % nch;   // logit row, chunk
-  const int v0 = c * kVocabChunk, v1 = min(V, v0 + kVocabChunk);
-  float* part = a.partials + (((size_t)r * nrow + j) * nch + c) * 2;
+  const int nbl = accept_blocks_per_stat(V);            // CTAs per logit row
+  const int j = blockIdx.x / nbl;                       // logit row
+  const int c = (blockIdx.x % nbl) * kSampWarps + (threadIdx.x >> 5);   // this warp's chunk
 
-  // ---- phase A: one (logit row, chunk) per CTA ----
-  {
+  // ---- phase A: one (logit row, chunk) per warp, kSampWarps chunks per CTA ----
+  if (c < nch) {
+    const int v0 = c * kVocabChunk, v1 = min(V, v0 + kVocabChunk);
+    float* part = a.partials + (((size_t)r * nrow + j) * nch + c) * 2;
     const float* src = j <= K ? P + (size_t)j * V : Q + (size_t)(j - K - 1) * V;
     if (greedy) {
       float bv;
       int bi;
-      chunk_argmax(src, v0, v1, sm_a, sm_i, &bv, &bi);
-      if (threadIdx.x == 0) { part[0] = bv; part[1] = __int_as_float(bi); }
+      warp_chunk_argmax(src, v0, v1, &bv, &bi);
+      if ((threadIdx.x & 31) == 0) { part[0] = bv; part[1] = __int_as_float(bi); }
     } else {
       float m, sum;
-      chunk_softmax_stats(src, v0, v1, invT, sm_a, sm_b, &m, &sum);
-      if (threadIdx.x == 0) { part[0] = m; part[1] = sum; }
+      warp_chunk_softmax(src, v0, v1, invT, &m, &sum);
+      if ((threadIdx.x & 31) == 0) { part[0] = m; part[1] = sum; }
     }
   }
-  if (!last_arrival(a.tickets, r, nstat * nch, &sm_flag)) return;
+  if (!last_arrival(a.tickets, r, nstat * nbl, &sm_flag)) return;
 
   // ---- phase B: fold partials in chunk order, decisions ----
   // batch: row r is sequence r (its own step counter, Philox row word r,
@@ -553,7 +615,7 @@ cudaError_t launch_accept(const AcceptDesc& a, cudaStream_t st) {
   const int nch = vocab_chunks(a.V);
   if (nch > kMaxChunks) return cudaErrorInvalidValue;
   const int nstat = a.temperature == 0.f ? a.K + 1 : 2 * a.K + 1;
-  return launch_k(accept_kernel, dim3(nstat * nch, a.rows), dim3(kSampThreads), 0, st, a);
+  return launch_k(accept_kernel, dim3(nstat * accept_blocks_per_stat(a.V), a.rows), dim3(kSampThreads), 0, st, a);
 }
 
 }  // namespace sv

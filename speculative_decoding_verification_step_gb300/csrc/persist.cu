@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   const unsigned char* maps = reinterpret_cast<const unsigned char*>(p.tmaps);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = warp == kProducerWarp;
+  const bool epiw = warp == kEpiWarp;
   // phase descriptors: one word per thread, read at the start of the
   // previous phase and stored into its shared-memory slot at that phase's
   // end, so that the load's latency is not on the way to the grid barrier
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   __syncthreads();
   if (!s_ok) return;   // an earlier pass gave up: nothing arrived, nothing issued
   unsigned cpar = 0;   // consumers: parity of each stage's next full-barrier completion
+  unsigned gcount = 0, ecount = 0;   // tile groups handed over / finished (consumers / epilogue warp)
   int npre = 0;        // units of the current GEMM phase issued before its barrier
   for (int ph = 0; ph < p.nphases; ++ph) {
     const PhaseDesc& d = s_ph[ph & 1];
@@ -155,17 +157,19 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
       if (producer) {
         if (lane == 0) tma_produce(d, npre, tp, ring, maps);
         __syncwarp();
+      } else if (epiw) {
+        if (d.q4) tma_epilogue(d, tp, red, s_inv, ecount);
       } else if (d.q4) {
         if (d.xm == kXSmem)
-          tma_consume_q4<true>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
+          tma_consume_q4<true>(d, tp, cpar, gcount, ring, xreg, red, st ? st + 4 : nullptr);
         else
-          tma_consume_q4<false>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
+          tma_consume_q4<false>(d, tp, cpar, gcount, ring, xreg, red, st ? st + 4 : nullptr);
       } else if (d.xm == kXSmem) {
         tma_consume<true>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
       } else {
         tma_consume<false>(d, tp, cpar, ring, xreg, red, s_inv, st ? st + 4 : nullptr);
       }
-    } else if (!producer) {   // attention: the eight consumer warps
+    } else if (warp < kCWarps) {   // attention: the eight consumer warps
       for (int it = blockIdx.x; it < d.attn_items; it += gridDim.x)
         dattn_item_mode<HD, kGroup, false>(d.a, it, dsm, &s_last, dbars, dpar, st ? st + 3 : nullptr);
       if (st && threadIdx.x == 0) atomicMax(st + 4, global_ns());

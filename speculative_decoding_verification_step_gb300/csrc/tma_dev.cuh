@@ -28,14 +28,19 @@
 // w takes the stage's 64-k steps w and w + 8 (16 steps per stage: with
 // gt = 2 the first eight belong to the group's first tile, the last eight to
 // its second), each into its own accumulator chain.  At the end of a group
-// every warp leaves its partial sums in shared memory; after a barrier of
-// the consumer warps one warp per tile adds the eight partials in warp
-// order, applies 1/rms (RMSNorm'd inputs) and runs the tile's epilogue while
-// the other warps go on with the next stages (resident phases alternate two
-// partial buffers, so the next group's partials never overwrite ones still
-// being read).  The summation order depends on k and the warp count only, so
-// every pass is batch-invariant.  (Handing the partials to the epilogue warp
-// through mbarriers instead of the barrier measured slower.)
+// every warp leaves its partial sums in shared memory and the group's tiles
+// are finished -- the eight partials added in warp order, 1/rms applied
+// (RMSNorm'd inputs), the epilogue run -- in one of two ways:
+//  * bf16 phases (a group spans several stages): after a barrier of the
+//    consumer warps, by one of them per tile while the others go on with the
+//    next stages (resident phases alternate two partial buffers, so the next
+//    group's partials never overwrite ones still being read);
+//  * 4-bit phases (a whole tile per stage, so a group ends at every stage):
+//    by a warp of its own (kEpiWarp), which waits on an mbarrier for the
+//    eight partials, frees the buffer and runs the epilogue; the consumer
+//    warps then share no barrier and never wait for an epilogue.  (On the
+//    bf16 phases this hand-off measured ~1.5% slower than the barrier.)  The summation order depends on k and the warp
+// count only, so every pass is batch-invariant.
 //
 // Phase boundaries.  Between arriving at the grid barrier before a GEMM
 // phase and leaving it, the producer already fills the ring with the
@@ -76,12 +81,15 @@ constexpr int kStageSteps = kStageWeightBytes / (kTileRows * kStepK * 2);   // 6
 constexpr int kCWarps = 8;                        // consumer warps (attention uses them all)
 constexpr int kConsumerThreads = kCWarps * 32;
 constexpr int kProducerWarp = kCWarps;            // lane 0 issues the tensor copies
-constexpr int kPersistThreads = (kCWarps + 1) * 32;
+constexpr int kEpiWarp = kCWarps + 1;             // adds the partials and runs the epilogues
+// (ten warps: an SM partition holds at most three, as with nine, so the
+// register budget per thread is the same)
+constexpr int kPersistThreads = (kCWarps + 2) * 32;
 constexpr int kMaxStages = 8;
 constexpr int kMaxGroupTiles = 2;
 constexpr size_t kRingMaxBytes = 160 * 1024;      // weight ring (5 stages of 32 KB)
-// group partials: [2 buffers or kMaxGroupTiles tiles][8 warps][32 lanes] float4
-constexpr size_t kRedBytes = (size_t)2 * kCWarps * 32 * 16;
+// group partials: [kMaxGroupTiles tiles][8 warps][32 lanes] float4
+constexpr size_t kRedBytes = (size_t)kMaxGroupTiles * kCWarps * 32 * 16;
 constexpr size_t kXMinBytes = 36 * 1024;          // X region: at least a 2-token 8192-wide input
 constexpr long long kWaitLimit = 1LL << 22;
 constexpr long long kDrainLimit = 1LL << 16;
@@ -92,6 +100,8 @@ constexpr size_t kTensorMapBytes = 128;
 struct TmaPipe {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t rfull;               // a group's partials written (every consumer warp)
+  uint64_t rfree;               // ... and read (the epilogue warp)
   uint64_t xfull;               // the bulk X copies of a resident-X phase
   unsigned fills[kMaxStages];   // fills issued per slot (producer)
   unsigned xfills;              // X loads issued (their barrier's phase count)
@@ -105,6 +115,8 @@ SV_DEV void tma_init(TmaPipe& tp) {
       mbar_init(&tp.empty[i], kCWarps);   // released by every consumer warp
       tp.fills[i] = 0;
     }
+    mbar_init(&tp.rfull, kCWarps);
+    mbar_init(&tp.rfree, 1);
     mbar_init(&tp.xfull, 1);
     tp.xfills = 0;
     tp.abort = 0;
@@ -121,6 +133,25 @@ SV_DEV bool tma_wait(uint64_t* bar, unsigned parity, TmaPipe& tp) {
   long long spins = 0;
   while (true) {
     if (mbar_test(bar, parity)) return true;
+    if ((++spins & 63) == 0) {
+      if (*ab) return false;
+      if (spins > kWaitLimit) {
+        *ab = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// The same for a warp with nothing else to do (the epilogue warp): each
+// failed probe backs off 64 ns, so that its polling takes few issue slots
+// from the consumer warps sharing its SM partition.
+SV_DEV bool tma_wait_idle(uint64_t* bar, unsigned parity, TmaPipe& tp) {
+  volatile int* ab = &tp.abort;
+  long long spins = 0;
+  while (true) {
+    if (mbar_test(bar, parity)) return true;
+    __nanosleep(64);
     if ((++spins & 63) == 0) {
       if (*ab) return false;
       if (spins > kWaitLimit) {
@@ -380,14 +411,14 @@ SV_DEV void tma_step(float (&acc)[4], const unsigned char* blk, const uint4& x0,
   mma_bf16_16816(acc, a1.z, b1.z, a1.w, b1.w, x1.z, x1.w);
 }
 
-// End of a tile group (every consumer warp): each warp's partial sums of
-// the group's tiles (gt = 1: a + b, the warp's two chains; gt = 2: a for the
-// first tile, b for the second) go to shared memory; after a barrier of the
-// consumer warps one warp per tile adds the eight partials in warp order,
-// applies 1/rms (RMSNorm'd inputs) and runs the tile's epilogue.  Resident
-// phases alternate two partial buffers (the next group's partials never
-// overwrite ones still being read); streamed phases use both halves for
-// their two tiles and wait for the readers before the next group.
+// End of a tile group of a bf16 phase (every consumer warp): each warp's
+// partial sums of the group's tiles (gt = 1: a + b, the warp's two chains;
+// gt = 2: a for the first tile, b for the second) go to shared memory; after
+// a barrier of the consumer warps one warp per tile adds the eight partials
+// in warp order, applies 1/rms (RMSNorm'd inputs) and runs the tile's
+// epilogue.  Resident phases alternate two partial buffers (the next group's
+// partials never overwrite ones still being read); streamed phases use both
+// halves for their two tiles and wait for the readers before the next group.
 SV_DEV void tma_group_end(const TmaGeo& q, const GemmDesc& g, TmaPipe& tp, float4* red, const float* s_inv,
                           const float (&a)[4], const float (&b)[4], bool resident, int grp, int tb, int ng, int pos0,
                           int tiles_all) {
@@ -429,6 +460,83 @@ SV_DEV void tma_group_end(const TmaGeo& q, const GemmDesc& g, TmaPipe& tp, float
   // streamed X: the partial area is not double-buffered -- the next group's
   // partials wait until the epilogue warps have read these
   if (!resident && grp + 1 < q.ngroups) named_sync(kGemmBarrier, kConsumerThreads);
+}
+
+// End of a tile group of a 4-bit phase (every consumer warp): the warp's partial sums of the
+// group's tiles (gt = 1: a + b, its two chains; gt = 2: a for the first
+// tile, b for the second) go to the partial buffer -- once the epilogue warp
+// has read the previous group's -- and the warp arrives on its barrier.
+// gcount counts the groups of the launch (every consumer warp runs the same
+// groups).
+SV_DEV void tma_group_put(const TmaGeo& q, TmaPipe& tp, float4* red, const float (&a)[4], const float (&b)[4],
+                          unsigned& gcount) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (gcount > 0) tma_wait(&tp.rfree, (gcount - 1) & 1u, tp);
+  float4* rb = red;
+  if (q.gt == 1) {
+    rb[warp * 32 + lane] = make_float4(a[0] + b[0], a[1] + b[1], a[2] + b[2], a[3] + b[3]);
+  } else {
+    rb[warp * 32 + lane] = make_float4(a[0], a[1], a[2], a[3]);
+    rb[(kCWarps + warp) * 32 + lane] = make_float4(b[0], b[1], b[2], b[3]);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&tp.rfull);
+  ++gcount;
+}
+
+// The epilogue warp during a 4-bit GEMM phase d: for every tile group of the CTA, in
+// order, wait for the eight partials (ecount counts the groups of the launch,
+// as gcount does), add them in warp order, free the buffer, apply 1/rms
+// (RMSNorm'd inputs) and run the tiles' epilogues.
+SV_DEV void tma_epilogue(const PhaseDesc& d, TmaPipe& tp, const float4* red, const float* s_inv, unsigned& ecount) {
+  static_assert(kMaxGroupTiles == 2, "the epilogue warp holds two tiles' sums");
+  const GemmDesc& g = d.g;
+  const TmaGeo q = tma_geo(d, nullptr);
+  const int lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
+  const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
+  const int tiles_all = gemm_tiles_of(g);
+#pragma unroll 1
+  for (int grp = 0; grp < q.ngroups; ++grp) {
+    const int tb = q.t0 + grp * q.gt, ng = min(q.gt, q.t1 - tb);
+    const bool ok = tma_wait_idle(&tp.rfull, ecount & 1u, tp);
+    float y0[1][4] = {{0.f, 0.f, 0.f, 0.f}}, y1[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int w = 0; w < kCWarps; ++w) {
+      const float4 v = red[w * 32 + lane];
+      y0[0][0] += v.x;
+      y0[0][1] += v.y;
+      y0[0][2] += v.z;
+      y0[0][3] += v.w;
+    }
+    if (ng > 1) {
+#pragma unroll
+      for (int w = 0; w < kCWarps; ++w) {
+        const float4 v = red[(kCWarps + w) * 32 + lane];
+        y1[0][0] += v.x;
+        y1[0][1] += v.y;
+        y1[0][2] += v.z;
+        y1[0][3] += v.w;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tp.rfree);   // the consumers may write the next group's partials
+    ++ecount;
+    for (int gq = 0; gq < ng; ++gq) {
+      const int tile = tb + gq;
+      if (!ok || tp.abort || tile >= tiles_all) continue;
+      float (&y)[1][4] = gq ? y1 : y0;
+      if (g.x_norm == 2) {
+        const float sc0 = s_inv[2 * ci], sc1 = s_inv[2 * ci + 1];
+        y[0][0] *= sc0;
+        y[0][1] *= sc1;
+        y[0][2] *= sc0;
+        y[0][3] *= sc1;
+      }
+      EpiIn pre;
+      gemm_epi_load<false>(g, tile, pos0, gi, ci, pre);
+      gemm_epilogue<1, false>(g, tile, y, gi, ci, &pre);
+    }
+  }
 }
 
 // One 64-k group of a q4 tile for rows gi (half 0) and gi + 8 (half 1):
@@ -500,9 +608,9 @@ SV_DEV void q4_step(float (&tot)[4], const unsigned char* tile, int half, int ng
 // gt tile blocks; its (tile, group) steps are dealt to the warps round robin
 // (step s to warp s mod 8), each tile's sum kept in its own accumulator.
 template <bool kResident>
-SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const unsigned char* ring,
-                           const unsigned char* xreg, float4* red, const float* s_inv, unsigned long long* stamp) {
-  const GemmDesc& g = d.g;
+SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, unsigned& gcount,
+                           const unsigned char* ring, const unsigned char* xreg, float4* red,
+                           unsigned long long* stamp) {
   const TmaGeo q = tma_geo(d, nullptr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
   const int ngrp = q.kc / 64;               // 64-k groups per tile in a stage (a power of two)
@@ -516,8 +624,6 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
   const unsigned char* xrow = xreg + gx * xs_pitch + ci * 32;
   const int rbase = gi * 128 + (ci & 1) * 8;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
-  const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
-  const int tiles_all = gemm_tiles_of(g);
   bool xok = true;
   if (kResident && q.n > 0) {
     xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
@@ -583,7 +689,7 @@ SV_DEV void tma_consume_q4(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, cons
 #pragma unroll
       for (int e = 0; e < 4; ++e) accB[e] = 0.f;
     }
-    tma_group_end(q, g, tp, red, s_inv, accA, accB, kResident, grp, tb, ng, pos0, tiles_all);
+    tma_group_put(q, tp, red, accA, accB, gcount);
   }
 }
 
@@ -597,6 +703,8 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
                         const unsigned char* xreg, float4* red, const float* s_inv, unsigned long long* stamp) {
   const GemmDesc& g = d.g;
   const TmaGeo q = tma_geo(d, nullptr);
+  const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
+  const int tiles_all = gemm_tiles_of(g);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ci = lane & 3;
   const int spt = q.kc / kStepK;            // 64-k steps per tile in a stage (16 or 8)
   const int kbs = q.kc / kTmaK;             // 256-k blocks per tile in a stage
@@ -613,8 +721,6 @@ SV_DEV void tma_consume(const PhaseDesc& d, TmaPipe& tp, unsigned& cpar, const u
   const int xoffB = q.xoff + ((kB / 4) * q.ntok + gi) * kTmaRowBytes + (kB % 4) * (kStepK * 2) + ci * 32;
   const unsigned char* xrow = xreg + gi * xs_pitch + ci * 32;
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
-  const int pos0 = q.epi == kEpiQkvRope ? __ldcg(g.pos_base) + g.pos_off : 0;
-  const int tiles_all = gemm_tiles_of(g);
   bool xok = true;
   if (kResident && q.n > 0) xok = tma_wait(&tp.xfull, (tp.xfills - 1) & 1u, tp);   // X copied in
   int i = 0, slot = 0;

@@ -266,18 +266,24 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- ours
-def phase_summary(ph):
+def phase_summary(ph, plist=None):
     """Fold per-phase stamps of one persistent pass.  Per phase: total time
     from the previous release to this one, split into prep (release -> latest
     end of X preparation; attention: latest end of a key walk), stream (->
     latest delivery of a CTA's last weight unit; attention: end of the items,
     i.e. the merges), tail (-> latest arrival: reductions and epilogues) and
     barrier (latest arrival -> release).  Summed per phase kind
-    and per GEMM shape (with its weight GB/s over the whole phase)."""
+    and per GEMM shape (with its weight GB/s over the whole phase, 2 B per
+    weight).  plist: the pass's phase list (spec_phase_list), whose 16-row
+    tiles give the weight rows a GEMM streams (a SwiGLU tile is 8 gate + 8 up
+    rows of its n output rows: 2n rows); without it, n rows."""
     kinds = {0: "embed", 1: "gemm", 2: "attn"}
     out = {"phases": len(ph), "total_us": 0.0, "by_kind": {}, "gemm_shapes": {}}
+    if plist is not None and len(plist) != len(ph):
+        raise ValueError("phase list and phase times differ in length")
+    rows_of = {}
     prev = 0
-    for p in ph:
+    for i, p in enumerate(ph):
         end = p["release_ns"] if p["release_ns"] >= 0 else p["arrive_max_ns"]
         prep_end = p["prep_max_ns"] if p["prep_max_ns"] >= 0 else prev
         work_end = p["work_max_ns"] if p["work_max_ns"] >= 0 else prep_end
@@ -291,6 +297,7 @@ def phase_summary(ph):
             agg[f] = agg.get(f, 0.0) + v
         if p["kind"] == 1:
             key = f'{p["n"]}x{p["k"]}'
+            rows_of[key] = plist[i][4] * 16 if plist is not None else p["n"]
             g = out["gemm_shapes"].setdefault(key, {"count": 0})
             g["count"] += 1
             for f, v in parts.items():
@@ -298,8 +305,8 @@ def phase_summary(ph):
         prev = end
     out["total_us"] = round(prev / 1e3, 1)
     for key, g in out["gemm_shapes"].items():
-        n, k = (int(v) for v in key.split("x"))
-        g["gbs"] = round(g["count"] * n * k * 2 / (g["us"] * 1e3), 1)
+        k = int(key.split("x")[1])
+        g["gbs"] = round(g["count"] * rows_of[key] * k * 2 / (g["us"] * 1e3), 1)
     for table in (out["by_kind"], out["gemm_shapes"]):
         for agg in table.values():
             for f in list(agg):
@@ -494,7 +501,7 @@ def main():
             dec.step()
         dec.profile(3)   # runs the verify-only and plain-decoding passes too
         print(json.dumps({"phase_times": True, "workload": wl,
-                          "passes": {name: phase_summary(dec.phase_times(i))
+                          "passes": {name: phase_summary(dec.phase_times(i), dec.phase_list(i))
                                      for name, i in (("draft_1", 0), ("draft_2", 1), ("verify", K),
                                                      ("ar", K + 1))}}), flush=True)
         return 0

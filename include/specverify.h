@@ -28,7 +28,7 @@
  *  - A context holds `batch` independent sequences (1..SPEC_MAX_BATCH).
  *    Batch 1 runs each forward as one persistent kernel (bf16 models);
  *    batch > 1 needs bf16 models and runs one kernel per operation, with
- *    the sequences' tokens in one pass (groups of at most 256 tokens, each
+ *    the sequences' tokens in one pass (groups of at most 512 tokens, each
  *    group streaming the weights once; passes of more than 16 tokens on the
  *    tensor-memory GEMM).  Sequences advance independently
  *    (ragged acceptance): every sequence has its own committed length, step

@@ -528,10 +528,13 @@ bool tc_model_ok(const ModelState& m) {
 // + j; the LM-head logits of all B * spt rows go to logits ([B][spt][V]).
 // Sequences are processed in groups of at most c->tok_max tokens (each group
 // streams the weights once; groups of more than kGemmMaxTok tokens run their
-// GEMMs on the tensor-memory GEMM, when the model's shapes allow it).
+// GEMMs on the tensor-memory GEMM, when the model's shapes allow it); the
+// fewest groups, as even as whole sequences allow.
 void forward_batch(Launch& L, ModelState& m, int spt, int tok_off, int pos_off, float* logits) {
   spec_ctx* c = L.c;
-  const int per = std::max(1, (tc_model_ok(m) ? c->tok_max : kGemmMaxTok) / spt);
+  const int cap = std::max(1, (tc_model_ok(m) ? c->tok_max : kGemmMaxTok) / spt);
+  const int ngroups = (c->B + cap - 1) / cap;
+  const int per = (c->B + ngroups - 1) / ngroups;
   const size_t V = (size_t)m.d.vocab;
   for (int b0 = 0; b0 < c->B; b0 += per) {
     const int n = std::min(per, c->B - b0);

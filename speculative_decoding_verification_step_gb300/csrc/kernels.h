@@ -99,8 +99,9 @@ constexpr int kGemmMaxTok = 64;      // tokens per GEMM pass (8 groups of 8)
 // ([units][128][npad], at most max_units units, tc_gemm_partial_floats) that
 // a second launch sums and finishes; err raised when a bounded wait gives up.
 constexpr int kTcMinTok = 16;    // the tensor-memory GEMM takes passes of more tokens
-constexpr int kTcMaxTok = 256;
-constexpr int kTcSmemBytes = 4 * (128 * 64 * 2 + kTcMaxTok * 64 * 2) + 1024;
+constexpr int kTcMaxTok = 512;
+// stage ring: 4 stages at 256 tokens, 3 up to 448, 2 at 512 (+ 1 KB alignment)
+constexpr int kTcSmemBytes = 3 * (128 * 64 * 2 + 448 * 64 * 2) + 1024;
 bool tc_gemm_supported(const GemmDesc& g);
 size_t tc_gemm_partial_floats(int num_sms, int max_n);
 cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num_sms, long long max_units,
@@ -352,7 +353,7 @@ struct PersistDesc {
   const PhaseDesc* phases;   // device array
   int nphases;
   const TensorMap128* tmaps; // device array indexed by PhaseDesc::tm
-  int ring_bytes;            // dynamic shared memory: [ring][group partials][X region]
+  int ring_bytes;            // dynamic shared memory: [group partials][ring][X region]
   unsigned* bar;             // [1] arrival count (zero at start; the kernel leaves it zero)
   int* err;                  // set to 1 when a wait gives up
   // optional fault injection (null: off): [0] arrivals added to every grid-

@@ -97,9 +97,10 @@ SV_DEV void grid_leave(unsigned* bar, unsigned total) {
 
 template <int HD, bool kGroup>
 __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __grid_constant__ PersistDesc p) {
-  // dynamic shared memory: [weight ring, p.ring_bytes][group partials,
-  // kRedBytes][X region: resident GEMM inputs]; attention phases reuse it
-  // from offset 0
+  // dynamic shared memory: [group partials, kRedBytes][weight ring,
+  // p.ring_bytes][X region: resident GEMM inputs]; a streamed-X GEMM phase,
+  // which has no resident input, runs its ring on into the X region;
+  // attention phases reuse it all from offset 0
   extern __shared__ __align__(1024) unsigned char dsm[];
   __shared__ TmaPipe tp;
   __shared__ uint64_t dbars[kDWarps * kDMaxDepth];   // attention stage barriers
@@ -107,9 +108,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
   __shared__ int s_last, s_ok;
   // the current and the next phase descriptor, staged in shared memory
   __shared__ __align__(16) PhaseDesc s_ph[2];
-  unsigned char* ring = dsm;
-  float4* red = reinterpret_cast<float4*>(dsm + p.ring_bytes);
-  unsigned char* xreg = dsm + p.ring_bytes + kRedBytes;
+  float4* red = reinterpret_cast<float4*>(dsm);
+  unsigned char* ring = dsm + kRedBytes;
+  unsigned char* xreg = dsm + kRedBytes + p.ring_bytes;
   const unsigned char* maps = reinterpret_cast<const unsigned char*>(p.tmaps);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = warp == kProducerWarp;
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persist_forward(const __gr
     if (d.kind == kPhaseEmbed) {
       for (int t = blockIdx.x; t < d.e.ntok; t += gridDim.x) embed_token<bf16, false>(d.e, t);
     } else if (d.kind == kPhaseGemm) {
-      if (d.xm == kXSmem) tma_prepare_x(d, tp, s_inv, xreg);
+      // resident X copied in; 1/rms of an RMSNorm'd input (resident or streamed)
+      if (d.xm == kXSmem || d.g.x_norm == 2) tma_prepare_x(d, tp, s_inv, xreg);
       if (st && threadIdx.x == 0) atomicMax(st + 3, global_ns());
       if (producer) {
         if (lane == 0) tma_produce(d, npre, tp, ring, maps);
@@ -284,6 +286,12 @@ bool encode_kv_map(TensorMap128& m, const void* base, int hd, long long rows, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Shared memory a GEMM phase's ring may fill: the ring region, and for a
+// streamed-X phase the X region behind it as well (it holds no input then).
+static size_t persist_ring_bytes(const PhaseDesc& p, const PersistLayout& lay) {
+  return lay.ring + (p.xm == kXGlobal ? lay.xreg : 0);
+}
+
 // q4 phase (see tma_dev.cuh): tiles of two 8-row halves (plain matrices
 // too); X resident when it fits (one tile x 4096 k per stage), else
 // streamed (two tiles x 1024 k per stage).
@@ -340,7 +348,7 @@ static bool persist_phase_q4(PhaseDesc& p, const GemmDesc& g, std::vector<Tensor
   const int xstage = p.xm == kXGlobal ? nblk * g.ntok * kTmaRowBytes : 0;
   p.xoff = p.gt * p.tile_bytes;
   p.stage_bytes = (p.gt * p.tile_bytes + xstage + 1023) / 1024 * 1024;
-  p.stages = std::min<int>(kMaxStages, (int)(lay.ring / (size_t)p.stage_bytes));
+  p.stages = std::min<int>(kMaxStages, (int)(persist_ring_bytes(p, lay) / (size_t)p.stage_bytes));
   if (p.stages < 2) return false;
   const int units_max = ((tiles_max + p.gt - 1) / p.gt) * ((g.k + p.kc - 1) / p.kc);
   p.prefetch = p.xm == kXSmem && units_max <= 8 ? std::min(p.stages, 2) : p.stages;
@@ -399,7 +407,7 @@ bool persist_phase_from_gemm(PhaseDesc& p, const GemmDesc& g, std::vector<Tensor
   const int xstage = p.xm == kXGlobal ? (p.kc / kTmaK) * g.ntok * kTmaRowBytes : 0;
   p.xoff = kStageWeightBytes;
   p.stage_bytes = (kStageWeightBytes + xstage + 1023) / 1024 * 1024;
-  p.stages = std::min<int>(kMaxStages, (int)(lay.ring / (size_t)p.stage_bytes));
+  p.stages = std::min<int>(kMaxStages, (int)(persist_ring_bytes(p, lay) / (size_t)p.stage_bytes));
   if (p.stages < 2) return false;
   // units issued before the phase's barrier: a full ring, except that a
   // resident-X phase with few units per CTA takes only 3 ahead, so that its

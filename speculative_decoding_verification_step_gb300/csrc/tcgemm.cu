@@ -1,7 +1,7 @@
 // Tensor-core GEMM on the fifth-generation tensor cores for passes of many
 // tokens (a batch of sequences' K+1 verify positions): Y = X . W^T with the
 // weights W [n][k] bf16 (the q/k/v segments, or the gate/up pair) and
-// X [ntok][k] bf16, 16 < ntok <= 256, fp32 accumulation in tensor memory.
+// X [ntok][k] bf16, 16 < ntok <= 512, fp32 accumulation in tensor memory.
 //
 // Work unit = (row tile, k split).  A row tile is 128 output rows (gate/up:
 // 64 gate rows then the same 64 up rows); the k range of the GEMM is cut into
@@ -17,7 +17,12 @@
 //                    (A = weights, B = X, both K-major) into one of two
 //                    tensor-memory accumulators (unit i: buffer i mod 2);
 //                    tcgen05.commit frees the stage, a last commit per unit
-//                    signals its accumulator complete;
+//                    signals its accumulator complete.  Past 256 tokens (the
+//                    largest MMA N) every 16-k slice is two MMAs, one per
+//                    half of the tokens, on the same weight tile, and the
+//                    npad columns leave room for one accumulator only: a
+//                    unit's MMAs then wait for the previous unit's readout,
+//                    but the weights are still read once per pass;
 //   warps 2..5       read a finished accumulator (one TMEM lane quarter each)
 //                    into the unit's fp32 partial [128][npad] while the next
 //                    unit accumulates in the other buffer, then free it;
@@ -53,6 +58,8 @@ struct TcArgs {
   TensorMap128 xmap;      // X [ntok][k]: boxes of 64 k x npad rows
   GemmDesc g;
   int npad, tiles, splits, nkb, stages, tmem_cols;
+  int halves;             // token halves per stage (npad > 256: 2, MMA N = npad / 2)
+  int nbuf;               // tensor-memory accumulators (2, or 1 when two do not fit)
   float* partials;        // [tiles * splits][128][npad]
   int* err;
 };
@@ -246,7 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     *nk = (int)((long long)(split + 1) * a.nkb / a.splits) - *kb0;
     *rot = (int)(((long long)*tile * 5) % *nk);
   };
-  const int npad = a.npad;
+  const int npad = a.npad, nh = a.npad / a.halves, nbuf = a.nbuf;
   const unsigned stage_bytes = (unsigned)(kTcABytes + npad * kTcKb * 2);
   // 1024-aligned stage bases (the swizzle pattern repeats every 1024 bytes)
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm) + 1023) & ~uintptr_t(1023));
@@ -298,20 +305,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         } else {
           tma_load_2d_hint(stage_a(s), &a.wmap[seg], kb * kTcKb, row, &full[s], pol_w);
         }
-        tma_load_2d_hint(stage_b(s), &a.xmap, kb * kTcKb, 0, &full[s], pol_x);
+        for (int h = 0; h < a.halves; ++h)   // one box per token half (a box holds at most 256 rows)
+          tma_load_2d_hint(stage_b(s) + (size_t)h * nh * (kTcKb * 2), &a.xmap, kb * kTcKb, h * nh, &full[s], pol_x);
         s_issued = q + 1;
       }
     }
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer: unit i accumulates into buffer i & 1 ----
-    const uint32_t idesc = idesc_bf16(npad);
+    // ---- MMA issuer: unit i accumulates into buffer i mod nbuf ----
+    const uint32_t idesc = idesc_bf16(nh);
     int q = 0;   // stage fills consumed
     for (int i = 0; i < my_n && !s_abort; ++i) {
       int tile, kb0, nk, rot;
       unit_of(i, &tile, &kb0, &nk, &rot);
-      const int bi = i & 1;
-      // the readout of unit i - 2 has emptied this buffer
-      if (i >= 2 && !tc_wait(&tfree[bi], (unsigned)((i / 2 - 1) & 1), &s_abort)) break;
+      const int bi = i % nbuf;
+      // the readout of unit i - nbuf has emptied this buffer
+      if (i >= nbuf && !tc_wait(&tfree[bi], (unsigned)((i / nbuf - 1) & 1), &s_abort)) break;
       tc_fence_after();
       const uint32_t acc = tmem + (uint32_t)(bi * npad);
       bool ok = true;
@@ -323,10 +331,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         }
         s_consumed = q + 1;
         tc_fence_after();
-        const uint64_t ad = smem_desc_sw128(stage_a(s)), bd = smem_desc_sw128(stage_b(s));
+        const uint64_t ad = smem_desc_sw128(stage_a(s));
+        for (int h = 0; h < a.halves; ++h) {   // token half h: columns h * nh .. of the accumulator
+          const uint64_t bd = smem_desc_sw128(stage_b(s) + (size_t)h * nh * (kTcKb * 2));
 #pragma unroll
-        for (int kk = 0; kk < kTcKb / 16; ++kk)   // 16-k slices: +32 bytes = +2 in the start field
-          tc_mma(acc, ad + 2 * kk, bd + 2 * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTcKb / 16; ++kk)   // 16-k slices: +32 bytes = +2 in the start field
+            tc_mma(acc + (uint32_t)(h * nh), ad + 2 * kk, bd + 2 * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+        }
         tc_commit(&empty[s]);
       }
       tc_commit(&done[bi]);   // completes when every MMA issued above has
@@ -337,8 +348,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const int r = q * 32 + lane;                  // tile row
     for (int i = 0; i < my_n; ++i) {
-      const int bi = i & 1;
-      if (!tc_wait(&done[bi], (unsigned)((i / 2) & 1), &s_abort)) break;
+      const int bi = i % nbuf;
+      if (!tc_wait(&done[bi], (unsigned)((i / nbuf) & 1), &s_abort)) break;
       tc_fence_after();
       const int u = (int)blockIdx.x + i * (int)gridDim.x;
       float* part = a.partials + ((size_t)u * kTcM + r) * npad;
@@ -366,9 +377,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       while (!mbar_test(&full[q % a.stages], (unsigned)((q / a.stages) & 1)) && ++spins < (1LL << 20)) {
       }
     }
-    for (int i = s_units_done; i < my_n && i < s_units_done + 2; ++i) {
+    for (int i = s_units_done; i < my_n && i < s_units_done + nbuf; ++i) {
       long long spins = 0;
-      while (!mbar_test(&done[i & 1], (unsigned)((i / 2) & 1)) && ++spins < (1LL << 20)) {
+      while (!mbar_test(&done[i % nbuf], (unsigned)((i / nbuf) & 1)) && ++spins < (1LL << 20)) {
       }
     }
   }
@@ -487,7 +498,9 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
   if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
   TcArgs a{};
   a.g = g;
-  a.npad = (g.ntok + 15) / 16 * 16;
+  // tokens padded to 16 (one MMA N), past 256 to 32 (two MMAs of N = npad / 2)
+  a.npad = g.ntok <= 256 ? (g.ntok + 15) / 16 * 16 : (g.ntok + 31) / 32 * 32;
+  a.halves = a.npad > 256 ? 2 : 1;
   a.nkb = g.k / kTcKb;
   a.tiles = g.epi == kEpiSwiglu ? g.n / 64 : (g.n + kTcM - 1) / kTcM;
   // splits (at most 8, at least two k blocks each): the fewest rounds of
@@ -506,8 +519,11 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
   }
   const int stage_bytes = kTcABytes + a.npad * kTcKb * 2;
   a.stages = std::min(8, (kTcSmemBytes - 1024) / stage_bytes);
+  if (a.stages < 2) return cudaErrorInvalidValue;
+  // two accumulators of npad columns where they fit the 512 columns, else one
+  a.nbuf = 2 * a.npad <= 512 ? 2 : 1;
   int cols = 32;
-  while (cols < 2 * a.npad) cols *= 2;   // two accumulators
+  while (cols < a.nbuf * a.npad) cols *= 2;
   a.tmem_cols = cols;
   if ((long long)a.tiles * a.splits > max_units) return cudaErrorInvalidValue;
   a.partials = partials;
@@ -518,7 +534,7 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
     const long long rows = g.epi == kEpiSwiglu ? g.n : (g.seg_rows[s] > 0 ? g.seg_rows[s] : g.n);
     if (!tc_encode_rows(a.wmap[s], g.w[s], g.k, rows, g.k, box_rows)) return cudaErrorInvalidValue;
   }
-  if (!tc_encode_rows(a.xmap, g.x, g.k, g.ntok, g.ldx, a.npad)) return cudaErrorInvalidValue;
+  if (!tc_encode_rows(a.xmap, g.x, g.k, g.ntok, g.ldx, a.npad / a.halves)) return cudaErrorInvalidValue;
   const int grid = std::min(a.tiles * a.splits, num_sms);   // persistent: one CTA per SM
   cudaError_t e = launch_k(tc_gemm_kernel, dim3(grid), dim3(kTcThreads), (size_t)kTcSmemBytes, st, a);
   if (e != cudaSuccess) return e;

@@ -250,15 +250,16 @@ SV_DEV int chunk_blocks(const TmaGeo& q, int c) {
   return min(q.kc / kTmaK, (q.k - c * q.kc + kTmaK - 1) / kTmaK);
 }
 
-// Resident-X phase, before its units: the producer thread copies the ntok
-// input rows (k bf16 each; for an RMSNorm'd input the rows already carry the
-// norm's gain) into the X region with one bulk copy per token, completing on
-// tp.xfull; every warp meanwhile folds the per-tile sums of squares into
-// s_inv[tok] = 1 / rms (RMSNorm'd inputs only).  Ends with a CTA barrier.
+// Before a resident-X or RMSNorm'd phase's units: for resident X the
+// producer thread copies the ntok input rows (k bf16 each; for an RMSNorm'd
+// input the rows already carry the norm's gain) into the X region with one
+// bulk copy per token, completing on tp.xfull; every warp meanwhile folds the
+// per-tile sums of squares into s_inv[tok] = 1 / rms (RMSNorm'd inputs,
+// resident or streamed).  Ends with a CTA barrier.
 SV_DEV void tma_prepare_x(const PhaseDesc& d, TmaPipe& tp, float* s_inv, unsigned char* xreg) {
   const GemmDesc& g = d.g;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == kProducerWarp && lane == 0 && tma_geo(d, nullptr).n > 0) {
+  if (d.xm == kXSmem && warp == kProducerWarp && lane == 0 && tma_geo(d, nullptr).n > 0) {
     const int k = g.k, ntok = g.ntok, ldx = g.ldx;
     const bf16* x = (const bf16*)g.x;
     fence_proxy_async_global();   // X was written by other CTAs before the grid barrier

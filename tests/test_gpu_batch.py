@@ -1,7 +1,7 @@
 """Batched contexts (several sequences per step) through the C ABI.
 
 A batched context runs every forward once over all sequences' tokens (the
-per-operation path, groups of at most 256 tokens), samples and accepts one row
+per-operation path, groups of at most 512 tokens), samples and accepts one row
 per sequence, and commits each sequence by its own count (ragged
 acceptance).  The pages describe one sequence; a batch is that algorithm per
 sequence, with sequence b's Philox draws at row word b.
@@ -15,8 +15,9 @@ sequence, with sequence b's Philox draws at row word b.
   logits within the bf16 tolerance, stage (ii) the oracle's acceptance with
   row word b on the GPU's logits reproduces sequence b's emitted tokens.
 * Passes of more than 16 tokens (6 or 16 sequences x 5 positions; 64 x 5 in
-  two passes of at most 256) run their GEMMs on the tensor-memory (tcgen05)
-  GEMM; the teacher-forced parity above
+  one pass whose MMAs take the tokens in two halves of 160; 64 x 9 in two
+  passes of 32 sequences, halves of 144) run their GEMMs on the tensor-memory
+  (tcgen05) GEMM; the teacher-forced parity above
   covers every GEMM kind on that path (q/k/v + RoPE + KV append, residual
   adds, gate/up + SwiGLU, LM head).  With enough sequences for a wave of
   (sequence, KV head) items, attention items carry 2 or 3 eight-row tiles
@@ -81,15 +82,17 @@ def test_batch_sequences_match_single(temp):
         assert len(ctxs[b]) == 20 + sum(len(got[s][0][b]) for s in range(steps))
 
 
-@pytest.mark.parametrize("nseq,k", [(3, 3), (6, 4), (16, 4), (48, 2), (40, 4), (64, 4)],
+@pytest.mark.parametrize("nseq,k", [(3, 3), (6, 4), (16, 4), (48, 2), (40, 4), (64, 4), (64, 8)],
                          ids=["3x4tok", "6x5tok-tensor-memory-gemm", "16x5tok-tensor-memory-gemm",
-                              "48x3tok-wide2-attention", "40x5tok-wide3-attention", "64x5tok-two-passes"])
+                              "48x3tok-wide2-attention", "40x5tok-wide3-attention", "64x5tok-token-halves",
+                              "64x9tok-two-passes"])
 @pytest.mark.parametrize("temp", [0.0, 1.0])
 def test_batch_teacher_forced(temp, nseq, k):
     # 6 x 5 and 16 x 5 tokens per verify pass: the GEMMs run on the
     # tensor-memory (tcgen05) GEMM; 48 x 3 and 40 x 5 tokens (with 152 SMs):
-    # attention items of 2 and 3 eight-row tiles; 64 x 5 = 320 tokens: two
-    # passes (sequence groups of at most 256 tokens)
+    # attention items of 2 and 3 eight-row tiles; 64 x 5 = 320 tokens: one
+    # pass, two MMAs (token halves) per weight tile; 64 x 9 = 576 tokens: two
+    # passes of 288 (sequence groups of at most 512 tokens)
     max_ctx, steps, seed = 128, 5, 7
     w, dshape, dw = _pair(seed=3)
     prompts = workloads.make_prompt(SHAPE.vocab, 12, seed=9, batch=nseq).tolist()

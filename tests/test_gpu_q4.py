@@ -137,9 +137,14 @@ def test_q4_draft_equal_target_accepts_all(small, temp):
 
 
 def test_q4_full_width_teacher_forced():
-    """8B-width 4-bit target (1 layer, vocabulary 128256) with a 1B-width
-    4-bit draft (1 layer): every phase kind of the 4-bit benchmark pair."""
-    W8 = replace(workloads.EIGHT_B, n_layers=1, dtype="q4")
+    """8B-width 4-bit target (2 layers, vocabulary 128256) with a 1B-width
+    4-bit draft (1 layer): every phase kind of the 4-bit benchmark pair.  The
+    prefill chunks of 8 positions stream their RMSNorm'd 4096-wide inputs
+    (they do not fit the X region sized for K + 1 rows); the second layer
+    makes their 1/rms matter (every first-layer input is an embedding row of
+    nearly the same rms), and every step's K + 1 target rows are compared
+    with the oracle on the GPU's own drafts, whether or not the drafts agree."""
+    W8 = replace(workloads.EIGHT_B, n_layers=2, dtype="q4")
     W1 = replace(workloads.ONE_B, n_layers=1, dtype="q4")
     tw = workloads.make_q4_weights(W8, seed=45, device="cuda")
     dw = workloads.make_q4_weights(W1, seed=46, device="cuda")
@@ -152,8 +157,16 @@ def test_q4_full_width_teacher_forced():
         lists = dec.phase_list(K)
         gemm = {p[1:3]: p for p in lists if p[0] == 1}
         assert gemm[(4096, 14336)][7] == 0 and gemm[(6144, 4096)][7] == 1   # streamed / resident input rows
+
+        def target_rows(step, ctx, p, q, d, ref):
+            seq = ctx + [int(t) for t in d]
+            want = T.logits(seq, last=K + 1)
+            allow = 2e-2 + np.abs(Tb.logits(seq, last=K + 1) - want).max()
+            err = np.abs(p - want).max()
+            assert err < allow, (step, err, allow)
+
         _, steps, skipped, worst = helpers.teacher_forced(dec, T, D, prompt, K, 1.0, 10, 2e-2, seed=11,
-                                                          max_ctx=128, alt=(Tb, Db))
+                                                          max_ctx=128, alt=(Tb, Db), extra=target_rows)
         assert skipped <= max(1, steps // 3)
         print(f"q4 full width: {steps} steps, largest logit error {worst[0]:.4f} (allowed {worst[1]:.4f})")
     finally:

@@ -116,6 +116,7 @@ struct spec_ctx {
   int64_t seq_ld = 0;              // int32 stride between the sequences' token arrays
   int tok_max = kGemmMaxTok;       // tokens per forward pass (batch > 1: up to kTcMaxTok)
   float* tc_part = nullptr;        // tensor-core GEMM partials (batch > 1), tc_units work units
+  float* tc_inv = nullptr;         // tensor-core GEMM: 1/rms per token of a normalised input
   long long tc_units = 0;
   spec_opts opts{};
   cudaStream_t stream = nullptr;
@@ -281,7 +282,7 @@ struct Launch {
 void gemm(Launch& L, const GemmDesc& g, int dtype) {
   spec_ctx* c = L.c;
   if (c->tok_max > kGemmMaxTok && g.ntok > kTcMinTok && tc_gemm_supported(g)) {   // batched passes
-    L.note(launch_tc_gemm(g, c->tc_part, res_err(c), c->num_sms, c->tc_units, c->stream));
+    L.note(launch_tc_gemm(g, c->tc_part, c->tc_inv, res_err(c), c->num_sms, c->tc_units, c->stream));
     return;
   }
   const bool timed = c->timing_verify && c->ev_used + 2 <= (int)c->ev.size();
@@ -937,6 +938,7 @@ int spec_init(const spec_model_desc* target, const spec_model_desc* draft, int K
     const size_t tpf = tc_gemm_partial_floats(c->num_sms, maxn);
     c->tc_units = (long long)(tpf / ((size_t)128 * kTcMaxTok));
     INIT_TRY(dalloc(c, &c->tc_part, sizeof(float) * tpf));
+    INIT_TRY(dalloc(c, &c->tc_inv, sizeof(float) * kTcMaxTok));
   }
   const size_t nt = std::max(std::max(4, B), K);   // sampler rows: sequences, or the K head drafts
   INIT_TRY(dalloc(c, &c->samp_part, sizeof(float) * sample_partial_floats(std::max(B, K), V)));

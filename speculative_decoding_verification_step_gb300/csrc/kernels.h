@@ -95,17 +95,20 @@ constexpr int kGemmMaxTok = 64;      // tokens per GEMM pass (8 groups of 8)
 
 // Tensor-core (tcgen05) GEMM for batched passes of kTcMinTok < ntok <=
 // kTcMaxTok tokens (tcgemm.cu): work units of 128 weight rows x a k split,
-// taken by one persistent CTA per SM; every unit writes an fp32 partial
-// ([units][128][npad], at most max_units units, tc_gemm_partial_floats) that
-// a second launch sums and finishes; err raised when a bounded wait gives up.
+// taken by one persistent CTA per SM.  A GEMM whose tiles are not split runs
+// its epilogue straight from tensor memory; otherwise every unit writes an
+// fp32 partial ([units][128][npad], at most max_units units,
+// tc_gemm_partial_floats) that a second launch sums and finishes.  inv:
+// scratch of kTcMaxTok floats (1/rms per token of a normalised input, folded
+// by a first launch).  err raised when a bounded wait gives up.
 constexpr int kTcMinTok = 16;    // the tensor-memory GEMM takes passes of more tokens
 constexpr int kTcMaxTok = 512;
 // stage ring: 4 stages at 256 tokens, 3 up to 448, 2 at 512 (+ 1 KB alignment)
 constexpr int kTcSmemBytes = 3 * (128 * 64 * 2 + 448 * 64 * 2) + 1024;
 bool tc_gemm_supported(const GemmDesc& g);
 size_t tc_gemm_partial_floats(int num_sms, int max_n);
-cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num_sms, long long max_units,
-                           cudaStream_t st);
+cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, float* inv, int* err, int num_sms,
+                           long long max_units, cudaStream_t st);
 cudaError_t configure_tc_gemm();
 
 int gemm_grid(int num_sms);

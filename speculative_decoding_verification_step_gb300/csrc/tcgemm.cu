@@ -27,12 +27,17 @@
 //                    into the unit's fp32 partial [128][npad] while the next
 //                    unit accumulates in the other buffer, then free it;
 //   warp 6           allocates and frees the tensor-memory columns.
-// A second kernel, one CTA per (tile, 32-token block), sums the tile's
-// partials in split order, scales by 1/rms of the token (normalised inputs
-// arrive as x * gain in bf16, as in the skinny GEMM) and runs the operation's
-// epilogue (store / residual add with the next norm's sums of squares and
-// x * gain / SwiGLU / RoPE + KV append), so that reductions and epilogues are
-// spread over the whole GPU.
+// The epilogue (store / residual add with the next norm's sums of squares and
+// x * gain / SwiGLU / RoPE + KV append, after scaling by 1/rms of the token:
+// normalised inputs arrive as x * gain in bf16, as in the skinny GEMM) runs
+//  * fused, when the tiles are not split in k (the LM head, the larger
+//    batched GEMMs): warps 2..5 move each finished accumulator, 32 tokens at a
+//    time, through a shared-memory tile into the epilogue;
+//  * else in a second kernel, one CTA per (tile, 32-token block), that sums
+//    the tile's partials in split order first, so that reductions and
+//    epilogues are spread over the whole GPU.
+// A normalised input's 1/rms per token is folded once per GEMM by a first
+// small kernel (tc_rms_kernel).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -60,7 +65,9 @@ struct TcArgs {
   int npad, tiles, splits, nkb, stages, tmem_cols;
   int halves;             // token halves per stage (npad > 256: 2, MMA N = npad / 2)
   int nbuf;               // tensor-memory accumulators (2, or 1 when two do not fit)
-  float* partials;        // [tiles * splits][128][npad]
+  float* partials;        // [tiles * splits][128][npad] (unfused)
+  float* inv;             // [ntok] 1/rms of a normalised input's tokens
+  int fused;              // 1: epilogue from tensor memory (splits == 1)
   int* err;
 };
 
@@ -230,6 +237,13 @@ SV_DEV void tc_epilogue(const GemmDesc& g, int tile, const float* Y, int ld, int
   }
 }
 
+// Epilogue tile of the fused path and of the reduction: [32 tokens][129] fp32
+// (odd stride: conflict-free transposed writes).
+constexpr int kTcRedTok = 32;
+constexpr int kTcRedLd = kTcM + 1;
+constexpr int kTcYBytes = kTcRedTok * kTcRedLd * 4;
+constexpr int kTcEpiBar = 1;   // named barrier of the four readout warps
+
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(1024) unsigned char tsm[];
   // stage ring barriers; per accumulator buffer: MMAs done, readout done
@@ -343,7 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       tc_commit(&done[bi]);   // completes when every MMA issued above has
       if (!ok) break;
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 2 && warp <= 5 && !a.fused) {
     // ---- accumulator -> partial [128][npad] of unit blockIdx.x + i gridDim.x ----
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const int r = q * 32 + lane;                  // tile row
@@ -365,6 +379,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&tfree[bi]);
       if (threadIdx.x == 64) s_units_done = i + 1;
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---- fused: accumulator -> epilogue, 32 tokens at a time (unit = tile) ----
+    // Every readout warp runs the same units and blocks and meets both
+    // barriers of every block, also after an abort (it then skips the work).
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int tid = (int)threadIdx.x - 64;        // 0..127 over the four warps
+    float* Y = reinterpret_cast<float*>(base + (size_t)a.stages * stage_bytes);
+    for (int i = 0; i < my_n; ++i) {
+      const int bi = i % nbuf;
+      const bool ok = tc_wait(&done[bi], (unsigned)((i / nbuf) & 1), &s_abort);
+      tc_fence_after();
+      const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+      const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(bi * npad);
+      for (int t0 = 0; t0 < g.ntok; t0 += kTcRedTok) {
+        const int nt = min(kTcRedTok, g.ntok - t0);
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < kTcRedTok; c += 16) {
+            if (t0 + c >= npad) break;   // npad is a multiple of 16: no column past the buffer is read
+            float v[16];
+            tc_ld16(acc + (uint32_t)(t0 + c), v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int tl = c + e;
+              if (tl < nt) {
+                float y = 0.f;   // the reduction's arithmetic for one split
+                y += v[e];
+                Y[tl * kTcRedLd + r] = g.x_norm == 2 ? y * a.inv[t0 + tl] : y;
+              }
+            }
+          }
+        }
+        named_sync(kTcEpiBar, 128);
+        if (ok) tc_epilogue(g, tile, Y, kTcRedLd, t0, nt, tid, 128);
+        named_sync(kTcEpiBar, 128);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tfree[bi]);
+      if (ok && threadIdx.x == 64) s_units_done = i + 1;
     }
   }
   __syncthreads();
@@ -390,11 +446,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   }
 }
 
+// 1/rms of every token of a normalised input, once per GEMM: 8 threads per
+// token sum its k/16 per-tile sums of squares (tiles strided by 8, then a
+// shuffle sum in the group of 8).
+__global__ void __launch_bounds__(kTcThreads) tc_rms_kernel(const __grid_constant__ TcArgs a) {
+  const GemmDesc& g = a.g;
+  pdl_trigger();
+  pdl_wait();
+  const int tl = threadIdx.x / 8, sub = threadIdx.x % 8, nkt = g.k / 16;
+  const int t = (int)blockIdx.x * kTcRedTok + tl;
+  float sum = 0.f;
+  if (t < g.ntok)
+    for (int i = sub; i < nkt; i += 8) sum += __ldcg(g.ss_in + (size_t)i * g.ss_ld + t);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  if (sub == 0 && t < g.ntok) a.inv[t] = 1.0f / sqrtf(sum / (float)g.k + g.eps);
+}
+
 // Reduction and epilogue of a split GEMM: one CTA per (row tile, block of
 // kTcRedTok tokens) sums the splits' partials in split order (x 1/rms) and
 // runs the epilogue for those tokens.
-constexpr int kTcRedTok = 32;
-constexpr int kTcRedLd = kTcM + 1;   // odd stride: conflict-free transposed writes
 __global__ void __launch_bounds__(kTcThreads) tc_reduce_kernel(const __grid_constant__ TcArgs a) {
   __shared__ float Y[kTcRedTok * kTcRedLd];
   __shared__ float s_inv[kTcRedTok];
@@ -403,16 +475,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_reduce_kernel(const __grid_cons
   const int nt = min(kTcRedTok, g.ntok - t0), npad = a.npad;
   pdl_trigger();
   pdl_wait();
-  if (g.x_norm == 2) {   // 8 threads per token, k tiles strided, in-group shuffle sum
-    const int tl = threadIdx.x / 8, sub = threadIdx.x % 8, nkt = g.k / 16;
-    float sum = 0.f;
-    if (tl < nt)
-      for (int i = sub; i < nkt; i += 8) sum += __ldcg(g.ss_in + (size_t)i * g.ss_ld + t0 + tl);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    if (sub == 0 && tl < kTcRedTok) s_inv[tl] = 1.0f / sqrtf(sum / (float)g.k + g.eps);
-  }
+  if (g.x_norm == 2 && threadIdx.x < nt) s_inv[threadIdx.x] = __ldcg(a.inv + t0 + threadIdx.x);
   __syncthreads();
   const float* P = a.partials + (size_t)tile * a.splits * kTcM * npad + t0;
   // 4 elements per thread at a time, their partial loads in flight together;
@@ -493,8 +556,8 @@ bool tc_gemm_supported(const GemmDesc& g) {
   return true;
 }
 
-cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num_sms, long long max_units,
-                           cudaStream_t st) {
+cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, float* inv, int* err, int num_sms,
+                           long long max_units, cudaStream_t st) {
   if (!tc_gemm_supported(g)) return cudaErrorInvalidValue;
   TcArgs a{};
   a.g = g;
@@ -503,22 +566,27 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
   a.halves = a.npad > 256 ? 2 : 1;
   a.nkb = g.k / kTcKb;
   a.tiles = g.epi == kEpiSwiglu ? g.n / 64 : (g.n + kTcM - 1) / kTcM;
-  // splits (at most 8, at least two k blocks each): the fewest rounds of
-  // units per CTA times the k blocks of a unit, fewest splits on ties, within
-  // the partials
+  // splits (at most 8, at least two k blocks each): the least modelled time
+  // -- rounds of units per CTA times the k blocks of a unit, each block a
+  // stage of weights and X at ~50 GB/s per SM, plus for split tiles the
+  // partials written and read again (~50 GB/s per SM) and the reduction's
+  // launch -- fewest splits on ties, within the partials
+  const double kb_us = (double)(kTcABytes + a.npad * kTcKb * 2) / 50e3;
   a.splits = 1;
-  long long best = -1;
+  double best = -1.0;
   for (int sp = 1; sp <= std::max(1, std::min(8, a.nkb / 2)); ++sp) {
     const long long units = (long long)a.tiles * sp;
     if (units > max_units) break;
-    const long long cost = ((units + num_sms - 1) / num_sms) * ((a.nkb + sp - 1) / sp);
+    double cost = (double)((units + num_sms - 1) / num_sms) * ((a.nkb + sp - 1) / sp) * kb_us;
+    if (sp > 1) cost += (double)units * kTcM * a.npad * 8.0 / (50e3 * num_sms) + 5.0;
     if (best < 0 || cost < best) {
       best = cost;
       a.splits = sp;
     }
   }
+  a.fused = a.splits == 1 ? 1 : 0;
   const int stage_bytes = kTcABytes + a.npad * kTcKb * 2;
-  a.stages = std::min(8, (kTcSmemBytes - 1024) / stage_bytes);
+  a.stages = std::min(8, (kTcSmemBytes - 1024 - (a.fused ? kTcYBytes : 0)) / stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidValue;
   // two accumulators of npad columns where they fit the 512 columns, else one
   a.nbuf = 2 * a.npad <= 512 ? 2 : 1;
@@ -527,7 +595,9 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
   a.tmem_cols = cols;
   if ((long long)a.tiles * a.splits > max_units) return cudaErrorInvalidValue;
   a.partials = partials;
+  a.inv = inv;
   a.err = err;
+  if (g.x_norm == 2 && !inv) return cudaErrorInvalidValue;
   const int box_rows = g.epi == kEpiSwiglu ? 64 : kTcM;
   for (int s = 0; s < 3; ++s) {
     if (!g.w[s]) continue;
@@ -536,8 +606,13 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, int* err, int num
   }
   if (!tc_encode_rows(a.xmap, g.x, g.k, g.ntok, g.ldx, a.npad / a.halves)) return cudaErrorInvalidValue;
   const int grid = std::min(a.tiles * a.splits, num_sms);   // persistent: one CTA per SM
-  cudaError_t e = launch_k(tc_gemm_kernel, dim3(grid), dim3(kTcThreads), (size_t)kTcSmemBytes, st, a);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (g.x_norm == 2) {
+    e = launch_k(tc_rms_kernel, dim3((g.ntok + kTcRedTok - 1) / kTcRedTok), dim3(kTcThreads), 0, st, a);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_k(tc_gemm_kernel, dim3(grid), dim3(kTcThreads), (size_t)kTcSmemBytes, st, a);
+  if (e != cudaSuccess || a.fused) return e;
   return launch_k(tc_reduce_kernel, dim3(a.tiles, (g.ntok + kTcRedTok - 1) / kTcRedTok), dim3(kTcThreads), 0, st, a);
 }
 

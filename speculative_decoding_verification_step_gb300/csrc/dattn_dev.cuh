@@ -257,10 +257,14 @@ SV_DEV void dattn_item_rows(const AttnDesc& a, int it, unsigned char* sm, int* s
   const bool rv0 = 2 * ci < nrows, rv1 = 2 * ci + 1 < nrows;
   const int p0 = rv0 ? pbase + row_tok(2 * ci) : -1;
   const int p1 = rv1 ? pbase + row_tok(2 * ci + 1) : -1;
-  if (lane == 0)
+  if (lane == 0) {
+    // the region was last read and written through the generic proxy (the
+    // previous item's merge, the previous phase)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     for (int j = 0; j < D && j < nst; ++j)
       dattn_fetch<HD>(a, row0, first + kDWarps * j, vp, wb + j * L::kStageElems,
                       wb + j * L::kStageElems + L::kTileElems, &wbar[j]);
+  }
   // per-lane element offsets of the fragments (fixed for the whole walk)
   int koff_lo[NG][TW / 4], koff_hi[NG][TW / 4], voff[VD / 16];
 #pragma unroll
@@ -575,10 +579,12 @@ SV_DEV void dattn_item_wide(const AttnDesc& a, int it, unsigned char* sm, int* s
 #pragma unroll
     for (int mt = 0; mt < VD / 16; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
   }
-  if (lane == 0)
+  if (lane == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after generic-proxy use
     for (int j = 0; j < D && j < nst; ++j)
       dattn_fetch<HD>(a, row0, first + kDWarps * j, vp, wb + j * L::kStageElems,
                       wb + j * L::kStageElems + L::kTileElems, &wbar[j]);
+  }
   int koff_lo[NG][TW / 4], koff_hi[NG][TW / 4], voff[VD / 16];
 #pragma unroll
   for (int jg = 0; jg < NG; ++jg)

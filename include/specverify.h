@@ -288,12 +288,10 @@ SPEC_API int spec_accept_rows(const float* p_logits, int64_t p_row_stride,
  * comes from one fixed 4 MiB array compiled into the library (present on
  * every GPU that loads it, until the process exits); calls needing more
  * (about 750 rows at K=5, V=128256) fail with SPEC_E_ARG and a message.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current) and keeps it for the process; make that
- * first call before any stream capture.  A device reset (cudaDeviceReset, or
- * another library resetting the primary context) reloads the module and
- * invalidates the kept address: do not call this entry point after one.
- * All calls share the array: calls that overlap on the GPU race, so order
+ * Every call looks up the array's device address on the current device
+ * (nothing is cached, so a device reset that reloads the module is
+ * harmless); the first call on a device may load the module, so make it
+ * before any stream capture.  All calls share the array: calls that overlap on the GPU race, so order
  * them (one stream, or events).  Asynchronous on `stream`. */
 SPEC_API int spec_accept_rows_noalloc(const float* p_logits, int64_t p_row_stride,
                      const float* q_logits, int64_t q_row_stride,

@@ -16,7 +16,6 @@
 // the GPU (two streams, or two host threads without ordering) race on it.
 #include <cuda_runtime.h>
 
-#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -30,29 +29,17 @@ void set_thread_error(const std::string& msg);  // engine.cu
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the array on the current device, looked up once per
-// device (the host-side name is only a stand-in for the symbol) and kept for
-// the process: a device reset, which reloads the module, invalidates it.
+// Device address of the array on the current device, looked up on every
+// call (cheap; nothing cached, so a device reset that reloads the module
+// leaves no stale address behind).
 cudaError_t scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_accept_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

@@ -643,7 +643,9 @@ def main():
     Lp = args.prompt - 1                       # context length at the profile (prefill of prompt(0))
     fwd_bytes = (st["verify_weight_bytes"] + (Lp + K + 1) * kv_t + (K + 1) * tshape.vocab * 4)
     fwd_achieved = fwd_bytes / (prof["verify_forward_ms"] * 1e6)
-    traffic = persist_traffic_record()
+    # the record was taken on the 8B-shaped bf16 verify launch: other workloads'
+    # launches (other shapes, 4-bit phases) are not covered by it
+    traffic = persist_traffic_record() if args.workload == "8b" else None
     roofline = {"bound": "hbm",
                 "kernel": "persist_forward (target verify pass over the K+1 positions)",
                 "achieved": fwd_achieved, "peak": hbm_peak, "unit": "GB/s",

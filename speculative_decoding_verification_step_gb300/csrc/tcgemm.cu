@@ -570,15 +570,19 @@ cudaError_t launch_tc_gemm(const GemmDesc& g, float* partials, float* inv, int* 
   // -- rounds of units per CTA times the k blocks of a unit, each block a
   // stage of weights and X at ~50 GB/s per SM, plus for split tiles the
   // partials written and read again (~50 GB/s per SM) and the reduction's
-  // launch -- fewest splits on ties, within the partials
-  const double kb_us = (double)(kTcABytes + a.npad * kTcKb * 2) / 50e3;
+  // launch -- fewest splits on ties, within the partials.  The model is
+  // evaluated at a fixed 256-token width, so that the split, and with it the
+  // order in which a tile's k range is summed, depends on n, k and the grid
+  // only, never on the pass's token count.
+  constexpr int kModelTok = 256;
+  const double kb_us = (double)(kTcABytes + kModelTok * kTcKb * 2) / 50e3;
   a.splits = 1;
   double best = -1.0;
   for (int sp = 1; sp <= std::max(1, std::min(8, a.nkb / 2)); ++sp) {
     const long long units = (long long)a.tiles * sp;
     if (units > max_units) break;
     double cost = (double)((units + num_sms - 1) / num_sms) * ((a.nkb + sp - 1) / sp) * kb_us;
-    if (sp > 1) cost += (double)units * kTcM * a.npad * 8.0 / (50e3 * num_sms) + 5.0;
+    if (sp > 1) cost += (double)units * kTcM * kModelTok * 8.0 / (50e3 * num_sms) + 5.0;
     if (best < 0 || cost < best) {
       best = cost;
       a.splits = sp;

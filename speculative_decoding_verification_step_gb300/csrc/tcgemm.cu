@@ -24,15 +24,16 @@
 //                    unit's MMAs then wait for the previous unit's readout,
 //                    but the weights are still read once per pass;
 //   warps 2..5       read a finished accumulator (one TMEM lane quarter each)
-//                    into the unit's fp32 partial [128][npad] while the next
-//                    unit accumulates in the other buffer, then free it;
+//                    while the next unit accumulates in the other buffer --
+//                    into the unit's fp32 partial [128][npad], or through the
+//                    fused epilogue below -- then free it;
 //   warp 6           allocates and frees the tensor-memory columns.
 // The epilogue (store / residual add with the next norm's sums of squares and
 // x * gain / SwiGLU / RoPE + KV append, after scaling by 1/rms of the token:
 // normalised inputs arrive as x * gain in bf16, as in the skinny GEMM) runs
-//  * fused, when the tiles are not split in k (the LM head, the larger
-//    batched GEMMs): warps 2..5 move each finished accumulator, 32 tokens at a
-//    time, through a shared-memory tile into the epilogue;
+//  * fused, when the tiles are not split in k (the LM heads, GEMMs with at
+//    least about a wave of tiles): warps 2..5 move each finished accumulator,
+//    32 tokens at a time, through a shared-memory tile into the epilogue;
 //  * else in a second kernel, one CTA per (tile, 32-token block), that sums
 //    the tile's partials in split order first, so that reductions and
 //    epilogues are spread over the whole GPU.

@@ -11,6 +11,10 @@ workload (2 layers, d=128, vocab 256, fp32; draft = layer 0 + noise).
 * The mixed draft's previous-step rows, worked by hand on table models:
   before the first step they are the target rows at positions L-1-K .. L-1
   (L = the pending token's position), and draft i mixes with row i-1.
+* Plain decoding's draw: greedy by hand (lowest id on ties, the tie flag),
+  and at T > 0 a chi-square test of 6000 draws against softmax(logits / T)
+  that a draw at the wrong temperature fails; the top-2 gap by hand; the
+  step's uniforms on their streams and positions.
 """
 import numpy as np
 import pytest
@@ -108,3 +112,57 @@ def test_mixed_draft_rows_by_hand():
     assert res.drafts == [2, 3]
     # the target's argmax is 3 everywhere: draft 2 is rejected and replaced by 3
     assert res.emitted == [3] and res.n_accepted == 0
+
+
+def test_top2_gap_by_hand():
+    from oracle import accept as acc
+    assert acc.top2_gap([3.0, 1.0, 2.0]) == 1.0
+    assert acc.top2_gap([2.0, 2.0, 0.0]) == 0.0          # a tie at the top
+    assert acc.top2_gap([-1.0, -4.0]) == 3.0
+    assert acc.top2_gap([5.0]) == np.inf                 # one token: no runner-up
+
+
+def test_ar_greedy_draw_and_tie_flag():
+    """Plain decoding at T = 0 is the argmax, lowest id on ties, flagged when
+    the top-2 gap is under the tie window ([101] Floor 4's greedy rule)."""
+    from oracle import accept as acc
+    tok, fl = gen.ar_token_flagged([1.0, 5.0, 5.0, 2.0], 0.0, 0, 0)
+    assert tok == 1 and fl & acc.FLAG_NEAR_TIE
+    tok, fl = gen.ar_token_flagged([1.0, 5.0, 4.9], 0.0, 0, 0, tie_eps=0.2)
+    assert tok == 1 and fl & acc.FLAG_NEAR_TIE
+    tok, fl = gen.ar_token_flagged([1.0, 5.0, 4.9], 0.0, 0, 0, tie_eps=0.05)
+    assert tok == 1 and fl == 0
+
+
+def test_ar_sampled_draw_follows_softmax():
+    """Plain decoding at T > 0 draws from softmax(logits / T): over 6000
+    steps (each its own stream-4 uniform) the token counts pass a chi-square
+    test against the closed-form probabilities, and a draw at the wrong
+    temperature (a planted mistake, checked the same way) fails it."""
+    from scipy.stats import chisquare
+    logits = np.array([0.0, 1.0, -0.5, 2.0, 0.3])
+    temp, n = 0.7, 6000
+    e = np.exp((logits - logits.max()) / temp)
+    probs = e / e.sum()
+    counts = np.bincount([gen.ar_token(logits, temp, 11, s) for s in range(n)], minlength=logits.size)
+    assert chisquare(counts, probs * n).pvalue > 1e-3
+    wrong = np.bincount([gen.ar_token(logits, 1.0, 11, s) for s in range(n)], minlength=logits.size)
+    assert chisquare(wrong, probs * n).pvalue < 1e-6
+
+
+def test_step_uniforms_layout():
+    """The uniforms of one speculative step follow reading 7's layout: the
+    ratio tests r_i and the residual draws on streams 1 and 2 at positions
+    1..K, the bonus draw on stream 3 at position K+1, sequence b in the row
+    word -- so no two of them coincide and the rows are independent."""
+    from oracle import philox
+    k, seed, step = 4, 7, 3
+    r, u_res, u_bonus = gen.step_uniforms(seed, step, k)
+    for i in range(1, k + 1):
+        assert r[i - 1] == philox.uniform(seed, step, i, 1)
+        assert u_res[i - 1] == philox.uniform(seed, step, i, 2)
+    assert u_bonus == philox.uniform(seed, step, k + 1, 3)
+    allu = np.concatenate([r, u_res, [u_bonus]])
+    assert len(set(allu.tolist())) == allu.size and ((allu >= 0) & (allu < 1)).all()
+    r1, _, _ = gen.step_uniforms(seed, step, k, row=1)
+    assert not np.array_equal(r, r1)

@@ -1,6 +1,8 @@
 """Host-side logic of bench.py that needs no GPU: the per-phase fold of the
 persistent kernel's timestamps (spec_phase_times / spec_phase_list layouts,
-include/specverify.h) and the gate on the committed verify-traffic record."""
+include/specverify.h), the gate on the committed verify-traffic record, and
+the reference arm's behaviour on ranks other than 0 and on the 4-bit
+workload (which the oracle arm does not run)."""
 import json
 
 import pytest
@@ -56,3 +58,25 @@ def test_traffic_record_gated_by_source_hash(monkeypatch):
     assert bench.persist_traffic_record()["traffic_ratio"] == rec["traffic_ratio"]
     monkeypatch.setattr(bench, "persist_source_hash", lambda: "0" * 16)
     assert bench.persist_traffic_record() is None
+
+
+def _bench(args, env_extra):
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), *args], env=env,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    # under torchrun only rank 0 times the oracle and prints; the others leave
+    r = _bench(["--impl", "reference", "--gpus", "2"], {"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_4bit_workload_is_unavailable():
+    r = _bench(["--impl", "reference", "--workload", "8b-q4"], {"RANK": "0"})
+    assert r.returncode == 0
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and "unavailable" in line

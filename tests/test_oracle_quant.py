@@ -8,6 +8,8 @@
   groups stay zero.
 * Scales are bf16 values of max |w| / 7.
 * Streamed bytes: codes + scales, ~3.8x fewer than bf16 at group 64.
+* The benchmark's synthetic 4-bit matrices have the bf16 workloads' weight
+  scale (std ~0.02), by closed form and by sample.
 """
 import numpy as np
 import pytest
@@ -63,3 +65,21 @@ def test_bytes():
     n, k = 4096, 4096
     assert quant.bytes_q4(n, k, 64) == n * k // 2 + n * 64 * 2
     assert (n * k * 2) / quant.bytes_q4(n, k, 64) == pytest.approx(3.765, abs=1e-3)
+
+
+def test_synthetic_4bit_recipe_matches_bf16_weights():
+    """The benchmark's synthetic 4-bit matrices (workloads.q4_matrix: uniform
+    codes -8..7, scales 0.75-1.25 x 0.02/4.6 per group) dequantize to weights
+    of standard deviation ~0.02, the bf16 workloads' N(0, 0.02^2): the closed
+    form sqrt(E[c^2] E[s^2]) = sqrt(21.5 x 1.0208) x 0.02/4.6 = 0.0204, and
+    the sample agrees to 2%."""
+    import torch
+    import workloads
+    n, k = 256, 1024
+    g = torch.Generator().manual_seed(3)
+    buf = workloads.q4_matrix(n, k, g, "cpu")
+    packed, scales = workloads.q4_parts(buf, n, k)
+    w = quant.dequantize_q4(packed.numpy(), scales.numpy())
+    closed = np.sqrt(21.5 * (1 + 0.25 / 12)) * 0.02 / 4.6
+    assert abs(closed - 0.0204) < 1e-4
+    assert abs(w.std() / closed - 1) < 0.02
